@@ -1,0 +1,262 @@
+"""fp64 CPU oracle for speculative-sampling verification.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg use this package; the verification library
+never imports, links or calls it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``oracle.c`` (plain scalar loops in double precision);
+this module compiles it with gcc on first use, marshals arrays through ctypes
+and, for large batches, runs disjoint row ranges on Python threads (ctypes
+releases the GIL during the call). ``merge_trees`` (pure Python) restates the
+tree-merging code example of the TAPS page.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+import threading
+from concurrent.futures import ThreadPoolExecutor
+from typing import Dict, Optional
+
+import numpy as np
+
+from .merge import merge_trees  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+# -ffp-contract=off keeps a*b+c as two roundings on every host (gcc fuses
+# them by default on aarch64), so x86 and Arm builds agree bit for bit.
+CFLAGS = ["-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+F64, F32, BF16 = 0, 1, 2
+ST_TOKEN, ST_TARGET, ST_DRAFT, ST_TREE, ST_MASK = 1, 2, 4, 8, 16
+FL_ACCEPT, FL_SAMPLE, FL_ROUTE = 1, 2, 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(src: str = _SRC, out: str = _LIB, force: bool = False) -> str:
+    """Compile ``oracle.c`` into a shared library (atomic replace)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(out))
+    os.close(fd)
+    try:
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+        os.replace(tmp, out)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return out
+
+
+def load(path: Optional[str] = None):
+    """Load (building if needed) the oracle library; ``path`` loads another
+    build of the same source (used by the mutation tests)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def _declare(lib):
+    P = ctypes.c_void_p
+    i = ctypes.c_int
+    d = ctypes.c_double
+    lib.orc_verify_chain.argtypes = [P, P, i, P, P, P, d, i, i, i, i, i, P, P, P, P, P, P, P, P]
+    lib.orc_verify_chain.restype = None
+    lib.orc_verify_chain_greedy.argtypes = [P, i, P, i, i, i, i, i, P, P, P, P]
+    lib.orc_verify_chain_greedy.restype = None
+    lib.orc_verify_tree_greedy.argtypes = [P, i, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P]
+    lib.orc_verify_tree_greedy.restype = None
+    lib.orc_tree_bruteforce_depth.argtypes = [P, P, P, i]
+    lib.orc_tree_bruteforce_depth.restype = ctypes.c_int
+    lib.orc_tree_confidence.argtypes = [P, i, i, i, P, P, P]
+    lib.orc_tree_confidence.restype = None
+    return lib
+
+
+# ------------------------------------------------------------ marshalling --
+
+def _logits(a):
+    """numpy view + element-type code of a logit tensor (torch or numpy)."""
+    try:
+        import torch
+
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype == torch.bfloat16:
+                return a.view(torch.int16).numpy().view(np.uint16), BF16
+            if a.dtype == torch.float32:
+                return a.numpy(), F32
+            if a.dtype == torch.float64:
+                return a.numpy(), F64
+            raise TypeError(f"unsupported logit dtype {a.dtype}")
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float64:
+        return a, F64
+    if a.dtype == np.float32:
+        return a, F32
+    if a.dtype == np.uint16:
+        return a, BF16
+    raise TypeError(f"unsupported logit dtype {a.dtype}")
+
+
+def _np(a, dtype):
+    try:
+        import torch
+
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu()
+            if a.dtype == torch.bfloat16:
+                a = a.float()
+            a = a.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _ranges(B: int, threads: int):
+    threads = max(1, min(threads, B))
+    step = (B + threads - 1) // threads
+    return [(b, min(B, b + step)) for b in range(0, B, step)]
+
+
+def _run(fn, B: int, threads: int):
+    rs = _ranges(B, threads)
+    if len(rs) == 1:
+        fn(*rs[0])
+        return
+    with ThreadPoolExecutor(len(rs)) as ex:
+        list(ex.map(lambda r: fn(*r), rs))
+
+
+# ------------------------------------------------------------- functions --
+
+def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None) -> Dict[str, np.ndarray]:
+    """Speculative-sampling chain verification (T > 0) in fp64.
+
+    Returns accept_len [B], out_tokens [B, K+1], lse_p [B, K+1], lse_q [B, K],
+    px / qx [B, K] (target / draft probability of each draft token), status [B]
+    and flags [B] (FL_ACCEPT / FL_SAMPLE: a uniform within 1e-6 of a decision
+    boundary)."""
+    if not T > 0:
+        raise ValueError("verify_chain needs T > 0; use verify_chain_greedy for T == 0")
+    lib = lib or load()
+    lp, dt = _logits(Lp)
+    lq, dtq = _logits(Lq)
+    if dtq != dt:
+        raise TypeError("target and draft logits must share a dtype")
+    B, K1, V = lp.shape
+    K = K1 - 1
+    xs = _np(x, np.int32).reshape(B, K)
+    uas = _np(ua, np.float64).reshape(B, K)
+    urs = _np(ur, np.float64).reshape(B)
+    out = dict(
+        accept_len=np.empty(B, np.int32),
+        out_tokens=np.empty((B, K + 1), np.int32),
+        lse_p=np.empty((B, K + 1), np.float64),
+        lse_q=np.empty((B, K), np.float64),
+        px=np.empty((B, K), np.float64),
+        qx=np.empty((B, K), np.float64),
+        status=np.empty(B, np.int32),
+        flags=np.empty(B, np.int32),
+    )
+
+    def part(b0, b1):
+        lib.orc_verify_chain(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), B, K, V,
+                             b0, b1, _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["lse_p"]),
+                             _ptr(out["lse_q"]), _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["status"]),
+                             _ptr(out["flags"]))
+
+    _run(part, B, threads)
+    return out
+
+
+def verify_chain_greedy(Lp, x, threads: int = 1, lib=None) -> Dict[str, np.ndarray]:
+    """Greedy (temperature 0) chain verification. Returns accept_len [B],
+    out_tokens [B, K+1], argmax [B, K+1], status [B]."""
+    lib = lib or load()
+    lp, dt = _logits(Lp)
+    B, K1, V = lp.shape
+    K = K1 - 1
+    xs = _np(x, np.int32).reshape(B, K)
+    out = dict(
+        accept_len=np.empty(B, np.int32),
+        out_tokens=np.empty((B, K + 1), np.int32),
+        argmax=np.empty((B, K + 1), np.int32),
+        status=np.empty(B, np.int32),
+    )
+
+    def part(b0, b1):
+        lib.orc_verify_chain_greedy(_ptr(lp), dt, _ptr(xs), B, K, V, b0, b1, _ptr(out["accept_len"]),
+                                    _ptr(out["out_tokens"]), _ptr(out["argmax"]), _ptr(out["status"]))
+
+    _run(part, B, threads)
+    return out
+
+
+def verify_tree_greedy(Lt, tok, R, n1: int, mask=None, threads: int = 1, lib=None) -> Dict[str, np.ndarray]:
+    """Merged-tree greedy verification. Returns accept_len, best_row,
+    path [B, D], out_tokens [B, D], subtree, argmax [B, N], status."""
+    lib = lib or load()
+    lt, dt = _logits(Lt)
+    B, N, V = lt.shape
+    toks = _np(tok, np.int32).reshape(B, N)
+    Rs = _np(R, np.int32)
+    Rn, D = Rs.shape[1], Rs.shape[2]
+    ms = None if mask is None else _np(mask, np.uint8).reshape(B, N, N)
+    out = dict(
+        accept_len=np.empty(B, np.int32),
+        best_row=np.empty(B, np.int32),
+        path=np.empty((B, D), np.int32),
+        out_tokens=np.empty((B, D), np.int32),
+        subtree=np.empty(B, np.int32),
+        argmax=np.empty((B, N), np.int32),
+        status=np.empty(B, np.int32),
+    )
+
+    def part(b0, b1):
+        lib.orc_verify_tree_greedy(_ptr(lt), dt, _ptr(toks), _ptr(Rs), None if ms is None else _ptr(ms), B, N,
+                                   Rn, D, V, int(n1), b0, b1, _ptr(out["accept_len"]), _ptr(out["best_row"]),
+                                   _ptr(out["path"]), _ptr(out["out_tokens"]), _ptr(out["subtree"]),
+                                   _ptr(out["argmax"]), _ptr(out["status"]))
+
+    _run(part, B, threads)
+    return out
+
+
+def tree_bruteforce_depth(mask, tok, amax, lib=None) -> int:
+    """Longest accepted depth of one merged tree found from the ancestor mask
+    alone (no retrieve rows)."""
+    lib = lib or load()
+    m = _np(mask, np.uint8)
+    N = m.shape[0]
+    t = _np(tok, np.int32).reshape(N)
+    a = _np(amax, np.int32).reshape(N)
+    return int(lib.orc_tree_bruteforce_depth(_ptr(m), _ptr(t), _ptr(a), N))
+
+
+def tree_confidence(conf, n1: int, lib=None) -> Dict[str, np.ndarray]:
+    """Confidence routing: per-tree mean node confidence and the chosen tree
+    (1 or 2). Returns scores [B, 2] (fp64), choice [B], flags [B]."""
+    lib = lib or load()
+    c = _np(conf, np.float32)
+    B, N = c.shape
+    out = dict(scores=np.empty((B, 2), np.float64), choice=np.empty(B, np.int32), flags=np.empty(B, np.int32))
+    lib.orc_tree_confidence(_ptr(c), B, N, int(n1), _ptr(out["scores"]), _ptr(out["choice"]), _ptr(out["flags"]))
+    return out

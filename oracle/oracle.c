@@ -1,0 +1,385 @@
+/*
+ * oracle.c -- fp64 CPU oracle for speculative-sampling verification.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the package smoke check and the
+ * benchmark's CPU-baseline leg load this library; the verification library
+ * never does, and this file shares no code, header or constant table with it.
+ *
+ * Everything is a plain scalar loop in double precision, written in the order
+ * the method is stated:
+ *   - speculative sampling (Leviathan et al., ICML 2023, as summarised on the
+ *     ariser.io page, section "keeping the same distribution"; lotook.com,
+ *     "how does speculative decoding work step by step"): accept draft token x
+ *     with probability min(1, p(x)/q(x)); at the first rejection m draw from
+ *     max(0, p - q) renormalised; when all K are accepted draw the bonus token
+ *     from the target's position K+1;
+ *   - greedy verification (temperature 0): accept while the draft token is
+ *     the target's top choice (lotook.com, same section; SubSpec review,
+ *     Method 2, the "I left my keys" example);
+ *   - merged-tree verification (TAPS page, methodology: the target scores all
+ *     nodes of the merged tree in one pass and the longest accepted path is
+ *     kept) and confidence routing (TAPS page, methodology: arithmetic mean of
+ *     the nodes' predicted probabilities per drafter tree, higher wins).
+ *
+ * Readings where the pages are silent (each is listed with its reason in the
+ * design notes): a draft token is accepted iff u < p(x)/q(x) with u in [0,1);
+ * one accept uniform per draft position and one resample uniform per row; a
+ * discrete draw is the inverse CDF over ascending token id with a strict ">";
+ * a residual of total mass zero falls back to p at that position; greedy ties
+ * go to the lowest token id; among equally long tree paths the lowest
+ * retrieve row wins.
+ *
+ * Element types of logit buffers: 0 = fp64, 1 = fp32, 2 = bf16 bit patterns
+ * (uint16). Each element is widened exactly to double.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORC_F64 0
+#define ORC_F32 1
+#define ORC_BF16 2
+
+/* row_status bits (the library's header documents the same meanings) */
+#define ST_TOKEN 1      /* a draft / node token outside [0, V) */
+#define ST_TARGET 2     /* a target row with a NaN or no finite maximum */
+#define ST_DRAFT 4      /* a draft row with a NaN or no finite maximum */
+#define ST_TREE 8       /* a malformed retrieve row */
+#define ST_MASK 16      /* a retrieve row that contradicts the ancestor mask */
+
+/* near-tie flags (oracle only): the GPU may legitimately differ here */
+#define FL_ACCEPT 1
+#define FL_SAMPLE 2
+#define FL_ROUTE 4
+#define NEAR 1e-6
+
+static double elem(const void* base, int dt, size_t i) {
+  if (dt == ORC_F64) return ((const double*)base)[i];
+  if (dt == ORC_F32) return (double)((const float*)base)[i];
+  uint32_t bits = (uint32_t)((const uint16_t*)base)[i] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* softmax(l / T) over one row: M = max_v l_v / T and Z = sum_v exp(l_v / T - M).
+ * Returns 1 when the row holds a NaN or has no finite maximum. */
+static int softmax_stats(const void* L, int dt, size_t off, int V, double T, double* M, double* Z) {
+  double m = -INFINITY;
+  int nan = 0;
+  for (int v = 0; v < V; ++v) {
+    double s = elem(L, dt, off + (size_t)v) / T;
+    if (isnan(s)) nan = 1;
+    else if (s > m) m = s;
+  }
+  if (nan || !isfinite(m)) {
+    *M = m;
+    *Z = NAN;
+    return 1;
+  }
+  double z = 0.0;
+  for (int v = 0; v < V; ++v) z += exp(elem(L, dt, off + (size_t)v) / T - m);
+  *M = m;
+  *Z = z;
+  return 0;
+}
+
+static double prob(const void* L, int dt, size_t off, int v, double T, double M, double Z) {
+  return exp(elem(L, dt, off + (size_t)v) / T - M) / Z;
+}
+
+/* Index of the largest entry, lowest index on ties; -1 when no entry is above
+ * -inf. *nan is set when the row holds a NaN (a NaN never wins). */
+static int row_argmax(const void* L, int dt, size_t off, int V, int* nan) {
+  int best = -1;
+  double bv = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double s = elem(L, dt, off + (size_t)v);
+    if (isnan(s)) *nan = 1;
+    else if (s > bv) {
+      bv = s;
+      best = v;
+    }
+  }
+  return best;
+}
+
+/* Speculative-sampling chain verification, T > 0, rows b in [b0, b1).
+ * Lp: target logits [B][K+1][V]; Lq: draft logits [B][K][V]; x: [B][K];
+ * ua: [B][K] accept uniforms; ur: [B] resample uniforms.
+ * Out: accept_len [B] (= m), out_tok [B][K+1] (x_0..x_{m-1}, then the drawn
+ * token, then -1), lse_p [B][K+1], lse_q [B][K], px / qx [B][K] (p_k(x_k),
+ * q_k(x_k)), status [B], flags [B] (near ties). */
+void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                      const double* ur, double T, int B, int K, int V, int b0, int b1,
+                      int32_t* accept_len, int32_t* out_tok, double* lse_p, double* lse_q, double* px,
+                      double* qx, int32_t* status, int32_t* flags) {
+  (void)B;
+  double Mp[K + 1], Zp[K + 1], Mq[K + 1], Zq[K + 1];
+  for (int b = b0; b < b1; ++b) {
+    int st = 0, fl = 0;
+    for (int k = 0; k <= K; ++k) {
+      size_t off = ((size_t)b * (K + 1) + k) * (size_t)V;
+      if (softmax_stats(Lp, dt, off, V, T, &Mp[k], &Zp[k])) st |= ST_TARGET;
+      lse_p[(size_t)b * (K + 1) + k] = Mp[k] + log(Zp[k]);
+    }
+    for (int k = 0; k < K; ++k) {
+      size_t off = ((size_t)b * K + k) * (size_t)V;
+      if (softmax_stats(Lq, dt, off, V, T, &Mq[k], &Zq[k])) st |= ST_DRAFT;
+      lse_q[(size_t)b * K + k] = Mq[k] + log(Zq[k]);
+      int xk = x[(size_t)b * K + k];
+      if (xk < 0 || xk >= V) st |= ST_TOKEN;
+    }
+    int32_t* out = out_tok + (size_t)b * (K + 1);
+    for (int j = 0; j <= K; ++j) out[j] = -1;
+    for (int k = 0; k < K; ++k) {
+      px[(size_t)b * K + k] = NAN;
+      qx[(size_t)b * K + k] = NAN;
+    }
+    status[b] = st;
+    if (st) {
+      accept_len[b] = -1;
+      flags[b] = 0;
+      continue;
+    }
+    for (int k = 0; k < K; ++k) {
+      int xk = x[(size_t)b * K + k];
+      px[(size_t)b * K + k] = prob(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, xk, T, Mp[k], Zp[k]);
+      qx[(size_t)b * K + k] = prob(Lq, dt, ((size_t)b * K + k) * (size_t)V, xk, T, Mq[k], Zq[k]);
+    }
+    /* left-to-right acceptance test; m = first rejection, K if none */
+    int m = K;
+    for (int k = 0; k < K; ++k) {
+      double p = px[(size_t)b * K + k], q = qx[(size_t)b * K + k];
+      double r = q > 0.0 ? p / q : INFINITY;
+      double u = ua[(size_t)b * K + k];
+      if (r < 1.0 && fabs(u - r) < NEAR) fl |= FL_ACCEPT;
+      if (!(u < r)) {
+        m = k;
+        break;
+      }
+    }
+    accept_len[b] = m;
+    for (int k = 0; k < m; ++k) out[k] = x[(size_t)b * K + k];
+
+    /* residual max(0, p_m - q_m) at a rejection, p_K for the bonus */
+    size_t offp = ((size_t)b * (K + 1) + m) * (size_t)V;
+    size_t offq = ((size_t)b * K + m) * (size_t)V;
+    int residual = m < K;
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) {
+      double w = prob(Lp, dt, offp, v, T, Mp[m], Zp[m]);
+      if (residual) w = fmax(0.0, w - prob(Lq, dt, offq, v, T, Mq[m], Zq[m]));
+      S += w;
+    }
+    if (residual && !(S > 0.0)) {
+      residual = 0; /* p_m == q_m numerically: draw from p_m */
+      S = 0.0;
+      for (int v = 0; v < V; ++v) S += prob(Lp, dt, offp, v, T, Mp[m], Zp[m]);
+    }
+    /* inverse CDF: smallest i with C_i > u * S */
+    double t = ur[b] * S, C = 0.0, Cprev = 0.0;
+    int tok = -1, last_pos = -1;
+    for (int v = 0; v < V; ++v) {
+      double w = prob(Lp, dt, offp, v, T, Mp[m], Zp[m]);
+      if (residual) w = fmax(0.0, w - prob(Lq, dt, offq, v, T, Mq[m], Zq[m]));
+      if (w > 0.0) last_pos = v;
+      Cprev = C;
+      C += w;
+      if (C > t) {
+        tok = v;
+        break;
+      }
+    }
+    if (tok < 0) {
+      tok = last_pos; /* rounding left no crossing */
+      fl |= FL_SAMPLE;
+    } else if (fabs(ur[b] - Cprev / S) < NEAR || fabs(ur[b] - C / S) < NEAR) {
+      fl |= FL_SAMPLE;
+    }
+    out[m] = tok;
+    flags[b] = fl;
+  }
+}
+
+/* Greedy chain verification (temperature 0), rows b in [b0, b1).
+ * a_k = argmax of target row k (k = 0..K); m = first k with x_k != a_k (K if
+ * none); emitted tokens x_0..x_{m-1}, a_m. amax [B][K+1] receives a_k. */
+void orc_verify_chain_greedy(const void* Lp, int dt, const int32_t* x, int B, int K, int V, int b0,
+                             int b1, int32_t* accept_len, int32_t* out_tok, int32_t* amax,
+                             int32_t* status) {
+  (void)B;
+  for (int b = b0; b < b1; ++b) {
+    int st = 0;
+    int32_t* a = amax + (size_t)b * (K + 1);
+    for (int k = 0; k <= K; ++k) {
+      int nan = 0;
+      a[k] = row_argmax(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, &nan);
+      if (nan || a[k] < 0) st |= ST_TARGET;
+    }
+    for (int k = 0; k < K; ++k) {
+      int xk = x[(size_t)b * K + k];
+      if (xk < 0 || xk >= V) st |= ST_TOKEN;
+    }
+    int32_t* out = out_tok + (size_t)b * (K + 1);
+    for (int j = 0; j <= K; ++j) out[j] = -1;
+    status[b] = st;
+    if (st) {
+      accept_len[b] = -1;
+      continue;
+    }
+    int m = K;
+    for (int k = 0; k < K; ++k) {
+      if (x[(size_t)b * K + k] != a[k]) {
+        m = k;
+        break;
+      }
+    }
+    accept_len[b] = m;
+    for (int k = 0; k < m; ++k) out[k] = x[(size_t)b * K + k];
+    out[m] = a[m];
+  }
+}
+
+/* Merged-tree greedy verification, rows b in [b0, b1).
+ * Lt: node logits [B][N][V]; tok: node tokens [B][N] (node 0 = shared root);
+ * R: retrieve rows [B][Rn][D], each a root-to-leaf path starting with node 0
+ * and padded with -1 (an all -1 row is padding); mask: [B][N][N] ancestor
+ * mask or NULL. For row r, L_r is the largest j such that every node on the
+ * path at depth t <= j carries the target's top token at the node before it.
+ * The best row is the lowest r with the largest L_r; the emitted tokens are
+ * the path's tokens at depths 1..L followed by the top token at depth L.
+ * subtree: 0 when only the root is accepted, 1 when the path runs through
+ * tree 1 (nodes 1..n1), 2 through tree 2. */
+void orc_verify_tree_greedy(const void* Lt, int dt, const int32_t* tok, const int32_t* R,
+                            const uint8_t* mask, int B, int N, int Rn, int D, int V, int n1, int b0,
+                            int b1, int32_t* accept_len, int32_t* best_row, int32_t* path,
+                            int32_t* out_tok, int32_t* subtree, int32_t* amax, int32_t* status) {
+  (void)B;
+  for (int b = b0; b < b1; ++b) {
+    int st = 0;
+    int32_t* a = amax + (size_t)b * N;
+    const int32_t* tk = tok + (size_t)b * N;
+    const int32_t* Rb = R + (size_t)b * Rn * D;
+    for (int i = 0; i < N; ++i) {
+      int nan = 0;
+      a[i] = row_argmax(Lt, dt, ((size_t)b * N + i) * (size_t)V, V, &nan);
+      if (nan || a[i] < 0) st |= ST_TARGET;
+    }
+    for (int i = 1; i < N; ++i)
+      if (tk[i] < 0 || tk[i] >= V) st |= ST_TOKEN;
+    int any_row = 0;
+    for (int r = 0; r < Rn; ++r) {
+      const int32_t* row = Rb + (size_t)r * D;
+      if (row[0] == -1) {
+        for (int t = 1; t < D; ++t)
+          if (row[t] != -1) st |= ST_TREE;
+        continue;
+      }
+      any_row = 1;
+      if (row[0] != 0) st |= ST_TREE;
+      int ended = 0;
+      for (int t = 1; t < D; ++t) {
+        int nd = row[t];
+        if (nd == -1) {
+          ended = 1;
+          continue;
+        }
+        if (ended || nd <= 0 || nd >= N) {
+          st |= ST_TREE;
+          continue;
+        }
+        if (mask && !mask[((size_t)b * N + nd) * N + row[t - 1]]) st |= ST_MASK;
+      }
+    }
+    if (!any_row) st |= ST_TREE;
+    int32_t* pth = path + (size_t)b * D;
+    int32_t* out = out_tok + (size_t)b * D;
+    for (int t = 0; t < D; ++t) {
+      pth[t] = -1;
+      out[t] = -1;
+    }
+    status[b] = st;
+    if (st) {
+      accept_len[b] = -1;
+      best_row[b] = -1;
+      subtree[b] = -1;
+      continue;
+    }
+    int bestL = -1, bestr = -1;
+    for (int r = 0; r < Rn; ++r) {
+      const int32_t* row = Rb + (size_t)r * D;
+      if (row[0] == -1) continue;
+      int L = 0;
+      for (int t = 1; t < D; ++t) {
+        int nd = row[t];
+        if (nd == -1 || tk[nd] != a[row[t - 1]]) break;
+        L = t;
+      }
+      if (L > bestL) {
+        bestL = L;
+        bestr = r;
+      }
+    }
+    const int32_t* row = Rb + (size_t)bestr * D;
+    accept_len[b] = bestL;
+    best_row[b] = bestr;
+    for (int t = 0; t <= bestL; ++t) pth[t] = row[t];
+    for (int t = 1; t <= bestL; ++t) out[t - 1] = tk[row[t]];
+    out[bestL] = a[row[bestL]];
+    subtree[b] = bestL == 0 ? 0 : (row[1] <= n1 ? 1 : 2);
+  }
+}
+
+/* Brute-force accepted depth of one merged tree, from the ancestor mask alone
+ * (no retrieve rows): depth(i) = #ancestors(i) excluding i; parent(i) = the
+ * ancestor j != i of largest depth; node i is accepted iff its parent is and
+ * tok[i] == a[parent(i)]; the root is accepted. Returns the largest accepted
+ * depth. mask: [N][N]; tok, a: [N]. */
+int orc_tree_bruteforce_depth(const uint8_t* mask, const int32_t* tok, const int32_t* a, int N) {
+  int depth[N], parent[N], acc[N];
+  for (int i = 0; i < N; ++i) {
+    int c = 0;
+    for (int j = 0; j < N; ++j) c += mask[(size_t)i * N + j] ? 1 : 0;
+    depth[i] = c - 1;
+  }
+  for (int i = 0; i < N; ++i) {
+    parent[i] = -1;
+    for (int j = 0; j < N; ++j)
+      if (j != i && mask[(size_t)i * N + j] && (parent[i] < 0 || depth[j] > depth[parent[i]]))
+        parent[i] = j;
+  }
+  int maxd = 0;
+  for (int i = 0; i < N; ++i)
+    if (depth[i] > maxd) maxd = depth[i];
+  for (int i = 0; i < N; ++i) acc[i] = (i == 0);
+  int best = 0;
+  for (int d = 1; d <= maxd; ++d)
+    for (int i = 0; i < N; ++i)
+      if (depth[i] == d && parent[i] >= 0 && acc[parent[i]] && tok[i] == a[parent[i]]) {
+        acc[i] = 1;
+        if (d > best) best = d;
+      }
+  return best;
+}
+
+/* Confidence routing: score of each drafter tree = arithmetic mean of its
+ * non-root node confidences (tree 1: nodes 1..n1, tree 2: n1+1..N-1; an
+ * empty tree scores -inf); choice = 2 if score_2 > score_1 else 1.
+ * conf: [B][N] fp32; scores: [B][2]. */
+void orc_tree_confidence(const float* conf, int B, int N, int n1, double* scores, int32_t* choice,
+                         int32_t* flags) {
+  for (int b = 0; b < B; ++b) {
+    const float* c = conf + (size_t)b * N;
+    double s1 = 0.0, s2 = 0.0;
+    for (int i = 1; i <= n1; ++i) s1 += (double)c[i];
+    for (int i = n1 + 1; i < N; ++i) s2 += (double)c[i];
+    int n2 = N - 1 - n1;
+    s1 = n1 > 0 ? s1 / n1 : -INFINITY;
+    s2 = n2 > 0 ? s2 / n2 : -INFINITY;
+    scores[2 * b] = s1;
+    scores[2 * b + 1] = s2;
+    choice[b] = s2 > s1 ? 2 : 1;
+    flags[b] = (isfinite(s1) && isfinite(s2) && fabs(s1 - s2) < NEAR) ? FL_ROUTE : 0;
+  }
+}

@@ -1,0 +1,425 @@
+"""Pins that tie the fp64 oracle to what the pages and the mathematics fix.
+
+Each ``pin_*`` function raises AssertionError when the oracle library ``lib``
+disagrees with a fixed fact; the test modules call them with the oracle as
+built, and the mutation test calls them with deliberately broken builds to
+show that plausible mistakes are caught.
+
+The law integrator treats the oracle's chain verification as a black box:
+for fixed logits and draft tokens the output is a piecewise-constant function
+of the uniforms, so its exact law is found by locating the breakpoints by
+bisection (to the last double) and weighting each cell by its length.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import itertools
+import json
+import math
+import os
+from collections import defaultdict
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class ChainCall:
+    """Direct single-row call of ``orc_verify_chain`` with fp64 inputs."""
+
+    def __init__(self, lib, Lp, Lq, x, T):
+        self.lib = lib
+        self.Lp = np.ascontiguousarray(Lp, np.float64)[None]
+        self.K = self.Lp.shape[1] - 1
+        self.V = self.Lp.shape[2]
+        self.Lq = np.ascontiguousarray(Lq, np.float64).reshape(1, self.K, self.V)
+        self.x = np.ascontiguousarray(x, np.int32).reshape(1, self.K)
+        self.T = float(T)
+        self.ua = np.zeros((1, self.K), np.float64)
+        self.ur = np.zeros(1, np.float64)
+        K, V = self.K, self.V
+        self.acc = np.zeros(1, np.int32)
+        self.out = np.zeros((1, K + 1), np.int32)
+        self.lp = np.zeros((1, K + 1))
+        self.lq = np.zeros((1, max(K, 1)))
+        self.px = np.zeros((1, max(K, 1)))
+        self.qx = np.zeros((1, max(K, 1)))
+        self.st = np.zeros(1, np.int32)
+        self.fl = np.zeros(1, np.int32)
+
+    def __call__(self, ua, ur):
+        self.ua[0, :] = ua
+        self.ur[0] = ur
+        self.lib.orc_verify_chain(_p(self.Lp), _p(self.Lq), oracle.F64, _p(self.x), _p(self.ua), _p(self.ur),
+                                  self.T, 1, self.K, self.V, 0, 1, _p(self.acc), _p(self.out), _p(self.lp),
+                                  _p(self.lq), _p(self.px), _p(self.qx), _p(self.st), _p(self.fl))
+        assert self.st[0] == 0, "unexpected row status"
+        m = int(self.acc[0])
+        return m, tuple(int(t) for t in self.out[0, : m + 1])
+
+
+ONE_MINUS = math.nextafter(1.0, 0.0)
+
+
+def _edge(pred):
+    """For a predicate true on [0, e) and false on [e, 1): return e (to the
+    last double); asserts the shape on the probed points."""
+    if not pred(0.0):
+        return 0.0
+    if pred(ONE_MINUS):
+        return 1.0
+    lo, hi = 0.0, ONE_MINUS
+    while True:
+        mid = 0.5 * (lo + hi)
+        if mid <= lo or mid >= hi:
+            return hi
+        if pred(mid):
+            lo = mid
+        else:
+            hi = mid
+
+
+def _cells(f):
+    """Cells of a nondecreasing step function f on [0, 1): list of (value,
+    length)."""
+    out = []
+    a = 0.0
+    while True:
+        va = f(a)
+        e = _edge_from(f, a, va)
+        out.append((va, e - a))
+        if e >= 1.0:
+            return out
+        assert f(e) > va, "inverse-CDF draw is not monotone in u"
+        a = e
+
+
+def _edge_from(f, a, va):
+    """Smallest double e in (a, 1) with f(e) != va, given f(a) == va and f
+    constant on [a, e); 1.0 when f stays at va."""
+    if f(ONE_MINUS) == va:
+        return 1.0
+    lo, hi = a, ONE_MINUS
+    while True:
+        mid = 0.5 * (lo + hi)
+        if mid <= lo or mid >= hi:
+            return hi
+        if f(mid) == va:
+            lo = mid
+        else:
+            hi = mid
+
+
+def chain_law(call: ChainCall):
+    """Exact law over emitted token tuples of one chain verification call."""
+    K = call.K
+    law = defaultdict(float)
+
+    def sample_stage(m, ua, vol):
+        # uniforms after the first rejection must not matter: probe both ends
+        late = list(ua[: m + 1]) + [ONE_MINUS] * (K - m - 1)
+        a = 0.0
+        for tok, length in _cells(lambda u: call(ua, u)[1][m]):
+            mid = a + 0.5 * length
+            a += length
+            if length <= 0:
+                continue
+            mm, emitted = call(ua, mid)
+            assert mm == m and emitted[m] == tok, "accept length changed with the resample uniform"
+            assert call(late, mid) == (mm, emitted), "output depends on uniforms after the first rejection"
+            law[emitted] += vol * length
+
+    def rec(k, ua, vol):
+        if k == K:
+            sample_stage(K, ua, vol)
+            return
+
+        def acc(u):
+            v = list(ua)
+            v[k] = u
+            return call(v, 0.5)[0] > k
+
+        th = _edge(acc)
+        if th > 0.0:
+            v = list(ua)
+            v[k] = 0.5 * th
+            rec(k + 1, v, vol * th)
+        if th < 1.0:
+            v = list(ua)
+            v[k] = 0.5 * (th + 1.0)
+            sample_stage(k, v, vol * (1.0 - th))
+
+    rec(0, [0.0] * K, 1.0)
+    return law
+
+
+def softmax(l, T):
+    s = np.asarray(l, np.float64) / T
+    e = np.exp(s - s.max())
+    return e / e.sum()
+
+
+def random_world(V, K, seed, scale=1.5, zero_some=False):
+    """Target and draft next-token logits for every prefix of length <= K."""
+    rng = np.random.default_rng(seed)
+    lp, lq = {}, {}
+    for n in range(K + 1):
+        for pre in itertools.product(range(V), repeat=n):
+            lp[pre] = rng.normal(0.0, scale, V)
+            lq[pre] = rng.normal(0.0, scale, V)
+            if zero_some and rng.random() < 0.3:
+                lq[pre][rng.integers(V)] = -np.inf  # a token the drafter never proposes
+    return lp, lq
+
+
+# ------------------------------------------------------------------ pins --
+
+def pin_ab_example(lib):
+    """Worked example (ariser.io page, section on keeping the same
+    distribution): P = (0.6, 0.4), Q = (0.8, 0.2)."""
+    g = golden("ab_example.json")
+    P, Q = g["target"], g["draft"]
+    lp = np.log(np.array([P, P]))
+    lq = np.log(np.array([Q]))
+    acc_rate = {}
+    joint = defaultdict(float)
+    for x in (0, 1):
+        call = ChainCall(lib, lp, lq, [x], 1.0)
+        th = _edge(lambda u: call([u], 0.5)[0] > 0)
+        acc_rate[x] = th
+        law = chain_law(call)
+        for seq, pr in law.items():
+            joint[seq] += Q[x] * pr
+        if x == 0:
+            rej = {seq: pr for seq, pr in law.items() if len(seq) == 1}
+            assert abs(sum(rej.values()) - (1 - g["accept_prob"]["A"])) < 1e-15
+            assert rej.get((1,), 0.0) > 0 and rej.get((0,), 0.0) == 0.0, "residual must put all mass on B"
+    assert abs(acc_rate[0] - g["accept_prob"]["A"]) < 1e-15, acc_rate
+    assert acc_rate[1] == 1.0, acc_rate
+    # joint masses of the first emitted token
+    first = defaultdict(float)
+    for seq, pr in joint.items():
+        first[seq[0]] += pr
+    mass = g["joint_mass"]
+    a_acc = sum(pr for seq, pr in joint.items() if len(seq) == 2 and seq[0] == 0)
+    b_acc = sum(pr for seq, pr in joint.items() if len(seq) == 2 and seq[0] == 1)
+    rej_b = sum(pr for seq, pr in joint.items() if len(seq) == 1)
+    assert abs(a_acc - mass["A_accepted"]) < 1e-15
+    assert abs(b_acc - mass["B_accepted"]) < 1e-15
+    assert abs(rej_b - mass["A_rejected_then_B"]) < 1e-15
+    assert abs(first[0] - g["final"]["A"]) < 1e-15 and abs(first[1] - g["final"]["B"]) < 1e-15, dict(first)
+    # uniform-grid acceptance of A: exactly 3/4 of the grid midpoints
+    call = ChainCall(lib, lp, lq, [0], 1.0)
+    n = 10_000
+    hits = sum(call([(i + 0.5) / n], 0.5)[0] == 1 for i in range(n))
+    assert hits == 7500, hits
+
+
+def pin_lossless(lib, V, K, T, seed, zero_some=False):
+    """Exhaustive check of losslessness (lotook.com: the rejection and
+    residual rules make each step emit exactly the target's distribution):
+    the law of draft-then-verify, with every emitted prefix continued by the
+    target alone, equals the target's own law over V^(K+1) sequences."""
+    lp, lq = random_world(V, K, seed, zero_some=zero_some)
+    P = {pre: softmax(l, T) for pre, l in lp.items()}
+    Q = {pre: softmax(l, T) for pre, l in lq.items()}
+    got = defaultdict(float)
+    for x in itertools.product(range(V), repeat=K):
+        wx = 1.0
+        for k in range(K):
+            wx *= Q[x[:k]][x[k]]
+        if wx == 0.0:
+            continue
+        Lp = np.stack([lp[x[:k]] for k in range(K + 1)])
+        Lq = np.stack([lq[x[:k]] for k in range(K)])
+        law = chain_law(ChainCall(lib, Lp, Lq, x, T))
+        for emitted, pr in law.items():
+            n = len(emitted)
+            for cont in itertools.product(range(V), repeat=K + 1 - n):
+                y = emitted + cont
+                w = wx * pr
+                for j in range(n, K + 1):
+                    w *= P[y[:j]][y[j]]
+                got[y] += w
+    err = 0.0
+    for y in itertools.product(range(V), repeat=K + 1):
+        want = 1.0
+        for j in range(K + 1):
+            want *= P[y[:j]][y[j]]
+        err = max(err, abs(got.get(y, 0.0) - want))
+    assert abs(sum(got.values()) - 1.0) < 1e-12
+    assert err < 1e-12, f"emitted law differs from the target law by {err}"
+
+
+def pin_greedy_world(lib, V=4, K=3, seed=0, ties=False):
+    """Temperature 0: the emitted tokens are the target's own greedy chain
+    (lotook.com FAQ: only the target's top prediction is accepted)."""
+    rng = np.random.default_rng(seed)
+    lp = {}
+    for n in range(K + 1):
+        for pre in itertools.product(range(V), repeat=n):
+            lp[pre] = rng.integers(0, 3, V).astype(np.float64) if ties else rng.normal(0, 1, V)
+    for x in itertools.product(range(V), repeat=K):
+        Lp = np.stack([lp[x[:k]] for k in range(K + 1)])[None]
+        r = oracle.verify_chain_greedy(Lp, np.array([x], np.int32), lib=lib)
+        g = []
+        for j in range(K + 1):
+            g.append(int(np.argmax(lp[tuple(g)])))  # numpy: first maximum
+        m = 0
+        while m < K and x[m] == g[m]:
+            m += 1
+        assert r["accept_len"][0] == m, (x, g, r)
+        assert list(r["out_tokens"][0, : m + 1]) == g[: m + 1], (x, g, r)
+        assert all(t == -1 for t in r["out_tokens"][0, m + 1:])
+
+
+def pin_greedy_example(lib):
+    """SubSpec review, Method 2: draft "keys at the office" after "I left my";
+    the target keeps "keys at", replaces "the" by "home", drops "office"."""
+    g = golden("greedy_keys_example.json")
+    ids = g["token_ids"]
+    V, K = g["V"], len(g["draft"])
+    Lp = np.zeros((1, K + 1, V))
+    for k, w in enumerate(g["target_top"]):
+        Lp[0, k, ids[w]] = 5.0
+    x = np.array([[ids[w] for w in g["draft"]]], np.int32)
+    r = oracle.verify_chain_greedy(Lp, x, lib=lib)
+    assert r["accept_len"][0] == g["accept_len"]
+    want = [ids[w] for w in g["emitted"]]
+    assert list(r["out_tokens"][0, : len(want)]) == want
+    assert all(t == -1 for t in r["out_tokens"][0, len(want):])
+
+
+def pin_accept_boundary(lib):
+    """Reading u < p/q: a uniform equal to the ratio rejects; zero-mass ids are
+    never drawn (inverse CDF with strict >, ur = 0)."""
+    # p = (0.5, 0.5), q = (1, 0): r(A) = 0.5 exactly
+    lp = np.log(np.array([[0.5, 0.5], [0.5, 0.5]]))
+    lq = np.array([[0.0, -np.inf]])
+    call = ChainCall(lib, lp, lq, [0], 1.0)
+    assert call([0.5], 0.5)[0] == 0
+    assert call([math.nextafter(0.5, 0.0)], 0.5)[0] == 1
+    # residual (0, 0.5): ur = 0 must still draw B
+    m, out = call([0.75], 0.0)
+    assert m == 0 and out == (1,), out
+    # bonus draw with a zero-mass head: p = (0, 0, 1/2, 1/2), ur = 0 -> id 2
+    lp2 = np.array([[0.0, 0.0, 0.0, 0.0], [-np.inf, -np.inf, 0.0, 0.0]])
+    lq2 = np.array([[0.0, 0.0, 0.0, 0.0]])
+    call2 = ChainCall(lib, lp2, lq2, [1], 1.0)
+    m, out = call2([0.0], 0.0)
+    assert m == 1 and out == (1, 2), out
+
+
+def pin_tree_bruteforce(lib, trials=60, seed=0):
+    """Longest accepted path from the retrieve-row scan equals a brute-force
+    search over the ancestor mask (TAPS: the longest accepted path is kept)."""
+    import torch
+
+    from gen import random_tree_parents, tree_from_parents
+    from gen.workloads import merged_parents
+
+    rng = np.random.default_rng(seed)
+    g = torch.Generator().manual_seed(seed)
+    for trial in range(trials):
+        n1 = int(rng.integers(0, 6))
+        n2 = int(rng.integers(0, 6))
+        p1 = random_tree_parents(n1, g, max_depth=4, max_children=3)
+        p2 = random_tree_parents(n2, g, max_depth=4, max_children=3)
+        pm = merged_parents(p1, p2)
+        N = len(pm)
+        R, mask, pos = tree_from_parents(pm, width=6)
+        V = 3
+        Lt = rng.normal(0, 1, (1, N, V))
+        tok = rng.integers(0, V, N).astype(np.int32)
+        r = oracle.verify_tree_greedy(Lt, tok[None], R.numpy()[None], n1, mask=mask.numpy()[None], lib=lib)
+        assert r["status"][0] == 0
+        a = [int(np.argmax(Lt[0, i])) for i in range(N)]
+        assert list(r["argmax"][0]) == a
+        L = oracle.tree_bruteforce_depth(mask.numpy(), tok, np.array(a, np.int32), lib=lib)
+        assert r["accept_len"][0] == L, (trial, r["accept_len"][0], L)
+        # the reported path is a real path whose tokens match
+        path = [int(v) for v in r["path"][0] if v != -1]
+        assert path[0] == 0 and len(path) == L + 1
+        for t in range(1, len(path)):
+            assert pm[path[t]] == path[t - 1]
+            assert tok[path[t]] == a[path[t - 1]]
+        out = [int(v) for v in r["out_tokens"][0] if v != -1]
+        assert out == [int(tok[v]) for v in path[1:]] + [a[path[-1]]]
+        sub = 0 if L == 0 else (1 if path[1] <= n1 else 2)
+        assert r["subtree"][0] == sub
+        # lowest retrieve row among the longest
+        Ls = []
+        for row in R.numpy():
+            Lr = 0
+            for t in range(1, len(row)):
+                if row[t] == -1 or tok[row[t]] != a[row[t - 1]]:
+                    break
+                Lr = t
+            Ls.append(Lr)
+        assert r["best_row"][0] == int(np.argmax(Ls))
+
+
+def pin_tree_chain_reduction(lib, seed=0):
+    """A merged tree whose tree 2 is empty and whose tree 1 is a single chain
+    verifies exactly like greedy chain verification of that chain."""
+    rng = np.random.default_rng(seed)
+    for trial in range(30):
+        K = int(rng.integers(1, 6))
+        V = 3
+        N = K + 1
+        Lt = rng.normal(0, 1, (1, N, V))
+        tok = rng.integers(0, V, N).astype(np.int32)
+        R = np.array([[list(range(N))]], np.int32)
+        t = oracle.verify_tree_greedy(Lt, tok[None], R, K, lib=lib)
+        c = oracle.verify_chain_greedy(Lt, tok[None, 1:], lib=lib)
+        assert t["accept_len"][0] == c["accept_len"][0]
+        L = int(c["accept_len"][0])
+        assert list(t["out_tokens"][0, : L + 1]) == list(c["out_tokens"][0, : L + 1])
+
+
+def pin_confidence(lib):
+    """TAPS confidence routing: arithmetic mean of node confidences per tree,
+    higher mean wins. Dyadic values make every mean exact."""
+    N, n1 = 9, 3
+    conf = np.full((4, N), 0.875, np.float32)  # entry 0 (the root) must be ignored
+    conf[0, 1:4] = 0.25
+    conf[0, 4:] = np.arange(1, 6) / 64.0  # mean 3/64
+    conf[1, 1:4] = [0.125, 0.5, 0.375]  # mean 1/3 * 1.0 = 0.3333...
+    conf[1, 4:] = 0.75
+    conf[2, 1:4] = 0.5
+    conf[2, 4:] = 0.5  # tie -> tree 1, flagged
+    conf[3, 1:4] = [1.0, 0.0, 0.5]
+    conf[3, 4:] = [0.0, 0.0, 0.0, 0.0, 2.5]
+    r = oracle.tree_confidence(conf, n1, lib=lib)
+    want = np.array([[0.25, 3 / 64], [1 / 3, 0.75], [0.5, 0.5], [0.5, 0.5]])
+    assert np.allclose(r["scores"], want, rtol=0, atol=1e-15), r["scores"]
+    assert list(r["choice"]) == [1, 2, 1, 1]
+    assert list(r["flags"] != 0) == [False, False, True, True]
+    r2 = oracle.tree_confidence(conf[:, :4], 3, lib=lib)  # tree 2 empty
+    assert np.all(np.isneginf(r2["scores"][:, 1])) and list(r2["choice"]) == [1, 1, 1, 1]
+
+
+ALL_PINS = [
+    ("ab_example", pin_ab_example),
+    ("lossless_V3K2", lambda lib: pin_lossless(lib, 3, 2, 1.0, 1)),
+    ("lossless_V3K2_T07", lambda lib: pin_lossless(lib, 3, 2, 0.7, 2)),
+    ("greedy_world", pin_greedy_world),
+    ("greedy_world_ties", lambda lib: pin_greedy_world(lib, ties=True, seed=3)),
+    ("greedy_example", pin_greedy_example),
+    ("accept_boundary", pin_accept_boundary),
+    ("tree_bruteforce", pin_tree_bruteforce),
+    ("tree_chain_reduction", pin_tree_chain_reduction),
+    ("confidence", pin_confidence),
+]

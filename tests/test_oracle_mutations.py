@@ -1,0 +1,69 @@
+"""Planted mistakes in a copy of the oracle must trip at least one pin.
+
+Each mutation edits the C source of a temporary copy of the oracle (a
+dropped clamp, a swapped operand, an off-by-one row, a wrong tie-break, ...),
+builds it with the same flags and runs the pins against it. This shows the
+pins constrain every step of the oracle, not just that it runs. CPU only; the
+real oracle is never modified.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+MUTATIONS = {
+    "residual_operands_swapped*": (
+        "w = fmax(0.0, w - prob(Lq, dt, offq, v, T, Mq[m], Zq[m]));",
+        "w = fmax(0.0, prob(Lq, dt, offq, v, T, Mq[m], Zq[m]) - w);"),
+    "residual_clamp_dropped": (
+        "w = fmax(0.0, w - prob(Lq, dt, offq, v, T, Mq[m], Zq[m]));",
+        "w = w - prob(Lq, dt, offq, v, T, Mq[m], Zq[m]);"),
+    "ratio_inverted": (
+        "double r = q > 0.0 ? p / q : INFINITY;",
+        "double r = p > 0.0 ? q / p : INFINITY;"),
+    "temperature_dropped_from_Z": (
+        "z += exp(elem(L, dt, off + (size_t)v) / T - m);",
+        "z += exp(elem(L, dt, off + (size_t)v) - m);"),
+    "last_rejection_instead_of_first": (
+        "        m = k;\n        break;\n      }\n    }\n    accept_len[b] = m;\n    for (int k = 0; k < m; ++k) out[k] = x[(size_t)b * K + k];\n\n",
+        "        m = k;\n      }\n    }\n    accept_len[b] = m;\n    for (int k = 0; k < m; ++k) out[k] = x[(size_t)b * K + k];\n\n"),
+    "accept_with_le": ("if (!(u < r))", "if (!(u <= r))"),
+    "cdf_with_ge": ("if (C > t)", "if (C >= t)"),
+    "bonus_from_previous_row": (
+        "size_t offp = ((size_t)b * (K + 1) + m) * (size_t)V;",
+        "size_t offp = ((size_t)b * (K + 1) + (m == K ? K - 1 : m)) * (size_t)V;"),
+    "px_with_draft_normaliser": (
+        "xk, T, Mp[k], Zp[k]);", "xk, T, Mq[k], Zq[k]);"),
+    "residual_not_normalised": ("double t = ur[b] * S,", "double t = ur[b],"),
+    "greedy_tie_to_highest": ("else if (s > bv)", "else if (s >= bv)"),
+    "greedy_emits_draft_at_m": ("out[m] = a[m];", "out[m] = m < K ? x[(size_t)b * K + m] : a[m];"),
+    "tree_compares_own_argmax": (
+        "if (nd == -1 || tk[nd] != a[row[t - 1]]) break;", "if (nd == -1 || tk[nd] != a[nd]) break;"),
+    "tree_last_best_row": ("if (L > bestL) {", "if (L >= bestL) {"),
+    "tree_bonus_from_parent": ("out[bestL] = a[row[bestL]];", "out[bestL] = a[row[bestL > 0 ? bestL - 1 : 0]];"),
+    "tree_subtree_boundary": ("(row[1] <= n1 ? 1 : 2)", "(row[1] < n1 ? 1 : 2)"),
+    "confidence_wrong_count": ("s2 = n2 > 0 ? s2 / n2 : -INFINITY;", "s2 = n2 > 0 ? s2 / n1 : -INFINITY;"),
+    "confidence_root_included": ("for (int i = 1; i <= n1; ++i) s1 +=", "for (int i = 0; i <= n1; ++i) s1 +="),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(oracle._SRC).read()
+    assert old in src, f"mutation anchor for {name} no longer in oracle.c"
+    mutated = tmp_path / "oracle_mut.c"
+    # a trailing "*" in the name applies the edit to every occurrence
+    mutated.write_text(src.replace(old, new) if name.endswith("*") else src.replace(old, new, 1))
+    lib = oracle.load(oracle.build(str(mutated), str(tmp_path / "liboracle_mut.so"), force=True))
+    caught = []
+    for pin_name, pin in P.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin_name)
+            break
+    assert caught, f"no pin caught mutation {name}"
