@@ -71,7 +71,7 @@ def _declare(lib):
     P = ctypes.c_void_p
     i = ctypes.c_int
     d = ctypes.c_double
-    lib.orc_verify_chain.argtypes = [P, P, i, P, P, P, d, i, i, i, i, i, P, P, P, P, P, P, P, P]
+    lib.orc_verify_chain.argtypes = [P, P, i, P, P, P, d, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_chain.restype = None
     lib.orc_verify_chain_greedy.argtypes = [P, i, P, i, i, i, i, i, P, P, P, P]
     lib.orc_verify_chain_greedy.restype = None
@@ -151,9 +151,9 @@ def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None) -> Dic
     """Speculative-sampling chain verification (T > 0) in fp64.
 
     Returns accept_len [B], out_tokens [B, K+1], lse_p [B, K+1], lse_q [B, K],
-    px / qx [B, K] (target / draft probability of each draft token), status [B]
-    and flags [B] (FL_ACCEPT / FL_SAMPLE: a uniform within 1e-6 of a decision
-    boundary)."""
+    px / qx [B, K] (target / draft probability of each draft token), status [B],
+    flags [B] (FL_ACCEPT / FL_SAMPLE: a uniform within 1e-6 of a decision
+    boundary) and margin [B] (distance to the nearest boundary met)."""
     if not T > 0:
         raise ValueError("verify_chain needs T > 0; use verify_chain_greedy for T == 0")
     lib = lib or load()
@@ -175,13 +175,14 @@ def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None) -> Dic
         qx=np.empty((B, K), np.float64),
         status=np.empty(B, np.int32),
         flags=np.empty(B, np.int32),
+        margin=np.empty(B, np.float64),
     )
 
     def part(b0, b1):
         lib.orc_verify_chain(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), B, K, V,
                              b0, b1, _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["lse_p"]),
                              _ptr(out["lse_q"]), _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["status"]),
-                             _ptr(out["flags"]))
+                             _ptr(out["flags"]), _ptr(out["margin"]))
 
     _run(part, B, threads)
     return out

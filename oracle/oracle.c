@@ -89,7 +89,7 @@ static double prob(const void* L, int dt, size_t off, int v, double T, double M,
 }
 
 /* Index of the largest entry, lowest index on ties; -1 when no entry is above
- * -inf. *nan is set when the row holds a NaN (a NaN never wins). */
+ * -inf or when the row holds a NaN (then *nan is set). */
 static int row_argmax(const void* L, int dt, size_t off, int V, int* nan) {
   int best = -1;
   double bv = -INFINITY;
@@ -101,7 +101,7 @@ static int row_argmax(const void* L, int dt, size_t off, int V, int* nan) {
       best = v;
     }
   }
-  return best;
+  return *nan ? -1 : best;
 }
 
 /* Speculative-sampling chain verification, T > 0, rows b in [b0, b1).
@@ -109,15 +109,19 @@ static int row_argmax(const void* L, int dt, size_t off, int V, int* nan) {
  * ua: [B][K] accept uniforms; ur: [B] resample uniforms.
  * Out: accept_len [B] (= m), out_tok [B][K+1] (x_0..x_{m-1}, then the drawn
  * token, then -1), lse_p [B][K+1], lse_q [B][K], px / qx [B][K] (p_k(x_k),
- * q_k(x_k)), status [B], flags [B] (near ties). */
+ * q_k(x_k)), status [B], flags [B] (near ties), margin [B] (distance of the
+ * row's uniforms to the nearest decision boundary it met: every tested
+ * acceptance threshold r_k < 1 and the two CDF boundaries of the drawn token;
+ * +inf when none). */
 void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
                       const double* ur, double T, int B, int K, int V, int b0, int b1,
                       int32_t* accept_len, int32_t* out_tok, double* lse_p, double* lse_q, double* px,
-                      double* qx, int32_t* status, int32_t* flags) {
+                      double* qx, int32_t* status, int32_t* flags, double* margin) {
   (void)B;
   double Mp[K + 1], Zp[K + 1], Mq[K + 1], Zq[K + 1];
   for (int b = b0; b < b1; ++b) {
     int st = 0, fl = 0;
+    double mg = INFINITY;
     for (int k = 0; k <= K; ++k) {
       size_t off = ((size_t)b * (K + 1) + k) * (size_t)V;
       if (softmax_stats(Lp, dt, off, V, T, &Mp[k], &Zp[k])) st |= ST_TARGET;
@@ -140,6 +144,7 @@ void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, 
     if (st) {
       accept_len[b] = -1;
       flags[b] = 0;
+      margin[b] = INFINITY;
       continue;
     }
     for (int k = 0; k < K; ++k) {
@@ -153,6 +158,7 @@ void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, 
       double p = px[(size_t)b * K + k], q = qx[(size_t)b * K + k];
       double r = q > 0.0 ? p / q : INFINITY;
       double u = ua[(size_t)b * K + k];
+      if (r < 1.0) mg = fmin(mg, fabs(u - r));
       if (r < 1.0 && fabs(u - r) < NEAR) fl |= FL_ACCEPT;
       if (!(u < r)) {
         m = k;
@@ -194,11 +200,15 @@ void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, 
     if (tok < 0) {
       tok = last_pos; /* rounding left no crossing */
       fl |= FL_SAMPLE;
-    } else if (fabs(ur[b] - Cprev / S) < NEAR || fabs(ur[b] - C / S) < NEAR) {
-      fl |= FL_SAMPLE;
+      mg = 0.0;
+    } else {
+      double near = fmin(fabs(ur[b] - Cprev / S), fabs(ur[b] - C / S));
+      mg = fmin(mg, near);
+      if (near < NEAR) fl |= FL_SAMPLE;
     }
     out[m] = tok;
     flags[b] = fl;
+    margin[b] = mg;
   }
 }
 
@@ -289,7 +299,8 @@ void orc_verify_tree_greedy(const void* Lt, int dt, const int32_t* tok, const in
           st |= ST_TREE;
           continue;
         }
-        if (mask && !mask[((size_t)b * N + nd) * N + row[t - 1]]) st |= ST_MASK;
+        int pv = row[t - 1];
+        if (mask && pv >= 0 && pv < N && !mask[((size_t)b * N + nd) * N + pv]) st |= ST_MASK;
       }
     }
     if (!any_row) st |= ST_TREE;

@@ -58,13 +58,14 @@ class ChainCall:
         self.qx = np.zeros((1, max(K, 1)))
         self.st = np.zeros(1, np.int32)
         self.fl = np.zeros(1, np.int32)
+        self.mg = np.zeros(1, np.float64)
 
     def __call__(self, ua, ur):
         self.ua[0, :] = ua
         self.ur[0] = ur
         self.lib.orc_verify_chain(_p(self.Lp), _p(self.Lq), oracle.F64, _p(self.x), _p(self.ua), _p(self.ur),
                                   self.T, 1, self.K, self.V, 0, 1, _p(self.acc), _p(self.out), _p(self.lp),
-                                  _p(self.lq), _p(self.px), _p(self.qx), _p(self.st), _p(self.fl))
+                                  _p(self.lq), _p(self.px), _p(self.qx), _p(self.st), _p(self.fl), _p(self.mg))
         assert self.st[0] == 0, "unexpected row status"
         m = int(self.acc[0])
         return m, tuple(int(t) for t in self.out[0, : m + 1])
