@@ -1,0 +1,442 @@
+"""Benchmark: verified draft positions per second on GB300.
+
+Default workload (one "step" = one call of the verification path over one
+batch): chain verification with sampling, B=64 rows, K=8 draft tokens,
+V=128256 (Llama-3-8B vocabulary), bf16 logits, temperature 0.7, per-row draft
+noise. The step runs the rowscan pass (normalisers of all 1088 rows), the
+acceptance decision and the residual / bonus draw.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload chain_batched|chain_single|chain_deep|greedy|tree]
+
+Under torchrun each rank verifies its own batch (seed + rank) on its own GPU:
+rows are independent, so there is no collective in the data path (weak
+scaling); a barrier brackets the timed region and the max time over ranks is
+reported. ``--impl reference`` times the fp64 CPU oracle instead (rank 0).
+
+Prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec & logit-read HBM GB/s (B=64,K=8,V=128256)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------- workloads --
+
+def make_workload(name: str, seed: int):
+    import gen
+
+    if name == "chain_batched":
+        c = gen.config_chain_batched(seed)
+        return c, dict(workload="chain verify, batched serving: B=64 K=8 V=128256 bf16 T=0.7, draft noise "
+                                "sigma_b~U(0.2,2)", B=64, K=8, V=128256, logits="bf16", temperature=0.7)
+    if name == "chain_single":
+        c = gen.config_chain_single(seed, T=1.0)
+        return c, dict(workload="chain verify, single stream: B=1 K=5 V=128256 bf16 T=1", B=1, K=5, V=128256,
+                       logits="bf16", temperature=1.0)
+    if name == "chain_deep":
+        c = gen.config_chain_deep(seed)
+        return c, dict(workload="chain verify, deep drafts: B=256 K=16 V=152064 fp32 T=1", B=256, K=16, V=152064,
+                       logits="f32", temperature=1.0)
+    if name == "greedy":
+        c = gen.chain_zipf(64, 8, 128256, __import__("torch").bfloat16, 0.0, 0.3, seed, name="greedy")
+        return c, dict(workload="greedy chain verify: B=64 K=8 V=128256 bf16 T=0", B=64, K=8, V=128256,
+                       logits="bf16", temperature=0.0)
+    if name == "tree":
+        t = gen.config_tree(seed)
+        return t, dict(workload="merged-tree greedy verify + confidence routing: B=16 N=61 V=128256 bf16", B=16,
+                       N=61, V=128256, logits="bf16")
+    raise SystemExit(f"unknown workload {name}")
+
+
+def units_per_step(name, w):
+    if name == "tree":
+        return w.B * (w.N - 1)  # verified nodes
+    return w.B * w.K  # verified draft positions
+
+
+def algorithmic_bytes(name, w):
+    """Logit bytes the dominant kernel (the rowscan pass) must read per
+    launch: every row once."""
+    es = w.Lt.element_size() if name == "tree" else w.Lp.element_size()
+    if name == "tree":
+        return w.B * w.N * w.V * es
+    if name == "greedy" or w.T == 0.0:
+        return w.B * (w.K + 1) * w.V * es
+    return w.B * (2 * w.K + 1) * w.V * es
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy)}
+
+
+# --------------------------------------------------------------- our arm --
+
+def traffic_for(kernel_key: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, valid only while the kernel's source is unchanged."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        ent = t[kernel_key]
+        src = open(os.path.join(ROOT, ent["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest()[:16] != ent["source_sha"]:
+            return None
+        return ent["bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_29_gb300 as sv
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w, cfg = make_workload(args.workload, args.seed + rank)
+    name = args.workload
+    stream = torch.cuda.current_stream()
+
+    if name == "tree":
+        Lt, tok, R, mask, conf = (w.Lt.to(dev), w.tok.to(dev), w.R.to(dev), w.mask.to(dev), w.conf.to(dev))
+        ws_t = sv.alloc_workspace(sv.workspace_bytes(w.B, w.N - 1, w.V, Lt.dtype), dev)
+        out = sv.spec_verify_tree_greedy(Lt, tok, R, w.n1, tree_mask=mask, workspace=ws_t)
+        cout = sv.spec_tree_confidence(conf, w.n1)
+
+        def step_dev():
+            sv.spec_verify_tree_greedy(Lt, tok, R, w.n1, tree_mask=mask, out=out, workspace=ws_t)
+            sv.spec_tree_confidence(conf, w.n1, out=cout)
+
+        def step_split(ev):
+            ev[0].record(stream)
+            sv.spec_verify_tree_greedy(Lt, tok, R, w.n1, tree_mask=mask, out=out, workspace=ws_t)
+            ev[1].record(stream)
+            sv.spec_tree_confidence(conf, w.n1, out=cout)
+            ev[2].record(stream)
+
+        launches_per_step = 3
+        host = [w.Lt, w.tok, w.R, w.mask, w.conf]
+    else:
+        Lp, Lq, x, ua, ur = (w.Lp.to(dev), w.Lq.to(dev), w.x.to(dev), w.ua.to(dev), w.ur.to(dev))
+        T = w.T
+        ws_t = sv.alloc_workspace(sv.workspace_bytes(w.B, w.K, w.V, Lp.dtype), dev)
+        if T == 0.0:
+            out = sv.spec_verify_chain_greedy(Lp, x, workspace=ws_t)
+
+            def step_dev():
+                sv.spec_verify_chain_greedy(Lp, x, out=out, workspace=ws_t)
+
+            def step_split(ev):
+                ev[0].record(stream)
+                sv.spec_verify_chain_greedy(Lp, x, out=out, workspace=ws_t)
+                ev[1].record(stream)
+                ev[2].record(stream)
+        else:
+            out = sv.spec_verify_chain(Lp, Lq, x, ua, ur, T, workspace=ws_t)
+
+            def step_dev():
+                sv.spec_verify_chain(Lp, Lq, x, ua, ur, T, out=out, workspace=ws_t)
+
+            def step_split(ev):
+                ev[0].record(stream)
+                sv.spec_chain_scan(Lp, Lq, x, ua, ur, T, out, ws_t)
+                ev[1].record(stream)
+                sv.spec_chain_sample(Lp, Lq, x, ua, ur, T, out, ws_t)
+                ev[2].record(stream)
+
+        launches_per_step = 2
+        host = [w.Lp, w.Lq, w.x, w.ua, w.ur]
+
+    # warm-up, then a short untimed soak so the clock sampler sees the load
+    for _ in range(max(args.warmup, 3)):
+        step_dev()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak:
+        for _ in range(20):
+            step_dev()
+        torch.cuda.synchronize()
+
+    # timed region: events around the dominant kernel and the whole step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        step_split(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the public API with pinned host buffers
+    pinned = [h.pin_memory() for h in host]
+    h2d = sum(h.numel() * h.element_size() for h in pinned)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    d2h = 0
+    for _ in range(e2e_steps):
+        if name == "tree":
+            o = sv.spec_verify_tree_greedy(pinned[0], pinned[1], pinned[2], w.n1, tree_mask=pinned[3], device=dev)
+            co = sv.spec_tree_confidence(pinned[4], w.n1, device=dev)
+            res = [o["accept_len"].cpu(), o["out_tokens"].cpu(), co["choice"].cpu()]
+        elif w.T == 0.0:
+            o = sv.spec_verify_chain_greedy(pinned[0], pinned[2], device=dev)
+            res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
+        else:
+            o = sv.spec_verify_chain(pinned[0], pinned[1], pinned[2], pinned[3], pinned[4], w.T, device=dev,
+                                     stats=False)
+            res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
+        d2h = sum(r.numel() * r.element_size() for r in res)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if ws > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    clk = clocks.stop() if clocks else None
+
+    units = units_per_step(name, w)
+    value = units * args.steps * ws / (total_ms / 1e3)
+    e2e_value = units * e2e_steps * ws / e2e_s
+    peak, peak_kind = _peaks()
+    alg = algorithmic_bytes(name, w)
+    k1_mean = float(np.mean(k1_ms))
+    achieved = alg / (k1_mean / 1e3) / 1e9
+    kernel_key = {"tree": "rowscan_argmax_tree", "greedy": "rowscan_argmax_chain"}.get(name, f"rowscan_stats_{name}")
+    line = {
+        "metric": METRIC if name == "chain_batched" else f"verified {'nodes' if name == 'tree' else 'draft positions'}/sec ({name})",
+        "value": value,
+        "unit": "nodes/s" if name == "tree" else "positions/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded generator: peaked logits, Gumbel-max draft tokens)",
+        "config": dict(cfg, parallelism=f"replicas x{ws} (independent batches, no data-path collective)",
+                       l2=f"inputs {alg / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB; no flush between steps"),
+        "logit_read_gbs": alg / (total_ms / args.steps / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "rowscan_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic_for(kernel_key), "algorithmic_bytes": alg,
+                     "kernel_ms_mean": k1_mean},
+        "e2e": {"value": e2e_value, "unit": "nodes/s" if name == "tree" else "positions/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if name != "tree":
+        al = out["accept_len"].cpu().numpy()
+        line["accept_len_mean"] = float(al[al >= 0].mean())
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(name, w, args.cpu_seconds)
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------ oracle (CPU) arm --
+
+def _oracle_step(name, w, rows, threads):
+    import torch
+
+    import oracle
+
+    idx = torch.as_tensor(rows)
+    if name == "tree":
+        oracle.verify_tree_greedy(w.Lt[idx], w.tok[idx], w.R[idx], w.n1, mask=w.mask[idx], threads=threads)
+        oracle.tree_confidence(w.conf[idx], w.n1)
+    elif w.T == 0.0:
+        oracle.verify_chain_greedy(w.Lp[idx], w.x[idx], threads=threads)
+    else:
+        oracle.verify_chain(w.Lp[idx], w.Lq[idx], w.x[idx], w.ua[idx], w.ur[idx], w.T, threads=threads)
+
+
+def _sample_rows(name, w, threads, budget_s):
+    """Rows per oracle step so that one step takes about budget_s seconds."""
+    t0 = time.perf_counter()
+    _oracle_step(name, w, [0], 1)
+    one = max(time.perf_counter() - t0, 1e-4)
+    n = int(budget_s * threads / one)
+    return max(1, min(w.B, n)), one
+
+
+def cpu_baseline(name, w, cpu_seconds):
+    threads = os.cpu_count() or 1
+    n, one = _sample_rows(name, w, threads, cpu_seconds / threads / 3)
+    rows = list(range(n))
+    reps, t_tot = 0, 0.0
+    while reps < 3:
+        t0 = time.perf_counter()
+        _oracle_step(name, w, rows, threads)
+        t_tot += time.perf_counter() - t0
+        reps += 1
+    per_row_units = (w.N - 1) if name == "tree" else w.K
+    return {"value": n * per_row_units * reps / t_tot, "unit": "nodes/s" if name == "tree" else "positions/s",
+            "cores": min(threads, n), "kind": "oracle",
+            "sample": f"{n} of {w.B} rows of the same batch, {reps} repeats, fp64 C oracle on {min(threads, n)} "
+                      f"threads ({t_tot:.1f} s wall)"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    w, cfg = make_workload(args.workload, args.seed)
+    name = args.workload
+    threads = os.cpu_count() or 1
+    step_budget = max(0.2, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    n, _ = _sample_rows(name, w, threads, step_budget)
+    rows = list(range(n))
+    for _ in range(args.warmup):
+        _oracle_step(name, w, rows, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(name, w, rows, threads)
+    dt = time.perf_counter() - t0
+    per_row_units = (w.N - 1) if name == "tree" else w.K
+    value = n * per_row_units * args.steps / dt
+    unit = "nodes/s" if name == "tree" else "positions/s"
+    line = {
+        "impl": "reference",
+        "metric": METRIC if name == "chain_batched" else f"verified positions/sec ({name})",
+        "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (same seeded generator)", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": min(threads, n), "kind": "oracle",
+                         "sample": f"each step verifies {n} of {w.B} rows of the batch on {min(threads, n)} threads"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="chain_batched",
+                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

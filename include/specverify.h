@@ -1,0 +1,180 @@
+/*
+ * specverify.h -- C ABI of the speculative-sampling verification library
+ * (libspecverify.so, CUDA kernels for sm_103a).
+ *
+ * What it computes. A target model scores K draft tokens plus one bonus
+ * position in one pass; these calls turn those scores into the tokens the
+ * target alone would emit.
+ *   - spec_verify_chain: temperature T on target and draft logits, softmax
+ *     over the full vocabulary, accept draft token x_k with probability
+ *     min(1, p_k(x_k) / q_k(x_k)) left to right, and at the first rejection m
+ *     draw from max(0, p_m - q_m) renormalised, or draw the bonus token from
+ *     p_K when all K are accepted (Leviathan et al., as summarised on the
+ *     ariser.io page, section on keeping the same distribution; lotook.com,
+ *     "how does speculative decoding work step by step").
+ *   - spec_verify_chain_greedy: temperature 0, accept while x_k is the
+ *     target's top token, then emit the target's top token (lotook.com, same
+ *     section and FAQ; SubSpec review, Method 2, the "I left my keys" example).
+ *   - spec_verify_tree_greedy: greedy verification of two drafter trees merged
+ *     under one shared root, keeping the longest accepted root-to-leaf path
+ *     (TAPS page, methodology, merged-tree verification; tree layout as in its
+ *     tree-merging code example).
+ *   - spec_tree_confidence: confidence routing, the arithmetic mean of the
+ *     nodes' drafter confidences per tree, higher wins (TAPS page,
+ *     methodology, confidence routing).
+ *
+ * Conventions shared by every call.
+ *   - Pointers marked "device" are device pointers owned by the caller; the
+ *     library allocates nothing, takes no ownership and keeps no pointer after
+ *     the call returns. `stream` is a cudaStream_t (NULL = legacy default).
+ *   - Calls are asynchronous: they validate sizes and pointers on the host,
+ *     enqueue kernels on `stream` and return. Results are ready when the
+ *     stream is synchronised. A non-zero return means nothing was enqueued
+ *     (except SPEC_ERR_CUDA, which reports a failed launch).
+ *   - Logit tensors are row-major and contiguous with V innermost; dtype is
+ *     spec_dtype. Rows are read with 16-byte vector loads when V * element
+ *     size is a multiple of 16 and the base pointer is 16-byte aligned;
+ *     otherwise a scalar path is used (correct, slower).
+ *   - Per-row data errors never trap or abort: they set bits in
+ *     row_status[b] (SPEC_ROW_*), and that row's integer outputs are -1 and
+ *     its float outputs NaN.
+ *   - Uniforms are caller-supplied (no device RNG): u_accept[b][k] is used
+ *     only for k <= m, u_resample[b] once per row. Accept iff
+ *     u_accept < p/q; a draw picks the smallest token id i whose cumulative
+ *     mass exceeds u * total (ids in ascending order, strict ">").
+ *   - Greedy ties (equal logits) go to the lowest token id.
+ *   - Integer outputs are exact. Float outputs (log-normalisers and
+ *     probabilities) are fp32, accumulated with fp32 partial sums combined
+ *     in compensated arithmetic.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of logit buffers. */
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+/* Return codes. */
+enum {
+  SPEC_OK = 0,
+  SPEC_ERR_ARG = -1,        /* a size, pointer, dtype or temperature is invalid */
+  SPEC_ERR_WORKSPACE = -2,  /* workspace NULL, misaligned (256 B) or too small */
+  SPEC_ERR_CUDA = -3,       /* a kernel launch failed (cudaGetLastError) */
+  SPEC_ERR_UNSUPPORTED = -4 /* sizes beyond the documented limits */
+};
+
+/* row_status bits. */
+#define SPEC_ROW_TOKEN 1  /* a draft or node token outside [0, V) */
+#define SPEC_ROW_TARGET 2 /* a target row holds a NaN or has no finite maximum
+                             (all -inf; with T > 0 also a +inf entry) */
+#define SPEC_ROW_DRAFT 4  /* the same for a draft row */
+#define SPEC_ROW_TREE 8   /* a malformed retrieve row */
+#define SPEC_ROW_MASK 16  /* a retrieve row that contradicts tree_mask */
+
+/* Limits: 1 <= B <= 65535; 0 <= K <= 255; 2 <= V <= 2^24; for trees
+ * 1 <= N <= 1024, 1 <= D <= 64, 1 <= R <= 4096. */
+
+/* Workspace bytes needed by spec_verify_chain / spec_verify_chain_greedy for
+ * (B, K, V, dtype), and by spec_verify_tree_greedy with K = N - 1. The
+ * workspace is scratch the caller allocates in device memory (256-byte
+ * aligned); its contents need no initialisation and are not meaningful after
+ * the call. Calls that share a workspace must not overlap on the GPU.
+ * Returns 0 for invalid sizes. */
+size_t spec_workspace_bytes(int B, int K, int V, int dtype);
+
+/* Chain verification with sampling (T > 0); T == 0 forwards to the greedy
+ * path (draft logits are then not read and the float outputs are NaN).
+ *   target_logits  device [B][K+1][V]  dtype
+ *   draft_logits   device [B][K][V]    dtype
+ *   draft_tokens   device [B][K] int32
+ *   u_accept       device [B][K] fp32 in [0,1)
+ *   u_resample     device [B]    fp32 in [0,1)
+ *   temperature    >= 0, finite; applied to both target and draft logits
+ * Outputs (device):
+ *   accept_len [B] int32: m, the number of accepted draft tokens (0..K)
+ *   out_tokens [B][K+1] int32: x_0..x_{m-1}, the drawn token, then -1
+ *   lse_target [B][K+1], lse_draft [B][K] fp32 or NULL: log-normalisers
+ *       log sum_v exp(l_v / T) of each row
+ *   p_at_x, q_at_x [B][K] fp32 or NULL: p_k(x_k), q_k(x_k)
+ *   row_status [B] int32 (SPEC_ROW_* bits, 0 = ok)
+ * Stages: spec_chain_scan then spec_chain_sample on the same stream. */
+int spec_verify_chain(const void* target_logits, const void* draft_logits, int dtype,
+                      const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                      float temperature, int B, int K, int V, int32_t* accept_len, int32_t* out_tokens,
+                      float* lse_target, float* lse_draft, float* p_at_x, float* q_at_x,
+                      int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage A of spec_verify_chain: the streaming pass, one read of every target
+ * and draft row, leaving per-chunk (max, sum of exp) partials in the
+ * workspace. T > 0. Same arguments as spec_verify_chain (only the logits,
+ * dtype, temperature, sizes, workspace and stream are used). */
+int spec_chain_scan(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                    const float* u_accept, const float* u_resample, float temperature, int B, int K, int V,
+                    int32_t* accept_len, int32_t* out_tokens, float* lse_target, float* lse_draft, float* p_at_x,
+                    float* q_at_x, int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage B of spec_verify_chain: per row b, the normalisers, the acceptance
+ * test, the accepted prefix and the residual or bonus draw; writes every
+ * output. Must follow spec_chain_scan on the same stream with the same
+ * arguments and workspace. */
+int spec_chain_sample(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                      const float* u_accept, const float* u_resample, float temperature, int B, int K, int V,
+                      int32_t* accept_len, int32_t* out_tokens, float* lse_target, float* lse_draft,
+                      float* p_at_x, float* q_at_x, int32_t* row_status, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* Greedy chain verification (temperature 0): reads target logits only.
+ *   target_logits device [B][K+1][V]; draft_tokens device [B][K] int32
+ * Outputs (device): accept_len [B]; out_tokens [B][K+1] (x_0..x_{m-1}, a_m,
+ * then -1); argmax_ids [B][K+1] int32 or NULL (a_k, the target's top token at
+ * each position); row_status [B]. */
+int spec_verify_chain_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens, int B,
+                             int K, int V, int32_t* accept_len, int32_t* out_tokens, int32_t* argmax_ids,
+                             int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Merged-tree greedy verification.
+ *   node_logits      device [B][N][V] dtype: the target's scores at every node
+ *   node_tokens      device [B][N] int32: node 0 is the shared root
+ *   retrieve_indices device [B][R][D] int32: each row a root-to-leaf path of
+ *                    node indices starting with 0, padded with -1; a row of
+ *                    all -1 is padding
+ *   tree_mask        device [B][N][N] uint8 or NULL: self-inclusive ancestor
+ *                    mask; when given, every retrieve step is checked
+ *                    against it (SPEC_ROW_MASK)
+ *   n1               nodes 1..n1 belong to tree 1, n1+1..N-1 to tree 2
+ * For row r, L_r is the largest j such that the node at depth t carries the
+ * top token of the node at depth t-1 for every t <= j. The lowest r with the
+ * largest L_r wins. Outputs (device): accept_len [B] (= L); best_row [B];
+ * path_nodes [B][D] (the accepted nodes, root first, -1 padded); out_tokens
+ * [B][D] (tokens at depths 1..L, then the top token at depth L, -1 padded);
+ * subtree [B] (0 = only the root accepted, 1 or 2 = the tree the path runs
+ * through); row_status [B]. Workspace: spec_workspace_bytes(B, N-1, V, dtype). */
+int spec_verify_tree_greedy(const void* node_logits, int dtype, const int32_t* node_tokens,
+                            const int32_t* retrieve_indices, const uint8_t* tree_mask, int B, int N, int R,
+                            int D, int V, int n1, int32_t* accept_len, int32_t* best_row,
+                            int32_t* path_nodes, int32_t* out_tokens, int32_t* subtree,
+                            int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Confidence routing over a merged tree.
+ *   node_conf device [B][N] fp32 (entry 0, the root, is ignored)
+ * Outputs (device): scores [B][2] fp32, the mean confidence of tree 1 (nodes
+ * 1..n1) and tree 2 (n1+1..N-1), -inf for an empty tree, summed in fp64 in
+ * node order; choice [B] int32, 2 if score_2 > score_1 (compared in fp64)
+ * else 1. */
+int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* scores, int32_t* choice,
+                         void* stream);
+
+/* Static description of a return code. */
+const char* spec_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

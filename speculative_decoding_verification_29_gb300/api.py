@@ -1,0 +1,193 @@
+"""Torch-facing binding of the C ABI: argument marshalling only.
+
+Each function takes torch tensors, allocates the outputs (and the
+workspace) on the logits' device unless they are passed in, and calls the
+C entry point of the same name on the current CUDA stream. Every step of
+verification runs in the library's CUDA kernels. Host (CPU) inputs are
+copied to ``device`` first; that is the end-to-end path a caller with host
+buffers uses.
+"""
+
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import _lib
+from ._lib import SPEC_BF16, SPEC_F32, check
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, device, dtype=None) -> torch.Tensor:
+    if t.device.type != "cuda":
+        t = t.to(device, non_blocking=True)
+    if dtype is not None and t.dtype != dtype:
+        t = t.to(dtype)
+    return t.contiguous()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def workspace_bytes(B: int, K: int, V: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32)
+    return int(_lib.load().spec_workspace_bytes(B, K, V, code))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """Device workspace with a 256-byte aligned start."""
+    buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off: off + nbytes]
+
+
+def spec_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
+                      out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                      device="cuda", stream=None, stats: bool = True) -> Dict[str, torch.Tensor]:
+    """Chain verification (sampling at T > 0, greedy at T == 0).
+
+    target_logits [B, K+1, V], draft_logits [B, K, V] (bf16 or fp32),
+    draft_tokens [B, K] int32, u_accept [B, K] fp32, u_resample [B] fp32.
+    Returns accept_len, out_tokens, row_status and (with ``stats``)
+    lse_target, lse_draft, p_at_x, q_at_x."""
+    lib = _lib.load()
+    dev = target_logits.device if target_logits.device.type == "cuda" else torch.device(device)
+    Lp = _dev(target_logits, dev)
+    Lq = _dev(draft_logits, dev)
+    x = _dev(draft_tokens, dev, torch.int32)
+    ua = _dev(u_accept, dev, torch.float32)
+    ur = _dev(u_resample, dev, torch.float32)
+    B, K1, V = Lp.shape
+    K = K1 - 1
+    dt = _dtype_code(Lp)
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+        if stats:
+            out.update(lse_target=torch.empty(B, K + 1, device=dev), lse_draft=torch.empty(B, K, device=dev),
+                       p_at_x=torch.empty(B, K, device=dev), q_at_x=torch.empty(B, K, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(B, K, V, dt), dev)
+    rc = lib.spec_verify_chain(
+        Lp.data_ptr(), Lq.data_ptr(), dt, x.data_ptr(), ua.data_ptr(), ur.data_ptr(), float(temperature), B, K, V,
+        out["accept_len"].data_ptr(), out["out_tokens"].data_ptr(), _ptr(out.get("lse_target")),
+        _ptr(out.get("lse_draft")), _ptr(out.get("p_at_x")), _ptr(out.get("q_at_x")), out["row_status"].data_ptr(),
+        workspace.data_ptr(), workspace.numel(), _stream(stream))
+    check("spec_verify_chain", rc)
+    return out
+
+
+def _stage(name, target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
+           out: Dict[str, torch.Tensor], workspace: torch.Tensor, stream=None) -> None:
+    B, K1, V = target_logits.shape
+    fn = getattr(_lib.load(), name)
+    rc = fn(target_logits.data_ptr(), draft_logits.data_ptr(), _dtype_code(target_logits), draft_tokens.data_ptr(),
+            u_accept.data_ptr(), u_resample.data_ptr(), float(temperature), B, K1 - 1, V, out["accept_len"].data_ptr(),
+            out["out_tokens"].data_ptr(), _ptr(out.get("lse_target")), _ptr(out.get("lse_draft")),
+            _ptr(out.get("p_at_x")), _ptr(out.get("q_at_x")), out["row_status"].data_ptr(), workspace.data_ptr(),
+            workspace.numel(), _stream(stream))
+    check(name, rc)
+
+
+def spec_chain_scan(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
+                    out: Dict[str, torch.Tensor], workspace: torch.Tensor, stream=None) -> None:
+    """Stage A only: streaming pass, normalisers and the acceptance decision
+    (device tensors, outputs preallocated as spec_verify_chain returns them)."""
+    _stage("spec_chain_scan", target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature, out,
+           workspace, stream)
+
+
+def spec_chain_sample(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
+                      out: Dict[str, torch.Tensor], workspace: torch.Tensor, stream=None) -> None:
+    """Stage B only: the residual / bonus draw (after spec_chain_scan)."""
+    _stage("spec_chain_sample", target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature, out,
+           workspace, stream)
+
+
+def spec_verify_chain_greedy(target_logits, draft_tokens, out: Optional[Dict[str, torch.Tensor]] = None,
+                             workspace: Optional[torch.Tensor] = None, device="cuda",
+                             stream=None) -> Dict[str, torch.Tensor]:
+    """Greedy chain verification: accept_len, out_tokens, argmax_ids, row_status."""
+    lib = _lib.load()
+    dev = target_logits.device if target_logits.device.type == "cuda" else torch.device(device)
+    Lp = _dev(target_logits, dev)
+    x = _dev(draft_tokens, dev, torch.int32)
+    B, K1, V = Lp.shape
+    K = K1 - 1
+    dt = _dtype_code(Lp)
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                   argmax_ids=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(B, K, V, dt), dev)
+    rc = lib.spec_verify_chain_greedy(Lp.data_ptr(), dt, x.data_ptr(), B, K, V, out["accept_len"].data_ptr(),
+                                      out["out_tokens"].data_ptr(), _ptr(out.get("argmax_ids")),
+                                      out["row_status"].data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                      _stream(stream))
+    check("spec_verify_chain_greedy", rc)
+    return out
+
+
+def spec_verify_tree_greedy(node_logits, node_tokens, retrieve_indices, n1: int, tree_mask=None,
+                            out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                            device="cuda", stream=None) -> Dict[str, torch.Tensor]:
+    """Merged-tree greedy verification: accept_len, best_row, path_nodes,
+    out_tokens, subtree, row_status."""
+    lib = _lib.load()
+    dev = node_logits.device if node_logits.device.type == "cuda" else torch.device(device)
+    Lt = _dev(node_logits, dev)
+    tok = _dev(node_tokens, dev, torch.int32)
+    R = _dev(retrieve_indices, dev, torch.int32)
+    mask = None if tree_mask is None else _dev(tree_mask, dev, torch.uint8)
+    B, N, V = Lt.shape
+    Rn, D = R.shape[1], R.shape[2]
+    dt = _dtype_code(Lt)
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   best_row=torch.empty(B, dtype=torch.int32, device=dev),
+                   path_nodes=torch.empty(B, D, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty(B, D, dtype=torch.int32, device=dev),
+                   subtree=torch.empty(B, dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(B, N - 1, V, dt), dev)
+    rc = lib.spec_verify_tree_greedy(Lt.data_ptr(), dt, tok.data_ptr(), R.data_ptr(), _ptr(mask), B, N, Rn, D, V,
+                                     int(n1), out["accept_len"].data_ptr(), out["best_row"].data_ptr(),
+                                     out["path_nodes"].data_ptr(), out["out_tokens"].data_ptr(),
+                                     out["subtree"].data_ptr(), out["row_status"].data_ptr(), workspace.data_ptr(),
+                                     workspace.numel(), _stream(stream))
+    check("spec_verify_tree_greedy", rc)
+    return out
+
+
+def spec_tree_confidence(node_conf, n1: int, out: Optional[Dict[str, torch.Tensor]] = None, device="cuda",
+                         stream=None) -> Dict[str, torch.Tensor]:
+    """Confidence routing: scores [B, 2] and choice [B] (1 or 2)."""
+    lib = _lib.load()
+    dev = node_conf.device if node_conf.device.type == "cuda" else torch.device(device)
+    c = _dev(node_conf, dev, torch.float32)
+    B, N = c.shape
+    if out is None:
+        out = dict(scores=torch.empty(B, 2, device=dev), choice=torch.empty(B, dtype=torch.int32, device=dev))
+    rc = lib.spec_tree_confidence(c.data_ptr(), B, N, int(n1), out["scores"].data_ptr(), out["choice"].data_ptr(),
+                                  _stream(stream))
+    check("spec_tree_confidence", rc)
+    return out

@@ -1,0 +1,338 @@
+// abi.cu -- the extern "C" entry points: host-side validation, workspace
+// layout and kernel sequencing. Argument meanings are documented in
+// include/specverify.h.
+#include <math.h>
+
+#include <algorithm>
+
+#include "internal.h"
+
+using namespace specv;
+
+namespace {
+
+constexpr int kMaxB = 65535;
+constexpr int kMaxV = 1 << 24;
+constexpr int kMaxN = 1024;
+constexpr int kMaxD = 64;
+constexpr int kMaxR = 4096;
+
+size_t elem_size(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
+
+bool dtype_ok(int dtype) { return dtype == SPEC_F32 || dtype == SPEC_BF16; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 16-byte vector path: every row starts on a 16-byte boundary.
+bool use_vec(int V, int dtype, const void* a, const void* b) {
+  return (static_cast<size_t>(V) * elem_size(dtype)) % 16 == 0 && aligned16(a) && (b == nullptr || aligned16(b));
+}
+
+int check_workspace(void* ws, size_t have, size_t need) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || have < need) return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
+
+size_t up256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// Workspace regions (each 256-byte aligned). Region sizes are upper bounds
+// over the vector and scalar load paths, so the layout depends only on the
+// sizes, never on pointer alignment.
+struct Layout {
+  size_t part, dec, slices, units, tickets, total;
+};
+
+Layout layout(int B, int TR, int DR, int V, int dtype) {
+  const long long nrows = static_cast<long long>(B) * (TR + DR);
+  const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
+  const long long NS = std::max(tail_slices(V, true, dtype), tail_slices(V, false, dtype));
+  Layout L{};
+  size_t off = 0;
+  L.part = off;
+  off += up256(static_cast<size_t>(nrows * P) * sizeof(float2));
+  L.dec = off;
+  off += up256(static_cast<size_t>(B) * sizeof(DecRec));
+  L.slices = off;
+  off += up256(static_cast<size_t>(B * NS) * kNRS * (kResThreads / 32) * sizeof(float2));
+  L.units = off;
+  off += up256(static_cast<size_t>(B * NS) * kNRS * sizeof(float2));
+  L.tickets = off;
+  off += up256(static_cast<size_t>(B) * sizeof(int));
+  L.total = off;
+  return L;
+}
+
+char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
+
+// A positive constant c as a float pair hi + lo with lo > 0, so that
+// (-inf) * lo never meets an opposite-signed infinity in fma(d, hi, d * lo).
+void split_pos(double c, float* hi, float* lo) {
+  float h = static_cast<float>(c);
+  if (static_cast<double>(h) > c) h = nextafterf(h, 0.f);
+  double l = c - static_cast<double>(h);
+  *hi = h;
+  *lo = static_cast<float>(l) > 0.f ? static_cast<float>(l) : 1.17549435e-38f;
+}
+
+// log2(e) / T as such a pair.
+void split_c(float T, float* hi, float* lo) { split_pos(1.4426950408889634074 / static_cast<double>(T), hi, lo); }
+
+int chain_args_ok(const void* Lp, const void* Lq, int dtype, int B, int K, int V, float T, bool need_draft) {
+  if (!Lp || (need_draft && K > 0 && !Lq)) return SPEC_ERR_ARG;
+  if (!dtype_ok(dtype)) return SPEC_ERR_ARG;
+  if (B < 1 || K < 0 || V < 2) return SPEC_ERR_ARG;
+  if (B > kMaxB || K > kMaxK || V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+  if (!(T >= 0.f) || !isfinite(T)) return SPEC_ERR_ARG;
+  return SPEC_OK;
+}
+
+// Work items (row chunks) must number below 2^31 on either path.
+int scan_grid_ok(long long rows, int V, int dtype, bool vec) {
+  long long items = rows * scan_chunks(V, vec, dtype);
+  return items < 0x7fffffffLL - kScanWarps ? SPEC_OK : SPEC_ERR_UNSUPPORTED;
+}
+
+int greedy_impl(const void* Lp, int dtype, const int32_t* x, int B, int K, int V, int32_t* accept_len,
+                int32_t* out_tokens, int32_t* argmax_ids, int32_t* row_status, void* ws, size_t ws_bytes,
+                cudaStream_t st, float* nan_out[4], const int nan_len[4]) {
+  int e = chain_args_ok(Lp, nullptr, dtype, B, K, V, 0.f, false);
+  if (e) return e;
+  if ((K > 0 && !x) || !accept_len || !out_tokens || !row_status) return SPEC_ERR_ARG;
+  const Layout L = layout(B, K + 1, 0, V, dtype);
+  if ((e = check_workspace(ws, ws_bytes, L.total))) return e;
+  const bool vec = use_vec(V, dtype, Lp, nullptr);
+  if ((e = scan_grid_ok(static_cast<long long>(B) * (K + 1), V, dtype, vec))) return e;
+  ScanArgs a{};
+  a.A = Lp;
+  a.B = B;
+  a.TR = K + 1;
+  a.DR = 0;
+  a.V = V;
+  a.P = scan_chunks(V, vec, dtype);
+  a.part = reinterpret_cast<float2*>(at(ws, L.part));
+  if (launch_rowscan(a, dtype, vec, kModeArgmax, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  DecideArgs d{};
+  d.A = Lp;
+  d.part = a.part;
+  d.B = B;
+  d.K = K;
+  d.V = V;
+  d.P = a.P;
+  d.x = x;
+  d.accept_len = accept_len;
+  d.out_tokens = out_tokens;
+  d.argmax_ids = argmax_ids;
+  d.row_status = row_status;
+  for (int i = 0; i < 4; ++i) {
+    d.nan_out[i] = nan_out ? nan_out[i] : nullptr;
+    d.nan_len[i] = nan_len ? nan_len[i] : 0;
+  }
+  return cuda_status(launch_greedy_decide(d, st));
+}
+
+struct ChainCall {
+  const void *Lp, *Lq;
+  int dtype;
+  const int32_t* x;
+  const float *ua, *ur;
+  float T;
+  int B, K, V;
+  int32_t *accept_len, *out_tokens;
+  float *lse_p, *lse_q, *px, *qx;
+  int32_t* row_status;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t st;
+};
+
+int chain_validate(const ChainCall& c, Layout* L, bool* vec) {
+  int e = chain_args_ok(c.Lp, c.Lq, c.dtype, c.B, c.K, c.V, c.T, true);
+  if (e) return e;
+  if (!(c.T > 0.f)) return SPEC_ERR_ARG;
+  if ((c.K > 0 && (!c.x || !c.ua)) || !c.ur || !c.accept_len || !c.out_tokens || !c.row_status) return SPEC_ERR_ARG;
+  *L = layout(c.B, c.K + 1, c.K, c.V, c.dtype);
+  if ((e = check_workspace(c.ws, c.ws_bytes, L->total))) return e;
+  *vec = use_vec(c.V, c.dtype, c.Lp, c.Lq);
+  return scan_grid_ok(static_cast<long long>(c.B) * (2 * c.K + 1), c.V, c.dtype, *vec);
+}
+
+int chain_scan(const ChainCall& c) {
+  Layout L;
+  bool vec;
+  int e = chain_validate(c, &L, &vec);
+  if (e) return e;
+  ScanArgs a{};
+  a.A = c.Lp;
+  a.Bd = c.Lq;
+  a.B = c.B;
+  a.TR = c.K + 1;
+  a.DR = c.K;
+  a.V = c.V;
+  a.P = scan_chunks(c.V, vec, c.dtype);
+  split_c(c.T, &a.c_hi, &a.c_lo);
+  a.part = reinterpret_cast<float2*>(at(c.ws, L.part));
+  a.zero = reinterpret_cast<int*>(at(c.ws, L.tickets));
+  a.nzero = c.B;
+  return cuda_status(launch_rowscan(a, c.dtype, vec, kModeStats, c.st));
+}
+
+int chain_sample(const ChainCall& c) {
+  Layout L;
+  bool vec;
+  int e = chain_validate(c, &L, &vec);
+  if (e) return e;
+  TailArgs t{};
+  t.Lp = c.Lp;
+  t.Lq = c.Lq;
+  t.part = reinterpret_cast<const float2*>(at(c.ws, L.part));
+  t.x = c.x;
+  t.ua = c.ua;
+  t.ur = c.ur;
+  t.B = c.B;
+  t.K = c.K;
+  t.V = c.V;
+  t.P = scan_chunks(c.V, vec, c.dtype);
+  t.NS = tail_slices(c.V, vec, c.dtype);
+  split_c(c.T, &t.c_hi, &t.c_lo);
+  t.invT = 1.0 / static_cast<double>(c.T);
+  split_pos(t.invT, &t.it_hi, &t.it_lo);
+  t.accept_len = c.accept_len;
+  t.out_tokens = c.out_tokens;
+  t.row_status = c.row_status;
+  t.lse_p = c.lse_p;
+  t.lse_q = c.lse_q;
+  t.px = c.px;
+  t.qx = c.qx;
+  t.warp_sum = reinterpret_cast<float2*>(at(c.ws, L.slices));
+  t.unit_sum = reinterpret_cast<float2*>(at(c.ws, L.units));
+  t.res_ticket = reinterpret_cast<int*>(at(c.ws, L.tickets));
+  return cuda_status(launch_chain_tail(t, c.dtype, vec, c.st));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_bytes(int B, int K, int V, int dtype) {
+  if (B < 1 || K < 0 || V < 2 || !dtype_ok(dtype) || B > kMaxB || K > kMaxK || V > kMaxV) return 0;
+  return layout(B, K + 1, K, V, dtype).total;
+}
+
+#define CHAIN_CALL                                                                                              \
+  ChainCall c{target_logits, draft_logits, dtype, draft_tokens, u_accept, u_resample, temperature, B, K, V,     \
+              accept_len, out_tokens, lse_target, lse_draft, p_at_x, q_at_x, row_status, workspace,             \
+              workspace_bytes, static_cast<cudaStream_t>(stream)}
+
+int spec_chain_scan(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                    const float* u_accept, const float* u_resample, float temperature, int B, int K, int V,
+                    int32_t* accept_len, int32_t* out_tokens, float* lse_target, float* lse_draft, float* p_at_x,
+                    float* q_at_x, int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream) {
+  CHAIN_CALL;
+  return chain_scan(c);
+}
+
+int spec_chain_sample(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                      const float* u_accept, const float* u_resample, float temperature, int B, int K, int V,
+                      int32_t* accept_len, int32_t* out_tokens, float* lse_target, float* lse_draft, float* p_at_x,
+                      float* q_at_x, int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream) {
+  CHAIN_CALL;
+  return chain_sample(c);
+}
+
+int spec_verify_chain(const void* target_logits, const void* draft_logits, int dtype, const int32_t* draft_tokens,
+                      const float* u_accept, const float* u_resample, float temperature, int B, int K, int V,
+                      int32_t* accept_len, int32_t* out_tokens, float* lse_target, float* lse_draft, float* p_at_x,
+                      float* q_at_x, int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream) {
+  int e = chain_args_ok(target_logits, draft_logits, dtype, B, K, V, temperature, temperature != 0.f);
+  if (e) return e;
+  if (temperature == 0.f) {
+    float* outs[4] = {lse_target, lse_draft, p_at_x, q_at_x};
+    int lens[4] = {K + 1, K, K, K};
+    return greedy_impl(target_logits, dtype, draft_tokens, B, K, V, accept_len, out_tokens, nullptr, row_status,
+                       workspace, workspace_bytes, static_cast<cudaStream_t>(stream), outs, lens);
+  }
+  CHAIN_CALL;
+  if ((e = chain_scan(c))) return e;
+  return chain_sample(c);
+}
+
+int spec_verify_chain_greedy(const void* target_logits, int dtype, const int32_t* draft_tokens, int B, int K, int V,
+                             int32_t* accept_len, int32_t* out_tokens, int32_t* argmax_ids, int32_t* row_status,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  return greedy_impl(target_logits, dtype, draft_tokens, B, K, V, accept_len, out_tokens, argmax_ids, row_status,
+                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, nullptr);
+}
+
+int spec_verify_tree_greedy(const void* node_logits, int dtype, const int32_t* node_tokens,
+                            const int32_t* retrieve_indices, const uint8_t* tree_mask, int B, int N, int R, int D,
+                            int V, int n1, int32_t* accept_len, int32_t* best_row, int32_t* path_nodes,
+                            int32_t* out_tokens, int32_t* subtree, int32_t* row_status, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!node_logits || !node_tokens || !retrieve_indices || !accept_len || !best_row || !path_nodes || !out_tokens ||
+      !subtree || !row_status || !dtype_ok(dtype))
+    return SPEC_ERR_ARG;
+  if (B < 1 || N < 1 || R < 1 || D < 1 || V < 2 || n1 < 0 || n1 > N - 1) return SPEC_ERR_ARG;
+  if (B > kMaxB || N > kMaxN || D > kMaxD || R > kMaxR || V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+  int e;
+  const Layout L = layout(B, N, 0, V, dtype);
+  if ((e = check_workspace(workspace, workspace_bytes, L.total))) return e;
+  const bool vec = use_vec(V, dtype, node_logits, nullptr);
+  if ((e = scan_grid_ok(static_cast<long long>(B) * N, V, dtype, vec))) return e;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ScanArgs a{};
+  a.A = node_logits;
+  a.B = B;
+  a.TR = N;
+  a.DR = 0;
+  a.V = V;
+  a.P = scan_chunks(V, vec, dtype);
+  a.part = reinterpret_cast<float2*>(at(workspace, L.part));
+  if (launch_rowscan(a, dtype, vec, kModeArgmax, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  TreeArgs t{};
+  t.tok = node_tokens;
+  t.R = retrieve_indices;
+  t.mask = tree_mask;
+  t.part = a.part;
+  t.B = B;
+  t.N = N;
+  t.Rn = R;
+  t.D = D;
+  t.V = V;
+  t.P = a.P;
+  t.n1 = n1;
+  t.accept_len = accept_len;
+  t.best_row = best_row;
+  t.path = path_nodes;
+  t.out_tokens = out_tokens;
+  t.subtree = subtree;
+  t.row_status = row_status;
+  return cuda_status(launch_tree_finish(t, st));
+}
+
+int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* scores, int32_t* choice, void* stream) {
+  if (!node_conf || !scores || !choice) return SPEC_ERR_ARG;
+  if (B < 1 || N < 1 || n1 < 0 || n1 > N - 1) return SPEC_ERR_ARG;
+  if (B > kMaxB || N > kMaxN) return SPEC_ERR_UNSUPPORTED;
+  return cuda_status(launch_tree_confidence(node_conf, B, N, n1, scores, choice, static_cast<cudaStream_t>(stream)));
+}
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK:
+      return "ok";
+    case SPEC_ERR_ARG:
+      return "invalid argument";
+    case SPEC_ERR_WORKSPACE:
+      return "workspace missing, misaligned or too small";
+    case SPEC_ERR_CUDA:
+      return "CUDA launch failed";
+    case SPEC_ERR_UNSUPPORTED:
+      return "sizes beyond the library's limits";
+    default:
+      return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,148 @@
+// fold.cuh -- folding a row's rowscan partials (one warp per row) and the
+// launch helper for kernels chained with programmatic dependent launch.
+#pragma once
+
+#include "internal.h"
+
+namespace specv {
+
+// Row max and sum of exp over P (max m_c, sum z_c) partials, folded by one
+// warp; every lane returns it. The row max comes first, then each partial is
+// rescaled once by 2^((m_c - M) * log2(e) / T) and summed as a float pair.
+__device__ __forceinline__ RowRec fold_stats(const float2* pr, int P, float c_hi, float c_lo, int lane) {
+  // up to 32 partials: one load per lane, kept in registers
+  const float2 q0 = lane < P ? __ldcg(pr + lane) : make_float2(-INFINITY, 0.f);
+  float m = q0.x;
+  for (int c = lane + 32; c < P; c += 32) m = fmax_nan(m, __ldcg(pr + c).x);
+  const float M = warp_max_nan(m);
+  RowRec r;
+  r.M = M;
+  r.idx = 0;
+  r.Zhi = 0.f;
+  r.Zlo = 0.f;
+  if (M != M) {
+    r.Zhi = NAN;
+    return r;
+  }
+  if (M == -INFINITY) return r;  // every entry -inf
+  float2 z = make_float2(0.f, 0.f);
+  for (int c = lane; c < P; c += 32) {
+    const float2 q = c < 32 ? q0 : __ldcg(pr + c);
+    if (q.x != -INFINITY) {
+      const float d = q.x - M;
+      z = ds_add(z, ds_from_prod(q.y, exp2f(fmaf(d, c_hi, d * c_lo))));
+    }
+  }
+#pragma unroll 1
+  for (int o = 16; o > 0; o >>= 1)
+    z = ds_add(z, make_float2(__shfl_xor_sync(0xffffffffu, z.x, o), __shfl_xor_sync(0xffffffffu, z.y, o)));
+  r.Zhi = z.x;
+  r.Zlo = z.y;
+  return r;
+}
+
+// Fold rows j = first, first + stride, ... (< nrows) of the stats partials at
+// `part` (row j at part + j * P) into rr[j], one warp. When every row of the
+// warp fits (at most 4 rows, P <= 64), all loads are issued before any
+// reduction, so the rows cost one memory round trip together.
+__device__ __forceinline__ void fold_stats_rows(const float2* part, int P, int first, int stride, int nrows,
+                                                float c_hi, float c_lo, int lane, RowRec* rr) {
+  constexpr int kR = 4;
+  if (P > 64 || first + kR * stride < nrows) {
+    for (int j = first; j < nrows; j += stride) {
+      const RowRec r = fold_stats(part + static_cast<long long>(j) * P, P, c_hi, c_lo, lane);
+      if (lane == 0) rr[j] = r;
+    }
+    return;
+  }
+  float2 q[kR][2];
+#pragma unroll
+  for (int i = 0; i < kR; ++i) {
+    const int j = first + i * stride;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int idx = lane + 32 * c;
+      q[i][c] = (j < nrows && idx < P) ? __ldcg(part + static_cast<long long>(j) * P + idx) : make_float2(-INFINITY, 0.f);
+    }
+  }
+  float M[kR];
+#pragma unroll
+  for (int i = 0; i < kR; ++i) M[i] = fmax_nan(q[i][0].x, q[i][1].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < kR; ++i) M[i] = fmax_nan(M[i], __shfl_xor_sync(0xffffffffu, M[i], o));
+  float2 z[kR];
+#pragma unroll
+  for (int i = 0; i < kR; ++i) {
+    z[i] = make_float2(0.f, 0.f);
+    if (M[i] == M[i] && M[i] != -INFINITY) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        if (q[i][c].x != -INFINITY) {
+          const float d = q[i][c].x - M[i];
+          z[i] = ds_add(z[i], ds_from_prod(q[i][c].y, exp2f(fmaf(d, c_hi, d * c_lo))));
+        }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < kR; ++i)
+      z[i] = ds_add(z[i], make_float2(__shfl_xor_sync(0xffffffffu, z[i].x, o), __shfl_xor_sync(0xffffffffu, z[i].y, o)));
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kR; ++i) {
+      const int j = first + i * stride;
+      if (j >= nrows) continue;
+      RowRec r;
+      r.M = M[i];
+      r.idx = 0;
+      r.Zhi = M[i] != M[i] ? NAN : z[i].x;
+      r.Zlo = M[i] != M[i] ? 0.f : z[i].y;
+      rr[j] = r;
+    }
+  }
+}
+
+// Row argmax over P (value, index) partials; every lane returns it.
+__device__ __forceinline__ RowRec fold_argmax(const float2* pr, int P, int lane) {
+  float v = -INFINITY;
+  int i = INT_MAX;
+  for (int c = lane; c < P; c += 32) {
+    const float2 q = __ldcg(pr + c);
+    merge_arg(v, i, q.x, __float_as_int(q.y));
+  }
+#pragma unroll 1
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    merge_arg(v, i, v2, i2);
+  }
+  RowRec r;
+  r.M = v;
+  r.idx = i;
+  r.Zhi = r.Zlo = 0.f;
+  return r;
+}
+
+// Launch `kernel` so that it may start while the preceding kernel in the
+// stream drains; the kernel calls griddep_wait() before reading its outputs.
+template <typename Args>
+inline cudaError_t launch_pdl(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t st, const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace specv

@@ -1,0 +1,131 @@
+// internal.h -- launchers and records shared between the kernel files and
+// the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace specv {
+
+constexpr int kModeStats = 0;   // rowscan: (max, sum of exp) per row
+constexpr int kModeArgmax = 1;  // rowscan: (value, index) of the row maximum
+constexpr int kMaxK = 255;
+
+// rowscan geometry: each warp reduces one chunk of kWV 16-byte vectors per
+// lane (vector path) or kScalarPerLane elements per lane (scalar path)
+constexpr int kWV = 8;
+constexpr int kScalarPerLane = 64;
+constexpr int kScanWarps = 8;
+constexpr int kScanThreads = kScanWarps * 32;
+
+// tail geometry: each CTA weighs kNRS rounds of 256 vectors of one row
+constexpr int kResThreads = 256;
+constexpr int kNRS = 8;
+
+// greedy decision kernel: one CTA of kDecideThreads per batch row
+constexpr int kDecideThreads = 512;
+
+// Per-row fold of the rowscan partials.
+struct RowRec {
+  float M;         // stats: max raw logit; argmax: max value (NaN: row holds NaN)
+  int idx;         // argmax: lowest index of the maximum (INT_MAX: none)
+  float Zhi, Zlo;  // stats: sum_v exp((l_v - M) / T) as a float pair
+};
+
+// Per-row-b decision: which row the draw uses and its constants.
+struct DecRec {
+  int status;  // row_status bits (0: row usable)
+  int m;       // first rejected position (K when all accepted)
+  int mode;    // 0: residual max(0, p_m - q_m); 1: draw from p_m
+  int pad;
+  float Mp, Mq;      // raw-logit maxima of target row m and draft row m
+  float dM;          // Mp - Mq
+  float D_hi, D_lo;  // log2(Zp / Zq) as a float pair
+  float pad2[3];
+};
+
+struct ScanArgs {
+  const void* A;   // target rows: [B][TR][V]
+  const void* Bd;  // draft rows:  [B][DR][V] (may be NULL when DR == 0)
+  int B, TR, DR, V;
+  int P;             // chunks (partials) per row
+  float c_hi, c_lo;  // log2(e) / T as a float pair, c_lo > 0
+  float2* part;      // [B * (TR + DR)][P]
+  int* zero;         // counters the next kernel uses, zeroed here (may be NULL)
+  int nzero;
+};
+
+// Warp chunks per row, and partials per row (one per CTA of kScanWarps
+// warps), for a vocabulary of V entries.
+__host__ __device__ inline int warp_chunks(int V, bool vec, int dtype) {
+  const long long per = vec ? static_cast<long long>(kWV) * 32 * (dtype == SPEC_BF16 ? 8 : 4)
+                            : static_cast<long long>(kScalarPerLane) * 32;
+  return static_cast<int>((V + per - 1) / per);
+}
+int scan_chunks(int V, bool vec, int dtype);
+cudaError_t launch_rowscan(const ScanArgs& a, int dtype, bool vec, int mode, cudaStream_t st);
+
+// Decision stage of greedy chain verification.
+struct DecideArgs {
+  const void* A;  // target logits [B][K+1][V]
+  const float2* part;
+  int B, K, V, P;
+  const int32_t* x;
+  int32_t* accept_len;
+  int32_t* out_tokens;
+  int32_t* row_status;
+  int32_t* argmax_ids;
+  float* nan_out[4];  // float outputs of a chain call forwarded at T = 0
+  int nan_len[4];
+};
+cudaError_t launch_greedy_decide(const DecideArgs& a, cudaStream_t st);
+
+// Decision and residual / bonus draw of chain verification (one kernel).
+struct TailArgs {
+  const void* Lp;  // target logits [B][K+1][V]
+  const void* Lq;  // draft logits  [B][K][V]
+  const float2* part;
+  const int32_t* x;
+  const float* ua;
+  const float* ur;
+  int B, K, V, P, NS;
+  float c_hi, c_lo;    // log2(e) / T, c_lo > 0
+  float it_hi, it_lo;  // 1 / T, it_lo > 0
+  double invT;
+  int32_t* accept_len;
+  int32_t* out_tokens;
+  int32_t* row_status;
+  float* lse_p;
+  float* lse_q;
+  float* px;
+  float* qx;
+  float2* warp_sum;  // [B][NS][kNRS][kResThreads / 32]
+  float2* unit_sum;  // [B][NS][kNRS]
+  int* res_ticket;   // [B], zero on entry (zeroed by the rowscan pass)
+};
+
+// Slices (CTAs per batch row) of the tail kernel.
+int tail_slices(int V, bool vec, int dtype);
+cudaError_t launch_chain_tail(const TailArgs& a, int dtype, bool vec, cudaStream_t st);
+
+struct TreeArgs {
+  const int32_t* tok;
+  const int32_t* R;
+  const uint8_t* mask;
+  const float2* part;
+  int B, N, Rn, D, V, P, n1;
+  int32_t* accept_len;
+  int32_t* best_row;
+  int32_t* path;
+  int32_t* out_tokens;
+  int32_t* subtree;
+  int32_t* row_status;
+};
+cudaError_t launch_tree_finish(const TreeArgs& a, cudaStream_t st);
+
+cudaError_t launch_tree_confidence(const float* conf, int B, int N, int n1, float* scores, int32_t* choice,
+                                   cudaStream_t st);
+
+}  // namespace specv

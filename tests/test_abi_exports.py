@@ -1,0 +1,82 @@
+"""The C ABI library builds, loads without a GPU and exports every function
+that include/specverify.h declares; argument validation runs on the host
+(CPU only: no kernel is launched)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_29_gb300 import _lib, build
+
+    build.build()
+    return _lib.load()
+
+
+def declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for n in ("spec_verify_chain", "spec_verify_chain_greedy", "spec_verify_tree_greedy", "spec_tree_confidence",
+              "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from speculative_decoding_verification_29_gb300 import _lib
+
+    for name in declared():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_workspace_sizes(lib):
+    assert lib.spec_workspace_bytes(64, 8, 128256, 1) % 256 == 0
+    assert lib.spec_workspace_bytes(64, 8, 128256, 1) >= 64 * 17 * 63 * 8
+    assert lib.spec_workspace_bytes(0, 8, 128256, 1) == 0
+    assert lib.spec_workspace_bytes(1, 300, 100, 1) == 0
+    assert lib.spec_workspace_bytes(1, 1, 1, 1) == 0
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    """Every failure here is caught on the host before any launch."""
+    from speculative_decoding_verification_29_gb300._lib import SPEC_ERR_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_WORKSPACE
+
+    fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    n = None
+    # NULL logits
+    assert lib.spec_verify_chain(n, fake, 1, fake, fake, fake, 1.0, 1, 1, 16, fake, fake, n, n, n, n, fake, fake,
+                                 1 << 20, n) == SPEC_ERR_ARG
+    # negative / NaN temperature
+    for T in (-1.0, float("nan"), float("inf")):
+        assert lib.spec_verify_chain(fake, fake, 1, fake, fake, fake, T, 1, 1, 16, fake, fake, n, n, n, n, fake,
+                                     fake, 1 << 20, n) == SPEC_ERR_ARG
+    # bad dtype, sizes
+    assert lib.spec_verify_chain(fake, fake, 7, fake, fake, fake, 1.0, 1, 1, 16, fake, fake, n, n, n, n, fake, fake,
+                                 1 << 20, n) == SPEC_ERR_ARG
+    assert lib.spec_verify_chain(fake, fake, 1, fake, fake, fake, 1.0, 1, 300, 16, fake, fake, n, n, n, n, fake,
+                                 fake, 1 << 20, n) == SPEC_ERR_UNSUPPORTED
+    # workspace too small / misaligned
+    assert lib.spec_verify_chain(fake, fake, 1, fake, fake, fake, 1.0, 1, 1, 16, fake, fake, n, n, n, n, fake, fake,
+                                 8, n) == SPEC_ERR_WORKSPACE
+    assert lib.spec_verify_chain(fake, fake, 1, fake, fake, fake, 1.0, 1, 1, 16, fake, fake, n, n, n, n, fake,
+                                 ctypes.c_void_p(4096 + 8), 1 << 20, n) == SPEC_ERR_WORKSPACE
+    assert lib.spec_verify_chain_greedy(fake, 1, n, 1, 2, 16, fake, fake, n, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    # trees: n1 out of range, N beyond the limit
+    assert lib.spec_verify_tree_greedy(fake, 1, fake, fake, n, 1, 5, 2, 3, 16, 5, fake, fake, fake, fake, fake, fake,
+                                       fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert lib.spec_verify_tree_greedy(fake, 1, fake, fake, n, 1, 5000, 2, 3, 16, 5, fake, fake, fake, fake, fake,
+                                       fake, fake, 1 << 30, n) == SPEC_ERR_UNSUPPORTED
+    assert lib.spec_tree_confidence(fake, 1, 5, 9, fake, fake, n) == SPEC_ERR_ARG
+    assert lib.spec_status_string(-2) == b"workspace missing, misaligned or too small"

@@ -1,0 +1,182 @@
+"""GPU chain verification (sampling) against the fp64 oracle, through the C ABI."""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import oracle_pins as P
+from gpu_helpers import compare_chain, gpu_chain, need_gpu, oracle_chain
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_chain_tiny(seed):
+    c = gen.chain_tiny(seed)
+    compare_chain(gpu_chain(c), oracle_chain(c))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V", [2, 3, 7, 1000, 1001, 4095, 8192, 8193, 33000])
+def test_chain_ragged_vocab(V, dtype):
+    """Vocabulary sizes off and on the chunk grid, on the vector and scalar
+    load paths (V * element size not a multiple of 16)."""
+    c = gen.chain_tiny(V % 97, B=6, K=3, V=V, T=0.9, dtype=dtype)
+    compare_chain(gpu_chain(c), oracle_chain(c))
+
+
+@pytest.mark.parametrize("T", [0.25, 0.7, 1.0, 1.9, 7.5])
+def test_chain_temperatures(T):
+    c = gen.chain_zipf(8, 4, 5000, torch.bfloat16, T, 1.0, seed=int(T * 10))
+    compare_chain(gpu_chain(c), oracle_chain(c))
+
+
+def test_chain_k0_bonus_only():
+    c = gen.chain_tiny(3, B=5, K=0, V=777)
+    g = gpu_chain(c)
+    o = oracle_chain(c)
+    compare_chain(g, o)
+    assert np.all(g["accept_len"] == 0)
+
+
+def test_ab_uniform_grid():
+    """Two-token worked example (ariser.io page): on a grid of accept
+    uniforms, A is kept exactly 3/4 of the time, B always; every rejection of
+    A draws B."""
+    n = 1000
+    g = gen.chain_ab(0)
+    Lp = g.Lp.float().repeat(n, 1, 1)
+    Lq = g.Lq.float().repeat(n, 1, 1)
+    ua = ((torch.arange(n, dtype=torch.float64) + 0.5) / n).float().view(n, 1)
+    ur = torch.rand(n, generator=torch.Generator().manual_seed(1))
+    for xt, want in ((0, 750), (1, n)):
+        x = torch.full((n, 1), xt, dtype=torch.int32)
+        c = gen.ChainBatch("ab", Lp, Lq, x, ua, ur, 1.0)
+        out = gpu_chain(c)
+        assert int((out["accept_len"] == 1).sum()) == want
+        rej = out["accept_len"] == 0
+        assert np.all(out["out_tokens"][rej, 0] == 1)
+        compare_chain(out, oracle_chain(c))
+
+
+def test_exhaustive_world_ids_match_oracle():
+    """Every draft sequence of a V=4, K=3 prefix-conditioned world, each with a
+    stratified grid of uniforms, verified in one batch: ids equal the oracle's."""
+    V, K, T = 4, 3, 1.0
+    lp, lq = P.random_world(V, K, seed=11, zero_some=True)
+    xs = list(itertools.product(range(V), repeat=K))
+    G = 8
+    rows = []
+    for x in xs:
+        Lp = np.stack([lp[x[:k]] for k in range(K + 1)])
+        Lq = np.stack([lq[x[:k]] for k in range(K)])
+        for i, j in itertools.product(range(G), range(G)):
+            rows.append((Lp, Lq, x, (i + 0.5) / G, (j + 0.37) / G))
+    B = len(rows)
+    Lp = torch.tensor(np.stack([r[0] for r in rows]), dtype=torch.float32)
+    Lq = torch.tensor(np.stack([r[1] for r in rows]), dtype=torch.float32)
+    x = torch.tensor([r[2] for r in rows], dtype=torch.int32)
+    ua = torch.tensor([[r[3]] * K for r in rows], dtype=torch.float32)
+    ur = torch.tensor([r[4] for r in rows], dtype=torch.float32)
+    c = gen.ChainBatch("world", Lp, Lq, x, ua, ur, T)
+    compare_chain(gpu_chain(c), oracle_chain(c), name="world_V4K3")
+
+
+def test_status_rows():
+    c = gen.chain_tiny(4, B=8, K=3, V=1024)
+    Lp, Lq, x = c.Lp.clone(), c.Lq.clone(), c.x.clone()
+    Lp[1, 2, 17] = float("nan")
+    Lq[2, 0, :] = float("-inf")
+    x[3, 1] = 1024
+    Lp[4, 0, 3] = float("inf")
+    Lp[5, 3, :] = float("-inf")
+    Lq[6, 1, :500] = float("-inf")  # partly masked draft row: valid
+    x[6, 1] = 600
+    Lp[7, 0, 5] = float("-inf")  # the draft token is impossible under the target
+    x[7, 0] = 5
+    c2 = gen.ChainBatch("status", Lp, Lq, x, c.ua, c.ur, 1.0)
+    g = gpu_chain(c2)
+    o = oracle_chain(c2)
+    compare_chain(g, o)
+    assert list(g["row_status"]) == [0, 2, 4, 1, 2, 2, 0, 0]
+    assert g["accept_len"][7] == 0 and g["out_tokens"][7, 0] != 5
+
+
+def test_draft_token_with_zero_draft_mass_is_accepted():
+    c = gen.chain_tiny(5, B=4, K=2, V=64)
+    Lq = c.Lq.clone()
+    x = c.x.clone()
+    Lq[:, 0, 9] = float("-inf")
+    x[:, 0] = 9
+    c2 = gen.ChainBatch("q0", c.Lp, Lq, x, c.ua, c.ur, 1.0)
+    g = gpu_chain(c2)
+    compare_chain(g, oracle_chain(c2))
+    assert np.all(g["accept_len"] >= 1)
+
+
+def test_extreme_logits():
+    c = gen.chain_tiny(6, B=6, K=3, V=2048)
+    Lp = c.Lp * 800.0  # huge spread: near one-hot softmax
+    Lq = torch.zeros_like(c.Lq)  # uniform draft
+    Lp[0] = 0.0  # uniform target row
+    c2 = gen.ChainBatch("extreme", Lp, Lq, c.x, c.ua, c.ur, 1.0)
+    compare_chain(gpu_chain(c2), oracle_chain(c2))
+
+
+def test_identical_draft_and_target_always_accepts():
+    c = gen.chain_tiny(7, B=16, K=4, V=3000)
+    c2 = gen.ChainBatch("same", c.Lp, c.Lp[:, :4].clone(), c.x, c.ua, c.ur, 1.0)
+    g = gpu_chain(c2)
+    compare_chain(g, oracle_chain(c2))
+    assert np.all(g["accept_len"] == 4)
+
+
+def test_temperature_zero_forwards_to_greedy():
+    c = gen.chain_tiny(8, B=8, K=4, V=4000, T=0.0)
+    g = gpu_chain(c)
+    o = oracle.verify_chain_greedy(c.Lp, c.x)
+    assert np.array_equal(g["accept_len"], o["accept_len"]) and np.array_equal(g["out_tokens"], o["out_tokens"])
+    assert np.all(np.isnan(g["lse_target"])) and np.all(np.isnan(g["p_at_x"]))
+
+
+def test_repeat_calls_identical():
+    c = gen.chain_zipf(16, 4, 20000, torch.bfloat16, 0.8, 1.0, seed=3)
+    a = gpu_chain(c)
+    b = gpu_chain(c)
+    for k in a:
+        assert np.array_equal(a[k], b[k], equal_nan=True), k
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_chain_single_stream_llama_vocab(seed):
+    """B=1, K=5, V=128256 bf16 at T=1."""
+    c = gen.config_chain_single(seed, T=1.0)
+    compare_chain(gpu_chain(c), oracle_chain(c))
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_chain_batched_serving_full(seed):
+    """B=64, K=8, V=128256 bf16, T=0.7, per-row draft noise: every row."""
+    c = gen.config_chain_batched(seed)
+    g = gpu_chain(c)
+    compare_chain(g, oracle_chain(c), name=f"chain_batched_s{seed}")
+    assert len(set(g["accept_len"].tolist())) >= 4  # accept lengths spread over 0..K
+
+
+def test_chain_deep_qwen_vocab_sampled_rows():
+    """B=256, K=16, V=152064 fp32 at full size; the oracle checks 24 rows."""
+    c = gen.config_chain_deep(0)
+    g = gpu_chain(c)
+    rows = list(range(0, 256, 11))
+    compare_chain(g, oracle_chain(c, rows), rows=rows, name="chain_deep")
+    assert float(np.mean(g["accept_len"])) > 4  # a close drafter: long accepted runs
