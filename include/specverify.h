@@ -129,6 +129,29 @@ int spec_chain_sample(const void* target_logits, const void* draft_logits, int d
                       float* p_at_x, float* q_at_x, int32_t* row_status, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/* spec_verify_chain for callers that cannot allocate device memory (no
+ * counterpart in the pages: an interface choice of this library). Some
+ * callers have no way to hand over a scratch workspace: a plain-C host that
+ * owns no device allocator and only receives the input and output buffers,
+ * or a serving runtime that has reserved all device memory and forbids
+ * further allocation, or a decode loop that avoids cudaMalloc because it
+ * synchronises the device. Same arguments and results as spec_verify_chain,
+ * without workspace / workspace_bytes: the scratch is an 8 MiB array inside
+ * this library's device memory, present once on every GPU that loads the
+ * library until the process exits; sizes whose spec_workspace_bytes exceeds
+ * 8 MiB return SPEC_ERR_UNSUPPORTED (B=64, K=8, V=128256 needs about 3 MiB).
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Nothing is allocated by any call. Every call on a device shares the array
+ * and leaves its contents behind (each call writes all the scratch it reads),
+ * so calls whose work overlaps on the GPU race and must be ordered by the
+ * caller. */
+int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logits, int dtype,
+                              const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                              float temperature, int B, int K, int V, int32_t* accept_len, int32_t* out_tokens,
+                              float* lse_target, float* lse_draft, float* p_at_x, float* q_at_x,
+                              int32_t* row_status, void* stream);
+
 /* Greedy chain verification (temperature 0): reads target logits only.
  *   target_logits device [B][K+1][V]; draft_tokens device [B][K] int32
  * Outputs (device): accept_len [B]; out_tokens [B][K+1] (x_0..x_{m-1}, a_m,
