@@ -367,20 +367,22 @@ def _sample_rows(name, w, threads, budget_s):
 
 
 def cpu_baseline(name, w, cpu_seconds):
+    """The oracle timed on this host's cores over whole batches of the same
+    workload, repeated until about `cpu_seconds` of CPU time were spent."""
     threads = os.cpu_count() or 1
-    n, one = _sample_rows(name, w, threads, cpu_seconds / threads / 3)
-    rows = list(range(n))
+    rows = list(range(w.B))
     reps, t_tot = 0, 0.0
-    while reps < 3:
+    while reps < 1 or (t_tot * min(threads, w.B) < cpu_seconds and reps < 50):
         t0 = time.perf_counter()
         _oracle_step(name, w, rows, threads)
         t_tot += time.perf_counter() - t0
         reps += 1
     per_row_units = (w.N - 1) if name == "tree" else w.K
-    return {"value": n * per_row_units * reps / t_tot, "unit": "nodes/s" if name == "tree" else "positions/s",
-            "cores": min(threads, n), "kind": "oracle",
-            "sample": f"{n} of {w.B} rows of the same batch, {reps} repeats, fp64 C oracle on {min(threads, n)} "
-                      f"threads ({t_tot:.1f} s wall)"}
+    cores = min(threads, w.B)
+    return {"value": w.B * per_row_units * reps / t_tot, "unit": "nodes/s" if name == "tree" else "positions/s",
+            "cores": cores, "kind": "oracle",
+            "sample": f"all {w.B} rows of the batch, {reps} repeats, fp64 C oracle on {cores} threads "
+                      f"({t_tot:.1f} s wall, about {t_tot * cores:.0f} CPU-s)"}
 
 
 def run_reference(args):
