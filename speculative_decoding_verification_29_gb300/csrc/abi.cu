@@ -41,7 +41,7 @@ size_t up256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 // over the vector and scalar load paths, so the layout depends only on the
 // sizes, never on pointer alignment.
 struct Layout {
-  size_t part, dec, slices, units, tickets, total;
+  size_t part, slices, tickets, total;
 };
 
 Layout layout(int B, int TR, int DR, int V, int dtype) {
@@ -52,12 +52,8 @@ Layout layout(int B, int TR, int DR, int V, int dtype) {
   size_t off = 0;
   L.part = off;
   off += up256(static_cast<size_t>(nrows * P) * sizeof(float2));
-  L.dec = off;
-  off += up256(static_cast<size_t>(B) * sizeof(DecRec));
   L.slices = off;
   off += up256(static_cast<size_t>(B * NS) * kNRS * (kResThreads / 32) * sizeof(float2));
-  L.units = off;
-  off += up256(static_cast<size_t>(B * NS) * kNRS * sizeof(float2));
   L.tickets = off;
   off += up256(static_cast<size_t>(B) * sizeof(int));
   L.total = off;
@@ -206,7 +202,6 @@ int chain_sample(const ChainCall& c) {
   t.px = c.px;
   t.qx = c.qx;
   t.warp_sum = reinterpret_cast<float2*>(at(c.ws, L.slices));
-  t.unit_sum = reinterpret_cast<float2*>(at(c.ws, L.units));
   t.res_ticket = reinterpret_cast<int*>(at(c.ws, L.tickets));
   return cuda_status(launch_chain_tail(t, c.dtype, vec, c.st));
 }

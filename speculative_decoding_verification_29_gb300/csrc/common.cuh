@@ -136,6 +136,10 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 // writes are visible (returns at once when launched without PDL).
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// PDL: allow the next kernel in the stream to be scheduled now (its
+// griddepcontrol.wait still waits for this whole grid to complete).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 2^x, hardware approximation (relative error about 2^-22), -inf -> 0.
 __device__ __forceinline__ float ex2_fast(float x) {
   float y;

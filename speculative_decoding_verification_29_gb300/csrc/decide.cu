@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(kDecideThreads) greedy_decide_kernel(DecideArg
   __shared__ int am[kMaxK + 1];
   __shared__ int s_st;
   if (tid == 0) s_st = 0;
+  griddep_launch_dependents();
   __syncthreads();
   griddep_wait();
   for (int j = warp; j <= K; j += kW) {

@@ -126,23 +126,4 @@ __device__ __forceinline__ RowRec fold_argmax(const float2* pr, int P, int lane)
   return r;
 }
 
-// Launch `kernel` so that it may start while the preceding kernel in the
-// stream drains; the kernel calls griddep_wait() before reading its outputs.
-template <typename Args>
-inline cudaError_t launch_pdl(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t st, const Args& args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
 }  // namespace specv

@@ -13,9 +13,11 @@ constexpr int kModeStats = 0;   // rowscan: (max, sum of exp) per row
 constexpr int kModeArgmax = 1;  // rowscan: (value, index) of the row maximum
 constexpr int kMaxK = 255;
 
-// rowscan geometry: each warp reduces one chunk of kWV 16-byte vectors per
-// lane (vector path) or kScalarPerLane elements per lane (scalar path)
+// rowscan geometry: each warp reduces one segment of kSegChunks chunks of kWV
+// 16-byte vectors per lane (vector path) or of kScalarPerLane elements per
+// lane (scalar path)
 constexpr int kWV = 8;
+constexpr int kSegChunks = 1;
 constexpr int kScalarPerLane = 64;
 constexpr int kScanWarps = 8;
 constexpr int kScanThreads = kScanWarps * 32;
@@ -57,10 +59,10 @@ struct ScanArgs {
   int nzero;
 };
 
-// Warp chunks per row, and partials per row (one per CTA of kScanWarps
-// warps), for a vocabulary of V entries.
+// Warp segments per row, and so partials per row, for a vocabulary of V
+// entries.
 __host__ __device__ inline int warp_chunks(int V, bool vec, int dtype) {
-  const long long per = vec ? static_cast<long long>(kWV) * 32 * (dtype == SPEC_BF16 ? 8 : 4)
+  const long long per = vec ? static_cast<long long>(kSegChunks) * kWV * 32 * (dtype == SPEC_BF16 ? 8 : 4)
                             : static_cast<long long>(kScalarPerLane) * 32;
   return static_cast<int>((V + per - 1) / per);
 }
@@ -101,8 +103,7 @@ struct TailArgs {
   float* lse_q;
   float* px;
   float* qx;
-  float2* warp_sum;  // [B][NS][kNRS][kResThreads / 32]
-  float2* unit_sum;  // [B][NS][kNRS]
+  float2* warp_sum;  // [B][NS][kNRS][kResThreads / 32] unit totals
   int* res_ticket;   // [B], zero on entry (zeroed by the rowscan pass)
 };
 
@@ -127,5 +128,24 @@ cudaError_t launch_tree_finish(const TreeArgs& a, cudaStream_t st);
 
 cudaError_t launch_tree_confidence(const float* conf, int B, int N, int n1, float* scores, int32_t* choice,
                                    cudaStream_t st);
+
+// Launch `kernel` so that it may start while the preceding kernel in the
+// stream drains; the kernel calls griddep_wait() before reading its outputs.
+template <typename Args>
+inline cudaError_t launch_pdl(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t st, const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 }  // namespace specv

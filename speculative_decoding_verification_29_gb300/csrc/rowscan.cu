@@ -1,52 +1,59 @@
 // rowscan.cu -- the streaming pass over logit rows (the hot loop).
 //
-// Every row is cut into chunks of kWV x 32 sixteen-byte vectors; one warp
-// loads its chunk with kWV streaming loads per lane in flight, reduces it and
-// writes one 8-byte partial, with no block-level synchronisation, no fence and
-// no atomic, so the pass runs at the read bandwidth of HBM:
-//   stats  (sampling): (m, z) with m the chunk's max raw logit and
+// Each row is cut into warp segments of kSegChunks chunks of kWV x 32
+// sixteen-byte vectors. One warp streams its segment chunk by chunk, kWV
+// streaming loads per lane in flight, keeps per-lane running results and
+// writes one 8-byte partial at the end; there is no block-level
+// synchronisation, no fence and no atomic, so the pass runs at the read
+// bandwidth of HBM:
+//   stats  (sampling): (m, z) with m the segment's max raw logit and
 //          z = sum 2^((l - m) * log2(e) / T) = sum exp((l - m) / T), the two
 //          numbers a softmax over the row needs (lotook.com, step "parallel
 //          verification": the target gives its own distribution at every
 //          draft position in one pass);
-//   argmax (greedy and trees): the chunk's max value and the lowest index
+//   argmax (greedy and trees): the segment's max value and the lowest index
 //          holding it (lotook.com: at temperature 0 a draft token is kept when
 //          it is the target's top choice).
 // The max runs on packed bf16 pairs, the exponent arithmetic on packed fp32
-// pairs (f32x2) with one accumulator per pair lane. Rows whose start is not
-// 16-byte aligned take a scalar-load variant of the same kernel. The partials
-// are folded per row by the decision kernels that follow (decide.cu,
-// tree.cu).
+// pairs (f32x2) with one accumulator per pair lane; a lane's running sum is
+// rescaled (exp2f, correctly rounded to within an ulp) when its running max
+// rises, and once more to the warp's max before the warp sum. Rows whose
+// start is not 16-byte aligned take a scalar-load variant of the same kernel.
+// The partials are folded per row by the decision kernels that follow.
+//
+// Grid: (segment groups of kScanWarps warps, batch row b, row kind q). No
+// index needs a division: blockIdx.z is the row kind in streaming order and
+// blockIdx.y the batch row, so blocks are dispatched kind by kind. The kernel
+// is launched with programmatic dependent launch: its first CTAs are resident
+// while the preceding kernel drains and start reading as soon as
+// griddepcontrol.wait returns.
 #include "internal.h"
 
 namespace specv {
 
 namespace {
 
-// Row order of the pass. The partial of row j of batch row b goes to slot
-// b * RPG + j (target row k at j = k, draft row k at j = TR + k). With draft
-// rows (sampling) the rows are streamed position-descending, all batch rows
-// of position K first and of position 0 last: the residual draw re-reads
-// target and draft row m (m = first rejection, usually small), and those are
-// then the rows read last, still in L2.
-__device__ __forceinline__ long long order_to_slot(const ScanArgs& a, long long o) {
-  if (a.DR == 0) return o;
-  const long long q = o / a.B;  // row kind in streaming order: T_K, T_K-1, D_K-1, ..., T_0, D_0
-  const long long b = o - q * a.B;
+// Partial slot of row kind q (streaming order) of batch row b; target row k
+// is j = k and draft row k is j = TR + k within batch row b. With draft rows
+// (sampling) the kinds run position-descending: T_K, T_K-1, D_K-1, ...,
+// T_0, D_0. The residual draw re-reads target and draft row m (m = first
+// rejection, usually small), and those are then the rows read last, still in
+// L2.
+__device__ __forceinline__ int kind_to_row(const ScanArgs& a, int q) {
+  if (a.DR == 0) return q;
   const int K = a.TR - 1;
-  const int k = K - static_cast<int>((q + 1) >> 1);
-  const int j = q == 0 ? K : ((q & 1) ? k : a.TR + k);
-  return b * (a.TR + a.DR) + j;
+  const int k = K - ((q + 1) >> 1);
+  return q == 0 ? K : ((q & 1) ? k : a.TR + k);
 }
 
 template <typename Raw>
-__device__ __forceinline__ const Raw* row_ptr(const ScanArgs& a, long long slot) {
-  const int RPG = a.TR + a.DR;
-  const long long b = slot / RPG;
-  const int j = static_cast<int>(slot - b * RPG);
-  return j < a.TR ? static_cast<const Raw*>(a.A) + (b * a.TR + j) * a.V
-                  : static_cast<const Raw*>(a.Bd) + (b * a.DR + (j - a.TR)) * a.V;
+__device__ __forceinline__ const Raw* row_ptr(const ScanArgs& a, int b, int j) {
+  return j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
+                  : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
 }
+
+// x * c with c = c_hi + c_lo (c_lo > 0, so x = -inf stays -inf).
+__device__ __forceinline__ float scale_c(float x, float c_hi, float c_lo) { return fmaf(x, c_hi, x * c_lo); }
 
 }  // namespace
 
@@ -55,81 +62,105 @@ int scan_chunks(int V, bool vec, int dtype) { return warp_chunks(V, vec, dtype);
 template <typename Raw, bool VEC, int MODE>
 __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  griddep_wait();  // launched early: the preceding kernel may still write the logits
   if (a.zero) {  // counters of the kernel that follows
-    const long long gt = static_cast<long long>(blockIdx.x) * kScanThreads + threadIdx.x;
+    const long long blk = blockIdx.x + static_cast<long long>(gridDim.x) * (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+    const long long gt = blk * kScanThreads + threadIdx.x;
     if (gt < a.nzero) a.zero[gt] = 0;
   }
-  // warp w of the grid reduces warp chunk (w mod P) of row (w div P)
-  const long long gw = static_cast<long long>(blockIdx.x) * kScanWarps + warp;
-  const long long o = gw / a.P;
-  if (o >= static_cast<long long>(a.B) * (a.TR + a.DR)) return;  // grid rounding (whole warp)
-  const int chunk = static_cast<int>(gw - o * a.P);
-  const long long slot = order_to_slot(a, o);
-  const Raw* row = row_ptr<Raw>(a, slot);
+  const int seg = blockIdx.x * kScanWarps + warp;
+  if (seg >= a.P) return;  // grid rounding (whole warp)
+  const int b = blockIdx.y;
+  const int j = kind_to_row(a, blockIdx.z);
+  const Raw* row = row_ptr<Raw>(a, b, j);
   float M, tail;  // tail: stats -> sum of exp; argmax -> index bits
   if constexpr (VEC) {
     using Vt = Vec<Raw>;
     constexpr int EPV = Elem<Raw>::kPerVec;
-    const long long nv = a.V / EPV;
-    const long long v0 = static_cast<long long>(chunk) * (kWV * 32) + lane;
+    const int nv = a.V / EPV;
+    const int v0 = seg * (kSegChunks * kWV * 32) + lane;
     const uint4 neg = make_uint4(Vt::kNegInf, Vt::kNegInf, Vt::kNegInf, Vt::kNegInf);
-    uint4 raw[kWV];
-#pragma unroll
-    for (int t = 0; t < kWV; ++t) {
-      const long long vi = v0 + t * 32;
-      raw[t] = vi < nv ? ld_stream_v4(row + vi * EPV) : neg;
-    }
-    float vm[kWV];
-    float m = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < kWV; ++t) {
-      vm[t] = Vt::vmax(raw[t]);
-      m = fmax_nan(m, vm[t]);
-    }
-    M = warp_max_nan(m);
     if constexpr (MODE == kModeStats) {
-      float z = 0.f;
-      if (M != -INFINITY) {
-        const float2 nm = make_float2(-M, -M), ch = make_float2(a.c_hi, a.c_hi), cl = make_float2(a.c_lo, a.c_lo);
-        float2 acc[Vt::kPairs];  // one accumulator per pair lane: independent add chains
+      const float2 ch = make_float2(a.c_hi, a.c_hi), cl = make_float2(a.c_lo, a.c_lo);
+      float mrun = -INFINITY;
+      float2 acc[Vt::kPairs];  // one accumulator per pair lane: independent add chains
 #pragma unroll
-        for (int i = 0; i < Vt::kPairs; ++i) acc[i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < Vt::kPairs; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int t = 0; t < kWV; ++t)
+      for (int g = 0; g < kSegChunks; ++g) {
+        uint4 raw[kWV];
 #pragma unroll
-          for (int i = 0; i < Vt::kPairs; ++i) {
-            float2 d = add2(Vt::pair(raw[t], i), nm);
-            float2 e = fma2(d, ch, mul2(d, cl));  // (l - M) * log2(e) / T; -inf stays -inf (c_lo > 0)
-            acc[i] = add2(acc[i], make_float2(ex2_fast(e.x), ex2_fast(e.y)));
-          }
+        for (int t = 0; t < kWV; ++t) {
+          const int vi = v0 + (g * kWV + t) * 32;
+          raw[t] = vi < nv ? ld_stream_v4(row + static_cast<long long>(vi) * EPV) : neg;
+        }
+        float m = -INFINITY;
 #pragma unroll
-        for (int i = 1; i < Vt::kPairs; ++i) acc[0] = add2(acc[0], acc[i]);
-        z = acc[0].x + acc[0].y;
+        for (int t = 0; t < kWV; ++t) m = fmax_nan(m, Vt::vmax(raw[t]));
+        const float mnew = fmax_nan(mrun, m);
+        if (mnew != -INFINITY) {  // NaN and +inf propagate into the partial (the row is flagged)
+          const float sc = exp2f(scale_c(mrun - mnew, a.c_hi, a.c_lo));  // 0 when mrun = -inf
+          const float2 sc2 = make_float2(sc, sc), nm = make_float2(-mnew, -mnew);
+#pragma unroll
+          for (int i = 0; i < Vt::kPairs; ++i) acc[i] = mul2(acc[i], sc2);
+#pragma unroll
+          for (int t = 0; t < kWV; ++t)
+#pragma unroll
+            for (int i = 0; i < Vt::kPairs; ++i) {
+              const float2 d = add2(Vt::pair(raw[t], i), nm);
+              const float2 e = fma2(d, ch, mul2(d, cl));  // (l - m) * log2(e) / T; -inf stays -inf
+              acc[i] = add2(acc[i], make_float2(ex2_fast(e.x), ex2_fast(e.y)));
+            }
+          mrun = mnew;
+        }
       }
+#pragma unroll
+      for (int i = 1; i < Vt::kPairs; ++i) acc[0] = add2(acc[0], acc[i]);
+      float z = acc[0].x + acc[0].y;
+      M = warp_max_nan(mrun);
+      if (M == M && M != -INFINITY) z = mrun == -INFINITY ? 0.f : z * exp2f(scale_c(mrun - M, a.c_hi, a.c_lo));
       tail = warp_sum(z);
     } else {
+      float best = -INFINITY;
+      int bidx = INT_MAX;
+      bool nan = false;
+#pragma unroll
+      for (int g = 0; g < kSegChunks; ++g) {
+        uint4 raw[kWV];
+#pragma unroll
+        for (int t = 0; t < kWV; ++t) {
+          const int vi = v0 + (g * kWV + t) * 32;
+          raw[t] = vi < nv ? ld_stream_v4(row + static_cast<long long>(vi) * EPV) : neg;
+        }
+#pragma unroll
+        for (int t = 0; t < kWV; ++t) {
+          const float vm = Vt::vmax(raw[t]);
+          nan |= vm != vm;
+          if (vm > best) {  // strictly: a lane visits its indices in increasing order
+            best = vm;
+            const int e0 = (v0 + (g * kWV + t) * 32) * EPV;
+            int idx = INT_MAX;
+#pragma unroll
+            for (int i = Vt::kPairs - 1; i >= 0; --i) {
+              const float2 p = Vt::pair(raw[t], i);
+              if (p.y == vm) idx = e0 + 2 * i + 1;
+              if (p.x == vm) idx = e0 + 2 * i;
+            }
+            bidx = idx;
+          }
+        }
+      }
+      M = warp_max_nan(nan ? __int_as_float(0x7fc00000) : best);
       int idx = INT_MAX;
       if (M != M) {
         idx = -1;
-      } else if (M != -INFINITY) {
-#pragma unroll
-        for (int t = 0; t < kWV; ++t) {
-          if (idx == INT_MAX && vm[t] == M) {
-#pragma unroll
-            for (int i = 0; i < Vt::kPairs; ++i) {
-              const float2 p = Vt::pair(raw[t], i);
-              const int e0 = static_cast<int>((v0 + t * 32) * EPV) + 2 * i;
-              if (idx == INT_MAX && p.x == M) idx = e0;
-              if (idx == INT_MAX && p.y == M) idx = e0 + 1;
-            }
-          }
-        }
-        idx = __reduce_min_sync(0xffffffffu, idx);
+      } else {
+        idx = __reduce_min_sync(0xffffffffu, best == M ? bidx : INT_MAX);
       }
       tail = __int_as_float(idx);
     }
   } else {
-    const long long v0 = static_cast<long long>(chunk) * (kScalarPerLane * 32) + lane;
+    const long long v0 = static_cast<long long>(seg) * (kScalarPerLane * 32) + lane;
     float e[kScalarPerLane];
 #pragma unroll
     for (int t = 0; t < kScalarPerLane; ++t) {
@@ -144,10 +175,7 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
       float z = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int t = 0; t < kScalarPerLane; ++t) {
-          const float d = e[t] - M;
-          z += ex2_fast(fmaf(d, a.c_hi, d * a.c_lo));
-        }
+        for (int t = 0; t < kScalarPerLane; ++t) z += ex2_fast(scale_c(e[t] - M, a.c_hi, a.c_lo));
       }
       tail = warp_sum(z);
     } else {
@@ -163,18 +191,17 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
       tail = __int_as_float(idx);
     }
   }
-  if (lane == 0) a.part[slot * a.P + chunk] = make_float2(M, tail);
+  if (lane == 0) a.part[(static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg] = make_float2(M, tail);
 }
 
 namespace {
 
 template <typename Raw, bool VEC, int MODE>
 cudaError_t launch_t(const ScanArgs& a, cudaStream_t st) {
-  const long long warps = static_cast<long long>(a.B) * (a.TR + a.DR) * a.P;
-  const long long blocks = (warps + kScanWarps - 1) / kScanWarps;
-  if (blocks <= 0) return cudaSuccess;
-  rowscan_kernel<Raw, VEC, MODE><<<static_cast<unsigned>(blocks), kScanThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>((a.P + kScanWarps - 1) / kScanWarps), static_cast<unsigned>(a.B),
+                  static_cast<unsigned>(a.TR + a.DR));
+  if (a.P <= 0 || a.B <= 0 || a.TR + a.DR <= 0) return cudaSuccess;
+  return launch_pdl(rowscan_kernel<Raw, VEC, MODE>, grid, dim3(kScanThreads), st, a);
 }
 
 template <typename Raw>

@@ -15,23 +15,25 @@
 //   2. weighs one slice of kNRS rounds of 256 vectors of row m for the draw
 //      that follows: after a rejection, from max(0, p_m - q_m) renormalised;
 //      after K acceptances, from the bonus position p_K (lotook.com, step
-//      "resampling and the bonus token"), writing per (round, warp) totals as
-//      float pairs;
+//      "resampling and the bonus token"), and writes the total of every
+//      (round, warp) unit of 32 vectors as a float pair;
 //   3. the last CTA of row b (atomic ticket, zeroed by the rowscan pass)
-//      draws: the smallest token id whose cumulative weight exceeds u * S,
-//      found on one warp by scanning the (slice, round) totals, the crossing
-//      round's warp totals, that warp's 32 re-weighed vectors and the
-//      crossing vector's elements.
+//      draws: the smallest token id whose cumulative weight exceeds u * S.
+//      One block-wide float-pair scan over all unit totals of the row gives
+//      S and the crossing unit; one warp re-weighs that unit's 32 vectors and
+//      scans them, then the crossing vector's elements.
 //
 // Arithmetic. The ratio r is formed in fp32 from float-pair normalisers
 // (relative error about 2e-7); when the uniform lies within 1e-5 of r it is
 // recomputed in fp64 (the common path has no fp64 transcendental: an fp64 exp
 // costs about a microsecond of latency on this part). The residual weight is
-// p~_v * (1 - 2^delta_v), p~_v the target's weight relative to its row
-// maximum and delta_v = log2(q_v / p_v) from exact logit differences;
-// 1 - 2^delta uses the Taylor series of expm1 (degree 8, relative error about
-// 1e-7) for -1 < delta < 0, so cancellation where p ~ q costs no accuracy;
-// constant factors on every p~_v cancel in the inverse CDF.
+// p~_v * (1 - 2^d_v), p~_v the target's weight relative to its row maximum
+// and d_v = log2(q_v / p_v) from exact logit differences; for -1 < d < 0,
+// 1 - 2^d = d * H(d) with H a degree-5 polynomial fitted to (1 - 2^d) / d on
+// [-1, 0] (relative error 1.2e-8, about 1.3e-7 after fp32 evaluation), so
+// cancellation where p ~ q costs no accuracy; below -1 the hardware 2^x
+// serves. Constant factors on every p~_v cancel in the inverse CDF, and the
+// cumulative sums above one vector are float pairs.
 #include "fold.cuh"
 
 namespace specv {
@@ -66,9 +68,10 @@ struct Consts {
   int mode;
 };
 
-// Coefficients of (e^(-s) - 1) / (-s) = sum_n (-s)^n / (n+1)!, n = 0..8.
-__constant__ float kH[9] = {1.0f,           -0.5f,          0.16666667163f,   -0.04166666791f, 0.00833333377f,
-                            -0.00138888892f, 0.00019841270f, -2.48015876e-05f, 2.75573188e-06f};
+// H(d) = (1 - 2^d) / d on [-1, 0] as sum_n kH[n] d^n: coefficients fitted
+// to minimise the relative error (1.2e-8) on that interval.
+__constant__ float kH[6] = {-6.931471825e-01f, -2.402261496e-01f, -5.549939722e-02f,
+                            -9.596990421e-03f, -1.291199587e-03f, -1.146293362e-04f};
 
 // Weights of two elements from their target and draft logits (packed).
 __device__ __forceinline__ float2 weight2(float2 lp, float2 lq, const Consts& k) {
@@ -79,17 +82,16 @@ __device__ __forceinline__ float2 weight2(float2 lp, float2 lq, const Consts& k)
   if (k.mode != 0) return pt;
   const float2 f = add2(fma2(lp, make_float2(-1.f, -1.f), lq), make_float2(k.dM, k.dM));  // (lq - Mq) - (lp - Mp)
   const float2 dl = add2(fma2(f, ch, fma2(f, cl, make_float2(k.D_lo, k.D_lo))), make_float2(k.D_hi, k.D_hi));
-  // dl = log2(q / p). 1 - 2^dl: Taylor series of expm1 for -1 < dl < 0, hardware 2^x below.
-  const float2 s = mul2(dl, make_float2(-0.693147180559945309f, -0.693147180559945309f));  // s = -dl ln 2 > 0
-  float2 h = make_float2(kH[8], kH[8]);
+  // dl = log2(q / p); 1 - 2^dl = dc * H(dc) with dc = min(dl, 0) (0 where q >= p,
+  // also for NaN from two -inf logits), the hardware 2^x below -1
+  const float2 dc = make_float2(fminf(dl.x, 0.f), fminf(dl.y, 0.f));
+  float2 h = make_float2(kH[5], kH[5]);
 #pragma unroll
-  for (int n = 7; n >= 0; --n) h = fma2(h, s, make_float2(kH[n], kH[n]));
-  const float2 gp = mul2(s, h);
-  const float2 gx = make_float2(1.f - ex2_fast(dl.x), 1.f - ex2_fast(dl.y));
-  float2 w;
-  w.x = dl.x < 0.f ? pt.x * (dl.x > -1.f ? gp.x : gx.x) : 0.f;
-  w.y = dl.y < 0.f ? pt.y * (dl.y > -1.f ? gp.y : gx.y) : 0.f;
-  return w;
+  for (int n = 4; n >= 0; --n) h = fma2(h, dc, make_float2(kH[n], kH[n]));
+  const float2 g1 = mul2(dc, h);
+  const float2 g2 = fma2(make_float2(ex2_fast(dl.x), ex2_fast(dl.y)), make_float2(-1.f, -1.f), make_float2(1.f, 1.f));
+  const float2 g = make_float2(dl.x <= -1.f ? g2.x : g1.x, dl.y <= -1.f ? g2.y : g1.y);
+  return mul2(pt, g);
 }
 
 __device__ __forceinline__ float weight1(float lp, float lq, const Consts& k) {
@@ -97,11 +99,12 @@ __device__ __forceinline__ float weight1(float lp, float lq, const Consts& k) {
 }
 
 // Weights of the elements of one 16-byte vector pair, in element order, and
-// their fp32 sum (w may be NULL).
+// their fp32 sum (even and odd elements summed apart, then added; w may be
+// NULL).
 template <typename Raw>
 __device__ __forceinline__ float vec_weights(const uint4& p, const uint4& q, const Consts& k, float* w) {
   using Vt = Vec<Raw>;
-  float s = 0.f;
+  float2 s = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < Vt::kPairs; ++i) {
     const float2 x = weight2(Vt::pair(p, i), Vt::pair(q, i), k);
@@ -109,10 +112,20 @@ __device__ __forceinline__ float vec_weights(const uint4& p, const uint4& q, con
       w[2 * i] = x.x;
       w[2 * i + 1] = x.y;
     }
-    s += x.x;
-    s += x.y;
+    s = add2(s, x);
   }
-  return s;
+  return __fadd_rn(s.x, s.y);
+}
+
+// Error-free sum of two floats as a (hi, lo) pair.
+__device__ __forceinline__ float2 two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return make_float2(s, (a - (s - bb)) + (b - bb));
+}
+
+__device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
+  return make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
 }
 
 template <typename Raw, bool VEC>
@@ -168,35 +181,40 @@ struct Slice {
     }
   }
 
-  // Weigh slice s and write its per-(round, warp) totals wt and per-round
-  // totals ut (float pairs). Contains __syncthreads: call from every thread.
+  // Weigh slice s and write the total of every (round, warp) unit as a float
+  // pair to wt[(s * kNRS + round) * warps + warp]. The eight per-round sums
+  // of the warp are reduced by a transposing butterfly: each exchange step
+  // halves the rounds a lane carries, so after three steps lane l holds part
+  // of round l / 4 and two more steps complete it.
   __device__ static __forceinline__ void publish(const Raw* P, const Raw* Q, int s, int tid, long long nv,
-                                                 const Consts& k, float2* wt, float2* ut) {
-    __shared__ float2 red[kNRS][kResThreads / 32];
+                                                 const Consts& k, float2* wt) {
+    static_assert(kNRS == 8, "the butterfly below is written for eight rounds");
+    const int lane = tid & 31;
     float vs[kNRS];
     sums(P, Q, s, tid, nv, k, vs);
-    float2 acc[kNRS];
+    float2 r4[4], r2[2];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
 #pragma unroll
-    for (int r = 0; r < kNRS; ++r) acc[r] = make_float2(vs[r], 0.f);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int r = 0; r < kNRS; ++r)
-        acc[r] = ds_add(acc[r], make_float2(__shfl_xor_sync(0xffffffffu, acc[r].x, o),
-                                            __shfl_xor_sync(0xffffffffu, acc[r].y, o)));
-    if ((tid & 31) == 0)
-#pragma unroll
-      for (int r = 0; r < kNRS; ++r) {
-        wt[(static_cast<long long>(s) * kNRS + r) * kResWarps + (tid >> 5)] = acc[r];
-        red[r][tid >> 5] = acc[r];
-      }
-    __syncthreads();
-    if (tid < kNRS) {
-      float2 u = red[tid][0];
-      for (int w = 1; w < kResWarps; ++w) u = ds_add(u, red[tid][w]);
-      ut[static_cast<long long>(s) * kNRS + tid] = u;
+    for (int i = 0; i < 4; ++i) {
+      const float send = b4 ? vs[i] : vs[4 + i];
+      const float keep = b4 ? vs[4 + i] : vs[i];
+      r4[i] = two_sum(keep, __shfl_xor_sync(0xffffffffu, send, 16));
     }
-    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 send = b3 ? r4[i] : r4[2 + i];
+      const float2 keep = b3 ? r4[2 + i] : r4[i];
+      r2[i] = ds_add(keep, shfl_xor2(send, 8));
+    }
+    float2 r1;
+    {
+      const float2 send = b2 ? r2[0] : r2[1];
+      const float2 keep = b2 ? r2[1] : r2[0];
+      r1 = ds_add(keep, shfl_xor2(send, 4));
+    }
+    r1 = ds_add(r1, shfl_xor2(r1, 2));
+    r1 = ds_add(r1, shfl_xor2(r1, 1));
+    if ((lane & 3) == 0) wt[(static_cast<long long>(s) * kNRS + (lane >> 2)) * kResWarps + (tid >> 5)] = r1;
   }
 };
 
@@ -223,9 +241,11 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
     if (s_x[k] < 0 || s_x[k] >= V) st |= SPEC_ROW_TOKEN;
   st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
   int m = K;
+  float2 Dm = make_float2(0.f, 0.f);  // log2(Zp_m / Zq_m), formed by every lane for its own position
   for (int k0 = 0; k0 < K; k0 += 32) {
     const int k = k0 + lane;
     bool rej = false;
+    float2 Dk = make_float2(0.f, 0.f);
     if (k < K) {
       if (st == 0) {
         const RowRec rp = rr[k], rq = rr[K + 1 + k];
@@ -245,10 +265,15 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
         } else {
           rej = !(u < r);
         }
+        Dk = ds_log2(ds_div(Zp, Zq));
       }
     }
     const unsigned msk = __ballot_sync(0xffffffffu, rej);
-    if (m == K && msk) m = k0 + __ffs(msk) - 1;
+    if (m == K && msk) {
+      const int l = __ffs(msk) - 1;
+      m = k0 + l;
+      Dm = make_float2(__shfl_sync(0xffffffffu, Dk.x, l), __shfl_sync(0xffffffffu, Dk.y, l));
+    }
   }
   if (st) m = -1;
   if (write) {
@@ -273,9 +298,8 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
         const RowRec rq = rr[K + 1 + m];
         d.Mq = rq.M;
         d.dM = rp.M - rq.M;
-        const float2 D = ds_log2(ds_div(make_float2(rp.Zhi, rp.Zlo), make_float2(rq.Zhi, rq.Zlo)));  // log2(Zp / Zq)
-        d.D_hi = D.x;
-        d.D_lo = D.y;
+        d.D_hi = Dm.x;
+        d.D_lo = Dm.y;
       }
     }
     *dec = d;
@@ -317,45 +341,42 @@ __device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane
   }
 }
 
-// Inclusive warp scan in fp64.
-__device__ __forceinline__ double warp_scan_d(double v, int lane) {
+// hi + lo > t.hi + t.lo for normalised float pairs.
+__device__ __forceinline__ bool ds_gt(float2 a, float2 t) { return a.x > t.x || (a.x == t.x && a.y > t.y); }
+
+// Inclusive warp scan of float pairs.
+__device__ __forceinline__ float2 warp_scan_ds(float2 x, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
+    const float2 y = make_float2(__shfl_up_sync(0xffffffffu, x.x, o), __shfl_up_sync(0xffffffffu, x.y, o));
+    if (lane >= o) x = ds_add(y, x);
   }
-  return v;
+  return x;
 }
 
-// One warp: among n units (value(i), i ascending), pick the first with
-// positive weight whose cumulative end exceeds t, else the last with positive
-// weight; returns its index (-1 if none) and sets *base to the weight before
-// it (counting from base0).
-template <typename F>
-__device__ __forceinline__ int warp_pick(int n, double t, double base0, int lane, F value, double* base) {
-  double carry = base0, picked_base = base0;
-  int pick = -1, last = -1;
-  for (int i0 = 0; i0 < n; i0 += 32) {
-    const int i = i0 + lane;
-    const double v = i < n ? value(i) : 0.0;
-    const double incl = warp_scan_d(v, lane) + carry;
-    const unsigned pos = __ballot_sync(0xffffffffu, v > 0.0);
-    const unsigned hit = __ballot_sync(0xffffffffu, v > 0.0 && incl > t);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      pick = i0 + l;
-      picked_base = __shfl_sync(0xffffffffu, incl - v, l);
-      break;
-    }
-    if (pos) {
-      const int l = 31 - __clz(pos);
-      last = i0 + l;
-      picked_base = __shfl_sync(0xffffffffu, incl - v, l);
-    }
-    carry = __shfl_sync(0xffffffffu, incl, 31);
+// Block-wide scan of two float pairs per thread (units 2 tid and 2 tid + 1 of
+// a tile of 2 kResThreads units), continuing from `carry`: ex0 / ex1 are the
+// exclusive prefixes of the two units, the return value the tile's end (the
+// same in every thread). Contains __syncthreads: call from every thread.
+__device__ __forceinline__ float2 block_scan2(float2 v0, float2 v1, float2 carry, float2* ex0, float2* ex1,
+                                              float2* sh_w) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float2 x = warp_scan_ds(ds_add(v0, v1), lane);
+  float2 ex = make_float2(__shfl_up_sync(0xffffffffu, x.x, 1), __shfl_up_sync(0xffffffffu, x.y, 1));
+  if (lane == 0) ex = make_float2(0.f, 0.f);
+  if (lane == 31) sh_w[warp] = x;
+  __syncthreads();
+  float2 base = carry, end = carry;
+#pragma unroll
+  for (int w = 0; w < kResWarps; ++w) {
+    const float2 t = sh_w[w];
+    if (w < warp) base = ds_add(base, t);
+    end = ds_add(end, t);
   }
-  *base = picked_base;
-  return pick >= 0 ? pick : last;
+  __syncthreads();  // sh_w is reused by the next call
+  *ex0 = ds_add(base, ex);
+  *ex1 = ds_add(*ex0, v0);
+  return end;
 }
 
 }  // namespace
@@ -364,12 +385,14 @@ template <typename Raw, bool VEC>
 __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) {
   using SL = Slice<Raw, VEC>;
   constexpr int EPV = SL::EPV;
+  constexpr int kTile = 2 * kResThreads;  // units per scan tile
   const int s = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, RPG = 2 * K + 1;
   __shared__ RowRec rr[2 * kMaxK + 1];
   __shared__ float s_lp[kMaxK], s_lq[kMaxK], s_u[kMaxK];
   __shared__ int s_x[kMaxK];
   __shared__ DecRec s_dec;
+  griddep_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
   // inputs first (the pass this kernel depends on does not write them), so
   // these gathers overlap the end of the streaming pass
   for (int k = tid; k < K; k += kResThreads) {
@@ -394,11 +417,12 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   const Raw* P = static_cast<const Raw*>(a.Lp) + (static_cast<long long>(b) * (K + 1) + d.m) * V;
   const Raw* Q = d.mode == 0 ? static_cast<const Raw*>(a.Lq) + (static_cast<long long>(b) * K + d.m) * V : P;
   Consts k{d.Mp, d.dM, d.D_hi, d.D_lo, a.c_hi, a.c_lo, d.mode};
-  float2* wt = a.warp_sum + static_cast<long long>(b) * a.NS * kNRS * kResWarps;  // [NS][kNRS][warps]
-  float2* ut = a.unit_sum + static_cast<long long>(b) * a.NS * kNRS;                // [NS][kNRS]
+  const int nu = a.NS * kNRS * kResWarps;  // (slice, round, warp) units, ascending token order
+  float2* wt = a.warp_sum + static_cast<long long>(b) * nu;
 
   __shared__ int s_last;
-  SL::publish(P, Q, s, tid, nv, k, wt, ut);
+  SL::publish(P, Q, s, tid, nv, k, wt);
+  __syncthreads();
   if (tid == 0) {
     __threadfence();
     s_last = atomicAdd(a.res_ticket + b, 1) == a.NS - 1;
@@ -407,84 +431,97 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   if (!s_last) return;
   __threadfence();
 
-  // ---- the draw (last CTA of row b); units are (slice, round) pairs
-  const int nu = a.NS * kNRS;
-  // unit totals: lane l keeps units l, l + 32, ... (up to kUL of them) in
-  // registers; beyond that they are re-read
-  constexpr int kUL = 4;
-  double uv[kUL];
-  auto unit = [&](int i) {
-    const int jj = i >> 5;
-    double v = 0.0;
-#pragma unroll
-    for (int x = 0; x < kUL; ++x)
-      if (jj == x) v = uv[x];
-    return jj < kUL ? v : ds_to_d(__ldcg(ut + i));
+  // ---- the draw (last CTA of row b)
+  __shared__ float2 sh_w[kResWarps];
+  __shared__ float2 sh_ex[kTile];
+  __shared__ int s_first, s_lastpos;
+  const int ntile = (nu + kTile - 1) / kTile;
+  auto load2 = [&](int tile, float2* v0, float2* v1) {
+    const int i = tile * kTile + 2 * tid;
+    const float4 q = i < nu ? __ldcg(reinterpret_cast<const float4*>(wt + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    *v0 = make_float2(q.x, q.y);
+    *v1 = make_float2(q.z, q.w);
   };
-  __shared__ double sh_S;
-  if (tid < 32) {
-#pragma unroll
-    for (int x = 0; x < kUL; ++x) uv[x] = lane + 32 * x < nu ? ds_to_d(__ldcg(ut + lane + 32 * x)) : 0.0;
-    double S = 0.0;
-    for (int i0 = 0; i0 < nu; i0 += 32) {
-      double v = 0.0;
-      if (i0 + lane < nu) v = (i0 >> 5) < kUL ? uv[0] : 0.0;
-#pragma unroll
-      for (int x = 1; x < kUL; ++x)
-        if ((i0 >> 5) == x && i0 + lane < nu) v = uv[x];
-      if ((i0 >> 5) >= kUL && i0 + lane < nu) v = ds_to_d(__ldcg(ut + i0 + lane));
-      S += warp_sum_d(v);
+  float2 v0, v1, ex0, ex1, S;
+  for (int pass = 0; pass < 2; ++pass) {
+    // S: the end of the scan over every tile (the single tile stays in registers)
+    S = make_float2(0.f, 0.f);
+    for (int tile = 0; tile < ntile; ++tile) {
+      load2(tile, &v0, &v1);
+      S = block_scan2(v0, v1, S, &ex0, &ex1, sh_w);
     }
-    if (lane == 0) sh_S = S;
-  }
-  __syncthreads();
-  if (k.mode == 0 && !(sh_S > 0.0)) {
+    if (k.mode != 0 || S.x > 0.f) break;
     // p_m == q_m numerically: draw from p_m (this CTA re-weighs every slice)
     k.mode = 1;
-    for (int sl = 0; sl < a.NS; ++sl) SL::publish(P, P, sl, tid, nv, k, wt, ut);
-    if (tid < 32) {
-#pragma unroll
-      for (int x = 0; x < kUL; ++x) uv[x] = lane + 32 * x < nu ? ds_to_d(__ldcg(ut + lane + 32 * x)) : 0.0;
-      double S = 0.0;
-      for (int i0 = 0; i0 < nu; i0 += 32) S += warp_sum_d(i0 + lane < nu ? ds_to_d(__ldcg(ut + i0 + lane)) : 0.0);
-      if (lane == 0) sh_S = S;
+    for (int sl = 0; sl < a.NS; ++sl) SL::publish(P, P, sl, tid, nv, k, wt);
+    __syncthreads();
+  }
+  float2 t = ds_mul_f(S, a.ur[b]);
+  int u = -1;
+  float2 base = make_float2(0.f, 0.f), carry = make_float2(0.f, 0.f);
+  int lastpos = -1;
+  float2 lastbase = base;
+  for (int tile = 0; tile < ntile && u < 0; ++tile) {
+    if (ntile > 1) {
+      load2(tile, &v0, &v1);
+      carry = block_scan2(v0, v1, carry, &ex0, &ex1, sh_w);
+    }
+    if (tid == 0) {
+      s_first = INT_MAX;
+      s_lastpos = -1;
+    }
+    sh_ex[2 * tid] = ex0;
+    sh_ex[2 * tid + 1] = ex1;
+    __syncthreads();
+    // first unit with positive weight whose cumulative end exceeds t
+    if (v0.x > 0.f && ds_gt(ds_add(ex0, v0), t)) atomicMin(&s_first, 2 * tid);
+    else if (v1.x > 0.f && ds_gt(ds_add(ex1, v1), t)) atomicMin(&s_first, 2 * tid + 1);
+    if (v1.x > 0.f) atomicMax(&s_lastpos, 2 * tid + 1);
+    else if (v0.x > 0.f) atomicMax(&s_lastpos, 2 * tid);
+    __syncthreads();
+    if (s_first != INT_MAX) {
+      u = tile * kTile + s_first;
+      base = sh_ex[s_first];
+    } else if (s_lastpos >= 0) {
+      lastpos = tile * kTile + s_lastpos;
+      lastbase = sh_ex[s_lastpos];
     }
     __syncthreads();
   }
+  if (u < 0 && lastpos >= 0) {  // rounding left no crossing: the last unit with weight
+    u = lastpos;
+    base = lastbase;
+    t = make_float2(INFINITY, 0.f);
+  }
   if (tid >= 32) return;
-  const double t = static_cast<double>(a.ur[b]) * sh_S;
   int32_t* out = a.out_tokens + static_cast<long long>(b) * (a.K + 1) + d.m;
-  // (slice, round) unit, then warp within the round, then lane, then element
-  double base;
-  const int u = warp_pick(nu, t, 0.0, lane, unit, &base);
   int token = -1;
   if (u >= 0) {
-    const float2* wr = wt + static_cast<long long>(u) * kResWarps;
-    const int w = warp_pick(kResWarps, t, base, lane, [&](int i) { return ds_to_d(__ldcg(wr + i)); }, &base);
-    if (w >= 0) {
-      const int sl = u / kNRS, r = u - sl * kNRS;
-      const long long vi = sl * SL::kSV + static_cast<long long>(r) * kResThreads + w * 32 + lane;
-      float ew[EPV];
-      const float vsum = SL::one(P, Q, vi, nv, k, ew);
-      const int l = warp_pick(
-          32, t, base, lane, [&](int i) { return static_cast<double>(__shfl_sync(0xffffffffu, vsum, i)); }, &base);
-      if (l >= 0 && lane == l) {
-        double cum = base;
-        int pick = -1, lastp = -1;
+    // the unit's 32 vectors, one per lane, then the crossing lane's elements
+    const int sl = u / (kNRS * kResWarps), r = (u / kResWarps) % kNRS, w = u % kResWarps;
+    const long long vi = sl * SL::kSV + static_cast<long long>(r) * kResThreads + w * 32 + lane;
+    float ew[EPV];
+    const float vsum = SL::one(P, Q, vi, nv, k, ew);
+    const float2 incl = ds_add(base, warp_scan_ds(make_float2(vsum, 0.f), lane));
+    float2 cum = make_float2(__shfl_up_sync(0xffffffffu, incl.x, 1), __shfl_up_sync(0xffffffffu, incl.y, 1));
+    if (lane == 0) cum = base;  // cum: the weight before this lane's vector
+    const unsigned hit = __ballot_sync(0xffffffffu, vsum > 0.f && ds_gt(incl, t));
+    const unsigned pos = __ballot_sync(0xffffffffu, vsum > 0.f);
+    const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    if (l >= 0 && lane == l) {
+      int pick = -1, lastp = -1;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          if (pick < 0 && ew[e] > 0.f) {
-            lastp = e;
-            cum += static_cast<double>(ew[e]);
-            if (cum > t) pick = e;
-          }
+      for (int e = 0; e < EPV; ++e) {
+        if (pick < 0 && ew[e] > 0.f) {
+          lastp = e;
+          cum = ds_add(cum, make_float2(ew[e], 0.f));
+          if (ds_gt(cum, t)) pick = e;
         }
-        if (pick < 0) pick = lastp;
-        token = pick < 0 ? -1 : static_cast<int>(vi * EPV + pick);
       }
-      token = __shfl_sync(0xffffffffu, token, l < 0 ? 0 : l);
-      if (l < 0) token = -1;
+      if (pick < 0) pick = lastp;
+      token = pick < 0 ? -1 : static_cast<int>(vi * EPV + pick);
     }
+    if (l >= 0) token = __shfl_sync(0xffffffffu, token, l);
   }
   if (lane == 0) *out = token;
 }

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kThreads) tree_finish_kernel(TreeArgs a) {
     s_any = 0;
     s_key = 0u;
   }
+  griddep_launch_dependents();
   __syncthreads();
   griddep_wait();
   const int lane = tid & 31, warp = tid >> 5;
