@@ -256,6 +256,34 @@ def run_ours(args):
             step_dev(i)
         torch.cuda.synchronize()
 
+    # --graph: each step captured once as a CUDA graph (one per input copy)
+    # and replayed. Eager launches through the API are the default: a graph
+    # launch per step ends the programmatic overlap between consecutive
+    # steps, which costs more than the host launches it saves here.
+    graphs, launch_mode = None, "eager"
+    if args.graph:
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for i in range(n_sets):
+                    step_dev(i)
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            graphs = []
+            for i in range(n_sets):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step_dev(i)
+                graphs.append(g)
+            launch_mode = "cuda_graph"
+        except Exception as e:  # report and time the eager path instead
+            graphs, launch_mode = None, f"eager (graph capture failed: {type(e).__name__})"
+    run_step = (lambda i: graphs[i % n_sets].replay()) if graphs else step_dev
+    for i in range(max(args.warmup, 3)):
+        run_step(i)
+    torch.cuda.synchronize()
+
     # timed region: K steps back to back, events only around the whole run
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -263,7 +291,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(args.steps):
-        step_dev(i)
+        run_step(i)
     end.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
@@ -335,6 +363,7 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic (seeded generator: peaked logits, Gumbel-max draft tokens)",
         "config": dict(cfg, parallelism=f"replicas x{ws} (independent batches, no data-path collective)",
+                       launch=launch_mode,
                        l2=(f"logits {alg / 1e6:.0f} MB per step, {n_sets} rotating copies ({n_sets * alg / 1e6:.0f} MB) "
                           f">= 2 x L2 {L2_BYTES / 1e6:.0f} MB; no flush between steps")),
         "logit_read_gbs": alg / (total_ms / args.steps / 1e3) / 1e9,
@@ -450,6 +479,7 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--graph", action="store_true", help="replay each step as a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

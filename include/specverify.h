@@ -100,7 +100,8 @@ size_t spec_workspace_bytes(int B, int K, int V, int dtype);
  *   accept_len [B] int32: m, the number of accepted draft tokens (0..K)
  *   out_tokens [B][K+1] int32: x_0..x_{m-1}, the drawn token, then -1
  *   lse_target [B][K+1], lse_draft [B][K] fp32 or NULL: log-normalisers
- *       log sum_v exp(l_v / T) of each row
+ *       log sum_v exp(l_v / T) of each row (NaN for a row holding NaN or
+ *       +inf or only -inf)
  *   p_at_x, q_at_x [B][K] fp32 or NULL: p_k(x_k), q_k(x_k)
  *   row_status [B] int32 (SPEC_ROW_* bits, 0 = ok)
  * Stages: spec_chain_scan then spec_chain_sample on the same stream. */

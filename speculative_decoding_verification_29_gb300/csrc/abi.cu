@@ -37,26 +37,19 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CU
 
 size_t up256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
-// Workspace regions (each 256-byte aligned). Region sizes are upper bounds
-// over the vector and scalar load paths, so the layout depends only on the
-// sizes, never on pointer alignment.
+// Workspace: the rowscan partials, one float pair per warp segment of every
+// row, sized for the larger of the vector and scalar load paths so that the
+// size depends only on the shapes, never on pointer alignment.
 struct Layout {
-  size_t part, slices, tickets, total;
+  size_t part, total;
 };
 
 Layout layout(int B, int TR, int DR, int V, int dtype) {
   const long long nrows = static_cast<long long>(B) * (TR + DR);
   const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
-  const long long NS = std::max(tail_slices(V, true, dtype), tail_slices(V, false, dtype));
   Layout L{};
-  size_t off = 0;
-  L.part = off;
-  off += up256(static_cast<size_t>(nrows * P) * sizeof(float2));
-  L.slices = off;
-  off += up256(static_cast<size_t>(B * NS) * kNRS * (kResThreads / 32) * sizeof(float2));
-  L.tickets = off;
-  off += up256(static_cast<size_t>(B) * sizeof(int));
-  L.total = off;
+  L.part = 0;
+  L.total = up256(static_cast<size_t>(nrows * P) * sizeof(float2));
   return L;
 }
 
@@ -169,8 +162,6 @@ int chain_scan(const ChainCall& c) {
   a.P = scan_chunks(c.V, vec, c.dtype);
   split_c(c.T, &a.c_hi, &a.c_lo);
   a.part = reinterpret_cast<float2*>(at(c.ws, L.part));
-  a.zero = reinterpret_cast<int*>(at(c.ws, L.tickets));
-  a.nzero = c.B;
   return cuda_status(launch_rowscan(a, c.dtype, vec, kModeStats, c.st));
 }
 
@@ -190,7 +181,8 @@ int chain_sample(const ChainCall& c) {
   t.K = c.K;
   t.V = c.V;
   t.P = scan_chunks(c.V, vec, c.dtype);
-  t.NS = tail_slices(c.V, vec, c.dtype);
+  const long long nv = vec ? static_cast<long long>(c.V) * static_cast<long long>(elem_size(c.dtype)) / 16 : c.V;
+  tail_geometry(nv, &t.NB, &t.G, &t.nvw);
   split_c(c.T, &t.c_hi, &t.c_lo);
   t.invT = 1.0 / static_cast<double>(c.T);
   split_pos(t.invT, &t.it_hi, &t.it_lo);
@@ -201,8 +193,6 @@ int chain_sample(const ChainCall& c) {
   t.lse_q = c.lse_q;
   t.px = c.px;
   t.qx = c.qx;
-  t.warp_sum = reinterpret_cast<float2*>(at(c.ws, L.slices));
-  t.res_ticket = reinterpret_cast<int*>(at(c.ws, L.tickets));
   return cuda_status(launch_chain_tail(t, c.dtype, vec, c.st));
 }
 

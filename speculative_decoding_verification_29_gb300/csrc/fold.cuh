@@ -6,52 +6,71 @@
 
 namespace specv {
 
+// log2 of a positive float pair, absolute error about 4e-8: split off the
+// binary exponent so the rest is near 1, then log1p of the remainder.
+__device__ __forceinline__ float2 ds_log2(float2 x) {
+  int e;
+  float f = frexpf(x.x, &e);  // x.x = f * 2^e, f in [0.5, 1)
+  if (f < 0.70710678f) {
+    f *= 2.f;
+    e -= 1;
+  }
+  const float eps = (f - 1.f) + ldexpf(x.y, -e);  // f - 1 is exact here
+  const float l = log1pf(eps) * 1.44269504088896341f;
+  const float hi = static_cast<float>(e) + l;
+  return make_float2(hi, l - (hi - static_cast<float>(e)));
+}
+
+__device__ __forceinline__ StatRec make_stat(float M, float2 z) {
+  StatRec r;
+  r.M = M;
+  r.Z = M != M ? NAN : z.x;
+  const float2 L = ds_log2(z);
+  r.Lhi = L.x;
+  r.Llo = L.y;
+  return r;
+}
+
 // Row max and sum of exp over P (max m_c, sum z_c) partials, folded by one
-// warp; every lane returns it. The row max comes first, then each partial is
-// rescaled once by 2^((m_c - M) * log2(e) / T) and summed as a float pair.
-__device__ __forceinline__ RowRec fold_stats(const float2* pr, int P, float c_hi, float c_lo, int lane) {
+// warp; every lane returns the max and the sum as a float pair. The row max
+// comes first, then each partial is rescaled once by
+// 2^((m_c - M) * log2(e) / T) and summed as a float pair.
+__device__ __forceinline__ float fold_stats(const float2* pr, int P, float c_hi, float c_lo, int lane, float2* zout) {
   // up to 32 partials: one load per lane, kept in registers
   const float2 q0 = lane < P ? __ldcg(pr + lane) : make_float2(-INFINITY, 0.f);
   float m = q0.x;
   for (int c = lane + 32; c < P; c += 32) m = fmax_nan(m, __ldcg(pr + c).x);
   const float M = warp_max_nan(m);
-  RowRec r;
-  r.M = M;
-  r.idx = 0;
-  r.Zhi = 0.f;
-  r.Zlo = 0.f;
-  if (M != M) {
-    r.Zhi = NAN;
-    return r;
-  }
-  if (M == -INFINITY) return r;  // every entry -inf
   float2 z = make_float2(0.f, 0.f);
-  for (int c = lane; c < P; c += 32) {
-    const float2 q = c < 32 ? q0 : __ldcg(pr + c);
-    if (q.x != -INFINITY) {
-      const float d = q.x - M;
-      z = ds_add(z, ds_from_prod(q.y, exp2f(fmaf(d, c_hi, d * c_lo))));
+  if (M == M && M != -INFINITY) {
+    for (int c = lane; c < P; c += 32) {
+      const float2 q = c < 32 ? q0 : __ldcg(pr + c);
+      if (q.x != -INFINITY) {
+        const float d = q.x - M;
+        z = ds_add(z, ds_from_prod(q.y, exp2f(fmaf(d, c_hi, d * c_lo))));
+      }
     }
-  }
 #pragma unroll 1
-  for (int o = 16; o > 0; o >>= 1)
-    z = ds_add(z, make_float2(__shfl_xor_sync(0xffffffffu, z.x, o), __shfl_xor_sync(0xffffffffu, z.y, o)));
-  r.Zhi = z.x;
-  r.Zlo = z.y;
-  return r;
+    for (int o = 16; o > 0; o >>= 1)
+      z = ds_add(z, make_float2(__shfl_xor_sync(0xffffffffu, z.x, o), __shfl_xor_sync(0xffffffffu, z.y, o)));
+  }
+  *zout = z;
+  return M;
 }
 
 // Fold rows j = first, first + stride, ... (< nrows) of the stats partials at
 // `part` (row j at part + j * P) into rr[j], one warp. When every row of the
 // warp fits (at most 4 rows, P <= 64), all loads are issued before any
-// reduction, so the rows cost one memory round trip together.
+// reduction, so the rows cost one memory round trip together, and lane i
+// forms the logarithm of row i.
 __device__ __forceinline__ void fold_stats_rows(const float2* part, int P, int first, int stride, int nrows,
-                                                float c_hi, float c_lo, int lane, RowRec* rr) {
+                                                float c_hi, float c_lo, int lane, StatRec* rr) {
   constexpr int kR = 4;
   if (P > 64 || first + kR * stride < nrows) {
     for (int j = first; j < nrows; j += stride) {
-      const RowRec r = fold_stats(part + static_cast<long long>(j) * P, P, c_hi, c_lo, lane);
-      if (lane == 0) rr[j] = r;
+      float2 z;
+      const float M = fold_stats(part + static_cast<long long>(j) * P, P, c_hi, c_lo, lane, &z);
+      if (lane == 0) rr[j] = make_stat(M, z);
     }
     return;
   }
@@ -90,18 +109,10 @@ __device__ __forceinline__ void fold_stats_rows(const float2* part, int P, int f
 #pragma unroll
     for (int i = 0; i < kR; ++i)
       z[i] = ds_add(z[i], make_float2(__shfl_xor_sync(0xffffffffu, z[i].x, o), __shfl_xor_sync(0xffffffffu, z[i].y, o)));
-  if (lane == 0) {
 #pragma unroll
-    for (int i = 0; i < kR; ++i) {
-      const int j = first + i * stride;
-      if (j >= nrows) continue;
-      RowRec r;
-      r.M = M[i];
-      r.idx = 0;
-      r.Zhi = M[i] != M[i] ? NAN : z[i].x;
-      r.Zlo = M[i] != M[i] ? 0.f : z[i].y;
-      rr[j] = r;
-    }
+  for (int i = 0; i < kR; ++i) {
+    const int j = first + i * stride;
+    if (lane == i && j < nrows) rr[j] = make_stat(M[i], z[i]);
   }
 }
 
@@ -122,7 +133,6 @@ __device__ __forceinline__ RowRec fold_argmax(const float2* pr, int P, int lane)
   RowRec r;
   r.M = v;
   r.idx = i;
-  r.Zhi = r.Zlo = 0.f;
   return r;
 }
 

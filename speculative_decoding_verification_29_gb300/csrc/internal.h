@@ -22,18 +22,23 @@ constexpr int kScalarPerLane = 64;
 constexpr int kScanWarps = 8;
 constexpr int kScanThreads = kScanWarps * 32;
 
-// tail geometry: each CTA weighs kNRS rounds of 256 vectors of one row
+// tail: threads per CTA (a cluster of CTAs serves one batch row)
 constexpr int kResThreads = 256;
-constexpr int kNRS = 8;
 
 // greedy decision kernel: one CTA of kDecideThreads per batch row
 constexpr int kDecideThreads = 512;
 
-// Per-row fold of the rowscan partials.
+// Per-row fold of the argmax partials.
 struct RowRec {
-  float M;         // stats: max raw logit; argmax: max value (NaN: row holds NaN)
-  int idx;         // argmax: lowest index of the maximum (INT_MAX: none)
-  float Zhi, Zlo;  // stats: sum_v exp((l_v - M) / T) as a float pair
+  float M;   // max value (NaN: row holds NaN)
+  int idx;   // lowest index of the maximum (INT_MAX: none)
+};
+
+// Per-row fold of the stats partials (16 bytes: one vector store).
+struct __align__(16) StatRec {
+  float M;         // max raw logit (NaN: row holds NaN)
+  float Z;         // sum_v exp((l_v - M) / T), rounded to fp32
+  float Lhi, Llo;  // log2 of that sum from its float-pair value, as a float pair
 };
 
 // Per-row-b decision: which row the draw uses and its constants.
@@ -55,8 +60,6 @@ struct ScanArgs {
   int P;             // chunks (partials) per row
   float c_hi, c_lo;  // log2(e) / T as a float pair, c_lo > 0
   float2* part;      // [B * (TR + DR)][P]
-  int* zero;         // counters the next kernel uses, zeroed here (may be NULL)
-  int nzero;
 };
 
 // Warp segments per row, and so partials per row, for a vocabulary of V
@@ -92,7 +95,9 @@ struct TailArgs {
   const int32_t* x;
   const float* ua;
   const float* ur;
-  int B, K, V, P, NS;
+  int B, K, V, P;
+  int NB, G;        // batches of kRB rounds per warp block, rounds per unit
+  long long nvw;    // vectors per warp block
   float c_hi, c_lo;    // log2(e) / T, c_lo > 0
   float it_hi, it_lo;  // 1 / T, it_lo > 0
   double invT;
@@ -103,12 +108,10 @@ struct TailArgs {
   float* lse_q;
   float* px;
   float* qx;
-  float2* warp_sum;  // [B][NS][kNRS][kResThreads / 32] unit totals
-  int* res_ticket;   // [B], zero on entry (zeroed by the rowscan pass)
 };
 
-// Slices (CTAs per batch row) of the tail kernel.
-int tail_slices(int V, bool vec, int dtype);
+// Weighing geometry of the tail kernel for rows of nv vectors.
+void tail_geometry(long long nv, int* NB, int* G, long long* nvw);
 cudaError_t launch_chain_tail(const TailArgs& a, int dtype, bool vec, cudaStream_t st);
 
 struct TreeArgs {
@@ -131,18 +134,27 @@ cudaError_t launch_tree_confidence(const float* conf, int B, int N, int n1, floa
 
 // Launch `kernel` so that it may start while the preceding kernel in the
 // stream drains; the kernel calls griddep_wait() before reading its outputs.
+// cluster > 1 groups that many consecutive CTAs along x into a cluster.
 template <typename Args>
-inline cudaError_t launch_pdl(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t st, const Args& args) {
+inline cudaError_t launch_pdl(void (*kernel)(Args), dim3 grid, dim3 block, cudaStream_t st, const Args& args,
+                              int cluster = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

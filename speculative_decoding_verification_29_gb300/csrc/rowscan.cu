@@ -63,11 +63,6 @@ template <typename Raw, bool VEC, int MODE>
 __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   griddep_wait();  // launched early: the preceding kernel may still write the logits
-  if (a.zero) {  // counters of the kernel that follows
-    const long long blk = blockIdx.x + static_cast<long long>(gridDim.x) * (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
-    const long long gt = blk * kScanThreads + threadIdx.x;
-    if (gt < a.nzero) a.zero[gt] = 0;
-  }
   const int seg = blockIdx.x * kScanWarps + warp;
   if (seg >= a.P) return;  // grid rounding (whole warp)
   const int b = blockIdx.y;

@@ -1,27 +1,28 @@
 // tail.cu -- decision and residual / bonus draw of chain verification, in
 // one kernel that follows the streaming pass.
 //
-// Grid (slices, B), launched with programmatic dependent launch so its CTAs
-// start as the rowscan pass drains (inputs they need that the pass does not
-// write are gathered before griddepcontrol.wait). Every CTA of batch row b:
-//   1. folds the rowscan partials of b's 2K+1 rows (one warp per row) and
-//      decides, on one warp: r_k = p_k(x_k) / q_k(x_k), x_k kept iff
-//      u_k < r_k, left to right, stopping at the first rejection m
-//      (speculative sampling as summarised on the ariser.io page, section on
-//      keeping the same distribution; lotook.com, step "accept or reject draft
-//      tokens"). The CTA of slice 0 writes the outputs; the others use the
-//      decision. Folding again in every CTA costs a few KB of L2 reads and
-//      saves a kernel boundary on the critical path;
-//   2. weighs one slice of kNRS rounds of 256 vectors of row m for the draw
-//      that follows: after a rejection, from max(0, p_m - q_m) renormalised;
-//      after K acceptances, from the bonus position p_K (lotook.com, step
-//      "resampling and the bonus token"), and writes the total of every
-//      (round, warp) unit of 32 vectors as a float pair;
-//   3. the last CTA of row b (atomic ticket, zeroed by the rowscan pass)
-//      draws: the smallest token id whose cumulative weight exceeds u * S.
-//      One block-wide float-pair scan over all unit totals of the row gives
-//      S and the crossing unit; one warp re-weighs that unit's 32 vectors and
-//      scans them, then the crossing vector's elements.
+// Grid (kCS, B): one thread-block cluster of kCS CTAs per batch row b,
+// launched with programmatic dependent launch so its CTAs start as the
+// rowscan pass drains (inputs they need that the pass does not write are
+// gathered before griddepcontrol.wait). The cluster
+//   1. folds the rowscan partials of b's 2K+1 rows, each row by one of its
+//      kCS x 8 warps, and sends every row's record to all its CTAs through
+//      distributed shared memory; after a cluster barrier each CTA decides
+//      on one warp: r_k = p_k(x_k) / q_k(x_k), x_k kept iff u_k < r_k, left
+//      to right, stopping at the first rejection m (speculative sampling as
+//      summarised on the ariser.io page, section on keeping the same
+//      distribution; lotook.com, step "accept or reject draft tokens"). The
+//      first CTA writes the outputs;
+//   2. weighs row m for the draw that follows, each warp one contiguous
+//      block of its vectors: after a rejection, from max(0, p_m - q_m)
+//      renormalised; after K acceptances, from the bonus position p_K
+//      (lotook.com, step "resampling and the bonus token"). Each warp sends
+//      the totals of its units (runs of consecutive vectors) to the first
+//      CTA's shared memory; a second cluster barrier ends the phase;
+//   3. draws on the first CTA: the smallest token id whose cumulative weight
+//      exceeds u * S. A block-wide float-pair scan over the row's unit totals
+//      gives S and the crossing unit; one warp re-weighs that unit round by
+//      round (32 vectors each), then scans the crossing vector's elements.
 //
 // Arithmetic. The ratio r is formed in fp32 from float-pair normalisers
 // (relative error about 2e-7); when the uniform lies within 1e-5 of r it is
@@ -46,22 +47,6 @@ template <typename Raw>
 __device__ __forceinline__ float logit_at(const void* base, long long row, int V, int v) {
   return Elem<Raw>::at(static_cast<const Raw*>(base) + row * static_cast<long long>(V), v);
 }
-
-// log2 of a positive float pair, absolute error about 4e-8: split off the
-// binary exponent so the rest is near 1, then log1p of the remainder.
-__device__ __forceinline__ float2 ds_log2(float2 x) {
-  int e;
-  float f = frexpf(x.x, &e);  // x.x = f * 2^e, f in [0.5, 1)
-  if (f < 0.70710678f) {
-    f *= 2.f;
-    e -= 1;
-  }
-  const float eps = (f - 1.f) + ldexpf(x.y, -e);  // f - 1 is exact here
-  const float l = log1pf(eps) * 1.44269504088896341f;
-  const float hi = static_cast<float>(e) + l;
-  return make_float2(hi, l - (hi - static_cast<float>(e)));
-}
-
 
 struct Consts {
   float Mp, dM, D_hi, D_lo, c_hi, c_lo;
@@ -128,115 +113,166 @@ __device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
   return make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
 }
 
-template <typename Raw, bool VEC>
-struct Slice {
-  static constexpr int EPV = VEC ? Elem<Raw>::kPerVec : 1;
-  static constexpr long long kSV = static_cast<long long>(kNRS) * kResThreads;  // vectors per slice
+// Cluster geometry. One cluster of kCS CTAs serves one batch row; its kBW
+// warps each weigh one contiguous block of the row's vectors, in batches of
+// kRB rounds of 32 vectors (one per lane), and report kUW unit totals (a
+// unit: G consecutive batches of the block) to the cluster's first CTA.
+constexpr int kCS = 8;
+constexpr int kBW = kCS * kResWarps;
+constexpr int kRB = 4;
+constexpr int kUW = 8;
+constexpr int kNU = kBW * kUW;  // units per batch row, ascending token order
+static_assert(kNU == 512, "the draw gives each lane of one warp 16 units");
 
-  // Weights of vector vi (element order) and their fp32 sum.
-  __device__ static __forceinline__ float one(const Raw* P, const Raw* Q, long long vi, long long nv, const Consts& k,
-                                              float (&w)[EPV]) {
+template <typename Raw, bool VEC>
+struct Block {
+  static constexpr int EPV = VEC ? Elem<Raw>::kPerVec : 1;
+
+  // Target and draft data of vector vi (scalar path: the element's bits in .x).
+  __device__ static __forceinline__ void load1(const Raw* P, const Raw* Q, long long vi, long long nv, const Consts& k,
+                                               uint4& p, uint4& q) {
+    const bool ok = vi < nv, okq = ok && k.mode == 0;
+    if constexpr (VEC) {
+      p = ok ? ld_stream_v4(P + vi * EPV) : make_uint4(0, 0, 0, 0);
+      q = okq ? ld_stream_v4(Q + vi * EPV) : make_uint4(0, 0, 0, 0);
+    } else {
+      p.x = ok ? __float_as_uint(Elem<Raw>::at(P, vi)) : 0u;
+      q.x = okq ? __float_as_uint(Elem<Raw>::at(Q, vi)) : 0u;
+    }
+  }
+
+  // Weights of vector vi from its loaded data (element order; w may be
+  // NULL) and their fp32 sum; zero beyond the row.
+  __device__ static __forceinline__ float weigh1(const uint4& p, const uint4& q, long long vi, long long nv,
+                                                 const Consts& k, float* w) {
     if (vi >= nv) {
+      if (w)
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) w[e] = 0.f;
+        for (int e = 0; e < EPV; ++e) w[e] = 0.f;
       return 0.f;
     }
     if constexpr (VEC) {
-      const uint4 p = ld_stream_v4(P + vi * EPV);
-      const uint4 q = k.mode == 0 ? ld_stream_v4(Q + vi * EPV) : make_uint4(0, 0, 0, 0);
       return vec_weights<Raw>(p, q, k, w);
     } else {
-      w[0] = weight1(Elem<Raw>::at(P, vi), k.mode == 0 ? Elem<Raw>::at(Q, vi) : 0.f, k);
-      return w[0];
+      const float v = weight1(__uint_as_float(p.x), __uint_as_float(q.x), k);
+      if (w) w[0] = v;
+      return v;
     }
   }
 
-  // Per-round vector sums of this thread in slice s (all loads issued first).
-  __device__ static __forceinline__ void sums(const Raw* P, const Raw* Q, int s, int tid, long long nv,
-                                              const Consts& k, float (&vs)[kNRS]) {
-    const long long v0 = s * kSV + tid;
-    if constexpr (VEC) {
-      // two batches of kNRS / 2 rounds: every load of a batch in flight at once,
-      // registers bounded so that four CTAs fit per SM
+  // This lane's share of the unit totals of warp block gw: rounds of 32
+  // vectors (vector gw * nvw + 32 j + lane in round j), G consecutive rounds
+  // per unit, kRB rounds loaded at a time. fp32: the unit totals only choose
+  // the unit the draw walks in float pairs.
+  __device__ static __forceinline__ void lane_units(const Raw* P, const Raw* Q, int gw, int lane, long long nv,
+                                                    long long nvw, int NB, int G, const Consts& k,
+                                                    float (&lu)[kUW]) {
+    const long long v0 = gw * nvw + lane;
+    if (NB * kRB <= kUW) {  // one round per unit
+      static_assert(kUW % kRB == 0, "whole batches per unit array");
 #pragma unroll
-      for (int r0 = 0; r0 < kNRS; r0 += kNRS / 2) {
-        uint4 rp[kNRS / 2], rq[kNRS / 2];
+      for (int bt = 0; bt < kUW / kRB; ++bt) {
+        uint4 p[kRB], q[kRB];
+        const long long vb = v0 + static_cast<long long>(bt) * (kRB * 32);
+        if (bt < NB)
 #pragma unroll
-        for (int r = 0; r < kNRS / 2; ++r) {
-          const long long vi = v0 + (r0 + r) * kResThreads;
-          const bool ok = vi < nv;
-          rp[r] = ok ? ld_stream_v4(P + vi * EPV) : make_uint4(0, 0, 0, 0);
-          rq[r] = (ok && k.mode == 0) ? ld_stream_v4(Q + vi * EPV) : make_uint4(0, 0, 0, 0);
+          for (int t = 0; t < kRB; ++t) load1(P, Q, vb + t * 32, nv, k, p[t], q[t]);
+#pragma unroll
+        for (int t = 0; t < kRB; ++t) lu[bt * kRB + t] = bt < NB ? weigh1(p[t], q[t], vb + t * 32, nv, k, nullptr) : 0.f;
+      }
+      return;
+    }
+#pragma unroll
+    for (int u = 0; u < kUW; ++u) lu[u] = 0.f;
+    const int J = NB * kRB;
+    float acc = 0.f;
+    int u = 0, rend = G;
+#pragma unroll 1
+    for (int bt = 0; bt < NB; ++bt) {
+      uint4 p[kRB], q[kRB];
+      const long long vb = v0 + static_cast<long long>(bt) * (kRB * 32);
+#pragma unroll
+      for (int t = 0; t < kRB; ++t) load1(P, Q, vb + t * 32, nv, k, p[t], q[t]);
+#pragma unroll
+      for (int t = 0; t < kRB; ++t) {
+        acc = __fadd_rn(acc, weigh1(p[t], q[t], vb + t * 32, nv, k, nullptr));
+        const int j = bt * kRB + t;
+        if (j + 1 == rend || j + 1 == J) {  // unit complete (the same for every lane)
+#pragma unroll
+          for (int uu = 0; uu < kUW; ++uu)
+            if (uu == u) lu[uu] = acc;
+          acc = 0.f;
+          ++u;
+          rend += G;
         }
-#pragma unroll
-        for (int r = 0; r < kNRS / 2; ++r)
-          vs[r0 + r] = v0 + (r0 + r) * kResThreads < nv ? vec_weights<Raw>(rp[r], rq[r], k, nullptr) : 0.f;
-      }
-    } else {
-#pragma unroll
-      for (int r = 0; r < kNRS; ++r) {
-        float w[1];
-        vs[r] = one(P, Q, v0 + r * kResThreads, nv, k, w);
       }
     }
-  }
-
-  // Weigh slice s and write the total of every (round, warp) unit as a float
-  // pair to wt[(s * kNRS + round) * warps + warp]. The eight per-round sums
-  // of the warp are reduced by a transposing butterfly: each exchange step
-  // halves the rounds a lane carries, so after three steps lane l holds part
-  // of round l / 4 and two more steps complete it.
-  __device__ static __forceinline__ void publish(const Raw* P, const Raw* Q, int s, int tid, long long nv,
-                                                 const Consts& k, float2* wt) {
-    static_assert(kNRS == 8, "the butterfly below is written for eight rounds");
-    const int lane = tid & 31;
-    float vs[kNRS];
-    sums(P, Q, s, tid, nv, k, vs);
-    float2 r4[4], r2[2];
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float send = b4 ? vs[i] : vs[4 + i];
-      const float keep = b4 ? vs[4 + i] : vs[i];
-      r4[i] = two_sum(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 send = b3 ? r4[i] : r4[2 + i];
-      const float2 keep = b3 ? r4[2 + i] : r4[i];
-      r2[i] = ds_add(keep, shfl_xor2(send, 8));
-    }
-    float2 r1;
-    {
-      const float2 send = b2 ? r2[0] : r2[1];
-      const float2 keep = b2 ? r2[1] : r2[0];
-      r1 = ds_add(keep, shfl_xor2(send, 4));
-    }
-    r1 = ds_add(r1, shfl_xor2(r1, 2));
-    r1 = ds_add(r1, shfl_xor2(r1, 1));
-    if ((lane & 3) == 0) wt[(static_cast<long long>(s) * kNRS + (lane >> 2)) * kResWarps + (tid >> 5)] = r1;
   }
 };
 
-// p(x) / q(x) in fp64 for decisions near the threshold (rarely taken; kept
-// out of line so its code is fetched only when needed).
-__device__ __noinline__ double ratio_fp64(float lp, float Mp, float lq, float Mq, double invT, float2 Zp, float2 Zq) {
-  const double dd = (static_cast<double>(lp) - static_cast<double>(Mp)) - (static_cast<double>(lq) - static_cast<double>(Mq));
-  return exp(dd * invT) * (ds_to_d(Zq) / ds_to_d(Zp));
+// Warp totals of eight floats per lane, as float pairs, by a transposing
+// butterfly: each exchange halves the values a lane carries, so after three
+// steps lane l holds part of value l / 4 and two more steps complete it.
+// Returns the total of value l / 4 (in every lane of the group of four).
+__device__ __forceinline__ float2 butterfly8(const float (&v)[8], int lane) {
+  float2 r4[4], r2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r4[i] = two_sum(b4 ? v[4 + i] : v[i], __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16));
+#pragma unroll
+  for (int i = 0; i < 2; ++i) r2[i] = ds_add(b3 ? r4[2 + i] : r4[i], shfl_xor2(b3 ? r4[i] : r4[2 + i], 8));
+  float2 r1 = ds_add(b2 ? r2[1] : r2[0], shfl_xor2(b2 ? r2[0] : r2[1], 4));
+  r1 = ds_add(r1, shfl_xor2(r1, 2));
+  return ds_add(r1, shfl_xor2(r1, 1));
 }
 
+// ---- thread-block cluster primitives (distributed shared memory)
+__device__ __forceinline__ unsigned cluster_ctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Address of `p` (this CTA's shared memory) in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, unsigned rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, const StatRec& r) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(r.M), "f"(r.Z), "f"(r.Lhi),
+               "f"(r.Llo)
+               : "memory");
+}
+
+// p(x) / q(x) in fp64 for decisions near the threshold (rarely taken; kept
+// out of line so its code is fetched only when needed).
+__device__ __noinline__ double ratio_fp64(float lp, float Mp, float lq, float Mq, double invT, float Zp, float Zq) {
+  const double dd = (static_cast<double>(lp) - static_cast<double>(Mp)) - (static_cast<double>(lq) - static_cast<double>(Mq));
+  return exp(dd * invT) * (static_cast<double>(Zq) / static_cast<double>(Zp));
+}
+
+__device__ __forceinline__ bool row_ok(const StatRec& r) { return isfinite(r.M) && isfinite(r.Z) && r.Z > 0.f; }
+
 // Acceptance decision for batch row b on one warp, from the folded rows rr
-// (target row k at k, draft row k at K + 1 + k) and the gathered inputs.
-// Outputs are written when `write`; the decision goes to *dec.
-__device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane, const RowRec* rr, const float* s_lp,
+// (target row k at k, draft row k at K + 1 + k) and the gathered inputs:
+// lane k forms log2 r_k = (l_p - M_p - l_q + M_q) log2(e) / T + log2 Z_q -
+// log2 Z_p and r_k = 2^that (relative error about 1e-6 at worst; decisions
+// within 1e-5 of the threshold are taken in fp64). Outputs are written when
+// `write`; the decision goes to *dec.
+__device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane, const StatRec* rr, const float* s_lp,
                                           const float* s_lq, const float* s_u, const int* s_x, bool write,
                                           DecRec* dec) {
   const int K = a.K, V = a.V, RPG = 2 * K + 1;
   int st = 0;
-  for (int j = lane; j < RPG; j += 32) {
-    const bool ok = isfinite(rr[j].M) && isfinite(rr[j].Zhi) && rr[j].Zhi > 0.f;
-    if (!ok) st |= j <= K ? SPEC_ROW_TARGET : SPEC_ROW_DRAFT;
-  }
+  for (int j = lane; j < RPG; j += 32)
+    if (!row_ok(rr[j])) st |= j <= K ? SPEC_ROW_TARGET : SPEC_ROW_DRAFT;
   for (int k = lane; k < K; k += 32)
     if (s_x[k] < 0 || s_x[k] >= V) st |= SPEC_ROW_TOKEN;
   st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
@@ -246,26 +282,22 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
     const int k = k0 + lane;
     bool rej = false;
     float2 Dk = make_float2(0.f, 0.f);
-    if (k < K) {
-      if (st == 0) {
-        const RowRec rp = rr[k], rq = rr[K + 1 + k];
-        const float lp = s_lp[k], lq = s_lq[k];
-        const float up = lp - rp.M, uq = lq - rq.M;  // exact for bf16 logits
-        const float2 Zp = make_float2(rp.Zhi, rp.Zlo), Zq = make_float2(rq.Zhi, rq.Zlo);
-        const float u = s_u[k];
-        float r;
-        if (lq == -INFINITY) {
-          r = INFINITY;  // q(x) = 0: accept
-        } else {
-          const float du = up - uq;
-          r = expf(fmaf(du, a.it_hi, du * a.it_lo)) * ds_div(Zq, Zp).x;
-        }
-        if (r < 1.f && fabsf(u - r) < 1e-5f) {  // near the threshold: decide in fp64
-          rej = !(static_cast<double>(u) < ratio_fp64(lp, rp.M, lq, rq.M, a.invT, Zp, Zq));
-        } else {
-          rej = !(u < r);
-        }
-        Dk = ds_log2(ds_div(Zp, Zq));
+    if (k < K && st == 0) {
+      const StatRec rp = rr[k], rq = rr[K + 1 + k];
+      const float lp = s_lp[k], lq = s_lq[k];
+      const float u = s_u[k];
+      Dk = ds_add(make_float2(rp.Lhi, rp.Llo), make_float2(-rq.Lhi, -rq.Llo));
+      float r;
+      if (lq == -INFINITY) {
+        r = INFINITY;  // q(x) = 0: accept
+      } else {
+        const float du = (lp - rp.M) - (lq - rq.M);  // exact for bf16 logits
+        r = ex2_fast(fmaf(du, a.c_hi, du * a.c_lo) - (Dk.x + Dk.y));
+      }
+      if (r < 1.f && fabsf(u - r) < 1e-5f) {  // near the threshold: decide in fp64
+        rej = !(static_cast<double>(u) < ratio_fp64(lp, rp.M, lq, rq.M, a.invT, rp.Z, rq.Z));
+      } else {
+        rej = !(u < r);
       }
     }
     const unsigned msk = __ballot_sync(0xffffffffu, rej);
@@ -291,13 +323,11 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
     d.status = st;
     d.m = m;
     if (st == 0) {
-      const RowRec rp = rr[m];
       d.mode = m < K ? 0 : 1;
-      d.Mp = rp.M;
+      d.Mp = rr[m].M;
       if (m < K) {
-        const RowRec rq = rr[K + 1 + m];
-        d.Mq = rq.M;
-        d.dM = rp.M - rq.M;
+        d.Mq = rr[K + 1 + m].M;
+        d.dM = d.Mp - d.Mq;
         d.D_hi = Dm.x;
         d.D_lo = Dm.y;
       }
@@ -308,21 +338,22 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
 
 // Optional float outputs for batch row b on one warp: lse of every row and
 // p_k(x_k), q_k(x_k) (NaN when the row is flagged).
-__device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane, const RowRec* rr, const float* s_lp,
+__device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane, const StatRec* rr, const float* s_lp,
                                            const float* s_lq, const int* s_x) {
   const int K = a.K, V = a.V, RPG = 2 * K + 1;
   int st = 0;
   for (int j = lane; j < RPG; j += 32)
-    if (!(isfinite(rr[j].M) && isfinite(rr[j].Zhi) && rr[j].Zhi > 0.f)) st = 1;
+    if (!row_ok(rr[j])) st = 1;
   for (int k = lane; k < K; k += 32)
     if (s_x[k] < 0 || s_x[k] >= V) st = 1;
   st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
   for (int k = lane; k < K; k += 32) {
     float pxv = NAN, qxv = NAN;
     if (st == 0) {
-      const float up = s_lp[k] - rr[k].M, uq = s_lq[k] - rr[K + 1 + k].M;
-      pxv = expf(fmaf(up, a.it_hi, up * a.it_lo)) / rr[k].Zhi;
-      qxv = expf(fmaf(uq, a.it_hi, uq * a.it_lo)) / rr[K + 1 + k].Zhi;
+      const StatRec rp = rr[k], rq = rr[K + 1 + k];
+      const float up = s_lp[k] - rp.M, uq = s_lq[k] - rq.M;
+      pxv = ex2_fast(fmaf(up, a.c_hi, up * a.c_lo) - rp.Lhi - rp.Llo);
+      qxv = ex2_fast(fmaf(uq, a.c_hi, uq * a.c_lo) - rq.Lhi - rq.Llo);
     }
     const long long ik = static_cast<long long>(b) * K + k;
     if (a.px) a.px[ik] = pxv;
@@ -330,8 +361,9 @@ __device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane
   }
   if (a.lse_p || a.lse_q) {
     for (int j = lane; j < RPG; j += 32) {
-      const RowRec r = rr[j];
-      const float v = fmaf(r.M, a.it_hi, r.M * a.it_lo) + (logf(r.Zhi) + r.Zlo / r.Zhi);
+      const StatRec r = rr[j];
+      // lse = M / T + ln Z; NaN for a row without a finite softmax
+      const float v = row_ok(r) ? fmaf(r.M, a.it_hi, r.M * a.it_lo) + (r.Lhi + r.Llo) * 0.693147180559945309f : NAN;
       if (j <= K) {
         if (a.lse_p) a.lse_p[static_cast<long long>(b) * (K + 1) + j] = v;
       } else if (a.lse_q) {
@@ -354,45 +386,24 @@ __device__ __forceinline__ float2 warp_scan_ds(float2 x, int lane) {
   return x;
 }
 
-// Block-wide scan of two float pairs per thread (units 2 tid and 2 tid + 1 of
-// a tile of 2 kResThreads units), continuing from `carry`: ex0 / ex1 are the
-// exclusive prefixes of the two units, the return value the tile's end (the
-// same in every thread). Contains __syncthreads: call from every thread.
-__device__ __forceinline__ float2 block_scan2(float2 v0, float2 v1, float2 carry, float2* ex0, float2* ex1,
-                                              float2* sh_w) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float2 x = warp_scan_ds(ds_add(v0, v1), lane);
-  float2 ex = make_float2(__shfl_up_sync(0xffffffffu, x.x, 1), __shfl_up_sync(0xffffffffu, x.y, 1));
-  if (lane == 0) ex = make_float2(0.f, 0.f);
-  if (lane == 31) sh_w[warp] = x;
-  __syncthreads();
-  float2 base = carry, end = carry;
-#pragma unroll
-  for (int w = 0; w < kResWarps; ++w) {
-    const float2 t = sh_w[w];
-    if (w < warp) base = ds_add(base, t);
-    end = ds_add(end, t);
-  }
-  __syncthreads();  // sh_w is reused by the next call
-  *ex0 = ds_add(base, ex);
-  *ex1 = ds_add(*ex0, v0);
-  return end;
-}
-
 }  // namespace
 
 template <typename Raw, bool VEC>
 __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) {
-  using SL = Slice<Raw, VEC>;
-  constexpr int EPV = SL::EPV;
-  constexpr int kTile = 2 * kResThreads;  // units per scan tile
-  const int s = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  using BL = Block<Raw, VEC>;
+  constexpr int EPV = BL::EPV;
+  const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int gw = rank * kResWarps + warp;  // warp of the cluster
   const int K = a.K, RPG = 2 * K + 1;
-  __shared__ RowRec rr[2 * kMaxK + 1];
+  __shared__ StatRec rr[2 * kMaxK + 1];
   __shared__ float s_lp[kMaxK], s_lq[kMaxK], s_u[kMaxK];
   __shared__ int s_x[kMaxK];
   __shared__ DecRec s_dec;
+  __shared__ __align__(16) float2 s_units[kNU];  // first CTA: unit totals of the row
+  __shared__ int s_first;
   griddep_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
+  cluster_arrive();             // every CTA of the cluster is running before any remote store
   // inputs first (the pass this kernel depends on does not write them), so
   // these gathers overlap the end of the streaming pass
   for (int k = tid; k < K; k += kResThreads) {
@@ -405,139 +416,191 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
     s_lq[k] = ok ? logit_at<Raw>(a.Lq, ik, a.V, xk) : 0.f;
   }
   griddep_wait();
-  fold_stats_rows(a.part + static_cast<long long>(b) * RPG * a.P, a.P, warp, kResWarps, RPG, a.c_hi, a.c_lo, lane, rr);
-  __syncthreads();
-  if (warp == 0) decide_chain(a, b, lane, rr, s_lp, s_lq, s_u, s_x, s == 0, &s_dec);
-  if (warp == 1 && s == 0 && (a.px || a.qx || a.lse_p || a.lse_q)) chain_outputs(a, b, lane, rr, s_lp, s_lq, s_x);
+  // 1. fold: cluster warp gw folds rows gw, gw + kBW, ... and sends each
+  //    record to every CTA of the cluster
+  fold_stats_rows(a.part + static_cast<long long>(b) * RPG * a.P, a.P, gw, kBW, RPG, a.c_hi, a.c_lo, lane, rr);
+  __syncwarp();
+  cluster_wait();
+  if (lane < kCS && lane != rank)
+    for (int j = gw; j < RPG; j += kBW) st_cluster(cluster_addr(&rr[j], lane), rr[j]);
+  __syncwarp();
+  cluster_arrive();
+  cluster_wait();
+  // 2. decision (the same in every CTA; the first CTA writes the outputs)
+  if (warp == 0) decide_chain(a, b, lane, rr, s_lp, s_lq, s_u, s_x, rank == 0, &s_dec);
+  if (warp == 1 && rank == 0 && (a.px || a.qx || a.lse_p || a.lse_q)) chain_outputs(a, b, lane, rr, s_lp, s_lq, s_x);
   __syncthreads();
   const DecRec d = s_dec;
-  if (d.status != 0) return;
   const long long V = a.V;
   const long long nv = VEC ? V / EPV : V;
-  const Raw* P = static_cast<const Raw*>(a.Lp) + (static_cast<long long>(b) * (K + 1) + d.m) * V;
-  const Raw* Q = d.mode == 0 ? static_cast<const Raw*>(a.Lq) + (static_cast<long long>(b) * K + d.m) * V : P;
+  const int mm = d.m < 0 ? 0 : d.m;  // flagged rows (m = -1) weigh nothing
+  const Raw* P = static_cast<const Raw*>(a.Lp) + (static_cast<long long>(b) * (K + 1) + mm) * V;
+  const Raw* Q = d.mode == 0 && mm < K ? static_cast<const Raw*>(a.Lq) + (static_cast<long long>(b) * K + mm) * V : P;
   Consts k{d.Mp, d.dM, d.D_hi, d.D_lo, a.c_hi, a.c_lo, d.mode};
-  const int nu = a.NS * kNRS * kResWarps;  // (slice, round, warp) units, ascending token order
-  float2* wt = a.warp_sum + static_cast<long long>(b) * nu;
-
-  __shared__ int s_last;
-  SL::publish(P, Q, s, tid, nv, k, wt);
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(a.res_ticket + b, 1) == a.NS - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // ---- the draw (last CTA of row b)
-  __shared__ float2 sh_w[kResWarps];
-  __shared__ float2 sh_ex[kTile];
-  __shared__ int s_first, s_lastpos;
-  const int ntile = (nu + kTile - 1) / kTile;
-  auto load2 = [&](int tile, float2* v0, float2* v1) {
-    const int i = tile * kTile + 2 * tid;
-    const float4 q = i < nu ? __ldcg(reinterpret_cast<const float4*>(wt + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    *v0 = make_float2(q.x, q.y);
-    *v1 = make_float2(q.z, q.w);
-  };
-  float2 v0, v1, ex0, ex1, S;
-  for (int pass = 0; pass < 2; ++pass) {
-    // S: the end of the scan over every tile (the single tile stays in registers)
-    S = make_float2(0.f, 0.f);
-    for (int tile = 0; tile < ntile; ++tile) {
-      load2(tile, &v0, &v1);
-      S = block_scan2(v0, v1, S, &ex0, &ex1, sh_w);
-    }
-    if (k.mode != 0 || S.x > 0.f) break;
-    // p_m == q_m numerically: draw from p_m (this CTA re-weighs every slice)
-    k.mode = 1;
-    for (int sl = 0; sl < a.NS; ++sl) SL::publish(P, P, sl, tid, nv, k, wt);
-    __syncthreads();
-  }
-  float2 t = ds_mul_f(S, a.ur[b]);
-  int u = -1;
-  float2 base = make_float2(0.f, 0.f), carry = make_float2(0.f, 0.f);
-  int lastpos = -1;
-  float2 lastbase = base;
-  for (int tile = 0; tile < ntile && u < 0; ++tile) {
-    if (ntile > 1) {
-      load2(tile, &v0, &v1);
-      carry = block_scan2(v0, v1, carry, &ex0, &ex1, sh_w);
-    }
-    if (tid == 0) {
-      s_first = INT_MAX;
-      s_lastpos = -1;
-    }
-    sh_ex[2 * tid] = ex0;
-    sh_ex[2 * tid + 1] = ex1;
-    __syncthreads();
-    // first unit with positive weight whose cumulative end exceeds t
-    if (v0.x > 0.f && ds_gt(ds_add(ex0, v0), t)) atomicMin(&s_first, 2 * tid);
-    else if (v1.x > 0.f && ds_gt(ds_add(ex1, v1), t)) atomicMin(&s_first, 2 * tid + 1);
-    if (v1.x > 0.f) atomicMax(&s_lastpos, 2 * tid + 1);
-    else if (v0.x > 0.f) atomicMax(&s_lastpos, 2 * tid);
-    __syncthreads();
-    if (s_first != INT_MAX) {
-      u = tile * kTile + s_first;
-      base = sh_ex[s_first];
-    } else if (s_lastpos >= 0) {
-      lastpos = tile * kTile + s_lastpos;
-      lastbase = sh_ex[s_lastpos];
-    }
-    __syncthreads();
-  }
-  if (u < 0 && lastpos >= 0) {  // rounding left no crossing: the last unit with weight
-    u = lastpos;
-    base = lastbase;
-    t = make_float2(INFINITY, 0.f);
-  }
-  if (tid >= 32) return;
-  int32_t* out = a.out_tokens + static_cast<long long>(b) * (a.K + 1) + d.m;
-  int token = -1;
-  if (u >= 0) {
-    // the unit's 32 vectors, one per lane, then the crossing lane's elements
-    const int sl = u / (kNRS * kResWarps), r = (u / kResWarps) % kNRS, w = u % kResWarps;
-    const long long vi = sl * SL::kSV + static_cast<long long>(r) * kResThreads + w * 32 + lane;
-    float ew[EPV];
-    const float vsum = SL::one(P, Q, vi, nv, k, ew);
-    const float2 incl = ds_add(base, warp_scan_ds(make_float2(vsum, 0.f), lane));
-    float2 cum = make_float2(__shfl_up_sync(0xffffffffu, incl.x, 1), __shfl_up_sync(0xffffffffu, incl.y, 1));
-    if (lane == 0) cum = base;  // cum: the weight before this lane's vector
-    const unsigned hit = __ballot_sync(0xffffffffu, vsum > 0.f && ds_gt(incl, t));
-    const unsigned pos = __ballot_sync(0xffffffffu, vsum > 0.f);
-    const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
-    if (l >= 0 && lane == l) {
-      int pick = -1, lastp = -1;
+  // 3. weigh this warp's block of row m; unit totals go to the first CTA
+  {
+    float lu[kUW];
+    if (d.status == 0) {
+      BL::lane_units(P, Q, gw, lane, nv, a.nvw, a.NB, a.G, k, lu);
+    } else {
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        if (pick < 0 && ew[e] > 0.f) {
-          lastp = e;
-          cum = ds_add(cum, make_float2(ew[e], 0.f));
-          if (ds_gt(cum, t)) pick = e;
-        }
-      }
-      if (pick < 0) pick = lastp;
-      token = pick < 0 ? -1 : static_cast<int>(vi * EPV + pick);
+      for (int u = 0; u < kUW; ++u) lu[u] = 0.f;
     }
-    if (l >= 0) token = __shfl_sync(0xffffffffu, token, l);
+    const float2 ut = butterfly8(lu, lane);
+    if ((lane & 3) == 0) st_cluster(cluster_addr(&s_units[gw * kUW + (lane >> 2)], 0), ut);
+    __syncwarp();
   }
-  if (lane == 0) *out = token;
+  cluster_arrive();
+  cluster_wait();
+  if (rank != 0 || d.status != 0) return;
+
+  // 4. the draw on one warp of the first CTA. Lane l owns units 16 l .. 16 l
+  //    + 15: a warp scan of the lane totals gives S and the crossing lane,
+  //    a scan of that lane's units the crossing unit.
+  constexpr int kUL = kNU / 32;
+  float2 tot = make_float2(0.f, 0.f), incl = tot, S = tot;
+  auto scan_lanes = [&]() {
+    const float4* su4 = reinterpret_cast<const float4*>(s_units) + lane * (kUL / 2);
+    float2 t[kUL / 2];
+#pragma unroll
+    for (int i = 0; i < kUL / 2; ++i) {
+      const float4 q = su4[i];
+      t[i] = ds_add(make_float2(q.x, q.y), make_float2(q.z, q.w));
+    }
+#pragma unroll
+    for (int w = kUL / 4; w > 0; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) t[i] = ds_add(t[i], t[i + w]);
+    tot = t[0];
+    incl = warp_scan_ds(tot, lane);
+    S = make_float2(__shfl_sync(0xffffffffu, incl.x, 31), __shfl_sync(0xffffffffu, incl.y, 31));
+  };
+  if (warp == 0) {
+    scan_lanes();
+    if (lane == 0) s_first = k.mode == 0 && !(S.x > 0.f);
+  }
+  __syncthreads();
+  if (s_first) {
+    // p_m == q_m numerically: draw from p_m (this CTA re-weighs the row)
+    k.mode = 1;
+    for (int g2 = warp; g2 < kBW; g2 += kResWarps) {
+      float lu[kUW];
+      BL::lane_units(P, P, g2, lane, nv, a.nvw, a.NB, a.G, k, lu);
+      const float2 ut = butterfly8(lu, lane);
+      if ((lane & 3) == 0) s_units[g2 * kUW + (lane >> 2)] = ut;
+    }
+    __syncthreads();
+    if (warp == 0) scan_lanes();
+  }
+  if (warp != 0) return;
+  int32_t* out = a.out_tokens + static_cast<long long>(b) * (a.K + 1) + d.m;
+  float2 thr = ds_mul_f(S, a.ur[b]);
+  // first lane (then unit) with positive weight whose cumulative end exceeds
+  // u * S; the last one with weight in case rounding left none
+  float2 exl = make_float2(__shfl_up_sync(0xffffffffu, incl.x, 1), __shfl_up_sync(0xffffffffu, incl.y, 1));
+  if (lane == 0) exl = make_float2(0.f, 0.f);
+  const unsigned hitL = __ballot_sync(0xffffffffu, tot.x > 0.f && ds_gt(incl, thr));
+  const unsigned posL = __ballot_sync(0xffffffffu, tot.x > 0.f);
+  if (!posL) {
+    if (lane == 0) *out = -1;
+    return;
+  }
+  int L;
+  if (hitL) {
+    L = __ffs(hitL) - 1;
+  } else {
+    L = 31 - __clz(posL);
+    thr = make_float2(INFINITY, 0.f);
+  }
+  const float2 lbase = make_float2(__shfl_sync(0xffffffffu, exl.x, L), __shfl_sync(0xffffffffu, exl.y, L));
+  const float2 uvl = lane < kUL ? s_units[L * kUL + lane] : make_float2(0.f, 0.f);
+  const float2 ui = ds_add(lbase, warp_scan_ds(uvl, lane));
+  float2 exu = make_float2(__shfl_up_sync(0xffffffffu, ui.x, 1), __shfl_up_sync(0xffffffffu, ui.y, 1));
+  if (lane == 0) exu = lbase;
+  const unsigned hitU = __ballot_sync(0xffffffffu, lane < kUL && uvl.x > 0.f && ds_gt(ui, thr));
+  const unsigned posU = __ballot_sync(0xffffffffu, lane < kUL && uvl.x > 0.f);
+  int iu;
+  if (hitU) {
+    iu = __ffs(hitU) - 1;
+  } else {
+    iu = 31 - __clz(posU);  // posU != 0: lane L's units hold weight
+    thr = make_float2(INFINITY, 0.f);
+  }
+  const int U = L * kUL + iu;
+  // 5. the unit's rounds on one warp (ascending token order)
+  const int ugw = U / kUW, uu = U % kUW;
+  const int j1 = min((uu + 1) * a.G, a.NB * kRB);
+  float2 carry = make_float2(__shfl_sync(0xffffffffu, exu.x, iu), __shfl_sync(0xffffffffu, exu.y, iu));
+  int token = -1;
+  long long lastv = -1;  // last vector with weight (fallback)
+  for (int j = uu * a.G; j < j1 && token == -1; ++j) {
+    const long long vi = ugw * a.nvw + static_cast<long long>(j) * 32 + lane;
+    uint4 p, q;
+    BL::load1(P, Q, vi, nv, k, p, q);
+    const float vsum = BL::weigh1(p, q, vi, nv, k, nullptr);
+    const float2 incl = ds_add(carry, warp_scan_ds(make_float2(vsum, 0.f), lane));
+    float2 cum = make_float2(__shfl_up_sync(0xffffffffu, incl.x, 1), __shfl_up_sync(0xffffffffu, incl.y, 1));
+    if (lane == 0) cum = carry;  // weight before this lane's vector
+    const unsigned hit = __ballot_sync(0xffffffffu, vsum > 0.f && ds_gt(incl, thr));
+    const unsigned pos = __ballot_sync(0xffffffffu, vsum > 0.f);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      int tk = -1;
+      if (lane == l) {
+        float ew[EPV];
+        BL::weigh1(p, q, vi, nv, k, ew);
+        int lastp = -1;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          if (tk < 0 && ew[e] > 0.f) {
+            lastp = e;
+            cum = ds_add(cum, make_float2(ew[e], 0.f));
+            if (ds_gt(cum, thr)) tk = e;
+          }
+        }
+        if (tk < 0) tk = lastp;
+        tk = tk < 0 ? -1 : static_cast<int>(vi * EPV + tk);
+      }
+      token = __shfl_sync(0xffffffffu, tk, l);
+      if (token < 0) token = -2;  // no element: stop, report none
+    } else {
+      if (pos) lastv = __shfl_sync(0xffffffffu, vi, 31 - __clz(pos));
+      carry = make_float2(__shfl_sync(0xffffffffu, incl.x, 31), __shfl_sync(0xffffffffu, incl.y, 31));
+    }
+  }
+  if (token == -1 && lastv >= 0) {
+    // rounding left no crossing inside the unit: its last element with weight
+    int tk = -1;
+    if (lane == 0) {
+      uint4 p, q;
+      BL::load1(P, Q, lastv, nv, k, p, q);
+      float ew[EPV];
+      BL::weigh1(p, q, lastv, nv, k, ew);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e)
+        if (ew[e] > 0.f) tk = static_cast<int>(lastv * EPV + e);
+    }
+    token = __shfl_sync(0xffffffffu, tk, 0);
+  }
+  if (lane == 0) *out = token < 0 ? -1 : token;
 }
 
-int tail_slices(int V, bool vec, int dtype) {
-  const long long per = static_cast<long long>(kNRS) * kResThreads * (vec ? (dtype == SPEC_BF16 ? 8 : 4) : 1);
-  return static_cast<int>((V + per - 1) / per);
+// Batches of kRB rounds per warp block, rounds per unit and vectors per warp
+// block for a row of nv vectors.
+void tail_geometry(long long nv, int* NB, int* G, long long* nvw) {
+  const long long per = static_cast<long long>(kBW) * kRB * 32;  // vectors per batch over the cluster
+  *NB = static_cast<int>((nv + per - 1) / per);
+  *G = (*NB * kRB + kUW - 1) / kUW;
+  *nvw = static_cast<long long>(*NB) * kRB * 32;
 }
 
 cudaError_t launch_chain_tail(const TailArgs& a, int dtype, bool vec, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>(a.NS), static_cast<unsigned>(a.B)), block(kResThreads);
+  const dim3 grid(kCS, static_cast<unsigned>(a.B)), block(kResThreads);
   if (dtype == SPEC_BF16)
-    return vec ? launch_pdl(chain_tail_kernel<uint16_t, true>, grid, block, st, a)
-               : launch_pdl(chain_tail_kernel<uint16_t, false>, grid, block, st, a);
-  return vec ? launch_pdl(chain_tail_kernel<float, true>, grid, block, st, a)
-             : launch_pdl(chain_tail_kernel<float, false>, grid, block, st, a);
+    return vec ? launch_pdl(chain_tail_kernel<uint16_t, true>, grid, block, st, a, kCS)
+               : launch_pdl(chain_tail_kernel<uint16_t, false>, grid, block, st, a, kCS);
+  return vec ? launch_pdl(chain_tail_kernel<float, true>, grid, block, st, a, kCS)
+             : launch_pdl(chain_tail_kernel<float, false>, grid, block, st, a, kCS);
 }
 
 }  // namespace specv
