@@ -188,9 +188,9 @@ int spec_verify_tree_greedy(const void* node_logits, int dtype, const int32_t* n
 /* Confidence routing over a merged tree.
  *   node_conf device [B][N] fp32 (entry 0, the root, is ignored)
  * Outputs (device): scores [B][2] fp32, the mean confidence of tree 1 (nodes
- * 1..n1) and tree 2 (n1+1..N-1), -inf for an empty tree, summed in fp64 in
- * node order; choice [B] int32, 2 if score_2 > score_1 (compared in fp64)
- * else 1. */
+ * 1..n1) and tree 2 (n1+1..N-1), -inf for an empty tree, summed in fp64
+ * (16 strided partial sums per tree, then combined); choice [B] int32, 2 if
+ * score_2 > score_1 (compared in fp64) else 1. */
 int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* scores, int32_t* choice,
                          void* stream);
 

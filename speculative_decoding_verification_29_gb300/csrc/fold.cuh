@@ -136,4 +136,58 @@ __device__ __forceinline__ RowRec fold_argmax(const float2* pr, int P, int lane)
   return r;
 }
 
+
+// Fold the argmax partials of rows j = first, first + stride, ... (< nrows)
+// at `part` (row j at part + j * P), one warp; lane 0 writes the top index of
+// row j to am[j] (-1 when the row holds NaN or has no maximum) and ORs `bad`
+// into *st for such rows. With at most 4 rows per warp and P <= 64 all loads
+// are issued before any reduction (one memory round trip).
+__device__ __forceinline__ void fold_argmax_rows(const float2* part, int P, int first, int stride, int nrows, int lane,
+                                                 int* am, int* st, int bad) {
+  constexpr int kR = 4;
+  auto put = [&](int j, float v, int i) {
+    const bool b = (v != v) || i == INT_MAX || i < 0;
+    am[j] = b ? -1 : i;
+    if (b) atomicOr(st, bad);
+  };
+  if (P > 64 || first + kR * stride < nrows) {
+    for (int j = first; j < nrows; j += stride) {
+      const RowRec r = fold_argmax(part + static_cast<long long>(j) * P, P, lane);
+      if (lane == 0) put(j, r.M, r.idx);
+    }
+    return;
+  }
+  float2 q[kR][2];
+#pragma unroll
+  for (int i = 0; i < kR; ++i) {
+    const int j = first + i * stride;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int idx = lane + 32 * c;
+      q[i][c] = (j < nrows && idx < P) ? __ldcg(part + static_cast<long long>(j) * P + idx)
+                                       : make_float2(-INFINITY, __int_as_float(INT_MAX));
+    }
+  }
+  float v[kR];
+  int ix[kR];
+#pragma unroll
+  for (int i = 0; i < kR; ++i) {
+    v[i] = q[i][0].x;
+    ix[i] = __float_as_int(q[i][0].y);
+    merge_arg(v[i], ix[i], q[i][1].x, __float_as_int(q[i][1].y));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < kR; ++i) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, v[i], o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, ix[i], o);
+      merge_arg(v[i], ix[i], v2, i2);
+    }
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < kR; ++i)
+      if (first + i * stride < nrows) put(first + i * stride, v[i], ix[i]);
+}
+
 }  // namespace specv

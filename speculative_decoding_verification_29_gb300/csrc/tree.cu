@@ -14,11 +14,16 @@
 namespace specv {
 
 constexpr int kMaxNodes = 1024;
+constexpr int kTreeThreads = 512;
+constexpr int kTreeWarps = kTreeThreads / 32;
+constexpr int kStagedR = 8192;  // retrieve-row entries staged in shared memory
 
-__global__ void __launch_bounds__(kThreads) tree_finish_kernel(TreeArgs a) {
+__global__ void __launch_bounds__(kTreeThreads) tree_finish_kernel(TreeArgs a) {
   const int b = blockIdx.x, tid = threadIdx.x;
   const int N = a.N, D = a.D, Rn = a.Rn;
   __shared__ int am[kMaxNodes];
+  __shared__ int s_tok[kMaxNodes];
+  __shared__ int s_R[kStagedR];
   __shared__ int s_st, s_any;
   __shared__ unsigned s_key;
   if (tid == 0) {
@@ -27,23 +32,25 @@ __global__ void __launch_bounds__(kThreads) tree_finish_kernel(TreeArgs a) {
     s_key = 0u;
   }
   griddep_launch_dependents();
+  // inputs the pass does not write, staged before the wait: node tokens and
+  // (when they fit) the retrieve rows
+  const int32_t* tk = a.tok + static_cast<long long>(b) * N;
+  const int32_t* Rb = a.R + static_cast<long long>(b) * Rn * D;
+  const bool staged = static_cast<long long>(Rn) * D <= kStagedR;
+  for (int i = tid; i < N; i += kTreeThreads) s_tok[i] = tk[i];
+  if (staged)
+    for (int i = tid; i < Rn * D; i += kTreeThreads) s_R[i] = Rb[i];
+  const int32_t* Rs = staged ? s_R : Rb;
   __syncthreads();
   griddep_wait();
   const int lane = tid & 31, warp = tid >> 5;
-  for (int i = warp; i < N; i += kWarps) {  // fold node i's partials (one warp per node)
-    const RowRec r = fold_argmax(a.part + (static_cast<long long>(b) * N + i) * a.P, a.P, lane);
-    if (lane == 0) {
-      const bool bad = (r.M != r.M) || r.idx == INT_MAX || r.idx < 0;
-      am[i] = bad ? -1 : r.idx;
-      if (bad) atomicOr(&s_st, SPEC_ROW_TARGET);
-    }
-  }
-  const int32_t* tk = a.tok + static_cast<long long>(b) * N;
-  for (int i = 1 + tid; i < N; i += kThreads)
-    if (tk[i] < 0 || tk[i] >= a.V) atomicOr(&s_st, SPEC_ROW_TOKEN);
-  const int32_t* Rb = a.R + static_cast<long long>(b) * Rn * D;
-  for (int r = tid; r < Rn; r += kThreads) {
-    const int32_t* row = Rb + static_cast<long long>(r) * D;
+  // fold every node's partials to the target's top token (lowest id on ties)
+  fold_argmax_rows(a.part + static_cast<long long>(b) * N * a.P, a.P, warp, kTreeWarps, N, lane, am, &s_st,
+                   SPEC_ROW_TARGET);
+  for (int i = 1 + tid; i < N; i += kTreeThreads)
+    if (s_tok[i] < 0 || s_tok[i] >= a.V) atomicOr(&s_st, SPEC_ROW_TOKEN);
+  for (int r = tid; r < Rn; r += kTreeThreads) {
+    const int32_t* row = Rs + static_cast<long long>(r) * D;
     int bad = 0;
     if (row[0] == -1) {
       for (int t = 1; t < D; ++t)
@@ -73,13 +80,13 @@ __global__ void __launch_bounds__(kThreads) tree_finish_kernel(TreeArgs a) {
   __syncthreads();
   const int st = s_st;
   if (st == 0) {
-    for (int r = tid; r < Rn; r += kThreads) {
-      const int32_t* row = Rb + static_cast<long long>(r) * D;
+    for (int r = tid; r < Rn; r += kTreeThreads) {
+      const int32_t* row = Rs + static_cast<long long>(r) * D;
       if (row[0] == -1) continue;
       int L = 0;
       for (int t = 1; t < D; ++t) {
         int nd = row[t];
-        if (nd == -1 || tk[nd] != am[row[t - 1]]) break;
+        if (nd == -1 || s_tok[nd] != am[row[t - 1]]) break;
         L = t;
       }
       // larger L first, then the lower row index
@@ -90,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) tree_finish_kernel(TreeArgs a) {
   int32_t* pth = a.path + static_cast<long long>(b) * D;
   int32_t* out = a.out_tokens + static_cast<long long>(b) * D;
   if (st) {
-    for (int t = tid; t < D; t += kThreads) {
+    for (int t = tid; t < D; t += kTreeThreads) {
       pth[t] = -1;
       out[t] = -1;
     }
@@ -104,10 +111,10 @@ __global__ void __launch_bounds__(kThreads) tree_finish_kernel(TreeArgs a) {
   }
   const int L = static_cast<int>(s_key >> 16);
   const int r = 0xFFFF - static_cast<int>(s_key & 0xFFFFu);
-  const int32_t* row = Rb + static_cast<long long>(r) * D;
-  for (int t = tid; t < D; t += kThreads) {
+  const int32_t* row = Rs + static_cast<long long>(r) * D;
+  for (int t = tid; t < D; t += kTreeThreads) {
     pth[t] = t <= L ? row[t] : -1;
-    out[t] = t < L ? tk[row[t + 1]] : (t == L ? am[row[L]] : -1);
+    out[t] = t < L ? s_tok[row[t + 1]] : (t == L ? am[row[L]] : -1);
   }
   if (tid == 0) {
     a.row_status[b] = 0;
@@ -118,34 +125,44 @@ __global__ void __launch_bounds__(kThreads) tree_finish_kernel(TreeArgs a) {
 }
 
 cudaError_t launch_tree_finish(const TreeArgs& a, cudaStream_t st) {
-  return launch_pdl(tree_finish_kernel, dim3(static_cast<unsigned>(a.B)), dim3(kThreads), st, a);
+  return launch_pdl(tree_finish_kernel, dim3(static_cast<unsigned>(a.B)), dim3(kTreeThreads), st, a);
 }
 
-// Mean confidence per drafter tree, summed in fp64 in node order (one lane
-// per tree), compared in fp64.
-__global__ void tree_confidence_kernel(const float* __restrict__ conf, int N, int n1, float* __restrict__ scores,
-                                       int32_t* __restrict__ choice) {
-  const int b = blockIdx.x, lane = threadIdx.x;
-  __shared__ double s[2];
-  if (lane < 2) {
-    const int lo = lane == 0 ? 1 : n1 + 1;
-    const int hi = lane == 0 ? n1 + 1 : N;
-    double acc = 0.0;
-    for (int i = lo; i < hi; ++i) acc += static_cast<double>(conf[static_cast<long long>(b) * N + i]);
-    s[lane] = hi > lo ? acc / (hi - lo) : -static_cast<double>(INFINITY);
-  }
-  __syncwarp();
+// Mean confidence per drafter tree, one warp per batch row: lanes 0-15 sum
+// tree 1's nodes and lanes 16-31 tree 2's in fp64 (strided, then a shuffle
+// reduction within each half), compared in fp64.
+struct ConfArgs {
+  const float* conf;
+  int N, n1;
+  float* scores;
+  int32_t* choice;
+};
+
+__global__ void __launch_bounds__(32) tree_confidence_kernel(ConfArgs a) {
+  const float* conf = a.conf;
+  const int N = a.N, n1 = a.n1;
+  const int b = blockIdx.x, lane = threadIdx.x, half = lane >> 4, hl = lane & 15;
+  griddep_launch_dependents();
+  griddep_wait();  // the node confidences may come from the preceding kernel
+  const int lo = half == 0 ? 1 : n1 + 1;
+  const int hi = half == 0 ? n1 + 1 : N;
+  double acc = 0.0;
+  for (int i = lo + hl; i < hi; i += 16) acc += static_cast<double>(conf[static_cast<long long>(b) * N + i]);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  const double mean = hi > lo ? acc / (hi - lo) : -static_cast<double>(INFINITY);
+  const double s2 = __shfl_sync(0xffffffffu, mean, 16);
   if (lane == 0) {
-    scores[2 * static_cast<long long>(b)] = static_cast<float>(s[0]);
-    scores[2 * static_cast<long long>(b) + 1] = static_cast<float>(s[1]);
-    choice[b] = s[1] > s[0] ? 2 : 1;
+    a.scores[2 * static_cast<long long>(b)] = static_cast<float>(mean);
+    a.scores[2 * static_cast<long long>(b) + 1] = static_cast<float>(s2);
+    a.choice[b] = s2 > mean ? 2 : 1;
   }
 }
 
 cudaError_t launch_tree_confidence(const float* conf, int B, int N, int n1, float* scores, int32_t* choice,
                                    cudaStream_t st) {
-  tree_confidence_kernel<<<B, 32, 0, st>>>(conf, N, n1, scores, choice);
-  return cudaGetLastError();
+  const ConfArgs a{conf, N, n1, scores, choice};
+  return launch_pdl(tree_confidence_kernel, dim3(static_cast<unsigned>(B)), dim3(32), st, a);
 }
 
 }  // namespace specv
