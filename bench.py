@@ -52,6 +52,29 @@ def _dist():
     return ws, rank, local
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank verifies its own batch: the generator seed is offset by the rank."""
+    return seed + rank
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """The slowest rank's time (all ranks get it); x itself when ws == 1."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(units_per_step: float, steps: int, ws: int, total_ms: float) -> float:
+    """Whole-job units per second: every rank does `steps` steps of
+    `units_per_step` units within the slowest rank's time."""
+    return units_per_step * steps * ws / (total_ms / 1e3)
+
+
 # ------------------------------------------------------------- workloads --
 
 def make_workload(name: str, seed: int):
@@ -181,7 +204,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     if ws > 1:
         dist.init_process_group("nccl", device_id=dev)
-    w, cfg = make_workload(args.workload, args.seed + rank)
+    w, cfg = make_workload(args.workload, rank_seed(args.seed, rank))
     name = args.workload
     stream = torch.cuda.current_stream()
     alg = algorithmic_bytes(name, w)
@@ -296,11 +319,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), ws, dev)
 
     # the dominant kernel: the same K steps again with events around the
     # streaming pass (an event between the two stages delays the second one,
@@ -335,16 +354,12 @@ def run_ours(args):
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
         d2h = sum(r.numel() * r.element_size() for r in res)
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
     clk = clocks.stop() if clocks else None
 
     units = units_per_step(name, w)
-    value = units * args.steps * ws / (total_ms / 1e3)
-    e2e_value = units * e2e_steps * ws / e2e_s
+    value = throughput(units, args.steps, ws, total_ms)
+    e2e_value = throughput(units, e2e_steps, ws, e2e_s * 1e3)
     peak, peak_kind = _peaks()
     k1_mean = float(np.mean(k1_ms))
     achieved = alg / (k1_mean / 1e3) / 1e9

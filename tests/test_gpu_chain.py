@@ -41,6 +41,25 @@ def test_chain_temperatures(T):
     compare_chain(gpu_chain(c), oracle_chain(c))
 
 
+@pytest.mark.parametrize("K", [33, 100, 255])
+def test_chain_long_drafts(K):
+    """Drafts longer than one warp of positions, up to the largest K: draft
+    noise small enough that decisions past position 32 matter; with K = 255
+    each warp of the cluster folds more than four rows."""
+    c = gen.chain_zipf(3, K, 512, torch.float32, 1.0, 0.02, seed=K)
+    g, o = gpu_chain(c), oracle_chain(c)
+    compare_chain(g, o)
+    assert o["accept_len"].max() > 32
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_chain_large_vocab(dtype):
+    """V = 300000: units of several rounds in the draw and more than 64
+    streaming partials per row."""
+    c = gen.chain_zipf(3, 2, 300000, dtype, 0.8, 1.0, seed=5)
+    compare_chain(gpu_chain(c), oracle_chain(c))
+
+
 def test_chain_k0_bonus_only():
     c = gen.chain_tiny(3, B=5, K=0, V=777)
     g = gpu_chain(c)
