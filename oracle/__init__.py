@@ -81,6 +81,9 @@ def _declare(lib):
     lib.orc_tree_bruteforce_depth.restype = ctypes.c_int
     lib.orc_tree_confidence.argtypes = [P, i, i, i, P, P, P]
     lib.orc_tree_confidence.restype = None
+    q = ctypes.c_longlong
+    lib.orc_kv_compact.argtypes = [P, i, i, i, i, i, q, q, q, P, P, i, P, P, P, P]
+    lib.orc_kv_compact.restype = None
     return lib
 
 
@@ -261,3 +264,27 @@ def tree_confidence(conf, n1: int, lib=None) -> Dict[str, np.ndarray]:
     out = dict(scores=np.empty((B, 2), np.float64), choice=np.empty(B, np.int32), flags=np.empty(B, np.int32))
     lib.orc_tree_confidence(_ptr(c), B, N, int(n1), _ptr(out["scores"]), _ptr(out["choice"]), _ptr(out["flags"]))
     return out
+
+
+def kv_compact(kv: np.ndarray, P: int, B: int, S: int, W: int, strides, base, acc, path=None, lib=None):
+    """KV-cache compaction of a copy of ``kv`` (any element type; strides in
+    elements: plane, batch row, position). ``path`` [B, D] int32 or None (a
+    chain). Returns (compacted copy, new_len [B], status [B])."""
+    lib = lib or load()
+    out = np.ascontiguousarray(kv).copy()
+    es = out.dtype.itemsize
+    sp, sb, ss = (int(s) for s in strides)
+    base = np.ascontiguousarray(base, dtype=np.int32)
+    acc = np.ascontiguousarray(acc, dtype=np.int32)
+    if path is not None:
+        path = np.ascontiguousarray(path, dtype=np.int32)
+        D = path.shape[1]
+    else:
+        D = 0
+    Lmax = max(1, int(acc.max(initial=0)) + 1, D)
+    tmp = np.empty(Lmax * W * es, np.uint8)
+    new_len = np.empty(B, np.int32)
+    status = np.empty(B, np.int32)
+    lib.orc_kv_compact(_ptr(out), es, P, B, S, W, sp, sb, ss, _ptr(base), None if path is None else _ptr(path), D,
+                       _ptr(acc), _ptr(new_len), _ptr(status), _ptr(tmp))
+    return out, new_len, status

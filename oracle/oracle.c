@@ -19,7 +19,11 @@
  *   - merged-tree verification (TAPS page, methodology: the target scores all
  *     nodes of the merged tree in one pass and the longest accepted path is
  *     kept) and confidence routing (TAPS page, methodology: arithmetic mean of
- *     the nodes' predicted probabilities per drafter tree, higher wins).
+ *     the nodes' predicted probabilities per drafter tree, higher wins);
+ *   - KV-cache compaction after verification (lotook.com, KV-cache section:
+ *     the rejected draft entries are cut from both caches; SubSpec review,
+ *     step "Update KV"): the accepted path's entries are moved to consecutive
+ *     positions and the cache length is cut after them.
  *
  * Readings where the pages are silent (each is listed with its reason in the
  * design notes): a draft token is accepted iff u < p(x)/q(x) with u in [0,1);
@@ -392,5 +396,61 @@ void orc_tree_confidence(const float* conf, int B, int N, int n1, double* scores
     scores[2 * b + 1] = s2;
     choice[b] = s2 > s1 ? 2 : 1;
     flags[b] = (isfinite(s1) && isfinite(s2) && fabs(s1 - s2) < NEAR) ? FL_ROUTE : 0;
+  }
+}
+
+/* KV-cache compaction after verification (lotook.com, section on the KV
+ * cache: once the target rejects the drafts after position m, both models'
+ * caches are cut back to drop the rejected entries; SubSpec review, step
+ * "Update KV": the entries of rejected candidates are removed).
+ *
+ * The cache holds, for plane p (one layer's keys or values) and batch row b,
+ * rows of W elements of es bytes; row s of (p, b) starts at element
+ * p * sp + b * sb + s * ss. The entries this verification step wrote for row
+ * b sit at positions base[b] + i, i the node (or draft position) index. With
+ * accept length L = acc[b] >= 0 and accepted path path[b][0..L] (path[0] = 0,
+ * the root), the result holds at position base + t, for t = 0..L and every
+ * plane, the row the INPUT held at base + path[t]; every other row keeps its
+ * input. new_len[b] = base + L + 1. path == NULL means path[t] = t (a chain:
+ * nothing moves, only the length is cut).
+ *
+ * A row with acc < 0 (flagged by verification) is left alone: new_len = -1,
+ * status 0. A row whose path does not start at 0, is not strictly
+ * increasing, has L >= D, or reaches outside [0, S) is left alone too:
+ * new_len = -1, status ST_TREE. */
+void orc_kv_compact(unsigned char* kv, int es, int P, int B, int S, int W, long long sp, long long sb,
+                    long long ss, const int32_t* base, const int32_t* path, int D, const int32_t* acc,
+                    int32_t* new_len, int32_t* status, unsigned char* tmp) {
+  const size_t rowb = (size_t)W * (size_t)es;
+  for (int b = 0; b < B; ++b) {
+    int L = acc[b];
+    int b0 = base[b];
+    status[b] = 0;
+    new_len[b] = -1;
+    if (L < 0) continue;
+    const int32_t* pr = path ? path + (size_t)b * D : NULL;
+    int ok = b0 >= 0 && (pr == NULL || L < D);
+    if (ok && pr) {
+      if (pr[0] != 0) ok = 0;
+      for (int t = 1; t <= L && ok; ++t)
+        if (pr[t] <= pr[t - 1]) ok = 0;
+    }
+    int last = pr ? (ok ? pr[L] : 0) : L;
+    if (ok && (long long)b0 + last >= S) ok = 0;
+    if (!ok) {
+      status[b] = ST_TREE;
+      continue;
+    }
+    for (int p = 0; p < P; ++p) {
+      unsigned char* plane = kv + ((size_t)p * (size_t)sp + (size_t)b * (size_t)sb) * (size_t)es;
+      /* read every source row first, then write: the result is defined from the input */
+      for (int t = 0; t <= L; ++t) {
+        int src = pr ? pr[t] : t;
+        memcpy(tmp + (size_t)t * rowb, plane + (size_t)(b0 + src) * (size_t)ss * (size_t)es, rowb);
+      }
+      for (int t = 0; t <= L; ++t)
+        memcpy(plane + (size_t)(b0 + t) * (size_t)ss * (size_t)es, tmp + (size_t)t * rowb, rowb);
+    }
+    new_len[b] = b0 + L + 1;
   }
 }

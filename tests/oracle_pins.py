@@ -412,6 +412,126 @@ def pin_confidence(lib):
     assert np.all(np.isneginf(r2["scores"][:, 1])) and list(r2["choice"]) == [1, 1, 1, 1]
 
 
+def _kv_cache(P, B, S, W, fill):
+    """int32 cache [P][B][S][W] with row (p, b, s) = fill(p, b, s) (a W-list)."""
+    kv = np.zeros((P, B, S, W), np.int32)
+    for p in range(P):
+        for b in range(B):
+            for s_ in range(S):
+                kv[p, b, s_] = fill(p, b, s_)
+    return kv
+
+
+def pin_kv_tree(lib, trials=25, seed=0):
+    """After tree verification, compacting the cache leaves at positions
+    base .. base+L the entries of the accepted path in order: the tokens
+    their rows were written for spell the root, then exactly the accepted
+    tokens the verification emitted; nothing else changes and the length
+    becomes base + L + 1 (lotook.com, KV-cache section: the rejected entries
+    are cut; SubSpec review, step "Update KV")."""
+    import torch
+
+    from gen import random_tree_parents, tree_from_parents
+    from gen.workloads import merged_parents
+
+    rng = np.random.default_rng(seed)
+    g = torch.Generator().manual_seed(seed)
+    longest = 0
+    for trial in range(trials):
+        n1, n2 = int(rng.integers(1, 7)), int(rng.integers(0, 7))
+        pm = merged_parents(random_tree_parents(n1, g, max_depth=4, max_children=2),
+                            random_tree_parents(n2, g, max_depth=4, max_children=2))
+        N = len(pm)
+        R, mask, _ = tree_from_parents(pm, width=6)
+        V = 5
+        Lt = rng.normal(0, 1, (1, N, V))
+        a = np.argmax(Lt[0], axis=1)
+        # tokens mostly the target's choice at the parent, so paths get long
+        tok = np.array([0] + [int(a[pm[i]]) if rng.random() < 0.8 else int(rng.integers(0, V)) for i in range(1, N)],
+                       np.int32)
+        r = oracle.verify_tree_greedy(Lt, tok[None], R.numpy()[None], n1, mask=mask.numpy()[None], lib=lib)
+        L = int(r["accept_len"][0])
+        longest = max(longest, L)
+        base, P_, W = int(rng.integers(0, 4)), 3, 4
+        S = base + N + 3
+        kv = _kv_cache(P_, 1, S, W, lambda p, b, s_: [int(tok[s_ - base]) if base <= s_ < base + N else -7, p, s_, 11])
+        out, nl, st = oracle.kv_compact(kv, P_, 1, S, W, (S * W, S * W, W), [base], r["accept_len"], path=r["path"],
+                                        lib=lib)
+        assert st[0] == 0 and nl[0] == base + L + 1
+        emitted = [int(v) for v in r["out_tokens"][0] if v != -1]
+        for p in range(P_):
+            seq = out[p, 0, base:base + L + 1]
+            assert seq[0, 2] == base  # the root stays
+            assert [int(v) for v in seq[1:, 0]] == emitted[:L]  # the accepted tokens, in order
+            assert np.all(seq[:, 1] == p) and np.all(np.diff(seq[:, 2]) > 0)
+            assert np.array_equal(out[p, 0, :base + 1], kv[p, 0, :base + 1])
+            assert np.array_equal(out[p, 0, base + L + 1:], kv[p, 0, base + L + 1:])
+    assert longest >= 3
+
+
+def pin_kv_chain(lib, seed=1):
+    """Chain verification keeps positions base .. base+m: the cache does not
+    move, only the length is cut to base + m + 1."""
+    rng = np.random.default_rng(seed)
+    P_, B, S, W = 2, 5, 20, 2
+    kv = rng.integers(-1000, 1000, (P_, B, S, W)).astype(np.int32)
+    base = rng.integers(0, 8, B).astype(np.int32)
+    acc = np.array([0, 3, 5, -1, 2], np.int32)
+    out, nl, st = oracle.kv_compact(kv, P_, B, S, W, (B * S * W, S * W, W), base, acc, lib=lib)
+    assert np.array_equal(out, kv)
+    assert list(nl) == [int(base[b]) + int(acc[b]) + 1 if acc[b] >= 0 else -1 for b in range(B)]
+    assert list(st) == [0] * B
+
+
+def pin_kv_order(lib):
+    """Each kept row comes from the input, not from a row already moved: the
+    path 0, 2, 3 moves input rows 2 and 3 to positions 1 and 2 (a move done
+    in place from the last position down would copy row 3 twice)."""
+    P_, B, S, W = 1, 1, 6, 1
+    kv = np.arange(S, dtype=np.int32).reshape(P_, B, S, W)
+    out, nl, st = oracle.kv_compact(kv, P_, B, S, W, (S, S, 1), [0], [2], path=np.array([[0, 2, 3]], np.int32), lib=lib)
+    assert [int(v) for v in out[0, 0, :, 0]] == [0, 2, 3, 3, 4, 5] and nl[0] == 3
+
+
+def pin_kv_invalid(lib):
+    """Paths that are not strictly increasing from the root, too long for
+    their width, or reaching past the cache leave the row untouched with
+    status 8 (malformed tree path) and length -1; a row flagged by
+    verification (accept length -1) is left untouched with status 0."""
+    P_, B, S, W, D = 1, 6, 8, 1, 4
+    kv = np.arange(B * S, dtype=np.int32).reshape(P_, B, S, W)
+    path = np.array([[1, 2, -1, -1], [0, 2, 2, -1], [0, 3, 1, -1], [0, 1, 2, 3], [0, 4, 6, -1], [0, 1, -1, -1]],
+                    np.int32)
+    acc = np.array([1, 2, 2, 4, 2, -1], np.int32)
+    base = np.array([0, 0, 0, 0, 3, 0], np.int32)
+    out, nl, st = oracle.kv_compact(kv, P_, B, S, W, (B * S, S, 1), base, acc, path=path, lib=lib)
+    assert np.array_equal(out, kv)
+    assert list(st) == [8, 8, 8, 8, 8, 0] and list(nl) == [-1] * 6
+
+
+def pin_kv_strided(lib, seed=2):
+    """Strided planes (layer and key/value with gaps between them, padded
+    rows): exactly W elements of every kept row move, padding and gaps keep
+    their contents; the result equals a gather of the input rows."""
+    rng = np.random.default_rng(seed)
+    P_, B, S, W, pad = 3, 2, 9, 5, 3
+    ss, sb = W + pad, (W + pad) * S + 7
+    sp = sb * B + 11
+    flat = rng.integers(0, 1 << 15, sp * P_).astype(np.int16)
+    path = np.array([[0, 1, 4, 6], [0, 2, 3, -1]], np.int32)
+    acc = np.array([3, 2], np.int32)
+    base = np.array([1, 2], np.int32)
+    out, nl, st = oracle.kv_compact(flat, P_, B, S, W, (sp, sb, ss), base, acc, path=path, lib=lib)
+    want = flat.copy()
+    for p in range(P_):
+        for b in range(B):
+            for t in range(int(acc[b]) + 1):
+                d = p * sp + b * sb + (int(base[b]) + t) * ss
+                s_ = p * sp + b * sb + (int(base[b]) + int(path[b, t])) * ss
+                want[d:d + W] = flat[s_:s_ + W]
+    assert np.array_equal(out, want) and list(nl) == [5, 5] and list(st) == [0, 0]
+
+
 ALL_PINS = [
     ("ab_example", pin_ab_example),
     ("lossless_V3K2", lambda lib: pin_lossless(lib, 3, 2, 1.0, 1)),
@@ -423,4 +543,9 @@ ALL_PINS = [
     ("tree_bruteforce", pin_tree_bruteforce),
     ("tree_chain_reduction", pin_tree_chain_reduction),
     ("confidence", pin_confidence),
+    ("kv_tree", pin_kv_tree),
+    ("kv_chain", pin_kv_chain),
+    ("kv_order", pin_kv_order),
+    ("kv_invalid", pin_kv_invalid),
+    ("kv_strided", pin_kv_strided),
 ]

@@ -47,6 +47,18 @@ MUTATIONS = {
     "tree_subtree_boundary": ("(row[1] <= n1 ? 1 : 2)", "(row[1] < n1 ? 1 : 2)"),
     "confidence_wrong_count": ("s2 = n2 > 0 ? s2 / n2 : -INFINITY;", "s2 = n2 > 0 ? s2 / n1 : -INFINITY;"),
     "confidence_root_included": ("for (int i = 1; i <= n1; ++i) s1 +=", "for (int i = 0; i <= n1; ++i) s1 +="),
+    "kv_dest_off_by_one": ("memcpy(plane + (size_t)(b0 + t) * (size_t)ss", "memcpy(plane + (size_t)(b0 + t + 1) * (size_t)ss"),
+    "kv_length_short": ("new_len[b] = b0 + L + 1;", "new_len[b] = b0 + L;"),
+    "kv_last_row_kept": (
+        "for (int t = 0; t <= L; ++t)\n        memcpy(plane", "for (int t = 0; t < L; ++t)\n        memcpy(plane"),
+    "kv_first_plane_only": ("for (int p = 0; p < P; ++p) {", "for (int p = 0; p < 1; ++p) {"),
+    "kv_batch_stride_ignored": ("(size_t)b * (size_t)sb) * (size_t)es", "(size_t)b * (size_t)ss) * (size_t)es"),
+    "kv_repeated_node_allowed": ("if (pr[t] <= pr[t - 1]) ok = 0;", "if (pr[t] < pr[t - 1]) ok = 0;"),
+    "kv_in_place_from_last_row": (
+        "      for (int t = 0; t <= L; ++t) {\n        int src = pr ? pr[t] : t;\n        memcpy(tmp + (size_t)t * rowb,",
+        "      for (int t = L; t >= 0; --t) {\n        int src = pr ? pr[t] : t;\n"
+        "        memmove(plane + (size_t)(b0 + t) * (size_t)ss * (size_t)es,"
+        " plane + (size_t)(b0 + src) * (size_t)ss * (size_t)es, rowb);\n        memcpy(tmp + (size_t)t * rowb,"),
 }
 
 
