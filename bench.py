@@ -402,6 +402,158 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------- KV-cache compaction --
+
+KV_PLANES, KV_S, KV_W, KV_SETS = 64, 2048, 1024, 16  # Llama-3-8B: 32 layers x K/V, 8 KV heads x 128
+
+
+def kv_setup(seed: int):
+    """Merged-tree workload (config of the tree bench) and its accepted paths
+    from the oracle's tree verification: the compaction that follows it."""
+    import numpy as np
+
+    import gen
+    import oracle
+
+    tb = gen.config_tree(seed)
+    o = oracle.verify_tree_greedy(tb.Lt, tb.tok, tb.R, tb.n1, mask=tb.mask, threads=os.cpu_count() or 1)
+    acc, path = o["accept_len"].astype(np.int32), o["path"].astype(np.int32)
+    moved_rows = sum(int(np.sum(path[b, 1:acc[b] + 1] != np.arange(1, acc[b] + 1))) for b in range(tb.B) if acc[b] > 0)
+    bases = [np.full(tb.B, 64 + 112 * j, np.int32) for j in range(KV_SETS)]
+    cfg = dict(workload=f"KV-cache compaction after merged-tree verify: B={tb.B} N={tb.N}, cache {KV_PLANES} planes "
+                        f"(32 layers x K/V) x S={KV_S} x {KV_W} bf16 (8 KV heads x 128)",
+               B=tb.B, N=tb.N, planes=KV_PLANES, S=KV_S, W=KV_W, kv="bf16",
+               accepted_tokens=int(acc[acc > 0].sum()), moved_rows_per_plane=moved_rows)
+    bytes_per_step = moved_rows * KV_PLANES * KV_W * 2 * 2  # each moved row read once and written once
+    return tb, acc, path, bases, bytes_per_step, cfg
+
+
+def run_kv(args):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verification_29_gb300 as sv
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    tb, acc, path, bases, bpstep, cfg = kv_setup(rank_seed(args.seed, rank))
+    B = tb.B
+    kv = torch.empty(KV_PLANES, B, KV_S, KV_W, dtype=torch.int16, device=dev)
+    for p in range(KV_PLANES):  # random bits, one plane at a time
+        kv[p].random_(-(1 << 15), 1 << 15)
+    kv = kv.view(torch.bfloat16)
+    acc_d, path_d = torch.as_tensor(acc, device=dev), torch.as_tensor(path, device=dev)
+    base_d = [torch.as_tensor(b_, device=dev) for b_ in bases]
+    out = sv.spec_kv_compact(kv, base_d[0], acc_d, path_d)
+    stream = torch.cuda.current_stream()
+
+    def step_dev(i):  # each step compacts a different region: nothing of the last 15 steps is in L2
+        sv.spec_kv_compact(kv, base_d[i % KV_SETS], acc_d, path_d, out=out)
+
+    for i in range(max(args.warmup, 3)):
+        step_dev(i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak:
+        for i in range(50):
+            step_dev(i)
+        torch.cuda.synchronize()
+    # the K steps captured as one CUDA graph and replayed once: one call takes
+    # a few microseconds on the GPU, less than a host launch through the API,
+    # so eager launches would time the host
+    launch = "cuda_graph (the K steps in one graph)"
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step_dev(0)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                step_dev(i)
+        run = graph.replay
+        run()
+    except Exception as e:
+        launch = f"eager (graph capture failed: {type(e).__name__})"
+
+        def run():
+            for i in range(args.steps):
+                step_dev(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    run()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total_ms = max_over_ranks(start.elapsed_time(end), ws, dev)
+    k_ms = total_ms / args.steps  # one kernel per step: the step time bounds the kernel's duration
+    # end to end: paths, lengths and bases from pinned host memory, lengths back
+    host = [torch.as_tensor(bases[0]).pin_memory(), torch.as_tensor(acc).pin_memory(), torch.as_tensor(path).pin_memory()]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        o = sv.spec_kv_compact(kv, host[0], host[1], host[2])
+        res = [o["new_len"].cpu(), o["row_status"].cpu()]
+    e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
+    clk = clocks.stop() if clocks else None
+    peak, peak_kind = _peaks()
+    gb = bpstep / 1e9
+    line = {
+        "metric": "KV-cache compaction: cache bytes moved/sec (read + write)", "value": gb * args.steps * ws / (total_ms / 1e3),
+        "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (moved as bits)",
+        "data": "synthetic (random cache bits; accepted paths from the oracle's verification of the merged trees)",
+        "config": dict(cfg, parallelism=f"replicas x{ws}", launch=launch,
+                       l2=f"{KV_SETS} cache regions in rotation, {bpstep / 1e6:.1f} MB moved per step; no flush"),
+        "roofline": {"bound": "hbm", "kernel": "kv_compact_kernel", "achieved": gb / (k_ms / 1e3), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": gb / (k_ms / 1e3) / peak, "traffic": None,
+                     "algorithmic_bytes": bpstep, "kernel_ms_mean": k_ms},
+        "e2e": {"value": gb * e2e_steps * ws / e2e_s, "unit": "GB/s",
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+                "d2h_bytes_per_step": sum(r.numel() * r.element_size() for r in res), "steps": e2e_steps},
+        "gpu_launches": args.steps, "clocks": clk,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = kv_cpu_baseline(tb, acc, path, bpstep, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def kv_cpu_baseline(tb, acc, path, bpstep, cpu_seconds, steps=None):
+    """The oracle's compaction of the same paths on a host cache holding the
+    touched positions (one thread)."""
+    import numpy as np
+
+    import oracle
+
+    S = 64 + tb.N + 8
+    kv = np.random.default_rng(0).integers(-(1 << 15), 1 << 15, (KV_PLANES, tb.B, S, KV_W)).astype(np.int16)
+    base = np.full(tb.B, 64, np.int32)
+    reps, t_tot = 0, 0.0
+    while reps < (steps or 1) or (steps is None and t_tot < cpu_seconds / 4 and reps < 20):
+        t0 = time.perf_counter()
+        oracle.kv_compact(kv, KV_PLANES, tb.B, S, KV_W, (tb.B * S * KV_W, S * KV_W, KV_W), base, acc, path=path)
+        t_tot += time.perf_counter() - t0
+        reps += 1
+    return {"value": bpstep / 1e9 * reps / t_tot, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} compactions of a {S}-position host cache with the same paths (the oracle copies the "
+                      f"whole cache each call: {t_tot:.1f} s)"}
+
+
 # ------------------------------------------------------ oracle (CPU) arm --
 
 def _oracle_step(name, w, rows, threads):
@@ -482,6 +634,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kv_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    tb, acc, path, bases, bpstep, cfg = kv_setup(args.seed)
+    b = kv_cpu_baseline(tb, acc, path, bpstep, 0.0, steps=max(1, min(args.steps, 20)))
+    line = {"impl": "reference", "metric": "KV-cache compaction: cache bytes moved/sec (read + write)",
+            "value": b["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (moved as bits)",
+            "data": "synthetic", "config": cfg, "cpu_baseline": b,
+            "e2e": {"value": b["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -489,7 +658,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="chain_batched",
-                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree"])
+                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "kv_compact"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -497,7 +666,12 @@ def main():
     ap.add_argument("--graph", action="store_true", help="replay each step as a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.workload == "kv_compact":
+        if args.impl == "reference":
+            run_kv_reference(args)
+        else:
+            run_kv(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

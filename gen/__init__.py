@@ -23,4 +23,5 @@ from .workloads import (  # noqa: F401
     random_tree_parents,
     tree_from_parents,
     tree_batch,
+    kv_cache,
 )

@@ -348,6 +348,19 @@ def config_tree(seed: int = 0, B: int = 16) -> TreeBatch:
     return tree_batch(B, 30, 128256, torch.bfloat16, seed, name="tree_merged")
 
 
+def kv_cache(P: int, B: int, S: int, W: int, dtype: torch.dtype = torch.bfloat16, seed: int = 0,
+             pad: int = 0) -> torch.Tensor:
+    """Synthetic KV cache: [P, B, S, W + pad] of random bit patterns (P
+    planes, e.g. layers x keys/values; rows of W elements plus ``pad`` unused
+    ones). Compaction moves bits, so any pattern is a valid entry."""
+    g = _gen(seed)
+    es = torch.empty((), dtype=dtype).element_size()
+    idt = {1: torch.int8, 2: torch.int16, 4: torch.int32, 8: torch.int64}[es]
+    lo, hi = (-(1 << 7), 1 << 7) if es == 1 else (-(1 << 15), 1 << 15)
+    bits = torch.randint(lo, hi, (P, B, S, W + pad), generator=g, dtype=torch.int64).to(idt)
+    return bits.view(dtype)
+
+
 CONFIGS: Dict[str, Callable] = {
     "chain_tiny": chain_tiny,
     "chain_single": config_chain_single,

@@ -22,6 +22,9 @@
  *   - spec_tree_confidence: confidence routing, the arithmetic mean of the
  *     nodes' drafter confidences per tree, higher wins (TAPS page,
  *     methodology, confidence routing).
+ *   - spec_kv_compact: after verification, keep the accepted entries of the
+ *     KV cache at consecutive positions and cut the length after them
+ *     (lotook.com, KV-cache section; SubSpec review, step "Update KV").
  *
  * Conventions shared by every call.
  *   - Pointers marked "device" are device pointers owned by the caller; the
@@ -193,6 +196,44 @@ int spec_verify_tree_greedy(const void* node_logits, int dtype, const int32_t* n
  * score_2 > score_1 (compared in fp64) else 1. */
 int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* scores, int32_t* choice,
                          void* stream);
+
+/* KV-cache compaction after a verification step (lotook.com, section on the
+ * KV cache: when the target rejects the drafts after position m, both
+ * models' caches are cut back to drop the rejected entries; SubSpec review,
+ * Method 2, step "Update KV": the entries of rejected candidates are
+ * removed). No counterpart beyond that: the layout and the in-place gather
+ * are this library's.
+ *
+ * The verification pass wrote, for batch row b, the entry of node i (tree)
+ * or draft position i (chain) at position base_pos[b] + i. This call keeps
+ * the accepted ones: for t = 0..L (L = accept_len[b]) position base + t
+ * receives the entry the cache held at base + path[b][t], in every plane,
+ * and new_len[b] = base + L + 1. Other positions are not touched (entries
+ * past new_len are dead). In place.
+ *   kv            device, the cache. Plane p (for example one layer's keys or
+ *                 values), batch row b, position s is the row of W elements
+ *                 of elem_bytes bytes (1, 2, 4 or 8) starting at element
+ *                 p * stride_plane + b * stride_batch + s * stride_pos; rows
+ *                 must not overlap (stride_pos >= W). Moves are 16 bytes wide
+ *                 when kv, the row size and every stride are multiples of 16
+ *                 bytes, else 4, else 1.
+ *   base_pos      device [B] int32, the position of node 0 (the root)
+ *   path          device [B][D] int32 or NULL: the accepted path written by
+ *                 spec_verify_tree_greedy (path[0] = 0, strictly increasing);
+ *                 NULL for chain verification, where path[t] = t and nothing
+ *                 moves (1 <= D <= 1024)
+ *   accept_len    device [B] int32, the accepted length L of the same call
+ * Outputs (device): new_len [B] int32; row_status [B] int32.
+ * A row with accept_len < 0 (flagged by verification) is left alone:
+ * new_len -1, status 0. A row whose path does not start at 0, is not
+ * strictly increasing, has L >= D or reaches position S or beyond (or whose
+ * base is negative) is left alone: new_len -1, status SPEC_ROW_TREE.
+ * Errors: SPEC_ERR_ARG for NULL pointers, sizes < 1, elem_bytes not 1/2/4/8,
+ * negative strides or stride_pos < W; SPEC_ERR_UNSUPPORTED for B > 65535 or
+ * D > 1024. */
+int spec_kv_compact(void* kv, int elem_bytes, int n_planes, int B, int S, int W, long long stride_plane,
+                    long long stride_batch, long long stride_pos, const int32_t* base_pos, const int32_t* path, int D,
+                    const int32_t* accept_len, int32_t* new_len, int32_t* row_status, void* stream);
 
 /* Static description of a return code. */
 const char* spec_status_string(int status);

@@ -191,3 +191,33 @@ def spec_tree_confidence(node_conf, n1: int, out: Optional[Dict[str, torch.Tenso
                                   _stream(stream))
     check("spec_tree_confidence", rc)
     return out
+
+
+def spec_kv_compact(kv: torch.Tensor, base_pos, accept_len, path=None, out: Optional[Dict[str, torch.Tensor]] = None,
+                    stream=None) -> Dict[str, torch.Tensor]:
+    """KV-cache compaction after verification, in place on ``kv``.
+
+    kv: a CUDA tensor viewed as [planes, B, S, W] (any strides, last dimension
+    contiguous), for example a [layers * 2, B, S, heads * head_dim] cache.
+    base_pos [B] int32: position of node 0; accept_len [B] int32 and path
+    [B, D] int32 (None for chain verification) as returned by the
+    verification call. Returns new_len [B] and row_status [B]."""
+    lib = _lib.load()
+    if kv.device.type != "cuda":
+        raise ValueError("kv must be a CUDA tensor (it is compacted in place)")
+    if kv.dim() != 4 or kv.stride(3) != 1:
+        raise ValueError("kv must be viewed as [planes, B, S, W] with a contiguous last dimension")
+    P_, B, S, W = kv.shape
+    sp, sb, ss, _ = kv.stride()
+    dev = kv.device
+    base = _dev(torch.as_tensor(base_pos), dev, torch.int32)
+    acc = _dev(torch.as_tensor(accept_len), dev, torch.int32)
+    pth = None if path is None else _dev(torch.as_tensor(path), dev, torch.int32)
+    if out is None:
+        out = dict(new_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+    D = 0 if pth is None else pth.shape[1]
+    check("spec_kv_compact", lib.spec_kv_compact(kv.data_ptr(), kv.element_size(), P_, B, S, W, sp, sb, ss,
+                                                 _ptr(base), _ptr(pth), D, _ptr(acc), _ptr(out["new_len"]),
+                                                 _ptr(out["row_status"]), _stream(stream)))
+    return out

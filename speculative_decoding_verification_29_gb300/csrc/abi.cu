@@ -303,6 +303,42 @@ int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* sc
   return cuda_status(launch_tree_confidence(node_conf, B, N, n1, scores, choice, static_cast<cudaStream_t>(stream)));
 }
 
+int spec_kv_compact(void* kv, int elem_bytes, int n_planes, int B, int S, int W, long long stride_plane,
+                    long long stride_batch, long long stride_pos, const int32_t* base_pos, const int32_t* path, int D,
+                    const int32_t* accept_len, int32_t* new_len, int32_t* row_status, void* stream) {
+  if (!kv || !base_pos || !accept_len || !new_len || !row_status) return SPEC_ERR_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) return SPEC_ERR_ARG;
+  if (n_planes < 1 || B < 1 || S < 1 || W < 1) return SPEC_ERR_ARG;
+  if (stride_plane < 0 || stride_batch < 0 || stride_pos < W) return SPEC_ERR_ARG;
+  if (path && D < 1) return SPEC_ERR_ARG;
+  if (B > kMaxB || (path && D > kv_max_path())) return SPEC_ERR_UNSUPPORTED;
+  const long long row_bytes = static_cast<long long>(W) * elem_bytes;
+  auto fits = [&](long long u) {
+    return reinterpret_cast<uintptr_t>(kv) % u == 0 && row_bytes % u == 0 && (stride_plane * elem_bytes) % u == 0 &&
+           (stride_batch * elem_bytes) % u == 0 && (stride_pos * elem_bytes) % u == 0;
+  };
+  const int unit = fits(16) ? 16 : (fits(4) ? 4 : 1);
+  const long long ncol = row_bytes / unit;
+  if (ncol * n_planes > 0x7fffffffLL * 256LL || ncol > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+  KvArgs a{};
+  a.kv = kv;
+  a.es = elem_bytes;
+  a.P = n_planes;
+  a.B = B;
+  a.S = S;
+  a.ncol = static_cast<int>(ncol);
+  a.sp = stride_plane;
+  a.sb = stride_batch;
+  a.ss = stride_pos;
+  a.base = base_pos;
+  a.path = path;
+  a.D = path ? D : 0;
+  a.acc = accept_len;
+  a.new_len = new_len;
+  a.row_status = row_status;
+  return cuda_status(launch_kv_compact(a, unit, static_cast<cudaStream_t>(stream)));
+}
+
 const char* spec_status_string(int status) {
   switch (status) {
     case SPEC_OK:

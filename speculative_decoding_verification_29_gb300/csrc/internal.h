@@ -132,6 +132,23 @@ cudaError_t launch_tree_finish(const TreeArgs& a, cudaStream_t st);
 cudaError_t launch_tree_confidence(const float* conf, int B, int N, int n1, float* scores, int32_t* choice,
                                    cudaStream_t st);
 
+// KV-cache compaction after verification.
+struct KvArgs {
+  void* kv;
+  int es;              // element bytes
+  int P, B, S;         // planes, batch rows, positions
+  int ncol;            // column slices per row (row bytes / unit)
+  long long sp, sb, ss;  // strides in elements: plane, batch row, position
+  const int32_t* base;   // [B] position of node 0
+  const int32_t* path;   // [B][D] or NULL (chain)
+  int D;
+  const int32_t* acc;    // [B] accept lengths
+  int32_t* new_len;      // [B]
+  int32_t* row_status;   // [B]
+};
+int kv_max_path();
+cudaError_t launch_kv_compact(const KvArgs& a, int unit, cudaStream_t st);
+
 // Launch `kernel` so that it may start while the preceding kernel in the
 // stream drains; the kernel calls griddep_wait() before reading its outputs.
 // cluster > 1 groups that many consecutive CTAs along x into a cluster.

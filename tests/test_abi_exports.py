@@ -29,7 +29,7 @@ def declared():
 def test_header_declares_the_boundary():
     names = declared()
     for n in ("spec_verify_chain", "spec_verify_chain_greedy", "spec_verify_tree_greedy", "spec_tree_confidence",
-              "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample"):
+              "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample", "spec_kv_compact"):
         assert n in names
 
 
@@ -79,4 +79,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.spec_verify_tree_greedy(fake, 1, fake, fake, n, 1, 5000, 2, 3, 16, 5, fake, fake, fake, fake, fake,
                                        fake, fake, 1 << 30, n) == SPEC_ERR_UNSUPPORTED
     assert lib.spec_tree_confidence(fake, 1, 5, 9, fake, fake, n) == SPEC_ERR_ARG
+    # KV compaction: NULL cache, element size, overlapping rows, negative stride, path width
+    kv = lambda *a: lib.spec_kv_compact(*a)
+    assert kv(n, 2, 4, 2, 64, 128, 16384, 8192, 128, fake, n, 0, fake, fake, fake, n) == SPEC_ERR_ARG
+    assert kv(fake, 3, 4, 2, 64, 128, 16384, 8192, 128, fake, n, 0, fake, fake, fake, n) == SPEC_ERR_ARG
+    assert kv(fake, 2, 4, 2, 64, 128, 16384, 8192, 64, fake, n, 0, fake, fake, fake, n) == SPEC_ERR_ARG
+    assert kv(fake, 2, 4, 2, 64, 128, -1, 8192, 128, fake, n, 0, fake, fake, fake, n) == SPEC_ERR_ARG
+    assert kv(fake, 2, 4, 2, 64, 128, 16384, 8192, 128, fake, fake, 0, fake, fake, fake, n) == SPEC_ERR_ARG
+    assert kv(fake, 2, 4, 2, 64, 128, 16384, 8192, 128, fake, fake, 2000, fake, fake, fake, n) == SPEC_ERR_UNSUPPORTED
+    assert kv(fake, 2, 4, 70000, 64, 128, 16384, 8192, 128, fake, n, 0, fake, fake, fake, n) == SPEC_ERR_UNSUPPORTED
     assert lib.spec_status_string(-2) == b"workspace missing, misaligned or too small"
