@@ -84,6 +84,8 @@ def _declare(lib):
     q = ctypes.c_longlong
     lib.orc_kv_compact.argtypes = [P, i, i, i, i, i, q, q, q, P, P, i, P, P, P, P]
     lib.orc_kv_compact.restype = None
+    lib.orc_tree_entropy.argtypes = [P, i, i, i, i, d, i, P, P, P, P, P]
+    lib.orc_tree_entropy.restype = None
     return lib
 
 
@@ -288,3 +290,17 @@ def kv_compact(kv: np.ndarray, P: int, B: int, S: int, W: int, strides, base, ac
     lib.orc_kv_compact(_ptr(out), es, P, B, S, W, sp, sb, ss, _ptr(base), None if path is None else _ptr(path), D,
                        _ptr(acc), _ptr(new_len), _ptr(status), _ptr(tmp))
     return out, new_len, status
+
+
+def tree_entropy(Ld, n1: int, T: float = 1.0, lib=None) -> Dict[str, np.ndarray]:
+    """Entropy routing over a merged tree's drafter logits [B, N, V]: per-node
+    entropies [B, N] (root NaN), per-tree mean scores [B, 2], choice [B]
+    (lower mean entropy wins, ties to 1), status [B], flags [B]."""
+    lib = lib or load()
+    L, dt = _logits(Ld)
+    B, N, V = L.shape
+    out = dict(entropy=np.empty((B, N), np.float64), scores=np.empty((B, 2), np.float64),
+               choice=np.empty(B, np.int32), status=np.empty(B, np.int32), flags=np.empty(B, np.int32))
+    lib.orc_tree_entropy(_ptr(L), dt, B, N, V, float(T), int(n1), _ptr(out["entropy"]), _ptr(out["scores"]),
+                         _ptr(out["choice"]), _ptr(out["status"]), _ptr(out["flags"]))
+    return out

@@ -20,6 +20,8 @@
  *     nodes of the merged tree in one pass and the longest accepted path is
  *     kept) and confidence routing (TAPS page, methodology: arithmetic mean of
  *     the nodes' predicted probabilities per drafter tree, higher wins);
+ *   - entropy routing, the signal the TAPS page compares confidence routing
+ *     with: mean drafter entropy per tree, lower wins;
  *   - KV-cache compaction after verification (lotook.com, KV-cache section:
  *     the rejected draft entries are cut from both caches; SubSpec review,
  *     step "Update KV"): the accepted path's entries are moved to consecutive
@@ -452,5 +454,59 @@ void orc_kv_compact(unsigned char* kv, int es, int P, int B, int S, int W, long 
         memcpy(plane + (size_t)(b0 + t) * (size_t)ss * (size_t)es, tmp + (size_t)t * rowb, rowb);
     }
     new_len[b] = b0 + L + 1;
+  }
+}
+
+/* Entropy routing, the signal the TAPS page compares confidence routing
+ * against (methodology and results: confidence picks the right drafter far
+ * more reliably than entropy). Reading: the entropy of drafter node i is that
+ * of its next-token distribution softmax(l / T) over the vocabulary,
+ * H_i = -sum_v p_v ln p_v = ln Z - sum_v p_v (s_v - M) with s = l / T,
+ * M = max s; a tree's score is the arithmetic mean of its non-root nodes'
+ * entropies (tree 1: 1..n1, tree 2: n1+1..N-1; an empty tree scores +inf);
+ * the lower score wins, ties to tree 1: choice = 2 if score_2 < score_1.
+ * Ld: [B][N][V] logits (root row ignored); ent: [B][N] (root: NaN).
+ * status: ST_DRAFT when a non-root node row holds a NaN or has no finite
+ * maximum (scores NaN, choice -1). flags: FL_ROUTE when both scores are
+ * finite and |score_1 - score_2| < NEAR_H. */
+#define NEAR_H 1e-5
+void orc_tree_entropy(const void* Ld, int dt, int B, int N, int V, double T, int n1, double* ent, double* scores,
+                      int32_t* choice, int32_t* status, int32_t* flags) {
+  for (int b = 0; b < B; ++b) {
+    int st = 0;
+    double* e = ent + (size_t)b * N;
+    e[0] = NAN;
+    for (int i = 1; i < N; ++i) {
+      size_t off = ((size_t)b * N + i) * (size_t)V;
+      double M, Z;
+      if (softmax_stats(Ld, dt, off, V, T, &M, &Z)) {
+        st |= ST_DRAFT;
+        e[i] = NAN;
+        continue;
+      }
+      double y = 0.0; /* sum_v exp(s_v - M) (s_v - M) */
+      for (int v = 0; v < V; ++v) {
+        double d = elem(Ld, dt, off + (size_t)v) / T - M;
+        if (d > -INFINITY) y += exp(d) * d;
+      }
+      e[i] = log(Z) - y / Z;
+    }
+    status[b] = st;
+    flags[b] = 0;
+    if (st) {
+      scores[2 * b] = scores[2 * b + 1] = NAN;
+      choice[b] = -1;
+      continue;
+    }
+    double s1 = 0.0, s2 = 0.0;
+    for (int i = 1; i <= n1; ++i) s1 += e[i];
+    for (int i = n1 + 1; i < N; ++i) s2 += e[i];
+    int n2 = N - 1 - n1;
+    s1 = n1 > 0 ? s1 / n1 : INFINITY;
+    s2 = n2 > 0 ? s2 / n2 : INFINITY;
+    scores[2 * b] = s1;
+    scores[2 * b + 1] = s2;
+    choice[b] = s2 < s1 ? 2 : 1;
+    if (isfinite(s1) && isfinite(s2) && fabs(s1 - s2) < NEAR_H) flags[b] = FL_ROUTE;
   }
 }

@@ -532,6 +532,58 @@ def pin_kv_strided(lib, seed=2):
     assert np.array_equal(out, want) and list(nl) == [5, 5] and list(st) == [0, 0]
 
 
+def pin_entropy(lib, seed=3):
+    """Per-node drafter entropy: ln V for a flat row, 0 for a one-hot row,
+    the binary entropy for two finite logits, scipy's entropy of the softmax
+    for random rows at several temperatures (TAPS page: the entropy signal
+    that confidence routing is compared with)."""
+    from scipy.special import softmax
+    from scipy.stats import entropy
+
+    rng = np.random.default_rng(seed)
+    V = 37
+    rows = [np.zeros(V), np.full(V, -np.inf), np.full(V, -np.inf)]
+    rows[1][5] = 2.0
+    rows[2][3], rows[2][30] = 1.25, -0.5
+    for _ in range(5):
+        rows.append(rng.normal(0, 3, V))
+    Ld = np.stack([np.zeros(V)] + rows)[None]  # root row first (ignored)
+    for T in (1.0, 0.4, 2.5):
+        r = oracle.tree_entropy(Ld, n1=3, T=T, lib=lib)
+        e = r["entropy"][0]
+        assert np.isnan(e[0]) and r["status"][0] == 0
+        assert abs(e[1] - np.log(V)) < 1e-12 and abs(e[2]) < 1e-15
+        p = 1.0 / (1.0 + np.exp(-(1.25 + 0.5) / T))
+        assert abs(e[3] - (-p * np.log(p) - (1 - p) * np.log(1 - p))) < 1e-12
+        for i in range(4, len(rows) + 1):
+            assert abs(e[i] - entropy(softmax(rows[i - 1] / T))) < 1e-11
+        # tree scores: means over nodes 1..3 and 4..N-1, lower wins
+        s1, s2 = np.mean(e[1:4]), np.mean(e[4:])
+        assert abs(r["scores"][0, 0] - s1) < 1e-12 and abs(r["scores"][0, 1] - s2) < 1e-12
+        assert r["choice"][0] == (2 if s2 < s1 else 1)
+
+
+def pin_entropy_routing(lib):
+    """Routing decisions: the tree with the lower mean entropy, ties to tree
+    1, an empty tree never chosen over a non-empty one, NaN rows flagged."""
+    V = 8
+    flat, peaked = np.zeros(V), np.array([4.0] + [0.0] * (V - 1))
+    Ld = np.stack([flat, flat, flat, peaked, peaked])[None]
+    assert oracle.tree_entropy(Ld, n1=2, lib=lib)["choice"][0] == 2  # tree 2 is more certain
+    Ld2 = np.stack([flat, peaked, peaked, flat, flat])[None]
+    assert oracle.tree_entropy(Ld2, n1=2, lib=lib)["choice"][0] == 1
+    tie = oracle.tree_entropy(np.stack([flat, peaked, peaked])[None], n1=1, lib=lib)
+    assert tie["choice"][0] == 1 and tie["flags"][0] == 4
+    e1 = oracle.tree_entropy(np.stack([flat, peaked, flat])[None], n1=2, lib=lib)  # tree 2 empty
+    assert e1["choice"][0] == 1 and np.isinf(e1["scores"][0, 1])
+    e2 = oracle.tree_entropy(np.stack([flat, flat, peaked])[None], n1=0, lib=lib)  # tree 1 empty
+    assert e2["choice"][0] == 2 and np.isinf(e2["scores"][0, 0])
+    bad = np.stack([flat, flat, flat])
+    bad[2, 1] = np.nan
+    r = oracle.tree_entropy(bad[None], n1=1, lib=lib)
+    assert r["status"][0] == 4 and r["choice"][0] == -1
+
+
 ALL_PINS = [
     ("ab_example", pin_ab_example),
     ("lossless_V3K2", lambda lib: pin_lossless(lib, 3, 2, 1.0, 1)),
@@ -548,4 +600,6 @@ ALL_PINS = [
     ("kv_order", pin_kv_order),
     ("kv_invalid", pin_kv_invalid),
     ("kv_strided", pin_kv_strided),
+    ("entropy", pin_entropy),
+    ("entropy_routing", pin_entropy_routing),
 ]

@@ -54,6 +54,12 @@ MUTATIONS = {
     "kv_first_plane_only": ("for (int p = 0; p < P; ++p) {", "for (int p = 0; p < 1; ++p) {"),
     "kv_batch_stride_ignored": ("(size_t)b * (size_t)sb) * (size_t)es", "(size_t)b * (size_t)ss) * (size_t)es"),
     "kv_repeated_node_allowed": ("if (pr[t] <= pr[t - 1]) ok = 0;", "if (pr[t] < pr[t - 1]) ok = 0;"),
+    "entropy_sign": ("e[i] = log(Z) - y / Z;", "e[i] = log(Z) + y / Z;"),
+    "entropy_temperature_dropped": ("double d = elem(Ld, dt, off + (size_t)v) / T - M;",
+                                    "double d = elem(Ld, dt, off + (size_t)v) - M;"),
+    "entropy_higher_wins": ("choice[b] = s2 < s1 ? 2 : 1;", "choice[b] = s2 > s1 ? 2 : 1;"),
+    "entropy_root_included": ("for (int i = 1; i <= n1; ++i) s1 += e[i];", "for (int i = 0; i <= n1; ++i) s1 += e[i];"),
+    "entropy_empty_tree_zero": ("s2 = n2 > 0 ? s2 / n2 : INFINITY;", "s2 = n2 > 0 ? s2 / n2 : 0.0;"),
     "kv_in_place_from_last_row": (
         "      for (int t = 0; t <= L; ++t) {\n        int src = pr ? pr[t] : t;\n        memcpy(tmp + (size_t)t * rowb,",
         "      for (int t = L; t >= 0; --t) {\n        int src = pr ? pr[t] : t;\n"
