@@ -100,11 +100,16 @@ def make_workload(name: str, seed: int):
         t = gen.config_tree(seed)
         return t, dict(workload="merged-tree greedy verify + confidence routing: B=16 N=61 V=128256 bf16", B=16,
                        N=61, V=128256, logits="bf16")
+    if name == "entropy":
+        t = gen.config_tree(seed)
+        t.Ld = gen.tree_draft_logits(t, seed)
+        return t, dict(workload="entropy routing of merged drafter trees: B=16 N=61 V=128256 bf16 drafter logits, T=1",
+                       B=16, N=61, V=128256, logits="bf16", temperature=1.0)
     raise SystemExit(f"unknown workload {name}")
 
 
 def units_per_step(name, w):
-    if name == "tree":
+    if name in ("tree", "entropy"):
         return w.B * (w.N - 1)  # verified nodes
     return w.B * w.K  # verified draft positions
 
@@ -112,8 +117,8 @@ def units_per_step(name, w):
 def algorithmic_bytes(name, w):
     """Logit bytes the dominant kernel (the rowscan pass) must read per
     launch: every row once."""
-    es = w.Lt.element_size() if name == "tree" else w.Lp.element_size()
-    if name == "tree":
+    es = w.Lt.element_size() if name in ("tree", "entropy") else w.Lp.element_size()
+    if name in ("tree", "entropy"):
         return w.B * w.N * w.V * es
     if name == "greedy" or w.T == 0.0:
         return w.B * (w.K + 1) * w.V * es
@@ -212,7 +217,23 @@ def run_ours(args):
     # steps never find their logits in L2
     n_sets = max(1, -(-2 * L2_BYTES // alg)) if alg < 2 * L2_BYTES else 1
 
-    if name == "tree":
+    if name == "entropy":
+        sets = [w.Ld.to(dev) for _ in range(n_sets)]
+        ws_t = sv.alloc_workspace(sv.workspace_bytes(w.B, w.N, w.V, w.Ld.dtype), dev)
+        out = sv.spec_tree_entropy(sets[0], w.n1, 1.0, workspace=ws_t)
+
+        def step_dev(i):
+            sv.spec_tree_entropy(sets[i % n_sets], w.n1, 1.0, out=out, workspace=ws_t)
+
+        def step_split(i, ev):
+            ev[0].record(stream)
+            sv.spec_tree_entropy(sets[i % n_sets], w.n1, 1.0, out=out, workspace=ws_t)
+            ev[1].record(stream)
+
+        launches_per_step = 2
+        timed_kernel = "rowscan_kernel (entropy) + tree_entropy_kernel (one call)"
+        host = [w.Ld]
+    elif name == "tree":
         sets = [tuple(t.to(dev) for t in (w.Lt, w.tok, w.R, w.mask, w.conf)) for _ in range(n_sets)]
         ws_t = sv.alloc_workspace(sv.workspace_bytes(w.B, w.N - 1, w.V, w.Lt.dtype), dev)
         out = sv.spec_verify_tree_greedy(*sets[0][:3], w.n1, tree_mask=sets[0][3], workspace=ws_t)
@@ -341,7 +362,10 @@ def run_ours(args):
     t0 = time.perf_counter()
     d2h = 0
     for _ in range(e2e_steps):
-        if name == "tree":
+        if name == "entropy":
+            o = sv.spec_tree_entropy(pinned[0], w.n1, 1.0, device=dev, node_entropy=False)
+            res = [o["choice"].cpu(), o["scores"].cpu()]
+        elif name == "tree":
             o = sv.spec_verify_tree_greedy(pinned[0], pinned[1], pinned[2], w.n1, tree_mask=pinned[3], device=dev)
             co = sv.spec_tree_confidence(pinned[4], w.n1, device=dev)
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu(), co["choice"].cpu()]
@@ -363,11 +387,13 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     k1_mean = float(np.mean(k1_ms))
     achieved = alg / (k1_mean / 1e3) / 1e9
-    kernel_key = {"tree": "rowscan_argmax_tree", "greedy": "rowscan_argmax_chain"}.get(name, f"rowscan_stats_{name}")
+    kernel_key = {"tree": "rowscan_argmax_tree", "greedy": "rowscan_argmax_chain",
+                  "entropy": "rowscan_entropy_tree"}.get(name, f"rowscan_stats_{name}")
     line = {
-        "metric": METRIC if name == "chain_batched" else f"verified {'nodes' if name == 'tree' else 'draft positions'}/sec ({name})",
+        "metric": METRIC if name == "chain_batched" else f"{'routed' if name == 'entropy' else 'verified'} "
+                  f"{'nodes' if name in ('tree', 'entropy') else 'draft positions'}/sec ({name})",
         "value": value,
-        "unit": "nodes/s" if name == "tree" else "positions/s",
+        "unit": "nodes/s" if name in ("tree", "entropy") else "positions/s",
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -386,12 +412,12 @@ def run_ours(args):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_for(kernel_key), "algorithmic_bytes": alg,
                      "kernel_ms_mean": k1_mean},
-        "e2e": {"value": e2e_value, "unit": "nodes/s" if name == "tree" else "positions/s",
+        "e2e": {"value": e2e_value, "unit": "nodes/s" if name in ("tree", "entropy") else "positions/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
-    if name != "tree":
+    if name not in ("tree", "entropy"):
         al = out["accept_len"].cpu().numpy()
         line["accept_len_mean"] = float(al[al >= 0].mean())
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -562,7 +588,9 @@ def _oracle_step(name, w, rows, threads):
     import oracle
 
     idx = torch.as_tensor(rows)
-    if name == "tree":
+    if name == "entropy":
+        oracle.tree_entropy(w.Ld[idx], w.n1)
+    elif name == "tree":
         oracle.verify_tree_greedy(w.Lt[idx], w.tok[idx], w.R[idx], w.n1, mask=w.mask[idx], threads=threads)
         oracle.tree_confidence(w.conf[idx], w.n1)
     elif w.T == 0.0:
@@ -591,9 +619,9 @@ def cpu_baseline(name, w, cpu_seconds):
         _oracle_step(name, w, rows, threads)
         t_tot += time.perf_counter() - t0
         reps += 1
-    per_row_units = (w.N - 1) if name == "tree" else w.K
-    cores = min(threads, w.B)
-    return {"value": w.B * per_row_units * reps / t_tot, "unit": "nodes/s" if name == "tree" else "positions/s",
+    per_row_units = (w.N - 1) if name in ("tree", "entropy") else w.K
+    cores = min(threads, w.B) if name != "entropy" else 1
+    return {"value": w.B * per_row_units * reps / t_tot, "unit": "nodes/s" if name in ("tree", "entropy") else "positions/s",
             "cores": cores, "kind": "oracle",
             "sample": f"all {w.B} rows of the batch, {reps} repeats, fp64 C oracle on {cores} threads "
                       f"({t_tot:.1f} s wall, about {t_tot * cores:.0f} CPU-s)"}
@@ -618,9 +646,9 @@ def run_reference(args):
     for _ in range(args.steps):
         _oracle_step(name, w, rows, threads)
     dt = time.perf_counter() - t0
-    per_row_units = (w.N - 1) if name == "tree" else w.K
+    per_row_units = (w.N - 1) if name in ("tree", "entropy") else w.K
     value = n * per_row_units * args.steps / dt
-    unit = "nodes/s" if name == "tree" else "positions/s"
+    unit = "nodes/s" if name in ("tree", "entropy") else "positions/s"
     line = {
         "impl": "reference",
         "metric": METRIC if name == "chain_batched" else f"verified positions/sec ({name})",
@@ -658,7 +686,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="chain_batched",
-                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "kv_compact"])
+                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")
     ap.add_argument("--e2e-steps", type=int, default=20)

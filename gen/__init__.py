@@ -24,4 +24,5 @@ from .workloads import (  # noqa: F401
     tree_from_parents,
     tree_batch,
     kv_cache,
+    tree_draft_logits,
 )

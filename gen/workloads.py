@@ -348,6 +348,22 @@ def config_tree(seed: int = 0, B: int = 16) -> TreeBatch:
     return tree_batch(B, 30, 128256, torch.bfloat16, seed, name="tree_merged")
 
 
+def tree_draft_logits(tb: "TreeBatch", seed: int = 0, sigma: float = 1.0) -> torch.Tensor:
+    """Drafter logits for every node of a merged tree batch: the node's target
+    logits scaled by a per-(row, drafter) sharpness s ~ U(0.4, 1.6) plus
+    N(0, sigma^2) noise, so that the two drafters' trees differ in entropy.
+    Same dtype as the target logits; row 0 (the root) included."""
+    g = _gen(seed)
+    B, N, V = tb.Lt.shape
+    sharp = 0.4 + 1.2 * torch.rand(B, 2, generator=g)
+    out = torch.empty(B, N, V, dtype=tb.Lt.dtype)
+    for b in range(B):
+        s_node = torch.where(torch.arange(N) <= tb.n1, sharp[b, 0], sharp[b, 1]).view(N, 1)
+        noise = sigma * torch.randn(N, V, generator=g)
+        out[b] = (tb.Lt[b].float() * s_node + noise).to(tb.Lt.dtype)
+    return out
+
+
 def kv_cache(P: int, B: int, S: int, W: int, dtype: torch.dtype = torch.bfloat16, seed: int = 0,
              pad: int = 0) -> torch.Tensor:
     """Synthetic KV cache: [P, B, S, W + pad] of random bit patterns (P

@@ -22,6 +22,8 @@
  *   - spec_tree_confidence: confidence routing, the arithmetic mean of the
  *     nodes' drafter confidences per tree, higher wins (TAPS page,
  *     methodology, confidence routing).
+ *   - spec_tree_entropy: entropy routing, the mean drafter entropy per tree,
+ *     lower wins (the signal the TAPS page compares confidence routing with).
  *   - spec_kv_compact: after verification, keep the accepted entries of the
  *     KV cache at consecutive positions and cut the length after them
  *     (lotook.com, KV-cache section; SubSpec review, step "Update KV").
@@ -196,6 +198,25 @@ int spec_verify_tree_greedy(const void* node_logits, int dtype, const int32_t* n
  * score_2 > score_1 (compared in fp64) else 1. */
 int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* scores, int32_t* choice,
                          void* stream);
+
+/* Entropy routing over a merged tree's drafter distributions: the signal
+ * the TAPS page compares confidence routing with (methodology and results:
+ * confidence picks the right drafter far more reliably than entropy). No
+ * formula is given there; this one is the plainest reading. Each non-root
+ * node's entropy is that of its next-token distribution softmax(l / T) over
+ * the vocabulary, H = -sum_v p_v ln p_v; a tree's score is the arithmetic
+ * mean over its nodes (tree 1: nodes 1..n1, tree 2: n1+1..N-1, +inf for an
+ * empty tree); the lower score wins, ties to tree 1.
+ *   draft_logits  device [B][N][V] (row 0, the root, is read but unused)
+ *   temperature   > 0, finite
+ *   workspace     spec_workspace_bytes(B, N, V, dtype) bytes suffice
+ * Outputs (device): node_entropy [B][N] fp32 or NULL (root NaN); scores
+ * [B][2] fp32; choice [B] int32 (1 or 2); row_status [B] int32
+ * (SPEC_ROW_DRAFT when a non-root row holds NaN or +inf or only -inf: that
+ * row's scores NaN, choice -1, entropies NaN). N <= 1024. */
+int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, int B, int N, int V, int n1,
+                      float* node_entropy, float* scores, int32_t* choice, int32_t* row_status, void* workspace,
+                      size_t workspace_bytes, void* stream);
 
 /* KV-cache compaction after a verification step (lotook.com, section on the
  * KV cache: when the target rejects the drafts after position m, both

@@ -221,3 +221,29 @@ def spec_kv_compact(kv: torch.Tensor, base_pos, accept_len, path=None, out: Opti
                                                  _ptr(base), _ptr(pth), D, _ptr(acc), _ptr(out["new_len"]),
                                                  _ptr(out["row_status"]), _stream(stream)))
     return out
+
+
+def spec_tree_entropy(draft_logits, n1: int, temperature: float = 1.0, out: Optional[Dict[str, torch.Tensor]] = None,
+                      workspace: Optional[torch.Tensor] = None, device="cuda", stream=None,
+                      node_entropy: bool = True) -> Dict[str, torch.Tensor]:
+    """Entropy routing over merged drafter trees: draft_logits [B, N, V]
+    (bf16 or fp32). Returns scores [B, 2], choice [B], row_status [B] and
+    (with ``node_entropy``) the per-node entropies [B, N]."""
+    lib = _lib.load()
+    dev = draft_logits.device if draft_logits.device.type == "cuda" else torch.device(device)
+    Ld = _dev(draft_logits, dev)
+    B, N, V = Ld.shape
+    code = _dtype_code(Ld)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(B, N, V, code), dev)
+    if out is None:
+        out = dict(scores=torch.empty(B, 2, dtype=torch.float32, device=dev),
+                   choice=torch.empty(B, dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+        if node_entropy:
+            out["node_entropy"] = torch.empty(B, N, dtype=torch.float32, device=dev)
+    check("spec_tree_entropy", lib.spec_tree_entropy(Ld.data_ptr(), code, float(temperature), B, N, V, int(n1),
+                                                     _ptr(out.get("node_entropy")), _ptr(out["scores"]),
+                                                     _ptr(out["choice"]), _ptr(out["row_status"]),
+                                                     workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return out

@@ -303,6 +303,46 @@ int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* sc
   return cuda_status(launch_tree_confidence(node_conf, B, N, n1, scores, choice, static_cast<cudaStream_t>(stream)));
 }
 
+int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, int B, int N, int V, int n1,
+                      float* node_entropy, float* scores, int32_t* choice, int32_t* row_status, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!draft_logits || !scores || !choice || !row_status) return SPEC_ERR_ARG;
+  if (!dtype_ok(dtype) || B < 1 || N < 1 || V < 2 || n1 < 0 || n1 > N - 1) return SPEC_ERR_ARG;
+  if (!(temperature > 0.f) || !isfinite(temperature)) return SPEC_ERR_ARG;
+  if (B > kMaxB || N > entropy_max_nodes() || V > kMaxV) return SPEC_ERR_UNSUPPORTED;
+  const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
+  const size_t need = up256(static_cast<size_t>(static_cast<long long>(B) * N * P) * sizeof(float4));
+  int e = check_workspace(workspace, workspace_bytes, need);
+  if (e) return e;
+  const bool vec = use_vec(V, dtype, draft_logits, nullptr);
+  if ((e = scan_grid_ok(static_cast<long long>(B) * N, V, dtype, vec))) return e;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ScanArgs a{};
+  a.A = draft_logits;
+  a.B = B;
+  a.TR = N;
+  a.DR = 0;
+  a.V = V;
+  a.P = scan_chunks(V, vec, dtype);
+  split_c(temperature, &a.c_hi, &a.c_lo);
+  a.part = static_cast<float2*>(workspace);
+  if (launch_rowscan(a, dtype, vec, kModeEntropy, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  EntArgs en{};
+  en.part = a.part;
+  en.B = B;
+  en.N = N;
+  en.P = a.P;
+  en.n1 = n1;
+  en.c_hi = a.c_hi;
+  en.c_lo = a.c_lo;
+  en.invT = 1.0 / static_cast<double>(temperature);
+  en.node_entropy = node_entropy;
+  en.scores = scores;
+  en.choice = choice;
+  en.row_status = row_status;
+  return cuda_status(launch_tree_entropy(en, st));
+}
+
 int spec_kv_compact(void* kv, int elem_bytes, int n_planes, int B, int S, int W, long long stride_plane,
                     long long stride_batch, long long stride_pos, const int32_t* base_pos, const int32_t* path, int D,
                     const int32_t* accept_len, int32_t* new_len, int32_t* row_status, void* stream) {

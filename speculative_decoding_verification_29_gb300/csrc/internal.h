@@ -11,6 +11,7 @@ namespace specv {
 
 constexpr int kModeStats = 0;   // rowscan: (max, sum of exp) per row
 constexpr int kModeArgmax = 1;  // rowscan: (value, index) of the row maximum
+constexpr int kModeEntropy = 2; // rowscan: (max, sum of exp, sum of exp * (l - max)) per row, float4 partials
 constexpr int kMaxK = 255;
 
 // rowscan geometry: each warp reduces one segment of kSegChunks chunks of kWV
@@ -131,6 +132,20 @@ cudaError_t launch_tree_finish(const TreeArgs& a, cudaStream_t st);
 
 cudaError_t launch_tree_confidence(const float* conf, int B, int N, int n1, float* scores, int32_t* choice,
                                    cudaStream_t st);
+
+// Entropy routing of two drafter trees (after the rowscan in entropy mode).
+struct EntArgs {
+  const float2* part;  // float4 partials [B * N][P]
+  int B, N, P, n1;
+  float c_hi, c_lo;    // log2(e) / T, c_lo > 0
+  double invT;
+  float* node_entropy; // [B][N] or NULL
+  float* scores;       // [B][2]
+  int32_t* choice;     // [B]
+  int32_t* row_status; // [B]
+};
+int entropy_max_nodes();
+cudaError_t launch_tree_entropy(const EntArgs& a, cudaStream_t st);
 
 // KV-cache compaction after verification.
 struct KvArgs {

@@ -13,7 +13,10 @@
 //          draft position in one pass);
 //   argmax (greedy and trees): the segment's max value and the lowest index
 //          holding it (lotook.com: at temperature 0 a draft token is kept when
-//          it is the target's top choice).
+//          it is the target's top choice);
+//   entropy (drafter trees): (m, z, y) with y = sum 2^((l - m) log2(e) / T)
+//          (l - m), from which a row's softmax entropy follows (TAPS page:
+//          entropy routing of drafter trees).
 // The max runs on packed bf16 pairs, the exponent arithmetic on packed fp32
 // pairs (f32x2) with one accumulator per pair lane; a lane's running sum is
 // rescaled (exp2f, correctly rounded to within an ulp) when its running max
@@ -69,18 +72,21 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
   const int j = kind_to_row(a, blockIdx.z);
   const Raw* row = row_ptr<Raw>(a, b, j);
   float M, tail;  // tail: stats -> sum of exp; argmax -> index bits
+  float ytail = 0.f;  // entropy: sum of exp * (l - M)
   if constexpr (VEC) {
     using Vt = Vec<Raw>;
     constexpr int EPV = Elem<Raw>::kPerVec;
     const int nv = a.V / EPV;
     const int v0 = seg * (kSegChunks * kWV * 32) + lane;
     const uint4 neg = make_uint4(Vt::kNegInf, Vt::kNegInf, Vt::kNegInf, Vt::kNegInf);
-    if constexpr (MODE == kModeStats) {
+    if constexpr (MODE != kModeArgmax) {
+      constexpr bool kEnt = MODE == kModeEntropy;
       const float2 ch = make_float2(a.c_hi, a.c_hi), cl = make_float2(a.c_lo, a.c_lo);
       float mrun = -INFINITY;
       float2 acc[Vt::kPairs];  // one accumulator per pair lane: independent add chains
+      float2 yac[Vt::kPairs];  // entropy: sum of exp * (l - m), l = -inf counted as 0
 #pragma unroll
-      for (int i = 0; i < Vt::kPairs; ++i) acc[i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < Vt::kPairs; ++i) acc[i] = yac[i] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int g = 0; g < kSegChunks; ++g) {
         uint4 raw[kWV];
@@ -96,6 +102,11 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
         if (mnew != -INFINITY) {  // NaN and +inf propagate into the partial (the row is flagged)
           const float sc = exp2f(scale_c(mrun - mnew, a.c_hi, a.c_lo));  // 0 when mrun = -inf
           const float2 sc2 = make_float2(sc, sc), nm = make_float2(-mnew, -mnew);
+          if constexpr (kEnt) {  // y(m') = sc (y(m) + (m - m') z(m)); nothing yet when mrun = -inf
+            const float sh = mrun == -INFINITY ? 0.f : mrun - mnew;
+#pragma unroll
+            for (int i = 0; i < Vt::kPairs; ++i) yac[i] = mul2(fma2(acc[i], make_float2(sh, sh), yac[i]), sc2);
+          }
 #pragma unroll
           for (int i = 0; i < Vt::kPairs; ++i) acc[i] = mul2(acc[i], sc2);
 #pragma unroll
@@ -104,17 +115,31 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
             for (int i = 0; i < Vt::kPairs; ++i) {
               const float2 d = add2(Vt::pair(raw[t], i), nm);
               const float2 e = fma2(d, ch, mul2(d, cl));  // (l - m) * log2(e) / T; -inf stays -inf
-              acc[i] = add2(acc[i], make_float2(ex2_fast(e.x), ex2_fast(e.y)));
+              const float2 x = make_float2(ex2_fast(e.x), ex2_fast(e.y));
+              acc[i] = add2(acc[i], x);
+              if constexpr (kEnt) yac[i] = fma2(x, make_float2(fmaxf(d.x, -3.0e38f), fmaxf(d.y, -3.0e38f)), yac[i]);
             }
           mrun = mnew;
         }
       }
 #pragma unroll
-      for (int i = 1; i < Vt::kPairs; ++i) acc[0] = add2(acc[0], acc[i]);
-      float z = acc[0].x + acc[0].y;
+      for (int i = 1; i < Vt::kPairs; ++i) {
+        acc[0] = add2(acc[0], acc[i]);
+        yac[0] = add2(yac[0], yac[i]);
+      }
+      float z = acc[0].x + acc[0].y, y = yac[0].x + yac[0].y;
       M = warp_max_nan(mrun);
-      if (M == M && M != -INFINITY) z = mrun == -INFINITY ? 0.f : z * exp2f(scale_c(mrun - M, a.c_hi, a.c_lo));
+      if (M == M && M != -INFINITY) {
+        if (mrun == -INFINITY) {
+          z = y = 0.f;
+        } else {
+          const float f = exp2f(scale_c(mrun - M, a.c_hi, a.c_lo));
+          y = f * fmaf(z, mrun - M, y);
+          z *= f;
+        }
+      }
       tail = warp_sum(z);
+      if constexpr (kEnt) ytail = warp_sum(y);
     } else {
       float best = -INFINITY;
       int bidx = INT_MAX;
@@ -166,13 +191,19 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
 #pragma unroll
     for (int t = 0; t < kScalarPerLane; ++t) m = fmax_nan(m, e[t]);
     M = warp_max_nan(m);
-    if constexpr (MODE == kModeStats) {
-      float z = 0.f;
+    if constexpr (MODE != kModeArgmax) {
+      float z = 0.f, y = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int t = 0; t < kScalarPerLane; ++t) z += ex2_fast(scale_c(e[t] - M, a.c_hi, a.c_lo));
+        for (int t = 0; t < kScalarPerLane; ++t) {
+          const float d = e[t] - M;
+          const float x = ex2_fast(scale_c(d, a.c_hi, a.c_lo));
+          z += x;
+          if constexpr (MODE == kModeEntropy) y = fmaf(x, fmaxf(d, -3.0e38f), y);
+        }
       }
       tail = warp_sum(z);
+      if constexpr (MODE == kModeEntropy) ytail = warp_sum(y);
     } else {
       int idx = INT_MAX;
       if (M != M) {
@@ -186,7 +217,13 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
       tail = __int_as_float(idx);
     }
   }
-  if (lane == 0) a.part[(static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg] = make_float2(M, tail);
+  const long long slot = (static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg;
+  if (lane == 0) {
+    if constexpr (MODE == kModeEntropy)
+      reinterpret_cast<float4*>(a.part)[slot] = make_float4(M, tail, ytail, 0.f);
+    else
+      a.part[slot] = make_float2(M, tail);
+  }
 }
 
 namespace {
@@ -199,10 +236,16 @@ cudaError_t launch_t(const ScanArgs& a, cudaStream_t st) {
   return launch_pdl(rowscan_kernel<Raw, VEC, MODE>, grid, dim3(kScanThreads), st, a);
 }
 
+template <typename Raw, bool VEC>
+cudaError_t launch_mode(const ScanArgs& a, int mode, cudaStream_t st) {
+  if (mode == kModeStats) return launch_t<Raw, VEC, kModeStats>(a, st);
+  if (mode == kModeEntropy) return launch_t<Raw, VEC, kModeEntropy>(a, st);
+  return launch_t<Raw, VEC, kModeArgmax>(a, st);
+}
+
 template <typename Raw>
 cudaError_t launch_typed(const ScanArgs& a, bool vec, int mode, cudaStream_t st) {
-  if (vec) return mode == kModeStats ? launch_t<Raw, true, kModeStats>(a, st) : launch_t<Raw, true, kModeArgmax>(a, st);
-  return mode == kModeStats ? launch_t<Raw, false, kModeStats>(a, st) : launch_t<Raw, false, kModeArgmax>(a, st);
+  return vec ? launch_mode<Raw, true>(a, mode, st) : launch_mode<Raw, false>(a, mode, st);
 }
 
 }  // namespace

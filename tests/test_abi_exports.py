@@ -29,7 +29,8 @@ def declared():
 def test_header_declares_the_boundary():
     names = declared()
     for n in ("spec_verify_chain", "spec_verify_chain_greedy", "spec_verify_tree_greedy", "spec_tree_confidence",
-              "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample", "spec_kv_compact"):
+              "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample", "spec_kv_compact",
+              "spec_tree_entropy"):
         assert n in names
 
 
@@ -79,6 +80,12 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.spec_verify_tree_greedy(fake, 1, fake, fake, n, 1, 5000, 2, 3, 16, 5, fake, fake, fake, fake, fake,
                                        fake, fake, 1 << 30, n) == SPEC_ERR_UNSUPPORTED
     assert lib.spec_tree_confidence(fake, 1, 5, 9, fake, fake, n) == SPEC_ERR_ARG
+    # entropy routing: temperature, n1, workspace
+    assert lib.spec_tree_entropy(fake, 1, 0.0, 2, 5, 16, 2, n, fake, fake, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert lib.spec_tree_entropy(fake, 1, 1.0, 2, 5, 16, 7, n, fake, fake, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert lib.spec_tree_entropy(fake, 1, 1.0, 2, 5, 16, 2, n, fake, fake, fake, fake, 8, n) == SPEC_ERR_WORKSPACE
+    assert lib.spec_tree_entropy(fake, 1, 1.0, 2, 2000, 16, 2, n, fake, fake, fake, fake, 1 << 30, n) == \
+        SPEC_ERR_UNSUPPORTED
     # KV compaction: NULL cache, element size, overlapping rows, negative stride, path width
     kv = lambda *a: lib.spec_kv_compact(*a)
     assert kv(n, 2, 4, 2, 64, 128, 16384, 8192, 128, fake, n, 0, fake, fake, fake, n) == SPEC_ERR_ARG
