@@ -662,6 +662,126 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def merge_setup(seed: int):
+    """Per-row drafter trees of the merged-tree workload (two 30-node trees per
+    row, B=16), as the two drafters hand them over."""
+    import numpy as np
+    import torch
+
+    import gen
+
+    tb = gen.config_tree(seed)
+
+    def batched(parents, toks):
+        per = [gen.tree_from_parents(p) for p in parents]
+        D = max(R.shape[1] for R, _, _ in per)
+        Rn = max(R.shape[0] for R, _, _ in per)
+        n = len(parents[0]) - 1
+        R = torch.full((tb.B, Rn, D), -1, dtype=torch.int32)
+        mask = torch.zeros(tb.B, n + 1, n + 1, dtype=torch.uint8)
+        pos = torch.zeros(tb.B, n + 1, dtype=torch.int32)
+        for b, (Rb, mb, pb) in enumerate(per):
+            R[b, : Rb.shape[0], : Rb.shape[1]] = Rb
+            mask[b], pos[b] = mb, pb
+        return [torch.as_tensor(np.array(toks), dtype=torch.int32), mask, R, pos]
+
+    t1 = batched(tb.parents1, tb.tok1)
+    t2 = batched(tb.parents2, tb.tok2)
+    cfg = dict(workload=f"batched merge of two drafter trees: B={tb.B}, {tb.n1} + {tb.N - 1 - tb.n1} non-root nodes",
+               B=tb.B, N=tb.N)
+    return tb, t1, t2, cfg
+
+
+def run_merge(args):
+    import torch
+
+    import speculative_decoding_verification_29_gb300 as sv
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tb, t1, t2, cfg = merge_setup(rank_seed(args.seed, rank))
+    d1, d2 = [t.to(dev) for t in t1], [t.to(dev) for t in t2]
+    out = sv.spec_merge_trees(*d1, *d2)
+    stream = torch.cuda.current_stream()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        sv.spec_merge_trees(*d1, *d2)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            sv.spec_merge_trees(*d1, *d2)
+    graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = max_over_ranks(start.elapsed_time(end), ws, dev)
+    host = [t.pin_memory() for t in t1 + t2]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        o = sv.spec_merge_trees(*host, device=dev)
+        res = [o["tokens"].cpu(), o["mask"].cpu(), o["retrieve"].cpu(), o["pos"].cpu()]
+    e2e_s = time.perf_counter() - t0
+    clk = clocks.stop() if clocks else None
+    nbytes = sum(t.numel() * t.element_size() for t in d1 + d2) + sum(v.numel() * v.element_size()
+                                                                     for k, v in out.items() if k != "n1")
+    units = tb.B * (tb.N - 1)
+    peak, peak_kind = _peaks()
+    k_ms = total_ms / args.steps
+    line = {"metric": "merged tree nodes/sec (batched merge of two drafter trees)",
+            "value": throughput(units, args.steps, ws, total_ms), "unit": "nodes/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": k_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32 / uint8", "data": "synthetic (the tree workload's drafter trees)",
+            "config": dict(cfg, parallelism=f"replicas x{ws}", launch="cuda_graph (the K steps in one graph)"),
+            "roofline": {"bound": "hbm", "kernel": "merge_trees_kernel", "achieved": nbytes / (k_ms / 1e3) / 1e9,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": nbytes / (k_ms / 1e3) / 1e9 / peak, "traffic": None, "algorithmic_bytes": nbytes,
+                         "kernel_ms_mean": k_ms},
+            "e2e": {"value": throughput(units, e2e_steps, ws, e2e_s * 1e3), "unit": "nodes/s",
+                    "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+                    "d2h_bytes_per_step": sum(r.numel() * r.element_size() for r in res), "steps": e2e_steps},
+            "gpu_launches": args.steps, "clocks": clk}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = merge_cpu_baseline(tb, t1, t2)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def merge_cpu_baseline(tb, t1, t2, reps=20):
+    import oracle
+
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        for b in range(tb.B):
+            oracle.merge_trees(t1[0][b:b + 1], t1[2][b], t1[1][b], t1[3][b], t2[0][b:b + 1], t2[2][b], t2[1][b],
+                               t2[3][b])
+    dt = time.perf_counter() - t0
+    return {"value": tb.B * (tb.N - 1) * reps / dt, "unit": "nodes/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} merges of the {tb.B} tree pairs (numpy, one thread: {dt:.2f} s)"}
+
+
+def run_merge_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    tb, t1, t2, cfg = merge_setup(args.seed)
+    b = merge_cpu_baseline(tb, t1, t2, reps=max(1, min(args.steps, 50)))
+    print(json.dumps({"impl": "reference", "metric": "merged tree nodes/sec (batched merge of two drafter trees)",
+                      "value": b["value"], "unit": "nodes/s", "n_gpus": ws, "steps": args.steps,
+                      "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                      "dtype": "int32 / uint8", "data": "synthetic", "config": cfg, "cpu_baseline": b,
+                      "e2e": {"value": b["value"], "unit": "nodes/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def run_kv_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -686,7 +806,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="chain_batched",
-                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact"])
+                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact", "merge"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -694,7 +814,12 @@ def main():
     ap.add_argument("--graph", action="store_true", help="replay each step as a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.workload == "kv_compact":
+    if args.workload == "merge":
+        if args.impl == "reference":
+            run_merge_reference(args)
+        else:
+            run_merge(args)
+    elif args.workload == "kv_compact":
         if args.impl == "reference":
             run_kv_reference(args)
         else:

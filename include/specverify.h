@@ -22,6 +22,9 @@
  *   - spec_tree_confidence: confidence routing, the arithmetic mean of the
  *     nodes' drafter confidences per tree, higher wins (TAPS page,
  *     methodology, confidence routing).
+ *   - spec_merge_trees: two drafter trees merged under one shared root on
+ *     the device, the input of spec_verify_tree_greedy (TAPS page,
+ *     tree-merging code example).
  *   - spec_tree_entropy: entropy routing, the mean drafter entropy per tree,
  *     lower wins (the signal the TAPS page compares confidence routing with).
  *   - spec_kv_compact: after verification, keep the accepted entries of the
@@ -198,6 +201,27 @@ int spec_verify_tree_greedy(const void* node_logits, int dtype, const int32_t* n
  * score_2 > score_1 (compared in fp64) else 1. */
 int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* scores, int32_t* choice,
                          void* stream);
+
+/* Merge two drafter token trees under one shared root, B tree pairs at once
+ * (TAPS page, tree-merging code example; merged-tree verification in its
+ * methodology). Inputs per tree, EAGLE-style: tokens [B][n+1] int32 (entry 0
+ * the root), mask [B][n+1][n+1] uint8 self-inclusive ancestor mask,
+ * retrieve [B][R][D] int32 root-to-leaf paths padded with -1 (may be NULL
+ * when R = 0), pos [B][n+1] int32 depths. Outputs (device), N = n1+n2+1,
+ * D = max(D1, D2): tokens [B][N] (tree 1's, then tree 2's without its
+ * root); mask [B][N][N] (the root cell, tree 1's rows below the root over
+ * tree 1's columns, tree-2 rows over the root column and tree 2's non-root
+ * block, zero elsewhere); retrieve [B][R1+R2][D] (tree 1's rows, then tree
+ * 2's with node indices above 0 shifted by n1, padded with -1; the example
+ * elides this part, and a row holding only the root becomes a padding row
+ * unless every row of the pair is root-only, in which case the first is
+ * kept); pos [B][N] (tree 1's, then tree 2's without its root). The output
+ * feeds spec_verify_tree_greedy with the same n1. Limits: N <= 1024,
+ * R1+R2 <= 4096, D1, D2 <= 64. */
+int spec_merge_trees(const int32_t* tokens1, const uint8_t* mask1, const int32_t* retrieve1, const int32_t* pos1,
+                     const int32_t* tokens2, const uint8_t* mask2, const int32_t* retrieve2, const int32_t* pos2,
+                     int B, int n1, int n2, int R1, int D1, int R2, int D2, int32_t* tokens, uint8_t* mask,
+                     int32_t* retrieve, int32_t* pos, void* stream);
 
 /* Entropy routing over a merged tree's drafter distributions: the signal
  * the TAPS page compares confidence routing with (methodology and results:

@@ -12,6 +12,7 @@ __all__ = [
     "spec_verify_chain_greedy",
     "spec_verify_tree_greedy",
     "spec_tree_confidence",
+    "spec_merge_trees",
     "spec_tree_entropy",
     "spec_kv_compact",
     "workspace_bytes",

@@ -31,6 +31,7 @@ SIGNATURES = {
     "spec_verify_chain_greedy": (I, [P, I, P, I, I, I, P, P, P, P, P, Z, P]),
     "spec_verify_tree_greedy": (I, [P, I, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, Z, P]),
     "spec_tree_confidence": (I, [P, I, I, I, P, P, P]),
+    "spec_merge_trees": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P]),
     "spec_tree_entropy": (I, [P, I, F, I, I, I, I, P, P, P, P, P, Z, P]),
     "spec_kv_compact": (I, [P, I, I, I, I, I, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong, P, P, I, P, P, P,
                             P]),

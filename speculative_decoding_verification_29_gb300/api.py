@@ -247,3 +247,31 @@ def spec_tree_entropy(draft_logits, n1: int, temperature: float = 1.0, out: Opti
                                                      _ptr(out["choice"]), _ptr(out["row_status"]),
                                                      workspace.data_ptr(), workspace.numel(), _stream(stream)))
     return out
+
+
+def spec_merge_trees(tokens1, mask1, retrieve1, pos1, tokens2, mask2, retrieve2, pos2, device="cuda",
+                     stream=None) -> Dict[str, torch.Tensor]:
+    """Merge B pairs of drafter trees under one shared root on the device.
+
+    tokens* [B, n+1] int32, mask* [B, n+1, n+1] uint8, retrieve* [B, R, D]
+    int32, pos* [B, n+1] int32. Returns tokens [B, N], mask [B, N, N],
+    retrieve [B, R1+R2, max(D1, D2)], pos [B, N] and n1."""
+    lib = _lib.load()
+    dev = tokens1.device if tokens1.device.type == "cuda" else torch.device(device)
+    t1, t2 = _dev(tokens1, dev, torch.int32), _dev(tokens2, dev, torch.int32)
+    m1, m2 = _dev(mask1, dev, torch.uint8), _dev(mask2, dev, torch.uint8)
+    r1, r2 = _dev(retrieve1, dev, torch.int32), _dev(retrieve2, dev, torch.int32)
+    p1, p2 = _dev(pos1, dev, torch.int32), _dev(pos2, dev, torch.int32)
+    B, n1, n2 = t1.shape[0], t1.shape[1] - 1, t2.shape[1] - 1
+    N, (R1, D1), (R2, D2) = n1 + n2 + 1, r1.shape[1:], r2.shape[1:]
+    D = max(D1, D2)
+    out = dict(tokens=torch.empty(B, N, dtype=torch.int32, device=dev),
+               mask=torch.empty(B, N, N, dtype=torch.uint8, device=dev),
+               retrieve=torch.empty(B, R1 + R2, D, dtype=torch.int32, device=dev),
+               pos=torch.empty(B, N, dtype=torch.int32, device=dev))
+    check("spec_merge_trees", lib.spec_merge_trees(_ptr(t1), _ptr(m1), _ptr(r1) if R1 else None, _ptr(p1), _ptr(t2),
+                                                   _ptr(m2), _ptr(r2) if R2 else None, _ptr(p2), B, n1, n2, R1, D1,
+                                                   R2, D2, _ptr(out["tokens"]), _ptr(out["mask"]),
+                                                   _ptr(out["retrieve"]), _ptr(out["pos"]), _stream(stream)))
+    out["n1"] = n1
+    return out

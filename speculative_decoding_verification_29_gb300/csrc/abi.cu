@@ -303,6 +303,20 @@ int spec_tree_confidence(const float* node_conf, int B, int N, int n1, float* sc
   return cuda_status(launch_tree_confidence(node_conf, B, N, n1, scores, choice, static_cast<cudaStream_t>(stream)));
 }
 
+int spec_merge_trees(const int32_t* tokens1, const uint8_t* mask1, const int32_t* retrieve1, const int32_t* pos1,
+                     const int32_t* tokens2, const uint8_t* mask2, const int32_t* retrieve2, const int32_t* pos2,
+                     int B, int n1, int n2, int R1, int D1, int R2, int D2, int32_t* tokens, uint8_t* mask,
+                     int32_t* retrieve, int32_t* pos, void* stream) {
+  if (!tokens1 || !mask1 || !pos1 || !tokens2 || !mask2 || !pos2 || !tokens || !mask || !retrieve || !pos)
+    return SPEC_ERR_ARG;
+  if ((R1 > 0 && !retrieve1) || (R2 > 0 && !retrieve2)) return SPEC_ERR_ARG;
+  if (B < 1 || n1 < 0 || n2 < 0 || R1 < 0 || R2 < 0 || R1 + R2 < 1 || D1 < 1 || D2 < 1) return SPEC_ERR_ARG;
+  if (B > kMaxB || n1 + n2 + 1 > kMaxN || R1 + R2 > kMaxR || D1 > kMaxD || D2 > kMaxD) return SPEC_ERR_UNSUPPORTED;
+  MergeArgs a{tokens1, retrieve1, pos1, mask1, tokens2, retrieve2, pos2, mask2, B, n1, n2, R1, D1, R2, D2,
+              std::max(D1, D2), tokens, retrieve, pos, mask};
+  return cuda_status(launch_merge_trees(a, static_cast<cudaStream_t>(stream)));
+}
+
 int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, int B, int N, int V, int n1,
                       float* node_entropy, float* scores, int32_t* choice, int32_t* row_status, void* workspace,
                       size_t workspace_bytes, void* stream) {

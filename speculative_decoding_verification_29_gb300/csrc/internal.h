@@ -147,6 +147,18 @@ struct EntArgs {
 int entropy_max_nodes();
 cudaError_t launch_tree_entropy(const EntArgs& a, cudaStream_t st);
 
+// Batched merge of two drafter trees under one shared root.
+struct MergeArgs {
+  const int32_t *tok1, *R1, *pos1;
+  const uint8_t* mask1;
+  const int32_t *tok2, *R2, *pos2;
+  const uint8_t* mask2;
+  int B, n1, n2, R1n, D1, R2n, D2, D;
+  int32_t *tok, *R, *pos;
+  uint8_t* mask;
+};
+cudaError_t launch_merge_trees(const MergeArgs& a, cudaStream_t st);
+
 // KV-cache compaction after verification.
 struct KvArgs {
   void* kv;
