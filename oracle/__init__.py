@@ -86,6 +86,8 @@ def _declare(lib):
     lib.orc_kv_compact.restype = None
     lib.orc_tree_entropy.argtypes = [P, i, i, i, i, d, i, P, P, P, P, P]
     lib.orc_tree_entropy.restype = None
+    lib.orc_verify_chain_warped.argtypes = [P, P, i, P, P, P, d, i, d, i, i, i, i, i, P, P, P, P, P, P, P, P, P, P]
+    lib.orc_verify_chain_warped.restype = None
     return lib
 
 
@@ -188,6 +190,40 @@ def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None) -> Dic
                              b0, b1, _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["lse_p"]),
                              _ptr(out["lse_q"]), _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["status"]),
                              _ptr(out["flags"]), _ptr(out["margin"]))
+
+    _run(part, B, threads)
+    return out
+
+
+def verify_chain_warped(Lp, Lq, x, ua, ur, T: float, top_k: int = 0, top_p: float = 1.0, threads: int = 1,
+                        lib=None) -> Dict[str, np.ndarray]:
+    """Chain verification with the sampling settings applied to p and q:
+    temperature T, then top-k (ties kept; 0 = off), then top-p (1.0 = off).
+    Returns accept_len, out_tokens, px / qx (warped probabilities of the draft
+    tokens), status, flags, margin as verify_chain."""
+    if not T > 0 or not top_p > 0:
+        raise ValueError("needs T > 0 and top_p > 0")
+    lib = lib or load()
+    lp, dt = _logits(Lp)
+    lq, dtq = _logits(Lq)
+    if dtq != dt:
+        raise TypeError("target and draft logits must share a dtype")
+    B, K1, V = lp.shape
+    K = K1 - 1
+    xs = _np(x, np.int32).reshape(B, K)
+    uas = _np(ua, np.float64).reshape(B, K)
+    urs = _np(ur, np.float64).reshape(B)
+    out = dict(accept_len=np.empty(B, np.int32), out_tokens=np.empty((B, K + 1), np.int32),
+               px=np.empty((B, K), np.float64), qx=np.empty((B, K), np.float64), status=np.empty(B, np.int32),
+               flags=np.empty(B, np.int32), margin=np.empty(B, np.float64))
+
+    def part(b0, b1):
+        wp, wq = np.empty(V, np.float64), np.empty(V, np.float64)
+        tmp = np.empty(V * 16, np.uint8)  # {double, int} entries, 16 bytes each
+        lib.orc_verify_chain_warped(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), int(top_k),
+                                    float(top_p), B, K, V, b0, b1, _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+                                    _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["status"]), _ptr(out["flags"]),
+                                    _ptr(out["margin"]), _ptr(wp), _ptr(wq), _ptr(tmp))
 
     _run(part, B, threads)
     return out

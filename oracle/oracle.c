@@ -20,6 +20,9 @@
  *     nodes of the merged tree in one pass and the longest accepted path is
  *     kept) and confidence routing (TAPS page, methodology: arithmetic mean of
  *     the nodes' predicted probabilities per drafter tree, higher wins);
+ *   - the sampling settings (top-k, top-p) applied to p and q before the
+ *     same steps (ariser.io page: p and q must be the distributions the
+ *     settings produce);
  *   - entropy routing, the signal the TAPS page compares confidence routing
  *     with: mean drafter entropy per tree, lower wins;
  *   - KV-cache compaction after verification (lotook.com, KV-cache section:
@@ -40,6 +43,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORC_F64 0
@@ -508,5 +512,159 @@ void orc_tree_entropy(const void* Ld, int dt, int B, int N, int V, double T, int
     scores[2 * b + 1] = s2;
     choice[b] = s2 < s1 ? 2 : 1;
     if (isfinite(s1) && isfinite(s2) && fabs(s1 - s2) < NEAR_H) flags[b] = FL_ROUTE;
+  }
+}
+
+/* ---- sampling settings applied to p and q (top-k, top-p) ---------------
+ * The ariser.io page (section on keeping the same distribution) notes that
+ * with sampling settings such as temperature or top-p, the p and q the
+ * algorithm uses must be the distributions those settings produce. Reading
+ * (the common order): temperature, then top-k, then top-p, the same
+ * settings for target and draft.
+ *   top-k: keep every token whose s = l / T is >= the k-th largest s (ties
+ *          kept; k <= 0 or k >= V keeps all);
+ *   top-p: on the renormalised remainder, keep token v iff the mass of the
+ *          kept tokens with a strictly larger s is < top_p (top_p >= 1 keeps
+ *          all);
+ * p'(v) = exp(s_v - M) / sum over kept tokens, 0 elsewhere. */
+typedef struct {
+  double s;
+  int v;
+} orc_sv;
+
+static int orc_sv_desc(const void* a, const void* b) {
+  const orc_sv* x = (const orc_sv*)a;
+  const orc_sv* y = (const orc_sv*)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return x->v < y->v ? -1 : (x->v > y->v);
+}
+
+/* Warped distribution of one row into out[V] (tmp: V scratch entries).
+ * Returns 1 when the row holds a NaN or has no finite maximum. */
+static int warped_row(const void* L, int dt, size_t off, int V, double T, int top_k, double top_p, double* out,
+                      orc_sv* tmp) {
+  double M, Z;
+  if (softmax_stats(L, dt, off, V, T, &M, &Z)) return 1;
+  for (int v = 0; v < V; ++v) {
+    double s = elem(L, dt, off + (size_t)v) / T;
+    tmp[v].s = s;
+    tmp[v].v = v;
+    out[v] = exp(s - M);
+  }
+  qsort(tmp, (size_t)V, sizeof(orc_sv), orc_sv_desc);
+  double tk = -INFINITY; /* keep s >= tk */
+  if (top_k > 0 && top_k < V) tk = tmp[top_k - 1].s;
+  double Zk = 0.0;
+  for (int v = 0; v < V; ++v)
+    if (elem(L, dt, off + (size_t)v) / T >= tk) Zk += out[v];
+  double thr = tk;
+  if (top_p < 1.0) {
+    double cum = 0.0, tp = tk;
+    int i = 0;
+    while (i < V && tmp[i].s >= tk) {
+      int j = i;
+      double g = 0.0;
+      while (j < V && tmp[j].s == tmp[i].s) g += out[tmp[j++].v];
+      if (!(cum < top_p * Zk)) break; /* this value and every smaller one are dropped */
+      tp = tmp[i].s;
+      cum += g;
+      i = j;
+    }
+    if (tp > thr) thr = tp;
+  }
+  double Zw = 0.0;
+  for (int v = 0; v < V; ++v)
+    if (elem(L, dt, off + (size_t)v) / T >= thr) Zw += out[v];
+  for (int v = 0; v < V; ++v) out[v] = elem(L, dt, off + (size_t)v) / T >= thr ? out[v] / Zw : 0.0;
+  return 0;
+}
+
+/* Chain verification with the warped p' and q' (see above); the same steps,
+ * outputs and flags as orc_verify_chain (lse outputs omitted). Scratch: wp,
+ * wq [V] doubles, tmp [V] entries. */
+void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                             const double* ur, double T, int top_k, double top_p, int B, int K, int V, int b0,
+                             int b1, int32_t* accept_len, int32_t* out_tok, double* px, double* qx, int32_t* status,
+                             int32_t* flags, double* margin, double* wp, double* wq, orc_sv* tmp) {
+  (void)B;
+  for (int b = b0; b < b1; ++b) {
+    int st = 0, fl = 0;
+    double mg = INFINITY, M, Z;
+    for (int k = 0; k <= K; ++k)
+      if (softmax_stats(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, &M, &Z)) st |= ST_TARGET;
+    for (int k = 0; k < K; ++k) {
+      if (softmax_stats(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, &M, &Z)) st |= ST_DRAFT;
+      int xk = x[(size_t)b * K + k];
+      if (xk < 0 || xk >= V) st |= ST_TOKEN;
+    }
+    int32_t* out = out_tok + (size_t)b * (K + 1);
+    for (int j = 0; j <= K; ++j) out[j] = -1;
+    for (int k = 0; k < K; ++k) px[(size_t)b * K + k] = qx[(size_t)b * K + k] = NAN;
+    status[b] = st;
+    if (st) {
+      accept_len[b] = -1;
+      flags[b] = 0;
+      margin[b] = INFINITY;
+      continue;
+    }
+    for (int k = 0; k < K; ++k) {
+      int xk = x[(size_t)b * K + k];
+      warped_row(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, top_k, top_p, wp, tmp);
+      warped_row(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, top_k, top_p, wq, tmp);
+      px[(size_t)b * K + k] = wp[xk];
+      qx[(size_t)b * K + k] = wq[xk];
+    }
+    int m = K;
+    for (int k = 0; k < K; ++k) {
+      double p = px[(size_t)b * K + k], q = qx[(size_t)b * K + k];
+      /* a token outside the draft's kept set (q' = 0, unreachable when x ~ q')
+         is accepted iff the target keeps it */
+      double r = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
+      double u = ua[(size_t)b * K + k];
+      if (r < 1.0) mg = fmin(mg, fabs(u - r));
+      if (r < 1.0 && fabs(u - r) < NEAR) fl |= FL_ACCEPT;
+      if (!(u < r)) {
+        m = k;
+        break;
+      }
+    }
+    accept_len[b] = m;
+    for (int k = 0; k < m; ++k) out[k] = x[(size_t)b * K + k];
+    /* residual max(0, p'_m - q'_m) at a rejection, p'_K for the bonus */
+    warped_row(Lp, dt, ((size_t)b * (K + 1) + m) * (size_t)V, V, T, top_k, top_p, wp, tmp);
+    int residual = m < K;
+    if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp);
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) S += residual ? fmax(0.0, wp[v] - wq[v]) : wp[v];
+    if (residual && !(S > 0.0)) {
+      residual = 0; /* p'_m == q'_m numerically: draw from p'_m */
+      S = 0.0;
+      for (int v = 0; v < V; ++v) S += wp[v];
+    }
+    double t = ur[b] * S, C = 0.0, Cprev = 0.0;
+    int tok = -1, last_pos = -1;
+    for (int v = 0; v < V; ++v) {
+      double w = residual ? fmax(0.0, wp[v] - wq[v]) : wp[v];
+      if (w > 0.0) last_pos = v;
+      Cprev = C;
+      C += w;
+      if (C > t) {
+        tok = v;
+        break;
+      }
+    }
+    if (tok < 0) {
+      tok = last_pos;
+      fl |= FL_SAMPLE;
+      mg = 0.0;
+    } else {
+      double near = fmin(fabs(ur[b] - Cprev / S), fabs(ur[b] - C / S));
+      mg = fmin(mg, near);
+      if (near < NEAR) fl |= FL_SAMPLE;
+    }
+    out[m] = tok;
+    flags[b] = fl;
+    margin[b] = mg;
   }
 }

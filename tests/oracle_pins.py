@@ -584,6 +584,128 @@ def pin_entropy_routing(lib):
     assert r["status"][0] == 4 and r["choice"][0] == -1
 
 
+class WarpedCall(ChainCall):
+    """Single-row call of ``orc_verify_chain_warped`` (top-k, top-p)."""
+
+    def __init__(self, lib, Lp, Lq, x, T, top_k, top_p):
+        super().__init__(lib, Lp, Lq, x, T)
+        self.top_k, self.top_p = int(top_k), float(top_p)
+        V = self.V
+        self.wp, self.wq, self.tmp = np.zeros(V), np.zeros(V), np.zeros(V * 16, np.uint8)
+
+    def __call__(self, ua, ur):
+        self.ua[0, :] = ua
+        self.ur[0] = ur
+        self.lib.orc_verify_chain_warped(_p(self.Lp), _p(self.Lq), oracle.F64, _p(self.x), _p(self.ua), _p(self.ur),
+                                         self.T, self.top_k, self.top_p, 1, self.K, self.V, 0, 1, _p(self.acc),
+                                         _p(self.out), _p(self.px), _p(self.qx), _p(self.st), _p(self.fl),
+                                         _p(self.mg), _p(self.wp), _p(self.wq), _p(self.tmp))
+        assert self.st[0] == 0, "unexpected row status"
+        m = int(self.acc[0])
+        return m, tuple(int(t) for t in self.out[0, : m + 1])
+
+
+def warp_np(l, T, top_k, top_p):
+    """Temperature, top-k (ties kept), then top-p on the renormalised rest
+    (keep v iff the mass of kept tokens strictly above it is < top_p),
+    written with numpy's sort for the test."""
+    s = np.asarray(l, np.float64) / T
+    e = np.exp(s - s.max())
+    keep = np.ones(len(s), bool)
+    if 0 < top_k < len(s):
+        keep &= s >= np.sort(s)[::-1][top_k - 1]
+    if top_p < 1.0:
+        pk = np.where(keep, e, 0.0) / np.where(keep, e, 0.0).sum()
+        above = np.array([pk[(s > s[v]) & keep].sum() for v in range(len(s))])
+        keep &= above < top_p
+    w = np.where(keep, e, 0.0)
+    return w / w.sum()
+
+
+def pin_warped_noop(lib, seed=5):
+    """Sampling settings that keep every token (top-k off or k = V, top-p
+    1) give exactly the plain verification."""
+    rng = np.random.default_rng(seed)
+    B, K, V = 6, 3, 12
+    Lp, Lq = rng.normal(0, 2, (B, K + 1, V)), rng.normal(0, 2, (B, K, V))
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    ua, ur = rng.random((B, K)), rng.random(B)
+    a = oracle.verify_chain(Lp, Lq, x, ua, ur, 0.9, lib=lib)
+    for k in (0, V):
+        b = oracle.verify_chain_warped(Lp, Lq, x, ua, ur, 0.9, top_k=k, top_p=1.0, lib=lib)
+        assert np.array_equal(a["out_tokens"], b["out_tokens"]) and np.array_equal(a["accept_len"], b["accept_len"])
+        assert np.allclose(a["px"], b["px"], rtol=1e-14, atol=0) and np.allclose(a["qx"], b["qx"], rtol=1e-14, atol=0)
+
+
+def pin_warped_topk1_is_greedy(lib, seed=6):
+    """Top-k with k = 1 keeps only each row's top token: with the drafter's
+    own top tokens as drafts the result is greedy verification's."""
+    rng = np.random.default_rng(seed)
+    B, K, V = 8, 3, 9
+    Lp, Lq = rng.normal(0, 2, (B, K + 1, V)), rng.normal(0, 2, (B, K, V))
+    x = Lq.argmax(-1).astype(np.int32)
+    x[::2] = Lp[::2, :K].argmax(-1)  # half the rows accept everything
+    b = oracle.verify_chain_warped(Lp, Lq, x, rng.random((B, K)), rng.random(B), 1.3, top_k=1, lib=lib)
+    g = oracle.verify_chain_greedy(Lp, x, lib=lib)
+    assert np.array_equal(b["accept_len"], g["accept_len"]) and np.array_equal(b["out_tokens"], g["out_tokens"])
+
+
+def pin_warped_examples(lib):
+    """Kept sets by hand: p = (.5, .3, .15, .05) keeps {0, 1} at top-p .79
+    and {0, 1, 2} at .81; ties at the boundary stay together for top-k and
+    top-p."""
+    def pprime(probs, top_k, top_p):
+        V = len(probs)
+        lp = np.log(np.array([probs, probs]))
+        out = []
+        for v in range(V):
+            call = WarpedCall(lib, lp, lp[:1], [v], 1.0, top_k, top_p)
+            call([0.5], 0.5)
+            out.append(float(call.px[0, 0]))
+        return np.array(out)
+    assert np.allclose(pprime([.5, .3, .15, .05], 0, .79), [.625, .375, 0, 0], atol=1e-14)
+    assert np.allclose(pprime([.5, .3, .15, .05], 0, .81), [.5 / .95, .3 / .95, .15 / .95, 0], atol=1e-14)
+    assert np.allclose(pprime([.4, .2, .2, .2], 2, 1.0), [.4, .2, .2, .2], atol=1e-14)  # tie at the 2nd value
+    assert np.allclose(pprime([.4, .2, .2, .2], 0, .5), [.4, .2, .2, .2], atol=1e-14)  # the tied group kept whole
+    assert np.allclose(pprime([.4, .2, .2, .2], 1, 1.0), [1, 0, 0, 0], atol=1e-14)
+    assert np.allclose(pprime([.5, .3, .15, .05], 3, .7), [.5 / .8, .3 / .8, 0, 0], atol=1e-14)  # top-p after top-k
+
+
+def pin_lossless_warped(lib, V, K, T, top_k, top_p, seed):
+    """Losslessness with the sampling settings applied (ariser.io page: p and
+    q must be the distributions the settings produce): drafts drawn from the
+    warped draft law, verified, continued by the warped target, give exactly
+    the warped target's law over V^(K+1) sequences."""
+    lp, lq = random_world(V, K, seed)
+    P = {pre: warp_np(l, T, top_k, top_p) for pre, l in lp.items()}
+    Q = {pre: warp_np(l, T, top_k, top_p) for pre, l in lq.items()}
+    got = defaultdict(float)
+    for x in itertools.product(range(V), repeat=K):
+        wx = 1.0
+        for k in range(K):
+            wx *= Q[x[:k]][x[k]]
+        if wx == 0.0:
+            continue
+        Lp = np.stack([lp[x[:k]] for k in range(K + 1)])
+        Lq = np.stack([lq[x[:k]] for k in range(K)])
+        law = chain_law(WarpedCall(lib, Lp, Lq, x, T, top_k, top_p))
+        for emitted, pr in law.items():
+            n = len(emitted)
+            for cont in itertools.product(range(V), repeat=K + 1 - n):
+                y = emitted + cont
+                w = wx * pr
+                for j in range(n, K + 1):
+                    w *= P[y[:j]][y[j]]
+                got[y] += w
+    err = 0.0
+    for y in itertools.product(range(V), repeat=K + 1):
+        want = 1.0
+        for j in range(K + 1):
+            want *= P[y[:j]][y[j]]
+        err = max(err, abs(got.get(y, 0.0) - want))
+    assert abs(sum(got.values()) - 1.0) < 1e-12 and err < 1e-12, err
+
+
 ALL_PINS = [
     ("ab_example", pin_ab_example),
     ("lossless_V3K2", lambda lib: pin_lossless(lib, 3, 2, 1.0, 1)),
@@ -602,4 +724,10 @@ ALL_PINS = [
     ("kv_strided", pin_kv_strided),
     ("entropy", pin_entropy),
     ("entropy_routing", pin_entropy_routing),
+    ("warped_noop", pin_warped_noop),
+    ("warped_topk1_greedy", pin_warped_topk1_is_greedy),
+    ("warped_examples", pin_warped_examples),
+    ("lossless_warped_topk", lambda lib: pin_lossless_warped(lib, 4, 2, 1.0, 2, 1.0, 7)),
+    ("lossless_warped_topp", lambda lib: pin_lossless_warped(lib, 4, 2, 0.8, 0, 0.7, 8)),
+    ("lossless_warped_both", lambda lib: pin_lossless_warped(lib, 4, 2, 1.2, 3, 0.8, 9)),
 ]

@@ -60,6 +60,14 @@ MUTATIONS = {
     "entropy_higher_wins": ("choice[b] = s2 < s1 ? 2 : 1;", "choice[b] = s2 > s1 ? 2 : 1;"),
     "entropy_root_included": ("for (int i = 1; i <= n1; ++i) s1 += e[i];", "for (int i = 0; i <= n1; ++i) s1 += e[i];"),
     "entropy_empty_tree_zero": ("s2 = n2 > 0 ? s2 / n2 : INFINITY;", "s2 = n2 > 0 ? s2 / n2 : 0.0;"),
+    "warped_topk_off_by_one": ("if (top_k > 0 && top_k < V) tk = tmp[top_k - 1].s;",
+                               "if (top_k > 0 && top_k < V) tk = tmp[top_k].s;"),
+    "warped_topp_drops_crossing_token": ("if (!(cum < top_p * Zk)) break;", "if (!(cum + g < top_p * Zk)) break;"),
+    "warped_topp_on_full_mass": ("if (!(cum < top_p * Zk)) break;", "if (!(cum < top_p * Z)) break;"),
+    "warped_not_renormalised": ("? out[v] / Zw : 0.0;", "? out[v] / Z : 0.0;"),
+    "warped_residual_unwarped_draft": (
+        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp);",
+        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, 0, 1.0, wq, tmp);"),
     "kv_in_place_from_last_row": (
         "      for (int t = 0; t <= L; ++t) {\n        int src = pr ? pr[t] : t;\n        memcpy(tmp + (size_t)t * rowb,",
         "      for (int t = L; t >= 0; --t) {\n        int src = pr ? pr[t] : t;\n"

@@ -44,3 +44,10 @@ def test_tree_with_empty_second_tree_is_chain(orc):
 
 def test_confidence_means(orc):
     P.pin_confidence(orc.load())
+
+
+@pytest.mark.parametrize("name", [n for n, _ in P.ALL_PINS])
+def test_every_pin_holds_on_the_oracle(orc, name):
+    """Each pin the planted-mistake tests rely on passes on the real oracle
+    (so a pin that trips on a mutant is tripping on the mistake)."""
+    dict(P.ALL_PINS)[name](orc.load())
