@@ -133,14 +133,18 @@ def _peaked_rows(rows: int, V: int, g: torch.Generator, boost: float, n_likely: 
     return base
 
 
-def _gumbel_draw(logits: torch.Tensor, T: float, g: torch.Generator) -> torch.Tensor:
+def _gumbel_draw(logits: torch.Tensor, T: float, g: torch.Generator, top_k: int = 0) -> torch.Tensor:
     """Draft tokens drawn from softmax(logits / T) by the Gumbel-max trick
-    (a stand-in for the drafter's own sampling; greedy argmax when T == 0)."""
+    (a stand-in for the drafter's own sampling; greedy argmax when T == 0).
+    top_k > 0: only among each row's k largest logits (ties at the k-th kept)."""
     lf = logits.float()
     if T == 0.0:
         return lf.argmax(dim=-1).to(torch.int32)
     u = torch.rand(lf.shape, generator=g).clamp_(min=1e-30, max=1.0 - 1e-7)
     gumbel = -torch.log(-torch.log(u))
+    if 0 < top_k < lf.shape[-1]:
+        kth = lf.topk(top_k, dim=-1).values[..., -1:]
+        lf = torch.where(lf >= kth, lf, torch.full_like(lf, -float("inf")))
     return (lf / T + gumbel).argmax(dim=-1).to(torch.int32)
 
 
@@ -182,11 +186,12 @@ def chain_tiny(seed: int = 0, B: int = 4, K: int = 4, V: int = 1000, T: float = 
 
 
 def chain_zipf(B: int, K: int, V: int, dtype: torch.dtype, T: float, sigma, seed: int,
-               boost: float = 8.0, n_likely: int = 20, name: str = "chain_zipf") -> ChainBatch:
+               boost: float = 8.0, n_likely: int = 20, name: str = "chain_zipf", draft_top_k: int = 0) -> ChainBatch:
     """Peaked synthetic logits: per position N(0,1) plus ``boost`` on
     ``n_likely`` random ids; draft = target + N(0, sigma_b^2) per row b
     (``sigma`` is a float or a callable ``sigma(g, B) -> [B]``). Draft tokens
-    come from softmax(draft / T) (argmax at T = 0). Built one row at a time
+    come from softmax(draft / T) (argmax at T = 0), among the draft's
+    ``draft_top_k`` largest logits when that is > 0. Built one row at a time
     to bound host memory."""
     g = _gen(seed)
     if callable(sigma):
@@ -202,7 +207,7 @@ def chain_zipf(B: int, K: int, V: int, dtype: torch.dtype, T: float, sigma, seed
         if K > 0:
             lq = base[:K] + float(sig[b]) * torch.randn(K, V, generator=g)
             Lq[b] = lq.to(dtype)
-            x[b] = _gumbel_draw(Lq[b], T, g)
+            x[b] = _gumbel_draw(Lq[b], T, g, draft_top_k)
     ua, ur = _uniforms(B, K, g)
     return ChainBatch(f"{name}_s{seed}", Lp, Lq, x, ua, ur, float(T))
 

@@ -12,6 +12,8 @@
  *     p_K when all K are accepted (Leviathan et al., as summarised on the
  *     ariser.io page, section on keeping the same distribution; lotook.com,
  *     "how does speculative decoding work step by step").
+ *   - spec_verify_chain_warped: the same with top-k / top-p applied to p and
+ *     q (ariser.io page: p and q must reflect the sampling settings).
  *   - spec_verify_chain_greedy: temperature 0, accept while x_k is the
  *     target's top token, then emit the target's top token (lotook.com, same
  *     section and FAQ; SubSpec review, Method 2, the "I left my keys" example).
@@ -84,6 +86,8 @@ enum {
 #define SPEC_ROW_DRAFT 4  /* the same for a draft row */
 #define SPEC_ROW_TREE 8   /* a malformed retrieve row */
 #define SPEC_ROW_MASK 16  /* a retrieve row that contradicts tree_mask */
+#define SPEC_ROW_WARP 32  /* top-p: the nucleus reaches past the row's 4096 largest tokens (whole groups of
+                             equal logits; spec_verify_chain_warped) */
 
 /* Limits: 1 <= B <= 65535; 0 <= K <= 255; 2 <= V <= 2^24; for trees
  * 1 <= N <= 1024, 1 <= D <= 64, 1 <= R <= 4096. */
@@ -160,6 +164,30 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logit
                               float temperature, int B, int K, int V, int32_t* accept_len, int32_t* out_tokens,
                               float* lse_target, float* lse_draft, float* p_at_x, float* q_at_x,
                               int32_t* row_status, void* stream);
+
+/* Chain verification with the sampling settings applied to p and q: the
+ * ariser.io page (section on keeping the same distribution) notes that with
+ * settings such as temperature or top-p the p and q the algorithm uses must
+ * be the distributions those settings produce. Order: temperature, top-k
+ * (every token whose logit is >= the k-th largest is kept, ties included;
+ * 0 = off), then top-p on the renormalised remainder (token v is kept iff
+ * the renormalised mass of kept tokens with a strictly larger logit is below
+ * top_p; 1 = off); the same settings for target and draft; then the steps of
+ * spec_verify_chain on p' and q'. A draft token outside the draft's kept set
+ * (q'(x) = 0, which a draft sampled with these settings never proposes) is
+ * accepted iff the target keeps it.
+ * Arguments as spec_verify_chain (no lse outputs; p_at_x, q_at_x are p', q'),
+ * plus temperature > 0, top_k >= 0, 0 < top_p <= 1. Workspace:
+ * spec_workspace_bytes(B, K, V, dtype). Extra passes over the rows: 2 (bf16)
+ * or 4 (fp32) for top-k; for top-p, 2 / 4 more to find the row's largest
+ * tokens (at most 4096, whole groups of equal logits, or its top-k when
+ * that is fewer) and one collecting them; one summing the kept mass. A row
+ * whose nucleus reaches past those tokens gets SPEC_ROW_WARP. */
+int spec_verify_chain_warped(const void* target_logits, const void* draft_logits, int dtype,
+                             const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                             float temperature, int top_k, float top_p, int B, int K, int V, int32_t* accept_len,
+                             int32_t* out_tokens, float* p_at_x, float* q_at_x, int32_t* row_status, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /* Greedy chain verification (temperature 0): reads target logits only.
  *   target_logits device [B][K+1][V]; draft_tokens device [B][K] int32

@@ -60,6 +60,7 @@
 /* near-tie flags (oracle only): the GPU may legitimately differ here */
 #define FL_ACCEPT 1
 #define FL_SAMPLE 2
+#define FL_WARP 8 /* a top-p decision within NEAR_P of its boundary */
 #define FL_ROUTE 4
 #define NEAR 1e-6
 
@@ -541,9 +542,13 @@ static int orc_sv_desc(const void* a, const void* b) {
 }
 
 /* Warped distribution of one row into out[V] (tmp: V scratch entries).
- * Returns 1 when the row holds a NaN or has no finite maximum. */
+ * Returns 1 when the row holds a NaN or has no finite maximum. *near is set
+ * when the top-p decision of a value group lies within NEAR_P (relative to
+ * the renormalised mass) of the boundary: its preceding mass is that close
+ * to top_p. */
+#define NEAR_P 1e-5
 static int warped_row(const void* L, int dt, size_t off, int V, double T, int top_k, double top_p, double* out,
-                      orc_sv* tmp) {
+                      orc_sv* tmp, int* near) {
   double M, Z;
   if (softmax_stats(L, dt, off, V, T, &M, &Z)) return 1;
   for (int v = 0; v < V; ++v) {
@@ -566,6 +571,7 @@ static int warped_row(const void* L, int dt, size_t off, int V, double T, int to
       int j = i;
       double g = 0.0;
       while (j < V && tmp[j].s == tmp[i].s) g += out[tmp[j++].v];
+      if (near && fabs(cum - top_p * Zk) < NEAR_P * Zk) *near = 1;
       if (!(cum < top_p * Zk)) break; /* this value and every smaller one are dropped */
       tp = tmp[i].s;
       cum += g;
@@ -589,7 +595,7 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
                              int32_t* flags, double* margin, double* wp, double* wq, orc_sv* tmp) {
   (void)B;
   for (int b = b0; b < b1; ++b) {
-    int st = 0, fl = 0;
+    int st = 0, fl = 0, near = 0;
     double mg = INFINITY, M, Z;
     for (int k = 0; k <= K; ++k)
       if (softmax_stats(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, &M, &Z)) st |= ST_TARGET;
@@ -610,8 +616,8 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
     }
     for (int k = 0; k < K; ++k) {
       int xk = x[(size_t)b * K + k];
-      warped_row(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, top_k, top_p, wp, tmp);
-      warped_row(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, top_k, top_p, wq, tmp);
+      warped_row(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, top_k, top_p, wp, tmp, &near);
+      warped_row(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, top_k, top_p, wq, tmp, &near);
       px[(size_t)b * K + k] = wp[xk];
       qx[(size_t)b * K + k] = wq[xk];
     }
@@ -632,9 +638,9 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
     accept_len[b] = m;
     for (int k = 0; k < m; ++k) out[k] = x[(size_t)b * K + k];
     /* residual max(0, p'_m - q'_m) at a rejection, p'_K for the bonus */
-    warped_row(Lp, dt, ((size_t)b * (K + 1) + m) * (size_t)V, V, T, top_k, top_p, wp, tmp);
+    warped_row(Lp, dt, ((size_t)b * (K + 1) + m) * (size_t)V, V, T, top_k, top_p, wp, tmp, &near);
     int residual = m < K;
-    if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp);
+    if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp, &near);
     double S = 0.0;
     for (int v = 0; v < V; ++v) S += residual ? fmax(0.0, wp[v] - wq[v]) : wp[v];
     if (residual && !(S > 0.0)) {
@@ -664,7 +670,7 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
       if (near < NEAR) fl |= FL_SAMPLE;
     }
     out[m] = tok;
-    flags[b] = fl;
+    flags[b] = fl | (near ? FL_WARP : 0);
     margin[b] = mg;
   }
 }

@@ -9,6 +9,7 @@ __all__ = [
     "spec_verify_chain",
     "spec_chain_scan",
     "spec_chain_sample",
+    "spec_verify_chain_warped",
     "spec_verify_chain_greedy",
     "spec_verify_tree_greedy",
     "spec_tree_confidence",

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "libspecverify.so")
 
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_WORKSPACE, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, -1, -2, -3, -4
-SPEC_ROW_TOKEN, SPEC_ROW_TARGET, SPEC_ROW_DRAFT, SPEC_ROW_TREE, SPEC_ROW_MASK = 1, 2, 4, 8, 16
+SPEC_ROW_TOKEN, SPEC_ROW_TARGET, SPEC_ROW_DRAFT, SPEC_ROW_TREE, SPEC_ROW_MASK, SPEC_ROW_WARP = 1, 2, 4, 8, 16, 32
 
 P = ctypes.c_void_p
 I = ctypes.c_int
@@ -28,6 +28,7 @@ SIGNATURES = {
     "spec_verify_chain_noalloc": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P]),
     "spec_chain_scan": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P, Z, P]),
     "spec_chain_sample": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P, Z, P]),
+    "spec_verify_chain_warped": (I, [P, P, I, P, P, P, F, I, F, I, I, I, P, P, P, P, P, P, Z, P]),
     "spec_verify_chain_greedy": (I, [P, I, P, I, I, I, P, P, P, P, P, Z, P]),
     "spec_verify_tree_greedy": (I, [P, I, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, Z, P]),
     "spec_tree_confidence": (I, [P, I, I, I, P, P, P]),

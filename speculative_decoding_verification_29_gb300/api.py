@@ -275,3 +275,35 @@ def spec_merge_trees(tokens1, mask1, retrieve1, pos1, tokens2, mask2, retrieve2,
                                                    _ptr(out["retrieve"]), _ptr(out["pos"]), _stream(stream)))
     out["n1"] = n1
     return out
+
+
+def spec_verify_chain_warped(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
+                             top_k: int = 0, top_p: float = 1.0, out: Optional[Dict[str, torch.Tensor]] = None,
+                             workspace: Optional[torch.Tensor] = None, device="cuda",
+                             stream=None) -> Dict[str, torch.Tensor]:
+    """Chain verification with top-k / top-p applied to p and q (0 and 1.0:
+    off). Returns accept_len, out_tokens, row_status, p_at_x, q_at_x."""
+    lib = _lib.load()
+    dev = target_logits.device if target_logits.device.type == "cuda" else torch.device(device)
+    Lp, Lq = _dev(target_logits, dev), _dev(draft_logits, dev)
+    B, K1, V = Lp.shape
+    K = K1 - 1
+    x = _dev(draft_tokens, dev, torch.int32)
+    ua = _dev(u_accept, dev, torch.float32)
+    ur = _dev(u_resample, dev, torch.float32)
+    code = _dtype_code(Lp)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(B, K, V, code), dev)
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev),
+                   p_at_x=torch.empty(B, K, dtype=torch.float32, device=dev),
+                   q_at_x=torch.empty(B, K, dtype=torch.float32, device=dev))
+    check("spec_verify_chain_warped",
+          lib.spec_verify_chain_warped(Lp.data_ptr(), Lq.data_ptr(), code, _ptr(x), _ptr(ua), _ptr(ur),
+                                       float(temperature), int(top_k), float(top_p), B, K, V,
+                                       _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out.get("p_at_x")),
+                                       _ptr(out.get("q_at_x")), _ptr(out["row_status"]), workspace.data_ptr(),
+                                       workspace.numel(), _stream(stream)))
+    return out

@@ -39,17 +39,26 @@ size_t up256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
 // Workspace: the rowscan partials, one float pair per warp segment of every
 // row, sized for the larger of the vector and scalar load paths so that the
-// size depends only on the shapes, never on pointer alignment.
+// size depends only on the shapes, never on pointer alignment; then, for the
+// sampling settings, one record, threshold and flag per row.
 struct Layout {
-  size_t part, total;
+  size_t part, rec, vtau, flag, total;
 };
 
 Layout layout(int B, int TR, int DR, int V, int dtype) {
   const long long nrows = static_cast<long long>(B) * (TR + DR);
   const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
   Layout L{};
-  L.part = 0;
-  L.total = up256(static_cast<size_t>(nrows * P) * sizeof(float2));
+  size_t off = 0;
+  L.part = off;
+  off += up256(static_cast<size_t>(nrows * P) * sizeof(float2));
+  L.rec = off;
+  off += up256(static_cast<size_t>(nrows) * sizeof(StatRec));
+  L.vtau = off;
+  off += up256(static_cast<size_t>(nrows) * sizeof(float));
+  L.flag = off;
+  off += up256(static_cast<size_t>(nrows) * sizeof(int32_t));
+  L.total = off;
   return L;
 }
 
@@ -134,6 +143,8 @@ struct ChainCall {
   void* ws;
   size_t ws_bytes;
   cudaStream_t st;
+  int top_k = 0;  // sampling settings (0 and 1: off)
+  float top_p = 1.f;
 };
 
 int chain_validate(const ChainCall& c, Layout* L, bool* vec) {
@@ -189,6 +200,28 @@ int chain_sample(const ChainCall& c) {
   t.accept_len = c.accept_len;
   t.out_tokens = c.out_tokens;
   t.row_status = c.row_status;
+  if (c.top_k > 0 || c.top_p < 1.f) {  // records of the sampling settings' kept sets
+    SelArgs s{};
+    s.A = c.Lp;
+    s.Bd = c.Lq;
+    s.B = c.B;
+    s.TR = c.K + 1;
+    s.DR = c.K;
+    s.V = c.V;
+    s.P = t.P;
+    s.c_hi = t.c_hi;
+    s.c_lo = t.c_lo;
+    s.top_k = c.top_k;
+    s.top_p = c.top_p;
+    s.part = t.part;
+    s.rec = reinterpret_cast<StatRec*>(at(c.ws, L.rec));
+    s.vtau = reinterpret_cast<float*>(at(c.ws, L.vtau));
+    s.row_flag = reinterpret_cast<int32_t*>(at(c.ws, L.flag));
+    if (launch_warp_select(s, c.dtype, vec, c.st) != cudaSuccess) return SPEC_ERR_CUDA;
+    t.rec = s.rec;
+    t.vtau = s.vtau;
+    t.row_flag = s.row_flag;
+  }
   t.lse_p = c.lse_p;
   t.lse_q = c.lse_q;
   t.px = c.px;
@@ -240,6 +273,22 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
   }
   CHAIN_CALL;
   if ((e = chain_scan(c))) return e;
+  return chain_sample(c);
+}
+
+int spec_verify_chain_warped(const void* target_logits, const void* draft_logits, int dtype,
+                             const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                             float temperature, int top_k, float top_p, int B, int K, int V, int32_t* accept_len,
+                             int32_t* out_tokens, float* p_at_x, float* q_at_x, int32_t* row_status, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!(temperature > 0.f) || top_k < 0 || !(top_p > 0.f) || !(top_p <= 1.f)) return SPEC_ERR_ARG;
+  float* lse_target = nullptr;
+  float* lse_draft = nullptr;
+  CHAIN_CALL;
+  c.top_k = top_k >= V ? 0 : top_k;
+  c.top_p = top_p;
+  int e = chain_scan(c);
+  if (e) return e;
   return chain_sample(c);
 }
 

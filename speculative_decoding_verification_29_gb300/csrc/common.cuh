@@ -211,6 +211,8 @@ __device__ __forceinline__ float2 ds_div(float2 a, float2 b) {
   return make_float2(hi, r - (hi - q));
 }
 __device__ __forceinline__ double ds_to_d(float2 a) { return static_cast<double>(a.x) + static_cast<double>(a.y); }
+// hi + lo > t.hi + t.lo for normalised float pairs.
+__device__ __forceinline__ bool ds_gt(float2 a, float2 t) { return a.x > t.x || (a.x == t.x && a.y > t.y); }
 
 // -------------------------------------------------------- combinations --
 

@@ -51,7 +51,8 @@ struct DecRec {
   float Mp, Mq;      // raw-logit maxima of target row m and draft row m
   float dM;          // Mp - Mq
   float D_hi, D_lo;  // log2(Zp / Zq) as a float pair
-  float pad2[3];
+  float vtp, vtq;    // sampling settings: kept iff logit >= these (-inf: all)
+  float pad2;
 };
 
 struct ScanArgs {
@@ -109,6 +110,9 @@ struct TailArgs {
   float* lse_q;
   float* px;
   float* qx;
+  const StatRec* rec;       // sampling settings: per-row kept mass records (NULL: none)
+  const float* vtau;        // per-row kept thresholds
+  const int32_t* row_flag;  // per-row SPEC_ROW_WARP bits
 };
 
 // Weighing geometry of the tail kernel for rows of nv vectors.
@@ -132,6 +136,22 @@ cudaError_t launch_tree_finish(const TreeArgs& a, cudaStream_t st);
 
 cudaError_t launch_tree_confidence(const float* conf, int B, int N, int n1, float* scores, int32_t* choice,
                                    cudaStream_t st);
+
+// Sampling settings (top-k, top-p) applied to p and q: per-row thresholds.
+struct SelArgs {
+  const void* A;   // target rows [B][TR][V]
+  const void* Bd;  // draft rows  [B][DR][V]
+  int B, TR, DR, V, P;
+  float c_hi, c_lo;  // log2(e) / T, c_lo > 0
+  int top_k;         // 0: off
+  float top_p;       // 1: off
+  const float2* part;  // stats partials [B * (TR + DR)][P]
+  StatRec* rec;        // [rows]: M, kept mass Z', log2 Z'
+  float* vtau;         // [rows]: a token is kept iff its logit >= vtau
+  int32_t* row_flag;   // [rows]: SPEC_ROW_WARP or 0
+};
+int select_candidates();
+cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st);
 
 // Entropy routing of two drafter trees (after the rowscan in entropy mode).
 struct EntArgs {

@@ -1,0 +1,372 @@
+// select.cu -- the sampling settings applied to p and q: per row, the
+// threshold of the kept tokens under top-k and top-p and the kept mass.
+//
+// The ariser.io page (section on keeping the same distribution) notes that
+// with sampling settings such as top-p the p and q the verification uses
+// must be the distributions those settings produce. Order applied here:
+// temperature, top-k (every token whose logit is >= the k-th largest is
+// kept, ties included), then top-p on the renormalised remainder (token v is
+// kept iff the mass of the kept tokens with a strictly larger logit is below
+// top_p). Both keep a set {v : key(l_v) >= tau}, key the order-preserving
+// unsigned image of the logit's bits.
+//
+// One CTA per row, after the stats pass (its partials give M and Z):
+//   top-k: radix select of the k-th largest key, 8 bits per pass over the
+//          row (2 passes for bf16, 4 for fp32), counts only: exact;
+//   top-p: the row's largest tokens, whole groups of equal logits and at
+//          most kCand of them (its top-k when that is fewer), are collected
+//          into shared memory, sorted by key, and their weights
+//          2^((l - M) log2(e) / T) scanned in float pairs; the last token
+//          whose preceding mass is below top_p * Z_k fixes tau. A row whose
+//          nucleus reaches past the collected tokens is flagged
+//          (SPEC_ROW_WARP);
+//   the kept mass Z' is the scan's total at tau, or (top-k alone) a pass
+//   summing the kept weights in float pairs.
+// Output per row: (M, Z', log2 Z') as a StatRec and tau.
+#include "fold.cuh"
+
+namespace specv {
+
+namespace {
+
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kCand = 4096;
+
+template <typename Raw>
+struct Key;
+// Order-preserving unsigned key of a logit's bits, -0 merged into +0 (equal
+// values tie), and the value of the element's bits.
+template <>
+struct Key<uint16_t> {
+  static constexpr int kBits = 16;
+  __device__ static __forceinline__ uint32_t of(uint32_t b) {
+    b = b == 0x8000u ? 0u : b;
+    return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+  }
+  __device__ static __forceinline__ float val(uint32_t b) { return __uint_as_float(b << 16); }
+};
+template <>
+struct Key<float> {
+  static constexpr int kBits = 32;
+  __device__ static __forceinline__ uint32_t of(uint32_t b) {
+    b = b == 0x80000000u ? 0u : b;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  __device__ static __forceinline__ float val(uint32_t b) { return __uint_as_float(b); }
+};
+
+// Value of the smallest logit whose key is >= tau (-inf for tau = 0: keep all).
+template <typename Raw>
+__device__ __forceinline__ float key_value(uint32_t tau) {
+  if (tau == 0u) return -INFINITY;
+  if constexpr (sizeof(Raw) == 2) {
+    const uint32_t b = (tau & 0x8000u) ? (tau & 0x7FFFu) : (~tau & 0xFFFFu);
+    return __uint_as_float(b << 16);
+  } else {
+    return __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
+  }
+}
+
+// Calls f(bits) for every element of the row (16-byte loads when VEC).
+template <typename Raw, bool VEC, typename F>
+__device__ __forceinline__ void for_row(const Raw* row, int V, F f) {
+  if constexpr (VEC) {
+    constexpr int EPV = Elem<Raw>::kPerVec;
+    const int nv = V / EPV;
+    for (int vi = threadIdx.x; vi < nv; vi += kSelThreads) {
+      const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row) + vi);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if constexpr (EPV == 8) {
+          f(w[i] & 0xFFFFu);
+          f(w[i] >> 16);
+        } else {
+          f(w[i]);
+        }
+      }
+    }
+  } else {
+    for (int v = threadIdx.x; v < V; v += kSelThreads) {
+      if constexpr (sizeof(Raw) == 2)
+        f(static_cast<uint32_t>(row[v]));
+      else
+        f(__float_as_uint(row[v]));
+    }
+  }
+}
+
+// Largest key K with #{keys >= K} >= k (the k-th largest key), over the
+// row, by 8-bit digits from the top. hist: kSelWarps x 256 counters.
+template <typename Raw, bool VEC>
+__device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, unsigned* s_tot, uint32_t* s_sel) {
+  using KY = Key<Raw>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t prefix = 0;
+  unsigned kk = static_cast<unsigned>(k);
+  for (int shift = KY::kBits - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < kSelWarps * 256; i += kSelThreads) hist[i] = 0;
+    __syncthreads();
+    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+    unsigned* h = hist + warp * 256;
+    for_row<Raw, VEC>(row, V, [&](uint32_t b) {
+      const uint32_t key = KY::of(b);
+      if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(h + ((key >> shift) & 0xFFu), 1u);
+    });
+    __syncthreads();
+    for (int bin = tid; bin < 256; bin += kSelThreads) {
+      unsigned c = 0;
+      for (int w = 0; w < kSelWarps; ++w) c += hist[w * 256 + bin];
+      s_tot[bin] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {  // bin where the count from the top reaches kk: lane l holds bins 255-8l .. 248-8l
+      unsigned c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = s_tot[255 - 8 * lane - i];
+        sum += c[i];
+      }
+      unsigned incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      unsigned above = incl - sum;  // count in higher bins than this lane's
+      const bool here = above < kk && kk <= incl;
+      const unsigned hit = __ballot_sync(0xffffffffu, here);
+      if (hit && lane == __ffs(hit) - 1) {
+        int i = 0;
+        while (above + c[i] < kk) above += c[i++];
+        s_sel[0] = static_cast<uint32_t>(255 - 8 * lane - i);
+        s_sel[1] = kk - above;
+      }
+      if (!hit && lane == 0) {  // fewer than kk keys match: keep them all (cannot happen for k <= V)
+        s_sel[0] = 0;
+        s_sel[1] = 1;
+      }
+    }
+    __syncthreads();
+    prefix |= s_sel[0] << shift;
+    kk = s_sel[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Sum of float pairs over the block (every thread gets it); sh: kSelWarps pairs.
+__device__ __forceinline__ float2 block_sum_ds(float2 v, float2* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    v = ds_add(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o)));
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+  for (int w = 0; w < kSelWarps; ++w) t = ds_add(t, sh[w]);
+  __syncthreads();
+  return t;
+}
+
+// Sum of the weights of the keys >= tau over the row, as a float pair
+// (every thread gets it): fp32 runs of 64 terms folded into a float pair.
+template <typename Raw, bool VEC, typename W>
+__device__ float2 kept_mass(const Raw* row, int V, uint32_t tau, W weight, float2* sh) {
+  float acc = 0.f;
+  float2 z = make_float2(0.f, 0.f);
+  int cnt = 0;
+  for_row<Raw, VEC>(row, V, [&](uint32_t bits) {
+    if (Key<Raw>::of(bits) >= tau) {
+      acc += weight(bits);
+      if (++cnt == 64) {
+        z = ds_add(z, make_float2(acc, 0.f));
+        acc = 0.f;
+        cnt = 0;
+      }
+    }
+  });
+  return block_sum_ds(ds_add(z, make_float2(acc, 0.f)), sh);
+}
+
+template <typename Raw, bool VEC>
+__global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
+  using KY = Key<Raw>;
+  const int row_id = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int RPG = a.TR + a.DR;
+  const int b = row_id / RPG, j = row_id - b * RPG;
+  const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
+                            : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
+  // shared memory: the radix histograms, later reused for the candidates
+  __shared__ __align__(16) uint32_t s_buf[2 * kCand];
+  unsigned* hist = s_buf;                                    // kSelWarps x 256 counters
+  uint32_t* s_key = s_buf;                                   // kCand keys
+  float* s_w = reinterpret_cast<float*>(s_buf + kCand);      // kCand weights
+  static_assert(kSelWarps * 256 <= 2 * kCand, "histograms fit the candidate buffer");
+  __shared__ unsigned s_tot[256];
+  __shared__ uint32_t s_sel[2];
+  __shared__ float2 s_ds[kSelWarps];
+  __shared__ int s_n, s_last;
+  __shared__ float s_M;
+  __shared__ float2 s_Z;
+  griddep_launch_dependents();
+  griddep_wait();
+  if (warp == 0) {  // M and Z of the row from the stats partials
+    float2 z;
+    const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+    if (lane == 0) {
+      s_M = M;
+      s_Z = z;
+    }
+  }
+  __syncthreads();
+  const float M = s_M;
+  const float2 Zfull = s_Z;
+  const bool ok = M == M && isfinite(M) && Zfull.x > 0.f;
+  auto weight = [&](uint32_t bits) {
+    const float d = KY::val(bits) - M;
+    return ex2_fast(fmaf(d, a.c_hi, d * a.c_lo));
+  };
+  StatRec out;
+  out.M = M;
+  out.Z = NAN;
+  out.Lhi = out.Llo = NAN;
+  uint32_t tau = 0;  // keep keys >= tau
+  int st = 0;
+  if (ok) {
+    const bool use_k = a.top_k > 0 && a.top_k < a.V;
+    if (use_k) tau = kth_largest<Raw, VEC>(row, a.V, a.top_k, hist, s_tot, s_sel);
+    if (a.top_p < 1.f) {
+      // candidates: the keys >= tc, whole groups of equal keys and at most
+      // kCand of them: tc is one above the (kCand + 1)-th largest key, or the
+      // top-k threshold when that is higher ("own": the candidates are then
+      // every token top-k keeps, and the whole row when top-k is off)
+      uint32_t tc = tau;
+      bool own = true;
+      if (a.V > kCand) {
+        const uint32_t kc = kth_largest<Raw, VEC>(row, a.V, kCand + 1, hist, s_tot, s_sel) + 1u;
+        if (kc > tc) {
+          tc = kc;
+          own = false;
+        }
+      }
+      float2 Zk = Zfull;
+      if (use_k && !own) Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);
+      if (tid == 0) s_n = 0;
+      __syncthreads();
+      for_row<Raw, VEC>(row, a.V, [&](uint32_t bits) {
+        const uint32_t key = KY::of(bits);
+        if (key >= tc) {
+          const int slot = atomicAdd(&s_n, 1);
+          if (slot < kCand) {
+            s_key[slot] = key;
+            s_w[slot] = weight(bits);
+          }
+        }
+      });
+      __syncthreads();
+      const int n = s_n;  // <= kCand by the choice of tc (checked all the same)
+      if (n > kCand) {
+        st = SPEC_ROW_WARP;
+      } else {
+        // bitonic sort, keys descending, padded to a power of two with key 0 (weight 0)
+        int n2 = 1;
+        while (n2 < n) n2 <<= 1;
+        for (int i = n + tid; i < n2; i += kSelThreads) {
+          s_key[i] = 0u;
+          s_w[i] = 0.f;
+        }
+        __syncthreads();
+        for (int size = 2; size <= n2; size <<= 1)
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < n2; i += kSelThreads) {
+              const int pj = i ^ stride;
+              if (pj > i) {
+                const bool desc = (i & size) == 0;
+                const uint32_t ki = s_key[i], kj = s_key[pj];
+                if (desc ? (ki < kj) : (ki > kj)) {
+                  s_key[i] = kj;
+                  s_key[pj] = ki;
+                  const float t = s_w[i];
+                  s_w[i] = s_w[pj];
+                  s_w[pj] = t;
+                }
+              }
+            }
+            __syncthreads();
+          }
+        // masses in key order: thread t owns entries kPer t .. kPer t + kPer - 1
+        constexpr int kPer = kCand / kSelThreads;
+        float2 mine = make_float2(0.f, 0.f);
+        for (int i = 0; i < kPer; ++i) {
+          const int e = tid * kPer + i;
+          if (e < n) mine = ds_add(mine, make_float2(s_w[e], 0.f));
+        }
+        float2 inc = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float2 y = make_float2(__shfl_up_sync(0xffffffffu, inc.x, o), __shfl_up_sync(0xffffffffu, inc.y, o));
+          if (lane >= o) inc = ds_add(y, inc);
+        }
+        float2 wex = make_float2(__shfl_up_sync(0xffffffffu, inc.x, 1), __shfl_up_sync(0xffffffffu, inc.y, 1));
+        if (lane == 0) wex = make_float2(0.f, 0.f);
+        if (lane == 31) s_ds[warp] = inc;
+        if (tid == 0) s_last = -1;
+        __syncthreads();
+        float2 before = make_float2(0.f, 0.f), total = before;
+        for (int w = 0; w < kSelWarps; ++w) {
+          if (w < warp) before = ds_add(before, s_ds[w]);
+          total = ds_add(total, s_ds[w]);
+        }
+        before = ds_add(before, wex);  // mass of the entries before this thread's first
+        if (own) Zk = total;           // the candidates are exactly the kept-by-top-k set
+        const float2 target = ds_mul_f(Zk, a.top_p);
+        int last = -1;
+        for (int i = 0; i < kPer; ++i) {
+          const int e = tid * kPer + i;
+          if (e < n && ds_gt(target, before)) last = e;
+          if (e < n) before = ds_add(before, make_float2(s_w[e], 0.f));
+        }
+        if (last >= 0) atomicMax(&s_last, last);
+        __syncthreads();
+        const int L = s_last;
+        // every candidate kept while tokens outside them hold mass before the target
+        const bool beyond = !own && L == n - 1 && ds_gt(target, total);
+        if (L < 0 || beyond) {
+          st = SPEC_ROW_WARP;
+        } else if (s_key[L] > tau) {
+          tau = s_key[L];
+        }
+        __syncthreads();  // s_key and s_w are free again
+      }
+    }
+    if (st == 0) {
+      const float2 Zw = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);
+      const float2 L2 = ds_log2(Zw);
+      out.Z = Zw.x;
+      out.Lhi = L2.x;
+      out.Llo = L2.y;
+    }
+  }
+  if (tid == 0) {
+    a.rec[row_id] = out;
+    a.vtau[row_id] = key_value<Raw>(tau);
+    a.row_flag[row_id] = st;
+  }
+}
+
+}  // namespace
+
+int select_candidates() { return kCand; }
+
+cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(static_cast<long long>(a.B) * (a.TR + a.DR))), block(kSelThreads);
+  if (dtype == SPEC_BF16)
+    return vec ? launch_pdl(warp_select_kernel<uint16_t, true>, grid, block, st, a)
+               : launch_pdl(warp_select_kernel<uint16_t, false>, grid, block, st, a);
+  return vec ? launch_pdl(warp_select_kernel<float, true>, grid, block, st, a)
+             : launch_pdl(warp_select_kernel<float, false>, grid, block, st, a);
+}
+
+}  // namespace specv

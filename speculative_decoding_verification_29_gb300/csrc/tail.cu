@@ -51,6 +51,7 @@ __device__ __forceinline__ float logit_at(const void* base, long long row, int V
 struct Consts {
   float Mp, dM, D_hi, D_lo, c_hi, c_lo;
   int mode;
+  float vtp, vtq;  // sampling settings: a token is kept iff its logit >= these (-inf: all)
 };
 
 // H(d) = (1 - 2^d) / d on [-1, 0] as sum_n kH[n] d^n: coefficients fitted
@@ -58,13 +59,19 @@ struct Consts {
 __constant__ float kH[6] = {-6.931471825e-01f, -2.402261496e-01f, -5.549939722e-02f,
                             -9.596990421e-03f, -1.291199587e-03f, -1.146293362e-04f};
 
-// Weights of two elements from their target and draft logits (packed).
+// Weights of two elements from their target and draft logits (packed). W:
+// the sampling settings' kept sets apply (weight 0 outside the target's,
+// plain p' outside the draft's).
+template <bool W>
 __device__ __forceinline__ float2 weight2(float2 lp, float2 lq, const Consts& k) {
   const float2 ch = make_float2(k.c_hi, k.c_hi), cl = make_float2(k.c_lo, k.c_lo);
   const float2 d = add2(lp, make_float2(-k.Mp, -k.Mp));
   const float2 a = fma2(d, ch, mul2(d, cl));  // (lp - Mp) * log2(e) / T; -inf stays -inf (c_lo > 0)
   const float2 pt = make_float2(ex2_fast(a.x), ex2_fast(a.y));
-  if (k.mode != 0) return pt;
+  if (k.mode != 0) {
+    if constexpr (W) return make_float2(lp.x >= k.vtp ? pt.x : 0.f, lp.y >= k.vtp ? pt.y : 0.f);
+    return pt;
+  }
   const float2 f = add2(fma2(lp, make_float2(-1.f, -1.f), lq), make_float2(k.dM, k.dM));  // (lq - Mq) - (lp - Mp)
   const float2 dl = add2(fma2(f, ch, fma2(f, cl, make_float2(k.D_lo, k.D_lo))), make_float2(k.D_hi, k.D_hi));
   // dl = log2(q / p); 1 - 2^dl = dc * H(dc) with dc = min(dl, 0) (0 where q >= p,
@@ -76,23 +83,29 @@ __device__ __forceinline__ float2 weight2(float2 lp, float2 lq, const Consts& k)
   const float2 g1 = mul2(dc, h);
   const float2 g2 = fma2(make_float2(ex2_fast(dl.x), ex2_fast(dl.y)), make_float2(-1.f, -1.f), make_float2(1.f, 1.f));
   const float2 g = make_float2(dl.x <= -1.f ? g2.x : g1.x, dl.y <= -1.f ? g2.y : g1.y);
-  return mul2(pt, g);
+  float2 w = mul2(pt, g);
+  if constexpr (W) {
+    w.x = lp.x >= k.vtp ? (lq.x >= k.vtq ? w.x : pt.x) : 0.f;
+    w.y = lp.y >= k.vtp ? (lq.y >= k.vtq ? w.y : pt.y) : 0.f;
+  }
+  return w;
 }
 
+template <bool W>
 __device__ __forceinline__ float weight1(float lp, float lq, const Consts& k) {
-  return weight2(make_float2(lp, lp), make_float2(lq, lq), k).x;
+  return weight2<W>(make_float2(lp, lp), make_float2(lq, lq), k).x;
 }
 
 // Weights of the elements of one 16-byte vector pair, in element order, and
 // their fp32 sum (even and odd elements summed apart, then added; w may be
 // NULL).
-template <typename Raw>
+template <typename Raw, bool W>
 __device__ __forceinline__ float vec_weights(const uint4& p, const uint4& q, const Consts& k, float* w) {
   using Vt = Vec<Raw>;
   float2 s = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < Vt::kPairs; ++i) {
-    const float2 x = weight2(Vt::pair(p, i), Vt::pair(q, i), k);
+    const float2 x = weight2<W>(Vt::pair(p, i), Vt::pair(q, i), k);
     if (w) {
       w[2 * i] = x.x;
       w[2 * i + 1] = x.y;
@@ -124,7 +137,7 @@ constexpr int kUW = 8;
 constexpr int kNU = kBW * kUW;  // units per batch row, ascending token order
 static_assert(kNU == 512, "the draw gives each lane of one warp 16 units");
 
-template <typename Raw, bool VEC>
+template <typename Raw, bool VEC, bool W>
 struct Block {
   static constexpr int EPV = VEC ? Elem<Raw>::kPerVec : 1;
 
@@ -152,9 +165,9 @@ struct Block {
       return 0.f;
     }
     if constexpr (VEC) {
-      return vec_weights<Raw>(p, q, k, w);
+      return vec_weights<Raw, W>(p, q, k, w);
     } else {
-      const float v = weight1(__uint_as_float(p.x), __uint_as_float(q.x), k);
+      const float v = weight1<W>(__uint_as_float(p.x), __uint_as_float(q.x), k);
       if (w) w[0] = v;
       return v;
     }
@@ -265,14 +278,20 @@ __device__ __forceinline__ bool row_ok(const StatRec& r) { return isfinite(r.M) 
 // lane k forms log2 r_k = (l_p - M_p - l_q + M_q) log2(e) / T + log2 Z_q -
 // log2 Z_p and r_k = 2^that (relative error about 1e-6 at worst; decisions
 // within 1e-5 of the threshold are taken in fp64). Outputs are written when
-// `write`; the decision goes to *dec.
+// `write`; the decision goes to *dec. W: the sampling settings' kept sets
+// apply (s_vt: per row, a token is kept iff its logit >= s_vt; rr holds the
+// kept masses): p'(x) = 0 outside the target's set, and a token outside
+// the draft's set is accepted iff the target keeps it.
+template <bool W>
 __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane, const StatRec* rr, const float* s_lp,
-                                          const float* s_lq, const float* s_u, const int* s_x, bool write,
-                                          DecRec* dec) {
+                                          const float* s_lq, const float* s_u, const int* s_x, const float* s_vt,
+                                          const int* s_rf, bool write, DecRec* dec) {
   const int K = a.K, V = a.V, RPG = 2 * K + 1;
   int st = 0;
-  for (int j = lane; j < RPG; j += 32)
-    if (!row_ok(rr[j])) st |= j <= K ? SPEC_ROW_TARGET : SPEC_ROW_DRAFT;
+  for (int j = lane; j < RPG; j += 32) {
+    if (W && s_rf[j]) st |= s_rf[j];
+    else if (!row_ok(rr[j])) st |= j <= K ? SPEC_ROW_TARGET : SPEC_ROW_DRAFT;
+  }
   for (int k = lane; k < K; k += 32)
     if (s_x[k] < 0 || s_x[k] >= V) st |= SPEC_ROW_TOKEN;
   st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
@@ -288,13 +307,16 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
       const float u = s_u[k];
       Dk = ds_add(make_float2(rp.Lhi, rp.Llo), make_float2(-rq.Lhi, -rq.Llo));
       float r;
-      if (lq == -INFINITY) {
-        r = INFINITY;  // q(x) = 0: accept
+      const bool kp = !W || lp >= s_vt[k], kq = !W || lq >= s_vt[K + 1 + k];
+      if (!kq || lq == -INFINITY) {
+        r = (kp && lp > -INFINITY) || !W ? INFINITY : 0.f;  // q(x) = 0: accept (W: iff p'(x) > 0)
+      } else if (!kp) {
+        r = 0.f;  // p'(x) = 0: reject
       } else {
         const float du = (lp - rp.M) - (lq - rq.M);  // exact for bf16 logits
         r = ex2_fast(fmaf(du, a.c_hi, du * a.c_lo) - (Dk.x + Dk.y));
       }
-      if (r < 1.f && fabsf(u - r) < 1e-5f) {  // near the threshold: decide in fp64
+      if (kp && kq && r < 1.f && fabsf(u - r) < 1e-5f) {  // near the threshold: decide in fp64
         rej = !(static_cast<double>(u) < ratio_fp64(lp, rp.M, lq, rq.M, a.invT, rp.Z, rq.Z));
       } else {
         rej = !(u < r);
@@ -325,11 +347,14 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
     if (st == 0) {
       d.mode = m < K ? 0 : 1;
       d.Mp = rr[m].M;
+      d.vtp = W ? s_vt[m] : -INFINITY;
+      d.vtq = -INFINITY;
       if (m < K) {
         d.Mq = rr[K + 1 + m].M;
         d.dM = d.Mp - d.Mq;
         d.D_hi = Dm.x;
         d.D_lo = Dm.y;
+        if (W) d.vtq = s_vt[K + 1 + m];
       }
     }
     *dec = d;
@@ -337,13 +362,14 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
 }
 
 // Optional float outputs for batch row b on one warp: lse of every row and
-// p_k(x_k), q_k(x_k) (NaN when the row is flagged).
+// p_k(x_k), q_k(x_k) (NaN when the row is flagged; W: the warped p', q').
+template <bool W>
 __device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane, const StatRec* rr, const float* s_lp,
-                                           const float* s_lq, const int* s_x) {
+                                           const float* s_lq, const int* s_x, const float* s_vt, const int* s_rf) {
   const int K = a.K, V = a.V, RPG = 2 * K + 1;
   int st = 0;
   for (int j = lane; j < RPG; j += 32)
-    if (!row_ok(rr[j])) st = 1;
+    if (!row_ok(rr[j]) || (W && s_rf[j])) st = 1;
   for (int k = lane; k < K; k += 32)
     if (s_x[k] < 0 || s_x[k] >= V) st = 1;
   st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
@@ -354,6 +380,8 @@ __device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane
       const float up = s_lp[k] - rp.M, uq = s_lq[k] - rq.M;
       pxv = ex2_fast(fmaf(up, a.c_hi, up * a.c_lo) - rp.Lhi - rp.Llo);
       qxv = ex2_fast(fmaf(uq, a.c_hi, uq * a.c_lo) - rq.Lhi - rq.Llo);
+      if (W && !(s_lp[k] >= s_vt[k])) pxv = 0.f;
+      if (W && !(s_lq[k] >= s_vt[K + 1 + k])) qxv = 0.f;
     }
     const long long ik = static_cast<long long>(b) * K + k;
     if (a.px) a.px[ik] = pxv;
@@ -373,8 +401,6 @@ __device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane
   }
 }
 
-// hi + lo > t.hi + t.lo for normalised float pairs.
-__device__ __forceinline__ bool ds_gt(float2 a, float2 t) { return a.x > t.x || (a.x == t.x && a.y > t.y); }
 
 // Inclusive warp scan of float pairs.
 __device__ __forceinline__ float2 warp_scan_ds(float2 x, int lane) {
@@ -388,9 +414,9 @@ __device__ __forceinline__ float2 warp_scan_ds(float2 x, int lane) {
 
 }  // namespace
 
-template <typename Raw, bool VEC>
+template <typename Raw, bool VEC, bool W>
 __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) {
-  using BL = Block<Raw, VEC>;
+  using BL = Block<Raw, VEC, W>;
   constexpr int EPV = BL::EPV;
   const int b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rank = static_cast<int>(cluster_ctarank());
@@ -399,6 +425,8 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   __shared__ StatRec rr[2 * kMaxK + 1];
   __shared__ float s_lp[kMaxK], s_lq[kMaxK], s_u[kMaxK];
   __shared__ int s_x[kMaxK];
+  __shared__ float s_vt[W ? 2 * kMaxK + 1 : 1];  // sampling settings: per-row kept thresholds
+  __shared__ int s_rf[W ? 2 * kMaxK + 1 : 1];
   __shared__ DecRec s_dec;
   __shared__ __align__(16) float2 s_units[kNU];  // first CTA: unit totals of the row
   __shared__ int s_first;
@@ -416,19 +444,34 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
     s_lq[k] = ok ? logit_at<Raw>(a.Lq, ik, a.V, xk) : 0.f;
   }
   griddep_wait();
-  // 1. fold: cluster warp gw folds rows gw, gw + kBW, ... and sends each
-  //    record to every CTA of the cluster
-  fold_stats_rows(a.part + static_cast<long long>(b) * RPG * a.P, a.P, gw, kBW, RPG, a.c_hi, a.c_lo, lane, rr);
-  __syncwarp();
-  cluster_wait();
-  if (lane < kCS && lane != rank)
-    for (int j = gw; j < RPG; j += kBW) st_cluster(cluster_addr(&rr[j], lane), rr[j]);
-  __syncwarp();
-  cluster_arrive();
-  cluster_wait();
+  if constexpr (W) {
+    // 1. the per-row records of the sampling settings' kept sets
+    for (int j = tid; j < RPG; j += kResThreads) {
+      const long long r = static_cast<long long>(b) * RPG + j;
+      rr[j] = a.rec[r];
+      s_vt[j] = a.vtau[r];
+      s_rf[j] = a.row_flag[r];
+    }
+    cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+    __syncthreads();
+  } else {
+    // 1. fold: cluster warp gw folds rows gw, gw + kBW, ... and sends each
+    //    record to every CTA of the cluster
+    fold_stats_rows(a.part + static_cast<long long>(b) * RPG * a.P, a.P, gw, kBW, RPG, a.c_hi, a.c_lo, lane, rr);
+    __syncwarp();
+    cluster_wait();
+    if (lane < kCS && lane != rank)
+      for (int j = gw; j < RPG; j += kBW) st_cluster(cluster_addr(&rr[j], lane), rr[j]);
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
+  }
   // 2. decision (the same in every CTA; the first CTA writes the outputs)
-  if (warp == 0) decide_chain(a, b, lane, rr, s_lp, s_lq, s_u, s_x, rank == 0, &s_dec);
-  if (warp == 1 && rank == 0 && (a.px || a.qx || a.lse_p || a.lse_q)) chain_outputs(a, b, lane, rr, s_lp, s_lq, s_x);
+  if (warp == 0) decide_chain<W>(a, b, lane, rr, s_lp, s_lq, s_u, s_x, s_vt, s_rf, rank == 0, &s_dec);
+  if (warp == 1 && rank == 0 && (a.px || a.qx || a.lse_p || a.lse_q))
+    chain_outputs<W>(a, b, lane, rr, s_lp, s_lq, s_x, s_vt, s_rf);
   __syncthreads();
   const DecRec d = s_dec;
   const long long V = a.V;
@@ -436,7 +479,7 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   const int mm = d.m < 0 ? 0 : d.m;  // flagged rows (m = -1) weigh nothing
   const Raw* P = static_cast<const Raw*>(a.Lp) + (static_cast<long long>(b) * (K + 1) + mm) * V;
   const Raw* Q = d.mode == 0 && mm < K ? static_cast<const Raw*>(a.Lq) + (static_cast<long long>(b) * K + mm) * V : P;
-  Consts k{d.Mp, d.dM, d.D_hi, d.D_lo, a.c_hi, a.c_lo, d.mode};
+  Consts k{d.Mp, d.dM, d.D_hi, d.D_lo, a.c_hi, a.c_lo, d.mode, d.vtp, d.vtq};
   // 3. weigh this warp's block of row m; unit totals go to the first CTA
   {
     float lu[kUW];
@@ -594,13 +637,18 @@ void tail_geometry(long long nv, int* NB, int* G, long long* nvw) {
   *nvw = static_cast<long long>(*NB) * kRB * 32;
 }
 
-cudaError_t launch_chain_tail(const TailArgs& a, int dtype, bool vec, cudaStream_t st) {
+template <bool W>
+cudaError_t launch_tail_w(const TailArgs& a, int dtype, bool vec, cudaStream_t st) {
   const dim3 grid(kCS, static_cast<unsigned>(a.B)), block(kResThreads);
   if (dtype == SPEC_BF16)
-    return vec ? launch_pdl(chain_tail_kernel<uint16_t, true>, grid, block, st, a, kCS)
-               : launch_pdl(chain_tail_kernel<uint16_t, false>, grid, block, st, a, kCS);
-  return vec ? launch_pdl(chain_tail_kernel<float, true>, grid, block, st, a, kCS)
-             : launch_pdl(chain_tail_kernel<float, false>, grid, block, st, a, kCS);
+    return vec ? launch_pdl(chain_tail_kernel<uint16_t, true, W>, grid, block, st, a, kCS)
+               : launch_pdl(chain_tail_kernel<uint16_t, false, W>, grid, block, st, a, kCS);
+  return vec ? launch_pdl(chain_tail_kernel<float, true, W>, grid, block, st, a, kCS)
+             : launch_pdl(chain_tail_kernel<float, false, W>, grid, block, st, a, kCS);
+}
+
+cudaError_t launch_chain_tail(const TailArgs& a, int dtype, bool vec, cudaStream_t st) {
+  return a.rec ? launch_tail_w<true>(a, dtype, vec, st) : launch_tail_w<false>(a, dtype, vec, st);
 }
 
 }  // namespace specv

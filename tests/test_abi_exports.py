@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     names = declared()
     for n in ("spec_verify_chain", "spec_verify_chain_greedy", "spec_verify_tree_greedy", "spec_tree_confidence",
               "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample", "spec_kv_compact",
-              "spec_tree_entropy", "spec_merge_trees"):
+              "spec_tree_entropy", "spec_merge_trees", "spec_verify_chain_warped"):
         assert n in names
 
 
@@ -80,6 +80,10 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.spec_verify_tree_greedy(fake, 1, fake, fake, n, 1, 5000, 2, 3, 16, 5, fake, fake, fake, fake, fake,
                                        fake, fake, 1 << 30, n) == SPEC_ERR_UNSUPPORTED
     assert lib.spec_tree_confidence(fake, 1, 5, 9, fake, fake, n) == SPEC_ERR_ARG
+    # sampling settings: top_p out of (0, 1], negative top_k, T = 0
+    for tk, tp, T in ((0, 0.0, 1.0), (0, 1.5, 1.0), (-1, 0.9, 1.0), (5, 0.9, 0.0)):
+        assert lib.spec_verify_chain_warped(fake, fake, 1, fake, fake, fake, T, tk, tp, 1, 1, 16, fake, fake, n, n,
+                                            fake, fake, 1 << 20, n) == SPEC_ERR_ARG
     # tree merge: no rows at all, a NULL output, N beyond the limit
     mt = lambda *a: lib.spec_merge_trees(*a)
     assert mt(fake, fake, fake, fake, fake, fake, fake, fake, 1, 3, 3, 0, 4, 0, 4, fake, fake, fake, fake, n) == \

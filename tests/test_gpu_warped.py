@@ -1,0 +1,116 @@
+"""GPU chain verification with top-k / top-p applied to p and q, against the
+oracle, through the C ABI. Integer outputs exact outside rows the oracle
+flags (a uniform within 1e-6 of a decision boundary, or a top-p decision
+within 1e-5 of its boundary); p'(x), q'(x) within 1e-5."""
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from gpu_helpers import need_gpu, np_
+
+pytestmark = pytest.mark.gpu
+
+SPEC_ROW_WARP = 32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def run(c, top_k, top_p, threads=8):
+    import speculative_decoding_verification_29_gb300 as sv
+
+    dev = torch.device("cuda")
+    g = sv.spec_verify_chain_warped(c.Lp.to(dev), c.Lq.to(dev), c.x.to(dev), c.ua.to(dev), c.ur.to(dev), c.T,
+                                    top_k=top_k, top_p=top_p)
+    torch.cuda.synchronize()
+    o = oracle.verify_chain_warped(c.Lp, c.Lq, c.x, c.ua, c.ur, c.T, top_k, top_p, threads=threads)
+    return {k: np_(v) for k, v in g.items()}, o
+
+
+def compare(g, o, allow_warp=False):
+    gs = g["row_status"]
+    if allow_warp:
+        warp = (gs & SPEC_ROW_WARP) != 0
+        gs = np.where(warp, o["status"], gs)
+    else:
+        warp = np.zeros_like(gs, bool)
+        assert not np.any(g["row_status"] & SPEC_ROW_WARP), g["row_status"]
+    assert np.array_equal(gs, o["status"]), (g["row_status"], o["status"])
+    ok = (o["status"] == 0) & ~warp
+    clean = ok & (o["flags"] == 0)
+    diff = (g["accept_len"] != o["accept_len"]) | np.any(g["out_tokens"] != o["out_tokens"], axis=1)
+    bad = np.nonzero(clean & diff)[0]
+    assert bad.size == 0, (bad[:5], g["accept_len"][bad[:5]], o["accept_len"][bad[:5]], g["out_tokens"][bad[:3]],
+                           o["out_tokens"][bad[:3]])
+    for gk, okk in (("p_at_x", "px"), ("q_at_x", "qx")):
+        a, b = g[gk][ok].astype(np.float64), o[okk][ok]
+        np.testing.assert_allclose(a, b, rtol=1e-5, atol=1e-30)
+    assert np.all(g["accept_len"][~ok & (o["status"] != 0)] == -1)
+    return int(warp.sum()), int((ok & (o["flags"] != 0)).sum())
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("top_k,top_p", [(20, 1.0), (0, 0.9), (50, 0.8), (1, 1.0), (3, 0.5), (4096, 0.95)])
+def test_warped_small(dtype, top_k, top_p):
+    c = gen.chain_zipf(16, 4, 5000, dtype, 0.8, 0.5, seed=top_k + int(100 * top_p),
+                       draft_top_k=top_k if top_k else 0)
+    compare(*run(c, top_k, top_p))
+
+
+def test_warped_topk1_equals_greedy_choices():
+    """top-k 1: with the drafter's top tokens the result is the target's
+    greedy chain (draft and target tops agree on about half the rows)."""
+    c = gen.chain_zipf(12, 4, 3000, torch.float32, 1.0, 0.4, seed=3, draft_top_k=1)
+    g, o = run(c, 1, 1.0)
+    compare(g, o)
+    gr = oracle.verify_chain_greedy(c.Lp, c.x)
+    assert np.array_equal(g["accept_len"], gr["accept_len"]) and np.array_equal(g["out_tokens"], gr["out_tokens"])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V", [2, 7, 1001, 4097, 8193])
+def test_warped_ragged_vocab(V, dtype):
+    c = gen.chain_zipf(6, 3, V, dtype, 0.9, 0.6, seed=V, draft_top_k=min(10, V - 1), n_likely=min(20, V))
+    compare(*run(c, min(10, V - 1), 0.85))
+
+
+def test_warped_flat_rows_beyond_candidates_are_flagged():
+    """Top-p alone on nearly flat rows (V = 20000): the nucleus holds far more
+    than 4096 tokens, which the GPU path reports instead of approximating."""
+    g0 = torch.Generator().manual_seed(4)
+    B, K, V = 3, 2, 20000
+    Lp = (0.01 * torch.randn(B, K + 1, V, generator=g0)).to(torch.float32)
+    Lq = (0.01 * torch.randn(B, K, V, generator=g0)).to(torch.float32)
+    c = gen.ChainBatch("flat", Lp, Lq, torch.randint(0, V, (B, K), generator=g0, dtype=torch.int32),
+                       torch.rand(B, K, generator=g0), torch.rand(B, generator=g0), 1.0)
+    g, o = run(c, 0, 0.9)
+    assert np.all(g["row_status"] == SPEC_ROW_WARP) and np.all(g["accept_len"] == -1)
+    # with top-k 4096 first, the same rows resolve and agree with the oracle
+    compare(*run(c, 4096, 0.9))
+
+
+def test_warped_ties_at_the_boundary():
+    """Many equal logits at the top-k / top-p boundary: the whole tied group
+    is kept (V = 3000, integer-valued logits)."""
+    g0 = torch.Generator().manual_seed(7)
+    B, K, V = 8, 3, 3000
+    Lp = torch.randint(-3, 4, (B, K + 1, V), generator=g0).float()
+    Lq = torch.randint(-3, 4, (B, K, V), generator=g0).float()
+    x = gen.workloads._gumbel_draw(Lq, 1.0, g0, 5)
+    c = gen.ChainBatch("ties", Lp, Lq, x, torch.rand(B, K, generator=g0), torch.rand(B, generator=g0), 1.0)
+    for k, p in ((5, 1.0), (0, 0.3), (100, 0.6)):
+        compare(*run(c, k, p), allow_warp=True)
+
+
+def test_warped_serving_batch():
+    """B=64, K=8, V=128256 bf16, T=0.7 (the batched serving workload) with
+    top-k 50 and top-p 0.9 on both models."""
+    c = gen.chain_zipf(64, 8, 128256, torch.bfloat16, 0.7, gen.workloads._sigma_spread, 0, name="chain_batched",
+                       draft_top_k=50)
+    nwarp, nflag = compare(*run(c, 50, 0.9, threads=16))
+    assert nflag <= 3

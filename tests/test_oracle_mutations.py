@@ -66,8 +66,8 @@ MUTATIONS = {
     "warped_topp_on_full_mass": ("if (!(cum < top_p * Zk)) break;", "if (!(cum < top_p * Z)) break;"),
     "warped_not_renormalised": ("? out[v] / Zw : 0.0;", "? out[v] / Z : 0.0;"),
     "warped_residual_unwarped_draft": (
-        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp);",
-        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, 0, 1.0, wq, tmp);"),
+        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp, &near);",
+        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, 0, 1.0, wq, tmp, &near);"),
     "kv_in_place_from_last_row": (
         "      for (int t = 0; t <= L; ++t) {\n        int src = pr ? pr[t] : t;\n        memcpy(tmp + (size_t)t * rowb,",
         "      for (int t = L; t >= 0; --t) {\n        int src = pr ? pr[t] : t;\n"
