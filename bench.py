@@ -100,6 +100,13 @@ def make_workload(name: str, seed: int):
         t = gen.config_tree(seed)
         return t, dict(workload="merged-tree greedy verify + confidence routing: B=16 N=61 V=128256 bf16", B=16,
                        N=61, V=128256, logits="bf16")
+    if name == "warped":
+        c = gen.chain_zipf(64, 8, 128256, __import__("torch").bfloat16, 0.7, gen.workloads._sigma_spread, seed,
+                           name="chain_batched", draft_top_k=50)
+        c.top_k, c.top_p = 50, 0.9
+        return c, dict(workload="chain verify with top-k 50 and top-p 0.9 on both models: B=64 K=8 V=128256 bf16 "
+                                "T=0.7, draft noise sigma_b~U(0.2,2)", B=64, K=8, V=128256, logits="bf16",
+                       temperature=0.7, top_k=50, top_p=0.9)
     if name == "entropy":
         t = gen.config_tree(seed)
         t.Ld = gen.tree_draft_logits(t, seed)
@@ -272,6 +279,18 @@ def run_ours(args):
                 ev[1].record(stream)
 
             timed_kernel = "rowscan_kernel + greedy_decide_kernel (one call)"
+        elif name == "warped":
+            out = sv.spec_verify_chain_warped(*sets[0], T, w.top_k, w.top_p, workspace=ws_t)
+
+            def step_dev(i):
+                sv.spec_verify_chain_warped(*sets[i % n_sets], T, w.top_k, w.top_p, out=out, workspace=ws_t)
+
+            def step_split(i, ev):
+                ev[0].record(stream)
+                sv.spec_verify_chain_warped(*sets[i % n_sets], T, w.top_k, w.top_p, out=out, workspace=ws_t)
+                ev[1].record(stream)
+
+            timed_kernel = "rowscan_kernel + warp_select_kernel + chain_tail_kernel (one call)"
         else:
             out = sv.spec_verify_chain(*sets[0], T, workspace=ws_t)
 
@@ -286,7 +305,7 @@ def run_ours(args):
                 sv.spec_chain_sample(*args_, T, out, ws_t)
 
             timed_kernel = "rowscan_kernel"
-        launches_per_step = 2
+        launches_per_step = 3 if name == "warped" else 2
         host = [w.Lp, w.Lq, w.x, w.ua, w.ur]
 
     # warm-up, then a short untimed soak so the clock sampler sees the load
@@ -371,6 +390,9 @@ def run_ours(args):
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu(), co["choice"].cpu()]
         elif w.T == 0.0:
             o = sv.spec_verify_chain_greedy(pinned[0], pinned[2], device=dev)
+            res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
+        elif name == "warped":
+            o = sv.spec_verify_chain_warped(*pinned, w.T, w.top_k, w.top_p, device=dev)
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
         else:
             o = sv.spec_verify_chain(pinned[0], pinned[1], pinned[2], pinned[3], pinned[4], w.T, device=dev,
@@ -593,6 +615,9 @@ def _oracle_step(name, w, rows, threads):
     elif name == "tree":
         oracle.verify_tree_greedy(w.Lt[idx], w.tok[idx], w.R[idx], w.n1, mask=w.mask[idx], threads=threads)
         oracle.tree_confidence(w.conf[idx], w.n1)
+    elif name == "warped":
+        oracle.verify_chain_warped(w.Lp[idx], w.Lq[idx], w.x[idx], w.ua[idx], w.ur[idx], w.T, w.top_k, w.top_p,
+                                   threads=threads)
     elif w.T == 0.0:
         oracle.verify_chain_greedy(w.Lp[idx], w.x[idx], threads=threads)
     else:
@@ -806,7 +831,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="chain_batched",
-                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact", "merge"])
+                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact", "merge", "warped"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")
     ap.add_argument("--e2e-steps", type=int, default=20)

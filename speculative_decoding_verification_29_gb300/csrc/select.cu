@@ -98,13 +98,15 @@ __device__ __forceinline__ void for_row(const Raw* row, int V, F f) {
 }
 
 // Largest key K with #{keys >= K} >= k (the k-th largest key), over the
-// row, by 8-bit digits from the top. hist: kSelWarps x 256 counters.
+// row, by 8-bit digits from the top; *count_ge receives #{keys >= K}.
+// hist: kSelWarps x 256 counters.
 template <typename Raw, bool VEC>
-__device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, unsigned* s_tot, uint32_t* s_sel) {
+__device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, unsigned* s_tot, uint32_t* s_sel,
+                                unsigned* count_ge) {
   using KY = Key<Raw>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint32_t prefix = 0;
-  unsigned kk = static_cast<unsigned>(k);
+  unsigned kk = static_cast<unsigned>(k), greater = 0, last_bin = 0;
   for (int shift = KY::kBits - 8; shift >= 0; shift -= 8) {
     for (int i = tid; i < kSelWarps * 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
@@ -142,17 +144,24 @@ __device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, un
         while (above + c[i] < kk) above += c[i++];
         s_sel[0] = static_cast<uint32_t>(255 - 8 * lane - i);
         s_sel[1] = kk - above;
+        s_sel[2] = above;  // keys in higher bins
+        s_sel[3] = c[i];   // keys in this bin
       }
       if (!hit && lane == 0) {  // fewer than kk keys match: keep them all (cannot happen for k <= V)
         s_sel[0] = 0;
         s_sel[1] = 1;
+        s_sel[2] = 0;
+        s_sel[3] = 0;
       }
     }
     __syncthreads();
     prefix |= s_sel[0] << shift;
     kk = s_sel[1];
+    greater += s_sel[2];
+    last_bin = s_sel[3];
     __syncthreads();
   }
+  *count_ge = greater + last_bin;  // the last digit's bin holds exactly the keys equal to K
   return prefix;
 }
 
@@ -205,7 +214,7 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
   float* s_w = reinterpret_cast<float*>(s_buf + kCand);      // kCand weights
   static_assert(kSelWarps * 256 <= 2 * kCand, "histograms fit the candidate buffer");
   __shared__ unsigned s_tot[256];
-  __shared__ uint32_t s_sel[2];
+  __shared__ uint32_t s_sel[4];
   __shared__ float2 s_ds[kSelWarps];
   __shared__ int s_n, s_last;
   __shared__ float s_M;
@@ -236,23 +245,22 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
   int st = 0;
   if (ok) {
     const bool use_k = a.top_k > 0 && a.top_k < a.V;
-    if (use_k) tau = kth_largest<Raw, VEC>(row, a.V, a.top_k, hist, s_tot, s_sel);
-    if (a.top_p < 1.f) {
-      // candidates: the keys >= tc, whole groups of equal keys and at most
-      // kCand of them: tc is one above the (kCand + 1)-th largest key, or the
-      // top-k threshold when that is higher ("own": the candidates are then
-      // every token top-k keeps, and the whole row when top-k is off)
-      uint32_t tc = tau;
-      bool own = true;
-      if (a.V > kCand) {
-        const uint32_t kc = kth_largest<Raw, VEC>(row, a.V, kCand + 1, hist, s_tot, s_sel) + 1u;
-        if (kc > tc) {
-          tc = kc;
-          own = false;
-        }
-      }
-      float2 Zk = Zfull;
-      if (use_k && !own) Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);
+    unsigned count_ge = static_cast<unsigned>(a.V);  // tokens top-k keeps
+    if (use_k) tau = kth_largest<Raw, VEC>(row, a.V, a.top_k, hist, s_tot, s_sel, &count_ge);
+    // candidates: the keys >= tc, whole groups of equal keys and at most kCand
+    // of them: every token top-k keeps when they fit ("own"), else the groups
+    // above the (kCand + 1)-th largest key
+    const bool own = count_ge <= static_cast<unsigned>(kCand);
+    uint32_t tc = tau;
+    if (a.top_p < 1.f && !own) {
+      unsigned cnt;
+      tc = kth_largest<Raw, VEC>(row, a.V, kCand + 1, hist, s_tot, s_sel, &cnt) + 1u;
+    }
+    float2 Zk = Zfull;  // mass of the tokens top-k keeps
+    if (a.top_p < 1.f && use_k && !own) Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);
+    if (a.top_p >= 1.f && !own) {
+      Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);  // top-k alone, more tokens than the buffer
+    } else {
       if (tid == 0) s_n = 0;
       __syncthreads();
       for_row<Raw, VEC>(row, a.V, [&](uint32_t bits) {
@@ -267,8 +275,13 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
       });
       __syncthreads();
       const int n = s_n;  // <= kCand by the choice of tc (checked all the same)
+      constexpr int kPer = kCand / kSelThreads;
       if (n > kCand) {
         st = SPEC_ROW_WARP;
+      } else if (a.top_p >= 1.f) {  // top-k alone: the candidates are the kept set
+        float2 mine = make_float2(0.f, 0.f);
+        for (int e = tid; e < n; e += kSelThreads) mine = ds_add(mine, make_float2(s_w[e], 0.f));
+        Zk = block_sum_ds(mine, s_ds);
       } else {
         // bitonic sort, keys descending, padded to a power of two with key 0 (weight 0)
         int n2 = 1;
@@ -297,7 +310,6 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
             __syncthreads();
           }
         // masses in key order: thread t owns entries kPer t .. kPer t + kPer - 1
-        constexpr int kPer = kCand / kSelThreads;
         float2 mine = make_float2(0.f, 0.f);
         for (int i = 0; i < kPer; ++i) {
           const int e = tid * kPer + i;
@@ -319,6 +331,7 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
           if (w < warp) before = ds_add(before, s_ds[w]);
           total = ds_add(total, s_ds[w]);
         }
+        __syncthreads();  // s_ds is reused below
         before = ds_add(before, wex);  // mass of the entries before this thread's first
         if (own) Zk = total;           // the candidates are exactly the kept-by-top-k set
         const float2 target = ds_mul_f(Zk, a.top_p);
@@ -335,16 +348,22 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
         const bool beyond = !own && L == n - 1 && ds_gt(target, total);
         if (L < 0 || beyond) {
           st = SPEC_ROW_WARP;
-        } else if (s_key[L] > tau) {
-          tau = s_key[L];
+        } else {
+          if (s_key[L] > tau) tau = s_key[L];
+          // kept mass: the candidates with key >= tau (whole groups)
+          float2 kept = make_float2(0.f, 0.f);
+          for (int i = 0; i < kPer; ++i) {
+            const int e = tid * kPer + i;
+            if (e < n && s_key[e] >= tau) kept = ds_add(kept, make_float2(s_w[e], 0.f));
+          }
+          Zk = block_sum_ds(kept, s_ds);
         }
-        __syncthreads();  // s_key and s_w are free again
       }
+      __syncthreads();  // s_key and s_w are free again
     }
     if (st == 0) {
-      const float2 Zw = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);
-      const float2 L2 = ds_log2(Zw);
-      out.Z = Zw.x;
+      const float2 L2 = ds_log2(Zk);
+      out.Z = Zk.x;
       out.Lhi = L2.x;
       out.Llo = L2.y;
     }
