@@ -88,6 +88,8 @@ def _declare(lib):
     lib.orc_tree_entropy.restype = None
     lib.orc_verify_chain_warped.argtypes = [P, P, i, P, P, P, d, i, d, i, i, i, i, i, P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_chain_warped.restype = None
+    lib.orc_tree_expand.argtypes = [P, i, d, P, i, i, i, i, P, P, P, P, P, P]
+    lib.orc_tree_expand.restype = None
     return lib
 
 
@@ -339,4 +341,22 @@ def tree_entropy(Ld, n1: int, T: float = 1.0, lib=None) -> Dict[str, np.ndarray]
                choice=np.empty(B, np.int32), status=np.empty(B, np.int32), flags=np.empty(B, np.int32))
     lib.orc_tree_entropy(_ptr(L), dt, B, N, V, float(T), int(n1), _ptr(out["entropy"]), _ptr(out["scores"]),
                          _ptr(out["choice"]), _ptr(out["status"]), _ptr(out["flags"]))
+    return out
+
+
+def tree_expand(Ld, logc, M: int, T: float = 1.0, lib=None) -> Dict[str, np.ndarray]:
+    """One expansion step of drafter trees by cumulative probability:
+    frontier drafter logits [B, F, V] and cumulative log-probabilities
+    logc [B, F]; the M best children (f, v) by logc[f] + log q_f(v), ties to
+    the lower f then v. Returns parent, token [B, M] int32, score [B, M]
+    fp64, status [B], flags [B] (near tie at the M-th place)."""
+    lib = lib or load()
+    L, dt = _logits(Ld)
+    B, F, V = L.shape
+    lc = _np(logc, np.float64).reshape(B, F)
+    out = dict(parent=np.empty((B, M), np.int32), token=np.empty((B, M), np.int32),
+               score=np.empty((B, M), np.float64), status=np.empty(B, np.int32), flags=np.empty(B, np.int32))
+    cand = np.empty(F * V * 16, np.uint8)  # {double, int, int} entries
+    lib.orc_tree_expand(_ptr(L), dt, float(T), _ptr(lc), B, F, V, int(M), _ptr(out["parent"]), _ptr(out["token"]),
+                        _ptr(out["score"]), _ptr(out["status"]), _ptr(out["flags"]), _ptr(cand))
     return out

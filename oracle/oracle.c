@@ -23,6 +23,8 @@
  *   - the sampling settings (top-k, top-p) applied to p and q before the
  *     same steps (ariser.io page: p and q must be the distributions the
  *     settings produce);
+ *   - tree expansion by cumulative probability (SubSpec review, Method 2):
+ *     the M children of highest cumulative probability over the frontier;
  *   - entropy routing, the signal the TAPS page compares confidence routing
  *     with: mean drafter entropy per tree, lower wins;
  *   - KV-cache compaction after verification (lotook.com, KV-cache section:
@@ -672,5 +674,68 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
     out[m] = tok;
     flags[b] = fl | (near ? FL_WARP : 0);
     margin[b] = mg;
+  }
+}
+
+/* One expansion step of a drafter token tree by cumulative probability
+ * (SubSpec review, Method 2: candidate paths branch, and at each step the
+ * cumulative probability of every candidate path is computed and the
+ * highest-scoring candidates are kept while the tree deepens). Reading: the
+ * frontier holds F nodes of each batch row with cumulative log-probabilities
+ * logc[f]; the drafter's next-token distribution at node f is softmax(l / T);
+ * every child (f, v) scores logc[f] + log q_f(v); the M best children are
+ * kept, ordered by score descending, ties to the lower frontier index, then
+ * the lower token id.
+ * Ld: [B][F][V]; logc: [B][F]; out: parent, token [B][M], score [B][M];
+ * status: ST_DRAFT for a frontier row with a NaN or no finite maximum;
+ * flags: FL_ROUTE when the M-th and (M+1)-th scores lie within NEAR. */
+typedef struct {
+  double s;
+  int f, v;
+} orc_cand;
+
+static int orc_cand_order(const void* a, const void* b) {
+  const orc_cand* x = (const orc_cand*)a;
+  const orc_cand* y = (const orc_cand*)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  if (x->f != y->f) return x->f < y->f ? -1 : 1;
+  return x->v < y->v ? -1 : (x->v > y->v);
+}
+
+void orc_tree_expand(const void* Ld, int dt, double T, const double* logc, int B, int F, int V, int M,
+                     int32_t* parent, int32_t* token, double* score, int32_t* status, int32_t* flags, orc_cand* cand) {
+  for (int b = 0; b < B; ++b) {
+    int st = 0;
+    size_t n = 0;
+    for (int f = 0; f < F; ++f) {
+      size_t off = ((size_t)b * F + f) * (size_t)V;
+      double Mx, Z;
+      if (softmax_stats(Ld, dt, off, V, T, &Mx, &Z)) {
+        st |= ST_DRAFT;
+        continue;
+      }
+      double lz = log(Z);
+      for (int v = 0; v < V; ++v) {
+        cand[n].s = logc[(size_t)b * F + f] + (elem(Ld, dt, off + (size_t)v) / T - Mx - lz);
+        cand[n].f = f;
+        cand[n].v = v;
+        ++n;
+      }
+    }
+    status[b] = st;
+    flags[b] = 0;
+    for (int i = 0; i < M; ++i) {
+      parent[(size_t)b * M + i] = token[(size_t)b * M + i] = -1;
+      score[(size_t)b * M + i] = NAN;
+    }
+    if (st) continue;
+    qsort(cand, n, sizeof(orc_cand), orc_cand_order);
+    for (int i = 0; i < M && (size_t)i < n; ++i) {
+      parent[(size_t)b * M + i] = cand[i].f;
+      token[(size_t)b * M + i] = cand[i].v;
+      score[(size_t)b * M + i] = cand[i].s;
+    }
+    if ((size_t)M < n && isfinite(cand[M].s) && fabs(cand[M - 1].s - cand[M].s) < NEAR) flags[b] = FL_ROUTE;
   }
 }

@@ -706,6 +706,38 @@ def pin_lossless_warped(lib, V, K, T, top_k, top_p, seed):
     assert abs(sum(got.values()) - 1.0) < 1e-12 and err < 1e-12, err
 
 
+def pin_tree_expand(lib, seed=11):
+    """One cumulative-probability expansion step (SubSpec review: keep the
+    candidate paths of highest cumulative probability): equals a brute-force
+    ranking of every child by log c_f + scipy's log-softmax, ties to the lower
+    frontier node then token; a single frontier node with c = 1 keeps its M
+    most probable tokens; kept sets are closed upward within a node."""
+    from scipy.special import log_softmax
+
+    rng = np.random.default_rng(seed)
+    for T in (1.0, 0.6):
+        B, F, V, M = 3, 4, 9, 7
+        Ld = rng.integers(-3, 4, (B, F, V)).astype(np.float64)  # small integers: ties in plenty
+        logc = np.log(rng.random((B, F)))
+        logc[0, 1] = logc[0, 2]  # two identical frontier nodes: every child ties across them
+        Ld[0, 2] = Ld[0, 1]
+        logc[0, 1] = logc[0, 2] = max(logc[0].max(), logc[0, 1])
+        r = oracle.tree_expand(Ld, logc, M, T=T, lib=lib)
+        for b in range(B):
+            cand = [(logc[b, f] + log_softmax(Ld[b, f] / T)[v], f, v) for f in range(F) for v in range(V)]
+            cand.sort(key=lambda c: (-c[0], c[1], c[2]))
+            assert [(c[1], c[2]) for c in cand[:M]] == list(zip(r["parent"][b], r["token"][b]))
+            assert np.allclose([c[0] for c in cand[:M]], r["score"][b], rtol=0, atol=1e-12)
+            for f in range(F):  # upward closed: every token of node f above a kept one is kept
+                kept = {v for pf, v in zip(r["parent"][b], r["token"][b]) if pf == f}
+                for v in kept:
+                    assert all(u in kept for u in range(V) if Ld[b, f, u] > Ld[b, f, v])
+    l = rng.normal(0, 2, 50)
+    r = oracle.tree_expand(l[None, None], np.zeros((1, 1)), 6, lib=lib)
+    assert list(r["token"][0]) == list(np.argsort(-l, kind="stable")[:6])
+    assert np.allclose(np.exp(r["score"][0]), np.exp(log_softmax(l))[r["token"][0]], rtol=1e-12)
+
+
 ALL_PINS = [
     ("ab_example", pin_ab_example),
     ("lossless_V3K2", lambda lib: pin_lossless(lib, 3, 2, 1.0, 1)),
@@ -724,6 +756,7 @@ ALL_PINS = [
     ("kv_strided", pin_kv_strided),
     ("entropy", pin_entropy),
     ("entropy_routing", pin_entropy_routing),
+    ("tree_expand", pin_tree_expand),
     ("warped_noop", pin_warped_noop),
     ("warped_topk1_greedy", pin_warped_topk1_is_greedy),
     ("warped_examples", pin_warped_examples),

@@ -68,6 +68,13 @@ MUTATIONS = {
     "warped_residual_unwarped_draft": (
         "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp, &near);",
         "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, 0, 1.0, wq, tmp, &near);"),
+    "expand_ties_to_higher_node": ("if (x->f != y->f) return x->f < y->f ? -1 : 1;",
+                                   "if (x->f != y->f) return x->f > y->f ? -1 : 1;"),
+    "expand_cumulative_dropped": ("cand[n].s = logc[(size_t)b * F + f] + (", "cand[n].s = 0.0 + ("),
+    "expand_temperature_dropped": ("+ (elem(Ld, dt, off + (size_t)v) / T - Mx - lz);",
+                                   "+ (elem(Ld, dt, off + (size_t)v) - Mx - lz);"),
+    "expand_unnormalised": ("+ (elem(Ld, dt, off + (size_t)v) / T - Mx - lz);",
+                            "+ (elem(Ld, dt, off + (size_t)v) / T - Mx);"),
     "kv_in_place_from_last_row": (
         "      for (int t = 0; t <= L; ++t) {\n        int src = pr ? pr[t] : t;\n        memcpy(tmp + (size_t)t * rowb,",
         "      for (int t = L; t >= 0; --t) {\n        int src = pr ? pr[t] : t;\n"
