@@ -711,7 +711,10 @@ void orc_tree_expand(const void* Ld, int dt, double T, const double* logc, int B
     for (int f = 0; f < F; ++f) {
       size_t off = ((size_t)b * F + f) * (size_t)V;
       double Mx, Z;
-      if (softmax_stats(Ld, dt, off, V, T, &Mx, &Z)) {
+      double lc = logc[(size_t)b * F + f];
+      /* a node without a usable distribution, or whose own path score is NaN
+       * or +inf, leaves the row unranked */
+      if (softmax_stats(Ld, dt, off, V, T, &Mx, &Z) || isnan(lc) || lc == INFINITY) {
         st |= ST_DRAFT;
         continue;
       }

@@ -736,6 +736,20 @@ def pin_tree_expand(lib, seed=11):
     r = oracle.tree_expand(l[None, None], np.zeros((1, 1)), 6, lib=lib)
     assert list(r["token"][0]) == list(np.argsort(-l, kind="stable")[:6])
     assert np.allclose(np.exp(r["score"][0]), np.exp(log_softmax(l))[r["token"][0]], rtol=1e-12)
+    # degenerate rows: a node with no distribution or a NaN / +inf path score
+    # leaves its row unranked; a node of probability 0 (log c = -inf) only
+    # contributes -inf children, ranked last
+    Ld = rng.normal(0, 1, (4, 2, 5))
+    logc = np.zeros((4, 2))
+    Ld[0, 1, 3] = np.nan
+    logc[1, 0] = np.nan
+    logc[2, 1] = np.inf
+    logc[3, 1] = -np.inf
+    r = oracle.tree_expand(Ld, logc, 7, lib=lib)
+    assert list(r["status"]) == [4, 4, 4, 0]
+    assert (r["parent"][:3] == -1).all() and np.isnan(r["score"][:3]).all()
+    assert list(r["parent"][3]) == [0] * 5 + [1, 1] and list(r["token"][3][5:]) == [0, 1]
+    assert np.isneginf(r["score"][3][5:]).all()
 
 
 ALL_PINS = [
