@@ -807,6 +807,141 @@ def run_merge_reference(args):
                               "d2h_bytes_per_step": 0}}), flush=True)
 
 
+EXP_B, EXP_F, EXP_M, EXP_V = 64, 10, 10, 128256
+EXP_METRIC = "expanded frontier nodes/sec (drafter-tree expansion by cumulative probability)"
+
+
+def expand_setup(seed: int):
+    """One expansion step of 64 drafter trees: 10 frontier nodes per tree,
+    the 10 best children kept, Llama-3 vocabulary, bf16 drafter logits."""
+    import gen
+
+    Ld, logc = gen.expand_frontier(EXP_B, EXP_F, EXP_V, seed=seed)
+    cfg = dict(workload=f"drafter-tree expansion by cumulative probability: B={EXP_B} trees, F={EXP_F} frontier "
+                        f"nodes, M={EXP_M} children kept, V={EXP_V} bf16 drafter logits, T=1",
+               B=EXP_B, F=EXP_F, M=EXP_M, V=EXP_V)
+    return Ld, logc, cfg
+
+
+def run_expand(args):
+    import torch
+
+    import speculative_decoding_verification_29_gb300 as sv
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    Ld, logc, cfg = expand_setup(rank_seed(args.seed, rank))
+    alg = Ld.numel() * Ld.element_size() + logc.numel() * 4 + EXP_B * EXP_M * 12
+    n_sets = max(1, -(-2 * L2_BYTES // alg))  # consecutive steps never find their logits in L2
+    sets = [(Ld.to(dev), logc.to(dev)) for _ in range(n_sets)]
+    from speculative_decoding_verification_29_gb300 import _lib
+
+    need = _lib.load().spec_expand_workspace_bytes(EXP_B, EXP_F, EXP_V, EXP_M, _lib.SPEC_BF16)
+    ws_t = sv.alloc_workspace(need, dev)
+    out = sv.spec_tree_expand(*sets[0], EXP_M, 1.0, workspace=ws_t)
+    stream = torch.cuda.current_stream()
+
+    def step_dev(i):
+        sv.spec_tree_expand(*sets[i % n_sets], EXP_M, 1.0, out=out, workspace=ws_t)
+
+    for i in range(max(args.warmup, 3)):
+        step_dev(i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak:
+        for i in range(20):
+            step_dev(i)
+        torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        step_dev(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total_ms = max_over_ranks(start.elapsed_time(end), ws, dev)
+    # per-call durations on the launching stream, for the roofline
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        step_dev(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    k_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    host = [Ld.pin_memory(), logc.pin_memory()]
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        o = sv.spec_tree_expand(host[0], host[1], EXP_M, 1.0, workspace=ws_t, device=dev)
+        res = [o["parent"].cpu(), o["token"].cpu(), o["score"].cpu(), o["row_status"].cpu()]
+    e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)
+    clk = clocks.stop() if clocks else None
+    peak, peak_kind = _peaks()
+    units = EXP_B * EXP_F
+    line = {
+        "metric": EXP_METRIC, "value": throughput(units, args.steps, ws, total_ms), "unit": "nodes/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 logits, f32 arithmetic",
+        "data": "synthetic (peaked drafter logits, random path scores)",
+        "config": dict(cfg, parallelism=f"replicas x{ws}", launch="eager",
+                       l2=f"{n_sets} input copies in rotation ({alg / 1e6:.0f} MB each); no flush"),
+        "roofline": {"bound": "hbm", "kernel": "rowscan_kernel + expand_rows_kernel + expand_merge_kernel (one call)",
+                     "achieved": alg / (k_ms / 1e3) / 1e9, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": alg / (k_ms / 1e3) / 1e9 / peak, "traffic": None, "algorithmic_bytes": alg,
+                     "kernel_ms_mean": k_ms},
+        "e2e": {"value": throughput(units, e2e_steps, ws, e2e_s * 1e3), "unit": "nodes/s",
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+                "d2h_bytes_per_step": sum(r.numel() * r.element_size() for r in res), "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps, "clocks": clk,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = expand_cpu_baseline(Ld, logc, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def expand_cpu_baseline(Ld, logc, cpu_seconds, rows=None):
+    """The oracle's expansion of whole trees (batch rows), one at a time, until
+    the budget is spent (one thread)."""
+    import oracle
+
+    oracle.load()
+    reps, t_tot, b = 0, 0.0, 0
+    while (rows is None and t_tot < cpu_seconds) or (rows is not None and reps < rows):
+        t0 = time.perf_counter()
+        oracle.tree_expand(Ld[b:b + 1], logc[b:b + 1].double(), EXP_M)
+        t_tot += time.perf_counter() - t0
+        reps += 1
+        b = (b + 1) % Ld.shape[0]
+    return {"value": reps * EXP_F / t_tot, "unit": "nodes/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} trees of the batch expanded one at a time ({reps * EXP_F} frontier nodes, fp64 "
+                      f"log-softmax and a full sort of the F*V children: {t_tot:.1f} s)"}
+
+
+def run_expand_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    Ld, logc, cfg = expand_setup(args.seed)
+    b = expand_cpu_baseline(Ld, logc, 0.0, rows=max(1, min(args.steps, 16)))
+    print(json.dumps({"impl": "reference", "metric": EXP_METRIC, "value": b["value"], "unit": "nodes/s",
+                      "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+                      "cpu_baseline": b, "e2e": {"value": b["value"], "unit": "nodes/s", "h2d_bytes_per_step": 0,
+                                                 "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def run_kv_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -831,7 +966,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="chain_batched",
-                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact", "merge", "warped"])
+                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact", "merge", "warped",
+                             "expand"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -839,7 +975,12 @@ def main():
     ap.add_argument("--graph", action="store_true", help="replay each step as a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.workload == "merge":
+    if args.workload == "expand":
+        if args.impl == "reference":
+            run_expand_reference(args)
+        else:
+            run_expand(args)
+    elif args.workload == "merge":
         if args.impl == "reference":
             run_merge_reference(args)
         else:

@@ -25,4 +25,5 @@ from .workloads import (  # noqa: F401
     tree_batch,
     kv_cache,
     tree_draft_logits,
+    expand_frontier,
 )

@@ -369,6 +369,22 @@ def tree_draft_logits(tb: "TreeBatch", seed: int = 0, sigma: float = 1.0) -> tor
     return out
 
 
+def expand_frontier(B: int, F: int, V: int, dtype: torch.dtype = torch.bfloat16, seed: int = 0, depth: int = 3,
+                    boost: float = 8.0, n_likely: int = 20) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Frontier of B drafter trees for one expansion step: logits [B, F, V]
+    (peaked rows, as for the chain workloads) and path log-scores logc [B, F]
+    fp32, each the sum of ``depth`` values log(U), U ~ U(0.05, 1), sorted
+    descending per row as a previous step leaves them. Built one row at a
+    time to bound host memory."""
+    g = _gen(seed)
+    Ld = torch.empty(B, F, V, dtype=dtype)
+    for b in range(B):
+        Ld[b] = _peaked_rows(F, V, g, boost, n_likely).to(dtype)
+    u = 0.05 + 0.95 * torch.rand(B, F, depth, generator=g, dtype=torch.float64)
+    logc = torch.log(u).sum(-1).sort(dim=1, descending=True).values.to(torch.float32)
+    return Ld, logc
+
+
 def kv_cache(P: int, B: int, S: int, W: int, dtype: torch.dtype = torch.bfloat16, seed: int = 0,
              pad: int = 0) -> torch.Tensor:
     """Synthetic KV cache: [P, B, S, W + pad] of random bit patterns (P

@@ -29,6 +29,8 @@
  *     tree-merging code example).
  *   - spec_tree_entropy: entropy routing, the mean drafter entropy per tree,
  *     lower wins (the signal the TAPS page compares confidence routing with).
+ *   - spec_tree_expand: one drafter-tree expansion step, the M children of
+ *     highest cumulative probability (SubSpec review, Method 2).
  *   - spec_kv_compact: after verification, keep the accepted entries of the
  *     KV cache at consecutive positions and cut the length after them
  *     (lotook.com, KV-cache section; SubSpec review, step "Update KV").
@@ -269,6 +271,37 @@ int spec_merge_trees(const int32_t* tokens1, const uint8_t* mask1, const int32_t
 int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, int B, int N, int V, int n1,
                       float* node_entropy, float* scores, int32_t* choice, int32_t* row_status, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/* One expansion step of B drafter token trees by cumulative probability
+ * (SubSpec review, Method 2: candidate paths branch, each path's cumulative
+ * probability is computed at every step and the best ones are kept as the
+ * tree grows). Row b has F frontier nodes; node f carries its path's log
+ * cumulative probability logc[b][f] and the drafter's logits at it. A child
+ * (f, v) scores logc[b][f] + log softmax(l_f / T)[v]; the M best children
+ * are returned in rank order, higher score first, equal scores to the lower
+ * f, then the lower v.
+ *   draft_logits  device [B][F][V] (dtype)
+ *   temperature   > 0, finite
+ *   logc          device [B][F] fp32: finite, or -inf for a path of
+ *                 probability 0 (its children score -inf and rank last)
+ *   M             1 <= M, F * M <= 2048
+ *   workspace     spec_expand_workspace_bytes(B, F, V, M, dtype) bytes,
+ *                 256-byte aligned
+ * Outputs (device): parent [B][M] int32 (frontier index), token [B][M]
+ * int32, score [B][M] fp32 (the child's log cumulative probability, the
+ * next step's logc), row_status [B] int32. Slots past F * V children are
+ * -1 / NaN. A frontier row with NaN or +inf logits or only -inf logits, or a
+ * NaN or +inf logc, sets SPEC_ROW_DRAFT; SPEC_ROW_WARP when more than 4096
+ * tokens of one node tie at its M-th largest logit; such a row's outputs
+ * are all -1 / NaN. Scores are exact to about 1e-6 (the normaliser's fp32
+ * exponentials); candidates of one node rank exactly by logit. Passes over
+ * each frontier row: one for the softmax statistics, one per 8-bit radix
+ * digit of the M-th largest logit (2 for bf16, 4 for fp32; none when
+ * M >= V) and one to collect the top M. */
+size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype);
+int spec_tree_expand(const void* draft_logits, int dtype, float temperature, const float* logc, int B, int F, int V,
+                     int M, int32_t* parent, int32_t* token, float* score, int32_t* row_status, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /* KV-cache compaction after a verification step (lotook.com, section on the
  * KV cache: when the target rejects the drafts after position m, both

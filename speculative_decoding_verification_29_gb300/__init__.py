@@ -15,6 +15,7 @@ __all__ = [
     "spec_tree_confidence",
     "spec_merge_trees",
     "spec_tree_entropy",
+    "spec_tree_expand",
     "spec_kv_compact",
     "workspace_bytes",
     "alloc_workspace",

@@ -34,6 +34,8 @@ SIGNATURES = {
     "spec_tree_confidence": (I, [P, I, I, I, P, P, P]),
     "spec_merge_trees": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P]),
     "spec_tree_entropy": (I, [P, I, F, I, I, I, I, P, P, P, P, P, Z, P]),
+    "spec_expand_workspace_bytes": (Z, [I, I, I, I, I]),
+    "spec_tree_expand": (I, [P, I, F, P, I, I, I, I, P, P, P, P, P, Z, P]),
     "spec_kv_compact": (I, [P, I, I, I, I, I, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong, P, P, I, P, P, P,
                             P]),
     "spec_status_string": (ctypes.c_char_p, [I]),

@@ -249,6 +249,38 @@ def spec_tree_entropy(draft_logits, n1: int, temperature: float = 1.0, out: Opti
     return out
 
 
+def spec_tree_expand(draft_logits, logc, M: int, temperature: float = 1.0,
+                     out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                     device="cuda", stream=None) -> Dict[str, torch.Tensor]:
+    """One drafter-tree expansion step by cumulative probability:
+    draft_logits [B, F, V] (bf16 or fp32) at the F frontier nodes, logc [B, F]
+    their paths' log cumulative probabilities. Returns the M best children
+    as parent, token [B, M] int32, score [B, M] fp32 and row_status [B]."""
+    lib = _lib.load()
+    dev = draft_logits.device if draft_logits.device.type == "cuda" else torch.device(device)
+    Ld = _dev(draft_logits, dev)
+    B, F, V = Ld.shape
+    lc = _dev(logc, dev, torch.float32)
+    if tuple(lc.shape) != (B, F):
+        raise ValueError(f"logc must be [{B}, {F}], got {tuple(lc.shape)}")
+    code = _dtype_code(Ld)
+    if workspace is None:
+        need = lib.spec_expand_workspace_bytes(B, F, V, int(M), code)
+        if need == 0:
+            check("spec_expand_workspace_bytes", _lib.SPEC_ERR_UNSUPPORTED)
+        workspace = alloc_workspace(need, dev)
+    if out is None:
+        out = dict(parent=torch.empty(B, M, dtype=torch.int32, device=dev),
+                   token=torch.empty(B, M, dtype=torch.int32, device=dev),
+                   score=torch.empty(B, M, dtype=torch.float32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+    check("spec_tree_expand", lib.spec_tree_expand(Ld.data_ptr(), code, float(temperature), lc.data_ptr(), B, F, V,
+                                                   int(M), out["parent"].data_ptr(), out["token"].data_ptr(),
+                                                   out["score"].data_ptr(), out["row_status"].data_ptr(),
+                                                   workspace.data_ptr(), workspace.numel(), _stream(stream)))
+    return out
+
+
 def spec_merge_trees(tokens1, mask1, retrieve1, pos1, tokens2, mask2, retrieve2, pos2, device="cuda",
                      stream=None) -> Dict[str, torch.Tensor]:
     """Merge B pairs of drafter trees under one shared root on the device.

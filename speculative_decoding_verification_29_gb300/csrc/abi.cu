@@ -406,6 +406,68 @@ int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, in
   return cuda_status(launch_tree_entropy(en, st));
 }
 
+size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype) {
+  int max_m = 0, max_fm = 0;
+  expand_limits(&max_m, &max_fm);
+  if (!dtype_ok(dtype) || B < 1 || F < 1 || V < 2 || M < 1) return 0;
+  if (B > kMaxB || V > kMaxV || M > max_m || static_cast<long long>(F) * M > max_fm) return 0;
+  const long long rows = static_cast<long long>(B) * F;
+  const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
+  return up256(static_cast<size_t>(rows * P) * sizeof(float2)) + up256(static_cast<size_t>(rows * M) * 16) +
+         up256(static_cast<size_t>(rows) * sizeof(int32_t));
+}
+
+int spec_tree_expand(const void* draft_logits, int dtype, float temperature, const float* logc, int B, int F, int V,
+                     int M, int32_t* parent, int32_t* token, float* score, int32_t* row_status, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!draft_logits || !logc || !parent || !token || !score || !row_status) return SPEC_ERR_ARG;
+  if (!dtype_ok(dtype) || B < 1 || F < 1 || V < 2 || M < 1) return SPEC_ERR_ARG;
+  if (!(temperature > 0.f) || !isfinite(temperature)) return SPEC_ERR_ARG;
+  const size_t need = spec_expand_workspace_bytes(B, F, V, M, dtype);
+  if (need == 0) return SPEC_ERR_UNSUPPORTED;
+  int e = check_workspace(workspace, workspace_bytes, need);
+  if (e) return e;
+  const bool vec = use_vec(V, dtype, draft_logits, nullptr);
+  const long long rows = static_cast<long long>(B) * F;
+  if ((e = scan_grid_ok(rows, V, dtype, vec))) return e;
+  if (rows > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ScanArgs a{};
+  a.A = draft_logits;
+  a.B = B;
+  a.TR = F;
+  a.DR = 0;
+  a.V = V;
+  a.P = scan_chunks(V, vec, dtype);
+  split_c(temperature, &a.c_hi, &a.c_lo);
+  a.part = static_cast<float2*>(workspace);
+  if (launch_rowscan(a, dtype, vec, 0, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  const long long Pmax = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
+  size_t off = up256(static_cast<size_t>(rows * Pmax) * sizeof(float2));
+  ExpArgs x{};
+  x.L = draft_logits;
+  x.logc = logc;
+  x.B = B;
+  x.F = F;
+  x.V = V;
+  x.M = M;
+  x.P = a.P;
+  x.c_hi = a.c_hi;
+  x.c_lo = a.c_lo;
+  const double it = 1.0 / static_cast<double>(temperature);
+  x.it_hi = static_cast<float>(it);
+  x.it_lo = static_cast<float>(it - static_cast<double>(x.it_hi));
+  x.part = a.part;
+  x.cand = at(workspace, off);
+  off += up256(static_cast<size_t>(rows * M) * 16);
+  x.row_flag = reinterpret_cast<int32_t*>(at(workspace, off));
+  x.parent = parent;
+  x.token = token;
+  x.score = score;
+  x.row_status = row_status;
+  return cuda_status(launch_expand(x, dtype, vec, st));
+}
+
 int spec_kv_compact(void* kv, int elem_bytes, int n_planes, int B, int S, int W, long long stride_plane,
                     long long stride_batch, long long stride_pos, const int32_t* base_pos, const int32_t* path, int D,
                     const int32_t* accept_len, int32_t* new_len, int32_t* row_status, void* stream) {

@@ -1,0 +1,231 @@
+// expand.cu -- one expansion step of drafter token trees by cumulative
+// probability (SubSpec review, Method 2: candidate paths branch, and at each
+// step the cumulative probability of every candidate path is computed and
+// the highest-scoring candidates are kept while the tree deepens).
+//
+// Per batch row: F frontier nodes with cumulative log-probabilities logc[f]
+// and the drafter's logits at each; child (f, v) scores logc[f] +
+// log softmax(l_f / T)[v]; the M best children are kept, by score, ties to
+// the lower frontier node, then the lower token id. Only a node's own M most
+// probable tokens can be among them, so:
+//   rowscan (stats) over the F rows, then one CTA per frontier row selects
+//   its M largest logits (radix select on order-preserving keys, then the
+//   tokens at or above the M-th key sorted by key and id) and writes their
+//   log-probabilities as float pairs; one CTA per batch row sorts the F x M
+//   candidates by score (float pairs), node and token and keeps M.
+#include "select.cuh"
+
+namespace specv {
+
+namespace {
+
+using namespace sel;
+
+struct Cand {
+  float hi, lo;  // score as a float pair
+  int f, v;
+};
+
+// a before b: higher score, then lower node, then lower token
+__device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
+  if (a.hi != b.hi || a.lo != b.lo) return ds_gt(make_float2(a.hi, a.lo), make_float2(b.hi, b.lo));
+  if (a.f != b.f) return a.f < b.f;
+  return a.v < b.v;
+}
+
+template <typename Raw, bool VEC>
+__global__ void __launch_bounds__(kSelThreads) expand_rows_kernel(ExpArgs a) {
+  using KY = Key<Raw>;
+  const int row_id = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
+  __shared__ __align__(16) uint32_t s_buf[2 * kCand];
+  unsigned* hist = s_buf;
+  uint32_t* s_key = s_buf;
+  int* s_idx = reinterpret_cast<int*>(s_buf + kCand);
+  __shared__ unsigned s_tot[256];
+  __shared__ uint32_t s_sel[4];
+  __shared__ int s_n;
+  __shared__ float s_M;
+  __shared__ float2 s_lz;
+  griddep_launch_dependents();
+  griddep_wait();
+  if (warp == 0) {
+    float2 z;
+    const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+    if (lane == 0) {
+      s_M = M;
+      const float2 l2 = ds_log2(z);  // ln Z = log2 Z * ln 2, as a float pair
+      const float ln2_hi = 0.693147182464599609375f, ln2_lo = -1.904654323148236e-09f;
+      s_lz = ds_add(ds_mul_f(l2, ln2_hi), make_float2(l2.x * ln2_lo, 0.f));
+      if (!(M == M) || !isfinite(M) || !(z.x > 0.f)) s_M = NAN;
+    }
+  }
+  __syncthreads();
+  const float M = s_M;
+  const int Mk = a.M;
+  Cand* out = static_cast<Cand*>(a.cand) + static_cast<long long>(row_id) * Mk;
+  if (!(M == M)) {  // no distribution at this node
+    for (int i = tid; i < Mk; i += kSelThreads) out[i] = Cand{NAN, 0.f, -1, -1};
+    if (tid == 0) a.row_flag[row_id] = SPEC_ROW_DRAFT;
+    return;
+  }
+  const float2 lz = s_lz;
+  const int take = Mk < a.V ? Mk : a.V;
+  unsigned cnt = static_cast<unsigned>(a.V);
+  uint32_t tau = 0u;
+  if (take < a.V) tau = kth_largest<Raw, VEC>(row, a.V, take, hist, s_tot, s_sel, &cnt);
+  int st = 0;
+  if (cnt > static_cast<unsigned>(kCand)) {
+    st = SPEC_ROW_WARP;  // more tokens tie at the M-th value than the buffer holds
+  } else {
+    if (tid == 0) s_n = 0;
+    __syncthreads();
+    for_row_i<Raw, VEC>(row, a.V, [&](int v, uint32_t bits) {
+      const uint32_t key = KY::of(bits);
+      if (key >= tau) {
+        const int slot = atomicAdd(&s_n, 1);
+        if (slot < kCand) {
+          s_key[slot] = key;
+          s_idx[slot] = v;
+        }
+      }
+    });
+    __syncthreads();
+    const int n = s_n < kCand ? s_n : kCand;
+    int n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (int i = n + tid; i < n2; i += kSelThreads) {
+      s_key[i] = 0u;
+      s_idx[i] = 0x7fffffff;
+    }
+    __syncthreads();
+    // bitonic sort: key descending, then index ascending
+    for (int size = 2; size <= n2; size <<= 1)
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < n2; i += kSelThreads) {
+          const int pj = i ^ stride;
+          if (pj > i) {
+            const bool first = (i & size) == 0;
+            const uint32_t ki = s_key[i], kj = s_key[pj];
+            const int ii = s_idx[i], ij = s_idx[pj];
+            const bool i_before = ki > kj || (ki == kj && ii < ij);
+            if (first ? !i_before : i_before) {
+              s_key[i] = kj;
+              s_key[pj] = ki;
+              s_idx[i] = ij;
+              s_idx[pj] = ii;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    // log-probabilities of the first `take` tokens: (l - M) / T - ln Z, float pairs
+    for (int i = tid; i < Mk; i += kSelThreads) {
+      if (i < take) {
+        const int v = s_idx[i];
+        uint32_t bits;
+        if constexpr (sizeof(Raw) == 2)
+          bits = static_cast<uint32_t>(row[v]);
+        else
+          bits = __float_as_uint(row[v]);
+        const float2 d = ds_add(make_float2(KY::val(bits), 0.f), make_float2(-M, 0.f));  // exact
+        float2 lp = ds_mul_f(d, a.it_hi);
+        lp = ds_add(lp, make_float2(d.x * a.it_lo, 0.f));
+        lp = ds_add(lp, make_float2(-lz.x, -lz.y));
+        if (!(lp.x > -INFINITY)) lp = make_float2(-INFINITY, 0.f);  // a -inf logit: probability 0
+        out[i] = Cand{lp.x, lp.y, 0, v};
+      } else {
+        out[i] = Cand{-INFINITY, 0.f, 0, -1};  // fewer tokens than M in the vocabulary
+      }
+    }
+  }
+  if (st)
+    for (int i = tid; i < Mk; i += kSelThreads) out[i] = Cand{NAN, 0.f, -1, -1};
+  if (tid == 0) a.row_flag[row_id] = st;
+}
+
+constexpr int kMergeT = 256;
+constexpr int kMergeCap = 2048;  // F x M candidates held in shared memory (32 KB)
+
+// One CTA per batch row: the F x M candidates, scored and ranked.
+__global__ void __launch_bounds__(kMergeT) expand_merge_kernel(ExpArgs a) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int F = a.F, Mk = a.M, n = F * Mk;
+  __shared__ Cand s_c[kMergeCap];
+  __shared__ int s_st;
+  if (tid == 0) s_st = 0;
+  griddep_launch_dependents();
+  griddep_wait();
+  __syncthreads();
+  for (int f = tid; f < F; f += kMergeT) {
+    const float lc = a.logc[static_cast<long long>(b) * F + f];
+    const int fl = a.row_flag[static_cast<long long>(b) * F + f] | ((lc != lc || lc == INFINITY) ? SPEC_ROW_DRAFT : 0);
+    if (fl) atomicOr(&s_st, fl);
+  }
+  __syncthreads();
+  const int st = s_st;
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  for (int i = tid; i < n2; i += kMergeT) {
+    Cand c{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
+    if (i < n) {
+      const int f = i / Mk;
+      c = static_cast<const Cand*>(a.cand)[static_cast<long long>(b) * n + i];
+      c.f = f;
+      const float2 s = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
+      c.hi = s.x > -INFINITY ? s.x : -INFINITY;
+      c.lo = s.x > -INFINITY ? s.y : 0.f;
+      if (c.v < 0) c = Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};  // a slot past the vocabulary
+    }
+    s_c[i] = c;
+  }
+  __syncthreads();
+  for (int size = 2; size <= n2; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n2; i += kMergeT) {
+        const int pj = i ^ stride;
+        if (pj > i) {
+          const bool first = (i & size) == 0;
+          const Cand ci = s_c[i], cj = s_c[pj];
+          const bool i_before = cand_before(ci, cj);
+          if (first ? !i_before : i_before) {
+            s_c[i] = cj;
+            s_c[pj] = ci;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  for (int i = tid; i < Mk; i += kMergeT) {
+    const long long o = static_cast<long long>(b) * Mk + i;
+    const Cand c = s_c[i];
+    const bool ok = !st && c.v != 0x7fffffff;
+    a.parent[o] = ok ? c.f : -1;
+    a.token[o] = ok ? c.v : -1;
+    a.score[o] = ok ? c.hi + c.lo : NAN;
+  }
+  if (tid == 0) a.row_status[b] = st;
+}
+
+}  // namespace
+
+int expand_limits(int* max_m, int* max_fm) {
+  *max_m = kCand;
+  *max_fm = kMergeCap;
+  return 0;
+}
+
+cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st) {
+  const dim3 g1(static_cast<unsigned>(static_cast<long long>(a.B) * a.F));
+  cudaError_t e;
+  if (dtype == SPEC_BF16)
+    e = vec ? launch_pdl(expand_rows_kernel<uint16_t, true>, g1, dim3(kSelThreads), st, a)
+            : launch_pdl(expand_rows_kernel<uint16_t, false>, g1, dim3(kSelThreads), st, a);
+  else
+    e = vec ? launch_pdl(expand_rows_kernel<float, true>, g1, dim3(kSelThreads), st, a)
+            : launch_pdl(expand_rows_kernel<float, false>, g1, dim3(kSelThreads), st, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(expand_merge_kernel, dim3(static_cast<unsigned>(a.B)), dim3(kMergeT), st, a);
+}
+
+}  // namespace specv

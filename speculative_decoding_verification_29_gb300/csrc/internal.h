@@ -153,6 +153,24 @@ struct SelArgs {
 int select_candidates();
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st);
 
+// One expansion step of drafter trees by cumulative probability.
+struct ExpArgs {
+  const void* L;        // frontier logits [B][F][V]
+  const float* logc;    // [B][F] cumulative log-probabilities
+  int B, F, V, M, P;
+  float c_hi, c_lo;     // log2(e) / T
+  float it_hi, it_lo;   // 1 / T
+  const float2* part;   // stats partials [B * F][P]
+  void* cand;           // per frontier row: M candidates (score pair, node, token)
+  int32_t* row_flag;    // [B * F]
+  int32_t* parent;      // [B][M]
+  int32_t* token;       // [B][M]
+  float* score;         // [B][M]
+  int32_t* row_status;  // [B]
+};
+int expand_limits(int* max_m, int* max_fm);
+cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st);
+
 // Entropy routing of two drafter trees (after the rowscan in entropy mode).
 struct EntArgs {
   const float2* part;  // float4 partials [B * N][P]

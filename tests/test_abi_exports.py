@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     names = declared()
     for n in ("spec_verify_chain", "spec_verify_chain_greedy", "spec_verify_tree_greedy", "spec_tree_confidence",
               "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample", "spec_kv_compact",
-              "spec_tree_entropy", "spec_merge_trees", "spec_verify_chain_warped"):
+              "spec_tree_entropy", "spec_merge_trees", "spec_verify_chain_warped", "spec_tree_expand",
+              "spec_expand_workspace_bytes"):
         assert n in names
 
 
@@ -106,4 +107,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert kv(fake, 2, 4, 2, 64, 128, 16384, 8192, 128, fake, fake, 0, fake, fake, fake, n) == SPEC_ERR_ARG
     assert kv(fake, 2, 4, 2, 64, 128, 16384, 8192, 128, fake, fake, 2000, fake, fake, fake, n) == SPEC_ERR_UNSUPPORTED
     assert kv(fake, 2, 4, 70000, 64, 128, 16384, 8192, 128, fake, n, 0, fake, fake, fake, n) == SPEC_ERR_UNSUPPORTED
+    # tree expansion: temperature, M, the F x M limit, workspace
+    ex = lambda *a: lib.spec_tree_expand(*a)
+    assert ex(fake, 1, 0.0, fake, 2, 4, 64, 8, fake, fake, fake, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert ex(fake, 1, 1.0, fake, 2, 4, 64, 0, fake, fake, fake, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert ex(fake, 1, 1.0, n, 2, 4, 64, 8, fake, fake, fake, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert ex(fake, 1, 1.0, fake, 2, 64, 64, 64, fake, fake, fake, fake, fake, 1 << 30, n) == SPEC_ERR_UNSUPPORTED
+    assert ex(fake, 1, 1.0, fake, 2, 4, 64, 8, fake, fake, fake, fake, fake, 8, n) == SPEC_ERR_WORKSPACE
+    assert lib.spec_expand_workspace_bytes(2, 4, 64, 8, 1) % 256 == 0
+    assert lib.spec_expand_workspace_bytes(2, 64, 64, 64, 1) == 0
     assert lib.spec_status_string(-2) == b"workspace missing, misaligned or too small"
