@@ -9,9 +9,10 @@
 // the lower frontier node, then the lower token id. Only a node's own M most
 // probable tokens can be among them, so:
 //   rowscan (stats) over the F rows, then one CTA per frontier row selects
-//   its M largest logits (radix select on order-preserving keys, then the
-//   tokens at or above the M-th key sorted by key and id) and writes their
-//   log-probabilities as float pairs; one CTA per batch row sorts the F x M
+//   its M largest logits (one filtering pass for M <= 256, else a radix
+//   select on order-preserving keys; then the tokens at or above the M-th
+//   key sorted by key and id) and writes their log-probabilities as float
+//   pairs; one CTA per batch row sorts the F x M
 //   candidates by score (float pairs), node and token and keeps M.
 #include "select.cuh"
 
@@ -34,7 +35,7 @@ __device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
 }
 
 template <typename Raw, bool VEC>
-__global__ void __launch_bounds__(kSelThreads) expand_rows_kernel(ExpArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 5) expand_rows_kernel(ExpArgs a) {
   using KY = Key<Raw>;
   const int row_id = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
@@ -43,16 +44,21 @@ __global__ void __launch_bounds__(kSelThreads) expand_rows_kernel(ExpArgs a) {
   uint32_t* s_key = s_buf;
   int* s_idx = reinterpret_cast<int*>(s_buf + kCand);
   __shared__ unsigned s_tot[256];
+  __shared__ unsigned s_wh[kSelWarps * 256];
   __shared__ uint32_t s_sel[4];
+  __shared__ int s_cnt[kSelWarps];
   __shared__ int s_n;
-  __shared__ float s_M;
+  __shared__ float s_M, s_t0;
   __shared__ float2 s_lz;
   griddep_launch_dependents();
   griddep_wait();
   if (warp == 0) {
     float2 z;
-    const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+    const float2* pr = a.part + static_cast<long long>(row_id) * a.P;
+    const float M = fold_stats(pr, a.P, a.c_hi, a.c_lo, lane, &z);
+    const float t0 = seg_bound(pr, a.P, a.M < a.V ? a.M : a.V, lane);
     if (lane == 0) {
+      s_t0 = t0;
       s_M = M;
       const float2 l2 = ds_log2(z);  // ln Z = log2 Z * ln 2, as a float pair
       const float ln2_hi = 0.693147182464599609375f, ln2_lo = -1.904654323148236e-09f;
@@ -73,24 +79,32 @@ __global__ void __launch_bounds__(kSelThreads) expand_rows_kernel(ExpArgs a) {
   const int take = Mk < a.V ? Mk : a.V;
   unsigned cnt = static_cast<unsigned>(a.V);
   uint32_t tau = 0u;
-  if (take < a.V) tau = kth_largest<Raw, VEC>(row, a.V, take, hist, s_tot, s_sel, &cnt);
+  int have = -1;  // candidates already gathered by the filtering pass
+  if (take < a.V && take <= kFiltMaxK) {
+    const FiltSmem fs{s_key, s_idx, s_wh, s_tot, s_cnt, s_sel, &s_n};
+    have = filter_top<Raw, VEC>(row, a.V, take, s_t0, fs, &tau);
+    if (have >= 0) cnt = static_cast<unsigned>(have);
+  }
+  if (have < 0 && take < a.V) tau = kth_largest<Raw, VEC>(row, a.V, take, hist, s_tot, s_sel, &cnt);
   int st = 0;
   if (cnt > static_cast<unsigned>(kCand)) {
     st = SPEC_ROW_WARP;  // more tokens tie at the M-th value than the buffer holds
   } else {
-    if (tid == 0) s_n = 0;
-    __syncthreads();
-    for_row_i<Raw, VEC>(row, a.V, [&](int v, uint32_t bits) {
-      const uint32_t key = KY::of(bits);
-      if (key >= tau) {
-        const int slot = atomicAdd(&s_n, 1);
-        if (slot < kCand) {
-          s_key[slot] = key;
-          s_idx[slot] = v;
+    if (have < 0) {
+      if (tid == 0) s_n = 0;
+      __syncthreads();
+      for_row_i<Raw, VEC>(row, a.V, [&](int v, uint32_t bits) {
+        const uint32_t key = KY::of(bits);
+        if (key >= tau) {
+          const int slot = atomicAdd(&s_n, 1);
+          if (slot < kCand) {
+            s_key[slot] = key;
+            s_idx[slot] = v;
+          }
         }
-      }
-    });
-    __syncthreads();
+      });
+      __syncthreads();
+    }
     const int n = s_n < kCand ? s_n : kCand;
     int n2 = 1;
     while (n2 < n) n2 <<= 1;

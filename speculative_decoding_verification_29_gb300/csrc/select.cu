@@ -11,8 +11,10 @@
 // unsigned image of the logit's bits.
 //
 // One CTA per row, after the stats pass (its partials give M and Z):
-//   top-k: radix select of the k-th largest key, 8 bits per pass over the
-//          row (2 passes for bf16, 4 for fp32), counts only: exact;
+//   top-k: for k <= 256 one filtering pass gathers the k largest keys (ties
+//          included) and their weights; otherwise, or when ties overflow its
+//          buffers, a radix select of the k-th largest key, 8 bits per pass
+//          over the row (2 passes for bf16, 4 for fp32), counts only: exact;
 //   top-p: the row's largest tokens, whole groups of equal logits and at
 //          most kCand of them (its top-k when that is fewer), are collected
 //          into shared memory, sorted by key, and their weights
@@ -52,7 +54,7 @@ __device__ float2 kept_mass(const Raw* row, int V, uint32_t tau, W weight, float
 }
 
 template <typename Raw, bool VEC>
-__global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) {
   using KY = Key<Raw>;
   const int row_id = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int RPG = a.TR + a.DR;
@@ -66,17 +68,22 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
   float* s_w = reinterpret_cast<float*>(s_buf + kCand);      // kCand weights
   static_assert(kSelWarps * 256 <= 2 * kCand, "histograms fit the candidate buffer");
   __shared__ unsigned s_tot[256];
+  __shared__ unsigned s_wh[kSelWarps * 256];
   __shared__ uint32_t s_sel[4];
   __shared__ float2 s_ds[kSelWarps];
+  __shared__ int s_cnt[kSelWarps];
   __shared__ int s_n, s_last;
-  __shared__ float s_M;
+  __shared__ float s_M, s_t0;
   __shared__ float2 s_Z;
   griddep_launch_dependents();
   griddep_wait();
-  if (warp == 0) {  // M and Z of the row from the stats partials
+  if (warp == 0) {  // M and Z of the row from the stats partials, and a lower bound of the k-th largest logit
     float2 z;
-    const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+    const float2* pr = a.part + static_cast<long long>(row_id) * a.P;
+    const float M = fold_stats(pr, a.P, a.c_hi, a.c_lo, lane, &z);
+    const float t0 = a.top_k > 0 ? seg_bound(pr, a.P, a.top_k, lane) : -INFINITY;
     if (lane == 0) {
+      s_t0 = t0;
       s_M = M;
       s_Z = z;
     }
@@ -85,10 +92,11 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
   const float M = s_M;
   const float2 Zfull = s_Z;
   const bool ok = M == M && isfinite(M) && Zfull.x > 0.f;
-  auto weight = [&](uint32_t bits) {
-    const float d = KY::val(bits) - M;
+  auto weight_v = [&](float l) {
+    const float d = l - M;
     return ex2_fast(fmaf(d, a.c_hi, d * a.c_lo));
   };
+  auto weight = [&](uint32_t bits) { return weight_v(KY::val(bits)); };
   StatRec out;
   out.M = M;
   out.Z = NAN;
@@ -98,7 +106,17 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
   if (ok) {
     const bool use_k = a.top_k > 0 && a.top_k < a.V;
     unsigned count_ge = static_cast<unsigned>(a.V);  // tokens top-k keeps
-    if (use_k) tau = kth_largest<Raw, VEC>(row, a.V, a.top_k, hist, s_tot, s_sel, &count_ge);
+    int have = -1;  // the top-k set already gathered (keys and weights) by the filtering pass
+    if (use_k && a.top_k <= kFiltMaxK) {
+      const FiltSmem fs{s_key, reinterpret_cast<int*>(s_w), s_wh, s_tot, s_cnt, s_sel, &s_n};
+      have = filter_top<Raw, VEC>(row, a.V, a.top_k, s_t0, fs, &tau);
+      if (have >= 0) {
+        count_ge = static_cast<unsigned>(have);
+        for (int e = tid; e < have; e += kSelThreads) s_w[e] = weight_v(key_value<Raw>(s_key[e]));
+        __syncthreads();
+      }
+    }
+    if (use_k && have < 0) tau = kth_largest<Raw, VEC>(row, a.V, a.top_k, hist, s_tot, s_sel, &count_ge);
     // candidates: the keys >= tc, whole groups of equal keys and at most kCand
     // of them: every token top-k keeps when they fit ("own"), else the groups
     // above the (kCand + 1)-th largest key
@@ -113,20 +131,22 @@ __global__ void __launch_bounds__(kSelThreads) warp_select_kernel(SelArgs a) {
     if (a.top_p >= 1.f && !own) {
       Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);  // top-k alone, more tokens than the buffer
     } else {
-      if (tid == 0) s_n = 0;
-      __syncthreads();
-      for_row<Raw, VEC>(row, a.V, [&](uint32_t bits) {
-        const uint32_t key = KY::of(bits);
-        if (key >= tc) {
-          const int slot = atomicAdd(&s_n, 1);
-          if (slot < kCand) {
-            s_key[slot] = key;
-            s_w[slot] = weight(bits);
+      if (have < 0) {
+        if (tid == 0) s_n = 0;
+        __syncthreads();
+        for_row<Raw, VEC>(row, a.V, [&](uint32_t bits) {
+          const uint32_t key = KY::of(bits);
+          if (key >= tc) {
+            const int slot = atomicAdd(&s_n, 1);
+            if (slot < kCand) {
+              s_key[slot] = key;
+              s_w[slot] = weight(bits);
+            }
           }
-        }
-      });
-      __syncthreads();
-      const int n = s_n;  // <= kCand by the choice of tc (checked all the same)
+        });
+        __syncthreads();
+      }
+      const int n = have >= 0 ? have : s_n;  // <= kCand by the choice of tc (checked all the same)
       constexpr int kPer = kCand / kSelThreads;
       if (n > kCand) {
         st = SPEC_ROW_WARP;

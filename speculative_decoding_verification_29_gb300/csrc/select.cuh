@@ -1,6 +1,7 @@
 // select.cuh -- per-row selection over logits: order-preserving keys, a
-// pass over a row, the k-th largest key by radix select, and block sums of
-// float pairs (one CTA of kSelThreads per row).
+// pass over a row, the k-th largest key (one filtering pass for small k, a
+// radix select over the row otherwise), and block sums of float pairs (one
+// CTA of kSelThreads per row).
 #pragma once
 
 #include "fold.cuh"
@@ -8,7 +9,7 @@
 namespace specv {
 namespace sel {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kCand = 4096;
 
@@ -105,6 +106,60 @@ __device__ __forceinline__ void for_row_i(const Raw* row, int V, F f) {
   }
 }
 
+__device__ __forceinline__ int warp_incl_scan(int c, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, c, o);
+    if (lane >= o) c += y;
+  }
+  return c;
+}
+
+// One digit of a radix select, on one full warp: hist holds the 256 bin
+// counts; the bin where the count from the top reaches kk. Every lane gets
+// the digit, the rank left inside that bin and (when asked) the counts above
+// the bin and in it.
+__device__ __forceinline__ void pick_digit(const unsigned* hist, unsigned kk, int lane, unsigned& digit,
+                                           unsigned& kk_in_bin, unsigned* above_bin = nullptr,
+                                           unsigned* in_bin = nullptr) {
+  unsigned c[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // lane l holds bins 255-8l .. 248-8l
+    c[i] = hist[255 - 8 * lane - i];
+    sum += c[i];
+  }
+  unsigned incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const unsigned above = incl - sum;
+  const bool here = above < kk && kk <= incl;
+  const unsigned hit = __ballot_sync(0xffffffffu, here);
+  unsigned d = 0, kn = 1, ab = above, cb = 0;
+  bool found = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (!found) {
+      if (ab + c[i] >= kk) {
+        found = true;
+        d = 255u - 8u * lane - i;
+        kn = kk - ab;
+        cb = c[i];
+      } else {
+        ab += c[i];
+      }
+    }
+  }
+  const int src = hit ? __ffs(hit) - 1 : 0;
+  digit = hit ? __shfl_sync(0xffffffffu, d, src) : 0u;
+  kk_in_bin = hit ? __shfl_sync(0xffffffffu, kn, src) : 1u;
+  // fewer than kk keys match (cannot happen for kk <= the keys counted): keep them all
+  if (above_bin) *above_bin = hit ? __shfl_sync(0xffffffffu, ab, src) : 0u;
+  if (in_bin) *in_bin = hit ? __shfl_sync(0xffffffffu, cb, src) : 0u;
+}
+
 // Largest key K with #{keys >= K} >= k (the k-th largest key), over the
 // row, by 8-bit digits from the top; *count_ge receives #{keys >= K}.
 // hist: kSelWarps x 256 counters.
@@ -131,35 +186,14 @@ __device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, un
       s_tot[bin] = c;
     }
     __syncthreads();
-    if (warp == 0) {  // bin where the count from the top reaches kk: lane l holds bins 255-8l .. 248-8l
-      unsigned c[8], sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = s_tot[255 - 8 * lane - i];
-        sum += c[i];
-      }
-      unsigned incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      unsigned above = incl - sum;  // count in higher bins than this lane's
-      const bool here = above < kk && kk <= incl;
-      const unsigned hit = __ballot_sync(0xffffffffu, here);
-      if (hit && lane == __ffs(hit) - 1) {
-        int i = 0;
-        while (above + c[i] < kk) above += c[i++];
-        s_sel[0] = static_cast<uint32_t>(255 - 8 * lane - i);
-        s_sel[1] = kk - above;
-        s_sel[2] = above;  // keys in higher bins
-        s_sel[3] = c[i];   // keys in this bin
-      }
-      if (!hit && lane == 0) {  // fewer than kk keys match: keep them all (cannot happen for k <= V)
-        s_sel[0] = 0;
-        s_sel[1] = 1;
-        s_sel[2] = 0;
-        s_sel[3] = 0;
+    if (warp == 0) {
+      unsigned d, kn, ab, cb;
+      pick_digit(s_tot, kk, lane, d, kn, &ab, &cb);
+      if (lane == 0) {
+        s_sel[0] = d;
+        s_sel[1] = kn;
+        s_sel[2] = ab;  // keys in higher bins
+        s_sel[3] = cb;  // keys in this bin
       }
     }
     __syncthreads();
@@ -171,6 +205,270 @@ __device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, un
   }
   *count_ge = greater + last_bin;  // the last digit's bin holds exactly the keys equal to K
   return prefix;
+}
+
+// ------------------------------------------------------- small k: filter --
+//
+// The k largest keys of a row in one pass. Warp w streams its own contiguous
+// slice of the row and appends every element whose value is >= its running
+// threshold t_w to a private buffer of kFiltCap (key, index) entries; when
+// the buffer would overflow it finds the k-th largest buffered key K_w (a
+// radix select in shared memory), drops the entries below it and raises t_w
+// to K_w. t_w starts at a lower bound t0 of the row's k-th largest value
+// and never exceeds the k-th largest key of the slice, hence never the
+// row's, so every element at or above the row's k-th largest key K stays
+// buffered. A block-level radix select over the buffers then gives K and the
+// exact count of keys >= K. Elements below a warp's threshold cost a packed
+// max and a compare per 16-byte vector; the row is read once.
+//
+// t0 comes from the stats pass: if k of its segment maxima are >= t, then k
+// elements of the row are >= t. Because the k largest elements of a row
+// usually sit in k different segments, the k-th largest segment maximum is
+// usually the row's k-th largest value itself, and only a handful of
+// elements ever take the appending path.
+
+// Largest t (to 16 bits of the order-preserving key) with at least k of the
+// P segment maxima (pr[c].x) >= t: a lower bound of the row's k-th largest
+// value; -inf when k > P or P > 256. One full warp; every lane gets it.
+__device__ __forceinline__ float seg_bound(const float2* pr, int P, int k, int lane) {
+  if (k > P || P > 256) return -INFINITY;
+  uint32_t key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int c = lane + 32 * i;
+    key[i] = c < P ? Key<float>::of(__float_as_uint(__ldcg(pr + c).x)) : 0u;
+  }
+  uint32_t prefix = 0;
+#pragma unroll 1
+  for (int bit = 31; bit >= 16; --bit) {
+    const uint32_t cand = prefix | (1u << bit);
+    unsigned cnt = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cnt += key[i] >= cand ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, cnt) >= static_cast<unsigned>(k)) prefix = cand;
+  }
+  return key_value<float>(prefix);
+}
+
+constexpr int kFiltCap = kCand / kSelWarps;  // entries per warp buffer
+constexpr int kFiltMaxK = 256;               // compaction keeps k < kFiltCap - one round of appends
+
+// k-th largest of the n keys of a warp buffer (n >= k); hist: 256 counters
+// private to the warp.
+template <int KBITS>
+__device__ uint32_t warp_kth(const uint32_t* keys, int n, unsigned k, unsigned* hist, int lane) {
+  uint32_t prefix = 0;
+  unsigned kk = k;
+#pragma unroll 1
+  for (int shift = KBITS - 8; shift >= 0; shift -= 8) {
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+    for (int e = lane; e < n; e += 32) {
+      const uint32_t key = keys[e];
+      if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(hist + ((key >> shift) & 0xFFu), 1u);
+    }
+    __syncwarp();
+    unsigned d, kn;
+    pick_digit(hist, kk, lane, d, kn);
+    prefix |= d << shift;
+    kk = kn;
+    __syncwarp();
+  }
+  return prefix;
+}
+
+// Shared memory of filter_top: key[kCand] and idx[kCand] (the warp buffers,
+// then the candidates), whist[kSelWarps * 256], tot[256], cnt[kSelWarps],
+// sel[2], n[1].
+struct FiltSmem {
+  uint32_t* key;
+  int* idx;
+  unsigned* whist;
+  unsigned* tot;
+  int* cnt;
+  uint32_t* sel;
+  int* n;
+};
+
+// The elements with key >= K, K the k-th largest key of the row (1 <= k <=
+// kFiltMaxK, k <= V; t0 <= the k-th largest value): their keys and indices
+// in key[0, n), idx[0, n) (no order), *tau = K, returns n (= #keys >= K,
+// ties included). Returns -1 when
+// some warp's ties at its threshold overflow its buffer (then the caller
+// selects by radix passes). Called by every thread of the CTA.
+template <typename Raw, bool VEC>
+__device__ int filter_top(const Raw* row, int V, int k, float t0, const FiltSmem& sm, uint32_t* tau) {
+  using KY = Key<Raw>;
+  constexpr int E = VEC ? Elem<Raw>::kPerVec : 1;  // elements per load
+  constexpr int U = VEC ? 4 : 8;                   // loads in flight per lane
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* wkey = sm.key + warp * kFiltCap;
+  int* widx = sm.idx + warp * kFiltCap;
+  unsigned* wh = sm.whist + warp * 256;
+  const int nunits = VEC ? V / E : V;
+  const int per = (nunits + kSelWarps - 1) / kSelWarps;
+  const int u0 = min(nunits, warp * per), u1 = min(nunits, u0 + per);
+  float t_val = t0;
+  int n = 0;
+  bool over = false;
+  for (int ub = u0; ub < u1 && !over; ub += 32 * U) {
+    uint4 q[U];
+    float s1[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int u = ub + i * 32 + lane;
+      if constexpr (VEC) {
+        q[i] = u < u1 ? ld_stream_v4(reinterpret_cast<const uint4*>(row) + u) : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        s1[i] = u < u1 ? Elem<Raw>::at(row, u) : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (over) continue;
+      const int u = ub + i * 32 + lane;
+      const bool valid = u < u1;
+      float vmax;
+      if constexpr (VEC)
+        vmax = Vec<Raw>::vmax(q[i]);
+      else
+        vmax = s1[i];
+      if (!__any_sync(0xffffffffu, valid && vmax >= t_val)) continue;
+      float v[E];
+      uint32_t bits[E];
+      if constexpr (VEC) {
+        Elem<Raw>::unpack(q[i], v);
+        const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if constexpr (E == 8)
+            bits[e] = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+          else
+            bits[e] = w[e];
+        }
+      } else {
+        v[0] = s1[i];
+        if constexpr (sizeof(Raw) == 2)
+          bits[0] = __float_as_uint(s1[i]) >> 16;
+        else
+          bits[0] = __float_as_uint(s1[i]);
+      }
+      unsigned m = 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (valid && v[e] >= t_val) m |= 1u << e;
+      int c = __popc(m);
+      int incl = warp_incl_scan(c, lane);
+      int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (n + total > kFiltCap) {  // n > kFiltCap - 32 E >= k: keep the keys >= the k-th largest
+        __syncwarp();
+        const uint32_t K = warp_kth<KY::kBits>(wkey, n, static_cast<unsigned>(k), wh, lane);
+        int nn = 0;
+        for (int e0 = 0; e0 < n; e0 += 32) {  // in place: an entry only moves down
+          const int e = e0 + lane;
+          uint32_t kv = 0;
+          int iv = 0;
+          if (e < n) {
+            kv = wkey[e];
+            iv = widx[e];
+          }
+          __syncwarp();
+          const bool keep = e < n && kv >= K;
+          const unsigned bm = __ballot_sync(0xffffffffu, keep);
+          if (keep) {
+            const int p = nn + __popc(bm & ((1u << lane) - 1u));
+            wkey[p] = kv;
+            widx[p] = iv;
+          }
+          nn += __popc(bm);
+          __syncwarp();
+        }
+        n = nn;
+        t_val = key_value<Raw>(K);
+        m = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (valid && v[e] >= t_val) m |= 1u << e;
+        c = __popc(m);
+        incl = warp_incl_scan(c, lane);
+        total = __shfl_sync(0xffffffffu, incl, 31);
+        if (n + total > kFiltCap) {  // ties at the threshold fill the buffer
+          over = true;
+          continue;
+        }
+      }
+      int p = n + incl - c;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if ((m >> e) & 1u) {
+          wkey[p] = KY::of(bits[e]);
+          widx[p] = VEC ? u * E + e : u;
+          ++p;
+        }
+      n += total;
+      __syncwarp();
+    }
+  }
+  if (lane == 0) sm.cnt[warp] = over ? -1 : n;
+  __syncthreads();
+  int bad = 0;
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) bad |= sm.cnt[w] < 0;
+  if (bad) return -1;
+  // K over the union of the buffers: radix select, one shared histogram
+  constexpr int kPer = kCand / kSelThreads;
+  uint32_t kr[kPer];
+  int ir[kPer];
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int e = tid + r * kSelThreads;
+    const bool ok = (e % kFiltCap) < sm.cnt[e / kFiltCap];
+    kr[r] = ok ? sm.key[e] : 0u;
+    ir[r] = ok ? sm.idx[e] : -1;
+  }
+  uint32_t prefix = 0;
+  unsigned kk = static_cast<unsigned>(k);
+#pragma unroll 1
+  for (int shift = KY::kBits - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kSelThreads) sm.tot[i] = 0;
+    __syncthreads();
+    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+#pragma unroll
+    for (int r = 0; r < kPer; ++r)
+      if (ir[r] >= 0 && (kr[r] & hi_mask) == (prefix & hi_mask)) atomicAdd(sm.tot + ((kr[r] >> shift) & 0xFFu), 1u);
+    __syncthreads();
+    if (warp == 0) {
+      unsigned d, kn;
+      pick_digit(sm.tot, kk, lane, d, kn);
+      if (lane == 0) {
+        sm.sel[0] = d;
+        sm.sel[1] = kn;
+      }
+    }
+    __syncthreads();
+    prefix |= sm.sel[0] << shift;
+    kk = sm.sel[1];
+  }
+  // the keys >= K, packed to the front
+  if (tid == 0) *sm.n = 0;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const bool keep = ir[r] >= 0 && kr[r] >= prefix;
+    const unsigned bm = __ballot_sync(0xffffffffu, keep);
+    int base = 0;
+    if (lane == 0 && bm) base = atomicAdd(sm.n, __popc(bm));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (keep) {
+      const int p = base + __popc(bm & ((1u << lane) - 1u));
+      sm.key[p] = kr[r];
+      sm.idx[p] = ir[r];
+    }
+  }
+  __syncthreads();
+  *tau = prefix;
+  return *sm.n;
 }
 
 // Sum of float pairs over the block (every thread gets it); sh: kSelWarps pairs.

@@ -102,6 +102,20 @@ def test_expand_ties(dtype):
         compare(*run(Ld, logc, M), M, 1.0)
 
 
+def test_expand_segment_bound_and_fallback():
+    """65536-token rows (32 stats segments, so the segment maxima bound the
+    filter's threshold) of quarter-step logits (ties in plenty); one node has
+    1000 tied maxima inside one warp's slice, which overflows the filtering
+    buffer and falls back to the radix passes."""
+    g = torch.Generator().manual_seed(8)
+    B, F, V = 3, 4, 65536
+    Ld = (torch.randint(-60, 61, (B, F, V), generator=g).float() / 4).to(torch.bfloat16)
+    logc = torch.log(torch.rand(B, F, generator=g)).float()
+    Ld[1, 2, :1000] = 20.0
+    for M in (5, 20, 32):
+        compare(*run(Ld, logc, M), M, 1.0)
+
+
 def test_expand_more_slots_than_children():
     """M >= V and M > F * V: every child is kept, the remaining slots are
     -1 / NaN."""

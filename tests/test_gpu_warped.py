@@ -107,6 +107,23 @@ def test_warped_ties_at_the_boundary():
         compare(*run(c, k, p), allow_warp=True)
 
 
+@pytest.mark.parametrize("top_k,top_p", [(5, 1.0), (20, 0.7), (50, 0.95)])
+def test_warped_segment_bound_and_fallback(top_k, top_p):
+    """65536-token bf16 rows of quarter-step logits (32 stats segments bound
+    the filtering threshold; ties in plenty); one row has 1000 tied maxima in
+    one warp's slice, which overflows the filtering buffer and falls back to
+    the radix passes."""
+    g0 = torch.Generator().manual_seed(9)
+    B, K, V = 4, 3, 65536
+    Lp = (torch.randint(-60, 61, (B, K + 1, V), generator=g0).float() / 4).to(torch.bfloat16)
+    Lq = (torch.randint(-60, 61, (B, K, V), generator=g0).float() / 4).to(torch.bfloat16)
+    Lp[1, 0, :1000] = 20.0
+    Lq[2, 1, 3000:4000] = 20.0
+    x = gen.workloads._gumbel_draw(Lq, 1.0, g0, top_k)
+    c = gen.ChainBatch("seg", Lp, Lq, x, torch.rand(B, K, generator=g0), torch.rand(B, generator=g0), 1.0)
+    compare(*run(c, top_k, top_p), allow_warp=True)
+
+
 def test_warped_serving_batch():
     """B=64, K=8, V=128256 bf16, T=0.7 (the batched serving workload) with
     top-k 50 and top-p 0.9 on both models."""
