@@ -180,11 +180,19 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logit
  * accepted iff the target keeps it.
  * Arguments as spec_verify_chain (no lse outputs; p_at_x, q_at_x are p', q'),
  * plus temperature > 0, top_k >= 0, 0 < top_p <= 1. Workspace:
- * spec_workspace_bytes(B, K, V, dtype). Extra passes over the rows: 2 (bf16)
- * or 4 (fp32) for top-k; for top-p, 2 / 4 more to find the row's largest
- * tokens (at most 4096, whole groups of equal logits, or its top-k when
- * that is fewer) and one collecting them; one summing the kept mass. A row
- * whose nucleus reaches past those tokens gets SPEC_ROW_WARP. */
+ * spec_workspace_bytes(B, K, V, dtype) bytes suffice; with
+ * spec_warped_workspace_bytes(B, K, V, dtype) bytes, and top_k at most the
+ * number of 4 KB segments of a row (63 for V = 128256 bf16), a filter pass
+ * lists each row's candidates for its top-k in the workspace and the
+ * selection reads only those lists (one extra pass over the rows in all).
+ * Otherwise the extra passes are: for top_k <= 256, one filtering the row
+ * (ties overflowing its buffers: as for larger top_k); for larger top_k,
+ * 2 (bf16) or 4 (fp32) radix passes; for top-p alone (or top-k sets of
+ * more than 4096 tokens), 2 / 4 more to find the row's largest tokens (at
+ * most 4096, whole groups of equal logits) and one collecting them; one
+ * summing the kept mass when the top-k set does not fit. A row whose
+ * nucleus reaches past those tokens gets SPEC_ROW_WARP. */
+size_t spec_warped_workspace_bytes(int B, int K, int V, int dtype);
 int spec_verify_chain_warped(const void* target_logits, const void* draft_logits, int dtype,
                              const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
                              float temperature, int top_k, float top_p, int B, int K, int V, int32_t* accept_len,
@@ -295,9 +303,11 @@ int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, in
  * tokens of one node tie at its M-th largest logit; such a row's outputs
  * are all -1 / NaN. Scores are exact to about 1e-6 (the normaliser's fp32
  * exponentials); candidates of one node rank exactly by logit. Passes over
- * each frontier row: one for the softmax statistics, one per 8-bit radix
- * digit of the M-th largest logit (2 for bf16, 4 for fp32; none when
- * M >= V) and one to collect the top M. */
+ * each frontier row: one for the softmax statistics, then (M < V) one
+ * filter pass listing the elements at or above the M-th largest segment
+ * maximum when M is at most the number of 4 KB segments of a row, or one
+ * filtering pass of the per-row selection for M <= 256, or 2 (bf16) / 4
+ * (fp32) radix passes and one collecting the top M otherwise. */
 size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype);
 int spec_tree_expand(const void* draft_logits, int dtype, float temperature, const float* logc, int B, int F, int V,
                      int M, int32_t* parent, int32_t* token, float* score, int32_t* row_status, void* workspace,

@@ -18,6 +18,7 @@ __all__ = [
     "spec_tree_expand",
     "spec_kv_compact",
     "workspace_bytes",
+    "warped_workspace_bytes",
     "alloc_workspace",
 ]
 

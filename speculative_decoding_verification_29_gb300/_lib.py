@@ -24,6 +24,7 @@ Z = ctypes.c_size_t
 
 SIGNATURES = {
     "spec_workspace_bytes": (Z, [I, I, I, I]),
+    "spec_warped_workspace_bytes": (Z, [I, I, I, I]),
     "spec_verify_chain": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P, Z, P]),
     "spec_verify_chain_noalloc": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P]),
     "spec_chain_scan": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P, Z, P]),

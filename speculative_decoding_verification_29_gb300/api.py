@@ -49,6 +49,13 @@ def workspace_bytes(B: int, K: int, V: int, dtype) -> int:
     return int(_lib.load().spec_workspace_bytes(B, K, V, code))
 
 
+def warped_workspace_bytes(B: int, K: int, V: int, dtype) -> int:
+    """Workspace with room for the top-k candidate lists of
+    spec_verify_chain_warped (workspace_bytes suffices, but is slower)."""
+    code = dtype if isinstance(dtype, int) else (SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32)
+    return int(_lib.load().spec_warped_workspace_bytes(B, K, V, code))
+
+
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
     """Device workspace with a 256-byte aligned start."""
     buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
@@ -325,7 +332,7 @@ def spec_verify_chain_warped(target_logits, draft_logits, draft_tokens, u_accept
     ur = _dev(u_resample, dev, torch.float32)
     code = _dtype_code(Lp)
     if workspace is None:
-        workspace = alloc_workspace(workspace_bytes(B, K, V, code), dev)
+        workspace = alloc_workspace(warped_workspace_bytes(B, K, V, code), dev)
     if out is None:
         out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
                    out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),

@@ -8,11 +8,13 @@
 // log softmax(l_f / T)[v]; the M best children are kept, by score, ties to
 // the lower frontier node, then the lower token id. Only a node's own M most
 // probable tokens can be among them, so:
-//   rowscan (stats) over the F rows, then one CTA per frontier row selects
-//   its M largest logits (one filtering pass for M <= 256, else a radix
-//   select on order-preserving keys; then the tokens at or above the M-th
-//   key sorted by key and id) and writes their log-probabilities as float
-//   pairs; one CTA per batch row sorts the F x M
+//   rowscan (stats) over the F rows; for M up to the number of stats
+//   segments the candidate filter pass lists each row's elements at or above
+//   its M-th largest segment maximum; then one CTA per frontier row selects
+//   its M largest logits (from the list when it is complete, else by one
+//   filtering pass over the row for M <= 256, else by radix select on
+//   order-preserving keys; then the tokens at or above the M-th key sorted
+//   by key and id) and writes their log-probabilities as float pairs; one CTA per batch row sorts the F x M
 //   candidates by score (float pairs), node and token and keeps M.
 #include "select.cuh"
 
@@ -56,9 +58,7 @@ __global__ void __launch_bounds__(kSelThreads, 5) expand_rows_kernel(ExpArgs a) 
     float2 z;
     const float2* pr = a.part + static_cast<long long>(row_id) * a.P;
     const float M = fold_stats(pr, a.P, a.c_hi, a.c_lo, lane, &z);
-    const float t0 = seg_bound(pr, a.P, a.M < a.V ? a.M : a.V, lane);
     if (lane == 0) {
-      s_t0 = t0;
       s_M = M;
       const float2 l2 = ds_log2(z);  // ln Z = log2 Z * ln 2, as a float pair
       const float ln2_hi = 0.693147182464599609375f, ln2_lo = -1.904654323148236e-09f;
@@ -79,9 +79,21 @@ __global__ void __launch_bounds__(kSelThreads, 5) expand_rows_kernel(ExpArgs a) 
   const int take = Mk < a.V ? Mk : a.V;
   unsigned cnt = static_cast<unsigned>(a.V);
   uint32_t tau = 0u;
-  int have = -1;  // candidates already gathered by the filtering pass
-  if (take < a.V && take <= kFiltMaxK) {
-    const FiltSmem fs{s_key, s_idx, s_wh, s_tot, s_cnt, s_sel, &s_n};
+  int have = -1;  // candidates already gathered (from the filter pass's list, or by filtering the row here)
+  const FiltSmem fs{s_key, s_idx, s_wh, s_tot, s_cnt, s_sel, &s_n};
+  if (take < a.V && a.cl.seg_cap > 0) {
+    const int n = gather_list(a.cl, row_id, fs);
+    if (n >= take) {  // a complete list
+      have = top_from_list<Raw>(n, take, fs, &tau);
+      cnt = static_cast<unsigned>(have);
+    }
+  }
+  if (have < 0 && take < a.V && take <= kFiltMaxK) {
+    if (warp == 0) {  // a lower bound of the M-th largest logit to start from
+      const float t0 = seg_bound(a.part + static_cast<long long>(row_id) * a.P, a.P, take, lane);
+      if (lane == 0) s_t0 = t0;
+    }
+    __syncthreads();
     have = filter_top<Raw, VEC>(row, a.V, take, s_t0, fs, &tau);
     if (have >= 0) cnt = static_cast<unsigned>(have);
   }

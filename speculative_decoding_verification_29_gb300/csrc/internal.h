@@ -64,6 +64,30 @@ struct ScanArgs {
   float2* part;      // [B * (TR + DR)][P]
 };
 
+// Per-row candidate lists of a top-k: every element at or above a lower
+// bound of the row's k-th largest logit, kept per stats segment (P segments
+// of seg_cap entries per row, no atomics between segments).
+struct CandList {
+  int seg_cap;     // entries per segment; 0: no lists
+  int P;           // segments per row
+  int32_t* cnt;    // [rows][P] elements at or above the bound (> seg_cap: that sublist is incomplete)
+  uint32_t* key;   // [rows][P][seg_cap] order-preserving keys
+  int32_t* idx;    // [rows][P][seg_cap] token ids
+};
+constexpr int kCandSeg = 16;   // entries per segment
+constexpr int kCandCap = 512;  // entries per row a selection gathers
+
+// The candidate filter pass (after the stats pass): rows as in ScanArgs.
+struct CandArgs {
+  const void* A;
+  const void* Bd;
+  int B, TR, DR, V, P;
+  int k;  // rank the lists must cover (1 <= k <= P <= 256)
+  const float2* part;
+  CandList cl;
+};
+cudaError_t launch_cand_filter(const CandArgs& a, int dtype, bool vec, cudaStream_t st);
+
 // Warp segments per row, and so partials per row, for a vocabulary of V
 // entries.
 __host__ __device__ inline int warp_chunks(int V, bool vec, int dtype) {
@@ -149,6 +173,7 @@ struct SelArgs {
   StatRec* rec;        // [rows]: M, kept mass Z', log2 Z'
   float* vtau;         // [rows]: a token is kept iff its logit >= vtau
   int32_t* row_flag;   // [rows]: SPEC_ROW_WARP or 0
+  CandList cl;         // top-k candidate lists from the filter pass (cap 0: none)
 };
 int select_candidates();
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st);
@@ -167,6 +192,7 @@ struct ExpArgs {
   int32_t* token;       // [B][M]
   float* score;         // [B][M]
   int32_t* row_status;  // [B]
+  CandList cl;          // top-M candidate lists from the filter pass (cap 0: none)
 };
 int expand_limits(int* max_m, int* max_fm);
 cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st);

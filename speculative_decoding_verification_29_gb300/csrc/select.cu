@@ -11,10 +11,13 @@
 // unsigned image of the logit's bits.
 //
 // One CTA per row, after the stats pass (its partials give M and Z):
-//   top-k: for k <= 256 one filtering pass gathers the k largest keys (ties
-//          included) and their weights; otherwise, or when ties overflow its
-//          buffers, a radix select of the k-th largest key, 8 bits per pass
-//          over the row (2 passes for bf16, 4 for fp32), counts only: exact;
+//   top-k: the k largest keys (ties included) and their weights come from
+//          the candidate filter pass's list of the row when it ran (k up to
+//          the number of stats segments) and the list is complete; else, for
+//          k <= 256, from one filtering pass over the row here; otherwise,
+//          or when ties overflow the buffers, a radix select of the k-th
+//          largest key, 8 bits per pass over the row (2 passes for bf16, 4
+//          for fp32), counts only: exact;
 //   top-p: the row's largest tokens, whole groups of equal logits and at
 //          most kCand of them (its top-k when that is fewer), are collected
 //          into shared memory, sorted by key, and their weights
@@ -75,15 +78,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
   __shared__ int s_n, s_last;
   __shared__ float s_M, s_t0;
   __shared__ float2 s_Z;
-  griddep_launch_dependents();
   griddep_wait();
   if (warp == 0) {  // M and Z of the row from the stats partials, and a lower bound of the k-th largest logit
     float2 z;
     const float2* pr = a.part + static_cast<long long>(row_id) * a.P;
     const float M = fold_stats(pr, a.P, a.c_hi, a.c_lo, lane, &z);
-    const float t0 = a.top_k > 0 ? seg_bound(pr, a.P, a.top_k, lane) : -INFINITY;
     if (lane == 0) {
-      s_t0 = t0;
       s_M = M;
       s_Z = z;
     }
@@ -106,9 +106,25 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
   if (ok) {
     const bool use_k = a.top_k > 0 && a.top_k < a.V;
     unsigned count_ge = static_cast<unsigned>(a.V);  // tokens top-k keeps
-    int have = -1;  // the top-k set already gathered (keys and weights) by the filtering pass
-    if (use_k && a.top_k <= kFiltMaxK) {
-      const FiltSmem fs{s_key, reinterpret_cast<int*>(s_w), s_wh, s_tot, s_cnt, s_sel, &s_n};
+    int have = -1;  // the top-k set already gathered (keys and weights): from the list or by filtering here
+    const FiltSmem fs{s_key, reinterpret_cast<int*>(s_w), s_wh, s_tot, s_cnt, s_sel, &s_n};
+    if (use_k && a.cl.seg_cap > 0) {
+      const int n = gather_list(a.cl, row_id, fs);
+      if (n >= a.top_k) {  // a complete list
+        have = top_from_list<Raw>(n, a.top_k, fs, &tau);
+        if (have >= 0) {
+          count_ge = static_cast<unsigned>(have);
+          for (int e = tid; e < have; e += kSelThreads) s_w[e] = weight_v(key_value<Raw>(s_key[e]));
+          __syncthreads();
+        }
+      }
+    }
+    if (use_k && have < 0 && a.top_k <= kFiltMaxK) {
+      if (warp == 0) {  // a lower bound of the k-th largest logit to start from
+        const float t0 = seg_bound(a.part + static_cast<long long>(row_id) * a.P, a.P, a.top_k, lane);
+        if (lane == 0) s_t0 = t0;
+      }
+      __syncthreads();
       have = filter_top<Raw, VEC>(row, a.V, a.top_k, s_t0, fs, &tau);
       if (have >= 0) {
         count_ge = static_cast<unsigned>(have);
@@ -240,6 +256,9 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
       out.Llo = L2.y;
     }
   }
+  // the trigger comes late: the tail's clusters would otherwise hold SM slots,
+  // idle, while rows are still being selected
+  griddep_launch_dependents();
   if (tid == 0) {
     a.rec[row_id] = out;
     a.vtau[row_id] = key_value<Raw>(tau);

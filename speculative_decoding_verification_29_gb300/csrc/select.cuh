@@ -228,26 +228,43 @@ __device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, un
 // elements ever take the appending path.
 
 // Largest t (to 16 bits of the order-preserving key) with at least k of the
-// P segment maxima (pr[c].x) >= t: a lower bound of the row's k-th largest
-// value; -inf when k > P or P > 256. One full warp; every lane gets it.
-__device__ __forceinline__ float seg_bound(const float2* pr, int P, int k, int lane) {
-  if (k > P || P > 256) return -INFINITY;
-  uint32_t key[8];
+// P segment maxima >= t: a lower bound of the row's k-th largest value; -inf
+// when k > P or P > 32 NV. sm[i] holds maximum lane + 32 i (i < NV). One
+// full warp; every lane gets it.
+template <int NV>
+__device__ __forceinline__ float seg_bound_regs(const float (&sm)[NV], int P, int k, int lane) {
+  if (k > P || P > 32 * NV) return -INFINITY;
+  uint32_t key[NV];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int c = lane + 32 * i;
-    key[i] = c < P ? Key<float>::of(__float_as_uint(__ldcg(pr + c).x)) : 0u;
-  }
+  for (int i = 0; i < NV; ++i) key[i] = lane + 32 * i < P ? Key<float>::of(__float_as_uint(sm[i])) : 0u;
   uint32_t prefix = 0;
 #pragma unroll 1
   for (int bit = 31; bit >= 16; --bit) {
     const uint32_t cand = prefix | (1u << bit);
     unsigned cnt = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cnt += key[i] >= cand ? 1u : 0u;
+    for (int i = 0; i < NV; ++i) cnt += key[i] >= cand ? 1u : 0u;
     if (__reduce_add_sync(0xffffffffu, cnt) >= static_cast<unsigned>(k)) prefix = cand;
   }
   return key_value<float>(prefix);
+}
+
+// The same from the stats partials pr[c] = (segment maximum, sum).
+template <int NV>
+__device__ __forceinline__ float seg_bound_n(const float2* pr, int P, int k, int lane) {
+  float sm[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + 32 * i;
+    sm[i] = c < P ? __ldcg(pr + c).x : -INFINITY;
+  }
+  return seg_bound_regs<NV>(sm, P, k, lane);
+}
+__device__ __forceinline__ float seg_bound(const float2* pr, int P, int k, int lane) {
+  if (k > P || P > 256) return -INFINITY;
+  if (P <= 64) return seg_bound_n<2>(pr, P, k, lane);
+  if (P <= 128) return seg_bound_n<4>(pr, P, k, lane);
+  return seg_bound_n<8>(pr, P, k, lane);
 }
 
 constexpr int kFiltCap = kCand / kSelWarps;  // entries per warp buffer
@@ -290,6 +307,66 @@ struct FiltSmem {
   uint32_t* sel;
   int* n;
 };
+
+// K = the k-th largest key over the valid slots e < NS of key[], idx[] (at
+// least k of them), by radix select with one shared histogram; the valid
+// entries with key >= K packed to the front of key[], idx[]. Returns their
+// count (ties included), *tau = K. Every thread of the CTA calls it.
+template <int KBITS, int NS, typename Valid>
+__device__ int select_slots(int k, const FiltSmem& sm, Valid valid, uint32_t* tau) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kPer = (NS + kSelThreads - 1) / kSelThreads;
+  uint32_t kr[kPer];
+  int ir[kPer];
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int e = tid + r * kSelThreads;
+    const bool ok = e < NS && valid(e);
+    kr[r] = ok ? sm.key[e] : 0u;
+    ir[r] = ok ? sm.idx[e] : -1;
+  }
+  uint32_t prefix = 0;
+  unsigned kk = static_cast<unsigned>(k);
+#pragma unroll 1
+  for (int shift = KBITS - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kSelThreads) sm.tot[i] = 0;
+    __syncthreads();
+    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+#pragma unroll
+    for (int r = 0; r < kPer; ++r)
+      if (ir[r] >= 0 && (kr[r] & hi_mask) == (prefix & hi_mask)) atomicAdd(sm.tot + ((kr[r] >> shift) & 0xFFu), 1u);
+    __syncthreads();
+    if (warp == 0) {
+      unsigned d, kn;
+      pick_digit(sm.tot, kk, lane, d, kn);
+      if (lane == 0) {
+        sm.sel[0] = d;
+        sm.sel[1] = kn;
+      }
+    }
+    __syncthreads();
+    prefix |= sm.sel[0] << shift;
+    kk = sm.sel[1];
+  }
+  if (tid == 0) *sm.n = 0;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const bool keep = ir[r] >= 0 && kr[r] >= prefix;
+    const unsigned bm = __ballot_sync(0xffffffffu, keep);
+    int base = 0;
+    if (lane == 0 && bm) base = atomicAdd(sm.n, __popc(bm));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (keep) {
+      const int p = base + __popc(bm & ((1u << lane) - 1u));
+      sm.key[p] = kr[r];
+      sm.idx[p] = ir[r];
+    }
+  }
+  __syncthreads();
+  *tau = prefix;
+  return *sm.n;
+}
 
 // The elements with key >= K, K the k-th largest key of the row (1 <= k <=
 // kFiltMaxK, k <= V; t0 <= the k-th largest value): their keys and indices
@@ -416,59 +493,49 @@ __device__ int filter_top(const Raw* row, int V, int k, float t0, const FiltSmem
 #pragma unroll
   for (int w = 0; w < kSelWarps; ++w) bad |= sm.cnt[w] < 0;
   if (bad) return -1;
-  // K over the union of the buffers: radix select, one shared histogram
-  constexpr int kPer = kCand / kSelThreads;
-  uint32_t kr[kPer];
-  int ir[kPer];
-#pragma unroll
-  for (int r = 0; r < kPer; ++r) {
-    const int e = tid + r * kSelThreads;
-    const bool ok = (e % kFiltCap) < sm.cnt[e / kFiltCap];
-    kr[r] = ok ? sm.key[e] : 0u;
-    ir[r] = ok ? sm.idx[e] : -1;
-  }
-  uint32_t prefix = 0;
-  unsigned kk = static_cast<unsigned>(k);
-#pragma unroll 1
-  for (int shift = KY::kBits - 8; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kSelThreads) sm.tot[i] = 0;
-    __syncthreads();
-    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
-#pragma unroll
-    for (int r = 0; r < kPer; ++r)
-      if (ir[r] >= 0 && (kr[r] & hi_mask) == (prefix & hi_mask)) atomicAdd(sm.tot + ((kr[r] >> shift) & 0xFFu), 1u);
-    __syncthreads();
-    if (warp == 0) {
-      unsigned d, kn;
-      pick_digit(sm.tot, kk, lane, d, kn);
-      if (lane == 0) {
-        sm.sel[0] = d;
-        sm.sel[1] = kn;
-      }
-    }
-    __syncthreads();
-    prefix |= sm.sel[0] << shift;
-    kk = sm.sel[1];
-  }
-  // the keys >= K, packed to the front
-  if (tid == 0) *sm.n = 0;
+  return select_slots<KY::kBits, kCand>(
+      k, sm, [&](int e) { return (e % kFiltCap) < sm.cnt[e / kFiltCap]; }, tau);
+}
+
+// A row's candidate list (the filter pass's per-segment sublists) gathered
+// into key[0, n), idx[0, n); returns n, or -1 when a sublist is incomplete
+// or n > kCandCap. Every thread of the CTA calls it (P <= kSelThreads).
+__device__ __forceinline__ int gather_list(const CandList& cl, long long row_id, const FiltSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int c = 0;
+  if (tid < cl.P) c = cl.cnt[row_id * cl.P + tid];
+  const int over = __syncthreads_or(c > cl.seg_cap);
+  if (over) return -1;
+  const int incl = warp_incl_scan(c, lane);
+  if (lane == 31) sm.cnt[warp] = incl;
   __syncthreads();
+  int before = incl - c, n = 0;
 #pragma unroll
-  for (int r = 0; r < kPer; ++r) {
-    const bool keep = ir[r] >= 0 && kr[r] >= prefix;
-    const unsigned bm = __ballot_sync(0xffffffffu, keep);
-    int base = 0;
-    if (lane == 0 && bm) base = atomicAdd(sm.n, __popc(bm));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (keep) {
-      const int p = base + __popc(bm & ((1u << lane) - 1u));
-      sm.key[p] = kr[r];
-      sm.idx[p] = ir[r];
+  for (int w = 0; w < kSelWarps; ++w) {
+    const int t = sm.cnt[w];
+    if (w < warp) before += t;
+    n += t;
+  }
+  __syncthreads();  // sm.cnt is reused by the caller
+  if (n > kCandCap) return -1;
+  if (c > 0) {
+    const long long sl = (row_id * cl.P + tid) * cl.seg_cap;
+    for (int i = 0; i < c; ++i) {
+      sm.key[before + i] = cl.key[sl + i];
+      sm.idx[before + i] = cl.idx[sl + i];
     }
   }
   __syncthreads();
-  *tau = prefix;
-  return *sm.n;
+  return n;
+}
+
+// The candidates of a per-row list (from the filter pass), n <= kCandCap
+// entries already in key[0, n), idx[0, n), n >= k: the entries with key >=
+// K, K their k-th largest key, packed to the front; returns their count,
+// *tau = K.
+template <typename Raw>
+__device__ int top_from_list(int n, int k, const FiltSmem& sm, uint32_t* tau) {
+  return select_slots<Key<Raw>::kBits, kCandCap>(k, sm, [&](int e) { return e < n; }, tau);
 }
 
 // Sum of float pairs over the block (every thread gets it); sh: kSelWarps pairs.
