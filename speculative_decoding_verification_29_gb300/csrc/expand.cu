@@ -36,11 +36,73 @@ __device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
   return a.v < b.v;
 }
 
+// ln Z of a row from its stats fold (log2 Z as a float pair, times ln 2).
+__device__ __forceinline__ float2 ln_of(float2 z) {
+  const float2 l2 = ds_log2(z);
+  const float ln2_hi = 0.693147182464599609375f, ln2_lo = -1.904654323148236e-09f;
+  return ds_add(ds_mul_f(l2, ln2_hi), make_float2(l2.x * ln2_lo, 0.f));
+}
+
+// log softmax(l / T) at a logit of value l: (l - M) / T - ln Z as a float
+// pair (l - M exact); -inf for a -inf logit.
+__device__ __forceinline__ float2 child_logp(float l, float M, float2 lz, float it_hi, float it_lo) {
+  const float2 d = ds_add(make_float2(l, 0.f), make_float2(-M, 0.f));
+  float2 lp = ds_mul_f(d, it_hi);
+  lp = ds_add(lp, make_float2(d.x * it_lo, 0.f));
+  lp = ds_add(lp, make_float2(-lz.x, -lz.y));
+  if (!(lp.x > -INFINITY)) lp = make_float2(-INFINITY, 0.f);
+  return lp;
+}
+
+template <typename Raw, int NR>
+__device__ void expand_sorted(const ExpArgs& a, int row_id, const uint64_t* buf, int n, float M, float2 lz,
+                              int lane) {
+  uint64_t r[NR];
+  warp_load_sort<NR>(buf, n, r, lane);
+  Cand* out = static_cast<Cand*>(a.cand) + static_cast<long long>(row_id) * a.M;
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int e = 32 * i + lane;
+    if (e < a.M) {  // a.M <= n here: the sorted list's first M entries
+      const float2 lp = child_logp(key_value<Raw>(comp_key(r[i])), M, lz, a.it_hi, a.it_lo);
+      out[e] = Cand{lp.x, lp.y, 0, comp_idx(r[i])};
+    }
+  }
+  if (lane == 0) a.row_flag[row_id] = 0;
+}
+
+// One warp selects a frontier row from its candidate list; false when the
+// row needs the whole CTA (no complete short list, or M >= V).
+template <typename Raw>
+__device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int lane) {
+  float2 z;
+  const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+  if (!(M == M) || !isfinite(M) || !(z.x > 0.f)) {  // no distribution at this node
+    Cand* out = static_cast<Cand*>(a.cand) + static_cast<long long>(row_id) * a.M;
+    for (int i = lane; i < a.M; i += 32) out[i] = Cand{NAN, 0.f, -1, -1};
+    if (lane == 0) a.row_flag[row_id] = SPEC_ROW_DRAFT;
+    return true;
+  }
+  if (a.M >= a.V || a.cl.seg_cap == 0) return false;
+  const int n = warp_gather(a.cl, row_id, buf, lane);
+  if (n < a.M) return false;  // incomplete or too long
+  const float2 lz = ln_of(z);
+  if (n <= 32)
+    expand_sorted<Raw, 1>(a, row_id, buf, n, M, lz, lane);
+  else if (n <= 64)
+    expand_sorted<Raw, 2>(a, row_id, buf, n, M, lz, lane);
+  else if (n <= 128)
+    expand_sorted<Raw, 4>(a, row_id, buf, n, M, lz, lane);
+  else
+    expand_sorted<Raw, 8>(a, row_id, buf, n, M, lz, lane);
+  return true;
+}
+
 template <typename Raw, bool VEC>
-__global__ void __launch_bounds__(kSelThreads, 5) expand_rows_kernel(ExpArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 4) expand_rows_kernel(ExpArgs a) {
   using KY = Key<Raw>;
-  const int row_id = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rows = a.B * a.F;
   __shared__ __align__(16) uint32_t s_buf[2 * kCand];
   unsigned* hist = s_buf;
   uint32_t* s_key = s_buf;
@@ -52,17 +114,28 @@ __global__ void __launch_bounds__(kSelThreads, 5) expand_rows_kernel(ExpArgs a) 
   __shared__ int s_n;
   __shared__ float s_M, s_t0;
   __shared__ float2 s_lz;
+  __shared__ int s_slow[kSelWarps];
   griddep_launch_dependents();
   griddep_wait();
+  {  // one warp per row with a short complete candidate list (s_buf: the warps' list buffers)
+    const int row_id = blockIdx.x * kSelWarps + warp;
+    static_assert(kSelWarps * kWarpList * 8 <= sizeof(uint32_t) * 2 * kCand, "list buffers fit");
+    const bool done =
+        row_id >= rows || expand_list_row<Raw>(a, row_id, reinterpret_cast<uint64_t*>(s_buf) + warp * kWarpList, lane);
+    if (lane == 0) s_slow[warp] = !done;
+  }
+  __syncthreads();
+  // the other rows, one at a time by the whole CTA
+  auto cta_row = [&](const int row_id) {
+  __syncthreads();  // shared memory is reused from the previous row
+  const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
   if (warp == 0) {
     float2 z;
     const float2* pr = a.part + static_cast<long long>(row_id) * a.P;
     const float M = fold_stats(pr, a.P, a.c_hi, a.c_lo, lane, &z);
     if (lane == 0) {
       s_M = M;
-      const float2 l2 = ds_log2(z);  // ln Z = log2 Z * ln 2, as a float pair
-      const float ln2_hi = 0.693147182464599609375f, ln2_lo = -1.904654323148236e-09f;
-      s_lz = ds_add(ds_mul_f(l2, ln2_hi), make_float2(l2.x * ln2_lo, 0.f));
+      s_lz = ln_of(z);
       if (!(M == M) || !isfinite(M) || !(z.x > 0.f)) s_M = NAN;
     }
   }
@@ -154,11 +227,7 @@ __global__ void __launch_bounds__(kSelThreads, 5) expand_rows_kernel(ExpArgs a) 
           bits = static_cast<uint32_t>(row[v]);
         else
           bits = __float_as_uint(row[v]);
-        const float2 d = ds_add(make_float2(KY::val(bits), 0.f), make_float2(-M, 0.f));  // exact
-        float2 lp = ds_mul_f(d, a.it_hi);
-        lp = ds_add(lp, make_float2(d.x * a.it_lo, 0.f));
-        lp = ds_add(lp, make_float2(-lz.x, -lz.y));
-        if (!(lp.x > -INFINITY)) lp = make_float2(-INFINITY, 0.f);  // a -inf logit: probability 0
+        const float2 lp = child_logp(KY::val(bits), M, lz, a.it_hi, a.it_lo);
         out[i] = Cand{lp.x, lp.y, 0, v};
       } else {
         out[i] = Cand{-INFINITY, 0.f, 0, -1};  // fewer tokens than M in the vocabulary
@@ -168,6 +237,9 @@ __global__ void __launch_bounds__(kSelThreads, 5) expand_rows_kernel(ExpArgs a) 
   if (st)
     for (int i = tid; i < Mk; i += kSelThreads) out[i] = Cand{NAN, 0.f, -1, -1};
   if (tid == 0) a.row_flag[row_id] = st;
+  };
+  for (int w = 0; w < kSelWarps; ++w)
+    if (s_slow[w]) cta_row(blockIdx.x * kSelWarps + w);
 }
 
 constexpr int kMergeT = 256;
@@ -242,7 +314,7 @@ int expand_limits(int* max_m, int* max_fm) {
 }
 
 cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st) {
-  const dim3 g1(static_cast<unsigned>(static_cast<long long>(a.B) * a.F));
+  const dim3 g1(static_cast<unsigned>((static_cast<long long>(a.B) * a.F + kSelWarps - 1) / kSelWarps));
   cudaError_t e;
   if (dtype == SPEC_BF16)
     e = vec ? launch_pdl(expand_rows_kernel<uint16_t, true>, g1, dim3(kSelThreads), st, a)

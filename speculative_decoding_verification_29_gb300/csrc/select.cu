@@ -10,7 +10,11 @@
 // top_p). Both keep a set {v : key(l_v) >= tau}, key the order-preserving
 // unsigned image of the logit's bits.
 //
-// One CTA per row, after the stats pass (its partials give M and Z):
+// After the stats pass (its partials give M and Z). A row whose top-k
+// candidate list (from the filter pass) is complete and short is selected
+// by one warp: the list sorted in registers, the top-k threshold its k-th
+// entry, then the top-p scan and the kept mass by shuffles. Every other row
+// is selected by a whole CTA:
 //   top-k: the k largest keys (ties included) and their weights come from
 //          the candidate filter pass's list of the row when it ran (k up to
 //          the number of stats segments) and the list is complete; else, for
@@ -56,14 +60,118 @@ __device__ float2 kept_mass(const Raw* row, int V, uint32_t tau, W weight, float
   return block_sum_ds(ds_add(z, make_float2(acc, 0.f)), sh);
 }
 
+// The row's record from its sorted candidate list (one warp): the top-k
+// threshold K is the k-th entry, the kept-by-top-k set the entries >= K;
+// top-p keeps the groups up to the last entry whose preceding kept mass is
+// below top_p of theirs.
+template <typename Raw, int NR>
+__device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf, int n, float M, int lane) {
+  uint64_t r[NR];
+  warp_load_sort<NR>(buf, n, r, lane);
+  const uint32_t K = comp_key(warp_entry<NR>(r, a.top_k - 1));
+  float w[NR];
+  bool ink[NR];
+  float2 zk = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const uint32_t key = comp_key(r[i]);
+    ink[i] = 32 * i + lane < n && key >= K;
+    float ww = 0.f;
+    if (ink[i]) {
+      const float d = key_value<Raw>(key) - M;
+      ww = ex2_fast(fmaf(d, a.c_hi, d * a.c_lo));
+    }
+    w[i] = ww;
+    zk = ds_add(zk, make_float2(ww, 0.f));
+  }
+  const float2 Zk = warp_sum_ds(zk);
+  uint32_t tau = K;
+  int st = 0;
+  if (a.top_p < 1.f) {
+    const float2 target = ds_mul_f(Zk, a.top_p);
+    float2 run = make_float2(0.f, 0.f);  // mass of the registers before
+    int last = -1;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      float2 inc = make_float2(w[i], 0.f);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float2 y = make_float2(__shfl_up_sync(0xffffffffu, inc.x, o), __shfl_up_sync(0xffffffffu, inc.y, o));
+        if (lane >= o) inc = ds_add(y, inc);
+      }
+      float2 ex = make_float2(__shfl_up_sync(0xffffffffu, inc.x, 1), __shfl_up_sync(0xffffffffu, inc.y, 1));
+      if (lane == 0) ex = make_float2(0.f, 0.f);
+      if (ink[i] && ds_gt(target, ds_add(run, ex))) last = 32 * i + lane;
+      run = ds_add(run, make_float2(__shfl_sync(0xffffffffu, inc.x, 31), __shfl_sync(0xffffffffu, inc.y, 31)));
+    }
+    const int L = __reduce_max_sync(0xffffffffu, last);
+    if (L < 0) {
+      st = SPEC_ROW_WARP;
+    } else {
+      const uint32_t kl = comp_key(warp_entry<NR>(r, L));
+      if (kl > tau) tau = kl;
+    }
+  }
+  float2 kept = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < NR; ++i)
+    if (ink[i] && comp_key(r[i]) >= tau) kept = ds_add(kept, make_float2(w[i], 0.f));
+  const float2 Zp = warp_sum_ds(kept);
+  if (lane == 0) {
+    StatRec out;
+    out.M = M;
+    out.Z = NAN;
+    out.Lhi = out.Llo = NAN;
+    if (st == 0) {
+      const float2 L2 = ds_log2(Zp);
+      out.Z = Zp.x;
+      out.Lhi = L2.x;
+      out.Llo = L2.y;
+    }
+    a.rec[row_id] = out;
+    a.vtau[row_id] = key_value<Raw>(tau);
+    a.row_flag[row_id] = st;
+  }
+}
+
+// One warp selects a row from its candidate list; false when the row needs
+// the whole CTA (no top-k, no complete short list).
+template <typename Raw>
+__device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int lane) {
+  float2 z;
+  const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+  if (!(M == M && isfinite(M) && z.x > 0.f)) {  // a flagged row: the record carries M only
+    if (lane == 0) {
+      StatRec out;
+      out.M = M;
+      out.Z = NAN;
+      out.Lhi = out.Llo = NAN;
+      a.rec[row_id] = out;
+      a.vtau[row_id] = key_value<Raw>(0u);
+      a.row_flag[row_id] = 0;
+    }
+    return true;
+  }
+  if (!(a.top_k > 0 && a.top_k < a.V) || a.cl.seg_cap == 0) return false;
+  const int n = warp_gather(a.cl, row_id, buf, lane);
+  if (n < a.top_k) return false;  // incomplete or too long
+  if (n <= 32)
+    warped_sorted<Raw, 1>(a, row_id, buf, n, M, lane);
+  else if (n <= 64)
+    warped_sorted<Raw, 2>(a, row_id, buf, n, M, lane);
+  else if (n <= 128)
+    warped_sorted<Raw, 4>(a, row_id, buf, n, M, lane);
+  else
+    warped_sorted<Raw, 8>(a, row_id, buf, n, M, lane);
+  return true;
+}
+
 template <typename Raw, bool VEC>
 __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) {
   using KY = Key<Raw>;
-  const int row_id = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int RPG = a.TR + a.DR;
-  const int b = row_id / RPG, j = row_id - b * RPG;
-  const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
-                            : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
+  const int rows = a.B * RPG;
   // shared memory: the radix histograms, later reused for the candidates
   __shared__ __align__(16) uint32_t s_buf[2 * kCand];
   unsigned* hist = s_buf;                                    // kSelWarps x 256 counters
@@ -78,7 +186,22 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
   __shared__ int s_n, s_last;
   __shared__ float s_M, s_t0;
   __shared__ float2 s_Z;
+  __shared__ int s_slow[kSelWarps];
   griddep_wait();
+  {  // one warp per row with a short complete candidate list (s_buf: the warps' list buffers)
+    const int row_id = blockIdx.x * kSelWarps + warp;
+    static_assert(kSelWarps * kWarpList * 8 <= sizeof(uint32_t) * 2 * kCand, "list buffers fit");
+    const bool done =
+        row_id >= rows || warped_list_row<Raw>(a, row_id, reinterpret_cast<uint64_t*>(s_buf) + warp * kWarpList, lane);
+    if (lane == 0) s_slow[warp] = !done;
+  }
+  __syncthreads();
+  // the other rows, one at a time by the whole CTA
+  auto cta_row = [&](const int row_id) {
+  __syncthreads();  // shared memory is reused from the previous row
+  const int b = row_id / RPG, j = row_id - b * RPG;
+  const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
+                            : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
   if (warp == 0) {  // M and Z of the row from the stats partials, and a lower bound of the k-th largest logit
     float2 z;
     const float2* pr = a.part + static_cast<long long>(row_id) * a.P;
@@ -256,14 +379,17 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
       out.Llo = L2.y;
     }
   }
-  // the trigger comes late: the tail's clusters would otherwise hold SM slots,
-  // idle, while rows are still being selected
-  griddep_launch_dependents();
   if (tid == 0) {
     a.rec[row_id] = out;
     a.vtau[row_id] = key_value<Raw>(tau);
     a.row_flag[row_id] = st;
   }
+  };
+  for (int w = 0; w < kSelWarps; ++w)
+    if (s_slow[w]) cta_row(blockIdx.x * kSelWarps + w);
+  // the trigger comes late: the tail's clusters would otherwise hold SM slots,
+  // idle, while rows are still being selected
+  griddep_launch_dependents();
 }
 
 }  // namespace
@@ -271,7 +397,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
 int select_candidates() { return kCand; }
 
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>(static_cast<long long>(a.B) * (a.TR + a.DR))), block(kSelThreads);
+  const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * (a.TR + a.DR) + kSelWarps - 1) / kSelWarps)),
+      block(kSelThreads);
   if (dtype == SPEC_BF16)
     return vec ? launch_pdl(warp_select_kernel<uint16_t, true>, grid, block, st, a)
                : launch_pdl(warp_select_kernel<uint16_t, false>, grid, block, st, a);

@@ -538,6 +538,137 @@ __device__ int top_from_list(int n, int k, const FiltSmem& sm, uint32_t* tau) {
   return select_slots<Key<Raw>::kBits, kCandCap>(k, sm, [&](int e) { return e < n; }, tau);
 }
 
+// ------------------------------------------------ one warp per listed row --
+//
+// A row whose candidate list is complete and short (at most kWarpList
+// entries) is selected by one warp, with no block barrier: the list is
+// gathered into the warp's shared buffer, sorted in registers (bitonic
+// network over 32 x NR entries: exchanges across lanes by shuffles, across a
+// lane's registers in place) by a 64-bit composite, key high and inverted
+// token id low (key descending, then token id ascending).
+
+constexpr int kWarpList = 256;  // entries one warp sorts (8 per lane)
+
+__device__ __forceinline__ uint64_t list_comp(uint32_t key, int idx) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint64_t>(~static_cast<uint32_t>(idx));
+}
+__device__ __forceinline__ uint32_t comp_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
+__device__ __forceinline__ int comp_idx(uint64_t c) { return static_cast<int>(~static_cast<uint32_t>(c)); }
+
+// The row's list as composites in buf[0, n) (buf: kWarpList entries private
+// to the warp); returns n, or -1 when a sublist is incomplete or n >
+// kWarpList. One full warp (P <= 256).
+__device__ __forceinline__ int warp_gather(const CandList& cl, long long row_id, uint64_t* buf, int lane) {
+  const int spl = (cl.P + 31) >> 5;  // segments per lane, contiguous
+  const int s0 = lane * spl;
+  int mine = 0;
+  bool over = false;
+  for (int i = 0; i < spl; ++i) {
+    const int sgi = s0 + i;
+    const int c = sgi < cl.P ? cl.cnt[row_id * cl.P + sgi] : 0;
+    over |= c > cl.seg_cap;
+    mine += c;
+  }
+  if (__any_sync(0xffffffffu, over)) return -1;
+  const int incl = warp_incl_scan(mine, lane);
+  const int n = __shfl_sync(0xffffffffu, incl, 31);
+  if (n > kWarpList) return -1;
+  int pos = incl - mine;
+  for (int i = 0; i < spl; ++i) {
+    const int sgi = s0 + i;
+    const int c = sgi < cl.P ? cl.cnt[row_id * cl.P + sgi] : 0;
+    const long long sl = (row_id * cl.P + sgi) * cl.seg_cap;
+    for (int e = 0; e < c; ++e) buf[pos++] = list_comp(cl.key[sl + e], cl.idx[sl + e]);
+  }
+  __syncwarp();
+  return n;
+}
+
+// One bitonic stage across lanes (stride < 32) over all NR registers.
+template <int NR>
+__device__ __forceinline__ void warp_stage_lanes(uint64_t (&r)[NR], int lane, int size, int stride) {
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int e = 32 * i + lane;
+    const bool desc = (e & size) == 0;  // this block's direction
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, r[i], stride);
+    const bool keep_max = ((lane & stride) == 0) == desc;
+    r[i] = keep_max ? (r[i] > o ? r[i] : o) : (r[i] < o ? r[i] : o);
+  }
+}
+
+// One bitonic stage within each lane (stride S >= 32: registers i, i ^ S/32).
+template <int NR, int S>
+__device__ __forceinline__ void warp_stage_regs(uint64_t (&r)[NR], int lane, int size) {
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    constexpr int d = S >> 5;
+    const int pi = i ^ d;
+    if (pi > i) {  // r[i] holds the lower index of the pair
+      const bool desc = ((32 * i + lane) & size) == 0;
+      const uint64_t lo = r[i], hi = r[pi];
+      const bool swap = desc ? lo < hi : lo > hi;
+      r[i] = swap ? hi : lo;
+      r[pi] = swap ? lo : hi;
+    }
+  }
+}
+
+// Sorts 32 NR composites descending: entry e = 32 i + lane lives in r[i].
+// Sizes and lane strides run as loops (the code stays small: it is fetched
+// cold by every SM), the in-lane strides are unrolled.
+template <int NR>
+__device__ __forceinline__ void warp_sort_desc(uint64_t (&r)[NR], int lane) {
+  constexpr int N = 32 * NR;
+#pragma unroll 1
+  for (int size = 2; size <= N; size <<= 1) {
+    if constexpr (NR >= 8) {
+      if (size >= 256) warp_stage_regs<NR, 128>(r, lane, size);
+    }
+    if constexpr (NR >= 4) {
+      if (size >= 128) warp_stage_regs<NR, 64>(r, lane, size);
+    }
+    if constexpr (NR >= 2) {
+      if (size >= 64) warp_stage_regs<NR, 32>(r, lane, size);
+    }
+#pragma unroll 1
+    for (int stride = (size >> 1) < 16 ? (size >> 1) : 16; stride > 0; stride >>= 1)
+      warp_stage_lanes<NR>(r, lane, size, stride);
+  }
+}
+
+// Loads n <= 32 NR composites of buf into r (entry e = 32 i + lane; 0
+// pads: below every composite of a listed element) and sorts them.
+template <int NR>
+__device__ __forceinline__ void warp_load_sort(const uint64_t* buf, int n, uint64_t (&r)[NR], int lane) {
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int e = 32 * i + lane;
+    r[i] = e < n ? buf[e] : 0ull;
+  }
+  warp_sort_desc<NR>(r, lane);
+}
+
+// Entry e of a sorted register set, for every lane.
+template <int NR>
+__device__ __forceinline__ uint64_t warp_entry(const uint64_t (&r)[NR], int e) {
+  uint64_t v = 0;
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const uint64_t x = __shfl_sync(0xffffffffu, r[i], e & 31);
+    if ((e >> 5) == i) v = x;
+  }
+  return v;
+}
+
+// Sum of float pairs over a warp (every lane gets it).
+__device__ __forceinline__ float2 warp_sum_ds(float2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    v = ds_add(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o)));
+  return v;
+}
+
 // Sum of float pairs over the block (every thread gets it); sh: kSelWarps pairs.
 __device__ __forceinline__ float2 block_sum_ds(float2 v, float2* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

@@ -116,6 +116,15 @@ def test_expand_segment_bound_and_fallback():
         compare(*run(Ld, logc, M), M, 1.0)
 
 
+@pytest.mark.parametrize("M", [1, 31, 40, 63])
+def test_expand_list_sizes(M):
+    """M up to the 63 stats segments of a 128256-token bf16 row: candidate
+    lists of a few to a few hundred entries, selected by one warp when they
+    hold at most 256, else by the whole CTA."""
+    Ld, logc = gen.expand_frontier(2, 4, 128256, torch.bfloat16, seed=M)
+    compare(*run(Ld, logc, M), M, 1.0)
+
+
 def test_expand_more_slots_than_children():
     """M >= V and M > F * V: every child is kept, the remaining slots are
     -1 / NaN."""
