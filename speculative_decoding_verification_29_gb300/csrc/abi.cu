@@ -44,7 +44,7 @@ char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 // size depends only on the shapes, never on pointer alignment; then, for the
 // sampling settings, one record, threshold and flag per row.
 struct Layout {
-  size_t part, rec, vtau, flag, cnt, ckey, cidx, total;
+  size_t part, rec, vtau, flag, bound, cnt, ckey, cidx, total;
 };
 
 // lists adds the top-k candidate lists: per row and stats segment a count
@@ -63,8 +63,10 @@ Layout layout(int B, int TR, int DR, int V, int dtype, bool lists = false) {
   off += up256(static_cast<size_t>(nrows) * sizeof(float));
   L.flag = off;
   off += up256(static_cast<size_t>(nrows) * sizeof(int32_t));
-  L.cnt = L.ckey = L.cidx = off;
+  L.cnt = L.ckey = L.cidx = L.bound = off;
   if (lists) {
+    off += up256(static_cast<size_t>(nrows) * sizeof(float));
+    L.cnt = off;
     off += up256(static_cast<size_t>(nrows * P) * sizeof(int32_t));
     L.ckey = off;
     off += up256(static_cast<size_t>(nrows * P) * kCandSeg * sizeof(uint32_t));
@@ -82,6 +84,7 @@ CandList cand_list(void* ws, const Layout& L, int P) {
   cl.cnt = reinterpret_cast<int32_t*>(at(ws, L.cnt));
   cl.key = reinterpret_cast<uint32_t*>(at(ws, L.ckey));
   cl.idx = reinterpret_cast<int32_t*>(at(ws, L.cidx));
+  cl.bound = reinterpret_cast<float*>(at(ws, L.bound));
   return cl;
 }
 
@@ -470,7 +473,8 @@ size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype) {
   const long long rows = static_cast<long long>(B) * F;
   const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
   return up256(static_cast<size_t>(rows * P) * sizeof(float2)) + up256(static_cast<size_t>(rows * M) * 16) +
-         up256(static_cast<size_t>(rows) * sizeof(int32_t)) + up256(static_cast<size_t>(rows * P) * sizeof(int32_t)) +
+         up256(static_cast<size_t>(rows) * sizeof(int32_t)) + up256(static_cast<size_t>(rows) * sizeof(float)) +
+         up256(static_cast<size_t>(rows * P) * sizeof(int32_t)) +
          2 * up256(static_cast<size_t>(rows * P) * kCandSeg * sizeof(uint32_t));
 }
 
@@ -507,6 +511,8 @@ int spec_tree_expand(const void* draft_logits, int dtype, float temperature, con
   if (take < V && cand_pass_fits(take, a.P)) {
     cl.seg_cap = kCandSeg;
     cl.P = a.P;
+    cl.bound = reinterpret_cast<float*>(at(workspace, loff));
+    loff += up256(static_cast<size_t>(rows) * sizeof(float));
     cl.cnt = reinterpret_cast<int32_t*>(at(workspace, loff));
     loff += up256(static_cast<size_t>(rows * Pmax) * sizeof(int32_t));
     cl.key = reinterpret_cast<uint32_t*>(at(workspace, loff));

@@ -1,11 +1,11 @@
 // cand.cu -- the candidate filter pass of a top-k over logit rows.
 //
-// Runs after the stats pass, on the same grid: one warp per segment of a
-// row, every load of the segment in flight at once. Each warp forms the
-// row's bound t0 from the stats partials (if k segment maxima are >= t, k
-// elements of the row are >= t, so the k-th largest segment maximum is a
-// lower bound of the k-th largest logit) while its loads are in flight, and
-// writes every element >= t0 of its segment, as (order-preserving key, token
+// Runs after the stats pass. A small kernel first forms each row's bound t0
+// from the stats partials, one warp per row (if k segment maxima are >= t,
+// k elements of the row are >= t, so the k-th largest segment maximum is a
+// lower bound of the k-th largest logit). Then the pass proper, on the stats
+// pass's grid: one warp per segment of a row, every load of the segment in
+// flight at once together with the row's bound; each warp writes every element >= t0 of its segment, as (order-preserving key, token
 // id), to the segment's own slots of the row's candidate list, and their
 // count (no atomics, so no warp waits on a returned slot). The k largest
 // elements of a row usually lie in k different segments, and then t0 is the
@@ -21,14 +21,26 @@ namespace {
 
 using namespace sel;
 
+// The rows' bounds, one warp per row, before the filter pass (so that no
+// warp of the pass waits on it).
+__global__ void __launch_bounds__(kScanThreads) cand_bound_kernel(CandArgs a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  griddep_wait();  // the partials come from the stats pass
+  const long long row_id = static_cast<long long>(blockIdx.x) * kScanWarps + warp;
+  if (row_id >= static_cast<long long>(a.B) * (a.TR + a.DR)) return;
+  const float t = seg_bound(a.part + row_id * a.P, a.P, a.k, lane);
+  if (lane == 0) a.cl.bound[row_id] = t;
+}
+
 template <typename Raw, bool VEC>
 __global__ void __launch_bounds__(kScanThreads, VEC ? 4 : 2) cand_filter_kernel(CandArgs a) {
   using KY = Key<Raw>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // no early trigger: the selection that follows would hold SM slots, idle,
   // while this pass still streams
-  griddep_wait();  // the partials come from the stats pass
-  const int seg = blockIdx.x * kScanWarps + warp;  // past the row's end (grid rounding): loads nothing
+  griddep_wait();  // the bounds come from the bound pass
+  const int seg = blockIdx.x * kScanWarps + warp;
+  if (seg >= a.P) return;  // grid rounding (whole warp)
   const int b = blockIdx.y, j = blockIdx.z;
   const long long row_id = static_cast<long long>(b) * (a.TR + a.DR) + j;
   const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
@@ -37,7 +49,7 @@ __global__ void __launch_bounds__(kScanThreads, VEC ? 4 : 2) cand_filter_kernel(
   constexpr int NL = VEC ? kSegChunks * kWV : kScalarPerLane;  // loads per lane
   const int nunits = VEC ? a.V / E : a.V;
   const int u0 = seg * (NL * 32) + lane;
-  __shared__ float s_t0;
+  const float t0 = __ldcg(a.cl.bound + row_id);
   uint4 q[VEC ? NL : 1];
   float s1[VEC ? 1 : NL];
 #pragma unroll
@@ -48,13 +60,6 @@ __global__ void __launch_bounds__(kScanThreads, VEC ? 4 : 2) cand_filter_kernel(
     else
       s1[t] = u < nunits ? Elem<Raw>::at(row, u) : -INFINITY;
   }
-  // the bound, once per CTA (its warps share the row) while the loads fly
-  if (warp == 0) {
-    const float t = seg_bound(a.part + row_id * a.P, a.P, a.k, lane);
-    if (lane == 0) s_t0 = t;
-  }
-  __syncthreads();
-  const float t0 = s_t0;
   // which loads hold an element >= t0 (one compare per load); the elements
   // >= t0 of those (rare) loads are appended by one copy of that code, not
   // one per load
@@ -131,6 +136,10 @@ __global__ void __launch_bounds__(kScanThreads, VEC ? 4 : 2) cand_filter_kernel(
 }  // namespace
 
 cudaError_t launch_cand_filter(const CandArgs& a, int dtype, bool vec, cudaStream_t st) {
+  const long long rows = static_cast<long long>(a.B) * (a.TR + a.DR);
+  cudaError_t e = launch_pdl(cand_bound_kernel, dim3(static_cast<unsigned>((rows + kScanWarps - 1) / kScanWarps)),
+                             dim3(kScanThreads), st, a);
+  if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((a.P + kScanWarps - 1) / kScanWarps), static_cast<unsigned>(a.B),
                   static_cast<unsigned>(a.TR + a.DR));
   if (dtype == SPEC_BF16)

@@ -73,6 +73,7 @@ struct CandList {
   int32_t* cnt;    // [rows][P] elements at or above the bound (> seg_cap: that sublist is incomplete)
   uint32_t* key;   // [rows][P][seg_cap] order-preserving keys
   int32_t* idx;    // [rows][P][seg_cap] token ids
+  float* bound;    // [rows] the filter's threshold: a lower bound of the k-th largest logit
 };
 constexpr int kCandSeg = 16;   // entries per segment
 constexpr int kCandCap = 512;  // entries per row a selection gathers
