@@ -72,19 +72,22 @@ __device__ void expand_sorted(const ExpArgs& a, int row_id, const uint64_t* buf,
 }
 
 // One warp selects a frontier row from its candidate list; false when the
-// row needs the whole CTA (no complete short list, or M >= V).
-template <typename Raw>
-__device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int lane) {
+// row needs the whole CTA (no complete short list, or M >= V). P <= 32 NV.
+template <typename Raw, int NV>
+__device__ bool expand_list_row_n(const ExpArgs& a, int row_id, uint64_t* buf, int lane) {
+  float2 q[NV];
+  int c[NV];
+  row_load<NV>(a.part + static_cast<long long>(row_id) * a.P, a.P, a.cl, row_id, lane, q, c);
   float2 z;
-  const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+  const float M = fold_regs<NV>(q, a.c_hi, a.c_lo, &z);
   if (!(M == M) || !isfinite(M) || !(z.x > 0.f)) {  // no distribution at this node
     Cand* out = static_cast<Cand*>(a.cand) + static_cast<long long>(row_id) * a.M;
     for (int i = lane; i < a.M; i += 32) out[i] = Cand{NAN, 0.f, -1, -1};
     if (lane == 0) a.row_flag[row_id] = SPEC_ROW_DRAFT;
     return true;
   }
-  if (a.M >= a.V || a.cl.seg_cap == 0) return false;
-  const int n = warp_gather(a.cl, row_id, buf, lane);
+  if (a.M >= a.V) return false;
+  const int n = gather_regs<NV>(a.cl, row_id, a.P, c, buf, lane);
   if (n < a.M) return false;  // incomplete or too long
   const float2 lz = ln_of(z);
   if (n <= 32)
@@ -98,11 +101,79 @@ __device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int
   return true;
 }
 
+template <typename Raw>
+__device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int lane) {
+  if (a.cl.seg_cap == 0 || a.P > 256) return false;  // no lists: the CTA selects every row
+  return expand_list_row_n<Raw, 8>(a, row_id, buf, lane);  // one instantiation: the code is fetched cold by every SM
+}
+
+constexpr int kMergeCap = 2048;  // F x M candidates held in shared memory (32 KB)
+
+// Tree b's F x M candidates, scored and ranked: higher score, then lower
+// node, then lower token; the first M kept. s_c: kMergeCap entries.
+__device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
+  const int tid = threadIdx.x;
+  const int F = a.F, Mk = a.M, n = F * Mk;
+  if (tid == 0) *s_st = 0;
+  __syncthreads();
+  for (int f = tid; f < F; f += kSelThreads) {
+    const float lc = a.logc[static_cast<long long>(b) * F + f];
+    const int fl = a.row_flag[static_cast<long long>(b) * F + f] | ((lc != lc || lc == INFINITY) ? SPEC_ROW_DRAFT : 0);
+    if (fl) atomicOr(s_st, fl);
+  }
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  for (int i = tid; i < n2; i += kSelThreads) {
+    Cand c{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
+    if (i < n) {
+      const int f = i / Mk;
+      c = static_cast<const Cand*>(a.cand)[static_cast<long long>(b) * n + i];
+      c.f = f;
+      const float2 sc = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
+      c.hi = sc.x > -INFINITY ? sc.x : -INFINITY;
+      c.lo = sc.x > -INFINITY ? sc.y : 0.f;
+      if (c.v < 0) c = Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};  // a slot past the vocabulary
+    }
+    s_c[i] = c;
+  }
+  __syncthreads();
+  const int st = *s_st;
+#pragma unroll 1
+  for (int size = 2; size <= n2; size <<= 1)
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n2; i += kSelThreads) {
+        const int pj = i ^ stride;
+        if (pj > i) {
+          const bool first = (i & size) == 0;
+          const Cand ci = s_c[i], cj = s_c[pj];
+          const bool i_before = cand_before(ci, cj);
+          if (first ? !i_before : i_before) {
+            s_c[i] = cj;
+            s_c[pj] = ci;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  for (int i = tid; i < Mk; i += kSelThreads) {
+    const long long o = static_cast<long long>(b) * Mk + i;
+    const Cand c = s_c[i];
+    const bool ok = !st && c.v != 0x7fffffff;
+    a.parent[o] = ok ? c.f : -1;
+    a.token[o] = ok ? c.v : -1;
+    a.score[o] = ok ? c.hi + c.lo : NAN;
+  }
+  if (tid == 0) a.row_status[b] = st;
+}
+
+// One CTA per tree: its frontier rows eight at a time (one warp each, or the
+// whole CTA for a row without a short complete list), then the merge.
 template <typename Raw, bool VEC>
-__global__ void __launch_bounds__(kSelThreads, 4) expand_rows_kernel(ExpArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 2) expand_tree_kernel(ExpArgs a) {
   using KY = Key<Raw>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rows = a.B * a.F;
+  const int b = blockIdx.x;
   __shared__ __align__(16) uint32_t s_buf[2 * kCand];
   unsigned* hist = s_buf;
   uint32_t* s_key = s_buf;
@@ -115,17 +186,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) expand_rows_kernel(ExpArgs a) 
   __shared__ float s_M, s_t0;
   __shared__ float2 s_lz;
   __shared__ int s_slow[kSelWarps];
+  __shared__ int s_st;
   griddep_launch_dependents();
   griddep_wait();
-  {  // one warp per row with a short complete candidate list (s_buf: the warps' list buffers)
-    const int row_id = blockIdx.x * kSelWarps + warp;
-    static_assert(kSelWarps * kWarpList * 8 <= sizeof(uint32_t) * 2 * kCand, "list buffers fit");
-    const bool done =
-        row_id >= rows || expand_list_row<Raw>(a, row_id, reinterpret_cast<uint64_t*>(s_buf) + warp * kWarpList, lane);
-    if (lane == 0) s_slow[warp] = !done;
-  }
-  __syncthreads();
-  // the other rows, one at a time by the whole CTA
+  // a row by the whole CTA
   auto cta_row = [&](const int row_id) {
   __syncthreads();  // shared memory is reused from the previous row
   const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
@@ -238,71 +302,22 @@ __global__ void __launch_bounds__(kSelThreads, 4) expand_rows_kernel(ExpArgs a) 
     for (int i = tid; i < Mk; i += kSelThreads) out[i] = Cand{NAN, 0.f, -1, -1};
   if (tid == 0) a.row_flag[row_id] = st;
   };
-  for (int w = 0; w < kSelWarps; ++w)
-    if (s_slow[w]) cta_row(blockIdx.x * kSelWarps + w);
-}
-
-constexpr int kMergeT = 256;
-constexpr int kMergeCap = 2048;  // F x M candidates held in shared memory (32 KB)
-
-// One CTA per batch row: the F x M candidates, scored and ranked.
-__global__ void __launch_bounds__(kMergeT) expand_merge_kernel(ExpArgs a) {
-  const int b = blockIdx.x, tid = threadIdx.x;
-  const int F = a.F, Mk = a.M, n = F * Mk;
-  __shared__ Cand s_c[kMergeCap];
-  __shared__ int s_st;
-  if (tid == 0) s_st = 0;
-  griddep_launch_dependents();
-  griddep_wait();
-  __syncthreads();
-  for (int f = tid; f < F; f += kMergeT) {
-    const float lc = a.logc[static_cast<long long>(b) * F + f];
-    const int fl = a.row_flag[static_cast<long long>(b) * F + f] | ((lc != lc || lc == INFINITY) ? SPEC_ROW_DRAFT : 0);
-    if (fl) atomicOr(&s_st, fl);
-  }
-  __syncthreads();
-  const int st = s_st;
-  int n2 = 1;
-  while (n2 < n) n2 <<= 1;
-  for (int i = tid; i < n2; i += kMergeT) {
-    Cand c{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
-    if (i < n) {
-      const int f = i / Mk;
-      c = static_cast<const Cand*>(a.cand)[static_cast<long long>(b) * n + i];
-      c.f = f;
-      const float2 s = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
-      c.hi = s.x > -INFINITY ? s.x : -INFINITY;
-      c.lo = s.x > -INFINITY ? s.y : 0.f;
-      if (c.v < 0) c = Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};  // a slot past the vocabulary
+  static_assert(kSelWarps * kWarpList * 8 <= sizeof(uint32_t) * 2 * kCand, "list buffers fit");
+  static_assert(kMergeCap * sizeof(Cand) <= sizeof(uint32_t) * 2 * kCand, "merge buffer fits");
+  for (int r0 = 0; r0 < a.F; r0 += kSelWarps) {
+    {  // one warp per row with a short complete candidate list (s_buf: the warps' list buffers)
+      const int r = r0 + warp;
+      const bool done =
+          r >= a.F ||
+          expand_list_row<Raw>(a, b * a.F + r, reinterpret_cast<uint64_t*>(s_buf) + warp * kWarpList, lane);
+      if (lane == 0) s_slow[warp] = !done;
     }
-    s_c[i] = c;
+    __syncthreads();
+    for (int w = 0; w < kSelWarps; ++w)
+      if (s_slow[w]) cta_row(b * a.F + r0 + w);
+    __syncthreads();
   }
-  __syncthreads();
-  for (int size = 2; size <= n2; size <<= 1)
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < n2; i += kMergeT) {
-        const int pj = i ^ stride;
-        if (pj > i) {
-          const bool first = (i & size) == 0;
-          const Cand ci = s_c[i], cj = s_c[pj];
-          const bool i_before = cand_before(ci, cj);
-          if (first ? !i_before : i_before) {
-            s_c[i] = cj;
-            s_c[pj] = ci;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  for (int i = tid; i < Mk; i += kMergeT) {
-    const long long o = static_cast<long long>(b) * Mk + i;
-    const Cand c = s_c[i];
-    const bool ok = !st && c.v != 0x7fffffff;
-    a.parent[o] = ok ? c.f : -1;
-    a.token[o] = ok ? c.v : -1;
-    a.score[o] = ok ? c.hi + c.lo : NAN;
-  }
-  if (tid == 0) a.row_status[b] = st;
+  merge_tree(a, b, reinterpret_cast<Cand*>(s_buf), &s_st);  // the rows' candidates are visible after the barrier
 }
 
 }  // namespace
@@ -314,16 +329,12 @@ int expand_limits(int* max_m, int* max_fm) {
 }
 
 cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st) {
-  const dim3 g1(static_cast<unsigned>((static_cast<long long>(a.B) * a.F + kSelWarps - 1) / kSelWarps));
-  cudaError_t e;
+  const dim3 g(static_cast<unsigned>(a.B));
   if (dtype == SPEC_BF16)
-    e = vec ? launch_pdl(expand_rows_kernel<uint16_t, true>, g1, dim3(kSelThreads), st, a)
-            : launch_pdl(expand_rows_kernel<uint16_t, false>, g1, dim3(kSelThreads), st, a);
-  else
-    e = vec ? launch_pdl(expand_rows_kernel<float, true>, g1, dim3(kSelThreads), st, a)
-            : launch_pdl(expand_rows_kernel<float, false>, g1, dim3(kSelThreads), st, a);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(expand_merge_kernel, dim3(static_cast<unsigned>(a.B)), dim3(kMergeT), st, a);
+    return vec ? launch_pdl(expand_tree_kernel<uint16_t, true>, g, dim3(kSelThreads), st, a)
+               : launch_pdl(expand_tree_kernel<uint16_t, false>, g, dim3(kSelThreads), st, a);
+  return vec ? launch_pdl(expand_tree_kernel<float, true>, g, dim3(kSelThreads), st, a)
+             : launch_pdl(expand_tree_kernel<float, false>, g, dim3(kSelThreads), st, a);
 }
 
 }  // namespace specv

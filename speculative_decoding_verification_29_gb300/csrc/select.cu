@@ -135,11 +135,14 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
 }
 
 // One warp selects a row from its candidate list; false when the row needs
-// the whole CTA (no top-k, no complete short list).
-template <typename Raw>
-__device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int lane) {
+// the whole CTA (no top-k, no complete short list). P <= 32 NV.
+template <typename Raw, int NV>
+__device__ bool warped_list_row_n(const SelArgs& a, int row_id, uint64_t* buf, int lane) {
+  float2 q[NV];
+  int c[NV];
+  row_load<NV>(a.part + static_cast<long long>(row_id) * a.P, a.P, a.cl, row_id, lane, q, c);
   float2 z;
-  const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+  const float M = fold_regs<NV>(q, a.c_hi, a.c_lo, &z);
   if (!(M == M && isfinite(M) && z.x > 0.f)) {  // a flagged row: the record carries M only
     if (lane == 0) {
       StatRec out;
@@ -153,7 +156,7 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
     return true;
   }
   if (!(a.top_k > 0 && a.top_k < a.V) || a.cl.seg_cap == 0) return false;
-  const int n = warp_gather(a.cl, row_id, buf, lane);
+  const int n = gather_regs<NV>(a.cl, row_id, a.P, c, buf, lane);
   if (n < a.top_k) return false;  // incomplete or too long
   if (n <= 32)
     warped_sorted<Raw, 1>(a, row_id, buf, n, M, lane);
@@ -164,6 +167,12 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
   else
     warped_sorted<Raw, 8>(a, row_id, buf, n, M, lane);
   return true;
+}
+
+template <typename Raw>
+__device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int lane) {
+  if (a.cl.seg_cap == 0 || a.P > 256) return false;  // no lists: the CTA selects every row
+  return warped_list_row_n<Raw, 8>(a, row_id, buf, lane);  // one instantiation: the code is fetched cold by every SM
 }
 
 template <typename Raw, bool VEC>

@@ -584,6 +584,82 @@ __device__ __forceinline__ int warp_gather(const CandList& cl, long long row_id,
   return n;
 }
 
+// A row's stats partials and list counts, loaded in one round trip:
+// segment lane + 32 i in q[i], c[i] (P <= 32 NV; padding (-inf, 0) and 0).
+template <int NV>
+__device__ __forceinline__ void row_load(const float2* pr, int P, const CandList& cl, long long row_id, int lane,
+                                         float2 (&q)[NV], int (&c)[NV]) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int sgi = lane + 32 * i;
+    const bool in = sgi < P;
+    q[i] = in ? __ldcg(pr + sgi) : make_float2(-INFINITY, 0.f);
+    c[i] = in && cl.seg_cap > 0 ? __ldcg(cl.cnt + row_id * P + sgi) : 0;
+  }
+}
+
+// fold_stats from partials already in registers (same order of operations).
+template <int NV>
+__device__ __forceinline__ float fold_regs(const float2 (&q)[NV], float c_hi, float c_lo, float2* zout) {
+  float m = q[0].x;
+#pragma unroll
+  for (int i = 1; i < NV; ++i) m = fmax_nan(m, q[i].x);
+  const float M = warp_max_nan(m);
+  float2 z = make_float2(0.f, 0.f);
+  if (M == M && M != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (q[i].x != -INFINITY) {
+        const float d = q[i].x - M;
+        z = ds_add(z, ds_from_prod(q[i].y, exp2f(fmaf(d, c_hi, d * c_lo))));
+      }
+#pragma unroll 1
+    for (int o = 16; o > 0; o >>= 1)
+      z = ds_add(z, make_float2(__shfl_xor_sync(0xffffffffu, z.x, o), __shfl_xor_sync(0xffffffffu, z.y, o)));
+  }
+  *zout = z;
+  return M;
+}
+
+// The row's list, counts in c (as row_load leaves them), as composites in
+// buf[0, n); returns n, or -1 when a sublist is incomplete or n >
+// kWarpList. Entries are loaded four at a time.
+template <int NV>
+__device__ __forceinline__ int gather_regs(const CandList& cl, long long row_id, int P, const int (&c)[NV],
+                                           uint64_t* buf, int lane) {
+  int mine = 0;
+  bool over = false;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    over |= c[i] > cl.seg_cap;
+    mine += c[i];
+  }
+  if (__any_sync(0xffffffffu, over)) return -1;
+  const int incl = warp_incl_scan(mine, lane);
+  const int n = __shfl_sync(0xffffffffu, incl, 31);
+  if (n > kWarpList) return -1;
+  int pos = incl - mine;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const long long sl = (row_id * P + lane + 32 * i) * cl.seg_cap;
+    for (int e0 = 0; e0 < c[i]; e0 += 4) {
+      uint32_t kk[4];
+      int ii[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (e0 + t < c[i]) {
+          kk[t] = __ldcg(cl.key + sl + e0 + t);
+          ii[t] = __ldcg(cl.idx + sl + e0 + t);
+        }
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (e0 + t < c[i]) buf[pos++] = list_comp(kk[t], ii[t]);
+    }
+  }
+  __syncwarp();
+  return n;
+}
+
 // One bitonic stage across lanes (stride < 32) over all NR registers.
 template <int NR>
 __device__ __forceinline__ void warp_stage_lanes(uint64_t (&r)[NR], int lane, int size, int stride) {
