@@ -743,6 +743,10 @@ def run_merge(args):
     graph.replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(local) if rank == 0 else None
+    t_soak = time.time()  # untimed replays so the clock sampler sees the load
+    while time.time() - t_soak < max(args.soak, 0.5):
+        graph.replay()
+        torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     graph.replay()

@@ -5,9 +5,10 @@
 // k elements of the row are >= t, so the k-th largest segment maximum is a
 // lower bound of the k-th largest logit). Then the pass proper, on the stats
 // pass's grid: one warp per segment of a row, every load of the segment in
-// flight at once together with the row's bound; each warp writes every element >= t0 of its segment, as (order-preserving key, token
-// id), to the segment's own slots of the row's candidate list, and their
-// count (no atomics, so no warp waits on a returned slot). The k largest
+// flight at once together with the row's bound; each warp writes every
+// element >= t0 of its segment, as (order-preserving key, token id), to the
+// segment's own slots of the row's candidate list, and their count (no
+// atomics, so no warp waits on a returned slot). The k largest
 // elements of a row usually lie in k different segments, and then t0 is the
 // k-th largest logit itself: a list holds little more than the top k, and
 // the per-row selection that follows reads the list instead of the row. A
