@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["abi.cu", "cand.cu", "rowscan.cu", "decide.cu", "tail.cu", "tree.cu", "noalloc.cu", "kv.cu", "entropy.cu", "merge.cu", "select.cu", "expand.cu"]
+SOURCES = ["abi.cu", "rowscan.cu", "decide.cu", "tail.cu", "tree.cu", "noalloc.cu", "kv.cu", "entropy.cu", "merge.cu", "select.cu", "expand.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC] + ARCH
 

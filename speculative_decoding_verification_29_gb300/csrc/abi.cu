@@ -42,15 +42,14 @@ char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 // Workspace: the rowscan partials, one float pair per warp segment of every
 // row, sized for the larger of the vector and scalar load paths so that the
 // size depends only on the shapes, never on pointer alignment; then, for the
-// sampling settings, one record, threshold and flag per row.
+// sampling settings, one record, threshold and flag per row; and, for the
+// top-k paths, every lane's maximum from the stats pass (32 floats per
+// segment).
 struct Layout {
-  size_t part, rec, vtau, flag, bound, cnt, ckey, cidx, total;
+  size_t part, rec, vtau, flag, lanes, total;
 };
 
-// lists adds the top-k candidate lists: per row and stats segment a count
-// and kCandSeg entries (sized for the larger segment count of the two load
-// paths).
-Layout layout(int B, int TR, int DR, int V, int dtype, bool lists = false) {
+Layout layout(int B, int TR, int DR, int V, int dtype, bool lanes = false) {
   const long long nrows = static_cast<long long>(B) * (TR + DR);
   const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
   Layout L{};
@@ -63,35 +62,15 @@ Layout layout(int B, int TR, int DR, int V, int dtype, bool lists = false) {
   off += up256(static_cast<size_t>(nrows) * sizeof(float));
   L.flag = off;
   off += up256(static_cast<size_t>(nrows) * sizeof(int32_t));
-  L.cnt = L.ckey = L.cidx = L.bound = off;
-  if (lists) {
-    off += up256(static_cast<size_t>(nrows) * sizeof(float));
-    L.cnt = off;
-    off += up256(static_cast<size_t>(nrows * P) * sizeof(int32_t));
-    L.ckey = off;
-    off += up256(static_cast<size_t>(nrows * P) * kCandSeg * sizeof(uint32_t));
-    L.cidx = off;
-    off += up256(static_cast<size_t>(nrows * P) * kCandSeg * sizeof(int32_t));
-  }
+  L.lanes = off;
+  if (lanes) off += up256(static_cast<size_t>(nrows * P) * 32 * sizeof(float));
   L.total = off;
   return L;
 }
 
-CandList cand_list(void* ws, const Layout& L, int P) {
-  CandList cl{};
-  cl.seg_cap = kCandSeg;
-  cl.P = P;
-  cl.cnt = reinterpret_cast<int32_t*>(at(ws, L.cnt));
-  cl.key = reinterpret_cast<uint32_t*>(at(ws, L.ckey));
-  cl.idx = reinterpret_cast<int32_t*>(at(ws, L.cidx));
-  cl.bound = reinterpret_cast<float*>(at(ws, L.bound));
-  return cl;
-}
-
-// The candidate filter pass serves a top-k when k is at most the number of
-// stats segments (so that the segment maxima bound the k-th largest logit).
-bool cand_pass_fits(int k, int P) { return k > 0 && k <= P && P <= 256; }
-
+// The lane maxima serve a top-k when k is at most the number of stats
+// segments (so that the segment maxima bound the k-th largest logit).
+bool lanes_fit(int k, int P) { return k > 0 && k <= P && P <= 256; }
 
 // A positive constant c as a float pair hi + lo with lo > 0, so that
 // (-inf) * lo never meets an opposite-signed infinity in fma(d, hi, d * lo).
@@ -176,12 +155,12 @@ struct ChainCall {
   float top_p = 1.f;
 };
 
-// Layout with the candidate lists; *use when the warped call's workspace
-// holds them and the filter pass serves its top-k.
-Layout chain_lists(const ChainCall& c, int P, bool* use) {
+// The lane maxima of the stats pass, when the warped call's workspace holds
+// them and they serve its top-k; NULL otherwise.
+float* chain_lanes(const ChainCall& c, int P) {
   const Layout Lx = layout(c.B, c.K + 1, c.K, c.V, c.dtype, true);
-  *use = cand_pass_fits(c.top_k, P) && c.ws_bytes >= Lx.total;
-  return Lx;
+  if (!lanes_fit(c.top_k, P) || c.ws_bytes < Lx.total) return nullptr;
+  return reinterpret_cast<float*>(at(c.ws, Lx.lanes));
 }
 
 int chain_validate(const ChainCall& c, Layout* L, bool* vec) {
@@ -210,7 +189,8 @@ int chain_scan(const ChainCall& c) {
   a.P = scan_chunks(c.V, vec, c.dtype);
   split_c(c.T, &a.c_hi, &a.c_lo);
   a.part = reinterpret_cast<float2*>(at(c.ws, L.part));
-  return cuda_status(launch_rowscan(a, c.dtype, vec, kModeStats, c.st));
+  a.lanes = chain_lanes(c, a.P);
+  return cuda_status(launch_rowscan(a, c.dtype, vec, a.lanes ? kModeStatsLanes : kModeStats, c.st));
 }
 
 int chain_sample(const ChainCall& c) {
@@ -254,23 +234,7 @@ int chain_sample(const ChainCall& c) {
     s.rec = reinterpret_cast<StatRec*>(at(c.ws, L.rec));
     s.vtau = reinterpret_cast<float*>(at(c.ws, L.vtau));
     s.row_flag = reinterpret_cast<int32_t*>(at(c.ws, L.flag));
-    bool use = false;
-    const Layout Lx = chain_lists(c, t.P, &use);
-    if (use) {
-      CandArgs f{};
-      f.A = c.Lp;
-      f.Bd = c.Lq;
-      f.B = c.B;
-      f.TR = c.K + 1;
-      f.DR = c.K;
-      f.V = c.V;
-      f.P = t.P;
-      f.k = c.top_k;
-      f.part = t.part;
-      f.cl = cand_list(c.ws, Lx, t.P);
-      if (launch_cand_filter(f, c.dtype, vec, c.st) != cudaSuccess) return SPEC_ERR_CUDA;
-      s.cl = f.cl;
-    }
+    s.lanes = chain_lanes(c, t.P);
     if (launch_warp_select(s, c.dtype, vec, c.st) != cudaSuccess) return SPEC_ERR_CUDA;
     t.rec = s.rec;
     t.vtau = s.vtau;
@@ -473,9 +437,7 @@ size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype) {
   const long long rows = static_cast<long long>(B) * F;
   const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
   return up256(static_cast<size_t>(rows * P) * sizeof(float2)) + up256(static_cast<size_t>(rows * M) * 16) +
-         up256(static_cast<size_t>(rows) * sizeof(int32_t)) + up256(static_cast<size_t>(rows) * sizeof(float)) +
-         up256(static_cast<size_t>(rows * P) * sizeof(int32_t)) +
-         2 * up256(static_cast<size_t>(rows * P) * kCandSeg * sizeof(uint32_t));
+         up256(static_cast<size_t>(rows) * sizeof(int32_t)) + up256(static_cast<size_t>(rows * P) * 32 * sizeof(float));
 }
 
 int spec_tree_expand(const void* draft_logits, int dtype, float temperature, const float* logc, int B, int F, int V,
@@ -504,35 +466,12 @@ int spec_tree_expand(const void* draft_logits, int dtype, float temperature, con
   a.part = static_cast<float2*>(workspace);
   const long long Pmax = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
   size_t off = up256(static_cast<size_t>(rows * Pmax) * sizeof(float2));
-  // candidate lists at the end of the workspace
-  size_t loff = off + up256(static_cast<size_t>(rows * M) * 16) + up256(static_cast<size_t>(rows) * sizeof(int32_t));
-  CandList cl{};
+  // the lane maxima at the end of the workspace
+  const size_t loff =
+      off + up256(static_cast<size_t>(rows * M) * 16) + up256(static_cast<size_t>(rows) * sizeof(int32_t));
   const int take = M < V ? M : V;
-  if (take < V && cand_pass_fits(take, a.P)) {
-    cl.seg_cap = kCandSeg;
-    cl.P = a.P;
-    cl.bound = reinterpret_cast<float*>(at(workspace, loff));
-    loff += up256(static_cast<size_t>(rows) * sizeof(float));
-    cl.cnt = reinterpret_cast<int32_t*>(at(workspace, loff));
-    loff += up256(static_cast<size_t>(rows * Pmax) * sizeof(int32_t));
-    cl.key = reinterpret_cast<uint32_t*>(at(workspace, loff));
-    loff += up256(static_cast<size_t>(rows * Pmax) * kCandSeg * sizeof(uint32_t));
-    cl.idx = reinterpret_cast<int32_t*>(at(workspace, loff));
-  }
-  if (launch_rowscan(a, dtype, vec, 0, st) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (cl.seg_cap) {
-    CandArgs f{};
-    f.A = draft_logits;
-    f.B = B;
-    f.TR = F;
-    f.DR = 0;
-    f.V = V;
-    f.P = a.P;
-    f.k = take;
-    f.part = a.part;
-    f.cl = cl;
-    if (launch_cand_filter(f, dtype, vec, st) != cudaSuccess) return SPEC_ERR_CUDA;
-  }
+  if (take < V && lanes_fit(take, a.P)) a.lanes = reinterpret_cast<float*>(at(workspace, loff));
+  if (launch_rowscan(a, dtype, vec, a.lanes ? kModeStatsLanes : kModeStats, st) != cudaSuccess) return SPEC_ERR_CUDA;
   ExpArgs x{};
   x.L = draft_logits;
   x.logc = logc;
@@ -554,7 +493,7 @@ int spec_tree_expand(const void* draft_logits, int dtype, float temperature, con
   x.token = token;
   x.score = score;
   x.row_status = row_status;
-  x.cl = cl;
+  x.lanes = a.lanes;
   return cuda_status(launch_expand(x, dtype, vec, st));
 }
 

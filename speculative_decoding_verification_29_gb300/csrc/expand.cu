@@ -8,14 +8,15 @@
 // log softmax(l_f / T)[v]; the M best children are kept, by score, ties to
 // the lower frontier node, then the lower token id. Only a node's own M most
 // probable tokens can be among them, so:
-//   rowscan (stats) over the F rows; for M up to the number of stats
-//   segments the candidate filter pass lists each row's elements at or above
-//   its M-th largest segment maximum; then one CTA per frontier row selects
-//   its M largest logits (from the list when it is complete, else by one
-//   filtering pass over the row for M <= 256, else by radix select on
-//   order-preserving keys; then the tokens at or above the M-th key sorted
-//   by key and id) and writes their log-probabilities as float pairs; one CTA per batch row sorts the F x M
-//   candidates by score (float pairs), node and token and keeps M.
+//   rowscan (stats, and every lane's maximum) over the F rows; then one CTA
+//   per tree. For M up to the number of stats segments one warp per
+//   frontier row rereads the lanes whose maximum reaches the row's M-th
+//   largest segment maximum, sorts those candidates and writes the top M's
+//   log-probabilities as float pairs; other rows are selected by the whole
+//   CTA (one filtering pass over the row for M <= 256, else radix select on
+//   order-preserving keys, then the tokens at or above the M-th key sorted
+//   by key and id); then the same CTA sorts the tree's F x M candidates by
+//   score (float pairs), node and token and keeps M.
 #include "select.cuh"
 
 namespace specv {
@@ -71,24 +72,32 @@ __device__ void expand_sorted(const ExpArgs& a, int row_id, const uint64_t* buf,
   if (lane == 0) a.row_flag[row_id] = 0;
 }
 
-// One warp selects a frontier row from its candidate list; false when the
-// row needs the whole CTA (no complete short list, or M >= V). P <= 32 NV.
-template <typename Raw, int NV>
-__device__ bool expand_list_row_n(const ExpArgs& a, int row_id, uint64_t* buf, int lane) {
-  float2 q[NV];
-  int c[NV];
-  row_load<NV>(a.part + static_cast<long long>(row_id) * a.P, a.P, a.cl, row_id, lane, q, c);
+// One warp selects a frontier row: its elements at or above the M-th
+// largest segment maximum, gathered by rereading the lanes of the stats pass
+// whose maximum reaches it; false when the row needs the whole CTA (no lane
+// maxima, M above the segment count or >= V, too many candidates).
+template <typename Raw, bool VEC>
+__device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int* chunks, int lane) {
+  if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
+  float2 q[8];
+  load_parts<8>(a.part + static_cast<long long>(row_id) * a.P, a.P, lane, q);
   float2 z;
-  const float M = fold_regs<NV>(q, a.c_hi, a.c_lo, &z);
+  const float M = fold_regs<8>(q, a.c_hi, a.c_lo, &z);
   if (!(M == M) || !isfinite(M) || !(z.x > 0.f)) {  // no distribution at this node
     Cand* out = static_cast<Cand*>(a.cand) + static_cast<long long>(row_id) * a.M;
     for (int i = lane; i < a.M; i += 32) out[i] = Cand{NAN, 0.f, -1, -1};
     if (lane == 0) a.row_flag[row_id] = SPEC_ROW_DRAFT;
     return true;
   }
-  if (a.M >= a.V) return false;
-  const int n = gather_regs<NV>(a.cl, row_id, a.P, c, buf, lane);
-  if (n < a.M) return false;  // incomplete or too long
+  if (a.M >= a.V || a.M > a.P) return false;
+  float sm[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sm[i] = q[i].x;
+  const float t0 = seg_bound_regs<8>(sm, a.P, a.M, lane);
+  const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
+  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, buf,
+                                        chunks, lane);
+  if (n < a.M) return false;  // too many candidates
   const float2 lz = ln_of(z);
   if (n <= 32)
     expand_sorted<Raw, 1>(a, row_id, buf, n, M, lz, lane);
@@ -99,12 +108,6 @@ __device__ bool expand_list_row_n(const ExpArgs& a, int row_id, uint64_t* buf, i
   else
     expand_sorted<Raw, 8>(a, row_id, buf, n, M, lz, lane);
   return true;
-}
-
-template <typename Raw>
-__device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int lane) {
-  if (a.cl.seg_cap == 0 || a.P > 256) return false;  // no lists: the CTA selects every row
-  return expand_list_row_n<Raw, 8>(a, row_id, buf, lane);  // one instantiation: the code is fetched cold by every SM
 }
 
 constexpr int kMergeCap = 2048;  // F x M candidates held in shared memory (32 KB)
@@ -216,16 +219,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) expand_tree_kernel(ExpArgs a) 
   const int take = Mk < a.V ? Mk : a.V;
   unsigned cnt = static_cast<unsigned>(a.V);
   uint32_t tau = 0u;
-  int have = -1;  // candidates already gathered (from the filter pass's list, or by filtering the row here)
+  int have = -1;  // candidates already gathered by filtering the row here
   const FiltSmem fs{s_key, s_idx, s_wh, s_tot, s_cnt, s_sel, &s_n};
-  if (take < a.V && a.cl.seg_cap > 0) {
-    const int n = gather_list(a.cl, row_id, fs);
-    if (n >= take) {  // a complete list
-      have = top_from_list<Raw>(n, take, fs, &tau);
-      cnt = static_cast<unsigned>(have);
-    }
-  }
-  if (have < 0 && take < a.V && take <= kFiltMaxK) {
+  if (take < a.V && take <= kFiltMaxK) {
     if (warp == 0) {  // a lower bound of the M-th largest logit to start from
       const float t0 = seg_bound(a.part + static_cast<long long>(row_id) * a.P, a.P, take, lane);
       if (lane == 0) s_t0 = t0;
@@ -302,14 +298,15 @@ __global__ void __launch_bounds__(kSelThreads, 2) expand_tree_kernel(ExpArgs a) 
     for (int i = tid; i < Mk; i += kSelThreads) out[i] = Cand{NAN, 0.f, -1, -1};
   if (tid == 0) a.row_flag[row_id] = st;
   };
-  static_assert(kSelWarps * kWarpList * 8 <= sizeof(uint32_t) * 2 * kCand, "list buffers fit");
+  static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 4) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
   static_assert(kMergeCap * sizeof(Cand) <= sizeof(uint32_t) * 2 * kCand, "merge buffer fits");
+  uint64_t* wl = reinterpret_cast<uint64_t*>(s_buf);
+  int* wc = reinterpret_cast<int*>(wl + kSelWarps * kWarpList);
   for (int r0 = 0; r0 < a.F; r0 += kSelWarps) {
-    {  // one warp per row with a short complete candidate list (s_buf: the warps' list buffers)
+    {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
       const int r = r0 + warp;
       const bool done =
-          r >= a.F ||
-          expand_list_row<Raw>(a, b * a.F + r, reinterpret_cast<uint64_t*>(s_buf) + warp * kWarpList, lane);
+          r >= a.F || expand_list_row<Raw, VEC>(a, b * a.F + r, wl + warp * kWarpList, wc + warp * kChunkCap, lane);
       if (lane == 0) s_slow[warp] = !done;
     }
     __syncthreads();

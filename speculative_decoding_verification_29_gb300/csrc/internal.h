@@ -12,6 +12,7 @@ namespace specv {
 constexpr int kModeStats = 0;   // rowscan: (max, sum of exp) per row
 constexpr int kModeArgmax = 1;  // rowscan: (value, index) of the row maximum
 constexpr int kModeEntropy = 2; // rowscan: (max, sum of exp, sum of exp * (l - max)) per row, float4 partials
+constexpr int kModeStatsLanes = 3;  // rowscan: as kModeStats, and each lane's maximum (the top-k paths)
 constexpr int kMaxK = 255;
 
 // rowscan geometry: each warp reduces one segment of kSegChunks chunks of kWV
@@ -62,32 +63,9 @@ struct ScanArgs {
   int P;             // chunks (partials) per row
   float c_hi, c_lo;  // log2(e) / T as a float pair, c_lo > 0
   float2* part;      // [B * (TR + DR)][P]
+  float* lanes;      // kModeStatsLanes: [B * (TR + DR)][P][32] each lane's maximum over its elements
 };
 
-// Per-row candidate lists of a top-k: every element at or above a lower
-// bound of the row's k-th largest logit, kept per stats segment (P segments
-// of seg_cap entries per row, no atomics between segments).
-struct CandList {
-  int seg_cap;     // entries per segment; 0: no lists
-  int P;           // segments per row
-  int32_t* cnt;    // [rows][P] elements at or above the bound (> seg_cap: that sublist is incomplete)
-  uint32_t* key;   // [rows][P][seg_cap] order-preserving keys
-  int32_t* idx;    // [rows][P][seg_cap] token ids
-  float* bound;    // [rows] the filter's threshold: a lower bound of the k-th largest logit
-};
-constexpr int kCandSeg = 16;   // entries per segment
-constexpr int kCandCap = 512;  // entries per row a selection gathers
-
-// The candidate filter pass (after the stats pass): rows as in ScanArgs.
-struct CandArgs {
-  const void* A;
-  const void* Bd;
-  int B, TR, DR, V, P;
-  int k;  // rank the lists must cover (1 <= k <= P <= 256)
-  const float2* part;
-  CandList cl;
-};
-cudaError_t launch_cand_filter(const CandArgs& a, int dtype, bool vec, cudaStream_t st);
 
 // Warp segments per row, and so partials per row, for a vocabulary of V
 // entries.
@@ -174,7 +152,7 @@ struct SelArgs {
   StatRec* rec;        // [rows]: M, kept mass Z', log2 Z'
   float* vtau;         // [rows]: a token is kept iff its logit >= vtau
   int32_t* row_flag;   // [rows]: SPEC_ROW_WARP or 0
-  CandList cl;         // top-k candidate lists from the filter pass (cap 0: none)
+  const float* lanes;  // the stats pass's lane maxima [rows][P][32] (NULL: none)
 };
 int select_candidates();
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st);
@@ -193,7 +171,7 @@ struct ExpArgs {
   int32_t* token;       // [B][M]
   float* score;         // [B][M]
   int32_t* row_status;  // [B]
-  CandList cl;          // top-M candidate lists from the filter pass (cap 0: none)
+  const float* lanes;   // the stats pass's lane maxima [B * F][P][32] (NULL: none)
 };
 int expand_limits(int* max_m, int* max_fm);
 cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st);

@@ -16,7 +16,11 @@
 //          it is the target's top choice);
 //   entropy (drafter trees): (m, z, y) with y = sum 2^((l - m) log2(e) / T)
 //          (l - m), from which a row's softmax entropy follows (TAPS page:
-//          entropy routing of drafter trees).
+//          entropy routing of drafter trees);
+//   stats + lanes (top-k): as stats, and every lane's maximum over its own
+//          elements (8 sixteen-byte vectors, 32 vectors apart), so that a
+//          top-k selection can reread only the lanes whose maximum reaches
+//          its bound.
 // The max runs on packed bf16 pairs, the exponent arithmetic on packed fp32
 // pairs (f32x2) with one accumulator per pair lane; a lane's running sum is
 // rescaled (exp2f, correctly rounded to within an ulp) when its running max
@@ -128,6 +132,8 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
         yac[0] = add2(yac[0], yac[i]);
       }
       float z = acc[0].x + acc[0].y, y = yac[0].x + yac[0].y;
+      if constexpr (MODE == kModeStatsLanes)
+        a.lanes[((static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg) * 32 + lane] = mrun;
       M = warp_max_nan(mrun);
       if (M == M && M != -INFINITY) {
         if (mrun == -INFINITY) {
@@ -190,6 +196,8 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
     float m = -INFINITY;
 #pragma unroll
     for (int t = 0; t < kScalarPerLane; ++t) m = fmax_nan(m, e[t]);
+    if constexpr (MODE == kModeStatsLanes)
+      a.lanes[((static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg) * 32 + lane] = m;
     M = warp_max_nan(m);
     if constexpr (MODE != kModeArgmax) {
       float z = 0.f, y = 0.f;
@@ -240,6 +248,7 @@ template <typename Raw, bool VEC>
 cudaError_t launch_mode(const ScanArgs& a, int mode, cudaStream_t st) {
   if (mode == kModeStats) return launch_t<Raw, VEC, kModeStats>(a, st);
   if (mode == kModeEntropy) return launch_t<Raw, VEC, kModeEntropy>(a, st);
+  if (mode == kModeStatsLanes) return launch_t<Raw, VEC, kModeStatsLanes>(a, st);
   return launch_t<Raw, VEC, kModeArgmax>(a, st);
 }
 

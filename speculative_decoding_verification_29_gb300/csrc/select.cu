@@ -10,15 +10,14 @@
 // top_p). Both keep a set {v : key(l_v) >= tau}, key the order-preserving
 // unsigned image of the logit's bits.
 //
-// After the stats pass (its partials give M and Z). A row whose top-k
-// candidate list (from the filter pass) is complete and short is selected
-// by one warp: the list sorted in registers, the top-k threshold its k-th
-// entry, then the top-p scan and the kept mass by shuffles. Every other row
-// is selected by a whole CTA:
-//   top-k: the k largest keys (ties included) and their weights come from
-//          the candidate filter pass's list of the row when it ran (k up to
-//          the number of stats segments) and the list is complete; else, for
-//          k <= 256, from one filtering pass over the row here; otherwise,
+// After the stats pass (its partials give M and Z; in its top-k mode also
+// every lane's maximum). A row whose top-k has few candidates is selected by
+// one warp: the lanes whose maximum reaches the row's bound are reread, the
+// candidates sorted in registers, the top-k threshold is their k-th entry,
+// then the top-p scan and the kept mass by shuffles. Every other row is
+// selected by a whole CTA:
+//   top-k: for k <= 256 the k largest keys (ties included) and their
+//          weights come from one filtering pass over the row; otherwise,
 //          or when ties overflow the buffers, a radix select of the k-th
 //          largest key, 8 bits per pass over the row (2 passes for bf16, 4
 //          for fp32), counts only: exact;
@@ -134,15 +133,18 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
   }
 }
 
-// One warp selects a row from its candidate list; false when the row needs
-// the whole CTA (no top-k, no complete short list). P <= 32 NV.
-template <typename Raw, int NV>
-__device__ bool warped_list_row_n(const SelArgs& a, int row_id, uint64_t* buf, int lane) {
-  float2 q[NV];
-  int c[NV];
-  row_load<NV>(a.part + static_cast<long long>(row_id) * a.P, a.P, a.cl, row_id, lane, q, c);
+// One warp selects a row: the row's elements at or above a lower bound t0
+// of its k-th largest logit (the k-th largest segment maximum), gathered by
+// rereading the lanes of the stats pass whose maximum reaches t0; false when
+// the row needs the whole CTA (no top-k, no lane maxima, too many
+// candidates).
+template <typename Raw, bool VEC>
+__device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int* chunks, int lane) {
+  if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
+  float2 q[8];
+  load_parts<8>(a.part + static_cast<long long>(row_id) * a.P, a.P, lane, q);
   float2 z;
-  const float M = fold_regs<NV>(q, a.c_hi, a.c_lo, &z);
+  const float M = fold_regs<8>(q, a.c_hi, a.c_lo, &z);
   if (!(M == M && isfinite(M) && z.x > 0.f)) {  // a flagged row: the record carries M only
     if (lane == 0) {
       StatRec out;
@@ -155,9 +157,18 @@ __device__ bool warped_list_row_n(const SelArgs& a, int row_id, uint64_t* buf, i
     }
     return true;
   }
-  if (!(a.top_k > 0 && a.top_k < a.V) || a.cl.seg_cap == 0) return false;
-  const int n = gather_regs<NV>(a.cl, row_id, a.P, c, buf, lane);
-  if (n < a.top_k) return false;  // incomplete or too long
+  if (!(a.top_k > 0 && a.top_k <= a.P && a.top_k < a.V)) return false;
+  float sm[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sm[i] = q[i].x;
+  const float t0 = seg_bound_regs<8>(sm, a.P, a.top_k, lane);
+  const int RPG = a.TR + a.DR;
+  const int b = row_id / RPG, j = row_id - b * RPG;
+  const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
+                            : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
+  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, buf,
+                                        chunks, lane);
+  if (n < a.top_k) return false;  // too many candidates
   if (n <= 32)
     warped_sorted<Raw, 1>(a, row_id, buf, n, M, lane);
   else if (n <= 64)
@@ -167,12 +178,6 @@ __device__ bool warped_list_row_n(const SelArgs& a, int row_id, uint64_t* buf, i
   else
     warped_sorted<Raw, 8>(a, row_id, buf, n, M, lane);
   return true;
-}
-
-template <typename Raw>
-__device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int lane) {
-  if (a.cl.seg_cap == 0 || a.P > 256) return false;  // no lists: the CTA selects every row
-  return warped_list_row_n<Raw, 8>(a, row_id, buf, lane);  // one instantiation: the code is fetched cold by every SM
 }
 
 template <typename Raw, bool VEC>
@@ -197,11 +202,13 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
   __shared__ float2 s_Z;
   __shared__ int s_slow[kSelWarps];
   griddep_wait();
-  {  // one warp per row with a short complete candidate list (s_buf: the warps' list buffers)
+  {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
     const int row_id = blockIdx.x * kSelWarps + warp;
-    static_assert(kSelWarps * kWarpList * 8 <= sizeof(uint32_t) * 2 * kCand, "list buffers fit");
-    const bool done =
-        row_id >= rows || warped_list_row<Raw>(a, row_id, reinterpret_cast<uint64_t*>(s_buf) + warp * kWarpList, lane);
+    static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 4) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
+    uint64_t* wl = reinterpret_cast<uint64_t*>(s_buf);
+    int* wc = reinterpret_cast<int*>(wl + kSelWarps * kWarpList);
+    const bool done = row_id >= rows ||
+                      warped_list_row<Raw, VEC>(a, row_id, wl + warp * kWarpList, wc + warp * kChunkCap, lane);
     if (lane == 0) s_slow[warp] = !done;
   }
   __syncthreads();
@@ -238,20 +245,9 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
   if (ok) {
     const bool use_k = a.top_k > 0 && a.top_k < a.V;
     unsigned count_ge = static_cast<unsigned>(a.V);  // tokens top-k keeps
-    int have = -1;  // the top-k set already gathered (keys and weights): from the list or by filtering here
+    int have = -1;  // the top-k set already gathered (keys and weights) by filtering the row here
     const FiltSmem fs{s_key, reinterpret_cast<int*>(s_w), s_wh, s_tot, s_cnt, s_sel, &s_n};
-    if (use_k && a.cl.seg_cap > 0) {
-      const int n = gather_list(a.cl, row_id, fs);
-      if (n >= a.top_k) {  // a complete list
-        have = top_from_list<Raw>(n, a.top_k, fs, &tau);
-        if (have >= 0) {
-          count_ge = static_cast<unsigned>(have);
-          for (int e = tid; e < have; e += kSelThreads) s_w[e] = weight_v(key_value<Raw>(s_key[e]));
-          __syncthreads();
-        }
-      }
-    }
-    if (use_k && have < 0 && a.top_k <= kFiltMaxK) {
+    if (use_k && a.top_k <= kFiltMaxK) {
       if (warp == 0) {  // a lower bound of the k-th largest logit to start from
         const float t0 = seg_bound(a.part + static_cast<long long>(row_id) * a.P, a.P, a.top_k, lane);
         if (lane == 0) s_t0 = t0;

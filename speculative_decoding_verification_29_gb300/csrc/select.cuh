@@ -497,55 +497,14 @@ __device__ int filter_top(const Raw* row, int V, int k, float t0, const FiltSmem
       k, sm, [&](int e) { return (e % kFiltCap) < sm.cnt[e / kFiltCap]; }, tau);
 }
 
-// A row's candidate list (the filter pass's per-segment sublists) gathered
-// into key[0, n), idx[0, n); returns n, or -1 when a sublist is incomplete
-// or n > kCandCap. Every thread of the CTA calls it (P <= kSelThreads).
-__device__ __forceinline__ int gather_list(const CandList& cl, long long row_id, const FiltSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int c = 0;
-  if (tid < cl.P) c = cl.cnt[row_id * cl.P + tid];
-  const int over = __syncthreads_or(c > cl.seg_cap);
-  if (over) return -1;
-  const int incl = warp_incl_scan(c, lane);
-  if (lane == 31) sm.cnt[warp] = incl;
-  __syncthreads();
-  int before = incl - c, n = 0;
-#pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
-    const int t = sm.cnt[w];
-    if (w < warp) before += t;
-    n += t;
-  }
-  __syncthreads();  // sm.cnt is reused by the caller
-  if (n > kCandCap) return -1;
-  if (c > 0) {
-    const long long sl = (row_id * cl.P + tid) * cl.seg_cap;
-    for (int i = 0; i < c; ++i) {
-      sm.key[before + i] = cl.key[sl + i];
-      sm.idx[before + i] = cl.idx[sl + i];
-    }
-  }
-  __syncthreads();
-  return n;
-}
-
-// The candidates of a per-row list (from the filter pass), n <= kCandCap
-// entries already in key[0, n), idx[0, n), n >= k: the entries with key >=
-// K, K their k-th largest key, packed to the front; returns their count,
-// *tau = K.
-template <typename Raw>
-__device__ int top_from_list(int n, int k, const FiltSmem& sm, uint32_t* tau) {
-  return select_slots<Key<Raw>::kBits, kCandCap>(k, sm, [&](int e) { return e < n; }, tau);
-}
-
-// ------------------------------------------------ one warp per listed row --
+// ------------------------------------------------ one warp per row --
 //
-// A row whose candidate list is complete and short (at most kWarpList
-// entries) is selected by one warp, with no block barrier: the list is
-// gathered into the warp's shared buffer, sorted in registers (bitonic
-// network over 32 x NR entries: exchanges across lanes by shuffles, across a
-// lane's registers in place) by a 64-bit composite, key high and inverted
-// token id low (key descending, then token id ascending).
+// A row with few candidates (at most kWarpList) is selected by one warp, with
+// no block barrier: the candidates are gathered into the warp's shared
+// buffer, sorted in registers (bitonic network over 32 x NR entries:
+// exchanges across lanes by shuffles, across a lane's registers in place) by
+// a 64-bit composite, key high and inverted token id low (key descending,
+// then token id ascending).
 
 constexpr int kWarpList = 256;  // entries one warp sorts (8 per lane)
 
@@ -554,49 +513,6 @@ __device__ __forceinline__ uint64_t list_comp(uint32_t key, int idx) {
 }
 __device__ __forceinline__ uint32_t comp_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
 __device__ __forceinline__ int comp_idx(uint64_t c) { return static_cast<int>(~static_cast<uint32_t>(c)); }
-
-// The row's list as composites in buf[0, n) (buf: kWarpList entries private
-// to the warp); returns n, or -1 when a sublist is incomplete or n >
-// kWarpList. One full warp (P <= 256).
-__device__ __forceinline__ int warp_gather(const CandList& cl, long long row_id, uint64_t* buf, int lane) {
-  const int spl = (cl.P + 31) >> 5;  // segments per lane, contiguous
-  const int s0 = lane * spl;
-  int mine = 0;
-  bool over = false;
-  for (int i = 0; i < spl; ++i) {
-    const int sgi = s0 + i;
-    const int c = sgi < cl.P ? cl.cnt[row_id * cl.P + sgi] : 0;
-    over |= c > cl.seg_cap;
-    mine += c;
-  }
-  if (__any_sync(0xffffffffu, over)) return -1;
-  const int incl = warp_incl_scan(mine, lane);
-  const int n = __shfl_sync(0xffffffffu, incl, 31);
-  if (n > kWarpList) return -1;
-  int pos = incl - mine;
-  for (int i = 0; i < spl; ++i) {
-    const int sgi = s0 + i;
-    const int c = sgi < cl.P ? cl.cnt[row_id * cl.P + sgi] : 0;
-    const long long sl = (row_id * cl.P + sgi) * cl.seg_cap;
-    for (int e = 0; e < c; ++e) buf[pos++] = list_comp(cl.key[sl + e], cl.idx[sl + e]);
-  }
-  __syncwarp();
-  return n;
-}
-
-// A row's stats partials and list counts, loaded in one round trip:
-// segment lane + 32 i in q[i], c[i] (P <= 32 NV; padding (-inf, 0) and 0).
-template <int NV>
-__device__ __forceinline__ void row_load(const float2* pr, int P, const CandList& cl, long long row_id, int lane,
-                                         float2 (&q)[NV], int (&c)[NV]) {
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int sgi = lane + 32 * i;
-    const bool in = sgi < P;
-    q[i] = in ? __ldcg(pr + sgi) : make_float2(-INFINITY, 0.f);
-    c[i] = in && cl.seg_cap > 0 ? __ldcg(cl.cnt + row_id * P + sgi) : 0;
-  }
-}
 
 // fold_stats from partials already in registers (same order of operations).
 template <int NV>
@@ -619,45 +535,6 @@ __device__ __forceinline__ float fold_regs(const float2 (&q)[NV], float c_hi, fl
   }
   *zout = z;
   return M;
-}
-
-// The row's list, counts in c (as row_load leaves them), as composites in
-// buf[0, n); returns n, or -1 when a sublist is incomplete or n >
-// kWarpList. Entries are loaded four at a time.
-template <int NV>
-__device__ __forceinline__ int gather_regs(const CandList& cl, long long row_id, int P, const int (&c)[NV],
-                                           uint64_t* buf, int lane) {
-  int mine = 0;
-  bool over = false;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    over |= c[i] > cl.seg_cap;
-    mine += c[i];
-  }
-  if (__any_sync(0xffffffffu, over)) return -1;
-  const int incl = warp_incl_scan(mine, lane);
-  const int n = __shfl_sync(0xffffffffu, incl, 31);
-  if (n > kWarpList) return -1;
-  int pos = incl - mine;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const long long sl = (row_id * P + lane + 32 * i) * cl.seg_cap;
-    for (int e0 = 0; e0 < c[i]; e0 += 4) {
-      uint32_t kk[4];
-      int ii[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (e0 + t < c[i]) {
-          kk[t] = __ldcg(cl.key + sl + e0 + t);
-          ii[t] = __ldcg(cl.idx + sl + e0 + t);
-        }
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        if (e0 + t < c[i]) buf[pos++] = list_comp(kk[t], ii[t]);
-    }
-  }
-  __syncwarp();
-  return n;
 }
 
 // One bitonic stage across lanes (stride < 32) over all NR registers.
@@ -735,6 +612,134 @@ __device__ __forceinline__ uint64_t warp_entry(const uint64_t (&r)[NR], int e) {
     if ((e >> 5) == i) v = x;
   }
   return v;
+}
+
+// ------------------------------------------------ rereading the top lanes --
+
+constexpr int kChunkCap = 512;  // lanes of the stats pass one warp rereads for a row
+
+// The row's stats partials, P <= 32 NV: segment lane + 32 i in q[i]
+// (padding (-inf, 0)); one round trip.
+template <int NV>
+__device__ __forceinline__ void load_parts(const float2* pr, int P, int lane, float2 (&q)[NV]) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int sgi = lane + 32 * i;
+    q[i] = sgi < P ? __ldcg(pr + sgi) : make_float2(-INFINITY, 0.f);
+  }
+}
+
+// The row's elements >= t0 as composites in buf[0, n). Each such element
+// lies in a lane of the stats pass whose maximum (lanes: the row's P x 32
+// lane maxima) is >= t0, so only those lanes' elements are reread: 8
+// vectors 32 apart (or 64 elements 32 apart on the scalar path). Returns n,
+// or -1 when more than kChunkCap lanes or kWarpList elements qualify. One
+// full warp; chunks: kChunkCap ints private to the warp.
+template <typename Raw, bool VEC>
+__device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, float t0, uint64_t* buf, int* chunks,
+                             int lane) {
+  using KY = Key<Raw>;
+  const unsigned below = (1u << lane) - 1u;
+  // the qualifying lanes, from all P x 32 lane maxima (eight 16-byte loads per lane in flight)
+  const int nf4 = P * 8;
+  const float4* l4 = reinterpret_cast<const float4*>(lanes);
+  int nc = 0;
+  for (int f0 = 0; f0 < nf4; f0 += 32 * 8) {
+    float4 v[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int f = f0 + 32 * r + lane;
+      v[r] = f < nf4 ? __ldcg(l4 + f) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const bool hit = x[c] >= t0;
+        const unsigned bm = __ballot_sync(0xffffffffu, hit);
+        if (hit) {
+          const int p = nc + __popc(bm & below);
+          if (p < kChunkCap) chunks[p] = 4 * (f0 + 32 * r + lane) + c;
+        }
+        nc += __popc(bm);
+      }
+    }
+  }
+  if (nc > kChunkCap) return -1;
+  __syncwarp();
+  // reread them, one lane's elements per warp lane
+  int n = 0;
+  for (int i0 = 0; i0 < nc; i0 += 32) {
+    const int i = i0 + lane;
+    const int id = i < nc ? chunks[i] : -1;
+    const int sg = id >> 5, ls = id & 31;
+    int cnt = 0;
+    if constexpr (VEC) {
+      constexpr int NL = kSegChunks * kWV;
+      constexpr int E = Elem<Raw>::kPerVec;
+      const int nv = V / E;
+      const uint4 neg = make_uint4(Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf);
+      uint4 q[NL];
+#pragma unroll
+      for (int t = 0; t < NL; ++t) {
+        const int vi = sg * (NL * 32) + ls + t * 32;
+        q[t] = id >= 0 && vi < nv ? __ldcg(reinterpret_cast<const uint4*>(row) + vi) : neg;
+      }
+#pragma unroll
+      for (int t = 0; t < NL; ++t) {
+        float v[E];
+        Elem<Raw>::unpack(q[t], v);
+#pragma unroll
+        for (int e = 0; e < E; ++e) cnt += v[e] >= t0 ? 1 : 0;
+      }
+      const int incl = warp_incl_scan(cnt, lane);
+      int p = n + incl - cnt;
+#pragma unroll
+      for (int t = 0; t < NL; ++t) {
+        float v[E];
+        Elem<Raw>::unpack(q[t], v);
+        const uint32_t w[4] = {q[t].x, q[t].y, q[t].z, q[t].w};
+        const int vi = sg * (NL * 32) + ls + t * 32;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          if (v[e] >= t0) {
+            uint32_t bits;
+            if constexpr (E == 8)
+              bits = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+            else
+              bits = w[e];
+            if (p < kWarpList) buf[p] = list_comp(KY::of(bits), vi * E + e);
+            ++p;
+          }
+      }
+      n += __shfl_sync(0xffffffffu, incl, 31);
+    } else {
+      const int v0 = sg * (kScalarPerLane * 32) + ls;
+#pragma unroll 8
+      for (int t = 0; t < kScalarPerLane; ++t) {
+        const int v = v0 + t * 32;
+        if (id >= 0 && v < V && Elem<Raw>::at(row, v) >= t0) ++cnt;
+      }
+      const int incl = warp_incl_scan(cnt, lane);
+      int p = n + incl - cnt;
+#pragma unroll 8
+      for (int t = 0; t < kScalarPerLane; ++t) {
+        const int v = v0 + t * 32;
+        if (id >= 0 && v < V) {
+          const float x = Elem<Raw>::at(row, v);
+          if (x >= t0) {
+            const uint32_t bits = sizeof(Raw) == 2 ? (__float_as_uint(x) >> 16) : __float_as_uint(x);
+            if (p < kWarpList) buf[p] = list_comp(KY::of(bits), v);
+            ++p;
+          }
+        }
+      }
+      n += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncwarp();
+  return n > kWarpList ? -1 : n;
 }
 
 // Sum of float pairs over a warp (every lane gets it).
