@@ -77,7 +77,7 @@ __device__ void expand_sorted(const ExpArgs& a, int row_id, const uint64_t* buf,
 // whose maximum reaches it; false when the row needs the whole CTA (no lane
 // maxima, M above the segment count or >= V, too many candidates).
 template <typename Raw, bool VEC>
-__device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int* chunks, int lane) {
+__device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int* chunks, float* cmax, int lane) {
   if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
   float2 q[8];
   load_parts<8>(a.part + static_cast<long long>(row_id) * a.P, a.P, lane, q);
@@ -95,8 +95,8 @@ __device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int
   for (int i = 0; i < 8; ++i) sm[i] = q[i].x;
   const float t0 = seg_bound_regs<8>(sm, a.P, a.M, lane);
   const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
-  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, buf,
-                                        chunks, lane);
+  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, a.M,
+                                        buf, chunks, cmax, lane);
   if (n < a.M) return false;  // too many candidates
   const float2 lz = ln_of(z);
   if (n <= 32)
@@ -298,15 +298,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) expand_tree_kernel(ExpArgs a) 
     for (int i = tid; i < Mk; i += kSelThreads) out[i] = Cand{NAN, 0.f, -1, -1};
   if (tid == 0) a.row_flag[row_id] = st;
   };
-  static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 4) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
+  static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 8) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
   static_assert(kMergeCap * sizeof(Cand) <= sizeof(uint32_t) * 2 * kCand, "merge buffer fits");
   uint64_t* wl = reinterpret_cast<uint64_t*>(s_buf);
   int* wc = reinterpret_cast<int*>(wl + kSelWarps * kWarpList);
+  float* wm = reinterpret_cast<float*>(wc + kSelWarps * kChunkCap);
   for (int r0 = 0; r0 < a.F; r0 += kSelWarps) {
     {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
       const int r = r0 + warp;
-      const bool done =
-          r >= a.F || expand_list_row<Raw, VEC>(a, b * a.F + r, wl + warp * kWarpList, wc + warp * kChunkCap, lane);
+      const bool done = r >= a.F || expand_list_row<Raw, VEC>(a, b * a.F + r, wl + warp * kWarpList,
+                                                               wc + warp * kChunkCap, wm + warp * kChunkCap, lane);
       if (lane == 0) s_slow[warp] = !done;
     }
     __syncthreads();

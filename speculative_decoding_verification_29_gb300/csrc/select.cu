@@ -139,7 +139,7 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
 // the row needs the whole CTA (no top-k, no lane maxima, too many
 // candidates).
 template <typename Raw, bool VEC>
-__device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int* chunks, int lane) {
+__device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int* chunks, float* cmax, int lane) {
   if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
   float2 q[8];
   load_parts<8>(a.part + static_cast<long long>(row_id) * a.P, a.P, lane, q);
@@ -166,8 +166,8 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
   const int b = row_id / RPG, j = row_id - b * RPG;
   const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
                             : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
-  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, buf,
-                                        chunks, lane);
+  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, a.top_k,
+                                        buf, chunks, cmax, lane);
   if (n < a.top_k) return false;  // too many candidates
   if (n <= 32)
     warped_sorted<Raw, 1>(a, row_id, buf, n, M, lane);
@@ -204,11 +204,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) 
   griddep_wait();
   {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
     const int row_id = blockIdx.x * kSelWarps + warp;
-    static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 4) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
+    static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 8) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
     uint64_t* wl = reinterpret_cast<uint64_t*>(s_buf);
     int* wc = reinterpret_cast<int*>(wl + kSelWarps * kWarpList);
-    const bool done = row_id >= rows ||
-                      warped_list_row<Raw, VEC>(a, row_id, wl + warp * kWarpList, wc + warp * kChunkCap, lane);
+    float* wm = reinterpret_cast<float*>(wc + kSelWarps * kChunkCap);
+    const bool done = row_id >= rows || warped_list_row<Raw, VEC>(a, row_id, wl + warp * kWarpList,
+                                                                  wc + warp * kChunkCap, wm + warp * kChunkCap, lane);
     if (lane == 0) s_slow[warp] = !done;
   }
   __syncthreads();

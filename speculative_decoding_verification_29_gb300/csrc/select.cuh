@@ -616,7 +616,7 @@ __device__ __forceinline__ uint64_t warp_entry(const uint64_t (&r)[NR], int e) {
 
 // ------------------------------------------------ rereading the top lanes --
 
-constexpr int kChunkCap = 512;  // lanes of the stats pass one warp rereads for a row
+constexpr int kChunkCap = 256;  // lanes of the stats pass one warp considers for a row
 
 // The row's stats partials, P <= 32 NV: segment lane + 32 i in q[i]
 // (padding (-inf, 0)); one round trip.
@@ -629,15 +629,20 @@ __device__ __forceinline__ void load_parts(const float2* pr, int P, int lane, fl
   }
 }
 
-// The row's elements >= t0 as composites in buf[0, n). Each such element
-// lies in a lane of the stats pass whose maximum (lanes: the row's P x 32
-// lane maxima) is >= t0, so only those lanes' elements are reread: 8
-// vectors 32 apart (or 64 elements 32 apart on the scalar path). Returns n,
-// or -1 when more than kChunkCap lanes or kWarpList elements qualify. One
-// full warp; chunks: kChunkCap ints private to the warp.
+// The row's candidates for its k largest elements as composites in
+// buf[0, n). t0 (a lower bound of the k-th largest value, from the segment
+// maxima) picks the lanes of the stats pass whose maximum (lanes: the row's
+// P x 32 lane maxima) is >= t0; when more than 32 do, the k-th largest of
+// those maxima, t1, is a tighter bound (k lanes hold an element >= t1) and
+// replaces t0. Every element >= the bound lies in a lane whose maximum is >=
+// it, so only those lanes' elements are reread: 8 vectors 32 apart (or 64
+// elements 32 apart on the scalar path). Returns n (the elements >= the
+// bound, n >= k), or -1 when more than kChunkCap
+// lanes or kWarpList elements qualify. One full warp; chunks, cmax:
+// kChunkCap entries private to the warp.
 template <typename Raw, bool VEC>
-__device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, float t0, uint64_t* buf, int* chunks,
-                             int lane) {
+__device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, float t0, int k, uint64_t* buf,
+                             int* chunks, float* cmax, int lane) {
   using KY = Key<Raw>;
   const unsigned below = (1u << lane) - 1u;
   // the qualifying lanes, from all P x 32 lane maxima (eight 16-byte loads per lane in flight)
@@ -660,14 +665,39 @@ __device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, f
         const unsigned bm = __ballot_sync(0xffffffffu, hit);
         if (hit) {
           const int p = nc + __popc(bm & below);
-          if (p < kChunkCap) chunks[p] = 4 * (f0 + 32 * r + lane) + c;
+          if (p < kChunkCap) {
+            chunks[p] = 4 * (f0 + 32 * r + lane) + c;
+            cmax[p] = x[c];
+          }
         }
         nc += __popc(bm);
       }
     }
   }
-  if (nc > kChunkCap) return -1;
+  if (nc > kChunkCap || nc < k) return -1;
   __syncwarp();
+  // t1: the k-th largest of the qualifying lane maxima (to 16 bits of the
+  // key), when enough lanes qualify for it to pay
+  if (nc > 32) {
+    float m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = lane + 32 * i < nc ? cmax[lane + 32 * i] : -INFINITY;
+    const float t1 = seg_bound_regs<8>(m8, nc, k, lane);
+    // keep the lanes whose maximum is >= t1, packed in place (an entry only moves down)
+    int kept = 0;
+    for (int i0 = 0; i0 < nc; i0 += 32) {
+      const int i = i0 + lane;
+      const int id = i < nc ? chunks[i] : 0;
+      const bool keep = i < nc && cmax[i] >= t1;
+      __syncwarp();
+      const unsigned bm = __ballot_sync(0xffffffffu, keep);
+      if (keep) chunks[kept + __popc(bm & below)] = id;
+      kept += __popc(bm);
+      __syncwarp();
+    }
+    nc = kept;
+    t0 = t1;
+  }
   // reread them, one lane's elements per warp lane
   int n = 0;
   for (int i0 = 0; i0 < nc; i0 += 32) {
