@@ -8,15 +8,15 @@
 // log softmax(l_f / T)[v]; the M best children are kept, by score, ties to
 // the lower frontier node, then the lower token id. Only a node's own M most
 // probable tokens can be among them, so:
-//   rowscan (stats, and every lane's maximum) over the F rows; then one CTA
-//   per tree. For M up to the number of stats segments one warp per
-//   frontier row rereads the lanes whose maximum reaches the row's M-th
-//   largest segment maximum, sorts those candidates and writes the top M's
-//   log-probabilities as float pairs; other rows are selected by the whole
+//   rowscan (stats, and every lane's maximum) over the F rows; then, for M
+//   up to the number of stats segments, one warp per frontier row rereads
+//   the lanes whose maximum reaches the row's M-th largest segment maximum,
+//   sorts those candidates and writes the top M's log-probabilities as
+//   float pairs; other rows are selected by the whole
 //   CTA (one filtering pass over the row for M <= 256, else radix select on
 //   order-preserving keys, then the tokens at or above the M-th key sorted
-//   by key and id); then the same CTA sorts the tree's F x M candidates by
-//   score (float pairs), node and token and keeps M.
+//   by key and id); then one CTA per tree sorts the tree's F x M candidates
+//   by score (float pairs), node and token and keeps M.
 #include "select.cuh"
 
 namespace specv {
@@ -113,7 +113,9 @@ __device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int
 constexpr int kMergeCap = 2048;  // F x M candidates held in shared memory (32 KB)
 
 // Tree b's F x M candidates, scored and ranked: higher score, then lower
-// node, then lower token; the first M kept. s_c: kMergeCap entries.
+// node, then lower token; the first M kept. Each row's M candidates arrive
+// sorted in that order, so for F <= 32 one warp merges the rows' heads;
+// otherwise the block sorts all F x M. s_c: kMergeCap entries.
 __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
   const int tid = threadIdx.x;
   const int F = a.F, Mk = a.M, n = F * Mk;
@@ -123,6 +125,52 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
     const float lc = a.logc[static_cast<long long>(b) * F + f];
     const int fl = a.row_flag[static_cast<long long>(b) * F + f] | ((lc != lc || lc == INFINITY) ? SPEC_ROW_DRAFT : 0);
     if (fl) atomicOr(s_st, fl);
+  }
+  if (F <= 32) {  // every row's candidates are sorted already: one warp merges the F heads
+    for (int i = tid; i < n; i += kSelThreads) {
+      const int f = i / Mk;
+      Cand c = static_cast<const Cand*>(a.cand)[static_cast<long long>(b) * n + i];
+      c.f = f;
+      const float2 sc = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
+      c.hi = sc.x > -INFINITY ? sc.x : -INFINITY;
+      c.lo = sc.x > -INFINITY ? sc.y : 0.f;
+      if (c.v < 0) c = Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};  // a slot past the vocabulary
+      s_c[i] = c;
+    }
+    __syncthreads();
+    const int st = *s_st;
+    if (tid < 32) {
+      const int lane = tid;
+      int head = 0;
+      for (int i = 0; i < Mk; ++i) {
+        Cand best{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
+        if (lane < F && head < Mk) best = s_c[lane * Mk + head];
+        int who = lane;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          Cand oc;
+          oc.hi = __shfl_xor_sync(0xffffffffu, best.hi, o);
+          oc.lo = __shfl_xor_sync(0xffffffffu, best.lo, o);
+          oc.f = __shfl_xor_sync(0xffffffffu, best.f, o);
+          oc.v = __shfl_xor_sync(0xffffffffu, best.v, o);
+          const int ow = __shfl_xor_sync(0xffffffffu, who, o);
+          if (cand_before(oc, best) || (!cand_before(best, oc) && ow < who)) {
+            best = oc;
+            who = ow;
+          }
+        }
+        if (lane == who) ++head;
+        if (lane == 0) {
+          const long long o = static_cast<long long>(b) * Mk + i;
+          const bool ok = !st && best.v != 0x7fffffff;
+          a.parent[o] = ok ? best.f : -1;
+          a.token[o] = ok ? best.v : -1;
+          a.score[o] = ok ? best.hi + best.lo : NAN;
+        }
+      }
+      if (lane == 0) a.row_status[b] = st;
+    }
+    return;
   }
   int n2 = 1;
   while (n2 < n) n2 <<= 1;
@@ -170,13 +218,13 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
   if (tid == 0) a.row_status[b] = st;
 }
 
-// One CTA per tree: its frontier rows eight at a time (one warp each, or the
-// whole CTA for a row without a short complete list), then the merge.
+// Eight frontier rows per CTA: one warp each, or the whole CTA for a row
+// with too many candidates or no lane maxima.
 template <typename Raw, bool VEC>
-__global__ void __launch_bounds__(kSelThreads, 2) expand_tree_kernel(ExpArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 2) expand_rows_kernel(ExpArgs a) {
   using KY = Key<Raw>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x;
+  const int rows = a.B * a.F;
   __shared__ __align__(16) uint32_t s_buf[2 * kCand];
   unsigned* hist = s_buf;
   uint32_t* s_key = s_buf;
@@ -189,7 +237,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) expand_tree_kernel(ExpArgs a) 
   __shared__ float s_M, s_t0;
   __shared__ float2 s_lz;
   __shared__ int s_slow[kSelWarps];
-  __shared__ int s_st;
   griddep_launch_dependents();
   griddep_wait();
   // a row by the whole CTA
@@ -299,23 +346,27 @@ __global__ void __launch_bounds__(kSelThreads, 2) expand_tree_kernel(ExpArgs a) 
   if (tid == 0) a.row_flag[row_id] = st;
   };
   static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 8) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
-  static_assert(kMergeCap * sizeof(Cand) <= sizeof(uint32_t) * 2 * kCand, "merge buffer fits");
   uint64_t* wl = reinterpret_cast<uint64_t*>(s_buf);
   int* wc = reinterpret_cast<int*>(wl + kSelWarps * kWarpList);
   float* wm = reinterpret_cast<float*>(wc + kSelWarps * kChunkCap);
-  for (int r0 = 0; r0 < a.F; r0 += kSelWarps) {
-    {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
-      const int r = r0 + warp;
-      const bool done = r >= a.F || expand_list_row<Raw, VEC>(a, b * a.F + r, wl + warp * kWarpList,
-                                                               wc + warp * kChunkCap, wm + warp * kChunkCap, lane);
-      if (lane == 0) s_slow[warp] = !done;
-    }
-    __syncthreads();
-    for (int w = 0; w < kSelWarps; ++w)
-      if (s_slow[w]) cta_row(b * a.F + r0 + w);
-    __syncthreads();
+  {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
+    const int row_id = blockIdx.x * kSelWarps + warp;
+    const bool done = row_id >= rows || expand_list_row<Raw, VEC>(a, row_id, wl + warp * kWarpList,
+                                                                  wc + warp * kChunkCap, wm + warp * kChunkCap, lane);
+    if (lane == 0) s_slow[warp] = !done;
   }
-  merge_tree(a, b, reinterpret_cast<Cand*>(s_buf), &s_st);  // the rows' candidates are visible after the barrier
+  __syncthreads();
+  for (int w = 0; w < kSelWarps; ++w)
+    if (s_slow[w]) cta_row(blockIdx.x * kSelWarps + w);
+}
+
+// One CTA per tree: the merge of its F x M candidates.
+__global__ void __launch_bounds__(kSelThreads) expand_merge_kernel(ExpArgs a) {
+  __shared__ Cand s_c[kMergeCap];
+  __shared__ int s_st;
+  griddep_launch_dependents();
+  griddep_wait();  // the rows' candidates come from expand_rows_kernel
+  merge_tree(a, blockIdx.x, s_c, &s_st);
 }
 
 }  // namespace
@@ -327,12 +378,16 @@ int expand_limits(int* max_m, int* max_fm) {
 }
 
 cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st) {
-  const dim3 g(static_cast<unsigned>(a.B));
+  const dim3 g(static_cast<unsigned>((static_cast<long long>(a.B) * a.F + kSelWarps - 1) / kSelWarps));
+  cudaError_t e;
   if (dtype == SPEC_BF16)
-    return vec ? launch_pdl(expand_tree_kernel<uint16_t, true>, g, dim3(kSelThreads), st, a)
-               : launch_pdl(expand_tree_kernel<uint16_t, false>, g, dim3(kSelThreads), st, a);
-  return vec ? launch_pdl(expand_tree_kernel<float, true>, g, dim3(kSelThreads), st, a)
-             : launch_pdl(expand_tree_kernel<float, false>, g, dim3(kSelThreads), st, a);
+    e = vec ? launch_pdl(expand_rows_kernel<uint16_t, true>, g, dim3(kSelThreads), st, a)
+            : launch_pdl(expand_rows_kernel<uint16_t, false>, g, dim3(kSelThreads), st, a);
+  else
+    e = vec ? launch_pdl(expand_rows_kernel<float, true>, g, dim3(kSelThreads), st, a)
+            : launch_pdl(expand_rows_kernel<float, false>, g, dim3(kSelThreads), st, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(expand_merge_kernel, dim3(static_cast<unsigned>(a.B)), dim3(kSelThreads), st, a);
 }
 
 }  // namespace specv
