@@ -182,10 +182,12 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logit
  * plus temperature > 0, top_k >= 0, 0 < top_p <= 1. Workspace:
  * spec_workspace_bytes(B, K, V, dtype) bytes suffice; with
  * spec_warped_workspace_bytes(B, K, V, dtype) bytes, and top_k at most the
- * number of 4 KB segments of a row (63 for V = 128256 bf16), a filter pass
- * lists each row's candidates for its top-k in the workspace and the
- * selection reads only those lists (one extra pass over the rows in all).
- * Otherwise the extra passes are: for top_k <= 256, one filtering the row
+ * number of 4 KB segments of a row (63 for V = 128256 bf16), the stats pass
+ * also keeps every lane's maximum (32 per segment) in the workspace, and a
+ * row's top-k candidates are reread from the few lanes whose maximum
+ * reaches the row's bound: no extra pass over the rows (rows with more than
+ * 256 candidates fall back as below). Otherwise the extra passes are: for
+ * top_k <= 256, one filtering the row
  * (ties overflowing its buffers: as for larger top_k); for larger top_k,
  * 2 (bf16) or 4 (fp32) radix passes; for top-p alone (or top-k sets of
  * more than 4096 tokens), 2 / 4 more to find the row's largest tokens (at
@@ -303,11 +305,12 @@ int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, in
  * tokens of one node tie at its M-th largest logit; such a row's outputs
  * are all -1 / NaN. Scores are exact to about 1e-6 (the normaliser's fp32
  * exponentials); candidates of one node rank exactly by logit. Passes over
- * each frontier row: one for the softmax statistics, then (M < V) one
- * filter pass listing the elements at or above the M-th largest segment
- * maximum when M is at most the number of 4 KB segments of a row, or one
- * filtering pass of the per-row selection for M <= 256, or 2 (bf16) / 4
- * (fp32) radix passes and one collecting the top M otherwise. */
+ * each frontier row: one for the softmax statistics (which also keeps
+ * every lane's maximum); then, when M < V and M is at most the number of 4
+ * KB segments of a row, only the lanes whose maximum reaches the row's M-th
+ * largest segment maximum are reread; otherwise (or with more than 256
+ * candidates) one filtering pass for M <= 256, or 2 (bf16) / 4 (fp32) radix
+ * passes and one collecting the top M. */
 size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype);
 int spec_tree_expand(const void* draft_logits, int dtype, float temperature, const float* logc, int B, int F, int V,
                      int M, int32_t* parent, int32_t* token, float* score, int32_t* row_status, void* workspace,

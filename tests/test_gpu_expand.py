@@ -118,9 +118,10 @@ def test_expand_segment_bound_and_fallback():
 
 @pytest.mark.parametrize("M", [1, 31, 40, 63])
 def test_expand_list_sizes(M):
-    """M up to the 63 stats segments of a 128256-token bf16 row: candidate
-    lists of a few to a few hundred entries, selected by one warp when they
-    hold at most 256, else by the whole CTA."""
+    """M up to the 63 stats segments of a 128256-token bf16 row: a few to a
+    few hundred candidates reread from the lanes whose maximum reaches the
+    bound, selected by one warp when they are at most 256, else by the whole
+    CTA."""
     Ld, logc = gen.expand_frontier(2, 4, 128256, torch.bfloat16, seed=M)
     compare(*run(Ld, logc, M), M, 1.0)
 
