@@ -656,23 +656,32 @@ __device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, f
       const int f = f0 + 32 * r + lane;
       v[r] = f < nf4 ? __ldcg(l4 + f) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
+    // each lane's hits as a bit mask, placed by one warp scan
+    unsigned hits = 0;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const bool hit = x[c] >= t0;
-        const unsigned bm = __ballot_sync(0xffffffffu, hit);
-        if (hit) {
-          const int p = nc + __popc(bm & below);
+      for (int c = 0; c < 4; ++c)
+        if (x[c] >= t0) hits |= 1u << (4 * r + c);
+    }
+    const int cnt = __popc(hits);
+    const int incl = warp_incl_scan(cnt, lane);
+    int p = nc + incl - cnt;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if ((hits >> (4 * r + c)) & 1u) {
           if (p < kChunkCap) {
             chunks[p] = 4 * (f0 + 32 * r + lane) + c;
             cmax[p] = x[c];
           }
+          ++p;
         }
-        nc += __popc(bm);
-      }
     }
+    nc += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (nc > kChunkCap || nc < k) return -1;
   __syncwarp();
