@@ -49,6 +49,10 @@ def test_workspace_sizes(lib):
     assert lib.spec_workspace_bytes(0, 8, 128256, 1) == 0
     assert lib.spec_workspace_bytes(1, 300, 100, 1) == 0
     assert lib.spec_workspace_bytes(1, 1, 1, 1) == 0
+    # the warped chain's larger workspace adds the lane maxima (32 floats per 4 KB segment and row)
+    plain, warped = lib.spec_workspace_bytes(64, 8, 128256, 1), lib.spec_warped_workspace_bytes(64, 8, 128256, 1)
+    assert warped >= plain + 64 * 17 * 63 * 32 * 4 and warped % 256 == 0
+    assert lib.spec_warped_workspace_bytes(0, 8, 128256, 1) == 0
 
 
 def test_host_validation_rejects_bad_arguments(lib):

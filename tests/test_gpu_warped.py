@@ -124,6 +124,24 @@ def test_warped_segment_bound_and_fallback(top_k, top_p):
     compare(*run(c, top_k, top_p), allow_warp=True)
 
 
+@pytest.mark.parametrize("top_k,top_p", [(50, 0.9), (10, 1.0)])
+def test_warped_plain_workspace(top_k, top_p):
+    """With only spec_workspace_bytes of workspace the stats pass keeps no
+    lane maxima and every row is selected by a whole CTA (the filtering pass
+    over the row): the same results."""
+    import speculative_decoding_verification_29_gb300 as sv
+
+    c = gen.chain_zipf(8, 4, 128256, torch.bfloat16, 0.7, 0.8, seed=11, draft_top_k=top_k)
+    dev = torch.device("cuda")
+    ws = sv.alloc_workspace(sv.workspace_bytes(c.B, c.K, c.V, c.Lp.dtype), dev)
+    assert sv.workspace_bytes(c.B, c.K, c.V, c.Lp.dtype) < sv.warped_workspace_bytes(c.B, c.K, c.V, c.Lp.dtype)
+    g = sv.spec_verify_chain_warped(c.Lp.to(dev), c.Lq.to(dev), c.x.to(dev), c.ua.to(dev), c.ur.to(dev), c.T,
+                                    top_k=top_k, top_p=top_p, workspace=ws)
+    torch.cuda.synchronize()
+    o = oracle.verify_chain_warped(c.Lp, c.Lq, c.x, c.ua, c.ur, c.T, top_k, top_p, threads=8)
+    compare({k: np_(v) for k, v in g.items()}, o)
+
+
 def test_warped_serving_batch():
     """B=64, K=8, V=128256 bf16, T=0.7 (the batched serving workload) with
     top-k 50 and top-p 0.9 on both models."""
