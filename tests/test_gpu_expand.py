@@ -126,6 +126,15 @@ def test_expand_list_sizes(M):
     compare(*run(Ld, logc, M), M, 1.0)
 
 
+@pytest.mark.parametrize("dtype,V", [(torch.float32, 152064), (torch.bfloat16, 600000)])
+def test_expand_large_vocab(dtype, V):
+    """fp32 rows of 149 stats segments (lane maxima held eight per lane) and
+    bf16 rows of 293 segments (more than 256: no lane maxima, every row
+    selected by a whole CTA)."""
+    Ld, logc = gen.expand_frontier(2, 3, V, dtype, seed=V % 7)
+    compare(*run(Ld, logc, 12), 12, 1.0)
+
+
 def test_expand_more_slots_than_children():
     """M >= V and M > F * V: every child is kept, the remaining slots are
     -1 / NaN."""

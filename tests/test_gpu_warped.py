@@ -124,6 +124,14 @@ def test_warped_segment_bound_and_fallback(top_k, top_p):
     compare(*run(c, top_k, top_p), allow_warp=True)
 
 
+@pytest.mark.parametrize("dtype,V", [(torch.float32, 152064), (torch.bfloat16, 600000)])
+def test_warped_large_vocab(dtype, V):
+    """fp32 rows of 149 stats segments and bf16 rows of 293 (no lane maxima:
+    every row selected by a whole CTA), top-k 40, top-p 0.9."""
+    c = gen.chain_zipf(3, 2, V, dtype, 0.9, 0.6, seed=V % 5, draft_top_k=40)
+    compare(*run(c, 40, 0.9))
+
+
 @pytest.mark.parametrize("top_k,top_p", [(50, 0.9), (10, 1.0)])
 def test_warped_plain_workspace(top_k, top_p):
     """With only spec_workspace_bytes of workspace the stats pass keeps no
