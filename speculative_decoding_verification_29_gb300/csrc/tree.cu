@@ -49,28 +49,28 @@ __global__ void __launch_bounds__(kTreeThreads) tree_finish_kernel(TreeArgs a) {
                    SPEC_ROW_TARGET);
   for (int i = 1 + tid; i < N; i += kTreeThreads)
     if (s_tok[i] < 0 || s_tok[i] >= a.V) atomicOr(&s_st, SPEC_ROW_TOKEN);
-  for (int r = tid; r < Rn; r += kTreeThreads) {
-    const int32_t* row = Rs + static_cast<long long>(r) * D;
+  // every (row, step) entry checked on its own thread: a step is malformed
+  // when an earlier step of its row is -1 or it lies outside 1..N-1, and
+  // must otherwise be a child of the previous node in the mask; a row that
+  // starts with -1 must be all -1
+  for (int e = tid; e < Rn * D; e += kTreeThreads) {
+    const int r = e / D, t = e - r * D;
+    const int nd = Rs[e];
+    const int r0 = Rs[static_cast<long long>(r) * D];
     int bad = 0;
-    if (row[0] == -1) {
-      for (int t = 1; t < D; ++t)
-        if (row[t] != -1) bad |= SPEC_ROW_TREE;
-    } else {
-      atomicOr(&s_any, 1);
-      if (row[0] != 0) bad |= SPEC_ROW_TREE;
-      bool ended = false;
-      for (int t = 1; t < D; ++t) {
-        int nd = row[t];
-        if (nd == -1) {
-          ended = true;
-          continue;
-        }
-        if (ended || nd <= 0 || nd >= N) {
-          bad |= SPEC_ROW_TREE;
-          continue;
-        }
-        int pv = row[t - 1];
-        if (a.mask && pv >= 0 && pv < N && !a.mask[(static_cast<long long>(b) * N + nd) * N + pv]) bad |= SPEC_ROW_MASK;
+    if (t == 0) {
+      if (nd != -1) {
+        atomicOr(&s_any, 1);
+        if (nd != 0) bad |= SPEC_ROW_TREE;
+      }
+    } else if (nd != -1) {
+      bool ended = r0 == -1;  // an earlier -1 in the row (the row's own entries, staged)
+      for (int u = 1; u < t && !ended; ++u) ended = Rs[static_cast<long long>(r) * D + u] == -1;
+      const int pv = Rs[e - 1];
+      if (ended || nd <= 0 || nd >= N) {
+        bad |= SPEC_ROW_TREE;
+      } else if (a.mask && pv >= 0 && pv < N && !a.mask[(static_cast<long long>(b) * N + nd) * N + pv]) {
+        bad |= SPEC_ROW_MASK;
       }
     }
     if (bad) atomicOr(&s_st, bad);
