@@ -183,9 +183,10 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logit
  * spec_workspace_bytes(B, K, V, dtype) bytes suffice; with
  * spec_warped_workspace_bytes(B, K, V, dtype) bytes, and top_k at most the
  * number of 4 KB segments of a row (63 for V = 128256 bf16), the stats pass
- * also keeps every lane's maximum (32 per segment) in the workspace, and a
- * row's top-k candidates are reread from the few lanes whose maximum
- * reaches the row's bound: no extra pass over the rows (rows with more than
+ * also keeps, for each of the 32 lanes of a segment, the maxima of the two
+ * halves of the lane's elements in the workspace, and a row's top-k
+ * candidates are reread from the few half-lanes whose maximum reaches the
+ * row's bound: no extra pass over the rows (rows with more than
  * 256 candidates fall back as below). Otherwise the extra passes are: for
  * top_k <= 256, one filtering the row
  * (ties overflowing its buffers: as for larger top_k); for larger top_k,
@@ -306,9 +307,9 @@ int spec_tree_entropy(const void* draft_logits, int dtype, float temperature, in
  * are all -1 / NaN. Scores are exact to about 1e-6 (the normaliser's fp32
  * exponentials); candidates of one node rank exactly by logit. Passes over
  * each frontier row: one for the softmax statistics (which also keeps
- * every lane's maximum); then, when M < V and M is at most the number of 4
- * KB segments of a row, only the lanes whose maximum reaches the row's M-th
- * largest segment maximum are reread; otherwise (or with more than 256
+ * the maxima of every lane's two halves); then, when M < V and M is at
+ * most the number of 4 KB segments of a row, only the half-lanes whose
+ * maximum reaches the row's M-th largest segment maximum are reread; otherwise (or with more than 256
  * candidates) one filtering pass for M <= 256, or 2 (bf16) / 4 (fp32) radix
  * passes and one collecting the top M. */
 size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype);

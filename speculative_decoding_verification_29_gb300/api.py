@@ -50,9 +50,9 @@ def workspace_bytes(B: int, K: int, V: int, dtype) -> int:
 
 
 def warped_workspace_bytes(B: int, K: int, V: int, dtype) -> int:
-    """Workspace with room for the stats pass's lane maxima, which let
-    spec_verify_chain_warped select top-k sets without a second pass over
-    the rows (workspace_bytes suffices, but is slower)."""
+    """Workspace with room for the stats pass's lane records (half-lane
+    maxima), which let spec_verify_chain_warped select top-k sets without a
+    second pass over the rows (workspace_bytes suffices, but is slower)."""
     code = dtype if isinstance(dtype, int) else (SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32)
     return int(_lib.load().spec_warped_workspace_bytes(B, K, V, code))
 

@@ -43,8 +43,9 @@ char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 // row, sized for the larger of the vector and scalar load paths so that the
 // size depends only on the shapes, never on pointer alignment; then, for the
 // sampling settings, one record, threshold and flag per row; and, for the
-// top-k paths, every lane's maximum from the stats pass (32 floats per
-// segment).
+// top-k paths, the stats pass's lane records (32 per segment: the maxima of
+// the two halves of each lane's elements, 4 bytes for bf16 rows, 8 for
+// fp32).
 struct Layout {
   size_t part, rec, vtau, flag, lanes, total;
 };
@@ -63,12 +64,12 @@ Layout layout(int B, int TR, int DR, int V, int dtype, bool lanes = false) {
   L.flag = off;
   off += up256(static_cast<size_t>(nrows) * sizeof(int32_t));
   L.lanes = off;
-  if (lanes) off += up256(static_cast<size_t>(nrows * P) * 32 * sizeof(float));
+  if (lanes) off += up256(static_cast<size_t>(nrows * P) * 32 * sizeof(float) * lane_words(dtype == SPEC_BF16));
   L.total = off;
   return L;
 }
 
-// The lane maxima serve a top-k when k is at most the number of stats
+// The lane records serve a top-k when k is at most the number of stats
 // segments (so that the segment maxima bound the k-th largest logit).
 bool lanes_fit(int k, int P) { return k > 0 && k <= P && P <= 256; }
 
@@ -155,7 +156,7 @@ struct ChainCall {
   float top_p = 1.f;
 };
 
-// The lane maxima of the stats pass, when the warped call's workspace holds
+// The lane records of the stats pass, when the warped call's workspace holds
 // them and they serve its top-k; NULL otherwise.
 float* chain_lanes(const ChainCall& c, int P) {
   const Layout Lx = layout(c.B, c.K + 1, c.K, c.V, c.dtype, true);
@@ -437,7 +438,8 @@ size_t spec_expand_workspace_bytes(int B, int F, int V, int M, int dtype) {
   const long long rows = static_cast<long long>(B) * F;
   const long long P = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
   return up256(static_cast<size_t>(rows * P) * sizeof(float2)) + up256(static_cast<size_t>(rows * M) * 16) +
-         up256(static_cast<size_t>(rows) * sizeof(int32_t)) + up256(static_cast<size_t>(rows * P) * 32 * sizeof(float));
+         up256(static_cast<size_t>(rows) * sizeof(int32_t)) +
+         up256(static_cast<size_t>(rows * P) * 32 * sizeof(float) * lane_words(dtype == SPEC_BF16));
 }
 
 int spec_tree_expand(const void* draft_logits, int dtype, float temperature, const float* logc, int B, int F, int V,
@@ -466,7 +468,7 @@ int spec_tree_expand(const void* draft_logits, int dtype, float temperature, con
   a.part = static_cast<float2*>(workspace);
   const long long Pmax = std::max(scan_chunks(V, true, dtype), scan_chunks(V, false, dtype));
   size_t off = up256(static_cast<size_t>(rows * Pmax) * sizeof(float2));
-  // the lane maxima at the end of the workspace
+  // the lane records at the end of the workspace
   const size_t loff =
       off + up256(static_cast<size_t>(rows * M) * 16) + up256(static_cast<size_t>(rows) * sizeof(int32_t));
   const int take = M < V ? M : V;

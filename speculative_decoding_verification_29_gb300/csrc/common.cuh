@@ -171,6 +171,19 @@ struct Vec<uint16_t> {
     uint32_t w = max_nan_bf16x2(max_nan_bf16x2(v.x, v.y), max_nan_bf16x2(v.z, v.w));
     return fmax_nan(bf16_lo(w), bf16_hi(w));
   }
+  // maximum over the elements of N consecutive vectors: reduced as packed
+  // pairs in a tree, one conversion at the end
+  template <int N>
+  __device__ static __forceinline__ float vmax_n(const uint4* v) {
+    uint32_t w[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = max_nan_bf16x2(max_nan_bf16x2(v[i].x, v[i].y), max_nan_bf16x2(v[i].z, v[i].w));
+#pragma unroll
+    for (int s = 1; s < N; s <<= 1)
+#pragma unroll
+      for (int i = 0; i + s < N; i += 2 * s) w[i] = max_nan_bf16x2(w[i], w[i + s]);
+    return fmax_nan(bf16_lo(w[0]), bf16_hi(w[0]));
+  }
   __device__ static __forceinline__ float2 pair(const uint4& v, int i) {
     uint32_t w = i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
     return bf16x2_to_float2(w);
@@ -184,6 +197,17 @@ struct Vec<float> {
   __device__ static __forceinline__ float vmax(const uint4& v) {
     return max3_nan(max3_nan(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z)),
                     __uint_as_float(v.w), __uint_as_float(v.w));
+  }
+  template <int N>
+  __device__ static __forceinline__ float vmax_n(const uint4* v) {
+    float m[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) m[i] = vmax(v[i]);
+#pragma unroll
+    for (int s = 1; s < N; s <<= 1)
+#pragma unroll
+      for (int i = 0; i + s < N; i += 2 * s) m[i] = fmax_nan(m[i], m[i + s]);
+    return m[0];
   }
   __device__ static __forceinline__ float2 pair(const uint4& v, int i) {
     return i == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))

@@ -79,6 +79,9 @@ __device__ void expand_sorted(const ExpArgs& a, int row_id, const uint64_t* buf,
 template <typename Raw, bool VEC>
 __device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int* chunks, float* cmax, int lane) {
   if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
+  const float* lanes = a.lanes + static_cast<long long>(row_id) * a.P * 32 * lane_words(sizeof(Raw) == 2);
+  uint4 lv[8];  // the first lane records, in flight while the bound is formed
+  lane_records_first<Raw>(lanes, a.P, lane, lv);
   float2 q[8];
   load_parts<8>(a.part + static_cast<long long>(row_id) * a.P, a.P, lane, q);
   float2 z;
@@ -95,8 +98,7 @@ __device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int
   for (int i = 0; i < 8; ++i) sm[i] = q[i].x;
   const float t0 = seg_bound_regs<8>(sm, a.P, a.M, lane);
   const Raw* row = static_cast<const Raw*>(a.L) + static_cast<long long>(row_id) * a.V;
-  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, a.M,
-                                        buf, chunks, cmax, lane);
+  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, lanes, lv, t0, a.M, buf, chunks, cmax, lane);
   if (n < a.M) return false;  // too many candidates
   const float2 lz = ln_of(z);
   if (n <= 32)

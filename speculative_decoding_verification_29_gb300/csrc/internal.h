@@ -12,7 +12,7 @@ namespace specv {
 constexpr int kModeStats = 0;   // rowscan: (max, sum of exp) per row
 constexpr int kModeArgmax = 1;  // rowscan: (value, index) of the row maximum
 constexpr int kModeEntropy = 2; // rowscan: (max, sum of exp, sum of exp * (l - max)) per row, float4 partials
-constexpr int kModeStatsLanes = 3;  // rowscan: as kModeStats, and each lane's maximum (the top-k paths)
+constexpr int kModeStatsLanes = 3;  // rowscan: as kModeStats, and each lane's two half maxima (the top-k paths)
 constexpr int kMaxK = 255;
 
 // rowscan geometry: each warp reduces one segment of kSegChunks chunks of kWV
@@ -23,6 +23,14 @@ constexpr int kSegChunks = 1;
 constexpr int kScalarPerLane = 64;
 constexpr int kScanWarps = 8;
 constexpr int kScanThreads = kScanWarps * 32;
+
+// Lane records of kModeStatsLanes, [rows][P][32], one per warp lane and
+// segment: the maxima of the lane's first and second half of elements (its
+// vectors 0 .. kWV/2 - 1 and kWV/2 .. kWV - 1, or on the scalar path its
+// first and last kScalarPerLane / 2 elements). bf16 rows pack both bf16
+// values into one 32-bit word (first half in the low 16 bits), fp32 rows
+// store a float pair: the record takes this many 32-bit words.
+__host__ __device__ constexpr int lane_words(bool bf16) { return bf16 ? 1 : 2; }
 
 // tail: threads per CTA (a cluster of CTAs serves one batch row)
 constexpr int kResThreads = 256;
@@ -63,7 +71,7 @@ struct ScanArgs {
   int P;             // chunks (partials) per row
   float c_hi, c_lo;  // log2(e) / T as a float pair, c_lo > 0
   float2* part;      // [B * (TR + DR)][P]
-  float* lanes;      // kModeStatsLanes: [B * (TR + DR)][P][32] each lane's maximum over its elements
+  float* lanes;      // kModeStatsLanes: the lane records [B * (TR + DR)][P][32] (raw words)
 };
 
 
@@ -152,7 +160,7 @@ struct SelArgs {
   StatRec* rec;        // [rows]: M, kept mass Z', log2 Z'
   float* vtau;         // [rows]: a token is kept iff its logit >= vtau
   int32_t* row_flag;   // [rows]: SPEC_ROW_WARP or 0
-  const float* lanes;  // the stats pass's lane maxima [rows][P][32] (NULL: none)
+  const float* lanes;  // the stats pass's lane records [rows][P][32] (NULL: none)
 };
 int select_candidates();
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st);
@@ -171,7 +179,7 @@ struct ExpArgs {
   int32_t* token;       // [B][M]
   float* score;         // [B][M]
   int32_t* row_status;  // [B]
-  const float* lanes;   // the stats pass's lane maxima [B * F][P][32] (NULL: none)
+  const float* lanes;   // the stats pass's lane records [B * F][P][32] (NULL: none)
 };
 int expand_limits(int* max_m, int* max_fm);
 cudaError_t launch_expand(const ExpArgs& a, int dtype, bool vec, cudaStream_t st);

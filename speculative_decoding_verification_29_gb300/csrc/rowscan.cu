@@ -17,10 +17,10 @@
 //   entropy (drafter trees): (m, z, y) with y = sum 2^((l - m) log2(e) / T)
 //          (l - m), from which a row's softmax entropy follows (TAPS page:
 //          entropy routing of drafter trees);
-//   stats + lanes (top-k): as stats, and every lane's maximum over its own
-//          elements (8 sixteen-byte vectors, 32 vectors apart), so that a
-//          top-k selection can reread only the lanes whose maximum reaches
-//          its bound.
+//   stats + lanes (top-k): as stats, and for every lane the maxima of the
+//          two halves of its own elements (4 + 4 sixteen-byte vectors, 32
+//          vectors apart), so that a top-k selection can reread only the
+//          half-lanes whose maximum reaches its bound.
 // The max runs on packed bf16 pairs, the exponent arithmetic on packed fp32
 // pairs (f32x2) with one accumulator per pair lane; a lane's running sum is
 // rescaled (exp2f, correctly rounded to within an ulp) when its running max
@@ -51,6 +51,16 @@ __device__ __forceinline__ int kind_to_row(const ScanArgs& a, int q) {
   const int K = a.TR - 1;
   const int k = K - ((q + 1) >> 1);
   return q == 0 ? K : ((q & 1) ? k : a.TR + k);
+}
+
+// The lane record: the maxima of the lane's two halves (bf16 rows: both as
+// bf16 in one word, the first half low; fp32 rows: a float pair).
+template <typename Raw>
+__device__ __forceinline__ void store_halves(float* lanes, long long slot, float lo, float hi) {
+  if constexpr (sizeof(Raw) == 2)
+    reinterpret_cast<uint32_t*>(lanes)[slot] = (__float_as_uint(hi) & 0xFFFF0000u) | (__float_as_uint(lo) >> 16);
+  else
+    reinterpret_cast<float2*>(lanes)[slot] = make_float2(lo, hi);
 }
 
 template <typename Raw>
@@ -99,9 +109,21 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
           const int vi = v0 + (g * kWV + t) * 32;
           raw[t] = vi < nv ? ld_stream_v4(row + static_cast<long long>(vi) * EPV) : neg;
         }
-        float m = -INFINITY;
+        float m;
+        if constexpr (MODE == kModeStatsLanes) {
+          static_assert(kSegChunks == 1 && kWV % 2 == 0, "a lane record covers one chunk in two halves");
+          float mlo = -INFINITY, mhi = -INFINITY;
 #pragma unroll
-        for (int t = 0; t < kWV; ++t) m = fmax_nan(m, Vt::vmax(raw[t]));
+          for (int t = 0; t < kWV / 2; ++t) {
+            mlo = fmax_nan(mlo, Vt::vmax(raw[t]));
+            mhi = fmax_nan(mhi, Vt::vmax(raw[t + kWV / 2]));
+          }
+          store_halves<Raw>(a.lanes, ((static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg) * 32 + lane, mlo,
+                            mhi);
+          m = fmax_nan(mlo, mhi);
+        } else {
+          m = Vt::template vmax_n<kWV>(raw);
+        }
         const float mnew = fmax_nan(mrun, m);
         if (mnew != -INFINITY) {  // NaN and +inf propagate into the partial (the row is flagged)
           const float sc = exp2f(scale_c(mrun - mnew, a.c_hi, a.c_lo));  // 0 when mrun = -inf
@@ -132,8 +154,6 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
         yac[0] = add2(yac[0], yac[i]);
       }
       float z = acc[0].x + acc[0].y, y = yac[0].x + yac[0].y;
-      if constexpr (MODE == kModeStatsLanes)
-        a.lanes[((static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg) * 32 + lane] = mrun;
       M = warp_max_nan(mrun);
       if (M == M && M != -INFINITY) {
         if (mrun == -INFINITY) {
@@ -193,11 +213,16 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
       const long long vi = v0 + t * 32;
       e[t] = vi < a.V ? Elem<Raw>::at(row, vi) : -INFINITY;
     }
-    float m = -INFINITY;
+    float mh[2] = {-INFINITY, -INFINITY};  // the maxima of the lane's two halves
 #pragma unroll
-    for (int t = 0; t < kScalarPerLane; ++t) m = fmax_nan(m, e[t]);
+    for (int t = 0; t < kScalarPerLane; ++t) {
+      const int h = 2 * t >= kScalarPerLane;
+      mh[h] = fmax_nan(mh[h], e[t]);
+    }
+    const float m = fmax_nan(mh[0], mh[1]);
     if constexpr (MODE == kModeStatsLanes)
-      a.lanes[((static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg) * 32 + lane] = m;
+      store_halves<Raw>(a.lanes, ((static_cast<long long>(b) * (a.TR + a.DR) + j) * a.P + seg) * 32 + lane, mh[0],
+                        mh[1]);
     M = warp_max_nan(m);
     if constexpr (MODE != kModeArgmax) {
       float z = 0.f, y = 0.f;

@@ -141,6 +141,9 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
 template <typename Raw, bool VEC>
 __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int* chunks, float* cmax, int lane) {
   if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
+  const float* lanes = a.lanes + static_cast<long long>(row_id) * a.P * 32 * lane_words(sizeof(Raw) == 2);
+  uint4 lv[8];  // the first lane records, in flight while the bound is formed
+  lane_records_first<Raw>(lanes, a.P, lane, lv);
   float2 q[8];
   load_parts<8>(a.part + static_cast<long long>(row_id) * a.P, a.P, lane, q);
   float2 z;
@@ -166,8 +169,7 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
   const int b = row_id / RPG, j = row_id - b * RPG;
   const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
                             : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
-  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, a.lanes + static_cast<long long>(row_id) * a.P * 32, t0, a.top_k,
-                                        buf, chunks, cmax, lane);
+  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, lanes, lv, t0, a.top_k, buf, chunks, cmax, lane);
   if (n < a.top_k) return false;  // too many candidates
   if (n <= 32)
     warped_sorted<Raw, 1>(a, row_id, buf, n, M, lane);
@@ -181,7 +183,7 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
 }
 
 template <typename Raw, bool VEC>
-__global__ void __launch_bounds__(kSelThreads, 4) warp_select_kernel(SelArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) {
   using KY = Key<Raw>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int RPG = a.TR + a.DR;

@@ -616,7 +616,7 @@ __device__ __forceinline__ uint64_t warp_entry(const uint64_t (&r)[NR], int e) {
 
 // ------------------------------------------------ rereading the top lanes --
 
-constexpr int kChunkCap = 256;  // lanes of the stats pass one warp considers for a row
+constexpr int kChunkCap = 256;  // half-lanes of the stats pass one warp considers for a row
 
 // The row's stats partials, P <= 32 NV: segment lane + 32 i in q[i]
 // (padding (-inf, 0)); one round trip.
@@ -629,70 +629,100 @@ __device__ __forceinline__ void load_parts(const float2* pr, int P, int lane, fl
   }
 }
 
+// The value of half h of a lane record word (bf16 rows: two bf16 maxima per
+// word, the first half low; fp32 rows: one float per half).
+template <typename Raw>
+__device__ __forceinline__ float half_value(uint32_t w, int h) {
+  if constexpr (sizeof(Raw) == 2) return __uint_as_float(h ? (w & 0xFFFF0000u) : (w << 16));
+  return __uint_as_float(w);
+}
+
+// The first round of a row's lane records: eight 16-byte loads per lane,
+// issued before the row's bound is known (padding: -inf in every half).
+template <typename Raw>
+__device__ __forceinline__ void lane_records_first(const float* lanes, int P, int lane, uint4 (&v)[8]) {
+  const int nf4 = P * 8 * lane_words(sizeof(Raw) == 2);
+  const uint32_t pad = sizeof(Raw) == 2 ? 0xFF80FF80u : 0xFF800000u;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int f = 32 * r + lane;
+    v[r] = f < nf4 ? __ldcg(reinterpret_cast<const uint4*>(lanes) + f) : make_uint4(pad, pad, pad, pad);
+  }
+}
+
 // The row's candidates for its k largest elements as composites in
-// buf[0, n). t0 (a lower bound of the k-th largest value, from the segment
-// maxima) picks the lanes of the stats pass whose maximum (lanes: the row's
-// P x 32 lane maxima) is >= t0; when more than 32 do, the k-th largest of
-// those maxima, t1, is a tighter bound (k lanes hold an element >= t1) and
-// replaces t0. Every element >= the bound lies in a lane whose maximum is >=
-// it, so only those lanes' elements are reread: 8 vectors 32 apart (or 64
-// elements 32 apart on the scalar path). Returns n (the elements >= the
-// bound, n >= k), or -1 when more than kChunkCap
-// lanes or kWarpList elements qualify. One full warp; chunks, cmax:
-// kChunkCap entries private to the warp.
+// buf[0, n). The stats pass's lane records give, per lane, the maxima of the
+// two halves of its elements; half h of record r (r = 32 segment + lane) is
+// half-lane 2 r + h. t0 (a lower bound of the k-th largest value, from the
+// segment maxima) picks the half-lanes whose maximum is >= t0; when more
+// than 32 do, the k-th largest of those maxima, t1, is a tighter bound (k
+// half-lanes hold an element >= t1) and replaces t0. Every element >= the
+// bound lies in a half-lane whose maximum is >= it, so only those
+// half-lanes' elements are reread: 4 vectors 32 apart (or 32 elements 32
+// apart on the scalar path). Returns n (the elements >= the bound, n >= k),
+// or -1 when more than kChunkCap half-lanes or kWarpList elements qualify.
+// One full warp; lanes: the row's P x 32 records, v: their first round from
+// lane_records_first (overwritten); chunks, cmax: kChunkCap entries private
+// to the warp.
 template <typename Raw, bool VEC>
-__device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, float t0, int k, uint64_t* buf,
-                             int* chunks, float* cmax, int lane) {
+__device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, uint4 (&v)[8], float t0, int k,
+                             uint64_t* buf, int* chunks, float* cmax, int lane) {
   using KY = Key<Raw>;
+  constexpr int HW = sizeof(Raw) == 2 ? 2 : 1;  // halves per 32-bit word
   const unsigned below = (1u << lane) - 1u;
-  // the qualifying lanes, from all P x 32 lane maxima (eight 16-byte loads per lane in flight)
-  const int nf4 = P * 8;
-  const float4* l4 = reinterpret_cast<const float4*>(lanes);
+  // the qualifying half-lanes, eight 16-byte loads per lane and round
+  const int nf4 = P * 8 * lane_words(HW == 2);
+  const uint32_t pad = HW == 2 ? 0xFF80FF80u : 0xFF800000u;
   int nc = 0;
   for (int f0 = 0; f0 < nf4; f0 += 32 * 8) {
-    float4 v[8];
+    if (f0 > 0)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int f = f0 + 32 * r + lane;
+        v[r] = f < nf4 ? __ldcg(reinterpret_cast<const uint4*>(lanes) + f) : make_uint4(pad, pad, pad, pad);
+      }
+    // each lane's hits as a bit mask (bit HW (4 r + c) + h), placed by one warp scan
+    uint64_t hits = 0;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      const int f = f0 + 32 * r + lane;
-      v[r] = f < nf4 ? __ldcg(l4 + f) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-    // each lane's hits as a bit mask, placed by one warp scan
-    unsigned hits = 0;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+      const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        if (x[c] >= t0) hits |= 1u << (4 * r + c);
+#pragma unroll
+        for (int h = 0; h < HW; ++h)
+          if (half_value<Raw>(w[c], h) >= t0) hits |= 1ull << (HW * (4 * r + c) + h);
     }
-    const int cnt = __popc(hits);
+    const int cnt = __popcll(hits);
     const int incl = warp_incl_scan(cnt, lane);
     int p = nc + incl - cnt;
+    while (hits) {  // a few hits per lane: visit the set bits only
+      const int bit = __ffsll(hits) - 1;
+      hits &= hits - 1;
+      const int wi = bit / HW, h = bit - wi * HW;
+      const int r = wi >> 2, c = wi & 3;
+      uint4 x = v[0];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float x[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if ((hits >> (4 * r + c)) & 1u) {
-          if (p < kChunkCap) {
-            chunks[p] = 4 * (f0 + 32 * r + lane) + c;
-            cmax[p] = x[c];
-          }
-          ++p;
-        }
+      for (int rr = 1; rr < 8; ++rr)
+        if (r == rr) x = v[rr];
+      const uint32_t w = c == 0 ? x.x : (c == 1 ? x.y : (c == 2 ? x.z : x.w));
+      if (p < kChunkCap) {
+        chunks[p] = HW * (4 * (f0 + 32 * r + lane) + c) + h;
+        cmax[p] = half_value<Raw>(w, h);
+      }
+      ++p;
     }
     nc += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (nc > kChunkCap || nc < k) return -1;
   __syncwarp();
-  // t1: the k-th largest of the qualifying lane maxima (to 16 bits of the
-  // key), when enough lanes qualify for it to pay
+  // t1: the k-th largest of the qualifying half-lane maxima (to 16 bits of
+  // the key), when enough half-lanes qualify for it to pay
   if (nc > 32) {
     float m8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) m8[i] = lane + 32 * i < nc ? cmax[lane + 32 * i] : -INFINITY;
     const float t1 = seg_bound_regs<8>(m8, nc, k, lane);
-    // keep the lanes whose maximum is >= t1, packed in place (an entry only moves down)
+    // keep the half-lanes whose maximum is >= t1, packed in place (an entry only moves down)
     int kept = 0;
     for (int i0 = 0; i0 < nc; i0 += 32) {
       const int i = i0 + lane;
@@ -707,26 +737,34 @@ __device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, f
     nc = kept;
     t0 = t1;
   }
-  // reread them, one lane's elements per warp lane
+  // reread them
   int n = 0;
-  for (int i0 = 0; i0 < nc; i0 += 32) {
-    const int i = i0 + lane;
-    const int id = i < nc ? chunks[i] : -1;
-    const int sg = id >> 5, ls = id & 31;
-    int cnt = 0;
-    if constexpr (VEC) {
-      constexpr int NL = kSegChunks * kWV;
-      constexpr int E = Elem<Raw>::kPerVec;
-      const int nv = V / E;
-      const uint4 neg = make_uint4(Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf);
-      uint4 q[NL];
+  if constexpr (VEC) {
+    constexpr int NL = kSegChunks * kWV;  // vectors per lane
+    constexpr int NH = NL / 2;            // per half-lane
+    constexpr int E = Elem<Raw>::kPerVec;
+    const int nv = V / E;
+    const uint4 neg = make_uint4(Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf);
+    for (int i0 = 0; i0 < nc; i0 += 64) {  // two half-lanes per warp lane
+      int vb[2];  // first vector of each (-1: none)
 #pragma unroll
-      for (int t = 0; t < NL; ++t) {
-        const int vi = sg * (NL * 32) + ls + t * 32;
-        q[t] = id >= 0 && vi < nv ? __ldcg(reinterpret_cast<const uint4*>(row) + vi) : neg;
+      for (int s = 0; s < 2; ++s) {
+        const int i = i0 + 32 * s + lane;
+        const int id = i < nc ? chunks[i] : -1;
+        const int rec = id >> 1;
+        vb[s] = id < 0 ? -1 : (rec >> 5) * (NL * 32) + (rec & 31) + (id & 1) * (NH * 32);
       }
+      uint4 q[2 * NH];
 #pragma unroll
-      for (int t = 0; t < NL; ++t) {
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int t = 0; t < NH; ++t) {
+          const int vi = vb[s] + t * 32;
+          q[s * NH + t] = vb[s] >= 0 && vi < nv ? __ldcg(reinterpret_cast<const uint4*>(row) + vi) : neg;
+        }
+      int cnt = 0;
+#pragma unroll
+      for (int t = 0; t < 2 * NH; ++t) {
         float v[E];
         Elem<Raw>::unpack(q[t], v);
 #pragma unroll
@@ -735,11 +773,11 @@ __device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, f
       const int incl = warp_incl_scan(cnt, lane);
       int p = n + incl - cnt;
 #pragma unroll
-      for (int t = 0; t < NL; ++t) {
+      for (int t = 0; t < 2 * NH; ++t) {
         float v[E];
         Elem<Raw>::unpack(q[t], v);
         const uint32_t w[4] = {q[t].x, q[t].y, q[t].z, q[t].w};
-        const int vi = sg * (NL * 32) + ls + t * 32;
+        const int vi = vb[t / NH] + (t % NH) * 32;
 #pragma unroll
         for (int e = 0; e < E; ++e)
           if (v[e] >= t0) {
@@ -753,17 +791,24 @@ __device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, f
           }
       }
       n += __shfl_sync(0xffffffffu, incl, 31);
-    } else {
-      const int v0 = sg * (kScalarPerLane * 32) + ls;
+    }
+  } else {
+    constexpr int NH = kScalarPerLane / 2;  // elements per half-lane
+    for (int i0 = 0; i0 < nc; i0 += 32) {
+      const int i = i0 + lane;
+      const int id = i < nc ? chunks[i] : -1;
+      const int rec = id >> 1;
+      const int v0 = (rec >> 5) * (kScalarPerLane * 32) + (rec & 31) + (id & 1) * (NH * 32);
+      int cnt = 0;
 #pragma unroll 8
-      for (int t = 0; t < kScalarPerLane; ++t) {
+      for (int t = 0; t < NH; ++t) {
         const int v = v0 + t * 32;
         if (id >= 0 && v < V && Elem<Raw>::at(row, v) >= t0) ++cnt;
       }
       const int incl = warp_incl_scan(cnt, lane);
       int p = n + incl - cnt;
 #pragma unroll 8
-      for (int t = 0; t < kScalarPerLane; ++t) {
+      for (int t = 0; t < NH; ++t) {
         const int v = v0 + t * 32;
         if (id >= 0 && v < V) {
           const float x = Elem<Raw>::at(row, v);

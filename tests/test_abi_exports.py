@@ -49,9 +49,13 @@ def test_workspace_sizes(lib):
     assert lib.spec_workspace_bytes(0, 8, 128256, 1) == 0
     assert lib.spec_workspace_bytes(1, 300, 100, 1) == 0
     assert lib.spec_workspace_bytes(1, 1, 1, 1) == 0
-    # the warped chain's larger workspace adds the lane maxima (32 floats per 4 KB segment and row)
+    # the warped chain's larger workspace adds the lane records (32 per 4 KB segment and row: two bf16
+    # half-lane maxima in 4 bytes, or two floats for fp32 rows)
     plain, warped = lib.spec_workspace_bytes(64, 8, 128256, 1), lib.spec_warped_workspace_bytes(64, 8, 128256, 1)
     assert warped >= plain + 64 * 17 * 63 * 32 * 4 and warped % 256 == 0
+    plain, warped = lib.spec_workspace_bytes(64, 8, 128256, 0), lib.spec_warped_workspace_bytes(64, 8, 128256, 0)
+    P = -(-128256 // 1024)  # fp32 vector segments (the scalar path's are twice as long)
+    assert warped >= plain + 64 * 17 * P * 32 * 8 and warped % 256 == 0
     assert lib.spec_warped_workspace_bytes(0, 8, 128256, 1) == 0
 
 

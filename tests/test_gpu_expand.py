@@ -119,7 +119,7 @@ def test_expand_segment_bound_and_fallback():
 @pytest.mark.parametrize("M", [1, 31, 40, 63])
 def test_expand_list_sizes(M):
     """M up to the 63 stats segments of a 128256-token bf16 row: a few to a
-    few hundred candidates reread from the lanes whose maximum reaches the
+    few hundred candidates reread from the half-lanes whose maximum reaches the
     bound, selected by one warp when they are at most 256, else by the whole
     CTA."""
     Ld, logc = gen.expand_frontier(2, 4, 128256, torch.bfloat16, seed=M)
@@ -128,8 +128,8 @@ def test_expand_list_sizes(M):
 
 @pytest.mark.parametrize("dtype,V", [(torch.float32, 152064), (torch.bfloat16, 600000)])
 def test_expand_large_vocab(dtype, V):
-    """fp32 rows of 149 stats segments (lane maxima held eight per lane) and
-    bf16 rows of 293 segments (more than 256: no lane maxima, every row
+    """fp32 rows of 149 stats segments (segment maxima held up to eight per warp lane) and
+    bf16 rows of 293 segments (more than 256: no lane records, every row
     selected by a whole CTA)."""
     Ld, logc = gen.expand_frontier(2, 3, V, dtype, seed=V % 7)
     compare(*run(Ld, logc, 12), 12, 1.0)

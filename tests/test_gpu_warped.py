@@ -126,7 +126,7 @@ def test_warped_segment_bound_and_fallback(top_k, top_p):
 
 @pytest.mark.parametrize("dtype,V", [(torch.float32, 152064), (torch.bfloat16, 600000)])
 def test_warped_large_vocab(dtype, V):
-    """fp32 rows of 149 stats segments and bf16 rows of 293 (no lane maxima:
+    """fp32 rows of 149 stats segments and bf16 rows of 293 (no lane records:
     every row selected by a whole CTA), top-k 40, top-p 0.9."""
     c = gen.chain_zipf(3, 2, V, dtype, 0.9, 0.6, seed=V % 5, draft_top_k=40)
     compare(*run(c, 40, 0.9))
@@ -135,7 +135,7 @@ def test_warped_large_vocab(dtype, V):
 @pytest.mark.parametrize("top_k,top_p", [(50, 0.9), (10, 1.0)])
 def test_warped_plain_workspace(top_k, top_p):
     """With only spec_workspace_bytes of workspace the stats pass keeps no
-    lane maxima and every row is selected by a whole CTA (the filtering pass
+    lane records and every row is selected by a whole CTA (the filtering pass
     over the row): the same results."""
     import speculative_decoding_verification_29_gb300 as sv
 
