@@ -126,6 +126,14 @@ def test_expand_list_sizes(M):
     compare(*run(Ld, logc, M), M, 1.0)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_expand_unaligned_rows(dtype):
+    """Odd V = 65537: scalar loads in the stats pass, lane records over 32 +
+    32 elements, M = 12 children per tree selected by one warp per row."""
+    Ld, logc = gen.expand_frontier(3, 4, 65537, dtype, seed=12)
+    compare(*run(Ld, logc, 12), 12, 1.0)
+
+
 @pytest.mark.parametrize("dtype,V", [(torch.float32, 152064), (torch.bfloat16, 600000)])
 def test_expand_large_vocab(dtype, V):
     """fp32 rows of 149 stats segments (segment maxima held up to eight per warp lane) and

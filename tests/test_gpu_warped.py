@@ -124,6 +124,16 @@ def test_warped_segment_bound_and_fallback(top_k, top_p):
     compare(*run(c, top_k, top_p), allow_warp=True)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_warped_unaligned_rows(dtype):
+    """Odd V = 65537: the rows are not 16-byte aligned, so the stats pass
+    takes its scalar loads (33 segments of 2048 elements; a lane record holds
+    the maxima of its first and last 32 elements) and one warp selects each
+    row's top-k 20 from those records."""
+    c = gen.chain_zipf(3, 3, 65537, dtype, 0.9, 0.6, seed=11, draft_top_k=20)
+    compare(*run(c, 20, 0.9))
+
+
 @pytest.mark.parametrize("dtype,V", [(torch.float32, 152064), (torch.bfloat16, 600000)])
 def test_warped_large_vocab(dtype, V):
     """fp32 rows of 149 stats segments and bf16 rows of 293 (no lane records:
