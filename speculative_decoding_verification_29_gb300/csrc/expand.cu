@@ -142,32 +142,33 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
     __syncthreads();
     const int st = *s_st;
     if (tid < 32) {
+      // lane f holds the head of row f's list; each round the best head is
+      // found by two 32-bit max reductions (the float pair's high, then low
+      // part, as order-preserving keys; the pairs are normalised, so this is
+      // their numeric order) and the lowest node among equal scores; the
+      // winning lane writes the child and moves to its next candidate
       const int lane = tid;
       int head = 0;
+      Cand cur = lane < F ? s_c[lane * Mk] : Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
       for (int i = 0; i < Mk; ++i) {
-        Cand best{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
-        if (lane < F && head < Mk) best = s_c[lane * Mk + head];
-        int who = lane;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          Cand oc;
-          oc.hi = __shfl_xor_sync(0xffffffffu, best.hi, o);
-          oc.lo = __shfl_xor_sync(0xffffffffu, best.lo, o);
-          oc.f = __shfl_xor_sync(0xffffffffu, best.f, o);
-          oc.v = __shfl_xor_sync(0xffffffffu, best.v, o);
-          const int ow = __shfl_xor_sync(0xffffffffu, who, o);
-          if (cand_before(oc, best) || (!cand_before(best, oc) && ow < who)) {
-            best = oc;
-            who = ow;
-          }
+        const bool live = lane < F && head < Mk;
+        // 0: no candidate left; 1: a slot past the vocabulary (after every child)
+        const uint32_t k1 = !live ? 0u : (cur.v == 0x7fffffff ? 1u : Key<float>::of(__float_as_uint(cur.hi)));
+        const uint32_t m1 = __reduce_max_sync(0xffffffffu, k1);  // every lane takes part
+        unsigned tied = __ballot_sync(0xffffffffu, live && k1 == m1);
+        if (__popc(tied) > 1) {
+          const bool t = (tied >> lane) & 1u;
+          const uint32_t k2 = t ? Key<float>::of(__float_as_uint(cur.lo)) : 0u;
+          const uint32_t m2 = __reduce_max_sync(0xffffffffu, k2);
+          tied = __ballot_sync(0xffffffffu, t && k2 == m2);
         }
-        if (lane == who) ++head;
-        if (lane == 0) {
+        if (lane == __ffs(tied) - 1) {
           const long long o = static_cast<long long>(b) * Mk + i;
-          const bool ok = !st && best.v != 0x7fffffff;
-          a.parent[o] = ok ? best.f : -1;
-          a.token[o] = ok ? best.v : -1;
-          a.score[o] = ok ? best.hi + best.lo : NAN;
+          const bool ok = !st && cur.v != 0x7fffffff;
+          a.parent[o] = ok ? cur.f : -1;
+          a.token[o] = ok ? cur.v : -1;
+          a.score[o] = ok ? cur.hi + cur.lo : NAN;
+          if (++head < Mk) cur = s_c[lane * Mk + head];
         }
       }
       if (lane == 0) a.row_status[b] = st;
