@@ -204,6 +204,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
   __shared__ float2 s_Z;
   __shared__ int s_slow[kSelWarps];
   griddep_wait();
+  // the tail may launch now: the pass has completed, so its clusters take
+  // only SM room the selection leaves free while they wait for this grid
+  griddep_launch_dependents();
   {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
     const int row_id = blockIdx.x * kSelWarps + warp;
     static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 8) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
@@ -395,9 +398,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
   };
   for (int w = 0; w < kSelWarps; ++w)
     if (s_slow[w]) cta_row(blockIdx.x * kSelWarps + w);
-  // the trigger comes late: the tail's clusters would otherwise hold SM slots,
-  // idle, while rows are still being selected
-  griddep_launch_dependents();
 }
 
 }  // namespace
