@@ -372,10 +372,20 @@ def run_ours(args):
     torch.cuda.synchronize()
     k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API with pinned host buffers (the chain
+    # paths through the host-buffer entry point: the library stages the
+    # inputs, verifies and copies the outputs back in one call)
     pinned = [h.pin_memory() for h in host]
     h2d = sum(h.numel() * h.element_size() for h in pinned)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    host_chain = name not in ("entropy", "tree", "warped")
+    if host_chain and w.T == 0.0:  # greedy: only the target logits and the draft tokens are copied
+        h2d = pinned[0].numel() * pinned[0].element_size() + pinned[2].numel() * pinned[2].element_size()
+    if host_chain:
+        hws = sv.alloc_workspace(sv.host_workspace_bytes(w.B, w.K, w.V, w.Lp.dtype), dev)
+        hout = dict(accept_len=torch.empty(w.B, dtype=torch.int32).pin_memory(),
+                    out_tokens=torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory(),
+                    row_status=torch.empty(w.B, dtype=torch.int32).pin_memory())
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -389,16 +399,12 @@ def run_ours(args):
             o = sv.spec_verify_tree_greedy(pinned[0], pinned[1], pinned[2], w.n1, tree_mask=pinned[3], device=dev)
             co = sv.spec_tree_confidence(pinned[4], w.n1, device=dev)
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu(), co["choice"].cpu()]
-        elif w.T == 0.0:
-            o = sv.spec_verify_chain_greedy(pinned[0], pinned[2], device=dev)
-            res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
         elif name == "warped":
             o = sv.spec_verify_chain_warped(*pinned, w.T, w.top_k, w.top_p, device=dev)
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
-        else:
-            o = sv.spec_verify_chain(pinned[0], pinned[1], pinned[2], pinned[3], pinned[4], w.T, device=dev,
-                                     stats=False)
-            res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
+        else:  # sampling or greedy chain: host buffers in, host buffers out
+            o = sv.spec_verify_chain_host(*pinned, w.T, out=hout, workspace=hws, device=dev)
+            res = list(o.values())
         d2h = sum(r.numel() * r.element_size() for r in res)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, ws, dev)

@@ -125,6 +125,30 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
                       float* lse_target, float* lse_draft, float* p_at_x, float* q_at_x,
                       int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Device workspace bytes for spec_verify_chain_host: room to stage the
+ * inputs and outputs plus spec_workspace_bytes(B, K, V, dtype). 0 for invalid
+ * sizes. */
+size_t spec_host_workspace_bytes(int B, int K, int V, int dtype);
+
+/* spec_verify_chain from and to HOST buffers, for callers whose logits are
+ * in host memory. The call enqueues on `stream`, in order: one
+ * cudaMemcpyAsync host-to-device per input into the workspace, the
+ * verification kernels, and one cudaMemcpyAsync device-to-host per output
+ * (accept_len, out_tokens, row_status; no float outputs). It returns once
+ * they are enqueued: the caller synchronises the stream before reading the
+ * outputs, and keeps every host buffer valid and unmodified until then.
+ * Pinned host memory (cudaHostAlloc / cudaHostRegister) makes the copies
+ * asynchronous; pageable memory works but the runtime stages it
+ * synchronously. Arguments and row_status as spec_verify_chain (at T == 0
+ * draft_logits, u_accept and u_resample are not read); workspace: device
+ * memory of spec_host_workspace_bytes bytes, 256-byte aligned. Host-side
+ * errors (SPEC_ERR_ARG, SPEC_ERR_WORKSPACE, ...) return before any copy is
+ * enqueued; SPEC_ERR_CUDA means an enqueue failed. */
+int spec_verify_chain_host(const void* target_logits, const void* draft_logits, int dtype,
+                           const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                           float temperature, int B, int K, int V, int32_t* accept_len, int32_t* out_tokens,
+                           int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Stage A of spec_verify_chain: the streaming pass, one read of every target
  * and draft row, leaving per-chunk (max, sum of exp) partials in the
  * workspace. T > 0. Same arguments as spec_verify_chain (only the logits,

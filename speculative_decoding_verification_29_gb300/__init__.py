@@ -7,6 +7,7 @@ API is lazy so that the package can be inspected without a GPU.
 
 __all__ = [
     "spec_verify_chain",
+    "spec_verify_chain_host",
     "spec_chain_scan",
     "spec_chain_sample",
     "spec_verify_chain_warped",
@@ -19,6 +20,7 @@ __all__ = [
     "spec_kv_compact",
     "workspace_bytes",
     "warped_workspace_bytes",
+    "host_workspace_bytes",
     "alloc_workspace",
 ]
 

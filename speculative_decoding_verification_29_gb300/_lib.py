@@ -27,6 +27,8 @@ SIGNATURES = {
     "spec_warped_workspace_bytes": (Z, [I, I, I, I]),
     "spec_verify_chain": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P, Z, P]),
     "spec_verify_chain_noalloc": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P]),
+    "spec_host_workspace_bytes": (Z, [I, I, I, I]),
+    "spec_verify_chain_host": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, Z, P]),
     "spec_chain_scan": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P, Z, P]),
     "spec_chain_sample": (I, [P, P, I, P, P, P, F, I, I, I, P, P, P, P, P, P, P, P, Z, P]),
     "spec_verify_chain_warped": (I, [P, P, I, P, P, P, F, I, F, I, I, I, P, P, P, P, P, P, Z, P]),

@@ -101,6 +101,63 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_res
     return out
 
 
+def host_workspace_bytes(B: int, K: int, V: int, dtype) -> int:
+    """Device workspace for spec_verify_chain_host (staged inputs and
+    outputs plus the verification workspace)."""
+    code = dtype if isinstance(dtype, int) else _dtype_code(torch.empty(0, dtype=dtype))
+    return int(_lib.load().spec_host_workspace_bytes(B, K, V, code))
+
+
+def _host(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if t.device.type != "cpu" or not t.is_contiguous() or (dtype is not None and t.dtype != dtype):
+        raise ValueError(f"{name}: a contiguous CPU tensor{'' if dtype is None else f' of {dtype}'} is required")
+    return t
+
+
+def spec_verify_chain_host(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
+                           out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                           device="cuda", stream=None, synchronize: bool = True) -> Dict[str, torch.Tensor]:
+    """Chain verification from host (CPU) tensors through
+    spec_verify_chain_host: the library copies the inputs to the device,
+    verifies and copies accept_len, out_tokens and row_status back into host
+    tensors (pinned, allocated unless ``out`` holds them). Inputs: contiguous
+    CPU tensors as spec_verify_chain takes them (pinned memory makes the
+    copies asynchronous). With ``synchronize`` the stream is synchronised
+    before returning; otherwise the caller synchronises it before reading the
+    outputs and keeps the inputs alive until then."""
+    lib = _lib.load()
+    dev = torch.device(device)
+    Lp = _host(target_logits, "target_logits")
+    dt = _dtype_code(Lp)
+    B, K1, V = Lp.shape
+    K = K1 - 1
+    sampling = float(temperature) != 0.0
+    Lq = _host(draft_logits, "draft_logits", Lp.dtype) if sampling else None
+    x = _host(draft_tokens, "draft_tokens", torch.int32)
+    ua = _host(u_accept, "u_accept", torch.float32) if sampling else None
+    ur = _host(u_resample, "u_resample", torch.float32) if sampling else None
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, pin_memory=True),
+                   out_tokens=torch.empty(B, K + 1, dtype=torch.int32, pin_memory=True),
+                   row_status=torch.empty(B, dtype=torch.int32, pin_memory=True))
+    if workspace is None:
+        workspace = alloc_workspace(host_workspace_bytes(B, K, V, dt), dev)
+    st = _stream(stream)
+    rc = lib.spec_verify_chain_host(
+        Lp.data_ptr(), _ptr(Lq), dt, x.data_ptr(), _ptr(ua), _ptr(ur), float(temperature), B, K, V,
+        out["accept_len"].data_ptr(), out["out_tokens"].data_ptr(), out["row_status"].data_ptr(),
+        workspace.data_ptr(), workspace.numel(), st)
+    check("spec_verify_chain_host", rc)
+    if synchronize:
+        if stream is None:
+            torch.cuda.current_stream(dev).synchronize()
+        elif hasattr(stream, "synchronize"):
+            stream.synchronize()
+        else:
+            torch.cuda.ExternalStream(st).synchronize()
+    return out
+
+
 def _stage(name, target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
            out: Dict[str, torch.Tensor], workspace: torch.Tensor, stream=None) -> None:
     B, K1, V = target_logits.shape

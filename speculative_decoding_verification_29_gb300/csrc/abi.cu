@@ -248,6 +248,33 @@ int chain_sample(const ChainCall& c) {
   return cuda_status(launch_chain_tail(t, c.dtype, vec, c.st));
 }
 
+// Device workspace of spec_verify_chain_host: the staged inputs, the
+// outputs, then the verification workspace (every region 256-byte aligned).
+struct HostLayout {
+  size_t Lp, Lq, x, ua, ur, acc, tok, st, ws, total;
+};
+
+HostLayout host_layout(int B, int K, int V, int dtype) {
+  const size_t es = elem_size(dtype), b = static_cast<size_t>(B), k = static_cast<size_t>(K);
+  HostLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t& f, size_t n) {
+    f = off;
+    off += up256(n);
+  };
+  take(L.Lp, b * (k + 1) * V * es);
+  take(L.Lq, b * k * V * es);
+  take(L.x, b * k * sizeof(int32_t));
+  take(L.ua, b * k * sizeof(float));
+  take(L.ur, b * sizeof(float));
+  take(L.acc, b * sizeof(int32_t));
+  take(L.tok, b * (k + 1) * sizeof(int32_t));
+  take(L.st, b * sizeof(int32_t));
+  L.ws = off;
+  L.total = off + layout(B, K + 1, K, V, dtype).total;
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -298,6 +325,55 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
   CHAIN_CALL;
   if ((e = chain_scan(c))) return e;
   return chain_sample(c);
+}
+
+size_t spec_host_workspace_bytes(int B, int K, int V, int dtype) {
+  if (spec_workspace_bytes(B, K, V, dtype) == 0) return 0;
+  return host_layout(B, K, V, dtype).total;
+}
+
+int spec_verify_chain_host(const void* target_logits, const void* draft_logits, int dtype,
+                           const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                           float temperature, int B, int K, int V, int32_t* accept_len, int32_t* out_tokens,
+                           int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream) {
+  const bool sampling = temperature != 0.f;
+  int e = chain_args_ok(target_logits, draft_logits, dtype, B, K, V, temperature, sampling);
+  if (e) return e;
+  if ((K > 0 && !draft_tokens) || (sampling && ((K > 0 && !u_accept) || !u_resample))) return SPEC_ERR_ARG;
+  if (!accept_len || !out_tokens || !row_status) return SPEC_ERR_ARG;
+  const HostLayout L = host_layout(B, K, V, dtype);
+  if ((e = check_workspace(workspace, workspace_bytes, L.total))) return e;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t es = elem_size(dtype), b = static_cast<size_t>(B), k = static_cast<size_t>(K);
+  // one copy per buffer, in stream order with the kernels
+  struct Copy {
+    void* dst;
+    const void* src;
+    size_t n;
+  };
+  const Copy in[5] = {{at(workspace, L.Lp), target_logits, b * (k + 1) * V * es},
+                      {at(workspace, L.Lq), sampling ? draft_logits : nullptr, b * k * V * es},
+                      {at(workspace, L.x), draft_tokens, b * k * sizeof(int32_t)},
+                      {at(workspace, L.ua), sampling ? u_accept : nullptr, b * k * sizeof(float)},
+                      {at(workspace, L.ur), sampling ? u_resample : nullptr, b * sizeof(float)}};
+  for (const Copy& c : in)
+    if (c.src && c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
+  int32_t* tok = reinterpret_cast<int32_t*>(at(workspace, L.tok));
+  int32_t* rs = reinterpret_cast<int32_t*>(at(workspace, L.st));
+  e = spec_verify_chain(at(workspace, L.Lp), sampling ? at(workspace, L.Lq) : nullptr, dtype,
+                        reinterpret_cast<const int32_t*>(at(workspace, L.x)),
+                        reinterpret_cast<const float*>(at(workspace, L.ua)),
+                        reinterpret_cast<const float*>(at(workspace, L.ur)), temperature, B, K, V, acc, tok, nullptr,
+                        nullptr, nullptr, nullptr, rs, at(workspace, L.ws), workspace_bytes - L.ws, stream);
+  if (e) return e;
+  const Copy out[3] = {{accept_len, acc, b * sizeof(int32_t)},
+                       {out_tokens, tok, b * (k + 1) * sizeof(int32_t)},
+                       {row_status, rs, b * sizeof(int32_t)}};
+  for (const Copy& c : out)
+    if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }
 
 int spec_verify_chain_warped(const void* target_logits, const void* draft_logits, int dtype,

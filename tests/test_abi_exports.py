@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     for n in ("spec_verify_chain", "spec_verify_chain_greedy", "spec_verify_tree_greedy", "spec_tree_confidence",
               "spec_workspace_bytes", "spec_status_string", "spec_chain_scan", "spec_chain_sample", "spec_kv_compact",
               "spec_tree_entropy", "spec_merge_trees", "spec_verify_chain_warped", "spec_tree_expand",
-              "spec_expand_workspace_bytes"):
+              "spec_expand_workspace_bytes", "spec_verify_chain_host", "spec_host_workspace_bytes"):
         assert n in names
 
 
@@ -57,6 +57,11 @@ def test_workspace_sizes(lib):
     P = -(-128256 // 1024)  # fp32 vector segments (the scalar path's are twice as long)
     assert warped >= plain + 64 * 17 * P * 32 * 8 and warped % 256 == 0
     assert lib.spec_warped_workspace_bytes(0, 8, 128256, 1) == 0
+    # the host-buffer call stages the inputs and outputs in front of the verification workspace
+    host = lib.spec_host_workspace_bytes(64, 8, 128256, 1)
+    staged = 64 * 17 * 128256 * 2 + 64 * 8 * 8 + 64 * 4 + 64 * 9 * 4 + 2 * 64 * 4
+    assert host >= lib.spec_workspace_bytes(64, 8, 128256, 1) + staged and host % 256 == 0
+    assert lib.spec_host_workspace_bytes(0, 8, 128256, 1) == 0
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -83,6 +88,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.spec_verify_chain(fake, fake, 1, fake, fake, fake, 1.0, 1, 1, 16, fake, fake, n, n, n, n, fake,
                                  ctypes.c_void_p(4096 + 8), 1 << 20, n) == SPEC_ERR_WORKSPACE
     assert lib.spec_verify_chain_greedy(fake, 1, n, 1, 2, 16, fake, fake, n, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    # host buffers: NULL uniforms or outputs, workspace below spec_host_workspace_bytes
+    hc = lambda *a: lib.spec_verify_chain_host(*a)
+    assert hc(fake, fake, 1, fake, n, fake, 1.0, 1, 2, 16, fake, fake, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert hc(fake, fake, 1, fake, fake, fake, 1.0, 1, 2, 16, fake, n, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert hc(fake, n, 1, fake, fake, fake, 1.0, 1, 2, 16, fake, fake, fake, fake, 1 << 20, n) == SPEC_ERR_ARG
+    assert hc(fake, fake, 1, fake, fake, fake, 1.0, 1, 2, 16, fake, fake, fake, fake,
+              lib.spec_host_workspace_bytes(1, 2, 16, 1) - 256, n) == SPEC_ERR_WORKSPACE
     # trees: n1 out of range, N beyond the limit
     assert lib.spec_verify_tree_greedy(fake, 1, fake, fake, n, 1, 5, 2, 3, 16, 5, fake, fake, fake, fake, fake, fake,
                                        fake, 1 << 20, n) == SPEC_ERR_ARG
