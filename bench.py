@@ -7,7 +7,8 @@ noise. The step runs the rowscan pass (normalisers of all 1088 rows), the
 acceptance decision and the residual / bonus draw.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload chain_batched|chain_single|chain_deep|greedy|tree]
+                    [--workload chain_batched|chain_single|chain_deep|greedy|tree|entropy|
+                                warped|kv_compact|merge|expand]
 
 Under torchrun each rank verifies its own batch (seed + rank) on its own GPU:
 rows are independent, so there is no collective in the data path (weak
