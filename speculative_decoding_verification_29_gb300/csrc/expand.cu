@@ -30,6 +30,11 @@ struct Cand {
   int f, v;
 };
 
+// No candidate: a slot past the vocabulary or padding; it ranks after every
+// child and is written as -1 / NaN.
+constexpr int kNoTok = 0x7fffffff;
+__device__ __forceinline__ Cand no_cand() { return Cand{-INFINITY, 0.f, kNoTok, kNoTok}; }
+
 // a before b: higher score, then lower node, then lower token
 __device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
   if (a.hi != b.hi || a.lo != b.lo) return ds_gt(make_float2(a.hi, a.lo), make_float2(b.hi, b.lo));
@@ -136,7 +141,7 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
       const float2 sc = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
       c.hi = sc.x > -INFINITY ? sc.x : -INFINITY;
       c.lo = sc.x > -INFINITY ? sc.y : 0.f;
-      if (c.v < 0) c = Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};  // a slot past the vocabulary
+      if (c.v < 0) c = no_cand();  // a slot past the vocabulary
       s_c[i] = c;
     }
     __syncthreads();
@@ -149,11 +154,11 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
       // winning lane writes the child and moves to its next candidate
       const int lane = tid;
       int head = 0;
-      Cand cur = lane < F ? s_c[lane * Mk] : Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
+      Cand cur = lane < F ? s_c[lane * Mk] : no_cand();
       for (int i = 0; i < Mk; ++i) {
         const bool live = lane < F && head < Mk;
         // 0: no candidate left; 1: a slot past the vocabulary (after every child)
-        const uint32_t k1 = !live ? 0u : (cur.v == 0x7fffffff ? 1u : Key<float>::of(__float_as_uint(cur.hi)));
+        const uint32_t k1 = !live ? 0u : (cur.v == kNoTok ? 1u : Key<float>::of(__float_as_uint(cur.hi)));
         const uint32_t m1 = __reduce_max_sync(0xffffffffu, k1);  // every lane takes part
         unsigned tied = __ballot_sync(0xffffffffu, live && k1 == m1);
         if (__popc(tied) > 1) {
@@ -164,7 +169,7 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
         }
         if (lane == __ffs(tied) - 1) {
           const long long o = static_cast<long long>(b) * Mk + i;
-          const bool ok = !st && cur.v != 0x7fffffff;
+          const bool ok = !st && cur.v != kNoTok;
           a.parent[o] = ok ? cur.f : -1;
           a.token[o] = ok ? cur.v : -1;
           a.score[o] = ok ? cur.hi + cur.lo : NAN;
@@ -178,7 +183,7 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
   int n2 = 1;
   while (n2 < n) n2 <<= 1;
   for (int i = tid; i < n2; i += kSelThreads) {
-    Cand c{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};
+    Cand c = no_cand();
     if (i < n) {
       const int f = i / Mk;
       c = static_cast<const Cand*>(a.cand)[static_cast<long long>(b) * n + i];
@@ -186,7 +191,7 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
       const float2 sc = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
       c.hi = sc.x > -INFINITY ? sc.x : -INFINITY;
       c.lo = sc.x > -INFINITY ? sc.y : 0.f;
-      if (c.v < 0) c = Cand{-INFINITY, 0.f, 0x7fffffff, 0x7fffffff};  // a slot past the vocabulary
+      if (c.v < 0) c = no_cand();  // a slot past the vocabulary
     }
     s_c[i] = c;
   }
@@ -213,7 +218,7 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
   for (int i = tid; i < Mk; i += kSelThreads) {
     const long long o = static_cast<long long>(b) * Mk + i;
     const Cand c = s_c[i];
-    const bool ok = !st && c.v != 0x7fffffff;
+    const bool ok = !st && c.v != kNoTok;
     a.parent[o] = ok ? c.f : -1;
     a.token[o] = ok ? c.v : -1;
     a.score[o] = ok ? c.hi + c.lo : NAN;

@@ -637,17 +637,24 @@ __device__ __forceinline__ float half_value(uint32_t w, int h) {
   return __uint_as_float(w);
 }
 
-// The first round of a row's lane records: eight 16-byte loads per lane,
-// issued before the row's bound is known (padding: -inf in every half).
+// One round of a row's lane records, 16-byte groups f0 + 32 r + lane of
+// the row's P * 8 * lane_words (eight loads per lane; padding: -inf in every
+// half).
 template <typename Raw>
-__device__ __forceinline__ void lane_records_first(const float* lanes, int P, int lane, uint4 (&v)[8]) {
+__device__ __forceinline__ void lane_records_round(const float* lanes, int P, int f0, int lane, uint4 (&v)[8]) {
   const int nf4 = P * 8 * lane_words(sizeof(Raw) == 2);
   const uint32_t pad = sizeof(Raw) == 2 ? 0xFF80FF80u : 0xFF800000u;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    const int f = 32 * r + lane;
+    const int f = f0 + 32 * r + lane;
     v[r] = f < nf4 ? __ldcg(reinterpret_cast<const uint4*>(lanes) + f) : make_uint4(pad, pad, pad, pad);
   }
+}
+
+// The first round, issued before the row's bound is known.
+template <typename Raw>
+__device__ __forceinline__ void lane_records_first(const float* lanes, int P, int lane, uint4 (&v)[8]) {
+  lane_records_round<Raw>(lanes, P, 0, lane, v);
 }
 
 // The row's candidates for its k largest elements as composites in
@@ -672,15 +679,9 @@ __device__ int gather_chunks(const Raw* row, int V, int P, const float* lanes, u
   const unsigned below = (1u << lane) - 1u;
   // the qualifying half-lanes, eight 16-byte loads per lane and round
   const int nf4 = P * 8 * lane_words(HW == 2);
-  const uint32_t pad = HW == 2 ? 0xFF80FF80u : 0xFF800000u;
   int nc = 0;
   for (int f0 = 0; f0 < nf4; f0 += 32 * 8) {
-    if (f0 > 0)
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int f = f0 + 32 * r + lane;
-        v[r] = f < nf4 ? __ldcg(reinterpret_cast<const uint4*>(lanes) + f) : make_uint4(pad, pad, pad, pad);
-      }
+    if (f0 > 0) lane_records_round<Raw>(lanes, P, f0, lane, v);
     // each lane's hits as a bit mask (bit HW (4 r + c) + h), placed by one warp scan
     uint64_t hits = 0;
 #pragma unroll

@@ -111,6 +111,36 @@ def test_exhaustive_world_ids_match_oracle():
     compare_chain(gpu_chain(c), oracle_chain(c), name="world_V4K3")
 
 
+def test_first_token_law_statistical():
+    """Lossless sampling, measured: 10^6 rows share one target and one draft
+    table (V=8, K=3, T=1) with draft tokens drawn from q; the first emitted
+    token follows the target's p_0 (its softmax from the same fp32 logits,
+    in fp64) within a 5-sigma binomial bound for every token."""
+    import speculative_decoding_verification_29_gb300 as sv
+
+    g = torch.Generator().manual_seed(21)
+    V, K, T, Bc, calls = 8, 3, 1.0, 62500, 16
+    lp = (1.5 * torch.randn(K + 1, V, generator=g)).float()
+    lq = (lp[:K] + 0.8 * torch.randn(K, V, generator=g)).float()
+    q = torch.softmax(lq.double() / T, dim=-1)
+    dev = torch.device("cuda")
+    Lp = lp.expand(Bc, K + 1, V).contiguous().to(dev)
+    Lq = lq.expand(Bc, K, V).contiguous().to(dev)
+    ws = sv.alloc_workspace(sv.workspace_bytes(Bc, K, V, torch.float32), dev)
+    counts = np.zeros(V, np.int64)
+    for _ in range(calls):
+        x = torch.stack([torch.multinomial(q[k], Bc, replacement=True, generator=g) for k in range(K)], 1)
+        ua, ur = torch.rand(Bc, K, generator=g), torch.rand(Bc, generator=g)
+        out = sv.spec_verify_chain(Lp, Lq, x.int().to(dev), ua.to(dev), ur.to(dev), T, workspace=ws, stats=False)
+        assert int((out["row_status"] != 0).sum()) == 0
+        counts += np.bincount(out["out_tokens"][:, 0].cpu().numpy(), minlength=V)
+    n = Bc * calls
+    p0 = torch.softmax(lp[0].double() / T, dim=-1).numpy()
+    sigma = np.sqrt(n * p0 * (1 - p0))
+    assert counts.sum() == n
+    assert np.all(np.abs(counts - n * p0) <= 5 * sigma + 1), (counts, n * p0, sigma)
+
+
 def test_status_rows():
     c = gen.chain_tiny(4, B=8, K=3, V=1024)
     Lp, Lq, x = c.Lp.clone(), c.Lq.clone(), c.x.clone()
