@@ -29,6 +29,7 @@ struct Cand {
   float hi, lo;  // score as a float pair
   int f, v;
 };
+static_assert(sizeof(Cand) == 16, "a candidate is one 16-byte load");
 
 // No candidate: a slot past the vocabulary or padding; it ranks after every
 // child and is written as -1 / NaN.
@@ -118,83 +119,111 @@ __device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int
 }
 
 constexpr int kMergeCap = 2048;  // F x M candidates held in shared memory (32 KB)
+constexpr int kWarpMergeCap = 256;  // F x M up to which the merging warp loads every candidate at once
 
-// Tree b's F x M candidates, scored and ranked: higher score, then lower
-// node, then lower token; the first M kept. Each row's M candidates arrive
-// sorted in that order, so for F <= 32 one warp merges the rows' heads;
-// otherwise the block sorts all F x M. s_c: kMergeCap entries.
+// A row's stored candidate w (its log-probability pair, token) as child of
+// node f with path score lc (a slot past the vocabulary: no candidate).
+__device__ __forceinline__ Cand scored(int4 w, int f, float lc) {
+  if (w.w < 0) return no_cand();
+  const float2 sc = ds_add(make_float2(__int_as_float(w.x), __int_as_float(w.y)), make_float2(lc, 0.f));
+  return sc.x > -INFINITY ? Cand{sc.x, sc.y, f, w.w} : Cand{-INFINITY, 0.f, f, w.w};
+}
+
+// Candidate i of tree b (row i / M), scored.
+__device__ __forceinline__ Cand tree_cand(const ExpArgs& a, int b, int i) {
+  const int f = i / a.M;
+  return scored(__ldcg(static_cast<const int4*>(a.cand) + static_cast<long long>(b) * a.F * a.M + i), f,
+                __ldcg(a.logc + static_cast<long long>(b) * a.F + f));
+}
+
+// Status of tree b: its rows' flags, and SPEC_ROW_DRAFT for a NaN or +inf
+// path score. One warp; every lane gets it.
+__device__ __forceinline__ int tree_status(const ExpArgs& a, int b, int lane) {
+  int st = 0;
+  for (int f = lane; f < a.F; f += 32) {
+    const float lc = __ldcg(a.logc + static_cast<long long>(b) * a.F + f);
+    st |= __ldcg(a.row_flag + static_cast<long long>(b) * a.F + f) | ((lc != lc || lc == INFINITY) ? SPEC_ROW_DRAFT : 0);
+  }
+  return static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
+}
+
+// Tree b's top M children by one warp, F <= 32; s_c: F x M entries of
+// shared memory private to the warp. Every row's M candidates arrive sorted
+// (higher score, then lower node, then lower token), so lane f holds the
+// head of row f's list; each round the best head is found by two 32-bit max
+// reductions (the float pair's high, then low part, as order-preserving
+// keys; the pairs are normalised, so this is their numeric order) and the
+// lowest node among equal scores; the winning lane writes the child and
+// moves to its next candidate.
+__device__ void merge_tree_warp(const ExpArgs& a, int b, Cand* s_c, int lane) {
+  const int F = a.F, Mk = a.M, n = F * Mk;
+  int st;
+  if (n <= kWarpMergeCap) {  // every load in flight at once: one memory round trip
+    const long long rb = static_cast<long long>(b) * F;
+    const float lc = lane < F ? __ldcg(a.logc + rb + lane) : 0.f;  // lane f: row f's path score and flag
+    const int fl = lane < F ? __ldcg(a.row_flag + rb + lane) : 0;
+    constexpr int kPer = kWarpMergeCap / 32;
+    int4 w[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      w[j] = lane + 32 * j < n ? __ldcg(static_cast<const int4*>(a.cand) + rb * Mk + lane + 32 * j)
+                               : make_int4(0, 0, 0, -1);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = lane + 32 * j, f = i / Mk;
+      const float lcf = __shfl_sync(0xffffffffu, lc, f & 31);
+      if (i < n) s_c[i] = scored(w[j], f, lcf);
+    }
+    st = static_cast<int>(
+        __reduce_or_sync(0xffffffffu, static_cast<unsigned>(fl | ((lc != lc || lc == INFINITY) ? SPEC_ROW_DRAFT : 0))));
+  } else {
+    for (int i = lane; i < n; i += 32) s_c[i] = tree_cand(a, b, i);
+    st = tree_status(a, b, lane);
+  }
+  __syncwarp();
+  int head = 0;
+  Cand cur = lane < F ? s_c[lane * Mk] : no_cand();
+  for (int i = 0; i < Mk; ++i) {
+    const bool live = lane < F && head < Mk;
+    // 0: no candidate left; 1: a slot past the vocabulary (after every child)
+    const uint32_t k1 = !live ? 0u : (cur.v == kNoTok ? 1u : Key<float>::of(__float_as_uint(cur.hi)));
+    const uint32_t m1 = __reduce_max_sync(0xffffffffu, k1);  // every lane takes part
+    unsigned tied = __ballot_sync(0xffffffffu, live && k1 == m1);
+    if (__popc(tied) > 1) {
+      const bool t = (tied >> lane) & 1u;
+      const uint32_t k2 = t ? Key<float>::of(__float_as_uint(cur.lo)) : 0u;
+      const uint32_t m2 = __reduce_max_sync(0xffffffffu, k2);
+      tied = __ballot_sync(0xffffffffu, t && k2 == m2);
+    }
+    if (lane == __ffs(tied) - 1) {
+      const long long o = static_cast<long long>(b) * Mk + i;
+      const bool ok = !st && cur.v != kNoTok;
+      a.parent[o] = ok ? cur.f : -1;
+      a.token[o] = ok ? cur.v : -1;
+      a.score[o] = ok ? cur.hi + cur.lo : NAN;
+      if (++head < Mk) cur = s_c[lane * Mk + head];
+    }
+  }
+  if (lane == 0) a.row_status[b] = st;
+  __syncwarp();
+}
+
+// Tree b by the whole CTA: the warp merge for F <= 32, otherwise a block
+// sort of all F x M candidates. s_c: kMergeCap entries.
 __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
   const int tid = threadIdx.x;
   const int F = a.F, Mk = a.M, n = F * Mk;
-  if (tid == 0) *s_st = 0;
-  __syncthreads();
-  for (int f = tid; f < F; f += kSelThreads) {
-    const float lc = a.logc[static_cast<long long>(b) * F + f];
-    const int fl = a.row_flag[static_cast<long long>(b) * F + f] | ((lc != lc || lc == INFINITY) ? SPEC_ROW_DRAFT : 0);
-    if (fl) atomicOr(s_st, fl);
-  }
-  if (F <= 32) {  // every row's candidates are sorted already: one warp merges the F heads
-    for (int i = tid; i < n; i += kSelThreads) {
-      const int f = i / Mk;
-      Cand c = static_cast<const Cand*>(a.cand)[static_cast<long long>(b) * n + i];
-      c.f = f;
-      const float2 sc = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
-      c.hi = sc.x > -INFINITY ? sc.x : -INFINITY;
-      c.lo = sc.x > -INFINITY ? sc.y : 0.f;
-      if (c.v < 0) c = no_cand();  // a slot past the vocabulary
-      s_c[i] = c;
-    }
-    __syncthreads();
-    const int st = *s_st;
-    if (tid < 32) {
-      // lane f holds the head of row f's list; each round the best head is
-      // found by two 32-bit max reductions (the float pair's high, then low
-      // part, as order-preserving keys; the pairs are normalised, so this is
-      // their numeric order) and the lowest node among equal scores; the
-      // winning lane writes the child and moves to its next candidate
-      const int lane = tid;
-      int head = 0;
-      Cand cur = lane < F ? s_c[lane * Mk] : no_cand();
-      for (int i = 0; i < Mk; ++i) {
-        const bool live = lane < F && head < Mk;
-        // 0: no candidate left; 1: a slot past the vocabulary (after every child)
-        const uint32_t k1 = !live ? 0u : (cur.v == kNoTok ? 1u : Key<float>::of(__float_as_uint(cur.hi)));
-        const uint32_t m1 = __reduce_max_sync(0xffffffffu, k1);  // every lane takes part
-        unsigned tied = __ballot_sync(0xffffffffu, live && k1 == m1);
-        if (__popc(tied) > 1) {
-          const bool t = (tied >> lane) & 1u;
-          const uint32_t k2 = t ? Key<float>::of(__float_as_uint(cur.lo)) : 0u;
-          const uint32_t m2 = __reduce_max_sync(0xffffffffu, k2);
-          tied = __ballot_sync(0xffffffffu, t && k2 == m2);
-        }
-        if (lane == __ffs(tied) - 1) {
-          const long long o = static_cast<long long>(b) * Mk + i;
-          const bool ok = !st && cur.v != kNoTok;
-          a.parent[o] = ok ? cur.f : -1;
-          a.token[o] = ok ? cur.v : -1;
-          a.score[o] = ok ? cur.hi + cur.lo : NAN;
-          if (++head < Mk) cur = s_c[lane * Mk + head];
-        }
-      }
-      if (lane == 0) a.row_status[b] = st;
-    }
+  if (F <= 32) {
+    if (tid < 32) merge_tree_warp(a, b, s_c, tid);
     return;
+  }
+  if (tid < 32) {
+    const int st = tree_status(a, b, tid);
+    if (tid == 0) *s_st = st;
   }
   int n2 = 1;
   while (n2 < n) n2 <<= 1;
-  for (int i = tid; i < n2; i += kSelThreads) {
-    Cand c = no_cand();
-    if (i < n) {
-      const int f = i / Mk;
-      c = static_cast<const Cand*>(a.cand)[static_cast<long long>(b) * n + i];
-      c.f = f;
-      const float2 sc = ds_add(make_float2(c.hi, c.lo), make_float2(a.logc[static_cast<long long>(b) * F + f], 0.f));
-      c.hi = sc.x > -INFINITY ? sc.x : -INFINITY;
-      c.lo = sc.x > -INFINITY ? sc.y : 0.f;
-      if (c.v < 0) c = no_cand();  // a slot past the vocabulary
-    }
-    s_c[i] = c;
-  }
+  for (int i = tid; i < n2; i += kSelThreads) s_c[i] = i < n ? tree_cand(a, b, i) : no_cand();
   __syncthreads();
   const int st = *s_st;
 #pragma unroll 1
