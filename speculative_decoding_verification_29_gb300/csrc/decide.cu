@@ -18,10 +18,18 @@ __global__ void __launch_bounds__(kDecideThreads) greedy_decide_kernel(DecideArg
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = a.K, V = a.V;
   __shared__ int am[kMaxK + 1];
+  __shared__ int s_x[kMaxK];
   __shared__ int s_st;
   if (tid == 0) s_st = 0;
   griddep_launch_dependents();
   __syncthreads();
+  // the draft tokens (an input the pass does not write), staged and checked
+  // while the pass drains
+  for (int k = tid; k < K; k += kDecideThreads) {
+    const int xk = a.x[static_cast<long long>(b) * K + k];
+    s_x[k] = xk;
+    if (xk < 0 || xk >= V) atomicOr(&s_st, SPEC_ROW_TOKEN);
+  }
   griddep_wait();
   for (int j = warp; j <= K; j += kW) {
     const RowRec r = fold_argmax(a.part + (static_cast<long long>(b) * (K + 1) + j) * a.P, a.P, lane);
@@ -31,10 +39,6 @@ __global__ void __launch_bounds__(kDecideThreads) greedy_decide_kernel(DecideArg
       if (bad) atomicOr(&s_st, SPEC_ROW_TARGET);
       if (a.argmax_ids) a.argmax_ids[static_cast<long long>(b) * (K + 1) + j] = am[j];
     }
-  }
-  for (int k = tid; k < K; k += kDecideThreads) {
-    const int xk = a.x[static_cast<long long>(b) * K + k];
-    if (xk < 0 || xk >= V) atomicOr(&s_st, SPEC_ROW_TOKEN);
   }
   for (int q = 0; q < 4; ++q)
     if (a.nan_out[q])
@@ -47,7 +51,7 @@ __global__ void __launch_bounds__(kDecideThreads) greedy_decide_kernel(DecideArg
   if (st == 0) {
     for (int k0 = 0; k0 < K && m == K; k0 += 32) {
       const int k = k0 + lane;
-      const bool mis = k < K && a.x[static_cast<long long>(b) * K + k] != am[k];
+      const bool mis = k < K && s_x[k] != am[k];
       const unsigned msk = __ballot_sync(0xffffffffu, mis);
       if (msk) m = k0 + __ffs(msk) - 1;
     }
@@ -56,7 +60,7 @@ __global__ void __launch_bounds__(kDecideThreads) greedy_decide_kernel(DecideArg
   }
   for (int j = lane; j <= K; j += 32) {
     int v = -1;
-    if (st == 0) v = j < m ? a.x[static_cast<long long>(b) * K + j] : (j == m ? am[m] : -1);
+    if (st == 0) v = j < m ? s_x[j] : (j == m ? am[m] : -1);
     a.out_tokens[static_cast<long long>(b) * (K + 1) + j] = v;
   }
   if (lane == 0) {
