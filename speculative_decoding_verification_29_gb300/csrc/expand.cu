@@ -8,15 +8,16 @@
 // log softmax(l_f / T)[v]; the M best children are kept, by score, ties to
 // the lower frontier node, then the lower token id. Only a node's own M most
 // probable tokens can be among them, so:
-//   rowscan (stats, and every lane's maximum) over the F rows; then, for M
-//   up to the number of stats segments, one warp per frontier row rereads
-//   the lanes whose maximum reaches the row's M-th largest segment maximum,
-//   sorts those candidates and writes the top M's log-probabilities as
-//   float pairs; other rows are selected by the whole
+//   rowscan (stats, and the maxima of every lane's two halves) over the F
+//   rows; then, for M up to the number of stats segments, one warp per
+//   frontier row rereads the half-lanes whose maximum reaches the row's M-th
+//   largest segment maximum, sorts those candidates and writes the top M's
+//   log-probabilities as float pairs; other rows are selected by the whole
 //   CTA (one filtering pass over the row for M <= 256, else radix select on
 //   order-preserving keys, then the tokens at or above the M-th key sorted
-//   by key and id); then one CTA per tree sorts the tree's F x M candidates
-//   by score (float pairs), node and token and keeps M.
+//   by key and id); then, per tree, one warp merges the F sorted lists (F <=
+//   32) or the CTA sorts all F x M candidates by score (float pairs), node
+//   and token, and the first M are kept.
 #include "select.cuh"
 
 namespace specv {
@@ -79,9 +80,9 @@ __device__ void expand_sorted(const ExpArgs& a, int row_id, const uint64_t* buf,
 }
 
 // One warp selects a frontier row: its elements at or above the M-th
-// largest segment maximum, gathered by rereading the lanes of the stats pass
-// whose maximum reaches it; false when the row needs the whole CTA (no lane
-// maxima, M above the segment count or >= V, too many candidates).
+// largest segment maximum, gathered by rereading the half-lanes of the stats
+// pass whose maximum reaches it; false when the row needs the whole CTA (no
+// lane records, M above the segment count or >= V, too many candidates).
 template <typename Raw, bool VEC>
 __device__ bool expand_list_row(const ExpArgs& a, int row_id, uint64_t* buf, int* chunks, float* cmax, int lane) {
   if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
@@ -256,7 +257,7 @@ __device__ void merge_tree(const ExpArgs& a, int b, Cand* s_c, int* s_st) {
 }
 
 // Eight frontier rows per CTA: one warp each, or the whole CTA for a row
-// with too many candidates or no lane maxima.
+// with too many candidates or no lane records.
 template <typename Raw, bool VEC>
 __global__ void __launch_bounds__(kSelThreads, 2) expand_rows_kernel(ExpArgs a) {
   using KY = Key<Raw>;

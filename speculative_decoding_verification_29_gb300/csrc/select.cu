@@ -11,8 +11,9 @@
 // unsigned image of the logit's bits.
 //
 // After the stats pass (its partials give M and Z; in its top-k mode also
-// every lane's maximum). A row whose top-k has few candidates is selected by
-// one warp: the lanes whose maximum reaches the row's bound are reread, the
+// the maxima of every lane's two halves). A row whose top-k has few
+// candidates is selected by one warp: the half-lanes whose maximum reaches
+// the row's bound are reread, the
 // candidates sorted in registers, the top-k threshold is their k-th entry,
 // then the top-p scan and the kept mass by shuffles. Every other row is
 // selected by a whole CTA:
@@ -135,9 +136,9 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
 
 // One warp selects a row: the row's elements at or above a lower bound t0
 // of its k-th largest logit (the k-th largest segment maximum), gathered by
-// rereading the lanes of the stats pass whose maximum reaches t0; false when
-// the row needs the whole CTA (no top-k, no lane maxima, too many
-// candidates).
+// rereading the half-lanes of the stats pass whose maximum reaches t0;
+// false when the row needs the whole CTA (no top-k, no lane records, too
+// many candidates).
 template <typename Raw, bool VEC>
 __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int* chunks, float* cmax, int lane) {
   if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
