@@ -137,3 +137,22 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.spec_expand_workspace_bytes(2, 4, 64, 8, 1) % 256 == 0
     assert lib.spec_expand_workspace_bytes(2, 64, 64, 64, 1) == 0
     assert lib.spec_status_string(-2) == b"workspace missing, misaligned or too small"
+
+
+def test_host_buffer_binding_rejects_device_or_strided_inputs(lib):
+    """The host-buffer binding takes contiguous CPU tensors of the ABI's
+    dtypes and refuses anything else before any copy is enqueued."""
+    import torch
+
+    import speculative_decoding_verification_29_gb300 as sv
+
+    B, K, V = 2, 3, 64
+    Lp, Lq = torch.zeros(B, K + 1, V), torch.zeros(B, K, V)
+    x, ua, ur = torch.zeros(B, K, dtype=torch.int32), torch.zeros(B, K), torch.zeros(B)
+    with pytest.raises(ValueError, match="target_logits"):
+        sv.spec_verify_chain_host(torch.zeros(B, V, K + 1).transpose(1, 2), Lq, x, ua, ur, 1.0)
+    with pytest.raises(ValueError, match="draft_tokens"):
+        sv.spec_verify_chain_host(Lp, Lq, x.long(), ua, ur, 1.0)
+    with pytest.raises(ValueError, match="draft_logits"):
+        sv.spec_verify_chain_host(Lp, Lq.bfloat16(), x, ua, ur, 1.0)
+    assert sv.host_workspace_bytes(B, K, V, torch.float32) == lib.spec_host_workspace_bytes(B, K, V, 0)
