@@ -126,12 +126,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // PDL: wait until the preceding kernel in the stream has completed and its
 // writes are visible (returns at once when launched without PDL).
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -234,7 +228,6 @@ __device__ __forceinline__ float2 ds_div(float2 a, float2 b) {
   float hi = q + r;
   return make_float2(hi, r - (hi - q));
 }
-__device__ __forceinline__ double ds_to_d(float2 a) { return static_cast<double>(a.x) + static_cast<double>(a.y); }
 // hi + lo > t.hi + t.lo for normalised float pairs.
 __device__ __forceinline__ bool ds_gt(float2 a, float2 t) { return a.x > t.x || (a.x == t.x && a.y > t.y); }
 
