@@ -12,6 +12,8 @@
  *     p_K when all K are accepted (Leviathan et al., as summarised on the
  *     ariser.io page, section on keeping the same distribution; lotook.com,
  *     "how does speculative decoding work step by step").
+ *   - spec_verify_chain_host: the same from and to host buffers (the copies
+ *     are enqueued with the kernels on the caller's stream).
  *   - spec_verify_chain_warped: the same with top-k / top-p applied to p and
  *     q (ariser.io page: p and q must reflect the sampling settings).
  *   - spec_verify_chain_greedy: temperature 0, accept while x_k is the
@@ -36,7 +38,8 @@
  *     (lotook.com, KV-cache section; SubSpec review, step "Update KV").
  *
  * Conventions shared by every call.
- *   - Pointers marked "device" are device pointers owned by the caller; the
+ *   - Pointers marked "device" are device pointers owned by the caller (only
+ *     spec_verify_chain_host takes host buffers for its inputs and outputs); the
  *     library allocates nothing, takes no ownership and keeps no pointer after
  *     the call returns. `stream` is a cudaStream_t (NULL = legacy default).
  *   - Calls are asynchronous: they validate sizes and pointers on the host,
