@@ -55,6 +55,8 @@ class LibraryMissing(ImportError):
 def load(path: str = LIB_PATH):
     """Load the CUDA library once; raise LibraryMissing if it was not built."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(path):

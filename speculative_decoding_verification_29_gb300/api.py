@@ -31,15 +31,22 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 def _dev(t: torch.Tensor, device, dtype=None) -> torch.Tensor:
-    if t.device.type != "cuda":
+    if t.is_cuda and (dtype is None or t.dtype == dtype) and t.is_contiguous():
+        return t  # the common case, kept cheap: small batches are bound by this host path
+    if not t.is_cuda:
         t = t.to(device, non_blocking=True)
     if dtype is not None and t.dtype != dtype:
         t = t.to(dtype)
     return t.contiguous()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_stream is not None:  # the current stream's handle without building a Stream object
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -74,7 +81,7 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_res
     Returns accept_len, out_tokens, row_status and (with ``stats``)
     lse_target, lse_draft, p_at_x, q_at_x."""
     lib = _lib.load()
-    dev = target_logits.device if target_logits.device.type == "cuda" else torch.device(device)
+    dev = target_logits.device if target_logits.is_cuda else torch.device(device)
     Lp = _dev(target_logits, dev)
     Lq = _dev(draft_logits, dev)
     x = _dev(draft_tokens, dev, torch.int32)
@@ -190,7 +197,7 @@ def spec_verify_chain_greedy(target_logits, draft_tokens, out: Optional[Dict[str
                              stream=None) -> Dict[str, torch.Tensor]:
     """Greedy chain verification: accept_len, out_tokens, argmax_ids, row_status."""
     lib = _lib.load()
-    dev = target_logits.device if target_logits.device.type == "cuda" else torch.device(device)
+    dev = target_logits.device if target_logits.is_cuda else torch.device(device)
     Lp = _dev(target_logits, dev)
     x = _dev(draft_tokens, dev, torch.int32)
     B, K1, V = Lp.shape
@@ -381,7 +388,7 @@ def spec_verify_chain_warped(target_logits, draft_logits, draft_tokens, u_accept
     """Chain verification with top-k / top-p applied to p and q (0 and 1.0:
     off). Returns accept_len, out_tokens, row_status, p_at_x, q_at_x."""
     lib = _lib.load()
-    dev = target_logits.device if target_logits.device.type == "cuda" else torch.device(device)
+    dev = target_logits.device if target_logits.is_cuda else torch.device(device)
     Lp, Lq = _dev(target_logits, dev), _dev(draft_logits, dev)
     B, K1, V = Lp.shape
     K = K1 - 1
