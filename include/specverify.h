@@ -134,15 +134,16 @@ int spec_verify_chain(const void* target_logits, const void* draft_logits, int d
 size_t spec_host_workspace_bytes(int B, int K, int V, int dtype);
 
 /* spec_verify_chain from and to HOST buffers, for callers whose logits are
- * in host memory. The call enqueues on `stream`, in order: one
- * cudaMemcpyAsync host-to-device per input into the workspace, the
- * verification kernels, and one cudaMemcpyAsync device-to-host per output
- * (accept_len, out_tokens, row_status; no float outputs). It returns once
- * they are enqueued: the caller synchronises the stream before reading the
- * outputs, and keeps every host buffer valid and unmodified until then.
- * Pinned host memory (cudaHostAlloc / cudaHostRegister) makes the copies
- * asynchronous; pageable memory works but the runtime stages it
- * synchronously. Arguments and row_status as spec_verify_chain (at T == 0
+ * in host memory. The call enqueues on `stream`, in order: a
+ * cudaMemcpyAsync host-to-device of the target (and draft) logits into the
+ * workspace, the verification kernels, and the results. Pinned host buffers
+ * (cudaHostAlloc / cudaHostRegister) of the draft tokens, the uniforms and
+ * the outputs (accept_len, out_tokens, row_status; no float outputs) are
+ * read and written by the kernels in place; pageable ones are staged by one
+ * cudaMemcpyAsync each (which the runtime performs synchronously). The call
+ * returns once everything is enqueued: the caller synchronises the stream
+ * before reading the outputs, and keeps every host buffer valid and
+ * unmodified until then. Arguments and row_status as spec_verify_chain (at T == 0
  * draft_logits, u_accept and u_resample are not read); workspace: device
  * memory of spec_host_workspace_bytes bytes, 256-byte aligned. Host-side
  * errors (SPEC_ERR_ARG, SPEC_ERR_WORKSPACE, ...) return before any copy is

@@ -248,6 +248,19 @@ int chain_sample(const ChainCall& c) {
   return cuda_status(launch_chain_tail(t, c.dtype, vec, c.st));
 }
 
+// The device address of a host buffer the GPU reads and writes in place
+// (pinned memory: cudaHostAlloc / cudaHostRegister), or NULL for memory that
+// must be staged by a copy (pageable memory).
+const void* mapped(const void* p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // an unknown pointer: staged
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 // Device workspace of spec_verify_chain_host: the staged inputs, the
 // outputs, then the verification workspace (every region 256-byte aligned).
 struct HostLayout {
@@ -345,34 +358,40 @@ int spec_verify_chain_host(const void* target_logits, const void* draft_logits, 
   if ((e = check_workspace(workspace, workspace_bytes, L.total))) return e;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t es = elem_size(dtype), b = static_cast<size_t>(B), k = static_cast<size_t>(K);
-  // one copy per buffer, in stream order with the kernels
+  // the logits are copied (one stream of HBM reads beats reading the host
+  // link from every CTA); the small inputs and the outputs are read and
+  // written in place when pinned, else staged by one copy each
   struct Copy {
     void* dst;
     const void* src;
     size_t n;
   };
+  const void* in_dev[5] = {nullptr, nullptr, mapped(draft_tokens), sampling ? mapped(u_accept) : nullptr,
+                           sampling ? mapped(u_resample) : nullptr};
   const Copy in[5] = {{at(workspace, L.Lp), target_logits, b * (k + 1) * V * es},
                       {at(workspace, L.Lq), sampling ? draft_logits : nullptr, b * k * V * es},
                       {at(workspace, L.x), draft_tokens, b * k * sizeof(int32_t)},
                       {at(workspace, L.ua), sampling ? u_accept : nullptr, b * k * sizeof(float)},
                       {at(workspace, L.ur), sampling ? u_resample : nullptr, b * sizeof(float)}};
-  for (const Copy& c : in)
-    if (c.src && c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  for (int i = 0; i < 5; ++i)
+    if (!in_dev[i] && in[i].src && in[i].n &&
+        cudaMemcpyAsync(in[i].dst, in[i].src, in[i].n, cudaMemcpyHostToDevice, st) != cudaSuccess)
       return SPEC_ERR_CUDA;
-  int32_t* acc = reinterpret_cast<int32_t*>(at(workspace, L.acc));
-  int32_t* tok = reinterpret_cast<int32_t*>(at(workspace, L.tok));
-  int32_t* rs = reinterpret_cast<int32_t*>(at(workspace, L.st));
+  auto src = [&](int i) { return in_dev[i] ? in_dev[i] : static_cast<const void*>(in[i].dst); };
+  void* out_dev[3] = {const_cast<void*>(mapped(accept_len)), const_cast<void*>(mapped(out_tokens)),
+                      const_cast<void*>(mapped(row_status))};
+  const Copy out[3] = {{accept_len, at(workspace, L.acc), b * sizeof(int32_t)},
+                       {out_tokens, at(workspace, L.tok), b * (k + 1) * sizeof(int32_t)},
+                       {row_status, at(workspace, L.st), b * sizeof(int32_t)}};
+  auto dst = [&](int i) { return static_cast<int32_t*>(out_dev[i] ? out_dev[i] : const_cast<void*>(out[i].src)); };
   e = spec_verify_chain(at(workspace, L.Lp), sampling ? at(workspace, L.Lq) : nullptr, dtype,
-                        reinterpret_cast<const int32_t*>(at(workspace, L.x)),
-                        reinterpret_cast<const float*>(at(workspace, L.ua)),
-                        reinterpret_cast<const float*>(at(workspace, L.ur)), temperature, B, K, V, acc, tok, nullptr,
-                        nullptr, nullptr, nullptr, rs, at(workspace, L.ws), workspace_bytes - L.ws, stream);
+                        static_cast<const int32_t*>(src(2)), static_cast<const float*>(src(3)),
+                        static_cast<const float*>(src(4)), temperature, B, K, V, dst(0), dst(1), nullptr, nullptr,
+                        nullptr, nullptr, dst(2), at(workspace, L.ws), workspace_bytes - L.ws, stream);
   if (e) return e;
-  const Copy out[3] = {{accept_len, acc, b * sizeof(int32_t)},
-                       {out_tokens, tok, b * (k + 1) * sizeof(int32_t)},
-                       {row_status, rs, b * sizeof(int32_t)}};
-  for (const Copy& c : out)
-    if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToHost, st) != cudaSuccess) return SPEC_ERR_CUDA;
+  for (int i = 0; i < 3; ++i)
+    if (!out_dev[i] && cudaMemcpyAsync(out[i].dst, out[i].src, out[i].n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
