@@ -156,3 +156,29 @@ def test_host_buffer_binding_rejects_device_or_strided_inputs(lib):
     with pytest.raises(ValueError, match="draft_logits"):
         sv.spec_verify_chain_host(Lp, Lq.bfloat16(), x, ua, ur, 1.0)
     assert sv.host_workspace_bytes(B, K, V, torch.float32) == lib.spec_host_workspace_bytes(B, K, V, 0)
+
+
+def test_plain_c_caller_links_against_the_library(lib):
+    """The header is plain C99 and a C program links against the library and
+    calls a size query (no GPU needed for it)."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    from speculative_decoding_verification_29_gb300 import _lib
+
+    from pathlib import Path
+
+    work = Path(_lib.HERE) / "_build" / "c_caller"  # in-tree build folder (git-ignored)
+    work.mkdir(parents=True, exist_ok=True)
+    src = work / "caller.c"
+    src.write_text('#include "specverify.h"\n#include <stdio.h>\n'
+                   'int main(void) { size_t n = spec_workspace_bytes(64, 8, 128256, SPEC_BF16);\n'
+                   '  printf("%zu\\n", n); return n > 0 ? 0 : 1; }\n')
+    exe = work / "caller"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-o", str(exe), "-L", libdir, "-lspecverify", "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and int(r.stdout) == lib.spec_workspace_bytes(64, 8, 128256, 1)
