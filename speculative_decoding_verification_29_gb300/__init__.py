@@ -8,6 +8,7 @@ API is lazy so that the package can be inspected without a GPU.
 __all__ = [
     "spec_verify_chain",
     "spec_verify_chain_host",
+    "prepare_verify_chain",
     "spec_chain_scan",
     "spec_chain_sample",
     "spec_verify_chain_warped",

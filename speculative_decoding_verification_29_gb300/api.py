@@ -108,6 +108,52 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_res
     return out
 
 
+def prepare_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
+                         out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                         stats: bool = False):
+    """spec_verify_chain on fixed device buffers, for a serving loop that
+    refills the same tensors every step: the checks and the argument
+    marshalling happen once here, and the returned function enqueues one
+    verification on the current stream (or on the stream it is given) and
+    returns ``out``. The tensors must stay alive and keep their shapes; their
+    contents may change between calls."""
+    lib = _lib.load()
+    dev = target_logits.device
+    ts = [_dev(t, dev, d) for t, d in ((target_logits, None), (draft_logits, None), (draft_tokens, torch.int32),
+                                      (u_accept, torch.float32), (u_resample, torch.float32))]
+    if not all(t.is_cuda for t in ts):
+        raise ValueError("prepare_verify_chain takes device tensors")
+    Lp = ts[0]
+    B, K1, V = Lp.shape
+    K = K1 - 1
+    dt = _dtype_code(Lp)
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+        if stats:
+            out.update(lse_target=torch.empty(B, K + 1, device=dev), lse_draft=torch.empty(B, K, device=dev),
+                       p_at_x=torch.empty(B, K, device=dev), q_at_x=torch.empty(B, K, device=dev))
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(B, K, V, dt), dev)
+    fn = lib.spec_verify_chain
+    head = (Lp.data_ptr(), ts[1].data_ptr(), dt, ts[2].data_ptr(), ts[3].data_ptr(), ts[4].data_ptr(),
+            float(temperature), B, K, V, out["accept_len"].data_ptr(), out["out_tokens"].data_ptr(),
+            _ptr(out.get("lse_target")), _ptr(out.get("lse_draft")), _ptr(out.get("p_at_x")), _ptr(out.get("q_at_x")),
+            out["row_status"].data_ptr(), workspace.data_ptr(), workspace.numel())
+    keep = (ts, workspace)  # the buffers the pointers refer to stay alive with the function
+    index = dev.index if dev.index is not None else torch.cuda.current_device()
+
+    def call(stream=None):
+        rc = fn(*head, _raw_stream(index) if stream is None and _raw_stream is not None else _stream(stream))
+        if rc:
+            check("spec_verify_chain", rc)
+        return out
+
+    call.buffers = keep
+    return call
+
+
 def host_workspace_bytes(B: int, K: int, V: int, dtype) -> int:
     """Device workspace for spec_verify_chain_host (staged inputs and
     outputs plus the verification workspace)."""

@@ -141,6 +141,27 @@ def test_first_token_law_statistical():
     assert np.all(np.abs(counts - n * p0) <= 5 * sigma + 1), (counts, n * p0, sigma)
 
 
+def test_prepared_call_matches_the_plain_call():
+    """prepare_verify_chain: one prepared call on fixed buffers, refilled
+    between calls, gives the plain call's outputs every time (and the
+    oracle's)."""
+    import speculative_decoding_verification_29_gb300 as sv
+
+    dev = torch.device("cuda")
+    c0 = gen.chain_zipf(5, 4, 3000, torch.bfloat16, 0.8, 0.7, seed=30)
+    bufs = [t.to(dev) for t in (c0.Lp, c0.Lq, c0.x, c0.ua, c0.ur)]
+    call = sv.prepare_verify_chain(*bufs, c0.T, stats=True)
+    for seed in (30, 31, 32):
+        c = gen.chain_zipf(5, 4, 3000, torch.bfloat16, 0.8, 0.7, seed=seed)
+        for b_, t in zip(bufs, (c.Lp, c.Lq, c.x, c.ua, c.ur)):
+            b_.copy_(t)
+        got = {k: v.clone() for k, v in call().items()}
+        ref = gpu_chain(c)
+        for k in ("accept_len", "out_tokens", "row_status"):
+            assert np.array_equal(got[k].cpu().numpy(), ref[k]), k
+        compare_chain({k: v.cpu().numpy() for k, v in got.items()}, oracle_chain(c))
+
+
 def test_status_rows():
     c = gen.chain_tiny(4, B=8, K=3, V=1024)
     Lp, Lq, x = c.Lp.clone(), c.Lq.clone(), c.x.clone()
