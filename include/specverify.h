@@ -78,10 +78,14 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 /* Return codes. */
 enum {
   SPEC_OK = 0,
-  SPEC_ERR_ARG = -1,        /* a size, pointer, dtype or temperature is invalid */
-  SPEC_ERR_WORKSPACE = -2,  /* workspace NULL, misaligned (256 B) or too small */
-  SPEC_ERR_CUDA = -3,       /* a kernel launch failed (cudaGetLastError) */
-  SPEC_ERR_UNSUPPORTED = -4 /* sizes beyond the documented limits */
+  SPEC_ERR_ARG = -1,           /* a size, pointer, dtype or temperature is invalid */
+  SPEC_ERR_ALIGN = -2,         /* workspace NULL, misaligned (256 B) or too small */
+  SPEC_ERR_CUDA = -3,          /* a kernel launch or an enqueued copy failed */
+  SPEC_ERR_TIMEOUT = -4,       /* reserved: no kernel of this library waits on a flag, so none times out */
+  SPEC_ERR_UNIMPLEMENTED = -5, /* sizes beyond the documented limits */
+  /* older names of the same codes */
+  SPEC_ERR_WORKSPACE = SPEC_ERR_ALIGN,
+  SPEC_ERR_UNSUPPORTED = SPEC_ERR_UNIMPLEMENTED
 };
 
 /* row_status bits. */

@@ -32,8 +32,9 @@
  *     step "Update KV"): the accepted path's entries are moved to consecutive
  *     positions and the cache length is cut after them.
  *
- * Readings where the pages are silent (each is listed with its reason in the
- * design notes): a draft token is accepted iff u < p(x)/q(x) with u in [0,1);
+ * Readings where the pages are silent: a draft token is accepted iff
+ * u < p(x)/q(x) with u in [0,1) (the pages give the probability min(1, p/q);
+ * "<" and "<=" differ on a set of measure zero);
  * one accept uniform per draft position and one resample uniform per row; a
  * discrete draw is the inverse CDF over ascending token id with a strict ">";
  * a residual of total mass zero falls back to p at that position; greedy ties

@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libspecverify.so")
 
 SPEC_F32, SPEC_BF16 = 0, 1
-SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_WORKSPACE, SPEC_ERR_CUDA, SPEC_ERR_UNSUPPORTED = 0, -1, -2, -3, -4
+SPEC_OK, SPEC_ERR_ARG, SPEC_ERR_ALIGN, SPEC_ERR_CUDA, SPEC_ERR_TIMEOUT, SPEC_ERR_UNIMPLEMENTED = 0, -1, -2, -3, -4, -5
+SPEC_ERR_WORKSPACE, SPEC_ERR_UNSUPPORTED = SPEC_ERR_ALIGN, SPEC_ERR_UNIMPLEMENTED  # older names of the same codes
 SPEC_ROW_TOKEN, SPEC_ROW_TARGET, SPEC_ROW_DRAFT, SPEC_ROW_TREE, SPEC_ROW_MASK, SPEC_ROW_WARP = 1, 2, 4, 8, 16, 32
 
 P = ctypes.c_void_p

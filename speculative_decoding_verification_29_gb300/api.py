@@ -108,6 +108,42 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_res
     return out
 
 
+def _prepared_inputs(target_logits, draft_logits, draft_tokens, u_accept, u_resample):
+    """The prepared call's inputs exactly as the caller holds them: the
+    pointers baked into the call must be the caller's own buffers, or later
+    refills would go unseen. Nothing is converted or copied; anything else is
+    refused."""
+    named = (("target_logits", target_logits), ("draft_logits", draft_logits), ("draft_tokens", draft_tokens),
+             ("u_accept", u_accept), ("u_resample", u_resample))
+    for name, t in named:
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name}: a torch tensor is required")
+    if target_logits.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"target_logits: bfloat16 or float32 required, got {target_logits.dtype}")
+    want = dict(draft_logits=target_logits.dtype, draft_tokens=torch.int32, u_accept=torch.float32,
+                u_resample=torch.float32)
+    for name, t in named[1:]:
+        if t.dtype != want[name]:
+            raise ValueError(f"{name}: {want[name]} required, got {t.dtype} (it is not converted: the prepared "
+                             f"call must read the caller's own buffer)")
+    if target_logits.dim() != 3:
+        raise ValueError(f"target_logits must be [B, K+1, V], got {tuple(target_logits.shape)}")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    shapes = dict(draft_logits=(B, K, V), draft_tokens=(B, K), u_accept=(B, K), u_resample=(B,))
+    for name, t in named[1:]:
+        if tuple(t.shape) != shapes[name]:
+            raise ValueError(f"{name} must be {list(shapes[name])}, got {list(t.shape)}")
+    for name, t in named:
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: a contiguous tensor is required (a strided view is not copied)")
+    dev = target_logits.device
+    for name, t in named:
+        if t.device.type != "cuda" or t.device != dev:
+            raise ValueError(f"{name}: a CUDA tensor on {dev} is required, got {t.device}")
+    return B, K, V
+
+
 def prepare_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature: float,
                          out: Optional[Dict[str, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
                          stats: bool = False):
@@ -115,17 +151,16 @@ def prepare_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_
     refills the same tensors every step: the checks and the argument
     marshalling happen once here, and the returned function enqueues one
     verification on the current stream (or on the stream it is given) and
-    returns ``out``. The tensors must stay alive and keep their shapes; their
+    returns ``out``. The inputs must be contiguous CUDA tensors on one device
+    with the call's dtypes (bf16 or fp32 logits of one dtype, int32 tokens,
+    fp32 uniforms): the call keeps their addresses, so a tensor that would
+    need a conversion is refused (ValueError) rather than silently replaced
+    by a copy. The tensors must stay alive and keep their shapes; their
     contents may change between calls."""
+    B, K, V = _prepared_inputs(target_logits, draft_logits, draft_tokens, u_accept, u_resample)
     lib = _lib.load()
     dev = target_logits.device
-    ts = [_dev(t, dev, d) for t, d in ((target_logits, None), (draft_logits, None), (draft_tokens, torch.int32),
-                                      (u_accept, torch.float32), (u_resample, torch.float32))]
-    if not all(t.is_cuda for t in ts):
-        raise ValueError("prepare_verify_chain takes device tensors")
-    Lp = ts[0]
-    B, K1, V = Lp.shape
-    K = K1 - 1
+    Lp = target_logits
     dt = _dtype_code(Lp)
     if out is None:
         out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
@@ -137,11 +172,13 @@ def prepare_verify_chain(target_logits, draft_logits, draft_tokens, u_accept, u_
     if workspace is None:
         workspace = alloc_workspace(workspace_bytes(B, K, V, dt), dev)
     fn = lib.spec_verify_chain
-    head = (Lp.data_ptr(), ts[1].data_ptr(), dt, ts[2].data_ptr(), ts[3].data_ptr(), ts[4].data_ptr(),
-            float(temperature), B, K, V, out["accept_len"].data_ptr(), out["out_tokens"].data_ptr(),
-            _ptr(out.get("lse_target")), _ptr(out.get("lse_draft")), _ptr(out.get("p_at_x")), _ptr(out.get("q_at_x")),
-            out["row_status"].data_ptr(), workspace.data_ptr(), workspace.numel())
-    keep = (ts, workspace)  # the buffers the pointers refer to stay alive with the function
+    head = (Lp.data_ptr(), draft_logits.data_ptr(), dt, draft_tokens.data_ptr(), u_accept.data_ptr(),
+            u_resample.data_ptr(), float(temperature), B, K, V, out["accept_len"].data_ptr(),
+            out["out_tokens"].data_ptr(), _ptr(out.get("lse_target")), _ptr(out.get("lse_draft")),
+            _ptr(out.get("p_at_x")), _ptr(out.get("q_at_x")), out["row_status"].data_ptr(), workspace.data_ptr(),
+            workspace.numel())
+    # the buffers the pointers refer to stay alive with the function
+    keep = (target_logits, draft_logits, draft_tokens, u_accept, u_resample, workspace)
     index = dev.index if dev.index is not None else torch.cuda.current_device()
 
     def call(stream=None):

@@ -636,11 +636,13 @@ const char* spec_status_string(int status) {
       return "ok";
     case SPEC_ERR_ARG:
       return "invalid argument";
-    case SPEC_ERR_WORKSPACE:
+    case SPEC_ERR_ALIGN:
       return "workspace missing, misaligned or too small";
     case SPEC_ERR_CUDA:
       return "CUDA launch failed";
-    case SPEC_ERR_UNSUPPORTED:
+    case SPEC_ERR_TIMEOUT:
+      return "timed out (reserved; not returned by this library)";
+    case SPEC_ERR_UNIMPLEMENTED:
       return "sizes beyond the library's limits";
     default:
       return "unknown status";

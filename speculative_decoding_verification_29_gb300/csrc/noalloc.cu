@@ -11,12 +11,15 @@
 //
 // The array is kNoAllocScratchBytes long and exists once per GPU that loads
 // the library, for as long as the process lives. Every call on a device uses
-// the same array and leaves its contents behind; the kernels write every
-// scratch word they later read within the same call (the completion
-// counters are cleared by the first kernel), so nothing carries over between
-// calls. Two calls whose work overlaps on the GPU (different streams, or
-// different host threads on the same device) share the array and race: the
-// caller must order them.
+// the same array and leaves its contents behind. Nothing carries over from
+// one call to the next: each kernel of a call writes every scratch word it
+// later reads within that call (no kernel keeps a counter or any other
+// state that must start at zero), and the streaming pass, the call's first
+// kernel, waits at griddepcontrol.wait until the previous kernel on the same
+// stream (the previous call's last one) has completed before it writes. Two
+// calls whose work overlaps on the GPU (different streams, or different host
+// threads on the same device) share the array and race: the caller must
+// order them.
 #include <mutex>
 
 #include "internal.h"

@@ -182,3 +182,30 @@ def test_plain_c_caller_links_against_the_library(lib):
                     "-o", str(exe), "-L", libdir, "-lspecverify", "-Wl,-rpath," + libdir], check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and int(r.stdout) == lib.spec_workspace_bytes(64, 8, 128256, 1)
+
+
+def test_prepared_call_refuses_inputs_it_would_have_to_copy():
+    """prepare_verify_chain keeps the addresses of the caller's tensors, so
+    a tensor that would need a conversion (int64 tokens, a strided view of
+    the logits, fp64 uniforms, a host tensor, a wrong shape) is refused with
+    a ValueError instead of being replaced by a private copy that later
+    refills would never reach."""
+    import torch
+
+    import speculative_decoding_verification_29_gb300 as sv
+
+    B, K, V = 2, 3, 64
+    Lp, Lq = torch.zeros(B, K + 1, V), torch.zeros(B, K, V)
+    x, ua, ur = torch.zeros(B, K, dtype=torch.int32), torch.zeros(B, K), torch.zeros(B)
+    with pytest.raises(ValueError, match="draft_tokens.*int32"):
+        sv.prepare_verify_chain(Lp, Lq, x.long(), ua, ur, 1.0)
+    with pytest.raises(ValueError, match="draft_logits.*contiguous"):
+        sv.prepare_verify_chain(Lp, torch.zeros(B, K + 1, V)[:, :K], x, ua, ur, 1.0)
+    with pytest.raises(ValueError, match="u_accept.*float32"):
+        sv.prepare_verify_chain(Lp, Lq, x, ua.double(), ur, 1.0)
+    with pytest.raises(ValueError, match="draft_logits.*bfloat16"):
+        sv.prepare_verify_chain(Lp, Lq.bfloat16(), x, ua, ur, 1.0)
+    with pytest.raises(ValueError, match="u_resample must be"):
+        sv.prepare_verify_chain(Lp, Lq, x, ua, torch.zeros(B + 1), 1.0)
+    with pytest.raises(ValueError, match="target_logits: a CUDA tensor"):
+        sv.prepare_verify_chain(Lp, Lq, x, ua, ur, 1.0)
