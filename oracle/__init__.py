@@ -88,6 +88,15 @@ def _declare(lib):
     lib.orc_tree_entropy.restype = None
     lib.orc_verify_chain_warped.argtypes = [P, P, i, P, P, P, d, i, d, i, i, i, i, i, P, P, P, P, P, P, P, P, P, P]
     lib.orc_verify_chain_warped.restype = None
+    lib.orc_verify_chain_near.argtypes = [P, P, i, P, P, P, d, i, i, i, i, i, d, P, P, P, P, P, P, P, P, P, P]
+    lib.orc_verify_chain_near.restype = None
+    lib.orc_verify_chain_warped_near.argtypes = [P, P, i, P, P, P, d, i, d, i, i, i, i, i, d, d, P, P, P, P, P, P, P,
+                                                 P, P, P]
+    lib.orc_verify_chain_warped_near.restype = None
+    lib.orc_chain_valid.argtypes = [P, P, i, P, P, P, d, i, i, i, i, i, d, P, P, P]
+    lib.orc_chain_valid.restype = None
+    lib.orc_chain_warped_valid.argtypes = [P, P, i, P, P, P, d, i, d, i, i, i, i, i, d, d, P, P, P, P, P, P, P, P]
+    lib.orc_chain_warped_valid.restype = None
     lib.orc_tree_expand.argtypes = [P, i, d, P, i, i, i, i, P, P, P, P, P, P]
     lib.orc_tree_expand.restype = None
     return lib
@@ -156,16 +165,11 @@ def _run(fn, B: int, threads: int):
 
 # ------------------------------------------------------------- functions --
 
-def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None) -> Dict[str, np.ndarray]:
-    """Speculative-sampling chain verification (T > 0) in fp64.
+NEAR = 1e-6  # the flag window on uniforms the pages' tolerance states
+NEAR_P = 1e-6  # the flag window on top-p cuts, relative to the kept mass
 
-    Returns accept_len [B], out_tokens [B, K+1], lse_p [B, K+1], lse_q [B, K],
-    px / qx [B, K] (target / draft probability of each draft token), status [B],
-    flags [B] (FL_ACCEPT / FL_SAMPLE: a uniform within 1e-6 of a decision
-    boundary) and margin [B] (distance to the nearest boundary met)."""
-    if not T > 0:
-        raise ValueError("verify_chain needs T > 0; use verify_chain_greedy for T == 0")
-    lib = lib or load()
+
+def _chain_inputs(Lp, Lq, x, ua, ur):
     lp, dt = _logits(Lp)
     lq, dtq = _logits(Lq)
     if dtq != dt:
@@ -175,6 +179,23 @@ def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None) -> Dic
     xs = _np(x, np.int32).reshape(B, K)
     uas = _np(ua, np.float64).reshape(B, K)
     urs = _np(ur, np.float64).reshape(B)
+    return lp, lq, dt, xs, uas, urs, B, K, V
+
+
+def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None,
+                 near: float = NEAR) -> Dict[str, np.ndarray]:
+    """Speculative-sampling chain verification (T > 0) in fp64.
+
+    Returns accept_len [B], out_tokens [B, K+1], lse_p [B, K+1], lse_q [B, K],
+    px / qx [B, K] (target / draft probability of each draft token), status [B],
+    flags [B] (FL_ACCEPT / FL_SAMPLE: a uniform within ``near`` of a decision
+    boundary), margin [B] (distance to the nearest boundary met) and pflag [B]
+    (the probability of a flag at that window over the row's uniforms, given
+    its distributions and its first rejection)."""
+    if not T > 0:
+        raise ValueError("verify_chain needs T > 0; use verify_chain_greedy for T == 0")
+    lib = lib or load()
+    lp, lq, dt, xs, uas, urs, B, K, V = _chain_inputs(Lp, Lq, x, ua, ur)
     out = dict(
         accept_len=np.empty(B, np.int32),
         out_tokens=np.empty((B, K + 1), np.int32),
@@ -185,36 +206,49 @@ def verify_chain(Lp, Lq, x, ua, ur, T: float, threads: int = 1, lib=None) -> Dic
         status=np.empty(B, np.int32),
         flags=np.empty(B, np.int32),
         margin=np.empty(B, np.float64),
+        pflag=np.empty(B, np.float64),
     )
 
     def part(b0, b1):
-        lib.orc_verify_chain(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), B, K, V,
-                             b0, b1, _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["lse_p"]),
-                             _ptr(out["lse_q"]), _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["status"]),
-                             _ptr(out["flags"]), _ptr(out["margin"]))
+        lib.orc_verify_chain_near(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), B, K, V,
+                                  b0, b1, float(near), _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+                                  _ptr(out["lse_p"]), _ptr(out["lse_q"]), _ptr(out["px"]), _ptr(out["qx"]),
+                                  _ptr(out["status"]), _ptr(out["flags"]), _ptr(out["margin"]), _ptr(out["pflag"]))
 
     _run(part, B, threads)
     return out
 
 
+def chain_valid(Lp, Lq, x, ua, ur, T: float, accept_len, out_tokens, near: float = NEAR, threads: int = 1,
+                lib=None) -> np.ndarray:
+    """For each row, whether the given outcome (accept_len [B], out_tokens
+    [B, K+1]) is exactly what verify_chain emits with every uniform of the
+    row moved by at most ``near`` inside [0, 1). Returns a bool array [B]."""
+    lib = lib or load()
+    lp, lq, dt, xs, uas, urs, B, K, V = _chain_inputs(Lp, Lq, x, ua, ur)
+    acc = np.ascontiguousarray(accept_len, np.int32).reshape(B)
+    tok = np.ascontiguousarray(out_tokens, np.int32).reshape(B, K + 1)
+    valid = np.empty(B, np.int32)
+
+    def part(b0, b1):
+        lib.orc_chain_valid(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), B, K, V, b0, b1,
+                            float(near), _ptr(acc), _ptr(tok), _ptr(valid))
+
+    _run(part, B, threads)
+    return valid.astype(bool)
+
+
 def verify_chain_warped(Lp, Lq, x, ua, ur, T: float, top_k: int = 0, top_p: float = 1.0, threads: int = 1,
-                        lib=None) -> Dict[str, np.ndarray]:
+                        lib=None, near: float = NEAR, near_p: float = NEAR_P) -> Dict[str, np.ndarray]:
     """Chain verification with the sampling settings applied to p and q:
     temperature T, then top-k (ties kept; 0 = off), then top-p (1.0 = off).
     Returns accept_len, out_tokens, px / qx (warped probabilities of the draft
-    tokens), status, flags, margin as verify_chain."""
+    tokens), status, flags, margin as verify_chain; FL_WARP flags a top-p cut
+    within ``near_p`` (relative to the kept mass) of its target."""
     if not T > 0 or not top_p > 0:
         raise ValueError("needs T > 0 and top_p > 0")
     lib = lib or load()
-    lp, dt = _logits(Lp)
-    lq, dtq = _logits(Lq)
-    if dtq != dt:
-        raise TypeError("target and draft logits must share a dtype")
-    B, K1, V = lp.shape
-    K = K1 - 1
-    xs = _np(x, np.int32).reshape(B, K)
-    uas = _np(ua, np.float64).reshape(B, K)
-    urs = _np(ur, np.float64).reshape(B)
+    lp, lq, dt, xs, uas, urs, B, K, V = _chain_inputs(Lp, Lq, x, ua, ur)
     out = dict(accept_len=np.empty(B, np.int32), out_tokens=np.empty((B, K + 1), np.int32),
                px=np.empty((B, K), np.float64), qx=np.empty((B, K), np.float64), status=np.empty(B, np.int32),
                flags=np.empty(B, np.int32), margin=np.empty(B, np.float64))
@@ -222,13 +256,37 @@ def verify_chain_warped(Lp, Lq, x, ua, ur, T: float, top_k: int = 0, top_p: floa
     def part(b0, b1):
         wp, wq = np.empty(V, np.float64), np.empty(V, np.float64)
         tmp = np.empty(V * 16, np.uint8)  # {double, int} entries, 16 bytes each
-        lib.orc_verify_chain_warped(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), int(top_k),
-                                    float(top_p), B, K, V, b0, b1, _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
-                                    _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["status"]), _ptr(out["flags"]),
-                                    _ptr(out["margin"]), _ptr(wp), _ptr(wq), _ptr(tmp))
+        lib.orc_verify_chain_warped_near(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T),
+                                         int(top_k), float(top_p), B, K, V, b0, b1, float(near), float(near_p),
+                                         _ptr(out["accept_len"]), _ptr(out["out_tokens"]), _ptr(out["px"]),
+                                         _ptr(out["qx"]), _ptr(out["status"]), _ptr(out["flags"]),
+                                         _ptr(out["margin"]), _ptr(wp), _ptr(wq), _ptr(tmp))
 
     _run(part, B, threads)
     return out
+
+
+def chain_warped_valid(Lp, Lq, x, ua, ur, T: float, top_k: int, top_p: float, accept_len, out_tokens,
+                       near: float = NEAR, near_p: float = NEAR_P, threads: int = 1, lib=None) -> np.ndarray:
+    """chain_valid for warped verification: besides the uniforms (moved by
+    at most ``near``), the top-p cut of each row the outcome depends on may
+    fall at any value group within ``near_p`` of its target."""
+    lib = lib or load()
+    lp, lq, dt, xs, uas, urs, B, K, V = _chain_inputs(Lp, Lq, x, ua, ur)
+    acc = np.ascontiguousarray(accept_len, np.int32).reshape(B)
+    tok = np.ascontiguousarray(out_tokens, np.int32).reshape(B, K + 1)
+    valid = np.empty(B, np.int32)
+
+    def part(b0, b1):
+        wp, wq = np.empty(V, np.float64), np.empty(V, np.float64)
+        tmp = np.empty(V * 16, np.uint8)
+        nalt, alt = np.empty(2 * K + 2, np.int32), np.empty(2 * K + 2, np.int32)
+        lib.orc_chain_warped_valid(_ptr(lp), _ptr(lq), dt, _ptr(xs), _ptr(uas), _ptr(urs), float(T), int(top_k),
+                                   float(top_p), B, K, V, b0, b1, float(near), float(near_p), _ptr(acc), _ptr(tok),
+                                   _ptr(valid), _ptr(wp), _ptr(wq), _ptr(tmp), _ptr(nalt), _ptr(alt))
+
+    _run(part, B, threads)
+    return valid.astype(bool)
 
 
 def verify_chain_greedy(Lp, x, threads: int = 1, lib=None) -> Dict[str, np.ndarray]:

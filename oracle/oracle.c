@@ -118,6 +118,12 @@ static int row_argmax(const void* L, int dt, size_t off, int V, int* nan) {
   return *nan ? -1 : best;
 }
 
+/* Measure of the uniforms u in [0, 1) with |u - r| < near. */
+static double window_measure(double r, double near) {
+  double lo = fmax(0.0, r - near), hi = fmin(1.0, r + near);
+  return hi > lo ? hi - lo : 0.0;
+}
+
 /* Speculative-sampling chain verification, T > 0, rows b in [b0, b1).
  * Lp: target logits [B][K+1][V]; Lq: draft logits [B][K][V]; x: [B][K];
  * ua: [B][K] accept uniforms; ur: [B] resample uniforms.
@@ -127,11 +133,10 @@ static int row_argmax(const void* L, int dt, size_t off, int V, int* nan) {
  * row's uniforms to the nearest decision boundary it met: every tested
  * acceptance threshold r_k < 1 and the two CDF boundaries of the drawn token;
  * +inf when none). */
-void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
-                      const double* ur, double T, int B, int K, int V, int b0, int b1,
-                      int32_t* accept_len, int32_t* out_tok, double* lse_p, double* lse_q, double* px,
-                      double* qx, int32_t* status, int32_t* flags, double* margin) {
-  (void)B;
+static void chain_rows(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                       const double* ur, double T, int K, int V, int b0, int b1, double near,
+                       int32_t* accept_len, int32_t* out_tok, double* lse_p, double* lse_q, double* px,
+                       double* qx, int32_t* status, int32_t* flags, double* margin, double* pflag) {
   double Mp[K + 1], Zp[K + 1], Mq[K + 1], Zq[K + 1];
   for (int b = b0; b < b1; ++b) {
     int st = 0, fl = 0;
@@ -159,6 +164,7 @@ void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, 
       accept_len[b] = -1;
       flags[b] = 0;
       margin[b] = INFINITY;
+      if (pflag) pflag[b] = 0.0;
       continue;
     }
     for (int k = 0; k < K; ++k) {
@@ -168,12 +174,14 @@ void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, 
     }
     /* left-to-right acceptance test; m = first rejection, K if none */
     int m = K;
+    double pf = 0.0; /* probability that a uniform of this row falls within `near` of a boundary */
     for (int k = 0; k < K; ++k) {
       double p = px[(size_t)b * K + k], q = qx[(size_t)b * K + k];
       double r = q > 0.0 ? p / q : INFINITY;
       double u = ua[(size_t)b * K + k];
       if (r < 1.0) mg = fmin(mg, fabs(u - r));
-      if (r < 1.0 && fabs(u - r) < NEAR) fl |= FL_ACCEPT;
+      if (r < 1.0 && fabs(u - r) < near) fl |= FL_ACCEPT;
+      if (r < 1.0) pf += window_measure(r, near);
       if (!(u < r)) {
         m = k;
         break;
@@ -198,6 +206,14 @@ void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, 
       for (int v = 0; v < V; ++v) S += prob(Lp, dt, offp, v, T, Mp[m], Zp[m]);
     }
     /* inverse CDF: smallest i with C_i > u * S */
+    if (pflag) {
+      for (int v = 0; v < V; ++v) {
+        double w = prob(Lp, dt, offp, v, T, Mp[m], Zp[m]);
+        if (residual) w = fmax(0.0, w - prob(Lq, dt, offq, v, T, Mq[m], Zq[m]));
+        pf += fmin(w / S, 2.0 * near);
+      }
+      pflag[b] = fmin(pf, 1.0);
+    }
     double t = ur[b] * S, C = 0.0, Cprev = 0.0;
     int tok = -1, last_pos = -1;
     for (int v = 0; v < V; ++v) {
@@ -216,14 +232,41 @@ void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, 
       fl |= FL_SAMPLE;
       mg = 0.0;
     } else {
-      double near = fmin(fabs(ur[b] - Cprev / S), fabs(ur[b] - C / S));
-      mg = fmin(mg, near);
-      if (near < NEAR) fl |= FL_SAMPLE;
+      double dist = fmin(fabs(ur[b] - Cprev / S), fabs(ur[b] - C / S));
+      mg = fmin(mg, dist);
+      if (dist < near) fl |= FL_SAMPLE;
     }
     out[m] = tok;
     flags[b] = fl;
     margin[b] = mg;
   }
+}
+
+/* Speculative-sampling chain verification, T > 0, rows b in [b0, b1), with
+ * the pages' flag window NEAR (see chain_rows for the arguments). */
+void orc_verify_chain(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                      const double* ur, double T, int B, int K, int V, int b0, int b1,
+                      int32_t* accept_len, int32_t* out_tok, double* lse_p, double* lse_q, double* px,
+                      double* qx, int32_t* status, int32_t* flags, double* margin) {
+  (void)B;
+  chain_rows(Lp, Lq, dt, x, ua, ur, T, K, V, b0, b1, NEAR, accept_len, out_tok, lse_p, lse_q, px, qx, status,
+             flags, margin, NULL);
+}
+
+/* The same with the flag window `near` chosen by the caller, and, per row,
+ * pflag [B]: the probability, over the row's uniforms, of a flag at that
+ * window given the row's distributions and its first rejection m: for every
+ * tested acceptance threshold r_k < 1 the measure of the uniforms within
+ * `near` of it, plus, for the draw, sum over tokens t of min(w_t / S,
+ * 2 near) (a uniform lands in token t's interval of width w_t / S and within
+ * `near` of one of its ends). The sum is capped at 1. */
+void orc_verify_chain_near(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                           const double* ur, double T, int B, int K, int V, int b0, int b1, double near,
+                           int32_t* accept_len, int32_t* out_tok, double* lse_p, double* lse_q, double* px,
+                           double* qx, int32_t* status, int32_t* flags, double* margin, double* pflag) {
+  (void)B;
+  chain_rows(Lp, Lq, dt, x, ua, ur, T, K, V, b0, b1, near, accept_len, out_tok, lse_p, lse_q, px, qx, status,
+             flags, margin, pflag);
 }
 
 /* Greedy chain verification (temperature 0), rows b in [b0, b1).
@@ -545,14 +588,22 @@ static int orc_sv_desc(const void* a, const void* b) {
 }
 
 /* Warped distribution of one row into out[V] (tmp: V scratch entries).
- * Returns 1 when the row holds a NaN or has no finite maximum. *near is set
- * when the top-p decision of a value group lies within NEAR_P (relative to
- * the renormalised mass) of the boundary: its preceding mass is that close
- * to top_p. */
-#define NEAR_P 1e-5
-static int warped_row(const void* L, int dt, size_t off, int V, double T, int top_k, double top_p, double* out,
-                      orc_sv* tmp, int* near) {
+ * Returns 1 when the row holds a NaN or has no finite maximum.
+ *
+ * Top-p near ties. The mass before a value group (cum, the kept mass of the
+ * larger values) is compared with top_p * Zk; a group whose cum lies within
+ * near_p * Zk of that target is a near group, and *nnear (when given)
+ * receives their number. An implementation whose kept masses carry a
+ * relative error below near_p / 2 may draw the line at any near group, or
+ * keep them all: `alt` selects the cut. alt = 0 is the rule itself (keep a
+ * group iff cum < top_p * Zk); alt = 1 keeps every group with cum below the
+ * target plus the band; alt = 2 + j drops the j-th near group and every
+ * smaller value. */
+#define NEAR_P 1e-6
+static int warped_row_alt(const void* L, int dt, size_t off, int V, double T, int top_k, double top_p,
+                          double near_p, int alt, double* out, orc_sv* tmp, int* nnear) {
   double M, Z;
+  if (nnear) *nnear = 0;
   if (softmax_stats(L, dt, off, V, T, &M, &Z)) return 1;
   for (int v = 0; v < V; ++v) {
     double s = elem(L, dt, off + (size_t)v) / T;
@@ -568,14 +619,31 @@ static int warped_row(const void* L, int dt, size_t off, int V, double T, int to
     if (elem(L, dt, off + (size_t)v) / T >= tk) Zk += out[v];
   double thr = tk;
   if (top_p < 1.0) {
-    double cum = 0.0, tp = tk;
+    const double target = top_p * Zk, band = near_p * Zk;
+    /* the near groups and the cut chosen by alt */
+    double cut = target, cum = 0.0;
+    int nn = 0;
+    for (int i = 0; i < V && tmp[i].s >= tk && cum < target + band;) {
+      int j = i;
+      double g = 0.0;
+      while (j < V && tmp[j].s == tmp[i].s) g += out[tmp[j++].v];
+      if (fabs(cum - target) < band) {
+        if (alt == 2 + nn) cut = cum;
+        ++nn;
+      }
+      cum += g;
+      i = j;
+    }
+    if (alt == 1) cut = target + band;
+    if (nnear) *nnear = nn;
+    double tp = tk;
+    cum = 0.0;
     int i = 0;
     while (i < V && tmp[i].s >= tk) {
       int j = i;
       double g = 0.0;
       while (j < V && tmp[j].s == tmp[i].s) g += out[tmp[j++].v];
-      if (near && fabs(cum - top_p * Zk) < NEAR_P * Zk) *near = 1;
-      if (!(cum < top_p * Zk)) break; /* this value and every smaller one are dropped */
+      if (!(cum < cut)) break; /* this value and every smaller one are dropped */
       tp = tmp[i].s;
       cum += g;
       i = j;
@@ -589,14 +657,24 @@ static int warped_row(const void* L, int dt, size_t off, int V, double T, int to
   return 0;
 }
 
+/* The rule itself (alt 0); *near is set when the row has a near group. */
+static int warped_row(const void* L, int dt, size_t off, int V, double T, int top_k, double top_p, double near_p,
+                      double* out, orc_sv* tmp, int* near) {
+  int nn = 0;
+  int r = warped_row_alt(L, dt, off, V, T, top_k, top_p, near_p, 0, out, tmp, &nn);
+  if (near && nn) *near = 1;
+  return r;
+}
+
 /* Chain verification with the warped p' and q' (see above); the same steps,
- * outputs and flags as orc_verify_chain (lse outputs omitted). Scratch: wp,
- * wq [V] doubles, tmp [V] entries. */
-void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
-                             const double* ur, double T, int top_k, double top_p, int B, int K, int V, int b0,
-                             int b1, int32_t* accept_len, int32_t* out_tok, double* px, double* qx, int32_t* status,
-                             int32_t* flags, double* margin, double* wp, double* wq, orc_sv* tmp) {
-  (void)B;
+ * outputs and flags as chain_rows (lse outputs omitted), with the flag
+ * windows win (uniforms) and near_p (top-p, relative to the kept mass).
+ * Scratch: wp, wq [V] doubles, tmp [V] entries. */
+static void warped_chain_rows(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                              const double* ur, double T, int top_k, double top_p, int K, int V, int b0, int b1,
+                              double win, double near_p, int32_t* accept_len, int32_t* out_tok, double* px,
+                              double* qx, int32_t* status, int32_t* flags, double* margin, double* wp, double* wq,
+                              orc_sv* tmp) {
   for (int b = b0; b < b1; ++b) {
     int st = 0, fl = 0, near = 0;
     double mg = INFINITY, M, Z;
@@ -619,8 +697,8 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
     }
     for (int k = 0; k < K; ++k) {
       int xk = x[(size_t)b * K + k];
-      warped_row(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, top_k, top_p, wp, tmp, &near);
-      warped_row(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, top_k, top_p, wq, tmp, &near);
+      warped_row(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, top_k, top_p, near_p, wp, tmp, &near);
+      warped_row(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, top_k, top_p, near_p, wq, tmp, &near);
       px[(size_t)b * K + k] = wp[xk];
       qx[(size_t)b * K + k] = wq[xk];
     }
@@ -632,7 +710,7 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
       double r = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
       double u = ua[(size_t)b * K + k];
       if (r < 1.0) mg = fmin(mg, fabs(u - r));
-      if (r < 1.0 && fabs(u - r) < NEAR) fl |= FL_ACCEPT;
+      if (r < 1.0 && fabs(u - r) < win) fl |= FL_ACCEPT;
       if (!(u < r)) {
         m = k;
         break;
@@ -641,9 +719,9 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
     accept_len[b] = m;
     for (int k = 0; k < m; ++k) out[k] = x[(size_t)b * K + k];
     /* residual max(0, p'_m - q'_m) at a rejection, p'_K for the bonus */
-    warped_row(Lp, dt, ((size_t)b * (K + 1) + m) * (size_t)V, V, T, top_k, top_p, wp, tmp, &near);
+    warped_row(Lp, dt, ((size_t)b * (K + 1) + m) * (size_t)V, V, T, top_k, top_p, near_p, wp, tmp, &near);
     int residual = m < K;
-    if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp, &near);
+    if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, near_p, wq, tmp, &near);
     double S = 0.0;
     for (int v = 0; v < V; ++v) S += residual ? fmax(0.0, wp[v] - wq[v]) : wp[v];
     if (residual && !(S > 0.0)) {
@@ -668,14 +746,240 @@ void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32
       fl |= FL_SAMPLE;
       mg = 0.0;
     } else {
-      double near = fmin(fabs(ur[b] - Cprev / S), fabs(ur[b] - C / S));
-      mg = fmin(mg, near);
-      if (near < NEAR) fl |= FL_SAMPLE;
+      double dist = fmin(fabs(ur[b] - Cprev / S), fabs(ur[b] - C / S));
+      mg = fmin(mg, dist);
+      if (dist < win) fl |= FL_SAMPLE;
     }
     out[m] = tok;
     flags[b] = fl | (near ? FL_WARP : 0);
     margin[b] = mg;
   }
+}
+
+/* Warped chain verification with the default windows (NEAR, NEAR_P). */
+void orc_verify_chain_warped(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                             const double* ur, double T, int top_k, double top_p, int B, int K, int V, int b0,
+                             int b1, int32_t* accept_len, int32_t* out_tok, double* px, double* qx, int32_t* status,
+                             int32_t* flags, double* margin, double* wp, double* wq, orc_sv* tmp) {
+  (void)B;
+  warped_chain_rows(Lp, Lq, dt, x, ua, ur, T, top_k, top_p, K, V, b0, b1, NEAR, NEAR_P, accept_len, out_tok, px, qx,
+                    status, flags, margin, wp, wq, tmp);
+}
+
+/* The same with the windows chosen by the caller. */
+void orc_verify_chain_warped_near(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                                  const double* ur, double T, int top_k, double top_p, int B, int K, int V, int b0,
+                                  int b1, double win, double near_p, int32_t* accept_len, int32_t* out_tok,
+                                  double* px, double* qx, int32_t* status, int32_t* flags, double* margin,
+                                  double* wp, double* wq, orc_sv* tmp) {
+  (void)B;
+  warped_chain_rows(Lp, Lq, dt, x, ua, ur, T, top_k, top_p, K, V, b0, b1, win, near_p, accept_len, out_tok, px, qx,
+                    status, flags, margin, wp, wq, tmp);
+}
+
+/* ---- validity of a given outcome under uniforms moved within a window ----
+ * An implementation that computes in lower precision than this oracle may
+ * decide differently when a uniform lies closer to a decision boundary than
+ * its error. These checks say whether a given outcome (the accepted length m
+ * and the emitted tokens) is exactly what this oracle emits when every
+ * uniform of the row is moved by at most `win` inside [0, 1). Each uniform
+ * decides one thing, so the outcome is reachable iff, separately: every
+ * position k < m can be accepted (some u' < r_k), position m, when m < K,
+ * can be rejected (some u' >= r_k), and the emitted token t carries weight
+ * and its interval [C_{t-1}, C_t) / S of the draw meets the moved resample
+ * uniform's range. */
+
+static const double kOneMinus = 1.0 - 1.0 / 9007199254740992.0; /* the largest double below 1 */
+
+static int decisions_reachable(const double* r, const double* u, int K, int m, double win) {
+  if (m < 0 || m > K) return 0;
+  for (int k = 0; k < m; ++k)
+    if (!(fmax(0.0, u[k] - win) < r[k])) return 0;
+  if (m < K && !(fmin(u[m] + win, kOneMinus) >= r[m])) return 0;
+  return 1;
+}
+
+/* Token t as the inverse-CDF draw from weights w[0..V) for some uniform
+ * within win of u: the smallest i with C_i > u' S, or (rounding left none)
+ * the last token with weight. */
+static int draw_reachable(const double* w, int V, double u, int t, double win) {
+  if (t < 0 || t >= V || !(w[t] > 0.0)) return 0;
+  double S = 0.0, Cprev = 0.0, C = 0.0;
+  int last_pos = -1;
+  for (int v = 0; v < V; ++v) {
+    S += w[v];
+    if (w[v] > 0.0) last_pos = v;
+  }
+  if (!(S > 0.0)) return 0;
+  for (int v = 0; v <= t; ++v) {
+    Cprev = C;
+    C += w[v];
+  }
+  const double lo = fmax(0.0, u - win), hi = fmin(u + win, kOneMinus);
+  if (Cprev <= hi * S && C > lo * S) return 1;
+  return t == last_pos && hi * S >= C; /* no crossing: the last token with weight */
+}
+
+/* The prefix and padding of an outcome: out[k] = x_k for k < m, the drawn
+ * token at m, -1 after it. */
+static int prefix_ok(const int32_t* out, const int32_t* x, int K, int m) {
+  for (int k = 0; k < m; ++k)
+    if (out[k] != x[k]) return 0;
+  for (int k = m + 1; k <= K; ++k)
+    if (out[k] != -1) return 0;
+  return 1;
+}
+
+/* Validity of outcomes (acc [B], tok [B][K+1]) of plain chain verification
+ * for rows b in [b0, b1): valid[b] = 1 when reachable as stated above. A row
+ * whose inputs are flagged (status bits) is valid iff its outcome is all -1. */
+void orc_chain_valid(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua, const double* ur,
+                     double T, int B, int K, int V, int b0, int b1, double win, const int32_t* acc,
+                     const int32_t* tok, int32_t* valid) {
+  (void)B;
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  double* Mp = (double*)malloc(sizeof(double) * (size_t)(2 * K + 2));
+  double* Zp = Mp + K + 1;
+  double* Mq = (double*)malloc(sizeof(double) * (size_t)(3 * K + 3));
+  double* Zq = Mq + K + 1;
+  double* r = Zq + K + 1;
+  for (int b = b0; b < b1; ++b) {
+    int st = 0;
+    for (int k = 0; k <= K; ++k)
+      if (softmax_stats(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, &Mp[k], &Zp[k])) st |= ST_TARGET;
+    for (int k = 0; k < K; ++k) {
+      if (softmax_stats(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, &Mq[k], &Zq[k])) st |= ST_DRAFT;
+      int xk = x[(size_t)b * K + k];
+      if (xk < 0 || xk >= V) st |= ST_TOKEN;
+    }
+    const int32_t* out = tok + (size_t)b * (K + 1);
+    const int m = acc[b];
+    if (st) {
+      int all = m == -1;
+      for (int j = 0; j <= K; ++j) all &= out[j] == -1;
+      valid[b] = all;
+      continue;
+    }
+    const int32_t* xb = x + (size_t)b * K;
+    if (m < 0 || m > K || !prefix_ok(out, xb, K, m)) {
+      valid[b] = 0;
+      continue;
+    }
+    for (int k = 0; k < K; ++k) {
+      double p = prob(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, xb[k], T, Mp[k], Zp[k]);
+      double q = prob(Lq, dt, ((size_t)b * K + k) * (size_t)V, xb[k], T, Mq[k], Zq[k]);
+      r[k] = q > 0.0 ? p / q : INFINITY;
+    }
+    int ok = decisions_reachable(r, ua + (size_t)b * K, K, m, win);
+    if (ok) {
+      size_t offp = ((size_t)b * (K + 1) + m) * (size_t)V, offq = ((size_t)b * K + m) * (size_t)V;
+      double S = 0.0;
+      for (int v = 0; v < V; ++v) {
+        w[v] = prob(Lp, dt, offp, v, T, Mp[m], Zp[m]);
+        if (m < K) w[v] = fmax(0.0, w[v] - prob(Lq, dt, offq, v, T, Mq[m], Zq[m]));
+        S += w[v];
+      }
+      if (m < K && !(S > 0.0))
+        for (int v = 0; v < V; ++v) w[v] = prob(Lp, dt, offp, v, T, Mp[m], Zp[m]);
+      ok = draw_reachable(w, V, ur[b], out[m], win);
+    }
+    valid[b] = ok;
+  }
+  free(w);
+  free(Mp);
+  free(Mq);
+}
+
+/* The same for warped chain verification. Besides the uniforms, the top-p
+ * cut of every row the outcome depends on (target rows 0..m, draft rows
+ * 0..min(m, K-1)) may fall at any of its near groups (window near_p, see
+ * warped_row_alt); every combination of cuts is tried, at most 4096 of
+ * them (a row needing more is reported invalid, valid = 0). Scratch: wp, wq
+ * [V] doubles, tmp [V] entries; ridx, nalt [2K+1] ints. */
+void orc_chain_warped_valid(const void* Lp, const void* Lq, int dt, const int32_t* x, const double* ua,
+                            const double* ur, double T, int top_k, double top_p, int B, int K, int V, int b0,
+                            int b1, double win, double near_p, const int32_t* acc, const int32_t* tok,
+                            int32_t* valid, double* wp, double* wq, orc_sv* tmp, int32_t* nalt, int32_t* alt) {
+  (void)B;
+  double* r = (double*)malloc(sizeof(double) * (size_t)(K + 1));
+  for (int b = b0; b < b1; ++b) {
+    int st = 0;
+    double M, Z;
+    for (int k = 0; k <= K; ++k)
+      if (softmax_stats(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, &M, &Z)) st |= ST_TARGET;
+    for (int k = 0; k < K; ++k) {
+      if (softmax_stats(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, &M, &Z)) st |= ST_DRAFT;
+      int xk = x[(size_t)b * K + k];
+      if (xk < 0 || xk >= V) st |= ST_TOKEN;
+    }
+    const int32_t* out = tok + (size_t)b * (K + 1);
+    const int m = acc[b];
+    if (st) {
+      int all = m == -1;
+      for (int j = 0; j <= K; ++j) all &= out[j] == -1;
+      valid[b] = all;
+      continue;
+    }
+    const int32_t* xb = x + (size_t)b * K;
+    if (m < 0 || m > K || !prefix_ok(out, xb, K, m)) {
+      valid[b] = 0;
+      continue;
+    }
+    /* rows the outcome depends on: slot 2k target row k, slot 2k+1 draft row k */
+    const int nslot = 2 * m + (m < K ? 2 : 1);
+    long long combos = 1;
+    for (int sl = 0; sl < nslot; ++sl) {
+      const int k = sl >> 1;
+      const size_t off = (sl & 1) ? ((size_t)b * K + k) * (size_t)V : ((size_t)b * (K + 1) + k) * (size_t)V;
+      int nn = 0;
+      warped_row_alt((sl & 1) ? Lq : Lp, dt, off, V, T, top_k, top_p, near_p, 0, wp, tmp, &nn);
+      nalt[sl] = nn ? 2 + nn : 1;
+      combos *= nalt[sl];
+      if (combos > 4096) break;
+    }
+    if (combos > 4096) {
+      valid[b] = 0;
+      continue;
+    }
+    int ok = 0;
+    for (int sl = 0; sl < nslot; ++sl) alt[sl] = 0;
+    for (long long c = 0; c < combos && !ok; ++c) {
+      /* decisions at k < m (accept) and m (reject, when m < K) */
+      for (int k = 0; k <= m && k < K; ++k) {
+        warped_row_alt(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, top_k, top_p, near_p, alt[2 * k], wp,
+                       tmp, NULL);
+        warped_row_alt(Lq, dt, ((size_t)b * K + k) * (size_t)V, V, T, top_k, top_p, near_p, alt[2 * k + 1], wq, tmp,
+                       NULL);
+        double p = wp[xb[k]], q = wq[xb[k]];
+        r[k] = q > 0.0 ? p / q : (p > 0.0 ? INFINITY : 0.0);
+      }
+      int dok = decisions_reachable(r, ua + (size_t)b * K, K, m, win);
+      if (dok) {
+        warped_row_alt(Lp, dt, ((size_t)b * (K + 1) + m) * (size_t)V, V, T, top_k, top_p, near_p, alt[2 * m], wp, tmp,
+                       NULL);
+        double S = 0.0;
+        if (m < K) {
+          warped_row_alt(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, near_p, alt[2 * m + 1], wq,
+                         tmp, NULL);
+          for (int v = 0; v < V; ++v) S += fmax(0.0, wp[v] - wq[v]);
+          if (S > 0.0)
+            for (int v = 0; v < V; ++v) wq[v] = fmax(0.0, wp[v] - wq[v]);
+          else
+            for (int v = 0; v < V; ++v) wq[v] = wp[v];
+        } else {
+          for (int v = 0; v < V; ++v) wq[v] = wp[v];
+        }
+        ok = draw_reachable(wq, V, ur[b], out[m], win);
+      }
+      /* next combination (mixed radix over the slots) */
+      for (int sl = 0; sl < nslot; ++sl) {
+        if (++alt[sl] < nalt[sl]) break;
+        alt[sl] = 0;
+      }
+    }
+    valid[b] = ok;
+  }
+  free(r);
 }
 
 /* One expansion step of a drafter token tree by cumulative probability

@@ -752,6 +752,180 @@ def pin_tree_expand(lib, seed=11):
     assert np.isneginf(r["score"][3][5:]).all()
 
 
+def _valid_one(lib, Lp, Lq, x, ua, ur, T, m, toks, win, warped=None):
+    """orc_chain_valid (or, with warped = (top_k, top_p, near_p), its warped
+    form) on one row and one outcome."""
+    Lp = np.ascontiguousarray(Lp, np.float64)[None]
+    K, V = Lp.shape[1] - 1, Lp.shape[2]
+    Lq = np.ascontiguousarray(Lq, np.float64).reshape(1, K, V)
+    xs = np.ascontiguousarray(x, np.int32).reshape(1, K)
+    uas = np.ascontiguousarray(ua, np.float64).reshape(1, K)
+    urs = np.array([ur], np.float64)
+    acc = np.array([m], np.int32)
+    tok = np.ascontiguousarray(toks, np.int32).reshape(1, K + 1)
+    valid = np.zeros(1, np.int32)
+    if warped is None:
+        lib.orc_chain_valid(_p(Lp), _p(Lq), oracle.F64, _p(xs), _p(uas), _p(urs), float(T), 1, K, V, 0, 1,
+                            float(win), _p(acc), _p(tok), _p(valid))
+    else:
+        top_k, top_p, near_p = warped
+        wp, wq, tmp = np.zeros(V), np.zeros(V), np.zeros(V * 16, np.uint8)
+        nalt, alt = np.zeros(2 * K + 2, np.int32), np.zeros(2 * K + 2, np.int32)
+        lib.orc_chain_warped_valid(_p(Lp), _p(Lq), oracle.F64, _p(xs), _p(uas), _p(urs), float(T), int(top_k),
+                                   float(top_p), 1, K, V, 0, 1, float(win), float(near_p), _p(acc), _p(tok),
+                                   _p(valid), _p(wp), _p(wq), _p(tmp), _p(nalt), _p(alt))
+    return bool(valid[0])
+
+
+def _moved(u, win, marks):
+    """Points of [u - win, u + win] inside [0, 1) that reach every side of
+    every mark: the two ends and each mark +- 1e-10 that lies inside."""
+    lo, hi = max(0.0, u - win), min(u + win, ONE_MINUS)
+    pts = {lo, hi}
+    for c in marks:
+        for d in (-1e-10, 1e-10):
+            if lo <= c + d <= hi:
+                pts.add(c + d)
+    return sorted(pts)
+
+
+def _draw_np(w, u):
+    """Inverse-CDF draw with a strict '>' (smallest i with C_i > u S)."""
+    C = np.cumsum(w)
+    hit = np.nonzero(C > u * C[-1])[0]
+    return int(hit[0]) if hit.size else int(np.nonzero(w > 0)[0][-1])
+
+
+def pin_chain_valid(lib, V=4, K=2, T=0.9, win=0.07, seed=13, trials=10):
+    """The validity check is the reachable set: an outcome is valid iff some
+    choice of the row's uniforms, each moved by at most win inside [0, 1),
+    makes the oracle emit it. Here the reachable set is found by brute force
+    (the oracle at every combination of points on each side of every
+    threshold and CDF boundary inside the moved ranges) and compared with the
+    check for every outcome (m, token) of tiny worlds."""
+    lp, lq = random_world(V, K, seed)
+    rng = np.random.default_rng(seed)
+    several = 0  # trials where the moved uniforms reach more than one outcome
+    for _ in range(trials):
+        x = tuple(int(v) for v in rng.integers(0, V, K))
+        Lp = np.stack([lp[x[:k]] for k in range(K + 1)])
+        Lq = np.stack([lq[x[:k]] for k in range(K)]) if K else np.zeros((0, V))
+        p = [softmax(Lp[k], T) for k in range(K + 1)]
+        q = [softmax(Lq[k], T) for k in range(K)]
+        r = [p[k][x[k]] / q[k][x[k]] for k in range(K)]
+        ws = [np.maximum(p[m] - q[m], 0.0) if m < K else p[K] for m in range(K + 1)]
+        bounds = [c for w in ws for c in np.cumsum(w) / w.sum()]
+        # uniforms placed near a threshold or boundary half of the time
+        ua = [float(np.clip(r[k] + rng.uniform(-win, win), 0, ONE_MINUS)) if rng.random() < 0.5 else rng.random()
+              for k in range(K)]
+        ur = float(np.clip(rng.choice(bounds) + rng.uniform(-win, win), 0, ONE_MINUS)) if rng.random() < 0.5 \
+            else rng.random()
+        call = ChainCall(lib, Lp, Lq, x, T)
+        reach = set()
+        for ua2 in itertools.product(*[_moved(ua[k], win, [r[k]]) for k in range(K)]):
+            for ur2 in _moved(ur, win, bounds):
+                reach.add(call(list(ua2), ur2))
+        several += len(reach) > 1
+        for m in range(K + 1):
+            for t in range(V):
+                toks = list(x[:m]) + [t] + [-1] * (K - m)
+                want = (m, tuple(x[:m]) + (t,)) in reach
+                assert _valid_one(lib, Lp, Lq, x, ua, ur, T, m, toks, win) == want, (x, m, t, want)
+        # a wrong accepted prefix is never valid
+        if K > 0:
+            m, toks = next(iter(reach))
+            bad = list(toks) + [-1] * (K - m)
+            if m > 0:
+                bad[0] = (bad[0] + 1) % V
+                assert not _valid_one(lib, Lp, Lq, x, ua, ur, T, m, bad, win)
+    assert several >= trials // 3, several
+
+
+def _cut_sets(s, e, top_k, top_p, near_p):
+    """Kept sets of one row for every top-p cut in (target - band, target +
+    band] (band = near_p times the top-k mass), on a dense grid of cuts plus
+    each group's own mass boundary: numpy, written for the test."""
+    keep_k = np.ones(len(s), bool)
+    if 0 < top_k < len(s):
+        keep_k = s >= np.sort(s)[::-1][top_k - 1]
+    if top_p >= 1.0:
+        return [keep_k]
+    Zk = e[keep_k].sum()
+    target, band = top_p * Zk, near_p * Zk
+    above = np.array([e[(s > s[v]) & keep_k].sum() for v in range(len(s))])
+    cuts = list(target - band + (np.arange(400) + 0.5) / 400 * 2 * band) + [target + band]
+    cuts += [a + d for a in above for d in (-1e-12, 1e-12) if target - band < a + d <= target + band]
+    sets = {tuple(keep_k & (above < c)) for c in cuts}
+    return [np.array(k) for k in sorted(sets)]
+
+
+def pin_chain_warped_valid(lib, V=5, K=1, T=1.0, top_k=4, top_p=0.6, near_p=0.25, win=0.05, seed=17, trials=12):
+    """The warped validity check against brute force: every kept set a top-p
+    cut within near_p of its target gives (a dense grid of cuts), combined
+    with uniforms moved by at most win, by numpy; compared with the check
+    for every outcome of tiny worlds."""
+    lp, lq = random_world(V, K, seed, scale=1.0)
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        x = tuple(int(v) for v in rng.integers(0, V, K))
+        Lp = np.stack([lp[x[:k]] for k in range(K + 1)])
+        Lq = np.stack([lq[x[:k]] for k in range(K)])
+        rows = [Lp[k] for k in range(K + 1)] + [Lq[k] for k in range(K)]
+        opts = []
+        for l in rows:
+            s = np.asarray(l, np.float64) / T
+            e = np.exp(s - s.max())
+            opts.append([np.where(kp, e, 0.0) / np.where(kp, e, 0.0).sum()
+                         for kp in _cut_sets(s, e, top_k, top_p, near_p)])
+        ua = list(rng.random(K))
+        ur = float(rng.random())
+        reach = set()
+        for combo in itertools.product(*opts):
+            P_, Q_ = combo[:K + 1], combo[K + 1:]
+            r = [P_[k][x[k]] / Q_[k][x[k]] if Q_[k][x[k]] > 0 else (np.inf if P_[k][x[k]] > 0 else 0.0)
+                 for k in range(K)]
+            ws = [np.maximum(P_[m] - Q_[m], 0.0) if m < K else P_[K] for m in range(K + 1)]
+            ws = [w if w.sum() > 0 else P_[m] for m, w in enumerate(ws)]
+            bounds = [c for w in ws for c in np.cumsum(w) / w.sum()]
+            for ua2 in itertools.product(*[_moved(ua[k], win, [r[k]]) for k in range(K)]):
+                m = next((k for k in range(K) if not ua2[k] < r[k]), K)
+                for ur2 in _moved(ur, win, bounds):
+                    reach.add((m, tuple(x[:m]) + (_draw_np(ws[m], ur2),)))
+        for m in range(K + 1):
+            for t in range(V):
+                toks = list(x[:m]) + [t] + [-1] * (K - m)
+                want = (m, tuple(x[:m]) + (t,)) in reach
+                got = _valid_one(lib, Lp, Lq, x, ua, ur, T, m, toks, win, warped=(top_k, top_p, near_p))
+                assert got == want, (x, m, t, want)
+
+
+def pin_flag_probability(lib, V=6, T=1.0, win=0.02, seed=19, n=20000):
+    """pflag, the oracle's probability of a flag over the row's uniforms,
+    against counting: with the accept uniform fixed (so the first rejection
+    is fixed) and the resample uniform swept over a fine grid, the share of
+    flagged draws equals the draw part of pflag, sum_t min(w_t / S, 2 win)."""
+    rng = np.random.default_rng(seed)
+    Lp, Lq = rng.normal(0, 1.5, (1, 2, V)), rng.normal(0, 1.5, (1, 1, V))
+    x = np.array([[int(np.argmax(Lq[0, 0]))]], np.int32)
+    p0, q0 = softmax(Lp[0, 0], T), softmax(Lq[0, 0], T)
+    r0 = p0[x[0, 0]] / q0[x[0, 0]]
+    for ua in (0.999, 0.0):  # rejected when r0 < 0.999, accepted (r0 > 0)
+        uas = np.full((n, 1), ua)
+        urs = (np.arange(n) + 0.5) / n
+        o = oracle.verify_chain(np.repeat(Lp, n, 0), np.repeat(Lq, n, 0), np.repeat(x, n, 0), uas, urs, T, lib=lib,
+                                near=win)
+        m = int(o["accept_len"][0])
+        share = float(np.mean((o["flags"] & oracle.FL_SAMPLE) != 0))
+        accept_part = window_part = 0.0
+        if r0 < 1.0:
+            accept_part = min(1.0, r0 + win) - max(0.0, r0 - win)
+        w = np.maximum(p0 - q0, 0.0) if m == 0 else softmax(Lp[0, 1], T)
+        window_part = float(np.minimum(w / w.sum(), 2 * win).sum())
+        assert abs(share - window_part) < 3.0 / n * V + 1e-3, (share, window_part)
+        assert abs(o["pflag"][0] - min(1.0, accept_part + window_part)) < 1e-9, (o["pflag"][0], accept_part,
+                                                                                   window_part)
+
+
 ALL_PINS = [
     ("ab_example", pin_ab_example),
     ("lossless_V3K2", lambda lib: pin_lossless(lib, 3, 2, 1.0, 1)),
@@ -777,4 +951,7 @@ ALL_PINS = [
     ("lossless_warped_topk", lambda lib: pin_lossless_warped(lib, 4, 2, 1.0, 2, 1.0, 7)),
     ("lossless_warped_topp", lambda lib: pin_lossless_warped(lib, 4, 2, 0.8, 0, 0.7, 8)),
     ("lossless_warped_both", lambda lib: pin_lossless_warped(lib, 4, 2, 1.2, 3, 0.8, 9)),
+    ("chain_valid", pin_chain_valid),
+    ("chain_warped_valid", pin_chain_warped_valid),
+    ("flag_probability", pin_flag_probability),
 ]

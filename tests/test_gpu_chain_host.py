@@ -40,7 +40,7 @@ def same_ints(h, g):
 def test_host_chain_matches_oracle_and_device_call(V, dtype):
     c = gen.chain_zipf(6, 4, V, dtype, 0.8, 0.7, seed=V % 13)
     h = host_chain(c)
-    compare_chain(h, oracle_chain(c))
+    compare_chain(h, oracle_chain(c), c)
     same_ints(h, gpu_chain(c, stats=False))
 
 
@@ -59,7 +59,7 @@ def test_host_chain_pageable_inputs_and_caller_stream():
     sv.spec_verify_chain_host(c.Lp, c.Lq, c.x, c.ua, c.ur, c.T, out=out, workspace=ws, stream=s, synchronize=False)
     s.synchronize()
     h = {k: v.numpy().copy() for k, v in out.items()}
-    compare_chain(h, oracle_chain(c))
+    compare_chain(h, oracle_chain(c), c)
 
 
 def test_host_chain_greedy_and_flagged_rows():

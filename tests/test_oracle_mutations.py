@@ -62,12 +62,21 @@ MUTATIONS = {
     "entropy_empty_tree_zero": ("s2 = n2 > 0 ? s2 / n2 : INFINITY;", "s2 = n2 > 0 ? s2 / n2 : 0.0;"),
     "warped_topk_off_by_one": ("if (top_k > 0 && top_k < V) tk = tmp[top_k - 1].s;",
                                "if (top_k > 0 && top_k < V) tk = tmp[top_k].s;"),
-    "warped_topp_drops_crossing_token": ("if (!(cum < top_p * Zk)) break;", "if (!(cum + g < top_p * Zk)) break;"),
-    "warped_topp_on_full_mass": ("if (!(cum < top_p * Zk)) break;", "if (!(cum < top_p * Z)) break;"),
+    "warped_topp_drops_crossing_token": ("if (!(cum < cut)) break;", "if (!(cum + g < cut)) break;"),
+    "warped_topp_on_full_mass": ("const double target = top_p * Zk,", "const double target = top_p * Z,"),
     "warped_not_renormalised": ("? out[v] / Zw : 0.0;", "? out[v] / Z : 0.0;"),
     "warped_residual_unwarped_draft": (
-        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, wq, tmp, &near);",
-        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, 0, 1.0, wq, tmp, &near);"),
+        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, top_k, top_p, near_p, wq, tmp, &near);",
+        "if (residual) warped_row(Lq, dt, ((size_t)b * K + m) * (size_t)V, V, T, 0, 1.0, near_p, wq, tmp, &near);"),
+    "valid_accept_window_ignored": ("if (!(fmax(0.0, u[k] - win) < r[k])) return 0;", "if (!(u[k] < r[k])) return 0;"),
+    "valid_reject_window_ignored": ("if (m < K && !(fmin(u[m] + win, kOneMinus) >= r[m])) return 0;",
+                                    "if (m < K && !(u[m] >= r[m])) return 0;"),
+    "valid_draw_interval_shifted": ("if (Cprev <= hi * S && C > lo * S) return 1;",
+                                    "if (C <= hi * S && C > lo * S) return 1;"),
+    "valid_prefix_unchecked": ("    if (out[k] != x[k]) return 0;", "    if (0) return 0;"),
+    "valid_warped_no_alternative_cuts": ("nalt[sl] = nn ? 2 + nn : 1;", "nalt[sl] = 1;"),
+    "valid_warped_keep_all_cut_missing": ("if (alt == 1) cut = target + band;", "if (alt == 1) cut = target;"),
+    "pflag_window_halved": ("pf += fmin(w / S, 2.0 * near);", "pf += fmin(w / S, near);"),
     "expand_ties_to_higher_node": ("if (x->f != y->f) return x->f < y->f ? -1 : 1;",
                                    "if (x->f != y->f) return x->f > y->f ? -1 : 1;"),
     "expand_cumulative_dropped": ("cand[n].s = logc[(size_t)b * F + f] + (", "cand[n].s = 0.0 + ("),

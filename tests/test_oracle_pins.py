@@ -51,3 +51,21 @@ def test_every_pin_holds_on_the_oracle(orc, name):
     """Each pin the planted-mistake tests rely on passes on the real oracle
     (so a pin that trips on a mutant is tripping on the mistake)."""
     dict(P.ALL_PINS)[name](orc.load())
+
+
+@pytest.mark.parametrize("V,K,T,win,seed", [(4, 2, 0.9, 0.07, 13), (3, 3, 1.2, 0.1, 14), (5, 1, 0.6, 0.02, 15),
+                                            (4, 0, 1.0, 0.05, 16)])
+def test_validity_is_the_reachable_set(orc, V, K, T, win, seed):
+    """An outcome passes the validity check iff moving the row's uniforms by
+    at most the window makes the oracle emit it (brute force)."""
+    P.pin_chain_valid(orc.load(), V=V, K=K, T=T, win=win, seed=seed)
+
+
+@pytest.mark.parametrize("V,K,T,top_k,top_p,near_p,seed", [(5, 1, 1.0, 4, 0.6, 0.12, 17),
+                                                           (6, 2, 0.8, 0, 0.7, 0.08, 18),
+                                                           (4, 1, 1.3, 3, 0.9, 0.2, 20)])
+def test_warped_validity_is_the_reachable_set(orc, V, K, T, top_k, top_p, near_p, seed):
+    """The same for warped verification, where top-p cuts within near_p of
+    their target may also fall either way."""
+    P.pin_chain_warped_valid(orc.load(), V=V, K=K, T=T, top_k=top_k, top_p=top_p, near_p=near_p, seed=seed,
+                             trials=5)
