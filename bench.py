@@ -465,17 +465,31 @@ def run_ours(args):
 KV_PLANES, KV_S, KV_W, KV_SETS = 64, 2048, 1024, 16  # Llama-3-8B: 32 layers x K/V, 8 KV heads x 128
 
 
-def kv_setup(seed: int):
-    """Merged-tree workload (config of the tree bench) and its accepted paths
-    from the oracle's tree verification: the compaction that follows it."""
+def kv_setup(seed: int, dev=None):
+    """Merged-tree workload (config of the tree bench) and its accepted paths:
+    the compaction that follows tree verification. On a device the paths come
+    from the library's own tree verification, as a caller would chain the two
+    calls; the reference arm (dev None) takes them from the oracle's."""
     import numpy as np
 
     import gen
-    import oracle
 
     tb = gen.config_tree(seed)
-    o = oracle.verify_tree_greedy(tb.Lt, tb.tok, tb.R, tb.n1, mask=tb.mask, threads=os.cpu_count() or 1)
-    acc, path = o["accept_len"].astype(np.int32), o["path"].astype(np.int32)
+    if dev is None:
+        import oracle
+
+        o = oracle.verify_tree_greedy(tb.Lt, tb.tok, tb.R, tb.n1, mask=tb.mask, threads=os.cpu_count() or 1)
+        acc, path = o["accept_len"].astype(np.int32), o["path"].astype(np.int32)
+    else:
+        import torch
+
+        import speculative_decoding_verification_29_gb300 as sv
+
+        v = sv.spec_verify_tree_greedy(tb.Lt.to(dev), tb.tok.to(dev), tb.R.to(dev), tb.n1,
+                                       tree_mask=tb.mask.to(dev))
+        torch.cuda.synchronize()
+        acc = v["accept_len"].cpu().numpy().astype(np.int32)
+        path = v["path_nodes"].cpu().numpy().astype(np.int32)
     moved_rows = sum(int(np.sum(path[b, 1:acc[b] + 1] != np.arange(1, acc[b] + 1))) for b in range(tb.B) if acc[b] > 0)
     bases = [np.full(tb.B, 64 + 112 * j, np.int32) for j in range(KV_SETS)]
     cfg = dict(workload=f"KV-cache compaction after merged-tree verify: B={tb.B} N={tb.N}, cache {KV_PLANES} planes "
@@ -499,7 +513,7 @@ def run_kv(args):
         import torch.distributed as dist
 
         dist.init_process_group("nccl", device_id=dev)
-    tb, acc, path, bases, bpstep, cfg = kv_setup(rank_seed(args.seed, rank))
+    tb, acc, path, bases, bpstep, cfg = kv_setup(rank_seed(args.seed, rank), dev)
     B = tb.B
     kv = torch.empty(KV_PLANES, B, KV_S, KV_W, dtype=torch.int16, device=dev)
     for p in range(KV_PLANES):  # random bits, one plane at a time

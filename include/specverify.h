@@ -95,8 +95,8 @@ enum {
 #define SPEC_ROW_DRAFT 4  /* the same for a draft row */
 #define SPEC_ROW_TREE 8   /* a malformed retrieve row */
 #define SPEC_ROW_MASK 16  /* a retrieve row that contradicts tree_mask */
-#define SPEC_ROW_WARP 32  /* top-p: the nucleus reaches past the row's 4096 largest tokens (whole groups of
-                             equal logits; spec_verify_chain_warped) */
+#define SPEC_ROW_WARP 32  /* spec_tree_expand: more than 4096 tokens of one frontier node tie at its M-th
+                             largest logit (never set by the chain calls) */
 
 /* Limits: 1 <= B <= 65535; 0 <= K <= 255; 2 <= V <= 2^24; for trees
  * 1 <= N <= 1024, 1 <= D <= 64, 1 <= R <= 4096. */
@@ -222,11 +222,12 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logit
  * 256 candidates fall back as below). Otherwise the extra passes are: for
  * top_k <= 256, one filtering the row
  * (ties overflowing its buffers: as for larger top_k); for larger top_k,
- * 2 (bf16) or 4 (fp32) radix passes; for top-p alone (or top-k sets of
- * more than 4096 tokens), 2 / 4 more to find the row's largest tokens (at
- * most 4096, whole groups of equal logits) and one collecting them; one
- * summing the kept mass when the top-k set does not fit. A row whose
- * nucleus reaches past those tokens gets SPEC_ROW_WARP. */
+ * 2 (bf16) or 4 (fp32) radix passes; then, when the tokens top-k keeps
+ * (all V for top-p alone) number at most 4096, one collecting them; when
+ * they number more, for top-p 1 + 2 (bf16) or 1 + 4 (fp32) passes of a
+ * mass-weighted radix select (weights summed in 64-bit fixed point, so the
+ * cut does not depend on summation order), or for top-k alone one summing
+ * the kept mass. Every nucleus size is resolved. */
 size_t spec_warped_workspace_bytes(int B, int K, int V, int dtype);
 int spec_verify_chain_warped(const void* target_logits, const void* draft_logits, int dtype,
                              const int32_t* draft_tokens, const float* u_accept, const float* u_resample,

@@ -40,6 +40,17 @@ namespace {
 
 using namespace sel;
 
+// Weight 2^((l - M) log2(e) / T) of d = l - M <= 0 with the exponent carried
+// as a float pair: relative error that of the hardware 2^x (about 2^-22)
+// instead of the exponent's rounding (|exponent| x 2^-24).
+__device__ __forceinline__ float weight_pair_exp(float d, float c_hi, float c_lo) {
+  if (!(d > -INFINITY)) return 0.f;
+  const float p = d * c_hi;
+  const float lo = fmaf(d, c_lo, fmaf(d, c_hi, -p));  // d c_lo + the rounding error of d c_hi
+  return ex2_fast(p) * fmaf(lo, 0.693147180559945309f, 1.f);
+}
+
+
 // Sum of the weights of the keys >= tau over the row, as a float pair
 // (every thread gets it): fp32 runs of 64 terms folded into a float pair.
 template <typename Raw, bool VEC, typename W>
@@ -77,10 +88,7 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
     const uint32_t key = comp_key(r[i]);
     ink[i] = 32 * i + lane < n && key >= K;
     float ww = 0.f;
-    if (ink[i]) {
-      const float d = key_value<Raw>(key) - M;
-      ww = ex2_fast(fmaf(d, a.c_hi, d * a.c_lo));
-    }
+    if (ink[i]) ww = weight_pair_exp(key_value<Raw>(key) - M, a.c_hi, a.c_lo);
     w[i] = ww;
     zk = ds_add(zk, make_float2(ww, 0.f));
   }
@@ -183,6 +191,149 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
   return true;
 }
 
+// ---- top-p over any number of tokens: a mass-weighted radix select ----
+//
+// The tokens top-p keeps are a prefix of the value groups in descending
+// order: group g is kept iff the mass of the tokens top-k keeps with a
+// strictly larger logit is below top_p Z_k. Its last group is found without
+// sorting. The weights are summed exactly in 64-bit fixed point (w 2^s, s
+// chosen so that V terms cannot overflow; the sums are deterministic and do
+// not depend on the order of the atomics) into histograms: first over 256
+// bins of the log-weight, 1/8 of a binary order of magnitude each (the bin
+// is a monotone function of the key, so a bin is a contiguous key range and
+// a group never straddles two bins), then over the 8-bit digits of the keys
+// inside the bin the cut falls in (2 passes for bf16 keys, 4 for fp32). Each
+// level keeps the last entry, in descending value order, that has mass and
+// whose preceding mass is below the target.
+
+// Log-weight bin of d = l - M: floor(-8 a) for a = d log2(e) / T in (-32, 0],
+// 255 below (and for -inf); monotone in l.
+__device__ __forceinline__ int mass_bin(float d, float c_hi, float c_lo) {
+  const float a = fmaf(d, c_hi, d * c_lo);
+  return a > -32.f ? static_cast<int>(-8.f * a) : 255;
+}
+
+struct MassSmem {
+  unsigned long long* wh;   // kSelWarps x 256 per-warp histograms
+  unsigned long long* tot;  // 256 totals, in descending value order
+  unsigned long long* sel;  // [0] the chosen entry, [1] the mass before it, [2] its mass
+};
+
+// One full warp: over tot[0..255] (descending value order), the last entry
+// with mass whose preceding mass A + sum_{e' < e} tot[e'] is below target.
+// Lane l holds entries 8 l .. 8 l + 7.
+__device__ __forceinline__ void last_below(const unsigned long long* tot, unsigned long long A, double target,
+                                           unsigned long long* sel, int lane) {
+  unsigned long long m[8], sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    m[i] = tot[8 * lane + i];
+    sum += m[i];
+  }
+  unsigned long long incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  unsigned long long run = A + (incl - sum), bb = 0, bm = 0;
+  int best = -1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (m[i] > 0ull && __ull2double_rn(run) < target) {
+      best = 8 * lane + i;
+      bb = run;
+      bm = m[i];
+    }
+    run += m[i];
+  }
+  const int e = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(best + 1)) - 1;
+  const int src = e < 0 ? 0 : e >> 3;
+  bb = __shfl_sync(0xffffffffu, bb, src);
+  bm = __shfl_sync(0xffffffffu, bm, src);
+  if (lane == 0) {
+    sel[0] = static_cast<unsigned long long>(static_cast<long long>(e));
+    sel[1] = bb;
+    sel[2] = bm;
+  }
+}
+
+// The top-p cut of one row over the tokens with key >= tau_k (0: all): the
+// key of the last kept group, and (*kept) the kept mass relative to the row
+// maximum as a float pair. Called by every thread of the CTA.
+template <typename Raw, bool VEC>
+__device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c_lo, uint32_t tau_k, float top_p,
+                             const MassSmem& sm, float2* kept) {
+  using KY = Key<Raw>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int s = 62 - (32 - __clz(V));                // V terms of at most 2^s stay below 2^62
+  const float fs = __int_as_float((127 + s) << 23);  // 2^s
+  unsigned long long* wh = sm.wh + warp * 256;
+  auto clear = [&]() {
+    for (int i = tid; i < kSelWarps * 256; i += kSelThreads) sm.wh[i] = 0ull;
+    __syncthreads();
+  };
+  auto reduce = [&](bool reverse) {  // per-warp histograms into tot (reverse: digit d at 255 - d)
+    __syncthreads();
+    for (int b = tid; b < 256; b += kSelThreads) {
+      unsigned long long t = 0;
+      for (int w = 0; w < kSelWarps; ++w) t += sm.wh[w * 256 + b];
+      sm.tot[reverse ? 255 - b : b] = t;
+    }
+    __syncthreads();
+  };
+  // level 1: the log-weight bins
+  clear();
+  for_row<Raw, VEC>(row, V, [&](uint32_t bits) {
+    if (KY::of(bits) < tau_k) return;
+    const float d = KY::val(bits) - M;
+    const unsigned long long fx = __float2ull_rn(weight_pair_exp(d, c_hi, c_lo) * fs);
+    if (fx) atomicAdd(wh + mass_bin(d, c_hi, c_lo), fx);
+  });
+  reduce(false);
+  __shared__ double s_target;
+  if (warp == 0) {
+    unsigned long long t = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += sm.tot[8 * lane + i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const double target = static_cast<double>(top_p) * __ull2double_rn(t);
+    if (lane == 0) s_target = target;
+    last_below(sm.tot, 0ull, target, sm.sel, lane);
+  }
+  __syncthreads();
+  const double target = s_target;
+  const int bin = static_cast<int>(static_cast<long long>(sm.sel[0]));
+  unsigned long long A = sm.sel[1], mg = sm.sel[2];
+  // level 2: the digits of the keys inside that bin, from the top
+  uint32_t prefix = 0;
+  for (int shift = KY::kBits - 8; shift >= 0; shift -= 8) {
+    __syncthreads();
+    clear();
+    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
+    for_row<Raw, VEC>(row, V, [&](uint32_t bits) {
+      const uint32_t key = KY::of(bits);
+      if (key < tau_k || (key & hi_mask) != (prefix & hi_mask)) return;
+      const float d = KY::val(bits) - M;
+      if (mass_bin(d, c_hi, c_lo) != bin) return;
+      const unsigned long long fx = __float2ull_rn(weight_pair_exp(d, c_hi, c_lo) * fs);
+      if (fx) atomicAdd(wh + ((key >> shift) & 0xFFu), fx);
+    });
+    reduce(true);
+    if (warp == 0) last_below(sm.tot, A, target, sm.sel, lane);
+    __syncthreads();
+    prefix |= (255u - static_cast<uint32_t>(sm.sel[0])) << shift;
+    A = sm.sel[1];
+    mg = sm.sel[2];
+  }
+  const double z = __ull2double_rn(A + mg) * __longlong_as_double(static_cast<long long>(1023 - s) << 52);
+  const float hi = static_cast<float>(z);
+  *kept = make_float2(hi, static_cast<float>(z - static_cast<double>(hi)));
+  __syncthreads();
+  return prefix;
+}
+
 template <typename Raw, bool VEC>
 __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) {
   using KY = Key<Raw>;
@@ -238,10 +389,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
   const float M = s_M;
   const float2 Zfull = s_Z;
   const bool ok = M == M && isfinite(M) && Zfull.x > 0.f;
-  auto weight_v = [&](float l) {
-    const float d = l - M;
-    return ex2_fast(fmaf(d, a.c_hi, d * a.c_lo));
-  };
+  auto weight_v = [&](float l) { return weight_pair_exp(l - M, a.c_hi, a.c_lo); };
   auto weight = [&](uint32_t bits) { return weight_v(KY::val(bits)); };
   StatRec out;
   out.M = M;
@@ -268,18 +416,21 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
       }
     }
     if (use_k && have < 0) tau = kth_largest<Raw, VEC>(row, a.V, a.top_k, hist, s_tot, s_sel, &count_ge);
-    // candidates: the keys >= tc, whole groups of equal keys and at most kCand
-    // of them: every token top-k keeps when they fit ("own"), else the groups
-    // above the (kCand + 1)-th largest key
+    // "own": every token top-k keeps (ties included) fits the candidate buffer
     const bool own = count_ge <= static_cast<unsigned>(kCand);
-    uint32_t tc = tau;
+    const uint32_t tc = tau;
+    float2 Zk = Zfull;  // mass of the tokens kept
     if (a.top_p < 1.f && !own) {
-      unsigned cnt;
-      tc = kth_largest<Raw, VEC>(row, a.V, kCand + 1, hist, s_tot, s_sel, &cnt) + 1u;
-    }
-    float2 Zk = Zfull;  // mass of the tokens top-k keeps
-    if (a.top_p < 1.f && use_k && !own) Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);
-    if (a.top_p >= 1.f && !own) {
+      // top-p over more tokens than the buffer holds (any nucleus size): the
+      // cut by a mass-weighted radix select over the row (s_buf is free: no
+      // filtered top-k set is held when the set does not fit)
+      static_assert(kSelWarps * 256 * 8 + 256 * 8 + 3 * 8 <= sizeof(uint32_t) * 2 * kCand, "mass histograms fit");
+      unsigned long long* mb = reinterpret_cast<unsigned long long*>(s_buf);
+      const MassSmem ms{mb, mb + kSelWarps * 256, mb + kSelWarps * 256 + 256};
+      float2 kept;
+      tau = topp_cut<Raw, VEC>(row, a.V, M, a.c_hi, a.c_lo, tau, a.top_p, ms, &kept);
+      Zk = kept;
+    } else if (a.top_p >= 1.f && !own) {
       Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);  // top-k alone, more tokens than the buffer
     } else {
       if (have < 0) {
@@ -356,7 +507,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
         }
         __syncthreads();  // s_ds is reused below
         before = ds_add(before, wex);  // mass of the entries before this thread's first
-        if (own) Zk = total;           // the candidates are exactly the kept-by-top-k set
+        Zk = total;                    // the candidates are exactly the kept-by-top-k set
         const float2 target = ds_mul_f(Zk, a.top_p);
         int last = -1;
         for (int i = 0; i < kPer; ++i) {
@@ -367,9 +518,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
         if (last >= 0) atomicMax(&s_last, last);
         __syncthreads();
         const int L = s_last;
-        // every candidate kept while tokens outside them hold mass before the target
-        const bool beyond = !own && L == n - 1 && ds_gt(target, total);
-        if (L < 0 || beyond) {
+        if (L < 0) {  // cannot happen: the first candidate has no mass before it and top_p > 0
           st = SPEC_ROW_WARP;
         } else {
           if (s_key[L] > tau) tau = s_key[L];
