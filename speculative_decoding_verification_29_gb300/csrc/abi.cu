@@ -194,11 +194,9 @@ int chain_scan(const ChainCall& c) {
   return cuda_status(launch_rowscan(a, c.dtype, vec, a.lanes ? kModeStatsLanes : kModeStats, c.st));
 }
 
-int chain_sample(const ChainCall& c) {
-  Layout L;
-  bool vec;
-  int e = chain_validate(c, &L, &vec);
-  if (e) return e;
+// The tail's arguments of a chain call (all but the sampling settings'
+// records).
+TailArgs tail_args(const ChainCall& c, const Layout& L, bool vec) {
   TailArgs t{};
   t.Lp = c.Lp;
   t.Lq = c.Lq;
@@ -218,6 +216,19 @@ int chain_sample(const ChainCall& c) {
   t.accept_len = c.accept_len;
   t.out_tokens = c.out_tokens;
   t.row_status = c.row_status;
+  t.lse_p = c.lse_p;
+  t.lse_q = c.lse_q;
+  t.px = c.px;
+  t.qx = c.qx;
+  return t;
+}
+
+int chain_sample(const ChainCall& c) {
+  Layout L;
+  bool vec;
+  int e = chain_validate(c, &L, &vec);
+  if (e) return e;
+  TailArgs t = tail_args(c, L, vec);
   if (c.top_k > 0 || c.top_p < 1.f) {  // records of the sampling settings' kept sets
     SelArgs s{};
     s.A = c.Lp;
@@ -241,10 +252,6 @@ int chain_sample(const ChainCall& c) {
     t.vtau = s.vtau;
     t.row_flag = s.row_flag;
   }
-  t.lse_p = c.lse_p;
-  t.lse_q = c.lse_q;
-  t.px = c.px;
-  t.qx = c.qx;
   return cuda_status(launch_chain_tail(t, c.dtype, vec, c.st));
 }
 
