@@ -269,3 +269,12 @@ def test_chain_single_stream_pooled(seed):
             c = gen.config_chain_single(seed * 8 + s2, T=T)
             compare_chain(gpu_chain(c), oracle_chain(c), c, name=f"chain_single_T{T}", pooled=pooled)
     assert_pooled(pooled, f"chain_single_{seed}")
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 5_000_000), (torch.float32, 2_100_001)])
+def test_chain_huge_vocab(dtype, V):
+    """Rows longer than 32 clusters of the streaming pass (bf16, 39 cluster
+    partials per row, folded 32 at a time by the tail) and an odd fp32 row on
+    the scalar path (17 partials)."""
+    c = gen.chain_zipf(1, 1, V, dtype, 1.0, 1.0, seed=V % 11)
+    compare_chain(gpu_chain(c), oracle_chain(c), c, name=f"chain_huge_{V}")
