@@ -196,61 +196,90 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
 // The tokens top-p keeps are a prefix of the value groups in descending
 // order: group g is kept iff the mass of the tokens top-k keeps with a
 // strictly larger logit is below top_p Z_k. Its last group is found without
-// sorting. The weights are summed exactly in 64-bit fixed point (w 2^s, s
-// chosen so that V terms cannot overflow; the sums are deterministic and do
-// not depend on the order of the atomics) into histograms: first over 256
-// bins of the log-weight, 1/8 of a binary order of magnitude each (the bin
-// is a monotone function of the key, so a bin is a contiguous key range and
-// a group never straddles two bins), then over the 8-bit digits of the keys
-// inside the bin the cut falls in (2 passes for bf16 keys, 4 for fp32). Each
-// level keeps the last entry, in descending value order, that has mass and
-// whose preceding mass is below the target.
+// sorting, by passes over the row that each split the remaining candidates
+// into 16 bins and keep the bin holding the cut. The weights are summed
+// exactly in 64-bit fixed point (w 2^s, s chosen so that V terms cannot
+// overflow), each thread into its own 16 bins in shared memory (no atomics:
+// the sums are exact, deterministic and free of contention when most of a
+// row falls into a few bins), then the bins are totalled over the CTA. The
+// first pass bins by the log-weight, 2 binary orders of magnitude per bin
+// (the bin is a monotone function of the key, so a bin is a contiguous key
+// range and a group never straddles two bins); the next passes bin the keys
+// inside the chosen bin by 4-bit digits from the top (4 passes for bf16
+// keys, 8 for fp32) until one key, the cut, is left. Each pass keeps the
+// last bin, in descending value order, that has mass and whose preceding
+// mass is below the target.
 
-// Log-weight bin of d = l - M: floor(-8 a) for a = d log2(e) / T in (-32, 0],
-// 255 below (and for -inf); monotone in l.
+// Log-weight bin of d = l - M: floor(-a / 2) for a = d log2(e) / T in
+// (-30, 0], 15 below (and for -inf); monotone in l.
 __device__ __forceinline__ int mass_bin(float d, float c_hi, float c_lo) {
   const float a = fmaf(d, c_hi, d * c_lo);
-  return a > -32.f ? static_cast<int>(-8.f * a) : 255;
+  return a > -30.f ? static_cast<int>(-0.5f * a) : 15;
 }
 
+constexpr int kMassBins = 16;
+
 struct MassSmem {
-  unsigned long long* wh;   // kSelWarps x 256 per-warp histograms
-  unsigned long long* tot;  // 256 totals, in descending value order
-  unsigned long long* sel;  // [0] the chosen entry, [1] the mass before it, [2] its mass
+  unsigned long long* th;   // [kMassBins][kSelThreads]: each thread's own bins
+  unsigned long long* tot;  // [kMassBins] totals, in descending value order
+  unsigned long long* sel;  // [0] the chosen bin, [1] the mass before it, [2] its mass
+  unsigned long long* loc;  // [2][kMassBins] this CTA's totals, read by the cluster (clusters only)
 };
 
-// One full warp: over tot[0..255] (descending value order), the last entry
+// A CTA's part of a row: its slice [off, off + len) and the cluster's size
+// (a row split over a cluster of C CTAs; C = 1: the whole row).
+struct RowPart {
+  int off, len, C;
+};
+
+// Bin totals over the CTA (reverse: bin d stored at kMassBins - 1 - d, so
+// that the totals run in descending value order), then over the cluster's
+// CTAs: each adds all C CTAs' totals from distributed shared memory in rank
+// order, so that every CTA holds the same sums. The CTA totals alternate
+// between the halves of loc (parity): a CTA writing the next pass's totals
+// has passed the cluster barrier that every CTA reaches only after reading
+// this pass's, so no totals are overwritten while another CTA reads them.
+__device__ __forceinline__ void mass_totals(const MassSmem& sm, bool reverse, int C, int parity) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long* dst = C > 1 ? sm.loc + parity * kMassBins : sm.tot;
+  __syncthreads();
+  for (int bin = warp; bin < kMassBins; bin += kSelWarps) {
+    unsigned long long t = 0;
+#pragma unroll
+    for (int i = 0; i < kSelThreads / 32; ++i) t += sm.th[bin * kSelThreads + lane + 32 * i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) dst[reverse ? kMassBins - 1 - bin : bin] = t;
+  }
+  if (C > 1) {
+    cluster_arrive();  // this CTA's totals are written (release)
+    cluster_wait();    // and every other CTA's (acquire)
+    if (tid < kMassBins) {
+      unsigned long long t = 0;
+      for (int r = 0; r < C; ++r) t += ld_cluster_u64(cluster_addr(dst + tid, static_cast<unsigned>(r)));
+      sm.tot[tid] = t;
+    }
+  }
+  __syncthreads();
+}
+
+// One full warp: over tot[0..15] (descending value order), the last entry
 // with mass whose preceding mass A + sum_{e' < e} tot[e'] is below target.
-// Lane l holds entries 8 l .. 8 l + 7.
 __device__ __forceinline__ void last_below(const unsigned long long* tot, unsigned long long A, double target,
                                            unsigned long long* sel, int lane) {
-  unsigned long long m[8], sum = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    m[i] = tot[8 * lane + i];
-    sum += m[i];
-  }
-  unsigned long long incl = sum;
+  const unsigned long long m = lane < kMassBins ? tot[lane] : 0ull;
+  unsigned long long incl = m;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  unsigned long long run = A + (incl - sum), bb = 0, bm = 0;
-  int best = -1;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (m[i] > 0ull && __ull2double_rn(run) < target) {
-      best = 8 * lane + i;
-      bb = run;
-      bm = m[i];
-    }
-    run += m[i];
-  }
-  const int e = __reduce_max_sync(0xffffffffu, static_cast<unsigned>(best + 1)) - 1;
-  const int src = e < 0 ? 0 : e >> 3;
-  bb = __shfl_sync(0xffffffffu, bb, src);
-  bm = __shfl_sync(0xffffffffu, bm, src);
+  const unsigned long long before = A + (incl - m);
+  const bool ok = lane < kMassBins && m > 0ull && __ull2double_rn(before) < target;
+  const unsigned bal = __ballot_sync(0xffffffffu, ok);
+  const int e = bal ? 31 - __clz(bal) : -1;
+  const int src = e < 0 ? 0 : e;
+  const unsigned long long bb = __shfl_sync(0xffffffffu, before, src), bm = __shfl_sync(0xffffffffu, m, src);
   if (lane == 0) {
     sel[0] = static_cast<unsigned long long>(static_cast<long long>(e));
     sel[1] = bb;
@@ -260,42 +289,37 @@ __device__ __forceinline__ void last_below(const unsigned long long* tot, unsign
 
 // The top-p cut of one row over the tokens with key >= tau_k (0: all): the
 // key of the last kept group, and (*kept) the kept mass relative to the row
-// maximum as a float pair. Called by every thread of the CTA.
+// maximum as a float pair. Called by every thread of the CTA, or of each CTA
+// of a cluster that splits the row (every CTA gets the same results; one
+// cluster barrier per pass, and one at the end so that no CTA exits while
+// another may still read its totals).
 template <typename Raw, bool VEC>
 __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c_lo, uint32_t tau_k, float top_p,
-                             const MassSmem& sm, float2* kept) {
+                             const MassSmem& sm, float2* kept, RowPart part) {
   using KY = Key<Raw>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = 62 - (32 - __clz(V));                // V terms of at most 2^s stay below 2^62
   const float fs = __int_as_float((127 + s) << 23);  // 2^s
-  unsigned long long* wh = sm.wh + warp * 256;
+  unsigned long long* mine = sm.th + tid;            // this thread's bin b at mine[b * kSelThreads]
   auto clear = [&]() {
-    for (int i = tid; i < kSelWarps * 256; i += kSelThreads) sm.wh[i] = 0ull;
-    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < kMassBins; ++b) mine[b * kSelThreads] = 0ull;
   };
-  auto reduce = [&](bool reverse) {  // per-warp histograms into tot (reverse: digit d at 255 - d)
-    __syncthreads();
-    for (int b = tid; b < 256; b += kSelThreads) {
-      unsigned long long t = 0;
-      for (int w = 0; w < kSelWarps; ++w) t += sm.wh[w * 256 + b];
-      sm.tot[reverse ? 255 - b : b] = t;
-    }
-    __syncthreads();
-  };
-  // level 1: the log-weight bins
+  const Raw* slice = row + part.off;
+  int parity = 0;
+  // pass 1: the log-weight bins
   clear();
-  for_row<Raw, VEC>(row, V, [&](uint32_t bits) {
+  for_row<Raw, VEC>(slice, part.len, [&](uint32_t bits) {
     if (KY::of(bits) < tau_k) return;
     const float d = KY::val(bits) - M;
     const unsigned long long fx = __float2ull_rn(weight_pair_exp(d, c_hi, c_lo) * fs);
-    if (fx) atomicAdd(wh + mass_bin(d, c_hi, c_lo), fx);
+    if (fx) mine[mass_bin(d, c_hi, c_lo) * kSelThreads] += fx;
   });
-  reduce(false);
+  mass_totals(sm, false, part.C, parity);
+  parity ^= 1;
   __shared__ double s_target;
   if (warp == 0) {
-    unsigned long long t = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) t += sm.tot[8 * lane + i];
+    unsigned long long t = lane < kMassBins ? sm.tot[lane] : 0ull;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
     const double target = static_cast<double>(top_p) * __ull2double_rn(t);
@@ -306,36 +330,66 @@ __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c
   const double target = s_target;
   const int bin = static_cast<int>(static_cast<long long>(sm.sel[0]));
   unsigned long long A = sm.sel[1], mg = sm.sel[2];
-  // level 2: the digits of the keys inside that bin, from the top
-  uint32_t prefix = 0;
-  for (int shift = KY::kBits - 8; shift >= 0; shift -= 8) {
-    __syncthreads();
+  // the bin is a contiguous key interval [klo, khi] (the bin does not
+  // increase with the key): its ends by binary search over the keys up to
+  // the row maximum's (the keys of NaN bit patterns, all below -inf's, fall
+  // in the last bin like -inf)
+  __shared__ uint32_t s_kr[2];
+  if (tid == 0) {
+    const uint32_t kM = KY::of(sizeof(Raw) == 2 ? (__float_as_uint(M) >> 16) : __float_as_uint(M));
+    auto first_at_most = [&](int b) {  // the smallest key <= kM whose bin is <= b (kM + 1: none)
+      uint32_t lo = 0u, hi = kM + 1u;
+      while (lo < hi) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        if (mass_bin(key_value<Raw>(mid) - M, c_hi, c_lo) <= b) hi = mid; else lo = mid + 1u;
+      }
+      return lo;
+    };
+    s_kr[0] = max(first_at_most(bin), tau_k);
+    s_kr[1] = first_at_most(bin - 1) - 1u;
+  }
+  __syncthreads();
+  const uint32_t klo = s_kr[0], khi = s_kr[1];
+  // the next passes: 4-bit digits of key - klo over the bits where the
+  // interval's keys differ, from the top
+  const uint32_t span = khi - klo;
+  const int nbits = span == 0u ? 0 : 32 - __clz(span);
+  uint32_t prefix = 0;  // of key - klo
+  for (int shift = ((nbits + 3) & ~3) - 4; shift >= 0; shift -= 4) {
+    __syncthreads();  // the totals of the last pass are read
     clear();
-    const uint32_t hi_mask = shift + 8 >= 32 ? 0u : ~((1u << (shift + 8)) - 1u);
-    for_row<Raw, VEC>(row, V, [&](uint32_t bits) {
-      const uint32_t key = KY::of(bits);
-      if (key < tau_k || (key & hi_mask) != (prefix & hi_mask)) return;
-      const float d = KY::val(bits) - M;
-      if (mass_bin(d, c_hi, c_lo) != bin) return;
-      const unsigned long long fx = __float2ull_rn(weight_pair_exp(d, c_hi, c_lo) * fs);
-      if (fx) atomicAdd(wh + ((key >> shift) & 0xFFu), fx);
+    const uint32_t hi_mask = shift + 4 >= 32 ? 0u : ~((1u << (shift + 4)) - 1u);
+    for_row<Raw, VEC>(slice, part.len, [&](uint32_t bits) {
+      const uint32_t rel = KY::of(bits) - klo;  // wraps for keys below klo
+      if (rel > span || (rel & hi_mask) != prefix) return;
+      const unsigned long long fx = __float2ull_rn(weight_pair_exp(KY::val(bits) - M, c_hi, c_lo) * fs);
+      if (fx) mine[((rel >> shift) & 0xFu) * kSelThreads] += fx;
     });
-    reduce(true);
+    mass_totals(sm, true, part.C, parity);
+    parity ^= 1;
     if (warp == 0) last_below(sm.tot, A, target, sm.sel, lane);
     __syncthreads();
-    prefix |= (255u - static_cast<uint32_t>(sm.sel[0])) << shift;
+    prefix |= (static_cast<uint32_t>(kMassBins - 1) - static_cast<uint32_t>(sm.sel[0])) << shift;
     A = sm.sel[1];
     mg = sm.sel[2];
   }
+  const uint32_t cut = klo + prefix;
   const double z = __ull2double_rn(A + mg) * __longlong_as_double(static_cast<long long>(1023 - s) << 52);
   const float hi = static_cast<float>(z);
   *kept = make_float2(hi, static_cast<float>(z - static_cast<double>(hi)));
+  if (part.C > 1) {
+    cluster_arrive();
+    cluster_wait();
+  }
   __syncthreads();
-  return prefix;
+  return cut;
 }
 
-template <typename Raw, bool VEC>
-__global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) {
+// ROWWISE: one CTA per row (blockIdx.x), every row by the whole-CTA path:
+// launched when no row can take the warp path (no lane records, no top-k, or
+// a top-k past the segment count), so that the rows run in parallel.
+template <typename Raw, bool VEC, bool ROWWISE>
+__global__ void __launch_bounds__(kSelThreads, ROWWISE ? 4 : 2) warp_select_kernel(SelArgs a) {
   using KY = Key<Raw>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int RPG = a.TR + a.DR;
@@ -347,7 +401,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
   float* s_w = reinterpret_cast<float*>(s_buf + kCand);      // kCand weights
   static_assert(kSelWarps * 256 <= 2 * kCand, "histograms fit the candidate buffer");
   __shared__ unsigned s_tot[256];
-  __shared__ unsigned s_wh[kSelWarps * 256];
+  __shared__ __align__(16) unsigned s_wh[kSelWarps * 256];
   __shared__ uint32_t s_sel[4];
   __shared__ float2 s_ds[kSelWarps];
   __shared__ int s_cnt[kSelWarps];
@@ -359,7 +413,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
   // the tail may launch now: the pass has completed, so its clusters take
   // only SM room the selection leaves free while they wait for this grid
   griddep_launch_dependents();
-  {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
+  if constexpr (!ROWWISE) {  // one warp per row with few candidates (s_buf: the warps' candidate and lane buffers)
     const int row_id = blockIdx.x * kSelWarps + warp;
     static_assert(kSelWarps * (kWarpList * 8 + kChunkCap * 8) <= sizeof(uint32_t) * 2 * kCand, "warp buffers fit");
     uint64_t* wl = reinterpret_cast<uint64_t*>(s_buf);
@@ -368,8 +422,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
     const bool done = row_id >= rows || warped_list_row<Raw, VEC>(a, row_id, wl + warp * kWarpList,
                                                                   wc + warp * kChunkCap, wm + warp * kChunkCap, lane);
     if (lane == 0) s_slow[warp] = !done;
+    __syncthreads();
   }
-  __syncthreads();
   // the other rows, one at a time by the whole CTA
   auto cta_row = [&](const int row_id) {
   __syncthreads();  // shared memory is reused from the previous row
@@ -424,11 +478,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
       // top-p over more tokens than the buffer holds (any nucleus size): the
       // cut by a mass-weighted radix select over the row (s_buf is free: no
       // filtered top-k set is held when the set does not fit)
-      static_assert(kSelWarps * 256 * 8 + 256 * 8 + 3 * 8 <= sizeof(uint32_t) * 2 * kCand, "mass histograms fit");
-      unsigned long long* mb = reinterpret_cast<unsigned long long*>(s_buf);
-      const MassSmem ms{mb, mb + kSelWarps * 256, mb + kSelWarps * 256 + 256};
+      static_assert(kMassBins * kSelThreads * 8 <= sizeof(uint32_t) * 2 * kCand, "the threads' bins fit");
+      static_assert(kMassBins * 8 + 3 * 8 <= sizeof(unsigned) * kSelWarps * 256, "the totals fit");
+      unsigned long long* mt = reinterpret_cast<unsigned long long*>(s_wh);
+      const MassSmem ms{reinterpret_cast<unsigned long long*>(s_buf), mt, mt + kMassBins, nullptr};
       float2 kept;
-      tau = topp_cut<Raw, VEC>(row, a.V, M, a.c_hi, a.c_lo, tau, a.top_p, ms, &kept);
+      tau = topp_cut<Raw, VEC>(row, a.V, M, a.c_hi, a.c_lo, tau, a.top_p, ms, &kept, RowPart{0, a.V, 1});
       Zk = kept;
     } else if (a.top_p >= 1.f && !own) {
       Zk = kept_mass<Raw, VEC>(row, a.V, tau, weight, s_ds);  // top-k alone, more tokens than the buffer
@@ -546,8 +601,67 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
     a.row_flag[row_id] = st;
   }
   };
-  for (int w = 0; w < kSelWarps; ++w)
-    if (s_slow[w]) cta_row(blockIdx.x * kSelWarps + w);
+  if constexpr (ROWWISE) {
+    cta_row(blockIdx.x);
+  } else {
+    for (int w = 0; w < kSelWarps; ++w)
+      if (s_slow[w]) cta_row(blockIdx.x * kSelWarps + w);
+  }
+}
+
+// Top-p alone over rows longer than the candidate buffer: a cluster of C
+// CTAs (the launch's cluster size) per row, each summing the weights of its
+// slice of the row; every CTA reaches the same cut and the first writes the
+// row's record.
+template <typename Raw, bool VEC>
+__global__ void __launch_bounds__(kSelThreads, 4) topp_rows_kernel(SelArgs a) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = static_cast<int>(cluster_nctarank()), rank = static_cast<int>(cluster_ctarank());
+  const int row_id = static_cast<int>(blockIdx.x) / C;
+  const int RPG = a.TR + a.DR;
+  const int b = row_id / RPG, j = row_id - b * RPG;
+  const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
+                            : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
+  __shared__ __align__(16) unsigned long long s_th[kMassBins * kSelThreads];
+  __shared__ unsigned long long s_tot[kMassBins], s_sel[4], s_loc[2 * kMassBins];
+  __shared__ float s_M;
+  __shared__ float2 s_Z;
+  griddep_wait();
+  griddep_launch_dependents();
+  if (warp == 0) {  // M and Z of the row from the stats partials
+    float2 z;
+    const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
+    if (lane == 0) {
+      s_M = M;
+      s_Z = z;
+    }
+  }
+  __syncthreads();
+  const float M = s_M;
+  const float2 Z = s_Z;
+  StatRec out;
+  out.M = M;
+  out.Z = NAN;
+  out.Lhi = out.Llo = NAN;
+  uint32_t tau = 0;
+  if (M == M && isfinite(M) && Z.x > 0.f) {  // the same in every CTA of the cluster
+    constexpr int kUnit = VEC ? Elem<Raw>::kPerVec : 1;  // slices start on 16-byte boundaries when VEC
+    const long long units = a.V / kUnit;
+    const long long lo = units * rank / C, hi = units * (rank + 1) / C;
+    const MassSmem ms{s_th, s_tot, s_sel, s_loc};
+    float2 kept;
+    tau = topp_cut<Raw, VEC>(row, a.V, M, a.c_hi, a.c_lo, 0u, a.top_p, ms, &kept,
+                             RowPart{static_cast<int>(lo * kUnit), static_cast<int>((hi - lo) * kUnit), C});
+    const float2 L2 = ds_log2(kept);
+    out.Z = kept.x;
+    out.Lhi = L2.x;
+    out.Llo = L2.y;
+  }
+  if (rank == 0 && tid == 0) {
+    a.rec[row_id] = out;
+    a.vtau[row_id] = key_value<Raw>(tau);
+    a.row_flag[row_id] = 0;
+  }
 }
 
 }  // namespace
@@ -555,13 +669,40 @@ __global__ void __launch_bounds__(kSelThreads, 2) warp_select_kernel(SelArgs a) 
 int select_candidates() { return kCand; }
 
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>((static_cast<long long>(a.B) * (a.TR + a.DR) + kSelWarps - 1) / kSelWarps)),
-      block(kSelThreads);
+  const long long rows = static_cast<long long>(a.B) * (a.TR + a.DR);
+  if (!(a.top_k > 0 && a.top_k < a.V) && a.top_p < 1.f && a.V > kCand) {
+    // top-p alone over rows longer than the candidate buffer: rows split over
+    // clusters of up to 8 CTAs while the rows alone leave SMs idle (four
+    // CTAs fit an SM)
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    int C = 1;
+    while (C < 8 && rows * C * 2 <= 4LL * sms) C *= 2;
+    const dim3 grid(static_cast<unsigned>(rows * C)), block(kSelThreads);
+    if (dtype == SPEC_BF16)
+      return vec ? launch_pdl(topp_rows_kernel<uint16_t, true>, grid, block, st, a, C)
+                 : launch_pdl(topp_rows_kernel<uint16_t, false>, grid, block, st, a, C);
+    return vec ? launch_pdl(topp_rows_kernel<float, true>, grid, block, st, a, C)
+               : launch_pdl(topp_rows_kernel<float, false>, grid, block, st, a, C);
+  }
+  // no row can take the warp path (it needs the lane records and a top-k of
+  // at most the segment count): one CTA per row
+  const bool rowwise = a.lanes == nullptr || a.P > 256 || !(a.top_k > 0 && a.top_k <= a.P && a.top_k < a.V);
+  const dim3 grid(static_cast<unsigned>(rowwise ? rows : (rows + kSelWarps - 1) / kSelWarps)), block(kSelThreads);
+  if (rowwise) {
+    if (dtype == SPEC_BF16)
+      return vec ? launch_pdl(warp_select_kernel<uint16_t, true, true>, grid, block, st, a)
+                 : launch_pdl(warp_select_kernel<uint16_t, false, true>, grid, block, st, a);
+    return vec ? launch_pdl(warp_select_kernel<float, true, true>, grid, block, st, a)
+               : launch_pdl(warp_select_kernel<float, false, true>, grid, block, st, a);
+  }
   if (dtype == SPEC_BF16)
-    return vec ? launch_pdl(warp_select_kernel<uint16_t, true>, grid, block, st, a)
-               : launch_pdl(warp_select_kernel<uint16_t, false>, grid, block, st, a);
-  return vec ? launch_pdl(warp_select_kernel<float, true>, grid, block, st, a)
-             : launch_pdl(warp_select_kernel<float, false>, grid, block, st, a);
+    return vec ? launch_pdl(warp_select_kernel<uint16_t, true, false>, grid, block, st, a)
+               : launch_pdl(warp_select_kernel<uint16_t, false, false>, grid, block, st, a);
+  return vec ? launch_pdl(warp_select_kernel<float, true, false>, grid, block, st, a)
+             : launch_pdl(warp_select_kernel<float, false, false>, grid, block, st, a);
 }
 
 }  // namespace specv

@@ -48,60 +48,110 @@ __device__ __forceinline__ float key_value(uint32_t tau) {
   }
 }
 
-// Calls f(bits) for every element of the row (16-byte loads when VEC).
+// Loads in flight per thread in the passes over a row (rows evicted from L2
+// are read at HBM latency: one load at a time left these passes waiting).
+constexpr int kRowLoads = 4;
+
+// Calls f(bits) for every element of the row (16-byte loads when VEC),
+// kRowLoads loads per thread in flight.
 template <typename Raw, bool VEC, typename F>
 __device__ __forceinline__ void for_row(const Raw* row, int V, F f) {
   if constexpr (VEC) {
     constexpr int EPV = Elem<Raw>::kPerVec;
     const int nv = V / EPV;
-    for (int vi = threadIdx.x; vi < nv; vi += kSelThreads) {
-      const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row) + vi);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kSelThreads * kRowLoads) {
+      uint4 q[kRowLoads];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if constexpr (EPV == 8) {
-          f(w[i] & 0xFFFFu);
-          f(w[i] >> 16);
-        } else {
-          f(w[i]);
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int vi = v0 + u * kSelThreads;
+        if (vi < nv) q[u] = __ldcg(reinterpret_cast<const uint4*>(row) + vi);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        if (v0 + u * kSelThreads >= nv) break;
+        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (EPV == 8) {
+            f(w[i] & 0xFFFFu);
+            f(w[i] >> 16);
+          } else {
+            f(w[i]);
+          }
         }
       }
     }
   } else {
-    for (int v = threadIdx.x; v < V; v += kSelThreads) {
-      if constexpr (sizeof(Raw) == 2)
-        f(static_cast<uint32_t>(row[v]));
-      else
-        f(__float_as_uint(row[v]));
+    for (int v0 = threadIdx.x; v0 < V; v0 += kSelThreads * kRowLoads) {
+      uint32_t q[kRowLoads];
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int v = v0 + u * kSelThreads;
+        if (v < V) {
+          if constexpr (sizeof(Raw) == 2)
+            q[u] = static_cast<uint32_t>(row[v]);
+          else
+            q[u] = __float_as_uint(row[v]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        if (v0 + u * kSelThreads >= V) break;
+        f(q[u]);
+      }
     }
   }
 }
 
-// Calls f(index, bits) for every element of the row (16-byte loads when VEC).
+// Calls f(index, bits) for every element of the row (16-byte loads when
+// VEC), kRowLoads loads per thread in flight.
 template <typename Raw, bool VEC, typename F>
 __device__ __forceinline__ void for_row_i(const Raw* row, int V, F f) {
   if constexpr (VEC) {
     constexpr int EPV = Elem<Raw>::kPerVec;
     const int nv = V / EPV;
-    for (int vi = threadIdx.x; vi < nv; vi += kSelThreads) {
-      const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row) + vi);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kSelThreads * kRowLoads) {
+      uint4 q[kRowLoads];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if constexpr (EPV == 8) {
-          f(vi * 8 + 2 * i, w[i] & 0xFFFFu);
-          f(vi * 8 + 2 * i + 1, w[i] >> 16);
-        } else {
-          f(vi * 4 + i, w[i]);
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int vi = v0 + u * kSelThreads;
+        if (vi < nv) q[u] = __ldcg(reinterpret_cast<const uint4*>(row) + vi);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int vi = v0 + u * kSelThreads;
+        if (vi >= nv) break;
+        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (EPV == 8) {
+            f(vi * 8 + 2 * i, w[i] & 0xFFFFu);
+            f(vi * 8 + 2 * i + 1, w[i] >> 16);
+          } else {
+            f(vi * 4 + i, w[i]);
+          }
         }
       }
     }
   } else {
-    for (int v = threadIdx.x; v < V; v += kSelThreads) {
-      if constexpr (sizeof(Raw) == 2)
-        f(v, static_cast<uint32_t>(row[v]));
-      else
-        f(v, __float_as_uint(row[v]));
+    for (int v0 = threadIdx.x; v0 < V; v0 += kSelThreads * kRowLoads) {
+      uint32_t q[kRowLoads];
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int v = v0 + u * kSelThreads;
+        if (v < V) {
+          if constexpr (sizeof(Raw) == 2)
+            q[u] = static_cast<uint32_t>(row[v]);
+          else
+            q[u] = __float_as_uint(row[v]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int v = v0 + u * kSelThreads;
+        if (v >= V) break;
+        f(v, q[u]);
+      }
     }
   }
 }

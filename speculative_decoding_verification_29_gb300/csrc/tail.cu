@@ -239,22 +239,7 @@ __device__ __forceinline__ float2 butterfly8(const float (&v)[8], int lane) {
   return ds_add(r1, shfl_xor2(r1, 1));
 }
 
-// ---- thread-block cluster primitives (distributed shared memory)
-__device__ __forceinline__ unsigned cluster_ctarank() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-// Address of `p` (this CTA's shared memory) in the shared memory of CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, unsigned rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(r)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
-  return r;
-}
+// ---- stores into another CTA's shared memory (cluster primitives in common.cuh)
 __device__ __forceinline__ void st_cluster(uint32_t addr, float2 v) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
 }

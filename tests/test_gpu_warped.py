@@ -126,6 +126,23 @@ def test_warped_large_nucleus(dtype, V, T, top_k, top_p):
     compare(*run(c, top_k, top_p), name=f"warped_nucleus_{V}_{top_k}_{top_p}")
 
 
+@pytest.mark.parametrize("B,K,V,dtype", [
+    (24, 8, 32000, torch.bfloat16),   # 408 rows: one CTA per row
+    (12, 8, 32000, torch.float32),    # 204 rows: clusters of 2
+    (1, 8, 128256, torch.bfloat16),   # 17 rows: clusters of 8
+    (2, 5, 40001, torch.bfloat16),    # odd length: element-wise slices
+    (3, 4, 65537, torch.float32),
+])
+def test_warped_topp_alone_row_splits(B, K, V, dtype):
+    """Top-p alone over rows longer than the candidate buffer, at batch sizes
+    that split each row over 1, 2 and 8 CTAs whose weight sums are totalled
+    through distributed shared memory, and on row lengths whose slices are
+    not 16-byte aligned: the same cuts as the oracle."""
+    c = gen.chain_zipf(B, K, V, dtype, 1.0, 0.7, seed=B + K)
+    compare(*run(c, 0, 0.9), name=f"warped_topp_split_{B}_{V}")
+    compare(*run(c, V, 0.6), name=f"warped_topp_split_{B}_{V}_kV")  # a top-k of V keeps every token
+
+
 def test_warped_large_nucleus_integer_ties():
     """Integer logits over 20000 tokens: huge groups of equal values at the
     top-p cut are kept or dropped whole (the radix digits isolate one key)."""
