@@ -8,7 +8,7 @@ acceptance decision and the residual / bonus draw.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload chain_batched|chain_single|chain_deep|greedy|tree|entropy|
-                                warped|kv_compact|merge|expand]
+                                warped|nucleus|kv_compact|merge|expand]
 
 Under torchrun each rank verifies its own batch (seed + rank) on its own GPU:
 rows are independent, so there is no collective in the data path (weak
@@ -108,6 +108,13 @@ def make_workload(name: str, seed: int):
         return c, dict(workload="chain verify with top-k 50 and top-p 0.9 on both models: B=64 K=8 V=128256 bf16 "
                                 "T=0.7, draft noise sigma_b~U(0.2,2)", B=64, K=8, V=128256, logits="bf16",
                        temperature=0.7, top_k=50, top_p=0.9)
+    if name == "nucleus":
+        c = gen.chain_zipf(64, 8, 128256, __import__("torch").bfloat16, 0.7, gen.workloads._sigma_spread, seed,
+                           name="chain_batched")
+        c.top_k, c.top_p = 0, 0.95
+        return c, dict(workload="chain verify with top-p 0.95 alone on both models (nuclei of thousands of tokens): "
+                                "B=64 K=8 V=128256 bf16 T=0.7, draft noise sigma_b~U(0.2,2)", B=64, K=8, V=128256,
+                       logits="bf16", temperature=0.7, top_k=0, top_p=0.95)
     if name == "entropy":
         t = gen.config_tree(seed)
         t.Ld = gen.tree_draft_logits(t, seed)
@@ -280,7 +287,7 @@ def run_ours(args):
                 ev[1].record(stream)
 
             timed_kernel = "rowscan_kernel + greedy_decide_kernel (one call)"
-        elif name == "warped":
+        elif name in ("warped", "nucleus"):
             ws_t = sv.alloc_workspace(sv.warped_workspace_bytes(w.B, w.K, w.V, w.Lp.dtype), dev)
             out = sv.spec_verify_chain_warped(*sets[0], T, w.top_k, w.top_p, workspace=ws_t)
 
@@ -292,7 +299,8 @@ def run_ours(args):
                 sv.spec_verify_chain_warped(*sets[i % n_sets], T, w.top_k, w.top_p, out=out, workspace=ws_t)
                 ev[1].record(stream)
 
-            timed_kernel = "rowscan_kernel + warp_select_kernel + chain_tail_kernel (one call)"
+            timed_kernel = ("rowscan_kernel + warp_select_kernel + chain_tail_kernel (one call)" if name == "warped"
+                            else "rowscan_kernel + topp_rows_kernel + chain_tail_kernel (one call)")
         else:
             out = sv.spec_verify_chain(*sets[0], T, workspace=ws_t)
             # one prepared call per rotating input set (the serving-loop form of the API)
@@ -309,7 +317,7 @@ def run_ours(args):
                 sv.spec_chain_sample(*args_, T, out, ws_t)
 
             timed_kernel = "rowscan_kernel"
-        launches_per_step = 3 if name == "warped" else 2
+        launches_per_step = 3 if name in ("warped", "nucleus") else 2
         host = [w.Lp, w.Lq, w.x, w.ua, w.ur]
 
     # warm-up, then a short untimed soak so the clock sampler sees the load
@@ -381,7 +389,7 @@ def run_ours(args):
     pinned = [h.pin_memory() for h in host]
     h2d = sum(h.numel() * h.element_size() for h in pinned)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    host_chain = name not in ("entropy", "tree", "warped")
+    host_chain = name not in ("entropy", "tree", "warped", "nucleus")
     if host_chain and w.T == 0.0:  # greedy: only the target logits and the draft tokens are copied
         h2d = pinned[0].numel() * pinned[0].element_size() + pinned[2].numel() * pinned[2].element_size()
     if host_chain:
@@ -402,7 +410,7 @@ def run_ours(args):
             o = sv.spec_verify_tree_greedy(pinned[0], pinned[1], pinned[2], w.n1, tree_mask=pinned[3], device=dev)
             co = sv.spec_tree_confidence(pinned[4], w.n1, device=dev)
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu(), co["choice"].cpu()]
-        elif name == "warped":
+        elif name in ("warped", "nucleus"):
             o = sv.spec_verify_chain_warped(*pinned, w.T, w.top_k, w.top_p, device=dev)
             res = [o["accept_len"].cpu(), o["out_tokens"].cpu()]
         else:  # sampling or greedy chain: host buffers in, host buffers out
@@ -639,7 +647,7 @@ def _oracle_step(name, w, rows, threads):
     elif name == "tree":
         oracle.verify_tree_greedy(w.Lt[idx], w.tok[idx], w.R[idx], w.n1, mask=w.mask[idx], threads=threads)
         oracle.tree_confidence(w.conf[idx], w.n1)
-    elif name == "warped":
+    elif name in ("warped", "nucleus"):
         oracle.verify_chain_warped(w.Lp[idx], w.Lq[idx], w.x[idx], w.ua[idx], w.ur[idx], w.T, w.top_k, w.top_p,
                                    threads=threads)
     elif w.T == 0.0:
@@ -995,7 +1003,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="chain_batched",
-                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact", "merge", "warped",
+                    choices=["chain_batched", "chain_single", "chain_deep", "greedy", "tree", "entropy", "kv_compact", "merge", "warped", "nucleus",
                              "expand"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds of steps before timing (clock samples)")

@@ -210,12 +210,12 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
 // last bin, in descending value order, that has mass and whose preceding
 // mass is below the target.
 
-// Log-weight bin of d = l - M: floor(-a / 2) for a = d log2(e) / T in
-// (-30, 0], 15 below (and for -inf); monotone in l.
-__device__ __forceinline__ int mass_bin(float d, float c_hi, float c_lo) {
-  const float a = fmaf(d, c_hi, d * c_lo);
-  return a > -30.f ? static_cast<int>(-0.5f * a) : 15;
-}
+// Log-weight bin from p = (l - M) c_hi, the leading part of the weight's
+// exponent: floor(-p / 2) for p in (-30, 0], 15 below (and for -inf); p is
+// a rounded product of l - M and a positive constant, so the bin does not
+// increase with l.
+__device__ __forceinline__ int mass_bin_p(float p) { return p > -30.f ? static_cast<int>(-0.5f * p) : 15; }
+__device__ __forceinline__ int mass_bin(float d, float c_hi) { return mass_bin_p(d * c_hi); }
 
 constexpr int kMassBins = 16;
 
@@ -307,13 +307,28 @@ __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c
   };
   const Raw* slice = row + part.off;
   int parity = 0;
-  // pass 1: the log-weight bins
+  // pass 1: the log-weight bins, two elements at a time in packed pairs
+  // (the weight as weight_pair_exp forms it, scaled by 2^s)
+  const float vtau = key_value<Raw>(tau_k);  // elements below it are not kept by top-k (-inf: all kept)
+  const float2 M2 = make_float2(-M, -M), ch2 = make_float2(c_hi, c_hi), cl2 = make_float2(c_lo, c_lo);
+  const float2 ln2 = make_float2(0.693147180559945309f, 0.693147180559945309f), one2 = make_float2(1.f, 1.f);
+  const float2 fs2 = make_float2(fs, fs);
   clear();
-  for_row<Raw, VEC>(slice, part.len, [&](uint32_t bits) {
-    if (KY::of(bits) < tau_k) return;
-    const float d = KY::val(bits) - M;
-    const unsigned long long fx = __float2ull_rn(weight_pair_exp(d, c_hi, c_lo) * fs);
-    if (fx) mine[mass_bin(d, c_hi, c_lo) * kSelThreads] += fx;
+  for_row_pairs<Raw, VEC>(slice, part.len, [&](float2 v) {
+    if (v.x < vtau) v.x = -INFINITY;
+    if (v.y < vtau) v.y = -INFINITY;
+    const float2 d = add2(v, M2);
+    const float2 pp = mul2(d, ch2);
+    const float2 lo = fma2(d, cl2, fma2(d, ch2, make_float2(-pp.x, -pp.y)));
+    const float2 w = mul2(mul2(make_float2(ex2_fast(pp.x), ex2_fast(pp.y)), fma2(lo, ln2, one2)), fs2);
+    if (d.x > -INFINITY) {
+      const unsigned long long fx = __float2ull_rn(w.x);
+      if (fx) mine[mass_bin_p(pp.x) * kSelThreads] += fx;
+    }
+    if (d.y > -INFINITY) {
+      const unsigned long long fx = __float2ull_rn(w.y);
+      if (fx) mine[mass_bin_p(pp.y) * kSelThreads] += fx;
+    }
   });
   mass_totals(sm, false, part.C, parity);
   parity ^= 1;
@@ -341,7 +356,7 @@ __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c
       uint32_t lo = 0u, hi = kM + 1u;
       while (lo < hi) {
         const uint32_t mid = lo + ((hi - lo) >> 1);
-        if (mass_bin(key_value<Raw>(mid) - M, c_hi, c_lo) <= b) hi = mid; else lo = mid + 1u;
+        if (mass_bin(key_value<Raw>(mid) - M, c_hi) <= b) hi = mid; else lo = mid + 1u;
       }
       return lo;
     };
@@ -358,12 +373,21 @@ __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c
   for (int shift = ((nbits + 3) & ~3) - 4; shift >= 0; shift -= 4) {
     __syncthreads();  // the totals of the last pass are read
     clear();
-    const uint32_t hi_mask = shift + 4 >= 32 ? 0u : ~((1u << (shift + 4)) - 1u);
-    for_row<Raw, VEC>(slice, part.len, [&](uint32_t bits) {
-      const uint32_t rel = KY::of(bits) - klo;  // wraps for keys below klo
-      if (rel > span || (rel & hi_mask) != prefix) return;
-      const unsigned long long fx = __float2ull_rn(weight_pair_exp(KY::val(bits) - M, c_hi, c_lo) * fs);
+    // the keys still in play, [klo + prefix, klo + prefix + 2^(shift + 4) - 1]
+    // within [klo, khi], as a value interval (keys at or below -inf's: -inf)
+    const uint32_t kl = klo + prefix;
+    const uint32_t kh = shift + 4 >= 32 || span - prefix < (1u << (shift + 4)) ? khi : kl + ((1u << (shift + 4)) - 1u);
+    const float vl = kl <= KY::of(sizeof(Raw) == 2 ? 0xFF80u : 0xFF800000u) ? -INFINITY : key_value<Raw>(kl);
+    const float vh = key_value<Raw>(kh);
+    auto one = [&](float x) {
+      if (!(x >= vl && x <= vh)) return;
+      const uint32_t rel = KY::of(sizeof(Raw) == 2 ? (__float_as_uint(x) >> 16) : __float_as_uint(x)) - klo;
+      const unsigned long long fx = __float2ull_rn(weight_pair_exp(x - M, c_hi, c_lo) * fs);
       if (fx) mine[((rel >> shift) & 0xFu) * kSelThreads] += fx;
+    };
+    for_row_pairs<Raw, VEC>(slice, part.len, [&](float2 v) {
+      one(v.x);
+      one(v.y);
     });
     mass_totals(sm, true, part.C, parity);
     parity ^= 1;

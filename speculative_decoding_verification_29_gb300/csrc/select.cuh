@@ -103,6 +103,40 @@ __device__ __forceinline__ void for_row(const Raw* row, int V, F f) {
   }
 }
 
+// Calls f(v) with the row's elements as float pairs (16-byte loads when
+// VEC, kRowLoads per thread in flight; without VEC one element per call,
+// paired with -inf).
+template <typename Raw, bool VEC, typename F>
+__device__ __forceinline__ void for_row_pairs(const Raw* row, int V, F f) {
+  if constexpr (VEC) {
+    constexpr int EPV = Elem<Raw>::kPerVec;
+    const int nv = V / EPV;
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kSelThreads * kRowLoads) {
+      uint4 q[kRowLoads];
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int vi = v0 + u * kSelThreads;
+        if (vi < nv) q[u] = __ldcg(reinterpret_cast<const uint4*>(row) + vi);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        if (v0 + u * kSelThreads >= nv) break;
+        if constexpr (EPV == 8) {
+          f(bf16x2_to_float2(q[u].x));
+          f(bf16x2_to_float2(q[u].y));
+          f(bf16x2_to_float2(q[u].z));
+          f(bf16x2_to_float2(q[u].w));
+        } else {
+          f(make_float2(__uint_as_float(q[u].x), __uint_as_float(q[u].y)));
+          f(make_float2(__uint_as_float(q[u].z), __uint_as_float(q[u].w)));
+        }
+      }
+    }
+  } else {
+    for (int v = threadIdx.x; v < V; v += kSelThreads) f(make_float2(Elem<Raw>::at(row, v), -INFINITY));
+  }
+}
+
 // Calls f(index, bits) for every element of the row (16-byte loads when
 // VEC), kRowLoads loads per thread in flight.
 template <typename Raw, bool VEC, typename F>
