@@ -34,7 +34,7 @@ CFLAGS = ["-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast
 
 F64, F32, BF16 = 0, 1, 2
 ST_TOKEN, ST_TARGET, ST_DRAFT, ST_TREE, ST_MASK = 1, 2, 4, 8, 16
-FL_ACCEPT, FL_SAMPLE, FL_ROUTE = 1, 2, 4
+FL_ACCEPT, FL_SAMPLE, FL_ROUTE, FL_WARP = 1, 2, 4, 8
 
 _lock = threading.Lock()
 _lib = None

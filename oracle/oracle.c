@@ -937,13 +937,24 @@ void orc_chain_warped_valid(const void* Lp, const void* Lq, int dt, const int32_
       combos *= nalt[sl];
       if (combos > 4096) break;
     }
-    if (combos > 4096) {
-      valid[b] = 0;
-      continue;
-    }
-    int ok = 0;
+    /* the combinations of the rows' alternatives, all of them when they
+     * number at most 4096; otherwise the rule's own outcome (alternative 0
+     * everywhere) and then every single row moved to each of its
+     * alternatives, up to 4096 tries (a found combination proves the outcome
+     * reachable; rows past the tries are reported invalid) */
+    const int exhaustive = combos <= 4096;
+    int ok = 0, tries = 0, dev_sl = 0, dev_j = 0;
     for (int sl = 0; sl < nslot; ++sl) alt[sl] = 0;
-    for (long long c = 0; c < combos && !ok; ++c) {
+    if (!exhaustive)
+      for (int sl = 0; sl < nslot; ++sl) {
+        int nn = 0;
+        const int k = sl >> 1;
+        const size_t off = (sl & 1) ? ((size_t)b * K + k) * (size_t)V : ((size_t)b * (K + 1) + k) * (size_t)V;
+        warped_row_alt((sl & 1) ? Lq : Lp, dt, off, V, T, top_k, top_p, near_p, 0, wp, tmp, &nn);
+        nalt[sl] = nn ? 2 + nn : 1;
+      }
+    while (!ok && tries < 4096) {
+      ++tries;
       /* decisions at k < m (accept) and m (reject, when m < K) */
       for (int k = 0; k <= m && k < K; ++k) {
         warped_row_alt(Lp, dt, ((size_t)b * (K + 1) + k) * (size_t)V, V, T, top_k, top_p, near_p, alt[2 * k], wp,
@@ -971,10 +982,23 @@ void orc_chain_warped_valid(const void* Lp, const void* Lq, int dt, const int32_
         }
         ok = draw_reachable(wq, V, ur[b], out[m], win);
       }
-      /* next combination (mixed radix over the slots) */
-      for (int sl = 0; sl < nslot; ++sl) {
-        if (++alt[sl] < nalt[sl]) break;
-        alt[sl] = 0;
+      if (exhaustive) {
+        /* next combination (mixed radix over the slots) */
+        int sl = 0;
+        for (; sl < nslot; ++sl) {
+          if (++alt[sl] < nalt[sl]) break;
+          alt[sl] = 0;
+        }
+        if (sl == nslot) break; /* all tried */
+      } else {
+        /* next single-row deviation */
+        alt[dev_sl] = 0;
+        while (dev_sl < nslot && ++dev_j >= nalt[dev_sl]) {
+          ++dev_sl;
+          dev_j = 0;
+        }
+        if (dev_sl == nslot) break;
+        alt[dev_sl] = dev_j;
       }
     }
     valid[b] = ok;

@@ -899,6 +899,33 @@ def pin_chain_warped_valid(lib, V=5, K=1, T=1.0, top_k=4, top_p=0.6, near_p=0.25
                 assert got == want, (x, m, t, want)
 
 
+def pin_chain_warped_valid_crowded(lib, V=2000, T=1.0, seed=23):
+    """The warped validity check past its combination cap. Every row holds
+    one dominant token and V - 1 tokens about e^-21 below it, with distinct
+    values, and top-p = 1 - 5e-7 puts the cut among the small ones: each row
+    then has hundreds of value groups within the near window, far more
+    combinations than the check enumerates. The rule's own outcome must
+    still be found valid, and a bonus token that no near cut keeps (the
+    row's smallest) invalid."""
+    rng = np.random.default_rng(seed)
+    K = 1
+    Lp = -21.0 + 0.1 * rng.standard_normal((1, K + 1, V))
+    Lq = -21.0 + 0.1 * rng.standard_normal((1, K, V))
+    Lp[..., 7] = 0.0
+    Lq[..., 7] = 0.0
+    x = np.array([[7]], np.int32)
+    ua, ur = np.array([[0.1]]), np.array([0.5])
+    top_p = 1.0 - 5e-7
+    o = oracle.verify_chain_warped(Lp, Lq, x, ua, ur, T, 0, top_p, lib=lib)
+    assert int(o["accept_len"][0]) == K and int(o["out_tokens"][0, K]) == 7, o
+    assert o["flags"][0] & oracle.FL_WARP, o["flags"]  # the cut is a near tie
+    assert oracle.chain_warped_valid(Lp, Lq, x, ua, ur, T, 0, top_p, o["accept_len"], o["out_tokens"], lib=lib)[0]
+    low = int(np.argmin(Lp[0, K]))
+    bad = o["out_tokens"].copy()
+    bad[0, K] = low
+    assert not oracle.chain_warped_valid(Lp, Lq, x, ua, ur, T, 0, top_p, o["accept_len"], bad, lib=lib)[0]
+
+
 def pin_flag_probability(lib, V=6, T=1.0, win=0.02, seed=19, n=20000):
     """pflag, the oracle's probability of a flag over the row's uniforms,
     against counting: with the accept uniform fixed (so the first rejection
@@ -953,5 +980,6 @@ ALL_PINS = [
     ("lossless_warped_both", lambda lib: pin_lossless_warped(lib, 4, 2, 1.2, 3, 0.8, 9)),
     ("chain_valid", pin_chain_valid),
     ("chain_warped_valid", pin_chain_warped_valid),
+    ("chain_warped_valid_crowded", pin_chain_warped_valid_crowded),
     ("flag_probability", pin_flag_probability),
 ]

@@ -143,6 +143,50 @@ def test_warped_topp_alone_row_splits(B, K, V, dtype):
     compare(*run(c, V, 0.6), name=f"warped_topp_split_{B}_{V}_kV")  # a top-k of V keeps every token
 
 
+def _topp_case(kind, dtype, seed):
+    """Rows that stress the top-p select's key interval and value filters."""
+    g0 = torch.Generator().manual_seed(seed)
+    B, K, V = 4, 3, 30000
+    T, p = 1.0, 0.9
+    base = torch.randn(B, K + 1, V, generator=g0)
+    if kind == "near_zero":  # magnitudes ~1e-3: the bin spans zero, where keys are densest
+        base = 1e-3 * base
+    elif kind == "masked":  # half the vocabulary at -inf
+        base = base + 8.0 * (torch.rand(B, K + 1, V, generator=g0) < 1e-3)
+        base[torch.rand(B, K + 1, V, generator=g0) < 0.5] = -float("inf")
+        T = 0.8
+    elif kind == "cold":  # T = 0.05: all but a few weights vanish in fixed point
+        base, T = 3.0 * base, 0.05
+    elif kind == "hot":  # T = 8: nearly flat
+        T = 8.0
+    elif kind == "two_groups":  # one big tied group at the cut, the rest ~e^-30 below
+        base = torch.where(torch.rand(B, K + 1, V, generator=g0) < 0.5, torch.zeros(()), torch.full((), -30.0))
+        base[..., :5] = 2.0
+        p = 0.6
+    elif kind == "last_bin":  # one dominant token; the cut lands among weights below 2^-30
+        base = torch.full((B, K + 1, V), -21.0) + 0.1 * base
+        base[..., 7] = 0.0
+        p = 0.99999
+    Lp = base.to(dtype)
+    Lq = (base + 0.3 * torch.randn(B, K + 1, V, generator=g0))[:, :K].to(dtype)
+    Lq[torch.isinf(base[:, :K])] = -float("inf")
+    x = gen.workloads._gumbel_draw(Lq.float(), T, g0)
+    ua = torch.rand(B, K, generator=g0)
+    ur = torch.rand(B, generator=g0)
+    return gen.ChainBatch(f"topp_{kind}", Lp, Lq, x, ua, ur, T), p
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("kind", ["near_zero", "masked", "cold", "hot", "two_groups", "last_bin"])
+def test_warped_topp_alone_adversarial(kind, dtype):
+    """Top-p alone on rows built against the select's shortcuts: logits near
+    zero, half the vocabulary masked, very cold and very hot temperatures, a
+    huge tied group at the cut, and a cut among weights below 2^-30 (the last
+    log-weight bin): the same cuts as the oracle."""
+    c, p = _topp_case(kind, dtype, seed=len(kind) + (dtype == torch.float32))
+    compare(*run(c, 0, p), name=f"warped_topp_{kind}")
+
+
 def test_warped_large_nucleus_integer_ties():
     """Integer logits over 20000 tokens: huge groups of equal values at the
     top-p cut are kept or dropped whole (the radix digits isolate one key)."""

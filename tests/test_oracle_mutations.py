@@ -76,6 +76,9 @@ MUTATIONS = {
     "valid_prefix_unchecked": ("    if (out[k] != x[k]) return 0;", "    if (0) return 0;"),
     "valid_warped_no_alternative_cuts": ("nalt[sl] = nn ? 2 + nn : 1;", "nalt[sl] = 1;"),
     "valid_warped_keep_all_cut_missing": ("if (alt == 1) cut = target + band;", "if (alt == 1) cut = target;"),
+    "valid_warped_gives_up_past_cap": ("    const int exhaustive = combos <= 4096;",
+                                       "    if (combos > 4096) {\n      valid[b] = 0;\n      continue;\n    }\n"
+                                       "    const int exhaustive = 1;"),
     "pflag_window_halved": ("pf += fmin(w / S, 2.0 * near);", "pf += fmin(w / S, near);"),
     "expand_ties_to_higher_node": ("if (x->f != y->f) return x->f < y->f ? -1 : 1;",
                                    "if (x->f != y->f) return x->f > y->f ? -1 : 1;"),
