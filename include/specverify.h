@@ -225,12 +225,13 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logit
  * 2 (bf16) or 4 (fp32) radix passes; then, when the tokens top-k keeps
  * (all V for top-p alone) number at most 4096, one collecting them; when
  * they number more, for top-p a mass-weighted radix select: one pass
- * binning the weights by log-weight, then one pass per 4 bits of the keys
- * that differ inside the chosen bin (at most 4 for bf16, 8 for fp32;
- * weights summed in 64-bit fixed point, so the cut does not depend on
- * summation order; top-p alone splits each row over a cluster of up to 8
- * CTAs when the rows alone leave SMs idle), or for top-k alone one pass
- * summing the kept mass. Every nucleus size is resolved. */
+ * binning the weights by log-weight, then passes splitting the chosen bin
+ * 16 ways (by value while its ends are finite, else by key digits) until
+ * one key is left, typically 2 or 3 (weights summed in 64-bit fixed point,
+ * so the cut does not depend on summation order; top-p alone splits each
+ * row over a cluster of up to 8 CTAs when the rows alone leave SMs idle or
+ * their slices would not stay in L2), or for top-k alone one pass summing
+ * the kept mass. Every nucleus size is resolved. */
 size_t spec_warped_workspace_bytes(int B, int K, int V, int dtype);
 int spec_verify_chain_warped(const void* target_logits, const void* draft_logits, int dtype,
                              const int32_t* draft_tokens, const float* u_accept, const float* u_resample,

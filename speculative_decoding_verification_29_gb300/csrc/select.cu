@@ -32,6 +32,8 @@
 //   the kept mass Z' is the scan's total at tau, or (top-k alone) a pass
 //   summing the kept weights in float pairs.
 // Output per row: (M, Z', log2 Z') as a StatRec and tau.
+#include <algorithm>
+
 #include "select.cuh"
 
 namespace specv {
@@ -210,11 +212,27 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
 // last bin, in descending value order, that has mass and whose preceding
 // mass is below the target.
 
-// Log-weight bin from p = (l - M) c_hi, the leading part of the weight's
-// exponent: floor(-p / 2) for p in (-30, 0], 15 below (and for -inf); p is
-// a rounded product of l - M and a positive constant, so the bin does not
-// increase with l.
-__device__ __forceinline__ int mass_bin_p(float p) { return p > -30.f ? static_cast<int>(-0.5f * p) : 15; }
+// round(wf) for 0 <= wf < 2^48, as __float2ull_rn rounds it, with one
+// 32-bit conversion: the float-to-64-bit conversion issues at about 2 per
+// clock and SM on this part, the 32-bit one at about 15. wf = hi 2^26 + rem
+// with hi = round(wf 2^-26) < 2^22, taken by a rounding add (no conversion),
+// and rem = wf - hi 2^26 in [-2^25, 2^25], exact in fp32 (wf's ulp divides
+// it) and holding wf's fraction: round(wf) = hi 2^26 + round(rem).
+__device__ __forceinline__ unsigned long long fx_round(float wf) {
+  const float y = fmaf(wf, 0x1p-26f, 12582912.0f);  // 1.5 2^23 + round(wf 2^-26)
+  const unsigned hi = __float_as_uint(y) - 0x4B400000u;
+  const float rem = fmaf(-(y - 12582912.0f), 0x1p26f, wf);
+  return static_cast<unsigned long long>((static_cast<long long>(hi) << 26) + __float2int_rn(rem));
+}
+
+// Log-weight bin from p = (l - M) c_hi <= 0, the leading part of the
+// weight's exponent: round(-p / 2) up to 15 (15 for -inf), read off a
+// rounding add (the bits of positive floats grow with their value), without
+// a conversion; p is a rounded product of l - M and a positive constant, so
+// the bin does not increase with l.
+__device__ __forceinline__ int mass_bin_p(float p) {
+  return static_cast<int>(min(15u, __float_as_uint(fmaf(p, -0.5f, 12582912.0f)) - 0x4B400000u));
+}
 __device__ __forceinline__ int mass_bin(float d, float c_hi) { return mass_bin_p(d * c_hi); }
 
 constexpr int kMassBins = 16;
@@ -287,6 +305,27 @@ __device__ __forceinline__ void last_below(const unsigned long long* tot, unsign
   }
 }
 
+// The smallest key in [lo, hi) for which pred holds (hi if none; pred does
+// not go from true back to false as the key grows), by one full warp in
+// rounds of 32-way search: each lane tests the last key of one of 32 equal
+// chunks, and the first chunk whose last key holds it holds the answer.
+template <typename Pred>
+__device__ __forceinline__ uint32_t warp_first(uint32_t lo, uint32_t hi, Pred pred, int lane) {
+  while (lo < hi) {
+    const unsigned long long len = hi - lo, step = (len + 31u) / 32u;
+    const unsigned long long t = lo + (static_cast<unsigned long long>(lane) + 1u) * step - 1u;
+    const bool holds = t >= hi || pred(static_cast<uint32_t>(t));
+    const unsigned bal = __ballot_sync(0xffffffffu, holds);
+    if (bal == 0u) return hi;  // no key of [lo, hi) holds it (lane 31 tested hi - 1)
+    const int i = __ffs(bal) - 1;
+    const unsigned long long ti = lo + (static_cast<unsigned long long>(i) + 1u) * step - 1u;
+    lo = static_cast<uint32_t>(lo + static_cast<unsigned long long>(i) * step);
+    if (ti < hi) hi = static_cast<uint32_t>(ti);
+    if (step == 1u) return hi;  // chunk i is the key itself
+  }
+  return hi;
+}
+
 // The top-p cut of one row over the tokens with key >= tau_k (0: all): the
 // key of the last kept group, and (*kept) the kept mass relative to the row
 // maximum as a float pair. Called by every thread of the CTA, or of each CTA
@@ -298,9 +337,14 @@ __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c
                              const MassSmem& sm, float2* kept, RowPart part) {
   using KY = Key<Raw>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int s = 62 - (32 - __clz(V));                // V terms of at most 2^s stay below 2^62
+  // V terms of at most 2^s stay below 2^62; at most 2^47, the range of
+  // fx_round (terms below 2^-47 of the row maximum add under 2^-35 in all)
+  const int s = min(62 - (32 - __clz(V)), 47);
   const float fs = __int_as_float((127 + s) << 23);  // 2^s
-  unsigned long long* mine = sm.th + tid;            // this thread's bin b at mine[b * kSelThreads]
+  // this thread's bin b at mine[b * kSelThreads]; added to by shared-memory
+  // atomics whose result is unused: the bins are private (no contention), and
+  // the thread does not wait for a read of the bin before its next element
+  unsigned long long* mine = sm.th + tid;
   auto clear = [&]() {
 #pragma unroll
     for (int b = 0; b < kMassBins; ++b) mine[b * kSelThreads] = 0ull;
@@ -314,20 +358,23 @@ __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c
   const float2 ln2 = make_float2(0.693147180559945309f, 0.693147180559945309f), one2 = make_float2(1.f, 1.f);
   const float2 fs2 = make_float2(fs, fs);
   clear();
+  const bool has_tau = tau_k != 0u;
   for_row_pairs<Raw, VEC>(slice, part.len, [&](float2 v) {
-    if (v.x < vtau) v.x = -INFINITY;
-    if (v.y < vtau) v.y = -INFINITY;
+    if (has_tau) {
+      if (v.x < vtau) v.x = -INFINITY;
+      if (v.y < vtau) v.y = -INFINITY;
+    }
     const float2 d = add2(v, M2);
     const float2 pp = mul2(d, ch2);
     const float2 lo = fma2(d, cl2, fma2(d, ch2, make_float2(-pp.x, -pp.y)));
     const float2 w = mul2(mul2(make_float2(ex2_fast(pp.x), ex2_fast(pp.y)), fma2(lo, ln2, one2)), fs2);
     if (d.x > -INFINITY) {
-      const unsigned long long fx = __float2ull_rn(w.x);
-      if (fx) mine[mass_bin_p(pp.x) * kSelThreads] += fx;
+      const unsigned long long fx = fx_round(w.x);
+      if (fx) atomicAdd(&mine[mass_bin_p(pp.x) * kSelThreads], fx);
     }
     if (d.y > -INFINITY) {
-      const unsigned long long fx = __float2ull_rn(w.y);
-      if (fx) mine[mass_bin_p(pp.y) * kSelThreads] += fx;
+      const unsigned long long fx = fx_round(w.y);
+      if (fx) atomicAdd(&mine[mass_bin_p(pp.y) * kSelThreads], fx);
     }
   });
   mass_totals(sm, false, part.C, parity);
@@ -345,59 +392,110 @@ __device__ uint32_t topp_cut(const Raw* row, int V, float M, float c_hi, float c
   const double target = s_target;
   const int bin = static_cast<int>(static_cast<long long>(sm.sel[0]));
   unsigned long long A = sm.sel[1], mg = sm.sel[2];
-  // the bin is a contiguous key interval [klo, khi] (the bin does not
-  // increase with the key): its ends by binary search over the keys up to
-  // the row maximum's (the keys of NaN bit patterns, all below -inf's, fall
-  // in the last bin like -inf)
+  // the bin is a contiguous key interval (the bin does not increase with
+  // the key): its ends by search over the keys up to the row maximum's (the
+  // keys of NaN bit patterns, all below -inf's, fall in the last bin like
+  // -inf)
   __shared__ uint32_t s_kr[2];
-  if (tid == 0) {
+  __shared__ float s_queue[kSelWarps][64];  // per warp: the elements in play not yet weighed
+  const uint32_t kNegInf = KY::of(sizeof(Raw) == 2 ? 0xFF80u : 0xFF800000u);  // -inf's key
+  if (warp == 0) {
     const uint32_t kM = KY::of(sizeof(Raw) == 2 ? (__float_as_uint(M) >> 16) : __float_as_uint(M));
-    auto first_at_most = [&](int b) {  // the smallest key <= kM whose bin is <= b (kM + 1: none)
-      uint32_t lo = 0u, hi = kM + 1u;
-      while (lo < hi) {
-        const uint32_t mid = lo + ((hi - lo) >> 1);
-        if (mass_bin(key_value<Raw>(mid) - M, c_hi) <= b) hi = mid; else lo = mid + 1u;
-      }
-      return lo;
-    };
-    s_kr[0] = max(first_at_most(bin), tau_k);
-    s_kr[1] = first_at_most(bin - 1) - 1u;
+    auto bin_of = [&](uint32_t k) { return mass_bin(key_value<Raw>(k) - M, c_hi); };
+    const uint32_t k0 = warp_first(0u, kM + 1u, [&](uint32_t k) { return bin_of(k) <= bin; }, lane);
+    const uint32_t k1 = warp_first(0u, kM + 1u, [&](uint32_t k) { return bin_of(k) <= bin - 1; }, lane) - 1u;
+    if (lane == 0) {
+      s_kr[0] = max(k0, tau_k);
+      s_kr[1] = k1;
+    }
   }
   __syncthreads();
-  const uint32_t klo = s_kr[0], khi = s_kr[1];
-  // the next passes: 4-bit digits of key - klo over the bits where the
-  // interval's keys differ, from the top
-  const uint32_t span = khi - klo;
-  const int nbits = span == 0u ? 0 : 32 - __clz(span);
-  uint32_t prefix = 0;  // of key - klo
-  for (int shift = ((nbits + 3) & ~3) - 4; shift >= 0; shift -= 4) {
+  uint32_t kl = s_kr[0], kh = s_kr[1];
+  // the next passes split the keys in play, [kl, kh], 16 ways and keep the
+  // part holding the cut, until one key is left: 16 equal value intervals
+  // of [value(kl), value(kh)] while both ends are finite (each pass leaves
+  // about 1/16 of the elements in play, where key digits would leave most
+  // elements of a range dense in keys, as near zero), else (the last bin,
+  // or after 6 such passes) 4-bit digits of key - kl from the highest one
+  // the span needs; the part's ends by search (the part index does not
+  // decrease with the key)
+  for (int pass = 0; kl < kh; ++pass) {
     __syncthreads();  // the totals of the last pass are read
     clear();
-    // the keys still in play, [klo + prefix, klo + prefix + 2^(shift + 4) - 1]
-    // within [klo, khi], as a value interval (keys at or below -inf's: -inf)
-    const uint32_t kl = klo + prefix;
-    const uint32_t kh = shift + 4 >= 32 || span - prefix < (1u << (shift + 4)) ? khi : kl + ((1u << (shift + 4)) - 1u);
-    const float vl = kl <= KY::of(sizeof(Raw) == 2 ? 0xFF80u : 0xFF800000u) ? -INFINITY : key_value<Raw>(kl);
-    const float vh = key_value<Raw>(kh);
-    auto one = [&](float x) {
-      if (!(x >= vl && x <= vh)) return;
-      const uint32_t rel = KY::of(sizeof(Raw) == 2 ? (__float_as_uint(x) >> 16) : __float_as_uint(x)) - klo;
-      const unsigned long long fx = __float2ull_rn(weight_pair_exp(x - M, c_hi, c_lo) * fs);
-      if (fx) mine[((rel >> shift) & 0xFu) * kSelThreads] += fx;
+    const uint32_t span = kh - kl;
+    const float vl = kl <= kNegInf ? -INFINITY : key_value<Raw>(kl), vh = key_value<Raw>(kh);
+    const bool linear = span >= 16u && vl > -INFINITY && pass < 6;
+    const float inv = linear ? 16.f / (vh - vl) : 0.f;
+    const int shift = linear ? 0 : max(0, ((32 - __clz(span) + 3) & ~3) - 4);
+    auto part_of_value = [&](float x) { return min(15, static_cast<int>((x - vl) * inv)); };
+    auto part_of_key = [&](uint32_t k) {
+      return linear ? part_of_value(key_value<Raw>(k)) : static_cast<int>(((k - kl) >> shift) & 0xFu);
     };
-    for_row_pairs<Raw, VEC>(slice, part.len, [&](float2 v) {
-      one(v.x);
-      one(v.y);
-    });
+    auto part_of = [&](float x) {
+      return linear ? part_of_value(x)
+                    : part_of_key(KY::of(sizeof(Raw) == 2 ? (__float_as_uint(x) >> 16) : __float_as_uint(x)));
+    };
+    // the elements in play weighed where they fall or, in the first of
+    // these passes (the whole bin in play: most warp steps hold some), first
+    // compacted per warp through a queue in shared memory and weighed 32 at
+    // a time, so that lanes do not idle through the weighing; later passes
+    // hold few, and a queue would cost every element more than it saves
+    auto weigh = [&](float x) {
+      const float d = x - M;
+      if (!(d > -INFINITY)) return;
+      const float pp = d * c_hi;
+      const float lo = fmaf(d, c_lo, fmaf(d, c_hi, -pp));
+      const unsigned long long fx = fx_round(ex2_fast(pp) * fmaf(lo, 0.693147180559945309f, 1.f) * fs);
+      if (fx) atomicAdd(&mine[part_of(x) * kSelThreads], fx);
+    };
+    float* q = s_queue[warp];
+    int qn = 0;  // the same in every lane
+    auto push = [&](float x) {
+      const bool in = x >= vl && x <= vh;
+      const unsigned m = __ballot_sync(0xffffffffu, in);
+      if (in) q[qn + __popc(m & ((1u << lane) - 1u))] = x;
+      qn += __popc(m);
+      __syncwarp();
+      if (qn >= 32) {
+        weigh(q[lane]);
+        __syncwarp();
+        if (lane < qn - 32) q[lane] = q[32 + lane];
+        qn -= 32;
+        __syncwarp();
+      }
+    };
+    if (pass == 0) {
+      for_row_pairs<Raw, VEC>(slice, part.len, [&](float2 v) {
+        push(v.x);
+        push(v.y);
+      });
+      if (lane < qn) weigh(q[lane]);
+    } else {
+      for_row_pairs<Raw, VEC>(slice, part.len, [&](float2 v) {
+        if (v.x >= vl && v.x <= vh) weigh(v.x);
+        if (v.y >= vl && v.y <= vh) weigh(v.y);
+      });
+    }
     mass_totals(sm, true, part.C, parity);
     parity ^= 1;
     if (warp == 0) last_below(sm.tot, A, target, sm.sel, lane);
     __syncthreads();
-    prefix |= (static_cast<uint32_t>(kMassBins - 1) - static_cast<uint32_t>(sm.sel[0])) << shift;
+    const int jsel = kMassBins - 1 - static_cast<int>(sm.sel[0]);
     A = sm.sel[1];
     mg = sm.sel[2];
+    if (warp == 0) {
+      const uint32_t a = warp_first(kl, kh + 1u, [&](uint32_t k) { return part_of_key(k) >= jsel; }, lane);
+      const uint32_t e = warp_first(kl, kh + 1u, [&](uint32_t k) { return part_of_key(k) > jsel; }, lane) - 1u;
+      if (lane == 0) {
+        s_kr[0] = a;
+        s_kr[1] = e;
+      }
+    }
+    __syncthreads();
+    kl = s_kr[0];
+    kh = s_kr[1];
   }
-  const uint32_t cut = klo + prefix;
+  const uint32_t cut = kl;
   const double z = __ull2double_rn(A + mg) * __longlong_as_double(static_cast<long long>(1023 - s) << 52);
   const float hi = static_cast<float>(z);
   *kept = make_float2(hi, static_cast<float>(z - static_cast<double>(hi)));
@@ -697,13 +795,17 @@ cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream
   if (!(a.top_k > 0 && a.top_k < a.V) && a.top_p < 1.f && a.V > kCand) {
     // top-p alone over rows longer than the candidate buffer: rows split over
     // clusters of up to 8 CTAs while the rows alone leave SMs idle (four
-    // CTAs fit an SM)
-    int dev = 0, sms = 0;
+    // CTAs fit an SM), or while the slices of the CTAs resident at once
+    // would not fit in three quarters of L2 (the passes after the first then
+    // read their slice from L2 instead of HBM)
+    int dev = 0, sms = 0, l2 = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
     if (e != cudaSuccess) return e;
+    const long long slots = 4LL * sms, row_bytes = static_cast<long long>(a.V) * (dtype == SPEC_BF16 ? 2 : 4);
     int C = 1;
-    while (C < 8 && rows * C * 2 <= 4LL * sms) C *= 2;
+    while (C < 8 && (rows * C * 2 <= slots || std::min(rows * C, slots) * (row_bytes / C) > 3LL * l2 / 4)) C *= 2;
     const dim3 grid(static_cast<unsigned>(rows * C)), block(kSelThreads);
     if (dtype == SPEC_BF16)
       return vec ? launch_pdl(topp_rows_kernel<uint16_t, true>, grid, block, st, a, C)

@@ -105,22 +105,25 @@ __device__ __forceinline__ void for_row(const Raw* row, int V, F f) {
 
 // Calls f(v) with the row's elements as float pairs (16-byte loads when
 // VEC, kRowLoads per thread in flight; without VEC one element per call,
-// paired with -inf).
+// paired with -inf). Every lane of a warp makes the same number of calls
+// (pairs past the row are -inf), so f may use warp-wide operations.
 template <typename Raw, bool VEC, typename F>
 __device__ __forceinline__ void for_row_pairs(const Raw* row, int V, F f) {
+  const int lane = threadIdx.x & 31;
   if constexpr (VEC) {
     constexpr int EPV = Elem<Raw>::kPerVec;
     const int nv = V / EPV;
-    for (int v0 = threadIdx.x; v0 < nv; v0 += kSelThreads * kRowLoads) {
+    const uint4 neg = make_uint4(Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf, Vec<Raw>::kNegInf);
+    for (int w0 = threadIdx.x - lane; w0 < nv; w0 += kSelThreads * kRowLoads) {
       uint4 q[kRowLoads];
 #pragma unroll
       for (int u = 0; u < kRowLoads; ++u) {
-        const int vi = v0 + u * kSelThreads;
-        if (vi < nv) q[u] = __ldcg(reinterpret_cast<const uint4*>(row) + vi);
+        const int vi = w0 + lane + u * kSelThreads;
+        q[u] = vi < nv ? __ldcg(reinterpret_cast<const uint4*>(row) + vi) : neg;
       }
 #pragma unroll
       for (int u = 0; u < kRowLoads; ++u) {
-        if (v0 + u * kSelThreads >= nv) break;
+        if (w0 + u * kSelThreads >= nv) break;  // the same for the whole warp
         if constexpr (EPV == 8) {
           f(bf16x2_to_float2(q[u].x));
           f(bf16x2_to_float2(q[u].y));
@@ -133,7 +136,10 @@ __device__ __forceinline__ void for_row_pairs(const Raw* row, int V, F f) {
       }
     }
   } else {
-    for (int v = threadIdx.x; v < V; v += kSelThreads) f(make_float2(Elem<Raw>::at(row, v), -INFINITY));
+    for (int w0 = threadIdx.x - lane; w0 < V; w0 += kSelThreads) {
+      const int v = w0 + lane;
+      f(make_float2(v < V ? Elem<Raw>::at(row, v) : -INFINITY, -INFINITY));
+    }
   }
 }
 
