@@ -143,6 +143,26 @@ def test_warped_topp_alone_row_splits(B, K, V, dtype):
     compare(*run(c, V, 0.6), name=f"warped_topp_split_{B}_{V}_kV")  # a top-k of V keeps every token
 
 
+def test_warped_topp_alone_serving_batch_sampled_rows():
+    """Top-p alone on the serving batch (B=64, K=8, V=128256 bf16, T=0.7,
+    top-p 0.95): 1088 rows whose slices would not stay in L2 one per CTA, so
+    each row is split over a cluster of 2. The whole batch runs on the GPU;
+    eight batch rows (rows are independent) are compared with the oracle."""
+    import speculative_decoding_verification_29_gb300 as sv
+
+    c = gen.chain_zipf(64, 8, 128256, torch.bfloat16, 0.7, gen.workloads._sigma_spread, 5, name="chain_batched")
+    dev = torch.device("cuda")
+    g = sv.spec_verify_chain_warped(c.Lp.to(dev), c.Lq.to(dev), c.x.to(dev), c.ua.to(dev), c.ur.to(dev), c.T,
+                                    top_k=0, top_p=0.95)
+    torch.cuda.synchronize()
+    g = {k: np_(v) for k, v in g.items()}
+    rows = torch.tensor([0, 9, 18, 27, 36, 45, 54, 63])
+    sub = gen.ChainBatch("topp_serving_rows", c.Lp[rows], c.Lq[rows], c.x[rows], c.ua[rows], c.ur[rows], c.T)
+    o = oracle.verify_chain_warped(sub.Lp, sub.Lq, sub.x, sub.ua, sub.ur, sub.T, 0, 0.95, threads=THREADS)
+    gs = {k: v[rows.numpy()] for k, v in g.items()}
+    compare(gs, o, sub, 0, 0.95, name="warped_topp_serving_rows")
+
+
 def _topp_case(kind, dtype, seed):
     """Rows that stress the top-p select's key interval and value filters."""
     g0 = torch.Generator().manual_seed(seed)
