@@ -97,9 +97,11 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
   const float2 Zk = warp_sum_ds(zk);
   uint32_t tau = K;
   int st = 0;
+  float2 Zp = Zk;  // top-k alone: the kept set is the top-k set
   if (a.top_p < 1.f) {
     const float2 target = ds_mul_f(Zk, a.top_p);
     float2 run = make_float2(0.f, 0.f);  // mass of the registers before
+    float2 pre[NR];                      // mass of the entries up to and including each
     int last = -1;
 #pragma unroll
     for (int i = 0; i < NR; ++i) {
@@ -112,6 +114,7 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
       float2 ex = make_float2(__shfl_up_sync(0xffffffffu, inc.x, 1), __shfl_up_sync(0xffffffffu, inc.y, 1));
       if (lane == 0) ex = make_float2(0.f, 0.f);
       if (ink[i] && ds_gt(target, ds_add(run, ex))) last = 32 * i + lane;
+      pre[i] = ds_add(run, inc);
       run = ds_add(run, make_float2(__shfl_sync(0xffffffffu, inc.x, 31), __shfl_sync(0xffffffffu, inc.y, 31)));
     }
     const int L = __reduce_max_sync(0xffffffffu, last);
@@ -120,13 +123,20 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
     } else {
       const uint32_t kl = comp_key(warp_entry<NR>(r, L));
       if (kl > tau) tau = kl;
+      // the kept entries (keys >= tau) are a prefix of the sorted list: its
+      // mass is the prefix sum at its last entry
+      int E = 0;
+#pragma unroll
+      for (int i = 0; i < NR; ++i)
+        E += __popc(__ballot_sync(0xffffffffu, 32 * i + lane < n && comp_key(r[i]) >= tau));
+      const int e = E - 1;  // E >= 1: entry L is kept
+      float2 v = pre[0];
+#pragma unroll
+      for (int i = 1; i < NR; ++i)
+        if ((e >> 5) == i) v = pre[i];
+      Zp = make_float2(__shfl_sync(0xffffffffu, v.x, e & 31), __shfl_sync(0xffffffffu, v.y, e & 31));
     }
   }
-  float2 kept = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int i = 0; i < NR; ++i)
-    if (ink[i] && comp_key(r[i]) >= tau) kept = ds_add(kept, make_float2(w[i], 0.f));
-  const float2 Zp = warp_sum_ds(kept);
   if (lane == 0) {
     StatRec out;
     out.M = M;
