@@ -320,43 +320,23 @@ __device__ uint32_t kth_largest(const Raw* row, int V, int k, unsigned* hist, un
 // Largest t (to 16 bits of the order-preserving key) with at least k of the
 // P segment maxima >= t: a lower bound of the row's k-th largest value; -inf
 // when k > P or P > 32 NV. sm[i] holds maximum lane + 32 i (i < NV). One
-// full warp; every lane gets it. Four rounds of 4 bits from the top: a round
-// counts the keys at or above each of the 15 nonzero digits at once (the
-// counts do not depend on one another) and keeps the largest digit with k;
-// the entries past P, NU = ceil(P / 32) <= NV, are never read.
-template <int NV, int NU>
-__device__ __forceinline__ float kth_bound(const float (&sm)[NV], int P, int k) {
-  const int lane = threadIdx.x & 31;
-  uint32_t key[NU];
-#pragma unroll
-  for (int i = 0; i < NU; ++i) key[i] = lane + 32 * i < P ? Key<float>::of(__float_as_uint(sm[i])) : 0u;
-  uint32_t prefix = 0;
-#pragma unroll 1
-  for (int shift = 28; shift >= 16; shift -= 4) {
-    uint32_t best = 0;
-#pragma unroll
-    for (uint32_t d = 1; d < 16; ++d) {
-      const uint32_t cand = prefix | (d << shift);
-      unsigned cnt = 0;
-#pragma unroll
-      for (int i = 0; i < NU; ++i) cnt += key[i] >= cand ? 1u : 0u;
-      if (__reduce_add_sync(0xffffffffu, cnt) >= static_cast<unsigned>(k)) best = d;  // counts fall with d
-    }
-    prefix |= best << shift;
-  }
-  return key_value<float>(prefix);
-}
+// full warp; every lane gets it.
 template <int NV>
 __device__ __forceinline__ float seg_bound_regs(const float (&sm)[NV], int P, int k, int lane) {
-  (void)lane;
   if (k > P || P > 32 * NV) return -INFINITY;
-  if constexpr (NV > 2) {
-    if (P <= 64) return kth_bound<NV, 2>(sm, P, k);
+  uint32_t key[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) key[i] = lane + 32 * i < P ? Key<float>::of(__float_as_uint(sm[i])) : 0u;
+  uint32_t prefix = 0;
+#pragma unroll 1
+  for (int bit = 31; bit >= 16; --bit) {
+    const uint32_t cand = prefix | (1u << bit);
+    unsigned cnt = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) cnt += key[i] >= cand ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, cnt) >= static_cast<unsigned>(k)) prefix = cand;
   }
-  if constexpr (NV > 4) {
-    if (P <= 128) return kth_bound<NV, 4>(sm, P, k);
-  }
-  return kth_bound<NV, NV>(sm, P, k);
+  return key_value<float>(prefix);
 }
 
 // The same from the stats partials pr[c] = (segment maximum, sum).
