@@ -231,7 +231,11 @@ int spec_verify_chain_noalloc(const void* target_logits, const void* draft_logit
  * so the cut does not depend on summation order; top-p alone splits each
  * row over a cluster of up to 8 CTAs when the rows alone leave SMs idle or
  * their slices would not stay in L2), or for top-k alone one pass summing
- * the kept mass. Every nucleus size is resolved. */
+ * the kept mass. Top-p alone over rows longer than 4096 first takes the
+ * warp path with the row's 48 largest elements (and their ties, from the
+ * lane records) and cuts there when their mass reaches top_p Z; only the
+ * rows whose nucleus reaches past them take the radix select. Every
+ * nucleus size is resolved. */
 size_t spec_warped_workspace_bytes(int B, int K, int V, int dtype);
 int spec_verify_chain_warped(const void* target_logits, const void* draft_logits, int dtype,
                              const int32_t* draft_tokens, const float* u_accept, const float* u_resample,

@@ -156,11 +156,20 @@ struct ChainCall {
   float top_p = 1.f;
 };
 
+// Top-p alone over rows longer than the candidate buffer: the candidates the
+// warp path gathers first (at most kToppProbe, one per stats segment); 0 when
+// the call has a top-k or the rows fit the buffer.
+int topp_probe(const ChainCall& c, int P) {
+  if (c.top_k > 0 || !(c.top_p < 1.f) || c.V <= select_candidates()) return 0;
+  return std::min(kToppProbe, P);
+}
+
 // The lane records of the stats pass, when the warped call's workspace holds
-// them and they serve its top-k; NULL otherwise.
+// them and they serve its top-k (or the top-p probe); NULL otherwise.
 float* chain_lanes(const ChainCall& c, int P) {
   const Layout Lx = layout(c.B, c.K + 1, c.K, c.V, c.dtype, true);
-  if (!lanes_fit(c.top_k, P) || c.ws_bytes < Lx.total) return nullptr;
+  const int k = c.top_k > 0 ? c.top_k : topp_probe(c, P);
+  if (!lanes_fit(k, P) || k >= c.V || c.ws_bytes < Lx.total) return nullptr;
   return reinterpret_cast<float*>(at(c.ws, Lx.lanes));
 }
 
@@ -247,6 +256,7 @@ int chain_sample(const ChainCall& c) {
     s.vtau = reinterpret_cast<float*>(at(c.ws, L.vtau));
     s.row_flag = reinterpret_cast<int32_t*>(at(c.ws, L.flag));
     s.lanes = chain_lanes(c, t.P);
+    s.probe_k = s.lanes ? topp_probe(c, t.P) : 0;
     if (launch_warp_select(s, c.dtype, vec, c.st) != cudaSuccess) return SPEC_ERR_CUDA;
     t.rec = s.rec;
     t.vtau = s.vtau;

@@ -159,9 +159,17 @@ struct SelArgs {
   const float2* part;  // stats partials [B * (TR + DR)][P]
   StatRec* rec;        // [rows]: M, kept mass Z', log2 Z'
   float* vtau;         // [rows]: a token is kept iff its logit >= vtau
-  int32_t* row_flag;   // [rows]: SPEC_ROW_WARP or 0
+  int32_t* row_flag;   // [rows]: SPEC_ROW_WARP or 0 (kRowDeferred between the two selection kernels)
   const float* lanes;  // the stats pass's lane records [rows][P][32] (NULL: none)
+  int probe_k;         // top-p alone: candidates the warp path gathers first (0: none)
+  int deferred_only;   // topp_rows_kernel: only the rows the warp path deferred
 };
+// Top-p alone over rows longer than the candidate buffer: the warp path
+// first gathers the row's kToppProbe largest elements (and every tie) and
+// resolves the row when their mass reaches the cut; other rows are marked
+// kRowDeferred (never seen by the caller) for the mass-weighted radix select.
+constexpr int kToppProbe = 48;
+constexpr int32_t kRowDeferred = 1 << 30;
 int select_candidates();
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st);
 

@@ -76,12 +76,17 @@ __device__ float2 kept_mass(const Raw* row, int V, uint32_t tau, W weight, float
 // The row's record from its sorted candidate list (one warp): the top-k
 // threshold K is the k-th entry, the kept-by-top-k set the entries >= K;
 // top-p keeps the groups up to the last entry whose preceding kept mass is
-// below top_p of theirs.
+// below top_p of theirs. Top-p alone (the probe: no top-k; the candidates
+// are every element >= a bound): the kept-by-top-k set is the whole row, of
+// mass Zfull, and the cut lies among the candidates exactly when their mass
+// reaches top_p Zfull; false (nothing written) when it does not.
 template <typename Raw, int NR>
-__device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf, int n, float M, int lane) {
+__device__ bool warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf, int n, float M, float2 Zfull,
+                              int lane) {
   uint64_t r[NR];
   warp_load_sort<NR>(buf, n, r, lane);
-  const uint32_t K = comp_key(warp_entry<NR>(r, a.top_k - 1));
+  const bool probe = a.top_k == 0;
+  const uint32_t K = probe ? 0u : comp_key(warp_entry<NR>(r, a.top_k - 1));
   float w[NR];
   bool ink[NR];
   float2 zk = make_float2(0.f, 0.f);
@@ -94,7 +99,8 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
     w[i] = ww;
     zk = ds_add(zk, make_float2(ww, 0.f));
   }
-  const float2 Zk = warp_sum_ds(zk);
+  const float2 Zc = warp_sum_ds(zk);  // mass of the candidates kept by top-k
+  const float2 Zk = probe ? Zfull : Zc;
   uint32_t tau = K;
   int st = 0;
   float2 Zp = Zk;  // top-k alone: the kept set is the top-k set
@@ -117,6 +123,7 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
       pre[i] = ds_add(run, inc);
       run = ds_add(run, make_float2(__shfl_sync(0xffffffffu, inc.x, 31), __shfl_sync(0xffffffffu, inc.y, 31)));
     }
+    if (probe && ds_gt(target, run)) return false;  // the cut lies below the candidates
     const int L = __reduce_max_sync(0xffffffffu, last);
     if (L < 0) {
       st = SPEC_ROW_WARP;
@@ -152,13 +159,15 @@ __device__ void warped_sorted(const SelArgs& a, int row_id, const uint64_t* buf,
     a.vtau[row_id] = key_value<Raw>(tau);
     a.row_flag[row_id] = st;
   }
+  return true;
 }
 
 // One warp selects a row: the row's elements at or above a lower bound t0
-// of its k-th largest logit (the k-th largest segment maximum), gathered by
-// rereading the half-lanes of the stats pass whose maximum reaches t0;
-// false when the row needs the whole CTA (no top-k, no lane records, too
-// many candidates).
+// of its k-th largest logit (the k-th largest segment maximum; k the top-k,
+// or for top-p alone the probe), gathered by rereading the half-lanes of the
+// stats pass whose maximum reaches t0; false when the row needs the whole
+// CTA (no top-k, no lane records, too many candidates) or, for top-p alone,
+// the radix select (the nucleus reaches past the candidates).
 template <typename Raw, bool VEC>
 __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int* chunks, float* cmax, int lane) {
   if (a.lanes == nullptr || a.P > 256) return false;  // the CTA selects every row
@@ -181,26 +190,22 @@ __device__ bool warped_list_row(const SelArgs& a, int row_id, uint64_t* buf, int
     }
     return true;
   }
-  if (!(a.top_k > 0 && a.top_k <= a.P && a.top_k < a.V)) return false;
+  const int k = a.top_k > 0 ? a.top_k : a.probe_k;  // the candidates: the top-k set, or the top-p probe
+  if (!(k > 0 && k <= a.P && k < a.V)) return false;
   float sm[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) sm[i] = q[i].x;
-  const float t0 = seg_bound_regs<8>(sm, a.P, a.top_k, lane);
+  const float t0 = seg_bound_regs<8>(sm, a.P, k, lane);
   const int RPG = a.TR + a.DR;
   const int b = row_id / RPG, j = row_id - b * RPG;
   const Raw* row = j < a.TR ? static_cast<const Raw*>(a.A) + (static_cast<long long>(b) * a.TR + j) * a.V
                             : static_cast<const Raw*>(a.Bd) + (static_cast<long long>(b) * a.DR + (j - a.TR)) * a.V;
-  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, lanes, lv, t0, a.top_k, buf, chunks, cmax, lane);
-  if (n < a.top_k) return false;  // too many candidates
-  if (n <= 32)
-    warped_sorted<Raw, 1>(a, row_id, buf, n, M, lane);
-  else if (n <= 64)
-    warped_sorted<Raw, 2>(a, row_id, buf, n, M, lane);
-  else if (n <= 128)
-    warped_sorted<Raw, 4>(a, row_id, buf, n, M, lane);
-  else
-    warped_sorted<Raw, 8>(a, row_id, buf, n, M, lane);
-  return true;
+  const int n = gather_chunks<Raw, VEC>(row, a.V, a.P, lanes, lv, t0, k, buf, chunks, cmax, lane);
+  if (n < k) return false;  // too many candidates
+  if (n <= 32) return warped_sorted<Raw, 1>(a, row_id, buf, n, M, z, lane);
+  if (n <= 64) return warped_sorted<Raw, 2>(a, row_id, buf, n, M, z, lane);
+  if (n <= 128) return warped_sorted<Raw, 4>(a, row_id, buf, n, M, z, lane);
+  return warped_sorted<Raw, 8>(a, row_id, buf, n, M, z, lane);
 }
 
 // ---- top-p over any number of tokens: a mass-weighted radix select ----
@@ -553,7 +558,11 @@ __global__ void __launch_bounds__(kSelThreads, ROWWISE ? 4 : 2) warp_select_kern
     float* wm = reinterpret_cast<float*>(wc + kSelWarps * kChunkCap);
     const bool done = row_id >= rows || warped_list_row<Raw, VEC>(a, row_id, wl + warp * kWarpList,
                                                                   wc + warp * kChunkCap, wm + warp * kChunkCap, lane);
-    if (lane == 0) s_slow[warp] = !done;
+    if (lane == 0) {
+      // top-p alone: a row the probe leaves open goes to topp_rows_kernel
+      if (!done && a.probe_k > 0) a.row_flag[row_id] = kRowDeferred;
+      s_slow[warp] = !done && a.probe_k == 0;
+    }
     __syncthreads();
   }
   // the other rows, one at a time by the whole CTA
@@ -760,6 +769,9 @@ __global__ void __launch_bounds__(kSelThreads, 4) topp_rows_kernel(SelArgs a) {
   __shared__ float2 s_Z;
   griddep_wait();
   griddep_launch_dependents();
+  // after the warp path: only the rows it deferred (the same in every CTA of
+  // the cluster, so all leave together)
+  if (a.deferred_only && a.row_flag[row_id] != kRowDeferred) return;
   if (warp == 0) {  // M and Z of the row from the stats partials
     float2 z;
     const float M = fold_stats(a.part + static_cast<long long>(row_id) * a.P, a.P, a.c_hi, a.c_lo, lane, &z);
@@ -800,45 +812,65 @@ __global__ void __launch_bounds__(kSelThreads, 4) topp_rows_kernel(SelArgs a) {
 
 int select_candidates() { return kCand; }
 
+namespace {
+
+// Top-p alone over rows longer than the candidate buffer (all rows, or with
+// a.deferred_only those the warp path deferred): rows split over clusters of
+// up to 8 CTAs while the rows alone leave SMs idle (four CTAs fit an SM), or
+// while the slices of the CTAs resident at once would not fit in three
+// quarters of L2 (the passes after the first then read their slice from L2
+// instead of HBM).
+cudaError_t launch_topp_rows(const SelArgs& a, int dtype, bool vec, cudaStream_t st) {
+  const long long rows = static_cast<long long>(a.B) * (a.TR + a.DR);
+  int dev = 0, sms = 0, l2 = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  if (e != cudaSuccess) return e;
+  const long long slots = 4LL * sms, row_bytes = static_cast<long long>(a.V) * (dtype == SPEC_BF16 ? 2 : 4);
+  int C = 1;
+  while (C < 8 && (rows * C * 2 <= slots || std::min(rows * C, slots) * (row_bytes / C) > 3LL * l2 / 4)) C *= 2;
+  const dim3 grid(static_cast<unsigned>(rows * C)), block(kSelThreads);
+  if (dtype == SPEC_BF16)
+    return vec ? launch_pdl(topp_rows_kernel<uint16_t, true>, grid, block, st, a, C)
+               : launch_pdl(topp_rows_kernel<uint16_t, false>, grid, block, st, a, C);
+  return vec ? launch_pdl(topp_rows_kernel<float, true>, grid, block, st, a, C)
+             : launch_pdl(topp_rows_kernel<float, false>, grid, block, st, a, C);
+}
+
+}  // namespace
+
 cudaError_t launch_warp_select(const SelArgs& a, int dtype, bool vec, cudaStream_t st) {
   const long long rows = static_cast<long long>(a.B) * (a.TR + a.DR);
-  if (!(a.top_k > 0 && a.top_k < a.V) && a.top_p < 1.f && a.V > kCand) {
-    // top-p alone over rows longer than the candidate buffer: rows split over
-    // clusters of up to 8 CTAs while the rows alone leave SMs idle (four
-    // CTAs fit an SM), or while the slices of the CTAs resident at once
-    // would not fit in three quarters of L2 (the passes after the first then
-    // read their slice from L2 instead of HBM)
-    int dev = 0, sms = 0, l2 = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
-    if (e != cudaSuccess) return e;
-    const long long slots = 4LL * sms, row_bytes = static_cast<long long>(a.V) * (dtype == SPEC_BF16 ? 2 : 4);
-    int C = 1;
-    while (C < 8 && (rows * C * 2 <= slots || std::min(rows * C, slots) * (row_bytes / C) > 3LL * l2 / 4)) C *= 2;
-    const dim3 grid(static_cast<unsigned>(rows * C)), block(kSelThreads);
-    if (dtype == SPEC_BF16)
-      return vec ? launch_pdl(topp_rows_kernel<uint16_t, true>, grid, block, st, a, C)
-                 : launch_pdl(topp_rows_kernel<uint16_t, false>, grid, block, st, a, C);
-    return vec ? launch_pdl(topp_rows_kernel<float, true>, grid, block, st, a, C)
-               : launch_pdl(topp_rows_kernel<float, false>, grid, block, st, a, C);
-  }
+  const bool topp_alone = !(a.top_k > 0 && a.top_k < a.V) && a.top_p < 1.f && a.V > kCand;
+  const int k = a.top_k > 0 ? a.top_k : a.probe_k;  // the warp path's candidates
+  const bool warp_path = a.lanes != nullptr && a.P <= 256 && k > 0 && k <= a.P && k < a.V;
+  // top-p alone without lane records: the radix select takes every row
+  if (topp_alone && !(warp_path && a.probe_k > 0)) return launch_topp_rows(a, dtype, vec, st);
   // no row can take the warp path (it needs the lane records and a top-k of
   // at most the segment count): one CTA per row
-  const bool rowwise = a.lanes == nullptr || a.P > 256 || !(a.top_k > 0 && a.top_k <= a.P && a.top_k < a.V);
+  const bool rowwise = !warp_path;
   const dim3 grid(static_cast<unsigned>(rowwise ? rows : (rows + kSelWarps - 1) / kSelWarps)), block(kSelThreads);
+  cudaError_t e;
   if (rowwise) {
     if (dtype == SPEC_BF16)
-      return vec ? launch_pdl(warp_select_kernel<uint16_t, true, true>, grid, block, st, a)
-                 : launch_pdl(warp_select_kernel<uint16_t, false, true>, grid, block, st, a);
-    return vec ? launch_pdl(warp_select_kernel<float, true, true>, grid, block, st, a)
-               : launch_pdl(warp_select_kernel<float, false, true>, grid, block, st, a);
+      e = vec ? launch_pdl(warp_select_kernel<uint16_t, true, true>, grid, block, st, a)
+              : launch_pdl(warp_select_kernel<uint16_t, false, true>, grid, block, st, a);
+    else
+      e = vec ? launch_pdl(warp_select_kernel<float, true, true>, grid, block, st, a)
+              : launch_pdl(warp_select_kernel<float, false, true>, grid, block, st, a);
+  } else if (dtype == SPEC_BF16) {
+    e = vec ? launch_pdl(warp_select_kernel<uint16_t, true, false>, grid, block, st, a)
+            : launch_pdl(warp_select_kernel<uint16_t, false, false>, grid, block, st, a);
+  } else {
+    e = vec ? launch_pdl(warp_select_kernel<float, true, false>, grid, block, st, a)
+            : launch_pdl(warp_select_kernel<float, false, false>, grid, block, st, a);
   }
-  if (dtype == SPEC_BF16)
-    return vec ? launch_pdl(warp_select_kernel<uint16_t, true, false>, grid, block, st, a)
-               : launch_pdl(warp_select_kernel<uint16_t, false, false>, grid, block, st, a);
-  return vec ? launch_pdl(warp_select_kernel<float, true, false>, grid, block, st, a)
-             : launch_pdl(warp_select_kernel<float, false, false>, grid, block, st, a);
+  if (e != cudaSuccess || !topp_alone) return e;
+  // top-p alone: the rows the probe left open
+  SelArgs d = a;
+  d.deferred_only = 1;
+  return launch_topp_rows(d, dtype, vec, st);
 }
 
 }  // namespace specv

@@ -143,6 +143,18 @@ def test_warped_topp_alone_row_splits(B, K, V, dtype):
     compare(*run(c, V, 0.6), name=f"warped_topp_split_{B}_{V}_kV")  # a top-k of V keeps every token
 
 
+@pytest.mark.parametrize("dtype,top_p", [(torch.bfloat16, 0.8), (torch.bfloat16, 0.85), (torch.float32, 0.8),
+                                          (torch.bfloat16, 0.9)])
+def test_warped_topp_alone_probe(dtype, top_p):
+    """Top-p alone on peaked rows of a 128K vocabulary (T=0.7, 20 boosted
+    tokens): where the nucleus lies within the warp path's probe (its 48
+    largest elements and their ties) the row is cut there; where it reaches
+    past them the row is deferred to the radix select. Both against the
+    oracle, in one batch."""
+    c = gen.chain_zipf(12, 4, 128256, dtype, 0.7, 0.7, seed=int(100 * top_p))
+    compare(*run(c, 0, top_p), name=f"warped_topp_probe_{top_p}")
+
+
 def test_warped_topp_alone_serving_batch_sampled_rows():
     """Top-p alone on the serving batch (B=64, K=8, V=128256 bf16, T=0.7,
     top-p 0.95): 1088 rows whose slices would not stay in L2 one per CTA, so
