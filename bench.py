@@ -300,7 +300,7 @@ def run_ours(args):
                 ev[1].record(stream)
 
             timed_kernel = ("rowscan_kernel + warp_select_kernel + chain_tail_kernel (one call)" if name == "warped"
-                            else "rowscan_kernel + topp_rows_kernel + chain_tail_kernel (one call)")
+                            else "rowscan_kernel + warp_select_kernel + topp_rows_kernel + chain_tail_kernel (one call)")
         else:
             out = sv.spec_verify_chain(*sets[0], T, workspace=ws_t)
             # one prepared call per rotating input set (the serving-loop form of the API)
@@ -317,7 +317,8 @@ def run_ours(args):
                 sv.spec_chain_sample(*args_, T, out, ws_t)
 
             timed_kernel = "rowscan_kernel"
-        launches_per_step = 3 if name in ("warped", "nucleus") else 2
+        # the nucleus workload: the warp path's probe, then the radix select of the rows it defers
+        launches_per_step = {"warped": 3, "nucleus": 4}.get(name, 2)
         host = [w.Lp, w.Lq, w.x, w.ua, w.ur]
 
     # warm-up, then a short untimed soak so the clock sampler sees the load
