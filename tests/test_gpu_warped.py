@@ -132,6 +132,9 @@ def test_warped_large_nucleus(dtype, V, T, top_k, top_p):
     (1, 8, 128256, torch.bfloat16),   # 17 rows: clusters of 8
     (2, 5, 40001, torch.bfloat16),    # odd length: element-wise slices
     (3, 4, 65537, torch.float32),
+    (4, 3, 4097, torch.bfloat16),     # just past the candidate buffer: 3 stats segments, a probe of 3 (scalar loads)
+    (4, 3, 8200, torch.bfloat16),     # 5 segments, a probe of 5 (vector loads)
+    (4, 3, 4100, torch.float32),
 ])
 def test_warped_topp_alone_row_splits(B, K, V, dtype):
     """Top-p alone over rows longer than the candidate buffer, at batch sizes
