@@ -2,11 +2,10 @@
 // one kernel that follows the streaming pass.
 //
 // Grid (kCS, B): one thread-block cluster of kCS CTAs per batch row b,
-// launched with programmatic dependent launch so its CTAs start as the
-// rowscan pass drains (inputs they need that the pass does not write are
-// gathered before griddepcontrol.wait). The cluster
+// launched with programmatic dependent launch. The cluster
 //   1. folds the rowscan partials of b's 2K+1 rows, each row by one of its
-//      kCS x 8 warps, and sends every row's record to all its CTAs through
+//      kCS x 7 folding warps (the eighth warp of each CTA gathers the inputs
+//      at the draft tokens meanwhile), and sends every row's record to all its CTAs through
 //      distributed shared memory; after a cluster barrier each CTA decides
 //      on one warp: r_k = p_k(x_k) / q_k(x_k), x_k kept iff u_k < r_k, left
 //      to right, stopping at the first rejection m (speculative sampling as
@@ -417,38 +416,47 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   __shared__ int s_first;
   griddep_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
   cluster_arrive();             // every CTA of the cluster is running before any remote store
-  // inputs first (the pass this kernel depends on does not write them), so
-  // these gathers overlap the end of the streaming pass
-  for (int k = tid; k < K; k += kResThreads) {
-    const long long ik = static_cast<long long>(b) * K + k;
-    const int xk = a.x[ik];
-    s_x[k] = xk;
-    s_u[k] = a.ua[ik];
-    const bool ok = xk >= 0 && xk < a.V;
-    s_lp[k] = ok ? logit_at<Raw>(a.Lp, static_cast<long long>(b) * (K + 1) + k, a.V, xk) : 0.f;
-    s_lq[k] = ok ? logit_at<Raw>(a.Lq, ik, a.V, xk) : 0.f;
-  }
   griddep_wait();
+  // the last warp of every CTA gathers the inputs at the draft tokens (two
+  // dependent load rounds) while the other warps load and fold the rows'
+  // records: the kernel starts only once the work before it has completed,
+  // so gathers placed before the wait would add their latency to every call
+  constexpr int kFW = kResWarps - 1;  // warps per CTA that fold or load records
+  if (warp == kFW) {
+    for (int k = lane; k < K; k += 32) {
+      const long long ik = static_cast<long long>(b) * K + k;
+      const int xk = a.x[ik];
+      s_x[k] = xk;
+      s_u[k] = a.ua[ik];
+      const bool ok = xk >= 0 && xk < a.V;
+      s_lp[k] = ok ? logit_at<Raw>(a.Lp, static_cast<long long>(b) * (K + 1) + k, a.V, xk) : 0.f;
+      s_lq[k] = ok ? logit_at<Raw>(a.Lq, ik, a.V, xk) : 0.f;
+    }
+  }
   if constexpr (W) {
     // 1. the per-row records of the sampling settings' kept sets
-    for (int j = tid; j < RPG; j += kResThreads) {
-      const long long r = static_cast<long long>(b) * RPG + j;
-      rr[j] = a.rec[r];
-      s_vt[j] = a.vtau[r];
-      s_rf[j] = a.row_flag[r];
-    }
+    if (warp < kFW)
+      for (int j = tid; j < RPG; j += kFW * 32) {
+        const long long r = static_cast<long long>(b) * RPG + j;
+        rr[j] = a.rec[r];
+        s_vt[j] = a.vtau[r];
+        s_rf[j] = a.row_flag[r];
+      }
     cluster_wait();
     cluster_arrive();
     cluster_wait();
     __syncthreads();
   } else {
-    // 1. fold: cluster warp gw folds rows gw, gw + kBW, ... and sends each
-    //    record to every CTA of the cluster
-    fold_stats_rows(a.part + static_cast<long long>(b) * RPG * a.P, a.P, gw, kBW, RPG, a.c_hi, a.c_lo, lane, rr);
+    // 1. fold: folding warp fw of the cluster folds rows fw, fw + kCS kFW,
+    //    ... and sends each record to every CTA of the cluster
+    const int fw = rank * kFW + warp;
+    if (warp < kFW)
+      fold_stats_rows(a.part + static_cast<long long>(b) * RPG * a.P, a.P, fw, kCS * kFW, RPG, a.c_hi, a.c_lo, lane,
+                      rr);
     __syncwarp();
     cluster_wait();
-    if (lane < kCS && lane != rank)
-      for (int j = gw; j < RPG; j += kBW) st_cluster(cluster_addr(&rr[j], lane), rr[j]);
+    if (warp < kFW && lane < kCS && lane != rank)
+      for (int j = fw; j < RPG; j += kCS * kFW) st_cluster(cluster_addr(&rr[j], lane), rr[j]);
     __syncwarp();
     cluster_arrive();
     cluster_wait();
