@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kScanThreads) rowscan_kernel(ScanArgs a) {
     if constexpr (MODE == kModeEntropy)
       reinterpret_cast<float4*>(a.part)[slot] = make_float4(M, tail, ytail, 0.f);
     else
-      a.part[slot] = make_float2(M, tail);
+      st_keep(a.part + slot, make_float2(M, tail));
   }
 }
 

@@ -414,15 +414,18 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   __shared__ DecRec s_dec;
   __shared__ __align__(16) float2 s_units[kNU];  // first CTA: unit totals of the row
   __shared__ int s_first;
+  __shared__ float s_ur;  // the draw's uniform
   griddep_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
   cluster_arrive();             // every CTA of the cluster is running before any remote store
   griddep_wait();
   // the last warp of every CTA gathers the inputs at the draft tokens (two
-  // dependent load rounds) while the other warps load and fold the rows'
-  // records: the kernel starts only once the work before it has completed,
-  // so gathers placed before the wait would add their latency to every call
+  // dependent load rounds) and the draw's uniform while the other warps load
+  // and fold the rows' records: the kernel starts only once the work before
+  // it has completed, so gathers placed before the wait would add their
+  // latency to every call
   constexpr int kFW = kResWarps - 1;  // warps per CTA that fold or load records
   if (warp == kFW) {
+    if (lane == 0 && rank == 0) s_ur = a.ur[b];
     for (int k = lane; k < K; k += 32) {
       const long long ik = static_cast<long long>(b) * K + k;
       const int xk = a.x[ik];
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   }
   if (warp != 0) return;
   int32_t* out = a.out_tokens + static_cast<long long>(b) * (a.K + 1) + d.m;
-  float2 thr = ds_mul_f(S, a.ur[b]);
+  float2 thr = ds_mul_f(S, s_ur);
   // first lane (then unit) with positive weight whose cumulative end exceeds
   // u * S; the last one with weight in case rounding left none
   float2 exl = make_float2(__shfl_up_sync(0xffffffffu, incl.x, 1), __shfl_up_sync(0xffffffffu, incl.y, 1));
