@@ -58,40 +58,18 @@ __device__ __forceinline__ float fold_stats(const float2* pr, int P, float c_hi,
   return M;
 }
 
-// Fold rows j = first, first + stride, ... (< nrows) of the stats partials at
-// `part` (row j at part + j * P) into rr[j], one warp. When every row of the
-// warp fits (at most 4 rows, P <= 64), all loads are issued before any
-// reduction, so the rows cost one memory round trip together, and lane i
-// forms the logarithm of row i.
-__device__ __forceinline__ void fold_stats_rows(const float2* part, int P, int first, int stride, int nrows,
-                                                float c_hi, float c_lo, int lane, StatRec* rr) {
-  constexpr int kR = 4;
-  if (P > 64 || first + kR * stride < nrows) {
-    for (int j = first; j < nrows; j += stride) {
-      float2 z;
-      const float M = fold_stats(part + static_cast<long long>(j) * P, P, c_hi, c_lo, lane, &z);
-      if (lane == 0) rr[j] = make_stat(M, z);
-    }
-    return;
-  }
-  float2 q[kR][2];
-#pragma unroll
-  for (int i = 0; i < kR; ++i) {
-    const int j = first + i * stride;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int idx = lane + 32 * c;
-      q[i][c] = (j < nrows && idx < P) ? __ldcg(part + static_cast<long long>(j) * P + idx) : make_float2(-INFINITY, 0.f);
-    }
-  }
-  float M[kR];
+// Row max and sum of exp of kR rows from their loaded partials (q[i][c]:
+// partial lane + 32 c of row i, -inf past the row), folded by one warp:
+// every lane returns each row's max and its sum as a float pair.
+template <int kR>
+__device__ __forceinline__ void fold_loaded(const float2 (&q)[kR][2], float c_hi, float c_lo, float (&M)[kR],
+                                            float2 (&z)[kR]) {
 #pragma unroll
   for (int i = 0; i < kR; ++i) M[i] = fmax_nan(q[i][0].x, q[i][1].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
     for (int i = 0; i < kR; ++i) M[i] = fmax_nan(M[i], __shfl_xor_sync(0xffffffffu, M[i], o));
-  float2 z[kR];
 #pragma unroll
   for (int i = 0; i < kR; ++i) {
     z[i] = make_float2(0.f, 0.f);
@@ -109,11 +87,6 @@ __device__ __forceinline__ void fold_stats_rows(const float2* part, int P, int f
 #pragma unroll
     for (int i = 0; i < kR; ++i)
       z[i] = ds_add(z[i], make_float2(__shfl_xor_sync(0xffffffffu, z[i].x, o), __shfl_xor_sync(0xffffffffu, z[i].y, o)));
-#pragma unroll
-  for (int i = 0; i < kR; ++i) {
-    const int j = first + i * stride;
-    if (lane == i && j < nrows) rr[j] = make_stat(M[i], z[i]);
-  }
 }
 
 // Row argmax over P (value, index) partials; every lane returns it.

@@ -3,15 +3,18 @@
 //
 // Grid (kCS, B): one thread-block cluster of kCS CTAs per batch row b,
 // launched with programmatic dependent launch. The cluster
-//   1. folds the rowscan partials of b's 2K+1 rows, each row by one of its
-//      kCS x 7 folding warps (the eighth warp of each CTA gathers the inputs
-//      at the draft tokens meanwhile), and sends every row's record to all its CTAs through
-//      distributed shared memory; after a cluster barrier each CTA decides
-//      on one warp: r_k = p_k(x_k) / q_k(x_k), x_k kept iff u_k < r_k, left
-//      to right, stopping at the first rejection m (speculative sampling as
-//      summarised on the ariser.io page, section on keeping the same
-//      distribution; lotook.com, step "accept or reject draft tokens"). The
-//      first CTA writes the outputs;
+//   1. runs one task per position k = 0 .. K, spread over its CTAs: the task
+//      folds the rowscan partials of target row k and draft row k (or loads
+//      their records), gathers x_k, u_k and the logits at x_k, and decides
+//      whether x_k is kept: r_k = p_k(x_k) / q_k(x_k), x_k kept iff u_k < r_k
+//      (speculative sampling as summarised on the ariser.io page, section on
+//      keeping the same distribution; lotook.com, step "accept or reject
+//      draft tokens"). It sends the rows' records and the position's record
+//      to every CTA through distributed shared memory; after a cluster
+//      barrier one warp of each CTA takes the first rejection m, left to
+//      right. The first CTA writes the outputs. Deciding inside the tasks
+//      keeps the single-warp step after the barrier short: on an SM where
+//      other clusters already weigh, every step of one warp runs slowly;
 //   2. weighs row m for the draw that follows, each warp one contiguous
 //      block of its vectors: after a rejection, from max(0, p_m - q_m)
 //      renormalised; after K acceptances, from the bonus position p_K
@@ -257,67 +260,164 @@ __device__ __noinline__ double ratio_fp64(float lp, float Mp, float lq, float Mq
 
 __device__ __forceinline__ bool row_ok(const StatRec& r) { return isfinite(r.M) && isfinite(r.Z) && r.Z > 0.f; }
 
-// Acceptance decision for batch row b on one warp, from the folded rows rr
-// (target row k at k, draft row k at K + 1 + k) and the gathered inputs:
-// lane k forms log2 r_k = (l_p - M_p - l_q + M_q) log2(e) / T + log2 Z_q -
-// log2 Z_p and r_k = 2^that (relative error about 1e-6 at worst; decisions
-// within 1e-5 of the threshold are taken in fp64). Outputs are written when
-// `write`; the decision goes to *dec. W: the sampling settings' kept sets
-// apply (s_vt: per row, a token is kept iff its logit >= s_vt; rr holds the
-// kept masses): p'(x) = 0 outside the target's set, and a token outside
-// the draft's set is accepted iff the target keeps it.
-template <bool W>
-__device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane, const StatRec* rr, const float* s_lp,
-                                          const float* s_lq, const float* s_u, const int* s_x, const float* s_vt,
-                                          const int* s_rf, bool write, DecRec* dec) {
+__device__ __forceinline__ StatRec shfl_stat(const StatRec& r, int src) {
+  StatRec o;
+  o.M = __shfl_sync(0xffffffffu, r.M, src);
+  o.Z = __shfl_sync(0xffffffffu, r.Z, src);
+  o.Lhi = __shfl_sync(0xffffffffu, r.Lhi, src);
+  o.Llo = __shfl_sync(0xffffffffu, r.Llo, src);
+  return o;
+}
+
+// What the task of position k sends to every CTA of the cluster.
+struct __align__(16) PosRec {
+  int flags;       // bit 0: x_k rejected; above it the row_status bits of rows k, K + 1 + k and of x_k
+  int x;           // the draft token x_k
+  float Dhi, Dlo;  // log2(Z_p / Z_q) of position k as a float pair
+  float vtp, vtq;  // sampling settings: kept iff logit >= these (-inf: all)
+  float lp, lq;    // the logits at x_k
+};
+
+__device__ __forceinline__ void st_cluster(uint32_t addr, const PosRec& r) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r.flags), "r"(r.x),
+               "r"(__float_as_uint(r.Dhi)), "r"(__float_as_uint(r.Dlo))
+               : "memory");
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr + 16), "f"(r.vtp), "f"(r.vtq), "f"(r.lp),
+               "f"(r.lq)
+               : "memory");
+}
+
+// The task of position k (0 <= k <= K) on one warp: the records of target row
+// k and draft row k (W: loaded; else folded from the rowscan partials), the
+// inputs at x_k, and whether x_k is kept: r_k = p_k(x_k) / q_k(x_k) from
+// log2 r_k = (l_p - M_p - l_q + M_q) log2(e) / T + log2 Z_q - log2 Z_p, x_k
+// kept iff u_k < r_k (speculative sampling as summarised on the ariser.io
+// page, section on keeping the same distribution; lotook.com, step "accept
+// or reject draft tokens"); decisions within 1e-5 of the threshold are
+// taken in fp64. Position K (the bonus row) has no draft row and no
+// decision. Every lane returns the same records. W: p'(x) = 0 outside the
+// target's kept set, and a token outside the draft's kept set is accepted
+// iff the target keeps it.
+template <typename Raw, bool W>
+__device__ __forceinline__ void chain_task(const TailArgs& a, int b, int k, int lane, StatRec& rp, StatRec& rq,
+                                           PosRec& pr) {
   const int K = a.K, V = a.V, RPG = 2 * K + 1;
+  const bool hasq = k < K;
+  const long long ik = static_cast<long long>(b) * K + k;
+  const long long jp = static_cast<long long>(b) * RPG + k, jq = jp + K + 1;
+  // every load is issued before the first result is needed: the token and
+  // the partials (or records) together, then the logits at the token while
+  // the partials are folded
+  const int xk = hasq ? a.x[ik] : -1;
+  const float uk = hasq ? a.ua[ik] : 0.f;
+  float vtp = -INFINITY, vtq = -INFINITY;
   int st = 0;
-  for (int j = lane; j < RPG; j += 32) {
-    if (W && s_rf[j]) st |= s_rf[j];
-    else if (!row_ok(rr[j])) st |= j <= K ? SPEC_ROW_TARGET : SPEC_ROW_DRAFT;
+  const float2* part = a.part;
+  const int P = a.P;
+  const bool fast = !W && P <= 64;  // both rows' partials in two loads per lane
+  float2 q[2][2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int idx = lane + 32 * c;
+    q[0][c] = fast && idx < P ? __ldcg(part + jp * P + idx) : make_float2(-INFINITY, 0.f);
+    q[1][c] = fast && hasq && idx < P ? __ldcg(part + jq * P + idx) : make_float2(-INFINITY, 0.f);
   }
-  for (int k = lane; k < K; k += 32)
-    if (s_x[k] < 0 || s_x[k] >= V) st |= SPEC_ROW_TOKEN;
-  st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
-  int m = K;
-  float2 Dm = make_float2(0.f, 0.f);  // log2(Zp_m / Zq_m), formed by every lane for its own position
-  for (int k0 = 0; k0 < K; k0 += 32) {
-    const int k = k0 + lane;
-    bool rej = false;
-    float2 Dk = make_float2(0.f, 0.f);
-    if (k < K && st == 0) {
-      const StatRec rp = rr[k], rq = rr[K + 1 + k];
-      const float lp = s_lp[k], lq = s_lq[k];
-      const float u = s_u[k];
-      Dk = ds_add(make_float2(rp.Lhi, rp.Llo), make_float2(-rq.Lhi, -rq.Llo));
-      float r;
-      const bool kp = !W || lp >= s_vt[k], kq = !W || lq >= s_vt[K + 1 + k];
-      if (!kq || lq == -INFINITY) {
-        r = (kp && lp > -INFINITY) || !W ? INFINITY : 0.f;  // q(x) = 0: accept (W: iff p'(x) > 0)
-      } else if (!kp) {
-        r = 0.f;  // p'(x) = 0: reject
-      } else {
-        const float du = (lp - rp.M) - (lq - rq.M);  // exact for bf16 logits
-        r = ex2_fast(fmaf(du, a.c_hi, du * a.c_lo) - (Dk.x + Dk.y));
-      }
-      if (kp && kq && r < 1.f && fabsf(u - r) < 1e-5f) {  // near the threshold: decide in fp64
-        rej = !(static_cast<double>(u) < ratio_fp64(lp, rp.M, lq, rq.M, a.invT, rp.Z, rq.Z));
-      } else {
-        rej = !(u < r);
+  if constexpr (W) {
+    rp = a.rec[jp];
+    vtp = a.vtau[jp];
+    const int fp = a.row_flag[jp];
+    int fq = 0;
+    if (hasq) {
+      rq = a.rec[jq];
+      vtq = a.vtau[jq];
+      fq = a.row_flag[jq];
+    }
+    st |= fp ? fp : (row_ok(rp) ? 0 : SPEC_ROW_TARGET);
+    if (hasq) st |= fq ? fq : (row_ok(rq) ? 0 : SPEC_ROW_DRAFT);
+  }
+  const bool ok = hasq && xk >= 0 && xk < V;
+  const int xs = ok ? xk : 0;
+  const float lpr = logit_at<Raw>(a.Lp, static_cast<long long>(b) * (K + 1) + k, V, xs);
+  const float lqr = hasq ? logit_at<Raw>(a.Lq, ik, V, xs) : 0.f;
+  if constexpr (!W) {
+    if (fast) {
+      float M[2];
+      float2 z[2];
+      fold_loaded<2>(q, a.c_hi, a.c_lo, M, z);
+      // the two rows' logarithms side by side: the target row's on lanes
+      // 0-15, the draft row's on lanes 16-31
+      const int h = lane >> 4;
+      const StatRec r = make_stat(h ? M[1] : M[0], h ? z[1] : z[0]);
+      rp = shfl_stat(r, 0);
+      if (hasq) rq = shfl_stat(r, 16);
+    } else {
+      float2 z;
+      float M = fold_stats(part + jp * P, P, a.c_hi, a.c_lo, lane, &z);
+      rp = make_stat(M, z);
+      if (hasq) {
+        M = fold_stats(part + jq * P, P, a.c_hi, a.c_lo, lane, &z);
+        rq = make_stat(M, z);
       }
     }
-    const unsigned msk = __ballot_sync(0xffffffffu, rej);
-    if (m == K && msk) {
-      const int l = __ffs(msk) - 1;
-      m = k0 + l;
-      Dm = make_float2(__shfl_sync(0xffffffffu, Dk.x, l), __shfl_sync(0xffffffffu, Dk.y, l));
+    if (!row_ok(rp)) st |= SPEC_ROW_TARGET;
+    if (hasq && !row_ok(rq)) st |= SPEC_ROW_DRAFT;
+  }
+  if (hasq && !ok) st |= SPEC_ROW_TOKEN;
+  const float lp = ok ? lpr : 0.f, lq = ok ? lqr : 0.f;
+  bool rej = false;
+  float2 D = make_float2(0.f, 0.f);
+  if (hasq && st == 0) {
+    D = ds_add(make_float2(rp.Lhi, rp.Llo), make_float2(-rq.Lhi, -rq.Llo));
+    float r;
+    const bool kp = !W || lp >= vtp, kq = !W || lq >= vtq;
+    if (!kq || lq == -INFINITY) {
+      r = (kp && lp > -INFINITY) || !W ? INFINITY : 0.f;  // q(x) = 0: accept (W: iff p'(x) > 0)
+    } else if (!kp) {
+      r = 0.f;  // p'(x) = 0: reject
+    } else {
+      const float du = (lp - rp.M) - (lq - rq.M);  // exact for bf16 logits
+      r = ex2_fast(fmaf(du, a.c_hi, du * a.c_lo) - (D.x + D.y));
+    }
+    if (kp && kq && r < 1.f && fabsf(uk - r) < 1e-5f) {  // near the threshold: decide in fp64
+      rej = !(static_cast<double>(uk) < ratio_fp64(lp, rp.M, lq, rq.M, a.invT, rp.Z, rq.Z));
+    } else {
+      rej = !(uk < r);
+    }
+  }
+  pr.flags = (st << 1) | (rej ? 1 : 0);
+  pr.x = xk;
+  pr.Dhi = D.x;
+  pr.Dlo = D.y;
+  pr.vtp = vtp;
+  pr.vtq = vtq;
+  pr.lp = lp;
+  pr.lq = lq;
+}
+
+// The batch row's status and first rejection m from the positions' records,
+// on one warp (the same in every CTA). Outputs are written when `write`;
+// the decision goes to *dec.
+template <bool W>
+__device__ __forceinline__ void finish_decision(const TailArgs& a, int b, int lane, const StatRec* rr,
+                                                const PosRec* pos, bool write, DecRec* dec) {
+  const int K = a.K;
+  int st = 0;
+  for (int j = lane; j <= K; j += 32) st |= pos[j].flags >> 1;
+  st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
+  int m = K;
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    const int k = k0 + lane;
+    const unsigned msk = __ballot_sync(0xffffffffu, k < K && (pos[k].flags & 1));
+    if (msk) {
+      m = k0 + __ffs(msk) - 1;
+      break;
     }
   }
   if (st) m = -1;
   if (write) {
     for (int j = lane; j <= K; j += 32) {
       if (st || j != m)  // position m is written by the draw
-        a.out_tokens[static_cast<long long>(b) * (K + 1) + j] = (st == 0 && j < m) ? s_x[j] : -1;
+        a.out_tokens[static_cast<long long>(b) * (K + 1) + j] = (st == 0 && j < m) ? pos[j].x : -1;
     }
     if (lane == 0) {
       a.accept_len[b] = m;
@@ -331,14 +431,14 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
     if (st == 0) {
       d.mode = m < K ? 0 : 1;
       d.Mp = rr[m].M;
-      d.vtp = W ? s_vt[m] : -INFINITY;
+      d.vtp = W ? pos[m].vtp : -INFINITY;
       d.vtq = -INFINITY;
       if (m < K) {
         d.Mq = rr[K + 1 + m].M;
         d.dM = d.Mp - d.Mq;
-        d.D_hi = Dm.x;
-        d.D_lo = Dm.y;
-        if (W) d.vtq = s_vt[K + 1 + m];
+        d.D_hi = pos[m].Dhi;
+        d.D_lo = pos[m].Dlo;
+        if (W) d.vtq = pos[m].vtq;
       }
     }
     *dec = d;
@@ -348,24 +448,22 @@ __device__ __forceinline__ void decide_chain(const TailArgs& a, int b, int lane,
 // Optional float outputs for batch row b on one warp: lse of every row and
 // p_k(x_k), q_k(x_k) (NaN when the row is flagged; W: the warped p', q').
 template <bool W>
-__device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane, const StatRec* rr, const float* s_lp,
-                                           const float* s_lq, const int* s_x, const float* s_vt, const int* s_rf) {
-  const int K = a.K, V = a.V, RPG = 2 * K + 1;
+__device__ __forceinline__ void chain_outputs(const TailArgs& a, int b, int lane, const StatRec* rr,
+                                              const PosRec* pos) {
+  const int K = a.K, RPG = 2 * K + 1;
   int st = 0;
-  for (int j = lane; j < RPG; j += 32)
-    if (!row_ok(rr[j]) || (W && s_rf[j])) st = 1;
-  for (int k = lane; k < K; k += 32)
-    if (s_x[k] < 0 || s_x[k] >= V) st = 1;
+  for (int j = lane; j <= K; j += 32) st |= pos[j].flags >> 1;
   st = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(st)));
   for (int k = lane; k < K; k += 32) {
     float pxv = NAN, qxv = NAN;
     if (st == 0) {
       const StatRec rp = rr[k], rq = rr[K + 1 + k];
-      const float up = s_lp[k] - rp.M, uq = s_lq[k] - rq.M;
+      const PosRec pk = pos[k];
+      const float up = pk.lp - rp.M, uq = pk.lq - rq.M;
       pxv = ex2_fast(fmaf(up, a.c_hi, up * a.c_lo) - rp.Lhi - rp.Llo);
       qxv = ex2_fast(fmaf(uq, a.c_hi, uq * a.c_lo) - rq.Lhi - rq.Llo);
-      if (W && !(s_lp[k] >= s_vt[k])) pxv = 0.f;
-      if (W && !(s_lq[k] >= s_vt[K + 1 + k])) qxv = 0.f;
+      if (W && !(pk.lp >= pk.vtp)) pxv = 0.f;
+      if (W && !(pk.lq >= pk.vtq)) qxv = 0.f;
     }
     const long long ik = static_cast<long long>(b) * K + k;
     if (a.px) a.px[ik] = pxv;
@@ -407,10 +505,7 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   const int gw = rank * kResWarps + warp;  // warp of the cluster
   const int K = a.K, RPG = 2 * K + 1;
   __shared__ StatRec rr[2 * kMaxK + 1];
-  __shared__ float s_lp[kMaxK], s_lq[kMaxK], s_u[kMaxK];
-  __shared__ int s_x[kMaxK];
-  __shared__ float s_vt[W ? 2 * kMaxK + 1 : 1];  // sampling settings: per-row kept thresholds
-  __shared__ int s_rf[W ? 2 * kMaxK + 1 : 1];
+  __shared__ PosRec s_pos[kMaxK + 1];
   __shared__ DecRec s_dec;
   __shared__ __align__(16) float2 s_units[kNU];  // first CTA: unit totals of the row
   __shared__ int s_first;
@@ -418,56 +513,31 @@ __global__ void __launch_bounds__(kResThreads, 4) chain_tail_kernel(TailArgs a) 
   griddep_launch_dependents();  // the next kernel may be scheduled (it waits for this grid)
   cluster_arrive();             // every CTA of the cluster is running before any remote store
   griddep_wait();
-  // the last warp of every CTA gathers the inputs at the draft tokens (two
-  // dependent load rounds) and the draw's uniform while the other warps load
-  // and fold the rows' records: the kernel starts only once the work before
-  // it has completed, so gathers placed before the wait would add their
-  // latency to every call
-  constexpr int kFW = kResWarps - 1;  // warps per CTA that fold or load records
-  if (warp == kFW) {
-    if (lane == 0 && rank == 0) s_ur = a.ur[b];
-    for (int k = lane; k < K; k += 32) {
-      const long long ik = static_cast<long long>(b) * K + k;
-      const int xk = a.x[ik];
-      s_x[k] = xk;
-      s_u[k] = a.ua[ik];
-      const bool ok = xk >= 0 && xk < a.V;
-      s_lp[k] = ok ? logit_at<Raw>(a.Lp, static_cast<long long>(b) * (K + 1) + k, a.V, xk) : 0.f;
-      s_lq[k] = ok ? logit_at<Raw>(a.Lq, ik, a.V, xk) : 0.f;
+  // 1. the positions' tasks, position k on warp k / kCS of CTA k % kCS (the
+  //    cluster's SMs share them): records of rows k and K + 1 + k, the
+  //    inputs at x_k and its decision, sent to every CTA of the cluster
+  const float ur = tid == 0 && rank == 0 ? a.ur[b] : 0.f;
+  int kt = warp * kCS + rank;
+  StatRec rp, rq;
+  PosRec pr;
+  if (kt <= K) chain_task<Raw, W>(a, b, kt, lane, rp, rq, pr);
+  cluster_wait();
+  while (kt <= K) {
+    if (lane < kCS) {
+      st_cluster(cluster_addr(&rr[kt], lane), rp);
+      if (kt < K) st_cluster(cluster_addr(&rr[K + 1 + kt], lane), rq);
+      st_cluster(cluster_addr(&s_pos[kt], lane), pr);
     }
+    kt += kBW;
+    if (kt <= K) chain_task<Raw, W>(a, b, kt, lane, rp, rq, pr);
   }
-  if constexpr (W) {
-    // 1. the per-row records of the sampling settings' kept sets
-    if (warp < kFW)
-      for (int j = tid; j < RPG; j += kFW * 32) {
-        const long long r = static_cast<long long>(b) * RPG + j;
-        rr[j] = a.rec[r];
-        s_vt[j] = a.vtau[r];
-        s_rf[j] = a.row_flag[r];
-      }
-    cluster_wait();
-    cluster_arrive();
-    cluster_wait();
-    __syncthreads();
-  } else {
-    // 1. fold: folding warp fw of the cluster folds rows fw, fw + kCS kFW,
-    //    ... and sends each record to every CTA of the cluster
-    const int fw = rank * kFW + warp;
-    if (warp < kFW)
-      fold_stats_rows(a.part + static_cast<long long>(b) * RPG * a.P, a.P, fw, kCS * kFW, RPG, a.c_hi, a.c_lo, lane,
-                      rr);
-    __syncwarp();
-    cluster_wait();
-    if (warp < kFW && lane < kCS && lane != rank)
-      for (int j = fw; j < RPG; j += kCS * kFW) st_cluster(cluster_addr(&rr[j], lane), rr[j]);
-    __syncwarp();
-    cluster_arrive();
-    cluster_wait();
-  }
-  // 2. decision (the same in every CTA; the first CTA writes the outputs)
-  if (warp == 0) decide_chain<W>(a, b, lane, rr, s_lp, s_lq, s_u, s_x, s_vt, s_rf, rank == 0, &s_dec);
-  if (warp == 1 && rank == 0 && (a.px || a.qx || a.lse_p || a.lse_q))
-    chain_outputs<W>(a, b, lane, rr, s_lp, s_lq, s_x, s_vt, s_rf);
+  if (tid == 0 && rank == 0) s_ur = ur;
+  __syncwarp();
+  cluster_arrive();
+  cluster_wait();
+  // 2. the first rejection (the same in every CTA; the first CTA writes the outputs)
+  if (warp == 0) finish_decision<W>(a, b, lane, rr, s_pos, rank == 0, &s_dec);
+  if (warp == 1 && rank == 0 && (a.px || a.qx || a.lse_p || a.lse_q)) chain_outputs<W>(a, b, lane, rr, s_pos);
   __syncthreads();
   const DecRec d = s_dec;
   const long long V = a.V;
