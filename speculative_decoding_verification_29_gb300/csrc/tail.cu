@@ -277,6 +277,7 @@ struct __align__(16) PosRec {
   float vtp, vtq;  // sampling settings: kept iff logit >= these (-inf: all)
   float lp, lq;    // the logits at x_k
 };
+static_assert(sizeof(PosRec) == 32, "a position record is two 16-byte stores");
 
 __device__ __forceinline__ void st_cluster(uint32_t addr, const PosRec& r) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r.flags), "r"(r.x),
