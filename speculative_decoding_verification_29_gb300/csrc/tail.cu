@@ -260,6 +260,7 @@ __device__ __noinline__ double ratio_fp64(float lp, float Mp, float lq, float Mq
 
 __device__ __forceinline__ bool row_ok(const StatRec& r) { return isfinite(r.M) && isfinite(r.Z) && r.Z > 0.f; }
 
+// Lane src's record, in every lane.
 __device__ __forceinline__ StatRec shfl_stat(const StatRec& r, int src) {
   StatRec o;
   o.M = __shfl_sync(0xffffffffu, r.M, src);
